@@ -1,0 +1,902 @@
+/*
+ * ppsim_oracle.c -- plain, slow, CPU reference of the pipeline-schedule evaluator.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the oracle that the CUDA library is
+ * checked against.  Only the tests, the smoke check and the benchmark's CPU
+ * baseline may load it; the product path never does.  It shares no code,
+ * header, table or constant with the CUDA library: every rule below is
+ * restated from the pages' text, in the pages' order.
+ *
+ * Page short names used in citations:
+ *   [1F1B]      "2. 1F1B"  (sgdbs.github.io, AI_Infra / 2.PipelineParallel / OneF1B)
+ *   [GPipe->ZB] "Pipeline parallelism: from GPipe to 1F1B and Zero Bubble" (dlog.com.cn)
+ *   [M040]      "Pipeline scheduling: GPipe, 1F1B, interleaving and overlap" (xuujii.github.io)
+ *   [Megatron3] "Megatron-LM distributed training (3): pipeline parallel PP and 1F1B"
+ *   [lpnh]      lpnh.cn news 2768528 (bubble formulas and 64xH100 table)
+ *
+ * What it computes, per schedule instance:
+ *   1. the per-device op order from the schedule's rules (orc_order);
+ *   2. every op's start/end tick with a discrete-event simulation on a global
+ *      tick clock and a min-heap of events (orc_des), following the checker that
+ *      [M040] §08 describes: each task waits for the previous task on its device
+ *      and for the result it needs from the neighbouring stage;
+ *   3. independently, the same times as a longest path over an explicit DAG in
+ *      topological (Kahn) order (orc_longest_path) -- a cross-check of 2;
+ *   4. makespan, busy/idle per device, the unreduced bubble pair and the peak
+ *      count of held activations (ledger +1 at F, -1 at B);
+ *   5. the validity checks [M040] §08 lists (no overlap on a device, every B
+ *      has its F before it, gradients flow back, every device runs M*v F and
+ *      M*v B).
+ *
+ * Readings taken where the pages are silent (each listed in the design notes):
+ *   - GPipe backward order is last-in-first-out (D..A), from [M040] §02's table.
+ *   - 1F1B stage k runs w = min(P-k, M) forwards, then (B, F) pairs taking the
+ *     oldest B first, then the remaining B.  This is [1F1B] §2.3/§3.2's "P-k
+ *     forwards" and equals [Megatron3]'s num_warmup = P-k-1 followed by the
+ *     first steady F; both give F^w (B F)^(M-w) B^w.
+ *   - Interleaved 1F1B: the op order is not printed on any page.  The oracle
+ *     takes the Megatron interleaved order the pages point to ([1F1B] §6.1,
+ *     [GPipe->ZB] Megatron section, [M040] §06): warmup 2(P-k-1)+(v-1)P
+ *     forwards, then (F, B) pairs, then the remaining B; forward j maps to
+ *     chunk (j mod Pv)/P and microbatch (j/(Pv))*P + j mod P, backward j to
+ *     chunk v-1-(j mod Pv)/P with the same microbatch.  It needs M % P == 0
+ *     ([M040] §06 divisibility note).
+ *   - comm is a latency added on each cross-stage dependency edge; it occupies
+ *     neither device.  comm[b] is the edge between virtual stages b and b+1.
+ *   - All times are exact integers (int64 here).  An instance whose times do
+ *     not fit in int32 is flagged ORC_ST_OVERFLOW; one with a negative cost or
+ *     comm is flagged ORC_ST_NEG_COST.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <pthread.h>
+
+#define ORC_GPIPE 0
+#define ORC_1F1B 1
+#define ORC_INTERLEAVED 2
+
+#define ORC_F 0
+#define ORC_B 1
+
+/* call-level return codes (numeric values follow the library's documented spec) */
+#define ORC_OK 0
+#define ORC_ERR_ARG 1
+#define ORC_ERR_DIVISIBILITY 2
+#define ORC_ERR_DEADLOCK 5
+#define ORC_ERR_INVARIANT 6
+#define ORC_ERR_NOMEM 7
+
+/* per-instance status codes */
+#define ORC_ST_OK 0
+#define ORC_ST_NEG_COST 1
+#define ORC_ST_OVERFLOW 2
+
+#define ORC_INT32_MAX 2147483647LL
+
+/* ORC_MUTANT plants one deliberate mistake (tests only: they compile mutant
+ * copies to show that the pins catch plausible errors).  0 = the oracle. */
+#ifndef ORC_MUTANT
+#define ORC_MUTANT 0
+#endif
+
+/* ------------------------------------------------------------------------- */
+/* 1. op order                                                               */
+/* ------------------------------------------------------------------------- */
+
+/* Fill the op order of device k: kind[j] (ORC_F / ORC_B), chunk[j], mb[j] for
+ * j < 2*M*v.  Returns the op count, or a negative ORC_ERR_* code. */
+int orc_order(int policy, int P, int M, int v, int k, int *kind, int *chunk, int *mb)
+{
+    int n = 0;
+    if (P < 1 || M < 1 || v < 1 || k < 0 || k >= P) return -ORC_ERR_ARG;
+    if (policy == ORC_GPIPE) {
+        /* [M040] §02 table: all forwards A..D, then backwards D..A. */
+        if (v != 1) return -ORC_ERR_ARG;
+        for (int i = 0; i < M; ++i) { kind[n] = ORC_F; chunk[n] = 0; mb[n] = i; ++n; }
+#if ORC_MUTANT == 3   /* mistake: first-in-first-out backward order */
+        for (int i = 0; i < M; ++i) { kind[n] = ORC_B; chunk[n] = 0; mb[n] = i; ++n; }
+#else
+        for (int i = M - 1; i >= 0; --i) { kind[n] = ORC_B; chunk[n] = 0; mb[n] = i; ++n; }
+#endif
+        return n;
+    }
+    if (policy == ORC_1F1B) {
+        /* [1F1B] §2.3 / §3.2 table: warmup of P-k forwards, steady F-B pairs,
+         * cooldown of the remaining B; the steady B is the oldest outstanding
+         * microbatch ([Megatron3] "pop(0)").  Clamped to M when M < P-k. */
+        if (v != 1) return -ORC_ERR_ARG;
+        int w = P - k;
+#if ORC_MUTANT == 2   /* mistake: Megatron's warmup count taken as the F count */
+        w = P - k - 1;
+#endif
+        if (w > M) w = M;
+        for (int i = 0; i < w; ++i) { kind[n] = ORC_F; chunk[n] = 0; mb[n] = i; ++n; }
+        for (int q = 0; q < M - w; ++q) {
+            kind[n] = ORC_B; chunk[n] = 0; mb[n] = q; ++n;
+            kind[n] = ORC_F; chunk[n] = 0; mb[n] = w + q; ++n;
+        }
+        for (int i = M - w; i < M; ++i) { kind[n] = ORC_B; chunk[n] = 0; mb[n] = i; ++n; }
+        return n;
+    }
+    if (policy == ORC_INTERLEAVED) {
+        /* Device k holds virtual stages k, k+P, ... ([1F1B] §6.1; [M040] §06). */
+        if (M % P != 0) return -ORC_ERR_DIVISIBILITY;
+        int total = M * v;
+        int w = 2 * (P - k - 1) + (v - 1) * P;
+        if (w > total) w = total;
+        int group = P * v;
+        /* forward virtual index j */
+#define FWD(j) do { int jj_ = (j); kind[n] = ORC_F; \
+                    chunk[n] = (jj_ % group) / P; \
+                    mb[n] = (jj_ / group) * P + jj_ % P; ++n; } while (0)
+#define BWD(j) do { int jj_ = (j); kind[n] = ORC_B; \
+                    chunk[n] = v - 1 - (jj_ % group) / P; \
+                    mb[n] = (jj_ / group) * P + jj_ % P; ++n; } while (0)
+        for (int j = 0; j < w; ++j) FWD(j);
+        for (int i = 0; i < total - w; ++i) { FWD(w + i); BWD(i); }
+        for (int i = total - w; i < total; ++i) BWD(i);
+#undef FWD
+#undef BWD
+        return n;
+    }
+    return -ORC_ERR_ARG;
+}
+
+/* ------------------------------------------------------------------------- */
+/* problem description shared by both evaluators                             */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    int P, M, v, S, O;          /* devices, microbatches, chunks, virtual stages, ops per device */
+    const int *kind, *chunk, *mb;   /* [P][O] op order */
+    const int64_t *tf, *tb;     /* [S][M] costs of this instance */
+    const int64_t *comm;        /* [S-1] edge latency (may be NULL: all 0) */
+} orc_inst;
+
+static int64_t op_cost(const orc_inst *in, int dev, int j)
+{
+    int s = in->chunk[dev * in->O + j] * in->P + dev;
+    int i = in->mb[dev * in->O + j];
+    return in->kind[dev * in->O + j] == ORC_F ? in->tf[(int64_t)s * in->M + i]
+                                              : in->tb[(int64_t)s * in->M + i];
+}
+
+static int64_t edge_comm(const orc_inst *in, int b)
+{
+    return in->comm ? in->comm[b] : 0;
+}
+
+/* Locate every op (kind, s, i): pos[(kind*S + s)*M + i] = dev*O + j, or -1.
+ * Returns 0, or ORC_ERR_INVARIANT if an op is missing, repeated or misplaced. */
+static int build_pos(const orc_inst *in, int *pos)
+{
+    int S = in->S, M = in->M, P = in->P, O = in->O;
+    for (int64_t x = 0; x < 2LL * S * M; ++x) pos[x] = -1;
+    for (int d = 0; d < P; ++d) {
+        for (int j = 0; j < O; ++j) {
+            int kd = in->kind[d * O + j], c = in->chunk[d * O + j], i = in->mb[d * O + j];
+            if ((kd != ORC_F && kd != ORC_B) || c < 0 || c >= in->v || i < 0 || i >= M)
+                return ORC_ERR_INVARIANT;
+            int s = c * P + d;
+            int64_t key = ((int64_t)kd * S + s) * M + i;
+            if (pos[key] != -1) return ORC_ERR_INVARIANT;   /* repeated op */
+            pos[key] = d * O + j;
+        }
+    }
+    for (int64_t x = 0; x < 2LL * S * M; ++x)
+        if (pos[x] == -1) return ORC_ERR_INVARIANT;          /* missing op */
+    return ORC_OK;
+}
+
+/* The dependencies of op (dev, j) from the pages' dependency model:
+ *   F(s,i) needs F(s-1,i) (arrives comm[s-1] after it ends)  -- forward flows down;
+ *   B(s,i) needs B(s+1,i) (arrives comm[s] after it ends)    -- gradient flows back;
+ *   B(s,i) needs F(s,i) on its own device (no comm)           -- [GPipe->ZB] GPipe
+ *   figure text: the backward needs the upper layer's B and the same layer's F;
+ *   [M040] §01.  Writes up to 2 (op index, latency) pairs; returns the count. */
+static int deps_of(const orc_inst *in, const int *pos, int dev, int j, int *dop, int64_t *dlat)
+{
+    int S = in->S, M = in->M, O = in->O;
+    int kd = in->kind[dev * O + j], i = in->mb[dev * O + j];
+    int s = in->chunk[dev * O + j] * in->P + dev;
+    int nd = 0;
+    if (kd == ORC_F) {
+#if ORC_MUTANT == 1   /* mistake: forward edges carry no comm */
+        if (s > 0) { dop[nd] = pos[((int64_t)ORC_F * S + (s - 1)) * M + i]; dlat[nd] = 0; ++nd; }
+#else
+        if (s > 0) { dop[nd] = pos[((int64_t)ORC_F * S + (s - 1)) * M + i]; dlat[nd] = edge_comm(in, s - 1); ++nd; }
+#endif
+    } else {
+#if ORC_MUTANT != 4   /* mutant 4's mistake: B ignores the downstream gradient */
+        if (s < S - 1) { dop[nd] = pos[((int64_t)ORC_B * S + (s + 1)) * M + i]; dlat[nd] = edge_comm(in, s); ++nd; }
+#endif
+        dop[nd] = pos[((int64_t)ORC_F * S + s) * M + i]; dlat[nd] = 0; ++nd;
+    }
+    return nd;
+}
+
+/* ------------------------------------------------------------------------- */
+/* 2. discrete-event simulation                                              */
+/* ------------------------------------------------------------------------- */
+
+typedef struct { int64_t t; int64_t seq; int dev; int type; } orc_event;   /* type 0: op end, 1: wake */
+
+typedef struct { orc_event *a; int64_t n, cap; } orc_heap;
+
+static int ev_less(const orc_event *x, const orc_event *y)
+{
+    return x->t < y->t || (x->t == y->t && x->seq < y->seq);
+}
+
+static int heap_push(orc_heap *h, orc_event e)
+{
+    if (h->n == h->cap) {
+        int64_t nc = h->cap ? 2 * h->cap : 64;
+        orc_event *na = (orc_event *)realloc(h->a, (size_t)nc * sizeof(orc_event));
+        if (!na) return ORC_ERR_NOMEM;
+        h->a = na; h->cap = nc;
+    }
+    int64_t c = h->n++;
+    h->a[c] = e;
+    while (c > 0) {
+        int64_t p = (c - 1) / 2;
+        if (!ev_less(&h->a[c], &h->a[p])) break;
+        orc_event t = h->a[c]; h->a[c] = h->a[p]; h->a[p] = t; c = p;
+    }
+    return ORC_OK;
+}
+
+static orc_event heap_pop(orc_heap *h)
+{
+    orc_event top = h->a[0];
+    h->a[0] = h->a[--h->n];
+    int64_t c = 0;
+    for (;;) {
+        int64_t l = 2 * c + 1, r = l + 1, m = c;
+        if (l < h->n && ev_less(&h->a[l], &h->a[m])) m = l;
+        if (r < h->n && ev_less(&h->a[r], &h->a[m])) m = r;
+        if (m == c) break;
+        orc_event t = h->a[c]; h->a[c] = h->a[m]; h->a[m] = t; c = m;
+    }
+    return top;
+}
+
+/* Simulate one instance.  start/end are [P][O].  Every device is free at tick
+ * 0 and every microbatch input is ready at tick 0 ([1F1B] §5.2: stage 0 loads
+ * microbatch i itself).  Ops are non-preemptive.  At each event time the
+ * simulator first retires every event due at that time, then lets each idle
+ * device start its next op if all its inputs have arrived; an input that is
+ * done but still in flight schedules a wake-up at its arrival tick.
+ * Returns ORC_OK or ORC_ERR_DEADLOCK (no event left while ops remain). */
+int orc_des_inst(const orc_inst *in, const int *pos, int64_t *start, int64_t *end)
+{
+    int P = in->P, O = in->O;
+    int total = P * O, finished = 0;
+    int *cursor = (int *)calloc((size_t)P, sizeof(int));
+    int *running = (int *)calloc((size_t)P, sizeof(int));
+    unsigned char *done = (unsigned char *)calloc((size_t)total, 1);
+    orc_heap h = {0, 0, 0};
+    int64_t seq = 0, now = 0;
+    int rc = ORC_OK;
+    if (!cursor || !running || !done) { rc = ORC_ERR_NOMEM; goto out; }
+
+    for (;;) {
+        /* try to start an op on every idle device at time `now` */
+        for (int d = 0; d < P; ++d) {
+            if (running[d] || cursor[d] >= O) continue;
+            int j = cursor[d];
+            int dop[2]; int64_t dlat[2];
+            int nd = deps_of(in, pos, d, j, dop, dlat);
+            int ready = 1; int64_t arrive = 0;
+            for (int x = 0; x < nd; ++x) {
+                if (!done[dop[x]]) { ready = 0; break; }
+                int64_t a = end[dop[x]] + dlat[x];
+                if (a > arrive) arrive = a;
+            }
+            if (!ready) continue;               /* retried when the input's op ends */
+            if (arrive > now) {                 /* input still on the wire */
+                orc_event e = { arrive, seq++, d, 1 };
+                if (heap_push(&h, e)) { rc = ORC_ERR_NOMEM; goto out; }
+                continue;
+            }
+            int64_t c = op_cost(in, d, j);
+            start[d * O + j] = now;
+            end[d * O + j] = now + c;
+            running[d] = 1;
+            orc_event e = { now + c, seq++, d, 0 };
+            if (heap_push(&h, e)) { rc = ORC_ERR_NOMEM; goto out; }
+        }
+        if (finished == total) break;
+        if (h.n == 0) { rc = ORC_ERR_DEADLOCK; break; }
+        /* advance the clock to the next event and retire everything due then */
+        now = h.a[0].t;
+        while (h.n > 0 && h.a[0].t == now) {
+            orc_event e = heap_pop(&h);
+            if (e.type == 0) {
+                int d = e.dev;
+                done[d * O + cursor[d]] = 1;
+                cursor[d] += 1;
+                running[d] = 0;
+                finished += 1;
+            }
+        }
+    }
+out:
+    free(cursor); free(running); free(done); free(h.a);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* 3. independent cross-check: longest path over the explicit DAG            */
+/* ------------------------------------------------------------------------- */
+
+/* Build the DAG (device-order edges plus dependency edges weighted by comm),
+ * order it with Kahn's algorithm and relax each node's start as the max over
+ * its in-edges of (predecessor end + weight).  A node left unordered means a
+ * cycle, i.e. the order deadlocks.  Returns ORC_OK or ORC_ERR_DEADLOCK. */
+int orc_longest_path_inst(const orc_inst *in, const int *pos, int64_t *start, int64_t *end)
+{
+    int P = in->P, O = in->O, total = P * O;
+    /* every node has at most 3 in-edges: previous op on its device + 2 deps */
+    int *indeg = (int *)calloc((size_t)total, sizeof(int));
+    int *succ = (int *)malloc((size_t)total * 3 * sizeof(int));
+    int64_t *sw = (int64_t *)malloc((size_t)total * 3 * sizeof(int64_t));
+    int *nsucc = (int *)calloc((size_t)total, sizeof(int));
+    int *queue = (int *)malloc((size_t)total * sizeof(int));
+    int rc = ORC_OK;
+    if (!indeg || !succ || !sw || !nsucc || !queue) { rc = ORC_ERR_NOMEM; goto out; }
+    for (int d = 0; d < P; ++d) {
+        for (int j = 0; j < O; ++j) {
+            int node = d * O + j;
+            if (j > 0) {
+                int pnode = node - 1;
+                succ[pnode * 3 + nsucc[pnode]] = node; sw[pnode * 3 + nsucc[pnode]] = 0; nsucc[pnode]++;
+                indeg[node]++;
+            }
+            int dop[2]; int64_t dlat[2];
+            int nd = deps_of(in, pos, d, j, dop, dlat);
+            for (int x = 0; x < nd; ++x) {
+                int pnode = dop[x];
+                if (nsucc[pnode] >= 3) { rc = ORC_ERR_INVARIANT; goto out; }
+                succ[pnode * 3 + nsucc[pnode]] = node; sw[pnode * 3 + nsucc[pnode]] = dlat[x]; nsucc[pnode]++;
+                indeg[node]++;
+            }
+        }
+    }
+    for (int x = 0; x < total; ++x) start[x] = 0;
+    int qh = 0, qt = 0;
+    for (int x = 0; x < total; ++x) if (indeg[x] == 0) queue[qt++] = x;
+    while (qh < qt) {
+        int u = queue[qh++];
+        int d = u / O, j = u % O;
+        end[u] = start[u] + op_cost(in, d, j);
+        for (int e = 0; e < nsucc[u]; ++e) {
+            int w = succ[u * 3 + e];
+            int64_t cand = end[u] + sw[u * 3 + e];
+            if (cand > start[w]) start[w] = cand;
+            if (--indeg[w] == 0) queue[qt++] = w;
+        }
+    }
+    if (qt != total) rc = ORC_ERR_DEADLOCK;
+out:
+    free(indeg); free(succ); free(sw); free(nsucc); free(queue);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* 4./5. reductions and validity checks                                      */
+/* ------------------------------------------------------------------------- */
+
+/* The ledger of held activations ([1F1B] §4.1 table; [M040] §02/§03): +1 when
+ * a forward finishes on the device, -1 when its backward releases it, counted
+ * in op order; peak = running maximum.  Writes peak[P]. */
+void orc_peak(int P, int O, const int *kind, int *peak)
+{
+    for (int d = 0; d < P; ++d) {
+        int held = 0, pk = 0;
+        for (int j = 0; j < O; ++j) {
+#if ORC_MUTANT == 5   /* mistake: ledger releases on F and holds on B */
+            held += kind[d * O + j] == ORC_F ? -1 : 1;
+#else
+            held += kind[d * O + j] == ORC_F ? 1 : -1;
+#endif
+            if (held > pk) pk = held;
+        }
+        peak[d] = pk;
+    }
+}
+
+/* Validity checks of [M040] §08: no two ops overlap on a device; every B has
+ * its F on the same device before it; every input arrives before the op that
+ * uses it starts; each device runs exactly M*v F and M*v B.  Returns ORC_OK or
+ * ORC_ERR_INVARIANT. */
+static int check_inst(const orc_inst *in, const int *pos, const int64_t *start, const int64_t *end)
+{
+    int P = in->P, O = in->O;
+    for (int d = 0; d < P; ++d) {
+        int nf = 0, nb = 0;
+        for (int j = 0; j < O; ++j) {
+            int node = d * O + j;
+            if (start[node] < 0 || end[node] != start[node] + op_cost(in, d, j)) return ORC_ERR_INVARIANT;
+            if (j > 0 && start[node] < end[node - 1]) return ORC_ERR_INVARIANT;
+            if (in->kind[node] == ORC_F) nf++; else nb++;
+            int dop[2]; int64_t dlat[2];
+            int nd = deps_of(in, pos, d, j, dop, dlat);
+            for (int x = 0; x < nd; ++x)
+                if (end[dop[x]] + dlat[x] > start[node]) return ORC_ERR_INVARIANT;
+            if (in->kind[node] == ORC_B) {
+                int fnode = dop[nd - 1];        /* F(s,i): same device, earlier */
+                if (fnode / O != d || fnode % O >= j) return ORC_ERR_INVARIANT;
+            }
+        }
+        if (nf != in->M * in->v || nb != in->M * in->v) return ORC_ERR_INVARIANT;
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* single-instance entry point (int64 everything; used by tests)              */
+/* ------------------------------------------------------------------------- */
+
+/* Evaluate one instance with an explicit op order (kind/chunk/mb [P][O]).
+ * method 0: discrete-event simulation; 1: longest path; 2: both, and compare.
+ * Outputs: start/end [P][O], makespan, busy[P], idle[P], bub (num, den), peak[P].
+ * Returns ORC_OK, ORC_ERR_DEADLOCK, ORC_ERR_INVARIANT or ORC_ERR_NOMEM. */
+int orc_eval_explicit(int P, int M, int v, const int *kind, const int *chunk, const int *mb,
+                      const int64_t *tf, const int64_t *tb, const int64_t *comm, int method,
+                      int64_t *start, int64_t *end, int64_t *makespan, int64_t *busy,
+                      int64_t *idle, int64_t *bub, int *peak)
+{
+    if (P < 1 || M < 1 || v < 1) return ORC_ERR_ARG;
+    orc_inst in = { P, M, v, P * v, 2 * M * v, kind, chunk, mb, tf, tb, comm };
+    int total = P * in.O;
+    int *pos = (int *)malloc((size_t)2 * in.S * M * sizeof(int));
+    int64_t *s2 = (int64_t *)malloc((size_t)total * sizeof(int64_t));
+    int64_t *e2 = (int64_t *)malloc((size_t)total * sizeof(int64_t));
+    int rc;
+    if (!pos || !s2 || !e2) { rc = ORC_ERR_NOMEM; goto out; }
+    rc = build_pos(&in, pos);
+    if (rc) goto out;
+    if (method == 1) rc = orc_longest_path_inst(&in, pos, start, end);
+    else rc = orc_des_inst(&in, pos, start, end);
+    if (rc) goto out;
+    if (method == 2) {
+        rc = orc_longest_path_inst(&in, pos, s2, e2);
+        if (rc) goto out;
+        for (int x = 0; x < total; ++x)
+            if (s2[x] != start[x] || e2[x] != end[x]) { rc = ORC_ERR_INVARIANT; goto out; }
+    }
+    rc = check_inst(&in, pos, start, end);
+    if (rc) goto out;
+    /* [M040] §04: window time, busy time per stage, bubble = idle / window;
+     * [1F1B] §4.3: bubble ratio = total idle over P * total time. */
+    int64_t mk = 0;
+    for (int x = 0; x < total; ++x) if (end[x] > mk) mk = end[x];
+    int64_t num = 0;
+    for (int d = 0; d < P; ++d) {
+        int64_t b = 0;
+        for (int j = 0; j < in.O; ++j) b += op_cost(&in, d, j);
+        busy[d] = b;
+        idle[d] = mk - b;
+        num += mk - b;
+    }
+    *makespan = mk;
+    bub[0] = num;
+    bub[1] = (int64_t)P * mk;
+#if ORC_MUTANT == 6   /* mistake: bubble over ideal time instead of over the window */
+    bub[1] = (int64_t)P * mk - num;
+#endif
+    orc_peak(P, in.O, kind, peak);
+out:
+    free(pos); free(s2); free(e2);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* batch entry point (int32 inputs with strides, as the library takes them)   */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    int policy, P, M, v;
+    int64_t n;
+    const int32_t *cost_f, *cost_b;
+    int64_t cs_inst, cs_stage, cs_mb;
+    const int32_t *comm;
+    int64_t ms_inst, ms_bnd;
+    int64_t *makespan, *idle, *bub_num, *bub_den;   /* idle [n][P] */
+    int8_t *status;
+    int64_t *op_start, *op_end;                      /* [n][P][O] or NULL */
+    int method;
+    const int *kind, *chunk, *mb;
+    int64_t lo, hi;
+    int rc;
+} orc_batch_job;
+
+static void *batch_worker(void *arg)
+{
+    orc_batch_job *jb = (orc_batch_job *)arg;
+    int P = jb->P, M = jb->M, v = jb->v, S = P * v, O = 2 * M * v;
+    int64_t *tf = (int64_t *)malloc((size_t)S * M * sizeof(int64_t));
+    int64_t *tb = (int64_t *)malloc((size_t)S * M * sizeof(int64_t));
+    int64_t *cm = (int64_t *)malloc((size_t)(S > 1 ? S - 1 : 1) * sizeof(int64_t));
+    int64_t *st = (int64_t *)malloc((size_t)P * O * sizeof(int64_t));
+    int64_t *en = (int64_t *)malloc((size_t)P * O * sizeof(int64_t));
+    int64_t *busy = (int64_t *)malloc((size_t)P * sizeof(int64_t));
+    int64_t *idle = (int64_t *)malloc((size_t)P * sizeof(int64_t));
+    int *peak = (int *)malloc((size_t)P * sizeof(int));
+    jb->rc = ORC_OK;
+    if (!tf || !tb || !cm || !st || !en || !busy || !idle || !peak) { jb->rc = ORC_ERR_NOMEM; goto out; }
+    for (int64_t x = jb->lo; x < jb->hi; ++x) {
+        int neg = 0;
+        for (int s = 0; s < S; ++s)
+            for (int i = 0; i < M; ++i) {
+                int64_t off = x * jb->cs_inst + s * jb->cs_stage + i * jb->cs_mb;
+                tf[s * M + i] = jb->cost_f[off];
+                tb[s * M + i] = jb->cost_b[off];
+                if (tf[s * M + i] < 0 || tb[s * M + i] < 0) neg = 1;
+            }
+        for (int b = 0; b < S - 1; ++b) {
+            cm[b] = jb->comm ? jb->comm[x * jb->ms_inst + b * jb->ms_bnd] : 0;
+            if (cm[b] < 0) neg = 1;
+        }
+        int64_t mk = 0, bub[2] = {0, 0};
+        int rc = ORC_OK;
+        if (!neg)
+            rc = orc_eval_explicit(P, M, v, jb->kind, jb->chunk, jb->mb, tf, tb, cm, jb->method,
+                                   st, en, &mk, busy, idle, bub, peak);
+        if (rc) { jb->rc = rc; goto out; }
+        int8_t status = ORC_ST_OK;
+        if (neg) status = ORC_ST_NEG_COST;
+        else if (mk > ORC_INT32_MAX) status = ORC_ST_OVERFLOW;
+        /* every time is <= makespan and every arrival is <= some start, so
+         * makespan <= INT32_MAX means every intermediate fits in int32 */
+        if (jb->status) jb->status[x] = status;
+        jb->makespan[x] = neg ? 0 : mk;
+        for (int d = 0; d < P; ++d) jb->idle[x * P + d] = neg ? 0 : idle[d];
+        jb->bub_num[x] = bub[0];
+        jb->bub_den[x] = bub[1];
+        if (jb->op_start)
+            for (int q = 0; q < P * O; ++q) {
+                jb->op_start[x * P * O + q] = neg ? 0 : st[q];
+                jb->op_end[x * P * O + q] = neg ? 0 : en[q];
+            }
+    }
+out:
+    free(tf); free(tb); free(cm); free(st); free(en); free(busy); free(idle); free(peak);
+    return NULL;
+}
+
+/* Evaluate n instances of one policy/shape.  Costs are int32 [inst][stage][mb]
+ * through element strides; comm is int32 [inst][boundary] through strides or
+ * NULL (all zero).  Outputs are int64 (makespan[n], idle[n][P], bub_num[n],
+ * bub_den[n]), int8 status[n], int32 peak[P], and optionally int64 op times
+ * [n][P][O].  Instances are split statically over `nthreads` threads.
+ * Returns ORC_OK or an ORC_ERR_* code. */
+int orc_eval_batch(int policy, int P, int M, int v, int64_t n,
+                   const int32_t *cost_f, const int32_t *cost_b,
+                   int64_t cs_inst, int64_t cs_stage, int64_t cs_mb,
+                   const int32_t *comm, int64_t ms_inst, int64_t ms_bnd,
+                   int64_t *makespan, int64_t *idle, int64_t *bub_num, int64_t *bub_den,
+                   int32_t *peak, int8_t *status, int64_t *op_start, int64_t *op_end,
+                   int method, int nthreads)
+{
+    if (P < 1 || M < 1 || v < 1 || n < 0) return ORC_ERR_ARG;
+    if (policy != ORC_INTERLEAVED && v != 1) return ORC_ERR_ARG;
+    int O = 2 * M * v;
+    int *kind = (int *)malloc((size_t)P * O * sizeof(int));
+    int *chunk = (int *)malloc((size_t)P * O * sizeof(int));
+    int *mbv = (int *)malloc((size_t)P * O * sizeof(int));
+    int *pk = (int *)malloc((size_t)P * sizeof(int));
+    int rc = ORC_OK;
+    if (!kind || !chunk || !mbv || !pk) { rc = ORC_ERR_NOMEM; goto out; }
+    for (int d = 0; d < P; ++d) {
+        int got = orc_order(policy, P, M, v, d, kind + d * O, chunk + d * O, mbv + d * O);
+        if (got < 0) { rc = -got; goto out; }
+    }
+    orc_peak(P, O, kind, pk);
+    if (peak) for (int d = 0; d < P; ++d) peak[d] = pk[d];
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if ((int64_t)nthreads > n) nthreads = n > 0 ? (int)n : 1;
+    orc_batch_job jobs[256];
+    pthread_t th[256];
+    for (int t = 0; t < nthreads; ++t) {
+        orc_batch_job *jb = &jobs[t];
+        jb->policy = policy; jb->P = P; jb->M = M; jb->v = v; jb->n = n;
+        jb->cost_f = cost_f; jb->cost_b = cost_b;
+        jb->cs_inst = cs_inst; jb->cs_stage = cs_stage; jb->cs_mb = cs_mb;
+        jb->comm = comm; jb->ms_inst = ms_inst; jb->ms_bnd = ms_bnd;
+        jb->makespan = makespan; jb->idle = idle; jb->bub_num = bub_num; jb->bub_den = bub_den;
+        jb->status = status; jb->op_start = op_start; jb->op_end = op_end;
+        jb->method = method; jb->kind = kind; jb->chunk = chunk; jb->mb = mbv;
+        jb->lo = n * t / nthreads; jb->hi = n * (t + 1) / nthreads;
+        jb->rc = ORC_OK;
+    }
+    if (nthreads == 1) batch_worker(&jobs[0]);
+    else {
+        for (int t = 0; t < nthreads; ++t) pthread_create(&th[t], NULL, batch_worker, &jobs[t]);
+        for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+    }
+    for (int t = 0; t < nthreads; ++t) if (jobs[t].rc) { rc = jobs[t].rc; break; }
+out:
+    free(kind); free(chunk); free(mbv); free(pk);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* brute force over every valid order (tiny P, M)                             */
+/* ------------------------------------------------------------------------- */
+
+/* Enumerate, for every device, every order of F0..F(M-1), B0..B(M-1) in which
+ * F_i precedes B_i (v = 1, unit costs, no comm), and run the simulator on every
+ * combination.  Reports how many combinations deadlock or run, the minimum
+ * makespan, how many orders reach it, and among those the minimum over orders
+ * of the stage-0 peak and of the largest per-device peak.  This is the
+ * exhaustive check behind [1F1B] §4.2 (no schedule that is not slower holds
+ * fewer than P activations on stage 0) and §4.3 (total time 2(M+P-1)). */
+int orc_bruteforce(int P, int M, int64_t *out /* [6] */)
+{
+    if (P < 1 || M < 1 || P > 4 || M > 4) return ORC_ERR_ARG;
+    int O = 2 * M;
+    {   /* refuse sizes whose enumeration would not finish quickly */
+        double per = 1.0, comb = 1.0;
+        for (int x = 2; x <= O; ++x) per *= x;
+        for (int x = 0; x < M; ++x) per /= 2.0;
+        for (int d = 0; d < P; ++d) comb *= per;
+        if (comb > 2.0e7) return ORC_ERR_ARG;
+    }
+    /* list all single-device orders */
+    int cap = 1;
+    for (int x = 2; x <= O; ++x) cap *= x;          /* (2M)! upper bound */
+    int *lists = (int *)malloc((size_t)cap * O * sizeof(int));   /* encoded op: kind*M + mb */
+    int nl = 0;
+    int perm[8];
+    /* iterate over all permutations of 0..O-1 (op codes), keep the valid ones */
+    for (int x = 0; x < O; ++x) perm[x] = x;
+    for (;;) {
+        int ok = 1;
+        for (int i = 0; i < M && ok; ++i) {
+            int pf = -1, pb = -1;
+            for (int x = 0; x < O; ++x) { if (perm[x] == i) pf = x; if (perm[x] == M + i) pb = x; }
+            if (pf > pb) ok = 0;
+        }
+        if (ok) { memcpy(lists + (size_t)nl * O, perm, (size_t)O * sizeof(int)); nl++; }
+        /* next lexicographic permutation */
+        int a = O - 2;
+        while (a >= 0 && perm[a] > perm[a + 1]) a--;
+        if (a < 0) break;
+        int b = O - 1;
+        while (perm[b] < perm[a]) b--;
+        int t = perm[a]; perm[a] = perm[b]; perm[b] = t;
+        for (int l = a + 1, r = O - 1; l < r; ++l, --r) { t = perm[l]; perm[l] = perm[r]; perm[r] = t; }
+    }
+    int *kind = (int *)malloc((size_t)P * O * sizeof(int));
+    int *chunk = (int *)calloc((size_t)P * O, sizeof(int));
+    int *mbv = (int *)malloc((size_t)P * O * sizeof(int));
+    int64_t *tf = (int64_t *)malloc((size_t)P * M * sizeof(int64_t));
+    int64_t *tb = (int64_t *)malloc((size_t)P * M * sizeof(int64_t));
+    int64_t *cm = (int64_t *)calloc((size_t)P, sizeof(int64_t));
+    int64_t *st = (int64_t *)malloc((size_t)P * O * sizeof(int64_t));
+    int64_t *en = (int64_t *)malloc((size_t)P * O * sizeof(int64_t));
+    int64_t busy[4], idle[4], bub[2], mk;
+    int peak[4];
+    for (int x = 0; x < P * M; ++x) { tf[x] = 1; tb[x] = 1; }
+    int64_t nvalid = 0, ndead = 0, best = -1, nbest = 0, bestpk0 = -1, bestpkmax = -1;
+    int idx[4] = {0, 0, 0, 0};
+    for (;;) {
+        for (int d = 0; d < P; ++d)
+            for (int j = 0; j < O; ++j) {
+                int code = lists[(size_t)idx[d] * O + j];
+                kind[d * O + j] = code < M ? ORC_F : ORC_B;
+                mbv[d * O + j] = code % M;
+            }
+        int rc = orc_eval_explicit(P, M, 1, kind, chunk, mbv, tf, tb, cm, 0, st, en, &mk, busy, idle, bub, peak);
+        if (rc == ORC_ERR_DEADLOCK) ndead++;
+        else if (rc == ORC_OK) {
+            nvalid++;
+            int pmax = 0;
+            for (int d = 0; d < P; ++d) if (peak[d] > pmax) pmax = peak[d];
+            if (best < 0 || mk < best) { best = mk; nbest = 0; bestpk0 = peak[0]; bestpkmax = pmax; }
+            if (mk == best) {
+                nbest++;
+                if (peak[0] < bestpk0) bestpk0 = peak[0];
+                if (pmax < bestpkmax) bestpkmax = pmax;
+            }
+        } else { free(lists); return rc; }
+        int d = 0;
+        while (d < P) { if (++idx[d] < nl) break; idx[d] = 0; d++; }
+        if (d == P) break;
+    }
+    out[0] = nvalid; out[1] = ndead; out[2] = best; out[3] = nbest; out[4] = bestpk0; out[5] = bestpkmax;
+    free(lists); free(kind); free(chunk); free(mbv); free(tf); free(tb); free(cm); free(st); free(en);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* candidate partition search                                                 */
+/* ------------------------------------------------------------------------- */
+
+/* SplitMix64 (Steele, Lea & Flood, "Fast splittable pseudorandom number
+ * generators", OOPSLA 2014; constants as in Vigna's public-domain
+ * splitmix64.c): advance the state by the golden gamma, then mix. */
+static uint64_t splitmix64_at(uint64_t state)
+{
+    uint64_t z = state + 0x9E3779B97F4A7C15ULL;
+#if ORC_MUTANT == 7   /* mistake: one shift constant mistyped */
+    z = (z ^ (z >> 31)) * 0xBF58476D1CE4E5B9ULL;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+    return z ^ (z >> 31);
+#endif
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+    return z ^ (z >> 31);
+}
+
+/* Binomial coefficient by Pascal's rule, exact in uint64 for n <= 1023, k <= 31
+ * when it fits; returns UINT64_MAX on overflow. */
+static uint64_t binom(int n, int k)
+{
+    if (k < 0 || n < 0 || k > n) return 0;
+    if (k > n - k) k = n - k;
+    uint64_t row[64];
+    for (int j = 0; j <= k; ++j) row[j] = 0;
+    row[0] = 1;
+    for (int m = 1; m <= n; ++m) {
+        int top = m < k ? m : k;
+        for (int j = top; j >= 1; --j) {
+            uint64_t s = row[j] + row[j - 1];
+            if (s < row[j] || row[j] == UINT64_MAX || row[j - 1] == UINT64_MAX) s = UINT64_MAX;
+            row[j] = s;
+        }
+    }
+    return row[k];
+}
+
+/* Combinatorial number system (colex order): rank r in [0, C(N,K)) maps to
+ * x_1 < ... < x_K in [0, N) with r = sum_i C(x_i, i); found greedily from i = K
+ * down to 1 by taking the largest x with C(x, i) <= remaining rank. */
+static void unrank_colex(uint64_t r, int N, int K, int *x)
+{
+    int hi = N - 1;
+    for (int i = K; i >= 1; --i) {
+        int c = hi;
+        while (c >= i - 1 && binom(c, i) > r) c--;
+#if ORC_MUTANT == 8   /* mistake: off-by-one in the greedy unranking */
+        if (c > i - 1) c--;
+#endif
+        x[i - 1] = c;
+        r -= binom(c, i);
+        hi = c - 1;
+    }
+}
+
+/* Candidate c's contiguous split of L layers into P non-empty stages: draw
+ * u = splitmix64(seed + c), rank = u mod C(L-1, P-1), unrank it to the P-1 cut
+ * positions x_1 < ... < x_{P-1} in [0, L-1); stage t starts at layer
+ * x_t + 1 (stage 0 at layer 0).  Writes first[P+1] (first layer of each stage,
+ * first[P] = L).  This is the seeded candidate set standing in for the
+ * profiling-based contiguous layer split ([GPipe->ZB] PipeDream/GPipe sections;
+ * [M040] §05; [lpnh]: 80 layers into 8 stages). */
+void orc_candidate_split(uint64_t seed, int64_t c, int L, int P, int *first)
+{
+    int K = P - 1;
+    int x[64];
+    uint64_t total = binom(L - 1, K);
+    uint64_t r = splitmix64_at(seed + (uint64_t)c) % total;
+    unrank_colex(r, L - 1, K, x);
+    first[0] = 0;
+    for (int t = 1; t <= K; ++t) first[t] = x[t - 1] + 1;
+    first[P] = L;
+}
+
+typedef struct {
+    const int32_t *ltf, *ltb; const int64_t *lact;
+    int L, P, M; int32_t comm; int64_t cap; uint64_t seed;
+    int64_t lo, hi;
+    int32_t *all_mk;
+    int64_t best_idx; int64_t best_mk;
+    const int *kind, *chunk, *mb; const int *peak;
+    int rc;
+} orc_search_job;
+
+static void *search_worker(void *arg)
+{
+    orc_search_job *jb = (orc_search_job *)arg;
+    int P = jb->P, M = jb->M, O = 2 * M;
+    int first[65];
+    int64_t *tf = (int64_t *)malloc((size_t)P * M * sizeof(int64_t));
+    int64_t *tb = (int64_t *)malloc((size_t)P * M * sizeof(int64_t));
+    int64_t *cm = (int64_t *)malloc((size_t)P * sizeof(int64_t));
+    int64_t *st = (int64_t *)malloc((size_t)P * O * sizeof(int64_t));
+    int64_t *en = (int64_t *)malloc((size_t)P * O * sizeof(int64_t));
+    int64_t *busy = (int64_t *)malloc((size_t)P * sizeof(int64_t));
+    int64_t *idle = (int64_t *)malloc((size_t)P * sizeof(int64_t));
+    int *pk = (int *)malloc((size_t)P * sizeof(int));
+    jb->best_idx = -1; jb->best_mk = -1; jb->rc = ORC_OK;
+    for (int b = 0; b < P; ++b) cm[b] = jb->comm;
+    for (int64_t c = jb->lo; c < jb->hi; ++c) {
+        orc_candidate_split(jb->seed, c, jb->L, P, first);
+        int rejected = 0;
+        for (int k = 0; k < P; ++k) {
+            int64_t sf = 0, sb = 0, sa = 0;
+            for (int l = first[k]; l < first[k + 1]; ++l) { sf += jb->ltf[l]; sb += jb->ltb[l]; sa += jb->lact[l]; }
+            /* peak bytes on stage k = held activations x bytes per activation */
+            if ((int64_t)jb->peak[k] * sa > jb->cap) rejected = 1;
+            for (int i = 0; i < M; ++i) { tf[k * M + i] = sf; tb[k * M + i] = sb; }
+        }
+        int64_t mk = -1, bub[2];
+        if (!rejected) {
+            int rc = orc_eval_explicit(P, M, 1, jb->kind, jb->chunk, jb->mb, tf, tb, cm, 0,
+                                       st, en, &mk, busy, idle, bub, pk);
+            if (rc) { jb->rc = rc; break; }
+            if (mk > ORC_INT32_MAX) mk = -2;
+        }
+        if (jb->all_mk) jb->all_mk[c - jb->lo] = (int32_t)mk;
+        if (mk >= 0 && (jb->best_idx < 0 || mk < jb->best_mk)) { jb->best_mk = mk; jb->best_idx = c; }
+    }
+    free(tf); free(tb); free(cm); free(st); free(en); free(busy); free(idle); free(pk);
+    return NULL;
+}
+
+/* Score candidates c in [c_lo, c_hi) under 1F1B with M microbatches: stage k's
+ * forward cost is the sum of its layers' forward costs, its backward cost the
+ * sum of the layers' backward costs, comm the same on every boundary; a
+ * candidate is rejected when some stage's peak held activations times its
+ * activation bytes exceeds `cap`.  all_mk[c - c_lo] gets the makespan, -1 if
+ * rejected, -2 if it overflows int32.  best = argmin (makespan, index) over the
+ * range; best_idx = -1 when nothing is feasible.  first_best[P+1] gets the
+ * winner's stage starts.  Returns ORC_OK or an ORC_ERR_* code. */
+int orc_search(const int32_t *layer_tf, const int32_t *layer_tb, const int64_t *layer_act,
+               int L, int P, int M, int32_t comm, int64_t cap, uint64_t seed,
+               int64_t c_lo, int64_t c_hi, int32_t *all_mk,
+               int64_t *best_idx, int64_t *best_mk, int *first_best, int nthreads)
+{
+    if (P < 1 || P > 64 || L < P || M < 1 || c_lo < 0 || c_hi < c_lo) return ORC_ERR_ARG;
+    if (binom(L - 1, P - 1) == UINT64_MAX) return ORC_ERR_ARG;
+    int O = 2 * M;
+    int *kind = (int *)malloc((size_t)P * O * sizeof(int));
+    int *chunk = (int *)malloc((size_t)P * O * sizeof(int));
+    int *mbv = (int *)malloc((size_t)P * O * sizeof(int));
+    int *pk = (int *)malloc((size_t)P * sizeof(int));
+    for (int d = 0; d < P; ++d) orc_order(ORC_1F1B, P, M, 1, d, kind + d * O, chunk + d * O, mbv + d * O);
+    orc_peak(P, O, kind, pk);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    int64_t n = c_hi - c_lo;
+    if (nthreads > n) nthreads = n > 0 ? (int)n : 1;
+    orc_search_job jobs[256];
+    pthread_t th[256];
+    for (int t = 0; t < nthreads; ++t) {
+        orc_search_job *jb = &jobs[t];
+        jb->ltf = layer_tf; jb->ltb = layer_tb; jb->lact = layer_act;
+        jb->L = L; jb->P = P; jb->M = M; jb->comm = comm; jb->cap = cap; jb->seed = seed;
+        jb->lo = c_lo + n * t / nthreads; jb->hi = c_lo + n * (t + 1) / nthreads;
+        jb->all_mk = all_mk ? all_mk + (jb->lo - c_lo) : NULL;
+        jb->kind = kind; jb->chunk = chunk; jb->mb = mbv; jb->peak = pk;
+    }
+    if (nthreads == 1) search_worker(&jobs[0]);
+    else {
+        for (int t = 0; t < nthreads; ++t) pthread_create(&th[t], NULL, search_worker, &jobs[t]);
+        for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+    }
+    int rc = ORC_OK;
+    *best_idx = -1; *best_mk = -1;
+    for (int t = 0; t < nthreads; ++t) {        /* ranges ascend, so first strict min wins ties */
+        if (jobs[t].rc) { rc = jobs[t].rc; break; }
+        if (jobs[t].best_idx >= 0 && (*best_idx < 0 || jobs[t].best_mk < *best_mk)) {
+            *best_idx = jobs[t].best_idx; *best_mk = jobs[t].best_mk;
+        }
+    }
+    if (first_best) {
+        if (*best_idx >= 0) orc_candidate_split(seed, *best_idx, L, P, first_best);
+        else for (int t = 0; t <= P; ++t) first_best[t] = -1;
+    }
+    free(kind); free(chunk); free(mbv); free(pk);
+    return rc;
+}
+
+/* exposed for tests: C(n, k) and the raw generator, to pin them against
+ * textbook values */
+uint64_t orc_binom(int n, int k) { return binom(n, k); }
+uint64_t orc_splitmix64(uint64_t state) { return splitmix64_at(state); }

@@ -1,0 +1,383 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+None of these compare the oracle with itself: each expected value is a cell of
+a table the pages print, a closed form the pages state, a brute-force optimum,
+a published test vector, or a library routine (math.comb, itertools).
+"""
+import itertools
+import math
+import os
+import subprocess
+import tempfile
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from conftest import read_golden
+
+pytestmark = pytest.mark.filterwarnings("ignore")
+
+
+def _table_from_oracle(r, P, names="ABCD"):
+    rows = []
+    for k in range(P):
+        row = ["-"] * r["makespan"]
+        for j in range(r["kind"].shape[1]):
+            kd = "F" if r["kind"][k, j] == 0 else "B"
+            row[r["start"][k, j]] = f"{kd}-{names[r['mb'][k, j]]}"
+        rows.append(row)
+    return rows
+
+
+@pytest.mark.parametrize("policy,fixture", [("gpipe", "m040_gpipe_2x4.txt"), ("1f1b", "m040_1f1b_2x4.txt")])
+def test_m040_worked_tables_cell_for_cell(orc, policy, fixture):
+    g = read_golden(fixture)
+    r = orc.evaluate(policy, 2, 4, 1, 1, 1)
+    assert _table_from_oracle(r, 2) == [g["stage0"], g["stage1"]]
+    assert r["makespan"] == int(g["window"][0])
+    assert r["peak"][0] == int(g["peak_stage0"][0])
+    if "busy_percent" in g:
+        num, den = r["bub"]
+        assert Fraction(den - num, den) == Fraction(int(g["busy_percent"][0]), 100)
+
+
+def test_onef1b_p4m6_diagram_and_ledger(orc):
+    g = read_golden("onef1b_p4m6.txt")
+    r = orc.evaluate("1f1b", 4, 6, 1, 1, 1)
+    k0 = [f"{'FB'[r['kind'][0, j]]}{r['mb'][0, j]}" for j in range(12)]
+    assert k0 == g["stage0_order"]
+    k3 = [f"{'FB'[r['kind'][3, j]]}{r['mb'][3, j]}" for j in range(12)]
+    assert k3 == g["stage3_order"]
+    times = dict(x.split("=") for x in g["stage0_time"])
+    for j, name in enumerate(k0):
+        if name in times:
+            assert r["start"][0, j] == int(times[name]), name
+    held, ledger = 0, []
+    for j in range(12):
+        held += 1 if r["kind"][0, j] == 0 else -1
+        ledger.append(held)
+    assert ledger == [int(x) for x in g["stage0_ledger"]]
+    assert r["peak"][0] == int(g["stage0_peak"][0])
+
+
+@pytest.mark.parametrize("policy", ["gpipe", "1f1b"])
+def test_uniform_closed_form(orc, policy):
+    # "2. 1F1B" §4.3 and M040 §04: total 2(M+P-1)tau, busy M/(M+P-1),
+    # bubble (P-1)/(M+P-1), identical for GPipe and 1F1B.
+    for P in range(1, 9):
+        for M in list(range(1, 13)) + [17, 24]:
+            for tau in (1, 3):
+                r = orc.evaluate(policy, P, M, 1, tau, tau, method=2)
+                assert r["makespan"] == 2 * (M + P - 1) * tau
+                num, den = r["bub"]
+                assert Fraction(num, den) == Fraction(P - 1, M + P - 1)
+                assert all(r["busy"] == 2 * M * tau)
+
+
+@pytest.mark.parametrize("policy", ["gpipe", "1f1b"])
+def test_tf_tb_closed_form(orc, policy):
+    # "From GPipe to 1F1B and Zero Bubble", Megatron section: bubble overhead
+    # (p-1)(t_f+t_b) on top of the ideal m(t_f+t_b); PipeDream-Flush has the same
+    # bubble.  So total = (m+p-1)(t_f+t_b), e.g. t_b = 2 t_f ("lpnh" article).
+    for P in range(1, 9):
+        for M in (1, 2, 5, 8, 13, 24):
+            for tf, tb in ((1, 2), (2, 4), (3, 1), (2, 5)):
+                r = orc.evaluate(policy, P, M, 1, tf, tb, method=2)
+                assert r["makespan"] == (M + P - 1) * (tf + tb)
+
+
+def test_lpnh_30_4_percent(orc):
+    # lpnh article: P = 8, M = 16 gives a 30.4 % bubble for GPipe.
+    for policy in ("gpipe", "1f1b"):
+        num, den = orc.evaluate(policy, 8, 16, 1, 1, 1)["bub"]
+        assert Fraction(num, den) == Fraction(7, 23)
+        assert round(100 * num / den, 1) == 30.4
+
+
+def test_config1_values(orc):
+    # P=4, M=8, t_f=1, t_b=2: (M+P-1)(t_f+t_b) = 33, busy 24 per stage, bubble 3/11.
+    for policy in ("gpipe", "1f1b"):
+        r = orc.evaluate(policy, 4, 8, 1, 1, 2, method=2)
+        assert r["makespan"] == 33
+        assert list(r["busy"]) == [24] * 4
+        assert list(r["idle"]) == [9] * 4
+        assert r["bub"] == (36, 132)
+    assert list(orc.evaluate("gpipe", 4, 8, 1, 1, 2)["peak"]) == [8, 8, 8, 8]
+    assert list(orc.evaluate("1f1b", 4, 8, 1, 1, 2)["peak"]) == [4, 3, 2, 1]
+
+
+def test_1f1b_phases_and_warmup_conventions(orc):
+    # "2. 1F1B" §2.3/§3.2: stage k runs P-k forwards before its first B, then
+    # M-(P-k) F-B pairs, then P-k backwards.  "Megatron-LM (3)": num_warmup =
+    # P-k-1, then the steady phase starts with a forward; same count.
+    for P in range(1, 9):
+        for M in range(1, 20):
+            kind, _, mb = orc.order("1f1b", P, M)
+            for k in range(P):
+                seq = list(kind[k])
+                first_b = seq.index(1)
+                assert first_b == min(P - k, M)
+                megatron_warmup = min(P - k - 1, M)
+                if M > P - k - 1:
+                    assert seq[megatron_warmup] == 0  # steady phase opens with F
+                if M >= P - k:
+                    w = P - k
+                    steady = seq[w:w + 2 * (M - w)]
+                    assert steady == [1, 0] * (M - w)
+                    assert seq[w + 2 * (M - w):] == [1] * w
+                # oldest outstanding microbatch first
+                bs = [mb[k, j] for j in range(2 * M) if kind[k, j] == 1]
+                assert bs == list(range(M))
+
+
+def test_peaks(orc):
+    # "2. 1F1B" §4.1/§4.5: 1F1B holds P on stage 0 whatever M is; GPipe holds M.
+    for P in range(1, 9):
+        for M in (1, 2, 3, 6, 60, 100):
+            p1 = orc.evaluate("1f1b", P, M, 1, 1, 1)["peak"]
+            assert list(p1) == [min(P - k, M) for k in range(P)]
+            assert max(p1) <= P
+            pg = orc.evaluate("gpipe", P, M, 1, 1, 1)["peak"]
+            assert list(pg) == [M] * P
+
+
+def test_interleaved_bubble_and_divisibility(orc):
+    # "2. 1F1B" §6.1: bubble (P-1)/(V*M+P-1) for interleaved 1F1B.
+    for P in (1, 2, 3, 4, 8):
+        for v in (2, 3, 4):
+            for M in (P, 2 * P, 4 * P):
+                r = orc.evaluate("interleaved", P, M, v, 1, 1, method=2)
+                num, den = r["bub"]
+                assert Fraction(num, den) == Fraction(P - 1, v * M + P - 1)
+    num, den = orc.evaluate("interleaved", 8, 128, 4, 1, 1)["bub"]
+    assert Fraction(num, den) == Fraction(7, 519)
+    # M040 §06: frameworks may require divisibility; M % P != 0 is refused.
+    with pytest.raises(orc.OracleError) as e:
+        orc.order("interleaved", 4, 6, 2)
+    assert e.value.code == orc.ERR_DIVISIBILITY
+
+
+def test_interleaved_placement(orc):
+    # "From GPipe to 1F1B and Zero Bubble", Megatron section; M040 §06: device k
+    # holds virtual stages k, k+P, ...; every device runs each chunk's M F and M B.
+    P, M, v = 4, 8, 2
+    kind, chunk, mb = orc.order("interleaved", P, M, v)
+    for k in range(P):
+        for c in range(v):
+            for kd in (0, 1):
+                sel = (kind[k] == kd) & (chunk[k] == c)
+                assert sorted(mb[k][sel]) == list(range(M))
+
+
+def test_gpipe_comm_invariant(orc):
+    # GPipe with every stage equally fast and uniform comm c: the forward wave
+    # reaches the last stage after (P-1)(t_f+c) + M t_f, the backward wave needs
+    # (P-1)(t_b+c) + M t_b more, so total = (M+P-1)(t_f+t_b) + 2(P-1)c.
+    for P in range(1, 7):
+        for M in (1, 3, 8):
+            for tf, tb, c in ((1, 1, 1), (1, 2, 3), (2, 3, 1)):
+                r = orc.evaluate("gpipe", P, M, 1, tf, tb, comm=c, method=2)
+                assert r["makespan"] == (M + P - 1) * (tf + tb) + 2 * (P - 1) * c
+
+
+def test_bruteforce_optimality(orc):
+    # "2. 1F1B" §4.2/§4.3: no valid order beats 2(M+P-1) at unit cost, and no
+    # order that is not slower holds fewer than min(P, M) activations on stage 0.
+    for P in (1, 2, 3):
+        for M in (1, 2, 3):
+            b = orc.bruteforce(P, M)
+            assert b["min_makespan"] == 2 * (M + P - 1)
+            assert b["min_peak0"] == min(P, M)
+            for policy in ("gpipe", "1f1b"):
+                assert orc.evaluate(policy, P, M, 1, 1, 1)["makespan"] == b["min_makespan"]
+            assert orc.evaluate("1f1b", P, M, 1, 1, 1)["peak"][0] == b["min_peak0"]
+
+
+def test_deadlock_detected_by_both_evaluators(orc):
+    # A cyclic order: stage 0 wants B0 before F1, stage 1 wants F1 before F0.
+    kind = np.array([[0, 1, 0, 1], [0, 1, 0, 1]], np.int32)
+    mb = np.array([[0, 0, 1, 1], [1, 1, 0, 0]], np.int32)
+    chunk = np.zeros((2, 4), np.int32)
+    for method in (0, 1):
+        with pytest.raises(orc.OracleError) as e:
+            orc.eval_explicit(2, 2, 1, kind, chunk, mb, 1, 1, method=method)
+        assert e.value.code == orc.ERR_DEADLOCK
+
+
+def test_des_matches_longest_path_random(orc):
+    rng = np.random.default_rng(123)
+    for _ in range(120):
+        policy = rng.choice(["gpipe", "1f1b", "interleaved"])
+        P = int(rng.integers(1, 7))
+        v = int(rng.integers(2, 4)) if policy == "interleaved" else 1
+        M = P * int(rng.integers(1, 4)) if policy == "interleaved" else int(rng.integers(1, 12))
+        S = P * v
+        tf = rng.integers(0, 9, (S, M))
+        tb = rng.integers(0, 9, (S, M))
+        cm = rng.integers(0, 5, max(S - 1, 1))
+        r = orc.evaluate(policy, P, M, v, tf, tb, comm=cm, method=2)   # raises on mismatch
+        # dependency and overlap invariants checked directly here as well
+        assert r["makespan"] == r["end"].max()
+        for k in range(P):
+            assert np.all(r["start"][k, 1:] >= r["end"][k, :-1])
+
+
+def test_batch_strides_status_and_overflow(orc):
+    rng = np.random.default_rng(5)
+    P, M, n = 3, 4, 6
+    cf = rng.integers(1, 5, (n, P, M)).astype(np.int32)
+    cb = rng.integers(1, 5, (n, P, M)).astype(np.int32)
+    cf[2, 1, 1] = -1
+    cb[4, 0, 0] = 2**31 - 1
+    out = orc.eval_batch("1f1b", P, M, 1, cf, cb, (P * M, M, 1), n=n, method=2)
+    assert out["status"][2] == orc.ST_NEG_COST
+    assert out["status"][4] == orc.ST_OVERFLOW
+    for x in (0, 1, 3, 5):
+        assert out["status"][x] == orc.ST_OK
+        r = orc.evaluate("1f1b", P, M, 1, cf[x], cb[x])
+        assert out["makespan"][x] == r["makespan"]
+        assert list(out["idle"][x]) == list(r["idle"])
+    # instance-minor layout gives the same numbers
+    cfT = np.ascontiguousarray(np.transpose(cf, (1, 2, 0)))
+    cbT = np.ascontiguousarray(np.transpose(cb, (1, 2, 0)))
+    out2 = orc.eval_batch("1f1b", P, M, 1, cfT, cbT, (1, M * n, n), n=n)
+    assert np.array_equal(out["makespan"], out2["makespan"])
+    assert np.array_equal(out["status"], out2["status"])
+
+
+def test_splitmix64_published_vector(orc):
+    g = read_golden("splitmix64_seed0.txt")
+    gamma = 0x9E3779B97F4A7C15
+    for n_str, (val,) in g.items():
+        n = int(n_str)
+        assert orc.splitmix64((gamma * n) % 2**64) == int(val, 16)
+
+
+def test_binom_and_unranking(orc):
+    assert orc.binom(79, 7) == math.comb(79, 7) == 2898753715
+    for n in range(0, 30):
+        for k in range(0, 8):
+            assert orc.binom(n, k) == math.comb(n, k)
+    # colex unranking against explicit enumeration: sort all K-subsets of
+    # range(N) by their reversed tuple; rank r is the r-th subset.
+    for N, K in ((7, 2), (9, 3), (10, 4)):
+        subsets = sorted(itertools.combinations(range(N), K), key=lambda s: s[::-1])
+        L, P = N + 1, K + 1
+        tot = math.comb(N, K)
+        for c in range(60):
+            u = orc.splitmix64(77 + c)
+            first = orc.candidate_split(77, c, L, P)
+            x = subsets[u % tot]
+            assert list(first) == [0] + [xi + 1 for xi in x] + [L]
+
+
+def test_search_finds_global_optimum_small(orc):
+    rng = np.random.default_rng(9)
+    L, P, M = 8, 3, 6
+    ltf = rng.integers(5, 15, L).astype(np.int32)
+    ltb = (2 * ltf).astype(np.int32)
+    lact = rng.integers(1, 4, L).astype(np.int64)
+    # brute force over every contiguous split with itertools
+    best = None
+    for cuts in itertools.combinations(range(1, L), P - 1):
+        bounds = [0, *cuts, L]
+        tf = [int(ltf[bounds[k]:bounds[k + 1]].sum()) for k in range(P)]
+        tb = [int(ltb[bounds[k]:bounds[k + 1]].sum()) for k in range(P)]
+        r = orc.evaluate("1f1b", P, M, 1, np.repeat(np.array(tf)[:, None], M, 1),
+                         np.repeat(np.array(tb)[:, None], M, 1))
+        if best is None or r["makespan"] < best:
+            best = r["makespan"]
+    res = orc.search(ltf, ltb, lact, P, M, 0, 10**12, 42, 0, 3000)
+    assert res["best_makespan"] == best
+    assert res["all_makespan"][res["best_idx"]] == best
+    assert res["all_makespan"].min() == best
+    assert res["first"][0] == 0 and res["first"][-1] == L
+    # the cap rejects splits: peak_k * act_k must stay <= cap
+    tight = orc.search(ltf, ltb, lact, P, M, 0, 0, 42, 0, 50)
+    assert tight["best_idx"] == -1 and (tight["all_makespan"] == -1).all()
+
+
+MUTANTS = {
+    1: "forward edges carry no comm",
+    2: "1F1B warmup off by one",
+    3: "GPipe backward FIFO",
+    4: "B ignores downstream gradient",
+    5: "ledger sign flipped",
+    6: "bubble over ideal time",
+    7: "splitmix64 shift mistyped",
+    8: "unranking off by one",
+}
+
+
+def _pin_suite(orc, lib):
+    """Run a compact version of the pins above against a given library;
+    returns the list of pins that fail."""
+    failed = []
+
+    def check(name, fn):
+        try:
+            ok = fn()
+        except Exception:
+            ok = False
+        if not ok:
+            failed.append(name)
+
+    def tables():
+        for policy, fx in (("gpipe", "m040_gpipe_2x4.txt"), ("1f1b", "m040_1f1b_2x4.txt")):
+            g = read_golden(fx)
+            r = orc.evaluate(policy, 2, 4, 1, 1, 1, lib=lib)
+            if _table_from_oracle(r, 2) != [g["stage0"], g["stage1"]]:
+                return False
+            if r["peak"][0] != int(g["peak_stage0"][0]):
+                return False
+        return True
+
+    def closed():
+        for policy in ("gpipe", "1f1b"):
+            r = orc.evaluate(policy, 4, 8, 1, 1, 1, lib=lib)
+            if r["makespan"] != 22 or Fraction(*r["bub"]) != Fraction(3, 11):
+                return False
+        return True
+
+    def comm():
+        r = orc.evaluate("gpipe", 4, 3, 1, 1, 2, comm=3, lib=lib)
+        return r["makespan"] == 6 * 3 + 2 * 3 * 3
+
+    def phases():
+        kind, _, _ = orc.order("1f1b", 4, 8, lib=lib)
+        return [list(kind[k]).index(1) for k in range(4)] == [4, 3, 2, 1]
+
+    def sm():
+        return orc.splitmix64(0, lib=lib) == 0xE220A8397B1DCDAF
+
+    def unrank():
+        subsets = sorted(itertools.combinations(range(9), 3), key=lambda s: s[::-1])
+        for c in range(40):
+            first = orc.candidate_split(5, c, 10, 4, lib=lib)
+            x = subsets[orc.splitmix64(5 + c, lib=lib) % math.comb(9, 3)]
+            if list(first) != [0] + [xi + 1 for xi in x] + [10]:
+                return False
+        return True
+
+    check("tables", tables)
+    check("closed", closed)
+    check("comm", comm)
+    check("phases", phases)
+    check("splitmix", sm)
+    check("unrank", unrank)
+    return failed
+
+
+def test_pins_pass_on_oracle(orc):
+    assert _pin_suite(orc, orc.load()) == []
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS))
+def test_pins_catch_planted_mistakes(orc, mutant):
+    with tempfile.TemporaryDirectory() as td:
+        path = os.path.join(td, f"liborc_m{mutant}.so")
+        orc.build(path, defines=(f"ORC_MUTANT={mutant}",))
+        lib = orc.load(path)
+        failed = _pin_suite(orc, lib)
+    assert failed, f"mutant {mutant} ({MUTANTS[mutant]}) passed every pin"
