@@ -1,0 +1,396 @@
+"""Benchmark: schedule op-times resolved per second on the heterogeneous 1F1B
+batch (P=8 stages, M=64 microbatches, 65,536 instances; t_f ~ U[80,120],
+t_b ~ U[160,240], comm ~ U[2,8]), with the HBM roofline of the evaluator
+kernel, the CPU oracle as a baseline, and an end-to-end number through the
+public host API.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+One step = one pp_sched_eval over the whole batch (op order from the cached
+plan, max-plus times, reductions to makespan / idle / bubble, peak held
+activations), inputs already resident in HBM.  N > 1 runs one process per GPU
+(torchrun); each rank evaluates its own batch (weak scaling, no collective on
+the data path); the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+P, M, N_INST = 8, 64, 65536
+METRIC = "schedule op-times resolved/sec (1F1B, P=8, M=64 batch); HBM GB/s vs peak"
+UNIT = "op-times/s"
+L2_BYTES = 129 * 10**6
+
+
+def algorithmic_bytes(n, P_=P, M_=M):
+    """Bytes one evaluation must move: every cost read once, every comm value
+    read once, and the summary outputs written once."""
+    costs = 2 * P_ * M_ * n * 4
+    comm = (P_ - 1) * n * 4
+    outs = n * 4 + n * P_ * 4 + 2 * n * 8 + n * 1 + P_ * 4  # makespan, idle, bub pair, status, peak
+    return costs + comm + outs
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clock sampling during the timed region (NVML through ctypes, read-only)
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, device_index):
+        self.samples = []
+        self.max_mhz = None
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            got = False
+            try:
+                import torch
+                uuid = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+                got = nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0
+            except Exception:
+                got = False
+            if not got:
+                vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+                idx = int(vis.split(",")[device_index]) if vis and vis.split(",")[device_index].isdigit() else device_index
+                if nv.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(h)) != 0:
+                    return
+            self.nv, self.h = nv, h
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._reason_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _run(self):
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) == 0 and \
+                    self._reason_fn(self.h, ctypes.byref(r)) == 0:
+                self.samples.append((c.value, r.value))
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": "nvml unavailable"}
+        mhz = [s[0] for s in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        reasons = [name for b, name in self.REASONS.items() if bits & b]
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(self.samples), "source": "nvml during timed region"}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle baseline (bounded sample of the same workload)
+# ---------------------------------------------------------------------------
+
+def oracle_baseline(batch, target_s=10.0, max_inst=None):
+    import oracle
+    threads = os.cpu_count() or 1
+    # calibrate on a small chunk, then run a sample sized for ~target_s of wall time
+    def run(n):
+        sub_f = batch.cost_f.reshape(P, M, batch.n)[:, :, :n]
+        sub_b = batch.cost_b.reshape(P, M, batch.n)[:, :, :n]
+        sub_c = batch.comm.reshape(P - 1, batch.n)[:, :n]
+        cf = np.ascontiguousarray(sub_f).reshape(-1)
+        cb = np.ascontiguousarray(sub_b).reshape(-1)
+        cm = np.ascontiguousarray(sub_c).reshape(-1)
+        t0 = time.perf_counter()
+        oracle.eval_batch(1, P, M, 1, cf, cb, (1, M * n, n), comm=cm, comm_strides=(1, n), n=n,
+                          method=0, nthreads=threads)
+        return time.perf_counter() - t0
+    n0 = min(batch.n, 64 * threads)
+    t0 = run(n0)
+    n = int(min(batch.n, max(n0, n0 * target_s / max(t0, 1e-6))))
+    if max_inst:
+        n = min(n, max_inst)
+    t = run(n)
+    ops = 2 * P * M * n
+    return {"value": ops / t, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"first {n} of the {batch.n} instances (1F1B P={P} M={M}), event simulation "
+                      f"only, {threads} threads, {t:.2f} s wall",
+            "seconds": t, "instances": n}
+
+
+# ---------------------------------------------------------------------------
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--n", type=int, default=N_INST)
+    ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    return rank, world, local
+
+
+def reference_arm(args):
+    """The oracle, as it stands, on this machine's host cores: each step is a
+    bounded sample of the same workload."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import pipeline_schedule_simulation_gb300.workloads as W
+    batch = W.config3(n=args.n)
+    threads = os.cpu_count() or 1
+    per_step = None
+    times = []
+    for i in range(args.warmup + args.steps):
+        r = oracle_baseline(batch, target_s=2.0, max_inst=per_step)
+        per_step = r["instances"]
+        if i >= args.warmup:
+            times.append(r["seconds"])
+    total = sum(times)
+    ops = 2 * P * M * per_step * len(times)
+    value = ops / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
+        "data": "synthetic",
+        "config": {"workload": f"1f1b_hetero_P{P}_M{M}_n{args.n}", "sample_instances_per_step": per_step},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"first {per_step} instances per step, event simulation, {threads} threads"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    import torch.distributed as dist
+
+    import pipeline_schedule_simulation_gb300.workloads as W
+    from pipeline_schedule_simulation_gb300 import binding as B
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    batch = W.config3(n=args.n, seed=3 + rank)
+    n = batch.n
+    dev = lambda a: torch.from_numpy(a).cuda()  # noqa: E731
+    cf, cb, cm = dev(batch.cost_f), dev(batch.cost_b), dev(batch.comm)
+    outs = {"makespan": torch.empty(n, dtype=torch.int32, device="cuda"),
+            "idle": torch.empty((n, P), dtype=torch.int32, device="cuda"),
+            "bub_num": torch.empty(n, dtype=torch.int64, device="cuda"),
+            "bub_den": torch.empty(n, dtype=torch.int64, device="cuda"),
+            "peak": torch.empty(P, dtype=torch.int32, device="cuda"),
+            "status": torch.empty(n, dtype=torch.int8, device="cuda")}
+    stream = torch.cuda.current_stream()
+
+    def step():
+        B.evaluate(batch.policy, P, M, 1, cf, cb, batch.strides, n, comm=cm,
+                   comm_strides=batch.comm_strides, out=outs, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert int(outs["status"].max()) == 0
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_all0, t_all1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    with sampler:
+        t_all0.record(stream)
+        for i in range(K):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        t_all1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    elapsed = t_all0.elapsed_time(t_all1) / 1e3
+    kern = [a.elapsed_time(b) / 1e3 for a, b in ev]
+    if world > 1:
+        t = torch.tensor([elapsed], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    ops_step = 2 * P * M * n
+    value = world * ops_step * K / elapsed
+    kavg = statistics.mean(kern)
+    peak_gbs, peak_src = measured_peaks()
+    abytes = algorithmic_bytes(n)
+    achieved = abytes / kavg / 1e9
+
+    # ----- end to end through the public host API (pinned host buffers) -----
+    host_f = torch.from_numpy(batch.cost_f).pin_memory()
+    host_b = torch.from_numpy(batch.cost_b).pin_memory()
+    host_c = torch.from_numpy(batch.comm).pin_memory()
+    staging = {}
+    for _ in range(2):
+        B.evaluate_host(batch.policy, P, M, 1, host_f, host_b, batch.strides, n, comm=host_c,
+                        comm_strides=batch.comm_strides, stream=stream, staging=staging)
+    torch.cuda.synchronize()
+    Ke = max(3, min(K, 100))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    h2d = d2h = 0
+    for _ in range(Ke):
+        _, h2d, d2h = B.evaluate_host(batch.policy, P, M, 1, host_f, host_b, batch.strides, n,
+                                      comm=host_c, comm_strides=batch.comm_strides, stream=stream,
+                                      staging=staging)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        t = torch.tensor([e2e_s], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = {"value": world * ops_step * Ke / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "steps": Ke,
+           "api": "binding.evaluate_host (pinned host buffers -> pp_sched_eval -> host)"}
+
+    extra = {}
+    if not args.no_extra and rank == 0:
+        extra = secondary(B, W, torch, stream)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+            "config": {"workload": f"1f1b_hetero_P{P}_M{M}_n{n}", "P": P, "M": M,
+                       "instances_per_gpu": n, "layout": "instance-minor [S][M][n]",
+                       "l2": f"inputs {2 * P * M * n * 4 / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB, no flush",
+                       "parallelism": f"instance-sharded x{world}"},
+            "gpu_launches": K,
+            "roofline": {"bound": "hbm", "kernel": "k_eval_reg<8,true,false>", "achieved": achieved,
+                         "peak": peak_gbs, "unit": "GB/s", "frac": achieved / peak_gbs,
+                         "peak_source": peak_src, "traffic": None,
+                         "algorithmic_bytes_per_launch": abytes, "avg_launch_us": kavg * 1e6},
+            "instances_per_s": world * n * K / elapsed,
+            "clocks": sampler.summary(),
+            "e2e": e2e,
+        }
+        if not args.no_cpu:
+            line["cpu_baseline"] = {k: v for k, v in oracle_baseline(batch).items()
+                                    if k not in ("seconds", "instances")}
+        if extra:
+            line["secondary"] = extra
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def secondary(B, W, torch, stream):
+    """Short timings of the other workloads (not the headline)."""
+    out = {}
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 1e3 / reps
+
+    # per-op start/end stored (instance-minor op layout)
+    b3 = W.config3(n=N_INST)
+    cf, cb, cm = (torch.from_numpy(x).cuda() for x in (b3.cost_f, b3.cost_b, b3.comm))
+    O = 2 * M
+    ops_out = {"op_start": torch.empty((P, O, N_INST), dtype=torch.int32, device="cuda"),
+               "op_end": torch.empty((P, O, N_INST), dtype=torch.int32, device="cuda")}
+    t = timed(lambda: B.evaluate(1, P, M, 1, cf, cb, b3.strides, N_INST, comm=cm, comm_strides=b3.comm_strides,
+                                 op_times=True, op_strides=(1, N_INST), out=ops_out, stream=stream), 20)
+    out["1f1b_P8_M64_with_op_times"] = {"op_times_per_s": 2 * P * M * N_INST / t, "ms": t * 1e3}
+    del ops_out, cf, cb, cm
+    for v in (2, 4):
+        il, base = W.config4(v)
+        for tag, bt in (("interleaved", il), ("1f1b_equal_work", base)):
+            f, g, c = (torch.from_numpy(x).cuda() for x in (bt.cost_f, bt.cost_b, bt.comm))
+            t = timed(lambda: B.evaluate(bt.policy, bt.P, bt.M, bt.v, f, g, bt.strides, bt.n, comm=c,
+                                         comm_strides=bt.comm_strides, stream=stream), 20)
+            out[f"{tag}_P8_v{v}_M128_n16384"] = {"op_times_per_s": bt.op_times / t, "ms": t * 1e3}
+    p = W.config5()
+    lt, lb, la = (torch.from_numpy(x).cuda() for x in (p.layer_tf, p.layer_tb, p.layer_act))
+    res = {}
+    t = timed(lambda: res.update(B.partition_search(lt, lb, la, p.P, p.M, p.comm, p.cap, p.seed, 0,
+                                                    p.n_cand, stream=stream)), 5)
+    out["partition_search_L80_P8_M128_1M"] = {
+        "candidates_per_s": p.n_cand / t, "ms": t * 1e3,
+        "best_idx": int(res["best_idx"].item()), "best_makespan": int(res["best_makespan"].item()),
+        "best_cuts": res["best_cuts"].cpu().tolist()}
+    return out
+
+
+if __name__ == "__main__":
+    sys.exit(main())

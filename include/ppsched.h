@@ -1,0 +1,198 @@
+/*
+ * ppsched.h -- C ABI of libppsched, a GB300 (sm_103a) batched evaluator of
+ * pipeline-parallel training schedules: GPipe, synchronous 1F1B
+ * (PipeDream-Flush) and interleaved 1F1B.
+ *
+ * Sources, by page title and section (short names in brackets):
+ *   [1F1B]      "2. 1F1B" (sgdbs.github.io, AI_Infra / 2.PipelineParallel / OneF1B)
+ *   [GPipe->ZB] "Pipeline parallelism: from GPipe to 1F1B and Zero Bubble" (dlog.com.cn)
+ *   [M040]      "Pipeline scheduling: GPipe, 1F1B, interleaving and compute-communication
+ *               overlap" (xuujii.github.io, ai-infra-kb M040)
+ *   [Megatron3] "Megatron-LM distributed training (3): pipeline parallelism PP and
+ *               1F1B scheduling" (swordlidev.github.io)
+ *   [lpnh]      lpnh.cn news 2768528 (GPipe / 1F1B / interleaved formulas, 80-layer model)
+ *
+ * The problem ([GPipe->ZB] Megatron section; [M040] §04; [lpnh]): P pipeline
+ * stages (devices), M microbatches, v model chunks per device (interleaved
+ * only; S = P*v virtual stages, device k holds virtual stages k, k+P, ...),
+ * a forward cost t_f and backward cost t_b per (virtual stage, microbatch) and
+ * a latency `comm` per stage boundary.  Dependencies ([GPipe->ZB] GPipe figure
+ * text; [M040] §01, §08): F(s,i) needs F(s-1,i); B(s,i) needs B(s+1,i) and
+ * F(s,i); a device runs one op at a time, in its schedule's order; a result
+ * crossing boundary b (between virtual stages b and b+1) arrives comm[b] ticks
+ * after its op ends.  Every op starts at the earliest tick its device is free
+ * and its inputs have arrived (max-plus longest path).
+ *
+ * Conventions for every entry point:
+ *   - Indices are 0-based.  O = 2*M*v ops per device; op position j indexes a
+ *     device's order.
+ *   - All times are int32 ticks; costs and comm must be >= 0.
+ *   - Array arguments are caller-owned DEVICE memory unless stated otherwise.
+ *   - Calls are asynchronous on `stream`.  pp_sched_eval and
+ *     pp_sched_partition_search allocate nothing once the plan for their shape
+ *     exists (pp_sched_plan, or the first call for that shape, builds it; that
+ *     first call allocates device memory and synchronizes `stream`).
+ *   - Return value: PP_OK or a PP_ERR_* code (argument errors are detected on the
+ *     host before anything is launched).  Per-instance data problems are written
+ *     to the optional `status` array instead.
+ *   - One GPU: the library works on the calling thread's current device.
+ */
+#ifndef PPSCHED_H
+#define PPSCHED_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PPSCHED_ABI_VERSION 1
+
+/* Schedule policies.
+ *  PP_GPIPE: every device runs F of microbatches 0..M-1, then B of M-1..0
+ *    ([M040] §02 table: backwards from D to A).
+ *  PP_1F1B: device k runs w = min(P-k, M) forwards, then M-w (B, F) pairs with
+ *    the oldest outstanding B first, then the remaining w backwards ([1F1B] §2.3,
+ *    §3.2 table; [Megatron3] "three phases": num_warmup = P-k-1 plus the first
+ *    steady F is the same sequence).
+ *  PP_INTERLEAVED_1F1B: v > 1 chunks per device; warmup 2(P-k-1)+(v-1)P forwards
+ *    (capped at M*v), then (F, B) pairs, then the remaining B; forward j is chunk
+ *    (j mod Pv)/P of microbatch (j/(Pv))*P + j mod P, backward j is chunk
+ *    v-1-(j mod Pv)/P of the same microbatch.  Requires M % P == 0 ([M040] §06).
+ *    The pages give the bubble, (P-1)/(vM+P-1) ([1F1B] §6.1), not the order; this
+ *    order is the Megatron interleaved schedule they refer to. */
+typedef enum {
+    PP_GPIPE = 0,
+    PP_1F1B = 1,
+    PP_INTERLEAVED_1F1B = 2
+} pp_policy_t;
+
+/* Return codes. */
+#define PP_OK 0
+#define PP_ERR_ARG 1           /* bad argument: P, M or v < 1, v != 1 for GPipe/1F1B,
+                                  v < 2 for interleaved, NULL required pointer,
+                                  n < 0, bad stride or alignment */
+#define PP_ERR_DIVISIBILITY 2  /* interleaved with M % P != 0 */
+#define PP_ERR_SIZE 3          /* shape beyond the limits below */
+#define PP_ERR_CUDA 4          /* a CUDA runtime call failed */
+#define PP_ERR_DEADLOCK 5      /* the generated order cannot run (internal check) */
+#define PP_ERR_INTERNAL 6      /* an internal consistency check failed */
+
+/* Per-instance status (int8) written by pp_sched_eval when `status` != NULL.
+ * The other outputs of a flagged instance are unspecified. */
+#define PP_ST_OK 0
+#define PP_ST_NEG_COST 1       /* some cost or comm of the instance is negative */
+#define PP_ST_OVERFLOW 2       /* some tick would exceed INT32_MAX (detected, not wrapped) */
+
+/* Limits. */
+#define PP_MAX_P 16            /* devices */
+#define PP_MAX_S 64            /* virtual stages P*v */
+#define PP_MAX_MV 32768        /* microbatches x chunks (ops per device = 2*M*v) */
+
+/* Packed op, as returned by pp_sched_plan_ops: bit 31 = kind (0 = F, 1 = B),
+ * bits 24..30 = chunk, bits 0..23 = microbatch. */
+#define PP_OP_KIND(x) ((int)(((uint32_t)(x)) >> 31))
+#define PP_OP_CHUNK(x) ((int)((((uint32_t)(x)) >> 24) & 0x7Fu))
+#define PP_OP_MB(x) ((int)(((uint32_t)(x)) & 0xFFFFFFu))
+
+/* Opaque plan: the schedule of one (policy, P, M, v), built on the GPU. */
+typedef struct pp_plan pp_plan_t;
+
+/* Build the plan for (policy, P, M, v) on the current device: the per-device op
+ * order, each op's wavefront round (its start tick at unit cost, which is a
+ * topological order of the dependency graph), the per-round op table the
+ * evaluator walks, and the peak held-activation count per device ([1F1B] §4.1
+ * ledger).  Allocates device memory and synchronizes `stream`.
+ * *plan receives a library-owned object; free it with pp_sched_plan_destroy.
+ * Errors: PP_ERR_ARG, PP_ERR_DIVISIBILITY, PP_ERR_SIZE, PP_ERR_DEADLOCK, PP_ERR_CUDA. */
+int pp_sched_plan(pp_policy_t policy, int P, int M, int v, pp_plan_t **plan, cudaStream_t stream);
+
+/* Plan facts: info[0] = rounds (unit-cost makespan), info[1] = ops per device,
+ * info[2] = dependency value slots the generic evaluator needs, info[3] = 1 if the
+ * register evaluator applies (GPipe, 1F1B), info[4] = P, info[5] = M, info[6] = v,
+ * info[7] = policy.  `info` is host memory of 8 int32. */
+int pp_sched_plan_info(const pp_plan_t *plan, int32_t *info);
+
+/* Copy the plan to HOST memory: host_ops [P][2Mv] packed ops (see PP_OP_*),
+ * host_peak [P] peak held activations per device, host_round [P][2Mv] each op's
+ * wavefront round.  Any pointer may be NULL.  Synchronous. */
+int pp_sched_plan_ops(const pp_plan_t *plan, uint32_t *host_ops, int32_t *host_peak, int32_t *host_round);
+
+/* Free a plan (NULL is ignored).  The caller must not use it in flight. */
+void pp_sched_plan_destroy(pp_plan_t *plan);
+
+/* Evaluate n_instances schedule instances of one policy and shape.
+ *
+ * Inputs (device, int32):
+ *   cost_f, cost_b: forward / backward cost of (instance x, virtual stage s,
+ *     microbatch i) at element offset x*stride_inst + s*stride_stage + i*stride_mb.
+ *     Strides may be 0 (broadcast).  The fast path wants stride_inst == 1 (the
+ *     instance-minor layout [S][M][n], every load coalesced and 128-bit wide) with
+ *     16-byte aligned bases and stride_stage, stride_mb multiples of 4; any other
+ *     layout is accepted and gathered 4 bytes at a time.
+ *   comm: latency of boundary b (virtual stages b and b+1) for instance x at
+ *     x*comm_stride_inst + b*comm_stride_bnd, b < S-1; NULL means 0 everywhere.
+ * Outputs (device; each may be NULL):
+ *   makespan [n]          last end tick over all devices ([M040] §04 window time)
+ *   idle [n][P]           makespan minus the device's summed op costs
+ *   bub_num, bub_den [n]  exact bubble fraction = sum of idle / (P * makespan)
+ *                         ([1F1B] §4.3; [M040] §04), unreduced; both 0 when the
+ *                         makespan is 0
+ *   peak [P]              peak held activations per device (cost-independent)
+ *   op_start, op_end      each op's start / end tick at element offset
+ *                         x*op_stride_inst + (k*O + j)*op_stride_op
+ *   status [n]            PP_ST_* per instance
+ * Errors: PP_ERR_ARG, PP_ERR_DIVISIBILITY, PP_ERR_SIZE, PP_ERR_CUDA, plus the plan
+ * errors on a shape's first call. */
+int pp_sched_eval(pp_policy_t policy, int P, int M, int v,
+                  const int32_t *cost_f, const int32_t *cost_b,
+                  int64_t stride_inst, int64_t stride_stage, int64_t stride_mb,
+                  const int32_t *comm, int64_t comm_stride_inst, int64_t comm_stride_bnd,
+                  int64_t n_instances,
+                  int32_t *makespan, int32_t *idle, int64_t *bub_num, int64_t *bub_den,
+                  int32_t *peak,
+                  int32_t *op_start, int32_t *op_end, int64_t op_stride_inst, int64_t op_stride_op,
+                  int8_t *status, cudaStream_t stream);
+
+/* Score contiguous layer-to-stage partitions under 1F1B and return the best.
+ * This is the profiling-based load balancing of [GPipe->ZB] (PipeDream and GPipe
+ * sections: split layers into stages by measured cost) and [M040] §05, on the
+ * [lpnh] workload (80 layers into 8 stages).
+ *
+ * Candidate c (c = cand_begin .. cand_begin+n_cand-1) is the split obtained by
+ *   u = SplitMix64 output for state seed + c (Steele, Lea & Flood 2014),
+ *   r = u mod C(L-1, P-1), and r unranked in colex order to cut positions
+ *   x_1 < ... < x_{P-1} in [0, L-1); stage t starts at layer x_t + 1.
+ * Stage k's forward cost is the sum of its layers' layer_tf, backward cost the
+ * sum of layer_tb, activation bytes the sum of layer_act; every boundary has
+ * latency `comm`.  A candidate is rejected when some stage's peak held
+ * activations under 1F1B times its activation bytes exceeds act_cap.  The rest
+ * are evaluated with M microbatches and the argmin (makespan, candidate index)
+ * is returned.
+ *
+ * Inputs (device): layer_tf, layer_tb int32 [L]; layer_act int64 [L].
+ * Outputs (device): best_idx int64 [1] (-1 if nothing is feasible),
+ *   best_makespan int32 [1] (-1 then), best_cuts int32 [P-1] (first layer of
+ *   stages 1..P-1; -1 then), all_makespan int32 [n_cand] or NULL (makespan, -1 if
+ *   rejected by the cap, -2 if a tick would exceed INT32_MAX).
+ * Limits: 1 <= P <= PP_MAX_P, P <= L <= 256, 0 <= n_cand < 2^32.
+ * Errors: PP_ERR_ARG, PP_ERR_SIZE, PP_ERR_CUDA. */
+int pp_sched_partition_search(const int32_t *layer_tf, const int32_t *layer_tb,
+                              const int64_t *layer_act, int L, int P, int M, int32_t comm,
+                              int64_t act_cap, uint64_t seed, int64_t cand_begin, int64_t n_cand,
+                              int64_t *best_idx, int32_t *best_makespan, int32_t *best_cuts,
+                              int32_t *all_makespan, cudaStream_t stream);
+
+/* Human-readable name of a PP_ERR_* return code. */
+const char *pp_sched_status_str(int code);
+
+/* Free every cached plan of the calling process (all devices).  Not safe while
+ * evaluations are in flight. */
+void pp_sched_cache_clear(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PPSCHED_H */

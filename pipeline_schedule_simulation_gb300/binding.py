@@ -1,0 +1,233 @@
+"""ctypes binding of libppsched (include/ppsched.h): argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels.  PyTorch
+provides device memory and streams.  There is no CPU fallback: if the library
+has not been built, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build_lib
+
+GPIPE, ONEF1B, INTERLEAVED = 0, 1, 2
+POLICIES = {"gpipe": GPIPE, "1f1b": ONEF1B, "interleaved": INTERLEAVED}
+
+PP_OK, PP_ERR_ARG, PP_ERR_DIVISIBILITY, PP_ERR_SIZE, PP_ERR_CUDA, PP_ERR_DEADLOCK, PP_ERR_INTERNAL = range(7)
+ST_OK, ST_NEG_COST, ST_OVERFLOW = 0, 1, 2
+
+EXPORTS = ("pp_sched_plan", "pp_sched_plan_info", "pp_sched_plan_ops", "pp_sched_plan_destroy",
+           "pp_sched_eval", "pp_sched_partition_search", "pp_sched_status_str",
+           "pp_sched_cache_clear")
+
+
+class PPSchedError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_str(code)} (code {code})")
+
+
+def _load():
+    path = build_lib.LIB
+    if not os.path.exists(path):
+        raise ImportError(
+            f"libppsched.so is not built ({path}); run __graft_entry__.build() or "
+            "python -m pipeline_schedule_simulation_gb300.build_lib")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64
+    lib.pp_sched_plan.argtypes = [i32, i32, i32, i32, ctypes.POINTER(vp), vp]
+    lib.pp_sched_plan.restype = i32
+    lib.pp_sched_plan_info.argtypes = [vp, vp]
+    lib.pp_sched_plan_info.restype = i32
+    lib.pp_sched_plan_ops.argtypes = [vp, vp, vp, vp]
+    lib.pp_sched_plan_ops.restype = i32
+    lib.pp_sched_plan_destroy.argtypes = [vp]
+    lib.pp_sched_plan_destroy.restype = None
+    lib.pp_sched_eval.argtypes = [i32, i32, i32, i32, vp, vp, i64, i64, i64, vp, i64, i64, i64,
+                                  vp, vp, vp, vp, vp, vp, vp, i64, i64, vp, vp]
+    lib.pp_sched_eval.restype = i32
+    lib.pp_sched_partition_search.argtypes = [vp, vp, vp, i32, i32, i32, ctypes.c_int32, i64, u64,
+                                              i64, i64, vp, vp, vp, vp, vp]
+    lib.pp_sched_partition_search.restype = i32
+    lib.pp_sched_status_str.argtypes = [i32]
+    lib.pp_sched_status_str.restype = ctypes.c_char_p
+    lib.pp_sched_cache_clear.argtypes = []
+    lib.pp_sched_cache_clear.restype = None
+    return lib
+
+
+LIB = _load()
+
+
+def status_str(code: int) -> str:
+    return LIB.pp_sched_status_str(code).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != PP_OK:
+        raise PPSchedError(rc, where)
+
+
+def _policy(p) -> int:
+    return POLICIES[p] if isinstance(p, str) else int(p)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class Plan:
+    """A library-owned plan (pp_sched_plan); freed when garbage-collected."""
+
+    def __init__(self, policy, P, M, v=1, stream=None):
+        self._h = ctypes.c_void_p()
+        _check(LIB.pp_sched_plan(_policy(policy), P, M, v, ctypes.byref(self._h), _stream(stream)),
+               "pp_sched_plan")
+        info = (ctypes.c_int32 * 8)()
+        _check(LIB.pp_sched_plan_info(self._h, info), "pp_sched_plan_info")
+        self.rounds, self.ops_per_device, self.value_slots, self.register_path = info[0:4]
+        self.P, self.M, self.v, self.policy = info[4:8]
+
+    def tables(self):
+        """Host copies: (ops uint32 [P][O], peak int32 [P], round int32 [P][O])."""
+        O = self.ops_per_device
+        ops = torch.zeros(self.P * O, dtype=torch.int64)
+        buf = (ctypes.c_uint32 * (self.P * O))()
+        peak = (ctypes.c_int32 * self.P)()
+        rnd = (ctypes.c_int32 * (self.P * O))()
+        _check(LIB.pp_sched_plan_ops(self._h, buf, peak, rnd), "pp_sched_plan_ops")
+        ops = torch.tensor(list(buf), dtype=torch.int64).reshape(self.P, O)
+        return ops, torch.tensor(list(peak), dtype=torch.int32), \
+            torch.tensor(list(rnd), dtype=torch.int32).reshape(self.P, O)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            LIB.pp_sched_plan_destroy(h)
+            self._h = None
+
+
+def op_fields(ops):
+    """Split packed ops (PP_OP_* layout) into (kind, chunk, microbatch)."""
+    ops = ops.to(torch.int64)
+    return (ops >> 31) & 1, (ops >> 24) & 0x7F, ops & 0xFFFFFF
+
+
+def evaluate(policy, P, M, v, cost_f, cost_b, strides, n, comm=None, comm_strides=(0, 0),
+             outputs=("makespan", "idle", "bub_num", "bub_den", "peak", "status"),
+             op_times=False, op_strides=None, out=None, stream=None):
+    """Call pp_sched_eval on DEVICE tensors.
+
+    cost_f / cost_b / comm are int32 CUDA tensors addressed through element
+    strides (see the header).  Returns a dict of int32/int64/int8 CUDA tensors;
+    `out` may supply preallocated ones.  op_times adds op_start / op_end
+    [n][P][O] (or through op_strides = (inst, op))."""
+    pol = _policy(policy)
+    dev = cost_f.device
+    out = dict(out or {})
+    O = 2 * M * v
+
+    def want(name, shape, dtype):
+        if name in out:
+            return out[name]
+        t = torch.empty(shape, dtype=dtype, device=dev)
+        out[name] = t
+        return t
+
+    mk = want("makespan", (n,), torch.int32) if "makespan" in outputs else None
+    idle = want("idle", (n, P), torch.int32) if "idle" in outputs else None
+    bn = want("bub_num", (n,), torch.int64) if "bub_num" in outputs else None
+    bd = want("bub_den", (n,), torch.int64) if "bub_den" in outputs else None
+    pk = want("peak", (P,), torch.int32) if "peak" in outputs else None
+    stt = want("status", (n,), torch.int8) if "status" in outputs else None
+    os_ = oe = None
+    if op_times:
+        os_ = want("op_start", (n, P, O), torch.int32)
+        oe = want("op_end", (n, P, O), torch.int32)
+        if op_strides is None:
+            op_strides = (P * O, 1)
+    else:
+        op_strides = (0, 0)
+    rc = LIB.pp_sched_eval(pol, P, M, v, _ptr(cost_f), _ptr(cost_b), strides[0], strides[1], strides[2],
+                           _ptr(comm), comm_strides[0], comm_strides[1], n,
+                           _ptr(mk), _ptr(idle), _ptr(bn), _ptr(bd), _ptr(pk), _ptr(os_), _ptr(oe),
+                           op_strides[0], op_strides[1], _ptr(stt), _stream(stream))
+    _check(rc, "pp_sched_eval")
+    return out
+
+
+def evaluate_host(policy, P, M, v, cost_f, cost_b, strides, n, comm=None, comm_strides=(0, 0),
+                  device="cuda", stream=None, staging=None):
+    """End-to-end call from HOST buffers (the public entry for CPU-resident
+    inputs): copies the inputs to the device, calls pp_sched_eval and copies
+    the summary outputs back, all on one stream.  `staging` may hold reusable
+    device buffers (dict) to avoid re-allocation across calls.  Returns
+    (outputs on host, bytes host->device, bytes device->host)."""
+    staging = staging if staging is not None else {}
+    s = stream or torch.cuda.current_stream()
+
+    def dev_copy(name, t):
+        if t is None:
+            return None
+        d = staging.get(name)
+        if d is None or d.numel() != t.numel() or d.dtype != t.dtype:
+            d = torch.empty(t.shape, dtype=t.dtype, device=device)
+            staging[name] = d
+        d.copy_(t, non_blocking=True)
+        return d
+
+    h2d = 0
+    with torch.cuda.stream(s):
+        df = dev_copy("cost_f", cost_f)
+        db = dev_copy("cost_b", cost_b)
+        dc = dev_copy("comm", comm)
+        h2d = sum(t.numel() * t.element_size() for t in (cost_f, cost_b, comm) if t is not None)
+        res = evaluate(policy, P, M, v, df, db, strides, n, comm=dc, comm_strides=comm_strides,
+                       out=staging.get("out"), stream=s)
+        staging["out"] = res
+        host = {}
+        d2h = 0
+        for k, t in res.items():
+            hk = staging.get("host_" + k)
+            if hk is None or hk.shape != t.shape:
+                hk = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                staging["host_" + k] = hk
+            hk.copy_(t, non_blocking=True)
+            host[k] = hk
+            d2h += t.numel() * t.element_size()
+    return host, h2d, d2h
+
+
+def partition_search(layer_tf, layer_tb, layer_act, P, M, comm, cap, seed, cand_begin, n_cand,
+                     all_makespan=False, out=None, stream=None):
+    """Call pp_sched_partition_search; layer arrays are CUDA tensors (int32,
+    int32, int64).  Returns dict(best_idx int64[1], best_makespan int32[1],
+    best_cuts int32[P-1], all_makespan int32[n_cand] if requested)."""
+    dev = layer_tf.device
+    out = dict(out or {})
+    bi = out.setdefault("best_idx", torch.empty(1, dtype=torch.int64, device=dev))
+    bm = out.setdefault("best_makespan", torch.empty(1, dtype=torch.int32, device=dev))
+    bc = out.setdefault("best_cuts", torch.empty(max(P - 1, 1), dtype=torch.int32, device=dev))
+    am = None
+    if all_makespan:
+        am = out.setdefault("all_makespan", torch.empty(n_cand, dtype=torch.int32, device=dev))
+    L = layer_tf.numel()
+    rc = LIB.pp_sched_partition_search(_ptr(layer_tf), _ptr(layer_tb), _ptr(layer_act), L, P, M,
+                                       int(comm), int(cap), ctypes.c_uint64(seed & (2**64 - 1)),
+                                       int(cand_begin), int(n_cand), _ptr(bi), _ptr(bm),
+                                       _ptr(bc) if P > 1 else None, _ptr(am), _stream(stream))
+    _check(rc, "pp_sched_partition_search")
+    return out
+
+
+def cache_clear():
+    LIB.pp_sched_cache_clear()

@@ -1,0 +1,170 @@
+// eval_common.cuh -- pieces shared by the two evaluator kernels.
+//
+// Work decomposition: one thread per schedule instance, one warp per 32
+// instances.  All instances of a call share the plan, so every lane of a warp
+// walks the same per-round op table: descriptor loads are warp-uniform and the
+// per-op branches never diverge.  A round holds at most one op per device, and
+// ops within a round are independent (rounds are a topological order of the
+// dependency graph), so a thread evaluates its instance round by round.
+//
+// Cost staging: each warp keeps a ring of NSLOT round-slices in shared memory,
+// laid out [slice][device][lane], filled D = NSLOT-1 rounds ahead with
+// cp.async.  With the instance-minor cost layout (stride_inst == 1) a group of
+// 8 lanes copies the 128 contiguous bytes of one (stage, microbatch) row for
+// the warp's 32 instances in 16-byte pieces, so every global load is
+// coalesced and 128-bit; the compute reads its own word conflict-free.
+#pragma once
+
+#include <cstdint>
+
+#include "internal.cuh"
+
+namespace pps {
+
+struct EvalArgs {
+    const uint32_t *desc;    // [R][PMAX]
+    const uint32_t *desc2;   // [R][PMAX] (generic evaluator)
+    int R, P, M, v, S, O, nslots;
+    const int32_t *cost_f, *cost_b;
+    int64_t s_inst, s_stage, s_mb;
+    const int32_t *comm;
+    int64_t c_inst, c_bnd;
+    int64_t n;
+    int32_t *makespan, *idle;
+    int64_t *bub_num, *bub_den;
+    int8_t *status;
+    int32_t *op_start, *op_end;
+    int64_t o_inst, o_op;
+};
+
+// Round slices kept per warp: enough prefetch depth to cover HBM latency
+// while the ring stays at 8 KB per warp.
+template <int PMAX>
+struct Ring {
+    static constexpr int kSlices = PMAX == 4 ? 16 : (PMAX == 8 ? 8 : 4);
+    static constexpr int kAhead = kSlices - 1;
+    static constexpr int kWords = kSlices * PMAX * 32;
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// Issue the copies of round `rl`'s costs into ring slice rl % kSlices.
+template <int PMAX, bool VEC>
+__device__ __forceinline__ void load_round(const EvalArgs &a, int rl, int32_t *ring, int64_t inst0,
+                                           int lane) {
+    using RG = Ring<PMAX>;
+    int32_t *slice = ring + (rl % RG::kSlices) * (PMAX * 32);
+    const uint32_t *drow = a.desc + (int64_t)rl * PMAX;
+    if constexpr (VEC) {
+        // lanes 8q..8q+7 cover device 4*i + q, 4 instances each
+        const int g = lane & 7;
+        const int64_t x0 = inst0 + 4 * g;
+        const int64_t left = a.n - x0;
+        const uint32_t bytes_in = left <= 0 ? 0u : (left >= 4 ? 16u : (uint32_t)left * 4u);
+#pragma unroll
+        for (int i = 0; i < PMAX / 4; ++i) {
+            const int k = 4 * i + (lane >> 3);
+            const uint32_t d = __ldg(drow + k);
+            const uint32_t kind = desc_kind(d);
+            const int32_t *base = kind == kBwd ? a.cost_b : a.cost_f;
+            const int64_t s = (int64_t)desc_chunk(d) * a.P + k;
+            const int32_t *src = base;
+            uint32_t nb = 0;
+            if (kind != kIdle && bytes_in) {
+                src = base + s * a.s_stage + (int64_t)desc_mb(d) * a.s_mb + x0;
+                nb = bytes_in;
+            }
+            cp_async16(smem_addr(slice + k * 32 + 4 * g), src, nb);
+        }
+    } else {
+        const int64_t x = inst0 + lane;
+        const bool live = x < a.n;
+#pragma unroll
+        for (int k = 0; k < PMAX; ++k) {
+            const uint32_t d = __ldg(drow + k);
+            const uint32_t kind = desc_kind(d);
+            const int32_t *base = kind == kBwd ? a.cost_b : a.cost_f;
+            const int32_t *src = base;
+            uint32_t nb = 0;
+            if (kind != kIdle && live) {
+                const int64_t s = (int64_t)desc_chunk(d) * a.P + k;
+                src = base + s * a.s_stage + (int64_t)desc_mb(d) * a.s_mb + x * a.s_inst;
+                nb = 4;
+            }
+            cp_async4(smem_addr(slice + k * 32 + lane), src, nb);
+        }
+    }
+}
+
+// Load the round's descriptors (identical for every lane of the warp).
+template <int PMAX>
+__device__ __forceinline__ void load_desc(const uint32_t *row, uint32_t (&d)[PMAX]) {
+    const uint4 *r4 = reinterpret_cast<const uint4 *>(row);
+#pragma unroll
+    for (int i = 0; i < PMAX / 4; ++i) {
+        const uint4 q = __ldg(r4 + i);
+        d[4 * i + 0] = q.x; d[4 * i + 1] = q.y; d[4 * i + 2] = q.z; d[4 * i + 3] = q.w;
+    }
+}
+
+// Write the per-instance reductions ("2. 1F1B" §4.3 and M040 §04: the window is
+// the last end tick; each stage's idle time is the window minus its busy time;
+// the bubble is total idle over P windows).
+template <int PMAX>
+__device__ __forceinline__ void write_results(const EvalArgs &a, int64_t x, const int (&fr)[PMAX],
+                                              const int (&busy)[PMAX], uint32_t neg_bits,
+                                              uint32_t ovf_bits) {
+    int mk = 0;
+#pragma unroll
+    for (int k = 0; k < PMAX; ++k) mk = max(mk, fr[k]);
+    int64_t num = 0;
+#pragma unroll
+    for (int k = 0; k < PMAX; ++k) {
+        if (k < a.P) {
+            const int idle = mk - busy[k];
+            num += idle;
+            if (a.idle) a.idle[x * a.P + k] = idle;
+        }
+    }
+    if (a.makespan) a.makespan[x] = mk;
+    if (a.bub_num) a.bub_num[x] = num;
+    if (a.bub_den) a.bub_den[x] = (int64_t)a.P * mk;
+    if (a.status) {
+        int8_t st = PP_ST_OK;
+        if (neg_bits >> 31) st = PP_ST_NEG_COST;
+        else if (ovf_bits >> 31) st = PP_ST_OVERFLOW;
+        a.status[x] = st;
+    }
+}
+
+// int32 add without C++ signed-overflow semantics; overflow is detected by the
+// sign bit of the result (all true values are >= 0 and < 2^31, so a sum of two
+// wraps past INT32_MAX exactly when its sign bit is set).
+__device__ __forceinline__ int wrap_add(int x, int y) {
+    return static_cast<int>(static_cast<uint32_t>(x) + static_cast<uint32_t>(y));
+}
+
+// Launchers (defined in eval_reg.cu / eval_slot.cu).
+int launch_eval_reg(const pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st);
+int launch_eval_slot(const pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st);
+
+}  // namespace pps

@@ -1,0 +1,77 @@
+// internal.cuh -- definitions shared by the library's translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/ppsched.h"
+
+namespace pps {
+
+// Per-round op descriptor, one uint32 per (round, device slot):
+//   bits 0..1  kind: 0 idle, 1 forward, 2 backward
+//   bits 2..7  chunk (virtual stage s = chunk*P + device)
+//   bits 8..31 microbatch
+constexpr uint32_t kIdle = 0, kFwd = 1, kBwd = 2;
+__host__ __device__ inline uint32_t desc_pack(uint32_t kind, uint32_t chunk, uint32_t mb) {
+    return kind | (chunk << 2) | (mb << 8);
+}
+__host__ __device__ inline uint32_t desc_kind(uint32_t d) { return d & 3u; }
+__host__ __device__ inline uint32_t desc_chunk(uint32_t d) { return (d >> 2) & 63u; }
+__host__ __device__ inline uint32_t desc_mb(uint32_t d) { return d >> 8; }
+
+// Dependency-slot descriptor for the generic evaluator, one uint32 per
+// (round, device slot):
+//   bits 0..7   value slot this op reads its input arrival from (0xFF none)
+//   bits 8..15  value slot this op writes its end tick to (0xFF none)
+//   bits 16..23 boundary whose comm is added to the input (0xFF none)
+constexpr uint32_t kNoSlot = 0xFFu;
+__host__ __device__ inline uint32_t d2_pack(uint32_t rs, uint32_t ws, uint32_t cb) {
+    return rs | (ws << 8) | (cb << 16);
+}
+__host__ __device__ inline uint32_t d2_rslot(uint32_t d) { return d & 0xFFu; }
+__host__ __device__ inline uint32_t d2_wslot(uint32_t d) { return (d >> 8) & 0xFFu; }
+__host__ __device__ inline uint32_t d2_cbnd(uint32_t d) { return (d >> 16) & 0xFFu; }
+
+constexpr int kMaxValueSlots = 64;
+
+// Width of the device dimension a kernel is compiled for (>= P).
+inline int pmax_for(int P) { return P <= 4 ? 4 : (P <= 8 ? 8 : 16); }
+
+}  // namespace pps
+
+// The plan object (opaque to callers).
+struct pp_plan {
+    int policy, P, M, v, S, O;
+    int R;              // rounds
+    int pmax;           // row width of the per-round tables
+    int nslots;         // value slots of the generic evaluator
+    int reg_ok;         // 1 if the register evaluator applies
+    int device;         // CUDA device the tables live on
+    uint32_t *d_ops;    // [P][O] packed ops (PP_OP_* layout)
+    int32_t *d_round;   // [P][O] wavefront round of each op
+    uint32_t *d_desc;   // [R][pmax]
+    uint32_t *d_desc2;  // [R][pmax] (generic evaluator), may be null
+    int32_t *d_peak;    // [P]
+    int32_t h_peak[PP_MAX_P];
+};
+
+namespace pps {
+
+// Status helpers (host).
+int cuda_status(cudaError_t e);
+
+// Plan cache used by the evaluation entry points: returns the plan of the
+// shape on the current device, building it on first use.
+int cached_plan(int policy, int P, int M, int v, cudaStream_t stream, const pp_plan **out);
+
+// Argument validation shared by plan construction and evaluation.
+int check_shape(int policy, int P, int M, int v);
+
+}  // namespace pps
+
+#define PPS_CUDA_TRY(expr)                                  \
+    do {                                                    \
+        cudaError_t e_ = (expr);                            \
+        if (e_ != cudaSuccess) return pps::cuda_status(e_); \
+    } while (0)

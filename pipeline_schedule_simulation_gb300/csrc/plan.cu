@@ -1,0 +1,396 @@
+// plan.cu -- the schedule plan, built on the GPU once per (policy, P, M, v).
+//
+// Steps (all kernels below):
+//   1. k_order: one thread per (device k, position j) writes the op from the
+//      policy's rules, and the inverse map (kind, virtual stage, microbatch) ->
+//      position.
+//   2. k_rounds: each op's wavefront round, i.e. its start tick when every op
+//      takes one tick and comm is 0: round = max(previous op on the device,
+//      the op it depends on) + 1.  Rounds are a topological order of the
+//      dependency graph, so evaluating ops round by round is valid for any
+//      costs.  One lane per device walks its order; a lane advances while the
+//      op it depends on already has its round.  Each pass either advances some
+//      lane or proves the order cyclic (deadlock), so the loop is bounded.
+//   3. k_desc: scatter ops into the per-round table [round][device].
+//   4. k_peak: the held-activation ledger per device ("2. 1F1B" §4.1 table:
+//      +1 at each F, -1 at each B, peak = running maximum).
+//   5. k_latest (GPipe/1F1B): checks that every input an op reads is the latest
+//      result of its kind on the neighbouring device at the start of its round,
+//      which lets the fast evaluator keep one register per (device, kind).
+//   6. k_slots (interleaved, or when 5 fails): greedy interval colouring of
+//      the in-flight results onto value slots for the generic evaluator.
+#include <algorithm>
+#include <cstdio>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "internal.cuh"
+
+namespace pps {
+
+namespace {
+
+constexpr uint32_t kOpB = 0x80000000u;  // PP_OP kind bit
+
+// The op at position j of device k, as a PP_OP-packed word.  Rules:
+//  GPipe: "Pipeline scheduling" (M040) §02 -- all F, then B from the last
+//    microbatch back to the first.
+//  1F1B: "2. 1F1B" §2.3 and §3.2 -- P-k forwards (at most M), then B,F pairs
+//    with the oldest outstanding backward first, then the remaining B.
+//  Interleaved: device k holds chunks c (virtual stage c*P+k); warmup
+//    2(P-k-1)+(v-1)P forwards, then F,B pairs, then the remaining B; forward j
+//    runs chunk (j mod Pv)/P of microbatch (j/(Pv))*P + j mod P and backward j
+//    runs chunk v-1-(j mod Pv)/P of the same microbatch.
+__device__ uint32_t op_at(int policy, int P, int M, int v, int k, int j) {
+    auto F = [](uint32_t c, uint32_t i) { return (c << 24) | i; };
+    auto B = [](uint32_t c, uint32_t i) { return kOpB | (c << 24) | i; };
+    if (policy == PP_GPIPE) {
+        return j < M ? F(0, j) : B(0, 2 * M - 1 - j);
+    }
+    if (policy == PP_1F1B) {
+        int w = min(P - k, M);
+        if (j < w) return F(0, j);
+        int t = j - w;
+        if (t < 2 * (M - w)) return (t & 1) ? F(0, w + (t >> 1)) : B(0, t >> 1);
+        return B(0, M - w + (t - 2 * (M - w)));
+    }
+    // interleaved
+    int total = M * v;
+    int w = min(2 * (P - k - 1) + (v - 1) * P, total);
+    int grp = P * v;
+    auto fwd = [&](int x) { return F((x % grp) / P, (x / grp) * P + x % P); };
+    auto bwd = [&](int x) { return B(v - 1 - (x % grp) / P, (x / grp) * P + x % P); };
+    if (j < w) return fwd(j);
+    int t = j - w;
+    if (t < 2 * (total - w)) return (t & 1) ? bwd(t >> 1) : fwd(w + (t >> 1));
+    return bwd(total - w + (t - 2 * (total - w)));
+}
+
+__device__ inline int op_kind(uint32_t op) { return op >> 31; }            // 0 F, 1 B
+__device__ inline int op_chunk(uint32_t op) { return (op >> 24) & 0x7F; }
+__device__ inline int op_mb(uint32_t op) { return op & 0xFFFFFF; }
+__device__ inline int64_t pos_key(int kind, int s, int mb, int S, int M) {
+    return ((int64_t)kind * S + s) * M + mb;
+}
+
+__global__ void k_order(int policy, int P, int M, int v, uint32_t *ops, int32_t *pos) {
+    const int O = 2 * M * v, S = P * v;
+    int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= (int64_t)P * O) return;
+    int k = (int)(t / O), j = (int)(t % O);
+    uint32_t op = op_at(policy, P, M, v, k, j);
+    ops[t] = op;
+    pos[pos_key(op_kind(op), op_chunk(op) * P + k, op_mb(op), S, M)] = j;
+}
+
+// info[0] = rounds, info[1] = 1 on deadlock.  Launched as one warp; P <= 32.
+__global__ void k_rounds(const uint32_t *ops, const int32_t *pos, int P, int M, int v,
+                         int32_t *round, int32_t *info) {
+    __shared__ int pub[32];
+    const int O = 2 * M * v, S = P * v;
+    const int k = threadIdx.x;
+    const bool active = k < P;
+    int cur = 0, rprev = -1;
+    pub[k] = active ? 0 : O;
+    __syncwarp();
+    const int64_t limit = (int64_t)P * O + 2;
+    bool dead = false;
+    for (int64_t it = 0; it < limit; ++it) {
+        bool moved = false;
+        while (active && cur < O) {
+            uint32_t op = ops[k * O + cur];
+            int kd = op_kind(op), s = op_chunk(op) * P + k, mb = op_mb(op);
+            int ddev = -1, dj = 0;
+            if (kd == 0 && s > 0) { ddev = (s - 1) % P; dj = pos[pos_key(0, s - 1, mb, S, M)]; }
+            if (kd == 1 && s < S - 1) { ddev = (s + 1) % P; dj = pos[pos_key(1, s + 1, mb, S, M)]; }
+            if (kd == 1 && pos[pos_key(0, s, mb, S, M)] >= cur) break;  // its own F not yet run
+            int rd = -1;
+            if (ddev >= 0) {
+                int avail = (ddev == k) ? cur : pub[ddev];
+                if (dj >= avail) break;
+                rd = round[ddev * O + dj];
+            }
+            int r = max(rprev + 1, rd + 1);
+            round[k * O + cur] = r;
+            rprev = r;
+            ++cur;
+            moved = true;
+        }
+        __syncwarp();
+        if (active) pub[k] = cur;
+        __syncwarp();
+        bool any = __any_sync(0xffffffffu, moved);
+        bool all = __all_sync(0xffffffffu, !active || cur == O);
+        if (all) break;
+        if (!any) { dead = true; break; }
+    }
+    int rmax = rprev;
+    for (int o = 16; o > 0; o >>= 1) rmax = max(rmax, __shfl_xor_sync(0xffffffffu, rmax, o));
+    if (k == 0) {
+        info[0] = rmax + 1;
+        info[1] = dead ? 1 : 0;
+    }
+}
+
+__global__ void k_desc(const uint32_t *ops, const int32_t *round, int P, int M, int v, int pmax,
+                       uint32_t *desc) {
+    const int O = 2 * M * v;
+    int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= (int64_t)P * O) return;
+    int k = (int)(t / O);
+    uint32_t op = ops[t];
+    desc[(int64_t)round[t] * pmax + k] =
+        desc_pack(op_kind(op) ? kBwd : kFwd, (uint32_t)op_chunk(op), (uint32_t)op_mb(op));
+}
+
+__global__ void k_peak(const uint32_t *ops, int P, int O, int32_t *peak) {
+    int k = threadIdx.x;
+    if (k >= P) return;
+    int held = 0, pk = 0;
+    for (int j = 0; j < O; ++j) {
+        held += op_kind(ops[k * O + j]) ? -1 : 1;
+        pk = max(pk, held);
+    }
+    peak[k] = pk;
+}
+
+// v == 1 only.  info[2] |= 1 if some input is not the latest result of its kind
+// on the producing device at the start of the consumer's round.
+__global__ void k_latest(const uint32_t *ops, const int32_t *pos, const int32_t *round, int P,
+                         int M, int32_t *info) {
+    const int O = 2 * M, S = P;
+    int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= (int64_t)P * O) return;
+    int k = (int)(t / O), j = (int)(t % O);
+    uint32_t op = ops[t];
+    int kd = op_kind(op), mb = op_mb(op);
+    int cdev;
+    if (kd == 0 && k < P - 1) cdev = k + 1;
+    else if (kd == 1 && k > 0) cdev = k - 1;
+    else return;  // no consumer on another device
+    int rc = round[cdev * O + pos[pos_key(kd, cdev, mb, S, M)]];
+    for (int q = j + 1; q < O; ++q) {
+        if (op_kind(ops[k * O + q]) == kd) {
+            if (round[k * O + q] < rc) atomicOr(&info[2], 1);
+            break;
+        }
+    }
+}
+
+// Greedy value-slot assignment, one thread.  info[3] = slots used, info[4] = 1
+// if more than kMaxValueSlots would be needed.
+__global__ void k_slots(const uint32_t *desc, int R, int P, int M, int v, int pmax,
+                        int32_t *slot_of, uint32_t *desc2, int32_t *info) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    const int S = P * v;
+    uint64_t used = 0;
+    int nmax = 0;
+    for (int r = 0; r < R; ++r) {
+        uint64_t freed = 0;
+        for (int k = 0; k < pmax; ++k) {
+            uint32_t d = desc[(int64_t)r * pmax + k];
+            uint32_t kind = desc_kind(d);
+            if (kind == kIdle) { desc2[(int64_t)r * pmax + k] = d2_pack(kNoSlot, kNoSlot, kNoSlot); continue; }
+            int s = (int)desc_chunk(d) * P + k, mb = (int)desc_mb(d);
+            uint32_t rs = kNoSlot, cb = kNoSlot, ws = kNoSlot;
+            if (kind == kFwd && s > 0) { rs = (uint32_t)slot_of[pos_key(0, s - 1, mb, S, M)]; cb = s - 1; }
+            if (kind == kBwd && s < S - 1) { rs = (uint32_t)slot_of[pos_key(1, s + 1, mb, S, M)]; cb = s; }
+            if (rs != kNoSlot) {
+                if (rs >= (uint32_t)kMaxValueSlots) { info[5] = 1; return; }  // never assigned
+                freed |= 1ull << rs;
+            }
+            bool produces = (kind == kFwd && s < S - 1) || (kind == kBwd && s > 0);
+            if (produces) {
+                if (used == ~0ull) { info[4] = 1; return; }
+                int b = __ffsll((long long)~used) - 1;
+                used |= 1ull << b;
+                nmax = max(nmax, b + 1);
+                ws = (uint32_t)b;
+                slot_of[pos_key(kind == kBwd ? 1 : 0, s, mb, S, M)] = b;
+            }
+            desc2[(int64_t)r * pmax + k] = d2_pack(rs, ws, cb);
+        }
+        used &= ~freed;
+    }
+    info[3] = nmax;
+}
+
+struct DevBuf {
+    void *p = nullptr;
+    ~DevBuf() { if (p) cudaFree(p); }
+    template <class T> T *as() { return static_cast<T *>(p); }
+};
+
+}  // namespace
+
+int cuda_status(cudaError_t e) {
+    (void)cudaGetLastError();
+    (void)e;
+    return PP_ERR_CUDA;
+}
+
+int check_shape(int policy, int P, int M, int v) {
+    if (policy < PP_GPIPE || policy > PP_INTERLEAVED_1F1B) return PP_ERR_ARG;
+    if (P < 1 || M < 1 || v < 1) return PP_ERR_ARG;
+    if (policy != PP_INTERLEAVED_1F1B && v != 1) return PP_ERR_ARG;
+    if (policy == PP_INTERLEAVED_1F1B && v < 2) return PP_ERR_ARG;
+    if (P > PP_MAX_P || (int64_t)P * v > PP_MAX_S || (int64_t)M * v > PP_MAX_MV) return PP_ERR_SIZE;
+    if (policy == PP_INTERLEAVED_1F1B && M % P != 0) return PP_ERR_DIVISIBILITY;
+    return PP_OK;
+}
+
+static int build_plan(int policy, int P, int M, int v, cudaStream_t st, pp_plan **out) {
+    int rc = check_shape(policy, P, M, v);
+    if (rc) return rc;
+    const int S = P * v, O = 2 * M * v, pmax = pmax_for(P);
+    const int64_t nops = (int64_t)P * O, npos = 2LL * S * M;
+    DevBuf ops, pos, round, info, peak, desc, desc2, slot_of;
+    PPS_CUDA_TRY(cudaMalloc(&ops.p, nops * sizeof(uint32_t)));
+    PPS_CUDA_TRY(cudaMalloc(&pos.p, npos * sizeof(int32_t)));
+    PPS_CUDA_TRY(cudaMalloc(&round.p, nops * sizeof(int32_t)));
+    PPS_CUDA_TRY(cudaMalloc(&info.p, 8 * sizeof(int32_t)));
+    PPS_CUDA_TRY(cudaMalloc(&peak.p, P * sizeof(int32_t)));
+    PPS_CUDA_TRY(cudaMemsetAsync(info.p, 0, 8 * sizeof(int32_t), st));
+    const int tpb = 256;
+    const unsigned nblk = (unsigned)((nops + tpb - 1) / tpb);
+    k_order<<<nblk, tpb, 0, st>>>(policy, P, M, v, ops.as<uint32_t>(), pos.as<int32_t>());
+    k_rounds<<<1, 32, 0, st>>>(ops.as<uint32_t>(), pos.as<int32_t>(), P, M, v, round.as<int32_t>(),
+                               info.as<int32_t>());
+    PPS_CUDA_TRY(cudaGetLastError());
+    int32_t h_info[8];
+    PPS_CUDA_TRY(cudaMemcpyAsync(h_info, info.p, sizeof(h_info), cudaMemcpyDeviceToHost, st));
+    PPS_CUDA_TRY(cudaStreamSynchronize(st));
+    if (h_info[1]) return PP_ERR_DEADLOCK;
+    const int R = h_info[0];
+    if (R < 1) return PP_ERR_INTERNAL;
+    PPS_CUDA_TRY(cudaMalloc(&desc.p, (int64_t)R * pmax * sizeof(uint32_t)));
+    PPS_CUDA_TRY(cudaMemsetAsync(desc.p, 0, (int64_t)R * pmax * sizeof(uint32_t), st));
+    k_desc<<<nblk, tpb, 0, st>>>(ops.as<uint32_t>(), round.as<int32_t>(), P, M, v, pmax,
+                                 desc.as<uint32_t>());
+    k_peak<<<1, 32, 0, st>>>(ops.as<uint32_t>(), P, O, peak.as<int32_t>());
+    int reg_ok = 0;
+    if (v == 1) {
+        k_latest<<<nblk, tpb, 0, st>>>(ops.as<uint32_t>(), pos.as<int32_t>(), round.as<int32_t>(), P, M,
+                                       info.as<int32_t>());
+        PPS_CUDA_TRY(cudaGetLastError());
+        PPS_CUDA_TRY(cudaMemcpyAsync(h_info, info.p, sizeof(h_info), cudaMemcpyDeviceToHost, st));
+        PPS_CUDA_TRY(cudaStreamSynchronize(st));
+        reg_ok = h_info[2] == 0;
+    }
+    int nslots = 0;
+    if (!reg_ok) {
+        PPS_CUDA_TRY(cudaMalloc(&desc2.p, (int64_t)R * pmax * sizeof(uint32_t)));
+        PPS_CUDA_TRY(cudaMalloc(&slot_of.p, npos * sizeof(int32_t)));
+        PPS_CUDA_TRY(cudaMemsetAsync(slot_of.p, 0xFF, npos * sizeof(int32_t), st));
+        k_slots<<<1, 32, 0, st>>>(desc.as<uint32_t>(), R, P, M, v, pmax, slot_of.as<int32_t>(),
+                                  desc2.as<uint32_t>(), info.as<int32_t>());
+        PPS_CUDA_TRY(cudaGetLastError());
+        PPS_CUDA_TRY(cudaMemcpyAsync(h_info, info.p, sizeof(h_info), cudaMemcpyDeviceToHost, st));
+        PPS_CUDA_TRY(cudaStreamSynchronize(st));
+        if (h_info[5]) return PP_ERR_INTERNAL;
+        if (h_info[4]) return PP_ERR_SIZE;
+        nslots = h_info[3];
+    }
+    pp_plan *p = new pp_plan();
+    p->policy = policy; p->P = P; p->M = M; p->v = v; p->S = S; p->O = O;
+    p->R = R; p->pmax = pmax; p->nslots = nslots; p->reg_ok = reg_ok;
+    PPS_CUDA_TRY(cudaGetDevice(&p->device));
+    if (cudaMemcpyAsync(p->h_peak, peak.p, P * sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        delete p;
+        return cuda_status(cudaErrorUnknown);
+    }
+    p->d_ops = ops.as<uint32_t>(); ops.p = nullptr;
+    p->d_round = round.as<int32_t>(); round.p = nullptr;
+    p->d_desc = desc.as<uint32_t>(); desc.p = nullptr;
+    p->d_desc2 = desc2.as<uint32_t>(); desc2.p = nullptr;
+    p->d_peak = peak.as<int32_t>(); peak.p = nullptr;
+    *out = p;
+    return PP_OK;
+}
+
+namespace {
+std::mutex g_cache_mu;
+std::map<std::tuple<int, int, int, int, int>, pp_plan *> g_cache;
+}  // namespace
+
+int cached_plan(int policy, int P, int M, int v, cudaStream_t stream, const pp_plan **out) {
+    int dev = 0;
+    PPS_CUDA_TRY(cudaGetDevice(&dev));
+    auto key = std::make_tuple(dev, policy, P, M, v);
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    auto it = g_cache.find(key);
+    if (it != g_cache.end()) { *out = it->second; return PP_OK; }
+    pp_plan *p = nullptr;
+    int rc = build_plan(policy, P, M, v, stream, &p);
+    if (rc) return rc;
+    g_cache[key] = p;
+    *out = p;
+    return PP_OK;
+}
+
+}  // namespace pps
+
+extern "C" {
+
+int pp_sched_plan(pp_policy_t policy, int P, int M, int v, pp_plan_t **plan, cudaStream_t stream) {
+    if (!plan) return PP_ERR_ARG;
+    *plan = nullptr;
+    return pps::build_plan((int)policy, P, M, v, stream, plan);
+}
+
+int pp_sched_plan_info(const pp_plan_t *p, int32_t *info) {
+    if (!p || !info) return PP_ERR_ARG;
+    info[0] = p->R; info[1] = p->O; info[2] = p->nslots; info[3] = p->reg_ok;
+    info[4] = p->P; info[5] = p->M; info[6] = p->v; info[7] = p->policy;
+    return PP_OK;
+}
+
+int pp_sched_plan_ops(const pp_plan_t *p, uint32_t *host_ops, int32_t *host_peak, int32_t *host_round) {
+    if (!p) return PP_ERR_ARG;
+    int cur = 0;
+    PPS_CUDA_TRY(cudaGetDevice(&cur));
+    if (cur != p->device) PPS_CUDA_TRY(cudaSetDevice(p->device));
+    const size_t n = (size_t)p->P * p->O;
+    int rc = PP_OK;
+    if (host_ops && cudaMemcpy(host_ops, p->d_ops, n * sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+        rc = PP_ERR_CUDA;
+    if (!rc && host_round && cudaMemcpy(host_round, p->d_round, n * sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+        rc = PP_ERR_CUDA;
+    if (host_peak) for (int k = 0; k < p->P; ++k) host_peak[k] = p->h_peak[k];
+    if (cur != p->device) cudaSetDevice(cur);
+    if (rc) (void)cudaGetLastError();
+    return rc;
+}
+
+void pp_sched_plan_destroy(pp_plan_t *p) {
+    if (!p) return;
+    cudaFree(p->d_ops);
+    cudaFree(p->d_round);
+    cudaFree(p->d_desc);
+    if (p->d_desc2) cudaFree(p->d_desc2);
+    cudaFree(p->d_peak);
+    delete p;
+}
+
+void pp_sched_cache_clear(void) {
+    std::lock_guard<std::mutex> lk(pps::g_cache_mu);
+    for (auto &kv : pps::g_cache) pp_sched_plan_destroy(kv.second);
+    pps::g_cache.clear();
+}
+
+const char *pp_sched_status_str(int code) {
+    switch (code) {
+        case PP_OK: return "ok";
+        case PP_ERR_ARG: return "invalid argument";
+        case PP_ERR_DIVISIBILITY: return "interleaved schedule needs M divisible by P";
+        case PP_ERR_SIZE: return "shape beyond the library's limits";
+        case PP_ERR_CUDA: return "CUDA runtime error";
+        case PP_ERR_DEADLOCK: return "schedule order deadlocks";
+        case PP_ERR_INTERNAL: return "internal consistency check failed";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

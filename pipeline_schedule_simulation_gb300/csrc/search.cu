@@ -1,0 +1,269 @@
+// search.cu -- candidate contiguous partitions of L layers into P stages,
+// scored under 1F1B on the GPU (pp_sched_partition_search).
+//
+// The pages balance stages by splitting the layer sequence into contiguous
+// ranges from profiled costs ("Pipeline parallelism: from GPipe to 1F1B and
+// Zero Bubble", PipeDream and GPipe sections; M040 §05: uneven stages make the
+// fast stage wait; lpnh: 80 layers into 8 stages).  Here each thread draws one
+// seeded candidate split, sums its stages' costs and activation bytes from
+// prefix sums, rejects it if a stage would hold more activation bytes than the
+// cap, and otherwise evaluates the 1F1B schedule with the register recurrence
+// (stage costs are constant over microbatches, so they live in registers).
+// The best (makespan, candidate) pair is reduced with warp shuffles and one
+// 64-bit atomicMin per warp into the caller's best_idx word, which a one-thread
+// kernel then turns into the index, makespan and cut positions.
+#include "internal.cuh"
+
+namespace pps {
+
+namespace {
+
+constexpr int kMaxL = 256;
+
+struct SearchArgs {
+    const uint32_t *desc;  // 1F1B plan [R][PMAX]
+    int R, P, M, L;
+    const int32_t *ltf, *ltb;
+    const int64_t *lact;
+    int32_t comm;
+    int64_t cap;
+    uint64_t seed;
+    int64_t begin, n;
+    uint64_t ncomb;        // C(L-1, P-1)
+    int32_t peak[PP_MAX_P];
+    int32_t *all_mk;
+    unsigned long long *key;  // the caller's best_idx word, used as the reduction cell
+};
+
+// SplitMix64 (Steele, Lea & Flood, OOPSLA 2014): add the golden gamma to the
+// state, then apply the two xor-shift-multiply rounds and a final xor-shift.
+__device__ __forceinline__ uint64_t splitmix64(uint64_t s) {
+    uint64_t z = s + 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+// Shared tables: prefix sums of layer costs and bytes, and C(n, i) for
+// n < L, i < P, computed with the multiplicative formula in 128-bit-safe steps.
+struct Tables {
+    int64_t pre_tf[kMaxL + 1], pre_tb[kMaxL + 1], pre_act[kMaxL + 1];
+    uint64_t C[kMaxL][PP_MAX_P];  // C[n][i]; saturates at ~0
+};
+
+__device__ uint64_t binom_mul(int n, int i) {
+    if (i < 0 || i > n) return 0;
+    if (i > n - i) i = n - i;
+    // C(n, i) = prod_{t=1..i} (n - i + t) / t, exact at every step
+    unsigned __int128 acc = 1;
+    for (int t = 1; t <= i; ++t) {
+        acc = acc * (unsigned)(n - i + t) / (unsigned)t;
+        if (acc > (unsigned __int128)0xFFFFFFFFFFFFFFFFull) return ~0ull;
+    }
+    return (uint64_t)acc;
+}
+
+__device__ void build_tables(const SearchArgs &a, Tables &t) {
+    const int tid = threadIdx.x;
+    for (int e = tid; e < a.L * a.P; e += blockDim.x) {
+        const int n = e / a.P, i = e % a.P;
+        t.C[n][i] = binom_mul(n, i);
+    }
+    if (tid == 0) {
+        int64_t f = 0, b = 0, c = 0;
+        t.pre_tf[0] = t.pre_tb[0] = t.pre_act[0] = 0;
+        for (int l = 0; l < a.L; ++l) {
+            f += a.ltf[l]; b += a.ltb[l]; c += a.lact[l];
+            t.pre_tf[l + 1] = f; t.pre_tb[l + 1] = b; t.pre_act[l + 1] = c;
+        }
+    }
+    __syncthreads();
+}
+
+// Colex unranking: the largest x with C(x, i) <= r for i = K..1, subtracting
+// as it goes; writes the first layer of stages 0..P (first[0] = 0, first[P] = L).
+template <int PMAX>
+__device__ __forceinline__ void unrank(const SearchArgs &a, const Tables &t, uint64_t r, int (&first)[PMAX + 1]) {
+    const int K = a.P - 1;
+    int hi = a.L - 2;  // positions 0..L-2
+#pragma unroll
+    for (int i = PMAX - 1; i >= 1; --i) {
+        if (i <= K) {
+            int c = hi;
+            while (c >= i && t.C[c][i] > r) --c;
+            r -= t.C[c][i];
+            first[i] = c + 1;
+            hi = c - 1;
+        }
+    }
+    first[0] = 0;
+#pragma unroll
+    for (int i = 1; i <= PMAX; ++i) if (i >= a.P) first[i] = a.L;
+}
+
+template <int PMAX>
+__global__ void __launch_bounds__(256) k_search(const SearchArgs a) {
+    __shared__ Tables t;
+    build_tables(a, t);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int lane = threadIdx.x & 31;
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < a.n; base += stride) {
+        const int64_t ci = base + threadIdx.x;  // index within this call
+        const bool live = ci < a.n;
+        int mk = -1;
+        if (live) {
+            const uint64_t u = splitmix64(a.seed + (uint64_t)(a.begin + ci));
+            int first[PMAX + 1];
+            unrank<PMAX>(a, t, u % a.ncomb, first);
+            int cf[PMAX], cb[PMAX];
+            bool ok = true;
+            uint32_t big = 0;
+#pragma unroll
+            for (int k = 0; k < PMAX; ++k) {
+                cf[k] = 0; cb[k] = 0;
+                if (k < a.P) {
+                    const int64_t sf = t.pre_tf[first[k + 1]] - t.pre_tf[first[k]];
+                    const int64_t sb = t.pre_tb[first[k + 1]] - t.pre_tb[first[k]];
+                    const int64_t sa = t.pre_act[first[k + 1]] - t.pre_act[first[k]];
+                    if ((int64_t)a.peak[k] * sa > a.cap) ok = false;
+                    if (sf < 0 || sb < 0 || sf > 0x7FFFFFFF || sb > 0x7FFFFFFF) big = 0x80000000u;
+                    cf[k] = (int)sf; cb[k] = (int)sb;
+                }
+            }
+            if (ok) {
+                // 1F1B max-plus recurrence over the plan's rounds (see eval_reg.cu)
+                int fr[PMAX], rf[PMAX], rb[PMAX];
+#pragma unroll
+                for (int k = 0; k < PMAX; ++k) { fr[k] = 0; rf[k] = 0; rb[k] = 0; }
+                uint32_t acc = big | (uint32_t)a.comm;
+                for (int r = 0; r < a.R; ++r) {
+                    const uint4 *row = reinterpret_cast<const uint4 *>(a.desc + (int64_t)r * PMAX);
+                    uint32_t d[PMAX];
+#pragma unroll
+                    for (int i = 0; i < PMAX / 4; ++i) {
+                        const uint4 q = __ldg(row + i);
+                        d[4 * i] = q.x; d[4 * i + 1] = q.y; d[4 * i + 2] = q.z; d[4 * i + 3] = q.w;
+                    }
+                    int rf0[PMAX], rb0[PMAX];
+#pragma unroll
+                    for (int k = 0; k < PMAX; ++k) { rf0[k] = rf[k]; rb0[k] = rb[k]; }
+#pragma unroll
+                    for (int k = 0; k < PMAX; ++k) {
+                        const uint32_t kind = desc_kind(d[k]);
+                        if (kind == kIdle) continue;
+                        int arr, c;
+                        if (kind == kFwd) { arr = k > 0 ? rf0[k > 0 ? k - 1 : 0] : 0; c = cf[k]; }
+                        else { arr = k < PMAX - 1 ? rb0[k < PMAX - 1 ? k + 1 : 0] : 0; c = cb[k]; }
+                        const int st = max(fr[k], arr);
+                        const int en = (int)((uint32_t)st + (uint32_t)c);
+                        fr[k] = en;
+                        acc |= (uint32_t)en | (uint32_t)arr;
+                        const int out = (int)((uint32_t)en + (uint32_t)((kind == kFwd ? k < a.P - 1 : k > 0) ? a.comm : 0));
+                        if (kind == kFwd) rf[k] = out; else rb[k] = out;
+                    }
+                }
+                mk = 0;
+#pragma unroll
+                for (int k = 0; k < PMAX; ++k) mk = max(mk, fr[k]);
+                if (acc >> 31) mk = -2;
+            }
+            if (a.all_mk) a.all_mk[ci] = mk;
+        }
+        unsigned long long key = ~0ull;
+        if (live && mk >= 0) key = ((unsigned long long)(uint32_t)mk << 32) | (uint32_t)ci;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
+            key = other < key ? other : key;
+        }
+        if (lane == 0 && key != ~0ull) atomicMin(a.key, key);
+    }
+}
+
+template <int PMAX>
+__global__ void k_search_finish(const SearchArgs a, int64_t *best_idx, int32_t *best_mk, int32_t *best_cuts) {
+    __shared__ Tables t;
+    build_tables(a, t);
+    if (threadIdx.x != 0) return;
+    const unsigned long long key = *a.key;
+    if (key == ~0ull) {
+        *best_idx = -1;
+        if (best_mk) *best_mk = -1;
+        if (best_cuts) for (int k = 0; k + 1 < a.P; ++k) best_cuts[k] = -1;
+        return;
+    }
+    const int64_t ci = (int64_t)(key & 0xFFFFFFFFull);
+    const int mk = (int)(key >> 32);
+    if (best_cuts) {
+        const uint64_t u = splitmix64(a.seed + (uint64_t)(a.begin + ci));
+        int first[PMAX + 1];
+        unrank<PMAX>(a, t, u % a.ncomb, first);
+        for (int k = 1; k < a.P; ++k) best_cuts[k - 1] = first[k];
+    }
+    if (best_mk) *best_mk = mk;
+    *best_idx = a.begin + ci;
+}
+
+uint64_t host_binom(int n, int k) {
+    if (k < 0 || k > n) return 0;
+    if (k > n - k) k = n - k;
+    unsigned __int128 acc = 1;
+    for (int t = 1; t <= k; ++t) {
+        acc = acc * (unsigned)(n - k + t) / (unsigned)t;
+        if (acc > (unsigned __int128)0xFFFFFFFFFFFFFFFFull) return ~0ull;
+    }
+    return (uint64_t)acc;
+}
+
+template <int PMAX>
+int run_search(SearchArgs &a, int64_t *best_idx, int32_t *best_mk, int32_t *best_cuts, cudaStream_t st) {
+    int dev = 0, sms = 0, per_sm = 0;
+    PPS_CUDA_TRY(cudaGetDevice(&dev));
+    PPS_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    PPS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_search<PMAX>, 256, 0));
+    if (per_sm < 1) per_sm = 1;
+    int64_t want = (a.n + 255) / 256;
+    int64_t grid = (int64_t)sms * per_sm;
+    if (want < grid) grid = want;
+    if (grid < 1) grid = 1;
+    if (a.n > 0) k_search<PMAX><<<(unsigned)grid, 256, 0, st>>>(a);
+    k_search_finish<PMAX><<<1, 64, 0, st>>>(a, best_idx, best_mk, best_cuts);
+    PPS_CUDA_TRY(cudaGetLastError());
+    return PP_OK;
+}
+
+}  // namespace
+
+}  // namespace pps
+
+extern "C" int pp_sched_partition_search(const int32_t *layer_tf, const int32_t *layer_tb,
+                                         const int64_t *layer_act, int L, int P, int M, int32_t comm,
+                                         int64_t act_cap, uint64_t seed, int64_t cand_begin,
+                                         int64_t n_cand, int64_t *best_idx, int32_t *best_makespan,
+                                         int32_t *best_cuts, int32_t *all_makespan, cudaStream_t stream) {
+    using namespace pps;
+    if (!layer_tf || !layer_tb || !layer_act || !best_idx) return PP_ERR_ARG;
+    if (P < 1 || M < 1 || L < P || n_cand < 0 || cand_begin < 0 || comm < 0) return PP_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(best_idx) & 7) != 0) return PP_ERR_ARG;
+    if (P > PP_MAX_P || L > kMaxL || M > PP_MAX_MV || n_cand >= (int64_t)1 << 32) return PP_ERR_SIZE;
+    const uint64_t ncomb = host_binom(L - 1, P - 1);
+    if (ncomb == ~0ull || ncomb == 0) return PP_ERR_SIZE;
+    const pp_plan *plan = nullptr;
+    int rc = cached_plan(PP_1F1B, P, M, 1, stream, &plan);
+    if (rc) return rc;
+    if (!plan->reg_ok) return PP_ERR_INTERNAL;
+    SearchArgs a;
+    a.desc = plan->d_desc; a.R = plan->R; a.P = P; a.M = M; a.L = L;
+    a.ltf = layer_tf; a.ltb = layer_tb; a.lact = layer_act;
+    a.comm = comm; a.cap = act_cap; a.seed = seed; a.begin = cand_begin; a.n = n_cand; a.ncomb = ncomb;
+    for (int k = 0; k < PP_MAX_P; ++k) a.peak[k] = k < P ? plan->h_peak[k] : 0;
+    a.all_mk = all_makespan;
+    a.key = reinterpret_cast<unsigned long long *>(best_idx);
+    PPS_CUDA_TRY(cudaMemsetAsync(best_idx, 0xFF, sizeof(int64_t), stream));
+    switch (plan->pmax) {
+        case 4: return run_search<4>(a, best_idx, best_makespan, best_cuts, stream);
+        case 8: return run_search<8>(a, best_idx, best_makespan, best_cuts, stream);
+        case 16: return run_search<16>(a, best_idx, best_makespan, best_cuts, stream);
+        default: return PP_ERR_INTERNAL;
+    }
+}

@@ -1,0 +1,73 @@
+"""The C-ABI library loads without a GPU and exports every declared entry
+point; host-side argument checks answer before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+def _declared():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for fn in sorted(os.listdir(inc)):
+        if fn.endswith(".h"):
+            src = open(os.path.join(inc, fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(pp_sched_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from pipeline_schedule_simulation_gb300 import build_lib
+    build_lib.build()
+    return ctypes.CDLL(build_lib.LIB)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert "pp_sched_eval" in names and "pp_sched_plan" in names
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_binding_exports_match_header():
+    from pipeline_schedule_simulation_gb300 import binding
+    assert sorted(binding.EXPORTS) == _declared()
+
+
+def test_host_argument_errors_without_gpu():
+    from pipeline_schedule_simulation_gb300 import binding as B
+    L = B.LIB
+    nul = None
+    def ev(pol, P, M, v, n=4, f=1, b=1, si=1):
+        return L.pp_sched_eval(pol, P, M, v, f, b, si, 0, 0, nul, 0, 0, n, nul, nul, nul, nul,
+                               nul, nul, nul, 0, 0, nul, nul)
+    assert ev(5, 4, 8, 1) == B.PP_ERR_ARG           # unknown policy
+    assert ev(B.ONEF1B, 0, 8, 1) == B.PP_ERR_ARG    # P < 1
+    assert ev(B.ONEF1B, 4, 0, 1) == B.PP_ERR_ARG    # M < 1
+    assert ev(B.ONEF1B, 4, 8, 2) == B.PP_ERR_ARG    # v != 1 for 1F1B
+    assert ev(B.INTERLEAVED, 4, 8, 1) == B.PP_ERR_ARG  # v < 2 for interleaved
+    assert ev(B.INTERLEAVED, 4, 6, 2) == B.PP_ERR_DIVISIBILITY
+    assert ev(B.ONEF1B, 17, 8, 1) == B.PP_ERR_SIZE  # P beyond the limit
+    assert ev(B.INTERLEAVED, 16, 32, 8) == B.PP_ERR_SIZE  # S = 128
+    assert ev(B.ONEF1B, 4, 8, 1, n=-1) == B.PP_ERR_ARG
+    assert ev(B.ONEF1B, 4, 8, 1, f=0) == B.PP_ERR_ARG   # NULL costs with n > 0
+    assert ev(B.ONEF1B, 4, 8, 1, si=-1) == B.PP_ERR_ARG
+    h = ctypes.c_void_p()
+    assert L.pp_sched_plan(B.GPIPE, 4, 8, 2, ctypes.byref(h), nul) == B.PP_ERR_ARG
+    assert L.pp_sched_plan(B.ONEF1B, 4, 8, 1, None, nul) == B.PP_ERR_ARG
+    # partition search argument checks
+    def ps(L_, P, M, n=10, ptr=8):
+        return L.pp_sched_partition_search(ptr, ptr, ptr, L_, P, M, 0, 0, 0, 0, n, ptr, nul, nul,
+                                           nul, nul)
+    assert ps(80, 0, 8) == B.PP_ERR_ARG
+    assert ps(4, 8, 8) == B.PP_ERR_ARG          # fewer layers than stages
+    assert ps(300, 8, 8) == B.PP_ERR_SIZE       # L beyond 256
+    assert ps(80, 8, 8, n=1 << 32) == B.PP_ERR_SIZE
+    assert ps(80, 8, 8, ptr=12) == B.PP_ERR_ARG  # best_idx not 8-byte aligned
+    for c in range(7):
+        assert L.pp_sched_status_str(c)

@@ -1,0 +1,185 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle,
+element by element, bit-exact (all quantities are integers; the bubble's float
+view is checked to 1e-12)."""
+import numpy as np
+import pytest
+
+import pipeline_schedule_simulation_gb300.workloads as W
+from gpu_helpers import assert_same, run_gpu, run_oracle, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from pipeline_schedule_simulation_gb300 import binding
+    return binding
+
+
+def test_config1_every_op(orc, B):
+    for batch in W.config1():
+        g = run_gpu(batch, op_times=True)
+        r = run_oracle(orc, batch, op_times=True)
+        assert_same(g, r, op_times=True)
+    # the worked 2x4 tables end in 10 units; config 1 in 33 with bubble 36/132
+    g = run_gpu(W.uniform_batch(W.ONEF1B, 4, 8, 1, [1], [2], [0]))
+    assert g["makespan"][0] == 33 and g["bub_num"][0] == 36 and g["bub_den"][0] == 132
+    assert list(g["peak"]) == [4, 3, 2, 1]
+
+
+def test_plan_tables_match_oracle(orc, B):
+    for policy, P, M, v in [(0, 4, 8, 1), (1, 4, 8, 1), (1, 8, 3, 1), (2, 4, 8, 2), (2, 8, 16, 4),
+                            (1, 16, 128, 1), (2, 3, 6, 3), (1, 1, 5, 1), (2, 1, 3, 4)]:
+        plan = B.Plan(policy, P, M, v)
+        ops, peak, rnd = plan.tables()
+        kind, chunk, mb = B.op_fields(ops)
+        okind, ochunk, omb = orc.order(policy, P, M, v)
+        assert np.array_equal(kind.numpy(), okind)
+        assert np.array_equal(chunk.numpy(), ochunk)
+        assert np.array_equal(mb.numpy(), omb)
+        # rounds are the start ticks at unit cost and zero comm
+        ref = orc.evaluate(policy, P, M, v, 1, 1)
+        assert np.array_equal(rnd.numpy(), ref["start"])
+        assert np.array_equal(peak.numpy(), ref["peak"])
+        assert plan.rounds == ref["makespan"]
+        assert plan.register_path == (1 if v == 1 else 0)
+
+
+SHAPES = [
+    (W.GPIPE, 1, 1, 1), (W.ONEF1B, 1, 7, 1), (W.GPIPE, 2, 4, 1), (W.ONEF1B, 3, 2, 1),
+    (W.ONEF1B, 4, 8, 1), (W.GPIPE, 5, 13, 1), (W.ONEF1B, 8, 3, 1), (W.ONEF1B, 8, 64, 1),
+    (W.GPIPE, 8, 64, 1), (W.ONEF1B, 12, 20, 1), (W.ONEF1B, 16, 40, 1), (W.GPIPE, 16, 9, 1),
+    (W.INTERLEAVED, 2, 4, 2), (W.INTERLEAVED, 4, 8, 2), (W.INTERLEAVED, 3, 9, 3),
+    (W.INTERLEAVED, 8, 16, 4), (W.INTERLEAVED, 16, 32, 2), (W.INTERLEAVED, 1, 3, 5),
+]
+
+
+@pytest.mark.parametrize("policy,P,M,v", SHAPES)
+@pytest.mark.parametrize("layout", ["inst_minor", "inst_major"])
+def test_random_batches(orc, B, policy, P, M, v, layout):
+    # several warps and a ragged tail: n = 32*k + r
+    for n, seed, mbz in ((77, 1, False), (161, 2, True)):
+        batch = W.random_batch(policy, P, M, v, n, seed=seed + 10 * P + M, hi=12, comm_hi=5,
+                               layout=layout, stride_mb_zero=mbz)
+        g = run_gpu(batch, op_times=True)
+        r = run_oracle(orc, batch, op_times=True)
+        assert_same(g, r, op_times=True)
+
+
+def test_zero_costs_and_empty(orc, B):
+    batch = W.random_batch(W.ONEF1B, 4, 6, 1, 40, seed=3, lo=0, hi=0, comm_hi=0)
+    g = run_gpu(batch)
+    assert (g["makespan"] == 0).all() and (g["bub_den"] == 0).all() and (g["bub_num"] == 0).all()
+    r = run_oracle(orc, batch)
+    assert_same(g, r)
+    empty = W.random_batch(W.ONEF1B, 4, 6, 1, 0, seed=3)
+    out = B.evaluate(1, 4, 6, 1, to_dev(np.zeros(4, np.int32)), to_dev(np.zeros(4, np.int32)),
+                     empty.strides, 0)
+    assert out["makespan"].numel() == 0
+
+
+def test_status_negative_and_overflow(orc, B):
+    batch = W.random_batch(W.ONEF1B, 4, 8, 1, 70, seed=4, layout="inst_major")
+    cf = batch.cost_f.reshape(70, 4, 8)
+    cb = batch.cost_b.reshape(70, 4, 8)
+    cf[3, 2, 5] = -1
+    cb[10, 0, 0] = 2**31 - 1
+    cb[11, 3, 7] = 2**30
+    cf[11, 0, 0] = 2**30
+    batch.comm.reshape(70, 3)[20, 1] = -4
+    batch.comm.reshape(70, 3)[21, 1] = 2**31 - 2
+    g = run_gpu(batch)
+    r = run_oracle(orc, batch)
+    assert g["status"][3] == B.ST_NEG_COST and g["status"][20] == B.ST_NEG_COST
+    assert g["status"][10] == B.ST_OVERFLOW and g["status"][21] == B.ST_OVERFLOW
+    assert_same(g, r)
+
+
+def test_config2_closed_form_sweep(orc, B):
+    """Every shape of the closed-form sweep (GPipe, 1F1B, interleaved v=2):
+    bit-exact against the oracle and equal to the pages' closed forms."""
+    from fractions import Fraction
+    for policy, P, M, v in W.config2_shapes():
+        batch = W.config2_batch(policy, P, M, v)
+        g = run_gpu(batch)
+        tf = batch.cost_f
+        tb = batch.cost_b
+        cm = batch.comm
+        if policy != W.INTERLEAVED:
+            base = (M + P - 1) * (tf.astype(np.int64) + tb)
+            nocomm = cm == 0
+            assert np.array_equal(g["makespan"][nocomm], base[nocomm])
+            if policy == W.GPIPE:
+                assert np.array_equal(g["makespan"], base + 2 * (P - 1) * cm)
+        else:
+            sel = (cm == 0) & (tf == tb)
+            for x in np.nonzero(sel)[0]:
+                assert Fraction(int(g["bub_num"][x]), int(g["bub_den"][x])) == Fraction(P - 1, v * M + P - 1)
+        if (P + M) % 5 == 0 or P in (2, 16) or M in (1, 128):
+            r = run_oracle(orc, batch)
+            assert_same(g, r)
+
+
+def test_config3_full_batch_sampled(orc, B):
+    """65,536 heterogeneous 1F1B instances (P=8, M=64) in the benchmark's
+    launch configuration; 600 sampled instances re-derived by the oracle, and
+    invariants that hold for every instance."""
+    batch = W.config3()
+    g = run_gpu(batch)
+    rng = np.random.default_rng(0)
+    sel = np.unique(np.concatenate([rng.choice(batch.n, 600, replace=False), [0, 31, 32, batch.n - 1]]))
+    r = run_oracle(orc, batch, select=sel)
+    assert_same(g, r, select=sel)
+    assert (g["status"] == 0).all()
+    # invariants for all: busy = makespan - idle equals the summed costs
+    cf = batch.cost_f.reshape(8, 64, batch.n).astype(np.int64)
+    cb = batch.cost_b.reshape(8, 64, batch.n).astype(np.int64)
+    busy = (cf.sum(axis=1) + cb.sum(axis=1)).T
+    assert np.array_equal(g["makespan"][:, None] - g["idle"], busy)
+    assert np.array_equal(g["bub_num"], g["idle"].astype(np.int64).sum(axis=1))
+    assert np.array_equal(g["bub_den"], 8 * g["makespan"].astype(np.int64))
+    # a lower bound every valid schedule meets: stage 0's own work plus the
+    # first microbatch's round trip
+    assert (g["makespan"] >= busy[:, 0]).all()
+
+
+@pytest.mark.parametrize("v", [2, 4])
+def test_config4_interleaved_sampled(orc, B, v):
+    il, base = W.config4(v)
+    for batch in (il, base):
+        g = run_gpu(batch)
+        sel = np.unique(np.random.default_rng(v).choice(batch.n, 96, replace=False))
+        r = run_oracle(orc, batch, select=sel)
+        assert_same(g, r, select=sel)
+        assert (g["status"] == 0).all()
+
+
+def test_split_call_equals_whole(orc, B):
+    """Sharding by instance range (one GPU, two calls) gives the same numbers."""
+    batch = W.config3(n=4096)
+    whole = run_gpu(batch)
+    import torch
+    cf, cb, cm = to_dev(batch.cost_f), to_dev(batch.cost_b), to_dev(batch.comm)
+    half = batch.n // 2
+    parts = []
+    for lo, hi in ((0, half), (half, batch.n)):
+        out = B.evaluate(batch.policy, 8, 64, 1, cf[lo:], cb[lo:], batch.strides, hi - lo,
+                         comm=cm[lo:], comm_strides=batch.comm_strides)
+        parts.append({k: t.cpu().numpy() for k, t in out.items()})
+    torch.cuda.synchronize()
+    for k in ("makespan", "idle", "bub_num", "bub_den", "status"):
+        assert np.array_equal(np.concatenate([p[k] for p in parts]), whole[k])
+
+
+def test_host_entry_end_to_end(B):
+    import torch
+    batch = W.config3(n=1000)
+    ref = run_gpu(batch)
+    host, h2d, d2h = B.evaluate_host(batch.policy, 8, 64, 1, torch.from_numpy(batch.cost_f).pin_memory(),
+                                     torch.from_numpy(batch.cost_b).pin_memory(), batch.strides, batch.n,
+                                     comm=torch.from_numpy(batch.comm).pin_memory(),
+                                     comm_strides=batch.comm_strides)
+    torch.cuda.synchronize()
+    assert h2d == batch.cost_f.nbytes * 2 + batch.comm.nbytes
+    for k in ("makespan", "idle", "bub_num", "bub_den", "status"):
+        assert np.array_equal(host[k].numpy(), ref[k])

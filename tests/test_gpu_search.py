@@ -1,0 +1,80 @@
+"""GPU partition search against the oracle's candidate scorer (bit-exact
+makespans, identical argmin with ties to the lower candidate index)."""
+import numpy as np
+import pytest
+import torch
+
+import pipeline_schedule_simulation_gb300.workloads as W
+from gpu_helpers import to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from pipeline_schedule_simulation_gb300 import binding
+    return binding
+
+
+def _gpu_search(B, p, begin, n, all_mk=True):
+    out = B.partition_search(to_dev(p.layer_tf), to_dev(p.layer_tb), to_dev(p.layer_act), p.P, p.M,
+                             p.comm, p.cap, p.seed, begin, n, all_makespan=all_mk)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+@pytest.mark.parametrize("L,P,M,comm,cap", [(8, 3, 6, 0, 10**12), (20, 5, 10, 2, 9), (12, 1, 4, 0, 10**9),
+                                            (30, 8, 16, 1, 40), (40, 16, 20, 0, 10**12)])
+def test_small_exact(orc, B, L, P, M, comm, cap):
+    rng = np.random.default_rng(L + P)
+    p = W.SearchProblem(rng.integers(1, 20, L).astype(np.int32), rng.integers(1, 40, L).astype(np.int32),
+                        rng.integers(1, 4, L).astype(np.int64), P, M, comm, cap, 1234 + L, 0)
+    n = 3000
+    g = _gpu_search(B, p, 0, n)
+    r = orc.search(p.layer_tf, p.layer_tb, p.layer_act, P, M, comm, cap, p.seed, 0, n, nthreads=8)
+    assert np.array_equal(g["all_makespan"], r["all_makespan"])
+    assert int(g["best_idx"][0]) == r["best_idx"]
+    assert int(g["best_makespan"][0]) == r["best_makespan"]
+    if P > 1 and r["best_idx"] >= 0:
+        assert list(g["best_cuts"]) == list(r["first"][1:P])
+
+
+def test_nothing_feasible(B):
+    p = W.SearchProblem(np.full(10, 5, np.int32), np.full(10, 9, np.int32), np.full(10, 100, np.int64),
+                        4, 8, 0, 10, 7, 0)
+    g = _gpu_search(B, p, 0, 500)
+    assert g["best_idx"][0] == -1 and g["best_makespan"][0] == -1
+    assert (g["best_cuts"] == -1).all() and (g["all_makespan"] == -1).all()
+
+
+def test_config5_full(orc, B):
+    """1,048,576 candidates of the 80-layer model at P=8, M=128: the winner is
+    the lowest-index minimum of all makespans; the oracle re-scores the winner,
+    its stage split and 200 sampled candidates."""
+    p = W.config5()
+    g = _gpu_search(B, p, 0, p.n_cand)
+    mk = g["all_makespan"]
+    feas = mk >= 0
+    assert feas.any()
+    best = int(g["best_idx"][0])
+    assert mk[best] == mk[feas].min() == int(g["best_makespan"][0])
+    assert best == int(np.nonzero(mk == mk[feas].min())[0][0])
+    r = orc.search(p.layer_tf, p.layer_tb, p.layer_act, p.P, p.M, p.comm, p.cap, p.seed, best, best + 1)
+    assert r["best_makespan"] == mk[best]
+    assert list(g["best_cuts"]) == list(r["first"][1:p.P])
+    rng = np.random.default_rng(55)
+    for start in rng.choice(p.n_cand - 8, 25, replace=False):
+        rs = orc.search(p.layer_tf, p.layer_tb, p.layer_act, p.P, p.M, p.comm, p.cap, p.seed,
+                        int(start), int(start) + 8, nthreads=8)
+        assert np.array_equal(rs["all_makespan"], mk[start:start + 8])
+
+
+def test_split_ranges_reduce_to_whole(B):
+    from pipeline_schedule_simulation_gb300.sharding import best_of
+    p = W.config5(n_cand=1 << 16)
+    whole = _gpu_search(B, p, 0, p.n_cand, all_mk=False)
+    parts = []
+    for lo, hi in ((0, 30000), (30000, 1 << 16)):
+        g = _gpu_search(B, p, lo, hi - lo, all_mk=False)
+        parts.append((int(g["best_makespan"][0]), int(g["best_idx"][0])))
+    assert best_of(parts) == (int(whole["best_makespan"][0]), int(whole["best_idx"][0]))
