@@ -24,6 +24,7 @@ namespace pps {
 struct EvalArgs {
     const uint32_t *desc;    // [R][PMAX]
     const uint32_t *desc2;   // [R][PMAX] (generic evaluator)
+    const uint64_t *rw;      // [R] per-round kind words and patterns
     int R, P, M, v, S, O, nslots;
     const int32_t *cost_f, *cost_b;
     int64_t s_inst, s_stage, s_mb;
@@ -67,30 +68,48 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// Issue the copies of round `rl`'s costs into ring slice rl % kSlices.
+// The loader's view of one round: the descriptors of the devices this lane
+// copies for (vector path: devices 4i + lane/8; scalar path: every device).
 template <int PMAX, bool VEC>
-__device__ __forceinline__ void load_round(const EvalArgs &a, int rl, int32_t *ring, int64_t inst0,
-                                           int lane) {
+struct LoadDesc {
+    static constexpr int kN = VEC ? PMAX / 4 : PMAX;
+    uint32_t d[kN];
+};
+
+template <int PMAX, bool VEC>
+__device__ __forceinline__ void fetch_load_desc(const EvalArgs &a, int rl, int lane, LoadDesc<PMAX, VEC> &ld) {
+    const uint32_t *drow = a.desc + (int64_t)rl * PMAX;
+#pragma unroll
+    for (int i = 0; i < LoadDesc<PMAX, VEC>::kN; ++i)
+        ld.d[i] = __ldg(drow + (VEC ? 4 * i + (lane >> 3) : i));
+}
+
+// Issue the copies of round `rl`'s costs into ring slice rl % kSlices.  The
+// vector path needs every element offset to fit in 32 bits (checked on the
+// host) and computes it in 32-bit arithmetic.
+template <int PMAX, bool VEC>
+__device__ __forceinline__ void load_round(const EvalArgs &a, int rl, const LoadDesc<PMAX, VEC> &ld,
+                                           int32_t *ring, int64_t inst0, int lane) {
     using RG = Ring<PMAX>;
     int32_t *slice = ring + (rl % RG::kSlices) * (PMAX * 32);
-    const uint32_t *drow = a.desc + (int64_t)rl * PMAX;
     if constexpr (VEC) {
         // lanes 8q..8q+7 cover device 4*i + q, 4 instances each
         const int g = lane & 7;
         const int64_t x0 = inst0 + 4 * g;
         const int64_t left = a.n - x0;
         const uint32_t bytes_in = left <= 0 ? 0u : (left >= 4 ? 16u : (uint32_t)left * 4u);
+        const int s_stage = (int)a.s_stage, s_mb = (int)a.s_mb;
 #pragma unroll
         for (int i = 0; i < PMAX / 4; ++i) {
             const int k = 4 * i + (lane >> 3);
-            const uint32_t d = __ldg(drow + k);
+            const uint32_t d = ld.d[i];
             const uint32_t kind = desc_kind(d);
             const int32_t *base = kind == kBwd ? a.cost_b : a.cost_f;
-            const int64_t s = (int64_t)desc_chunk(d) * a.P + k;
+            const int s = (int)desc_chunk(d) * a.P + k;
             const int32_t *src = base;
             uint32_t nb = 0;
             if (kind != kIdle && bytes_in) {
-                src = base + s * a.s_stage + (int64_t)desc_mb(d) * a.s_mb + x0;
+                src = base + (s * s_stage + (int)desc_mb(d) * s_mb) + x0;
                 nb = bytes_in;
             }
             cp_async16(smem_addr(slice + k * 32 + 4 * g), src, nb);
@@ -100,7 +119,7 @@ __device__ __forceinline__ void load_round(const EvalArgs &a, int rl, int32_t *r
         const bool live = x < a.n;
 #pragma unroll
         for (int k = 0; k < PMAX; ++k) {
-            const uint32_t d = __ldg(drow + k);
+            const uint32_t d = ld.d[k];
             const uint32_t kind = desc_kind(d);
             const int32_t *base = kind == kBwd ? a.cost_b : a.cost_f;
             const int32_t *src = base;

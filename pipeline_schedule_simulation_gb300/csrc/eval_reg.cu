@@ -13,9 +13,105 @@
 // neighbouring device at the start of the op's round, so the whole state of an
 // instance is four registers per device: the device's free tick, the arrival
 // tick of its latest F and latest B at the neighbour, and its busy ticks.
+#include <utility>
+
 #include "eval_common.cuh"
 
 namespace pps {
+
+// Register state of one instance: per device its free tick, the arrival tick
+// of its latest forward result at device k+1 (rf) and of its latest backward
+// result at device k-1 (rb), its busy ticks, and (per-op output only) its op
+// counter.  cF[k] is the comm of boundary k|k+1; a backward result of device k
+// crosses boundary k-1, whose comm is cF[k-1].
+template <int PMAX>
+struct RegState {
+    int fr[PMAX], rf[PMAX], rb[PMAX], busy[PMAX], cnt[PMAX], cF[PMAX];
+    uint32_t accE, accC;
+};
+
+// One op on device K with input arrival `arr` and cost `c`.
+template <int PMAX, bool OPS, bool FWD, int K>
+__device__ __forceinline__ void reg_op(RegState<PMAX> &S, int arr, int c, const EvalArgs &a, int64_t x,
+                                       bool live) {
+    const int st = max(S.fr[K], arr);
+    const int en = wrap_add(st, c);
+    S.fr[K] = en;
+    S.busy[K] = wrap_add(S.busy[K], c);
+    S.accE |= (uint32_t)en | (uint32_t)arr;
+    S.accC |= (uint32_t)c;
+    if constexpr (FWD) S.rf[K] = wrap_add(en, S.cF[K]);
+    else S.rb[K] = wrap_add(en, K > 0 ? S.cF[K > 0 ? K - 1 : 0] : 0);
+    if constexpr (OPS) {
+        if (live) {
+            const int64_t off = x * a.o_inst + ((int64_t)K * a.O + S.cnt[K]) * a.o_op;
+            if (a.op_start) a.op_start[off] = st;
+            if (a.op_end) a.op_end[off] = en;
+        }
+        ++S.cnt[K];
+    }
+}
+
+template <int PMAX, int K>
+__device__ __forceinline__ int in_fwd(const RegState<PMAX> &S) { return K > 0 ? S.rf[K > 0 ? K - 1 : 0] : 0; }
+template <int PMAX, int K>
+__device__ __forceinline__ int in_bwd(const RegState<PMAX> &S) {
+    return K < PMAX - 1 ? S.rb[K < PMAX - 1 ? K + 1 : 0] : 0;
+}
+
+// Static round bodies (every device busy, P == PMAX).  In the alternating
+// patterns a device's input comes from a neighbour running the other kind this
+// round, so no snapshot is needed; in all-F (all-B) rounds devices run from the
+// last (first) so each reads its input before the neighbour overwrites it.
+template <int PMAX, bool OPS, bool EVEN_FWD, int K = 0>
+__device__ __forceinline__ void round_alt(RegState<PMAX> &S, const int32_t *slice, int lane, const EvalArgs &a,
+                                          int64_t x, bool live) {
+    if constexpr (K < PMAX) {
+        const int c = slice[K * 32 + lane];
+        constexpr bool fwd = ((K & 1) == 0) == EVEN_FWD;
+        if constexpr (fwd) reg_op<PMAX, OPS, true, K>(S, in_fwd<PMAX, K>(S), c, a, x, live);
+        else reg_op<PMAX, OPS, false, K>(S, in_bwd<PMAX, K>(S), c, a, x, live);
+        round_alt<PMAX, OPS, EVEN_FWD, K + 1>(S, slice, lane, a, x, live);
+    }
+}
+
+template <int PMAX, bool OPS, int K = PMAX - 1>
+__device__ __forceinline__ void round_all_f(RegState<PMAX> &S, const int32_t *slice, int lane, const EvalArgs &a,
+                                            int64_t x, bool live) {
+    if constexpr (K >= 0) {
+        reg_op<PMAX, OPS, true, K>(S, in_fwd<PMAX, K>(S), slice[K * 32 + lane], a, x, live);
+        round_all_f<PMAX, OPS, K - 1>(S, slice, lane, a, x, live);
+    }
+}
+
+template <int PMAX, bool OPS, int K = 0>
+__device__ __forceinline__ void round_all_b(RegState<PMAX> &S, const int32_t *slice, int lane, const EvalArgs &a,
+                                            int64_t x, bool live) {
+    if constexpr (K < PMAX) {
+        reg_op<PMAX, OPS, false, K>(S, in_bwd<PMAX, K>(S), slice[K * 32 + lane], a, x, live);
+        round_all_b<PMAX, OPS, K + 1>(S, slice, lane, a, x, live);
+    }
+}
+
+// Any other round: inputs are read as of the start of the round, then each
+// device runs its op (or none) by its 2-bit kind.
+template <int PMAX, bool OPS>
+__device__ __forceinline__ void round_generic(RegState<PMAX> &S, uint32_t kinds, const int32_t *slice, int lane,
+                                              const EvalArgs &a, int64_t x, bool live) {
+    int inF[PMAX], inB[PMAX];
+#pragma unroll
+    for (int k = 0; k < PMAX; ++k) {
+        inF[k] = k > 0 ? S.rf[k > 0 ? k - 1 : 0] : 0;
+        inB[k] = k < PMAX - 1 ? S.rb[k < PMAX - 1 ? k + 1 : 0] : 0;
+    }
+    [&]<int... K>(std::integer_sequence<int, K...>) {
+        ([&] {
+            const uint32_t kind = (kinds >> (2 * K)) & 3u;
+            if (kind == kFwd) reg_op<PMAX, OPS, true, K>(S, inF[K], slice[K * 32 + lane], a, x, live);
+            else if (kind == kBwd) reg_op<PMAX, OPS, false, K>(S, inB[K], slice[K * 32 + lane], a, x, live);
+        }(), ...);
+    }(std::make_integer_sequence<int, PMAX>{});
+}
 
 template <int PMAX, bool VEC, bool OPS>
 __global__ void __launch_bounds__(128) k_eval_reg(const EvalArgs a) {
@@ -28,72 +124,53 @@ __global__ void __launch_bounds__(128) k_eval_reg(const EvalArgs a) {
     const int64_t x = inst0 + lane;
     const bool live = x < a.n;
 
-    // Outgoing comm per device: a forward result of device k crosses boundary k,
-    // a backward result of device k crosses boundary k-1.
-    int cF[PMAX], cB[PMAX];
+    RegState<PMAX> S;
     uint32_t neg = 0;
 #pragma unroll
     for (int k = 0; k < PMAX; ++k) {
-        cF[k] = 0;
-        cB[k] = 0;
-        if (a.comm && live) {
-            if (k < a.P - 1) cF[k] = a.comm[x * a.c_inst + (int64_t)k * a.c_bnd];
-            if (k >= 1 && k < a.P) cB[k] = a.comm[x * a.c_inst + (int64_t)(k - 1) * a.c_bnd];
-        }
-        neg |= (uint32_t)cF[k] | (uint32_t)cB[k];
+        S.cF[k] = 0;
+        if (a.comm && live && k < a.P - 1) S.cF[k] = a.comm[x * a.c_inst + (int64_t)k * a.c_bnd];
+        neg |= (uint32_t)S.cF[k];
+        S.fr[k] = 0; S.rf[k] = 0; S.rb[k] = 0; S.busy[k] = 0; S.cnt[k] = 0;
     }
-    int fr[PMAX], rf[PMAX], rb[PMAX], busy[PMAX], cnt[PMAX];
-#pragma unroll
-    for (int k = 0; k < PMAX; ++k) { fr[k] = 0; rf[k] = 0; rb[k] = 0; busy[k] = 0; cnt[k] = 0; }
-    uint32_t accE = 0, accC = 0;
+    S.accE = 0; S.accC = 0;
 
     const int R = a.R;
+    LoadDesc<PMAX, VEC> ld;
 #pragma unroll 1
     for (int q = 0; q < RG::kAhead; ++q) {
-        if (q < R) load_round<PMAX, VEC>(a, q, ring, inst0, lane);
+        if (q < R) {
+            fetch_load_desc<PMAX, VEC>(a, q, lane, ld);
+            load_round<PMAX, VEC>(a, q, ld, ring, inst0, lane);
+        }
         cp_async_commit();
     }
+    if (RG::kAhead < R) fetch_load_desc<PMAX, VEC>(a, RG::kAhead, lane, ld);
+    uint64_t w = __ldg(a.rw);
 #pragma unroll 1
     for (int r = 0; r < R; ++r) {
-        if (r + RG::kAhead < R) load_round<PMAX, VEC>(a, r + RG::kAhead, ring, inst0, lane);
+        const int rl = r + RG::kAhead;
+        if (rl < R) {
+            load_round<PMAX, VEC>(a, rl, ld, ring, inst0, lane);
+            if (rl + 1 < R) fetch_load_desc<PMAX, VEC>(a, rl + 1, lane, ld);
+        }
         cp_async_commit();
-        uint32_t d[PMAX];
-        load_desc<PMAX>(a.desc + (int64_t)r * PMAX, d);
+        const uint64_t wnext = r + 1 < R ? __ldg(a.rw + r + 1) : 0ull;
         cp_async_wait<RG::kAhead>();
         __syncwarp();
         const int32_t *slice = ring + (r % RG::kSlices) * (PMAX * 32);
-        int rf0[PMAX], rb0[PMAX];  // inputs are read as of the start of the round
-#pragma unroll
-        for (int k = 0; k < PMAX; ++k) { rf0[k] = rf[k]; rb0[k] = rb[k]; }
-#pragma unroll
-        for (int k = 0; k < PMAX; ++k) {
-            const uint32_t kind = desc_kind(d[k]);
-            if (kind == kIdle) continue;
-            const int c = slice[k * 32 + lane];
-            int arr;
-            if (kind == kFwd) arr = k > 0 ? rf0[k > 0 ? k - 1 : 0] : 0;
-            else arr = k < PMAX - 1 ? rb0[k < PMAX - 1 ? k + 1 : 0] : 0;
-            const int st = max(fr[k], arr);
-            const int en = wrap_add(st, c);
-            fr[k] = en;
-            busy[k] = wrap_add(busy[k], c);
-            accE |= (uint32_t)en | (uint32_t)arr;
-            accC |= (uint32_t)c;
-            if (kind == kFwd) rf[k] = wrap_add(en, cF[k]);
-            else rb[k] = wrap_add(en, cB[k]);
-            if constexpr (OPS) {
-                if (live) {
-                    const int64_t off = x * a.o_inst + ((int64_t)k * a.O + cnt[k]) * a.o_op;
-                    if (a.op_start) a.op_start[off] = st;
-                    if (a.op_end) a.op_end[off] = en;
-                }
-                ++cnt[k];
-            }
+        switch (rw_pattern(w)) {
+            case kPatAltA: round_alt<PMAX, OPS, true>(S, slice, lane, a, x, live); break;
+            case kPatAltB: round_alt<PMAX, OPS, false>(S, slice, lane, a, x, live); break;
+            case kPatAllF: round_all_f<PMAX, OPS>(S, slice, lane, a, x, live); break;
+            case kPatAllB: round_all_b<PMAX, OPS>(S, slice, lane, a, x, live); break;
+            default: round_generic<PMAX, OPS>(S, rw_kinds(w), slice, lane, a, x, live); break;
         }
+        w = wnext;
         __syncwarp();
     }
     cp_async_wait<0>();
-    if (live) write_results<PMAX>(a, x, fr, busy, accC | neg, accE);
+    if (live) write_results<PMAX>(a, x, S.fr, S.busy, S.accC | neg, S.accE);
 }
 
 template <int PMAX, bool VEC, bool OPS>
@@ -148,7 +225,7 @@ extern "C" int pp_sched_eval(pp_policy_t policy, int P, int M, int v, const int3
         PPS_CUDA_TRY(cudaMemcpyAsync(peak, plan->d_peak, P * sizeof(int32_t), cudaMemcpyDeviceToDevice, stream));
     if (n_instances == 0) return PP_OK;
     EvalArgs a;
-    a.desc = plan->d_desc; a.desc2 = plan->d_desc2;
+    a.desc = plan->d_desc; a.desc2 = plan->d_desc2; a.rw = plan->d_rw;
     a.R = plan->R; a.P = P; a.M = M; a.v = v; a.S = plan->S; a.O = plan->O; a.nslots = plan->nslots;
     a.cost_f = cost_f; a.cost_b = cost_b;
     a.s_inst = stride_inst; a.s_stage = stride_stage; a.s_mb = stride_mb;
@@ -158,7 +235,8 @@ extern "C" int pp_sched_eval(pp_policy_t policy, int P, int M, int v, const int3
     a.op_start = op_start; a.op_end = op_end; a.o_inst = op_stride_inst; a.o_op = op_stride_op;
     const bool vec = stride_inst == 1 && (reinterpret_cast<uintptr_t>(cost_f) & 15) == 0 &&
                      (reinterpret_cast<uintptr_t>(cost_b) & 15) == 0 && stride_stage % 4 == 0 &&
-                     stride_mb % 4 == 0;
+                     stride_mb % 4 == 0 &&
+                     (int64_t)(plan->S - 1) * stride_stage + (int64_t)(M - 1) * stride_mb < ((int64_t)1 << 31);
     const bool ops = op_start || op_end;
     if (plan->reg_ok) return launch_eval_reg(plan, a, vec, ops, stream);
     return launch_eval_slot(plan, a, vec, ops, stream);

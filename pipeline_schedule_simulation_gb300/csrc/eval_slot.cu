@@ -39,14 +39,21 @@ __global__ void __launch_bounds__(128) k_eval_slot(const EvalArgs a) {
     uint32_t accE = 0, accC = 0;
 
     const int R = a.R;
+    LoadDesc<PMAX, VEC> ld;
 #pragma unroll 1
     for (int q = 0; q < RG::kAhead; ++q) {
-        if (q < R) load_round<PMAX, VEC>(a, q, ring, inst0, lane);
+        if (q < R) {
+            fetch_load_desc<PMAX, VEC>(a, q, lane, ld);
+            load_round<PMAX, VEC>(a, q, ld, ring, inst0, lane);
+        }
         cp_async_commit();
     }
 #pragma unroll 1
     for (int r = 0; r < R; ++r) {
-        if (r + RG::kAhead < R) load_round<PMAX, VEC>(a, r + RG::kAhead, ring, inst0, lane);
+        if (r + RG::kAhead < R) {
+            fetch_load_desc<PMAX, VEC>(a, r + RG::kAhead, lane, ld);
+            load_round<PMAX, VEC>(a, r + RG::kAhead, ld, ring, inst0, lane);
+        }
         cp_async_commit();
         uint32_t d[PMAX], d2[PMAX];
         load_desc<PMAX>(a.desc + (int64_t)r * PMAX, d);

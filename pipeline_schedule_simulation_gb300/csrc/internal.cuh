@@ -35,6 +35,20 @@ __host__ __device__ inline uint32_t d2_cbnd(uint32_t d) { return (d >> 16) & 0xF
 
 constexpr int kMaxValueSlots = 64;
 
+// Per-round word, one uint64 per round:
+//   bits 0..31  kind of device k in bits 2k..2k+1 (kIdle / kFwd / kBwd)
+//   bits 32..39 pattern of the whole round, when every device runs an op and
+//               the device count equals the table width:
+//                 kPatAllF  every device runs a forward
+//                 kPatAllB  every device runs a backward
+//                 kPatAltA  even devices forward, odd devices backward
+//                 kPatAltB  even devices backward, odd devices forward
+//               (the 1F1B steady phase alternates A and B; GPipe's middle
+//               rounds are all-F then all-B); kPatGeneric otherwise.
+constexpr uint32_t kPatGeneric = 0, kPatAllF = 1, kPatAllB = 2, kPatAltA = 3, kPatAltB = 4;
+__host__ __device__ inline uint32_t rw_kinds(uint64_t w) { return (uint32_t)w; }
+__host__ __device__ inline uint32_t rw_pattern(uint64_t w) { return (uint32_t)(w >> 32) & 0xFFu; }
+
 // Width of the device dimension a kernel is compiled for (>= P).
 inline int pmax_for(int P) { return P <= 4 ? 4 : (P <= 8 ? 8 : 16); }
 
@@ -52,6 +66,7 @@ struct pp_plan {
     int32_t *d_round;   // [P][O] wavefront round of each op
     uint32_t *d_desc;   // [R][pmax]
     uint32_t *d_desc2;  // [R][pmax] (generic evaluator), may be null
+    uint64_t *d_rw;     // [R] per-round kind words and patterns
     int32_t *d_peak;    // [P]
     int32_t h_peak[PP_MAX_P];
 };

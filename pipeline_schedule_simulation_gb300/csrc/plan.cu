@@ -144,6 +144,30 @@ __global__ void k_desc(const uint32_t *ops, const int32_t *round, int P, int M, 
         desc_pack(op_kind(op) ? kBwd : kFwd, (uint32_t)op_chunk(op), (uint32_t)op_mb(op));
 }
 
+// One thread per round: pack the devices' kinds and classify the round.
+__global__ void k_rwords(const uint32_t *desc, int R, int P, int pmax, uint64_t *rw) {
+    int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= R) return;
+    uint32_t kinds = 0;
+    bool allF = true, allB = true, altA = true, altB = true;
+    for (int k = 0; k < pmax; ++k) {
+        uint32_t kd = desc_kind(desc[(int64_t)r * pmax + k]);
+        kinds |= kd << (2 * k);
+        allF &= kd == kFwd;
+        allB &= kd == kBwd;
+        altA &= kd == ((k & 1) ? kBwd : kFwd);
+        altB &= kd == ((k & 1) ? kFwd : kBwd);
+    }
+    uint32_t pat = kPatGeneric;
+    if (P == pmax) {
+        if (allF) pat = kPatAllF;
+        else if (allB) pat = kPatAllB;
+        else if (altA) pat = kPatAltA;
+        else if (altB) pat = kPatAltB;
+    }
+    rw[r] = (uint64_t)kinds | ((uint64_t)pat << 32);
+}
+
 __global__ void k_peak(const uint32_t *ops, int P, int O, int32_t *peak) {
     int k = threadIdx.x;
     if (k >= P) return;
@@ -245,7 +269,7 @@ static int build_plan(int policy, int P, int M, int v, cudaStream_t st, pp_plan 
     if (rc) return rc;
     const int S = P * v, O = 2 * M * v, pmax = pmax_for(P);
     const int64_t nops = (int64_t)P * O, npos = 2LL * S * M;
-    DevBuf ops, pos, round, info, peak, desc, desc2, slot_of;
+    DevBuf ops, pos, round, info, peak, desc, desc2, slot_of, rw;
     PPS_CUDA_TRY(cudaMalloc(&ops.p, nops * sizeof(uint32_t)));
     PPS_CUDA_TRY(cudaMalloc(&pos.p, npos * sizeof(int32_t)));
     PPS_CUDA_TRY(cudaMalloc(&round.p, nops * sizeof(int32_t)));
@@ -269,6 +293,8 @@ static int build_plan(int policy, int P, int M, int v, cudaStream_t st, pp_plan 
     k_desc<<<nblk, tpb, 0, st>>>(ops.as<uint32_t>(), round.as<int32_t>(), P, M, v, pmax,
                                  desc.as<uint32_t>());
     k_peak<<<1, 32, 0, st>>>(ops.as<uint32_t>(), P, O, peak.as<int32_t>());
+    PPS_CUDA_TRY(cudaMalloc(&rw.p, (int64_t)R * sizeof(uint64_t)));
+    k_rwords<<<(R + 255) / 256, 256, 0, st>>>(desc.as<uint32_t>(), R, P, pmax, rw.as<uint64_t>());
     int reg_ok = 0;
     if (v == 1) {
         k_latest<<<nblk, tpb, 0, st>>>(ops.as<uint32_t>(), pos.as<int32_t>(), round.as<int32_t>(), P, M,
@@ -305,6 +331,7 @@ static int build_plan(int policy, int P, int M, int v, cudaStream_t st, pp_plan 
     p->d_round = round.as<int32_t>(); round.p = nullptr;
     p->d_desc = desc.as<uint32_t>(); desc.p = nullptr;
     p->d_desc2 = desc2.as<uint32_t>(); desc2.p = nullptr;
+    p->d_rw = rw.as<uint64_t>(); rw.p = nullptr;
     p->d_peak = peak.as<int32_t>(); peak.p = nullptr;
     *out = p;
     return PP_OK;
@@ -370,6 +397,7 @@ void pp_sched_plan_destroy(pp_plan_t *p) {
     cudaFree(p->d_round);
     cudaFree(p->d_desc);
     if (p->d_desc2) cudaFree(p->d_desc2);
+    cudaFree(p->d_rw);
     cudaFree(p->d_peak);
     delete p;
 }
