@@ -134,6 +134,93 @@ __device__ __forceinline__ void load_round(const EvalArgs &a, int rl, const Load
     }
 }
 
+// Loader offset table, built once per CTA in shared memory: for every
+// (round, device) the element offset of the op's cost row relative to its
+// array, shifted left by one with bit 0 set for a backward op; 0xFFFFFFFF for
+// an idle slot.  Needs every offset below 2^30 (checked on the host).
+constexpr uint32_t kLtIdle = 0xFFFFFFFFu;
+
+template <int PMAX>
+__device__ __forceinline__ void build_load_table(const EvalArgs &a, uint32_t *lt) {
+    const int total = a.R * PMAX;
+    const int s_stage = (int)a.s_stage, s_mb = (int)a.s_mb;
+    for (int e = threadIdx.x; e < total; e += blockDim.x) {
+        const uint32_t d = __ldg(a.desc + e);
+        const uint32_t kind = desc_kind(d);
+        uint32_t v = kLtIdle;
+        if (kind != kIdle) {
+            const int s = (int)desc_chunk(d) * a.P + (e % PMAX);
+            const uint32_t off = (uint32_t)(s * s_stage + (int)desc_mb(d) * s_mb);
+            v = (off << 1) | (kind == kBwd ? 1u : 0u);
+        }
+        lt[e] = v;
+    }
+}
+
+// Vector loader driven by the table: lanes 8q..8q+7 copy device 4i+q's row for
+// the warp's 32 instances, 16 bytes (4 instances) each.
+template <int PMAX>
+__device__ __forceinline__ void load_round_lt(const uint32_t *lt, int rl, int32_t *ring, const int32_t *fbase,
+                                              const int32_t *bbase, uint32_t bytes_in, int lane) {
+    using RG = Ring<PMAX>;
+    int32_t *slice = ring + (rl % RG::kSlices) * (PMAX * 32);
+    const int g = lane & 7;
+#pragma unroll
+    for (int i = 0; i < PMAX / 4; ++i) {
+        const int k = 4 * i + (lane >> 3);
+        const uint32_t e = lt[rl * PMAX + k];
+        const int32_t *src = (e & 1u) ? bbase : fbase;
+        uint32_t nb = 0;
+        if (e != kLtIdle) {
+            src += e >> 1;
+            nb = bytes_in;
+        }
+        cp_async16(smem_addr(slice + k * 32 + 4 * g), src, nb);
+    }
+}
+
+// True if any cost of instance x is negative (read from global memory; used
+// only to classify an instance whose sticky sign flag was raised).
+static __device__ __noinline__ bool any_negative_cost(const EvalArgs &a, int64_t x) {
+    for (int s = 0; s < a.S; ++s)
+        for (int i = 0; i < a.M; ++i) {
+            const int64_t off = x * a.s_inst + (int64_t)s * a.s_stage + (int64_t)i * a.s_mb;
+            if (a.cost_f[off] < 0 || a.cost_b[off] < 0) return true;
+        }
+    return false;
+}
+
+// Per-instance reductions for the unsigned evaluators.  `flag` carries the
+// sign bits of every op's start tick and cost (see k_eval_reg): it is clear
+// exactly when no cost is negative and every tick fits in int32.  A raised
+// flag is classified by re-reading the instance's costs.
+template <int PMAX>
+__device__ __forceinline__ void write_results_u(const EvalArgs &a, int64_t x, const uint32_t (&fr)[PMAX],
+                                                const uint32_t (&busy)[PMAX], uint32_t flag, bool neg_comm) {
+    uint32_t mk = 0;
+#pragma unroll
+    for (int k = 0; k < PMAX; ++k) mk = max(mk, fr[k]);
+    flag |= mk;
+    int64_t num = 0;
+#pragma unroll
+    for (int k = 0; k < PMAX; ++k) {
+        if (k < a.P) {
+            const int idle = (int)(mk - busy[k]);
+            num += idle;
+            if (a.idle) a.idle[x * a.P + k] = idle;
+        }
+    }
+    if (a.makespan) a.makespan[x] = (int)mk;
+    if (a.bub_num) a.bub_num[x] = num;
+    if (a.bub_den) a.bub_den[x] = (int64_t)a.P * (int)mk;
+    if (a.status) {
+        int8_t st = PP_ST_OK;
+        if (neg_comm) st = PP_ST_NEG_COST;
+        else if (flag >> 31) st = any_negative_cost(a, x) ? PP_ST_NEG_COST : PP_ST_OVERFLOW;
+        a.status[x] = st;
+    }
+}
+
 // Load the round's descriptors (identical for every lane of the warp).
 template <int PMAX>
 __device__ __forceinline__ void load_desc(const uint32_t *row, uint32_t (&d)[PMAX]) {

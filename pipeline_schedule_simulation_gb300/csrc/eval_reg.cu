@@ -19,6 +19,19 @@
 
 namespace pps {
 
+// Overflow and negative-cost detection.  All true ticks are >= 0.  Ticks are
+// carried as uint32 and compared unsigned, and every op ORs its start tick and
+// its cost into one sticky word; the final makespan is ORed in too.  If no cost
+// is negative and every true tick is below 2^31, every value is exact and no
+// sign bit is ever set.  Otherwise take the first op, in evaluation order,
+// whose true end reaches 2^31: its inputs are exact and below 2^31 (an arrival
+// is an exact end plus a comm below 2^31, so below 2^32), hence its start is
+// exact; if the start reaches 2^31 it is flagged, else its end is exact and
+// becomes the free tick of the device, so the next op's start (an unsigned max
+// with it) or the final makespan carries the sign bit.  A negative cost carries
+// it directly.  So the word's sign bit is set exactly when the instance is
+// flagged; which flag is decided by re-reading the costs (rare path).
+
 // Register state of one instance: per device its free tick, the arrival tick
 // of its latest forward result at device k+1 (rf) and of its latest backward
 // result at device k-1 (rb), its busy ticks, and (per-op output only) its op
@@ -26,70 +39,75 @@ namespace pps {
 // crosses boundary k-1, whose comm is cF[k-1].
 template <int PMAX>
 struct RegState {
-    int fr[PMAX], rf[PMAX], rb[PMAX], busy[PMAX], cnt[PMAX], cF[PMAX];
-    uint32_t accE, accC;
+    uint32_t fr[PMAX], rf[PMAX], rb[PMAX], busy[PMAX], cF[PMAX];
+    int cnt[PMAX];
+    uint32_t flag;
 };
 
 // One op on device K with input arrival `arr` and cost `c`.
 template <int PMAX, bool OPS, bool FWD, int K>
-__device__ __forceinline__ void reg_op(RegState<PMAX> &S, int arr, int c, const EvalArgs &a, int64_t x,
-                                       bool live) {
-    const int st = max(S.fr[K], arr);
-    const int en = wrap_add(st, c);
+__device__ __forceinline__ void reg_op(RegState<PMAX> &S, uint32_t arr, uint32_t c, const EvalArgs &a,
+                                       int64_t x, bool live) {
+    const uint32_t st = max(S.fr[K], arr);
+    const uint32_t en = st + c;
     S.fr[K] = en;
-    S.busy[K] = wrap_add(S.busy[K], c);
-    S.accE |= (uint32_t)en | (uint32_t)arr;
-    S.accC |= (uint32_t)c;
-    if constexpr (FWD) S.rf[K] = wrap_add(en, S.cF[K]);
-    else S.rb[K] = wrap_add(en, K > 0 ? S.cF[K > 0 ? K - 1 : 0] : 0);
+    S.busy[K] += c;
+    S.flag |= st | c;
+    if constexpr (FWD) S.rf[K] = en + S.cF[K];
+    else S.rb[K] = en + (K > 0 ? S.cF[K > 0 ? K - 1 : 0] : 0u);
     if constexpr (OPS) {
         if (live) {
             const int64_t off = x * a.o_inst + ((int64_t)K * a.O + S.cnt[K]) * a.o_op;
-            if (a.op_start) a.op_start[off] = st;
-            if (a.op_end) a.op_end[off] = en;
+            if (a.op_start) a.op_start[off] = (int)st;
+            if (a.op_end) a.op_end[off] = (int)en;
         }
         ++S.cnt[K];
     }
 }
 
 template <int PMAX, int K>
-__device__ __forceinline__ int in_fwd(const RegState<PMAX> &S) { return K > 0 ? S.rf[K > 0 ? K - 1 : 0] : 0; }
+__device__ __forceinline__ uint32_t in_fwd(const RegState<PMAX> &S) { return K > 0 ? S.rf[K > 0 ? K - 1 : 0] : 0u; }
 template <int PMAX, int K>
-__device__ __forceinline__ int in_bwd(const RegState<PMAX> &S) {
-    return K < PMAX - 1 ? S.rb[K < PMAX - 1 ? K + 1 : 0] : 0;
+__device__ __forceinline__ uint32_t in_bwd(const RegState<PMAX> &S) {
+    return K < PMAX - 1 ? S.rb[K < PMAX - 1 ? K + 1 : 0] : 0u;
 }
 
-// Static round bodies (every device busy, P == PMAX).  In the alternating
-// patterns a device's input comes from a neighbour running the other kind this
-// round, so no snapshot is needed; in all-F (all-B) rounds devices run from the
-// last (first) so each reads its input before the neighbour overwrites it.
-template <int PMAX, bool OPS, bool EVEN_FWD, int K = 0>
-__device__ __forceinline__ void round_alt(RegState<PMAX> &S, const int32_t *slice, int lane, const EvalArgs &a,
-                                          int64_t x, bool live) {
+// Pattern round bodies.  In the alternating patterns a device's input comes
+// from a neighbour that runs the other kind (or nothing) this round, so it is
+// unchanged by the round; in all-F (all-B) rounds devices run from the last
+// (first) so each reads its input before the neighbour overwrites it.  MASKED
+// bodies run only the devices whose bit is set.
+template <int PMAX, bool OPS, bool MASKED, bool EVEN_FWD, int K = 0>
+__device__ __forceinline__ void round_alt(RegState<PMAX> &S, uint32_t mask, const int32_t *slice, int lane,
+                                          const EvalArgs &a, int64_t x, bool live) {
     if constexpr (K < PMAX) {
-        const int c = slice[K * 32 + lane];
-        constexpr bool fwd = ((K & 1) == 0) == EVEN_FWD;
-        if constexpr (fwd) reg_op<PMAX, OPS, true, K>(S, in_fwd<PMAX, K>(S), c, a, x, live);
-        else reg_op<PMAX, OPS, false, K>(S, in_bwd<PMAX, K>(S), c, a, x, live);
-        round_alt<PMAX, OPS, EVEN_FWD, K + 1>(S, slice, lane, a, x, live);
+        if (!MASKED || ((mask >> K) & 1u)) {
+            const uint32_t c = (uint32_t)slice[K * 32 + lane];
+            constexpr bool fwd = ((K & 1) == 0) == EVEN_FWD;
+            if constexpr (fwd) reg_op<PMAX, OPS, true, K>(S, in_fwd<PMAX, K>(S), c, a, x, live);
+            else reg_op<PMAX, OPS, false, K>(S, in_bwd<PMAX, K>(S), c, a, x, live);
+        }
+        round_alt<PMAX, OPS, MASKED, EVEN_FWD, K + 1>(S, mask, slice, lane, a, x, live);
     }
 }
 
-template <int PMAX, bool OPS, int K = PMAX - 1>
-__device__ __forceinline__ void round_all_f(RegState<PMAX> &S, const int32_t *slice, int lane, const EvalArgs &a,
-                                            int64_t x, bool live) {
+template <int PMAX, bool OPS, bool MASKED, int K = PMAX - 1>
+__device__ __forceinline__ void round_all_f(RegState<PMAX> &S, uint32_t mask, const int32_t *slice, int lane,
+                                            const EvalArgs &a, int64_t x, bool live) {
     if constexpr (K >= 0) {
-        reg_op<PMAX, OPS, true, K>(S, in_fwd<PMAX, K>(S), slice[K * 32 + lane], a, x, live);
-        round_all_f<PMAX, OPS, K - 1>(S, slice, lane, a, x, live);
+        if (!MASKED || ((mask >> K) & 1u))
+            reg_op<PMAX, OPS, true, K>(S, in_fwd<PMAX, K>(S), (uint32_t)slice[K * 32 + lane], a, x, live);
+        round_all_f<PMAX, OPS, MASKED, K - 1>(S, mask, slice, lane, a, x, live);
     }
 }
 
-template <int PMAX, bool OPS, int K = 0>
-__device__ __forceinline__ void round_all_b(RegState<PMAX> &S, const int32_t *slice, int lane, const EvalArgs &a,
-                                            int64_t x, bool live) {
+template <int PMAX, bool OPS, bool MASKED, int K = 0>
+__device__ __forceinline__ void round_all_b(RegState<PMAX> &S, uint32_t mask, const int32_t *slice, int lane,
+                                            const EvalArgs &a, int64_t x, bool live) {
     if constexpr (K < PMAX) {
-        reg_op<PMAX, OPS, false, K>(S, in_bwd<PMAX, K>(S), slice[K * 32 + lane], a, x, live);
-        round_all_b<PMAX, OPS, K + 1>(S, slice, lane, a, x, live);
+        if (!MASKED || ((mask >> K) & 1u))
+            reg_op<PMAX, OPS, false, K>(S, in_bwd<PMAX, K>(S), (uint32_t)slice[K * 32 + lane], a, x, live);
+        round_all_b<PMAX, OPS, MASKED, K + 1>(S, mask, slice, lane, a, x, live);
     }
 }
 
@@ -98,97 +116,150 @@ __device__ __forceinline__ void round_all_b(RegState<PMAX> &S, const int32_t *sl
 template <int PMAX, bool OPS>
 __device__ __forceinline__ void round_generic(RegState<PMAX> &S, uint32_t kinds, const int32_t *slice, int lane,
                                               const EvalArgs &a, int64_t x, bool live) {
-    int inF[PMAX], inB[PMAX];
+    uint32_t inF[PMAX], inB[PMAX];
 #pragma unroll
     for (int k = 0; k < PMAX; ++k) {
-        inF[k] = k > 0 ? S.rf[k > 0 ? k - 1 : 0] : 0;
-        inB[k] = k < PMAX - 1 ? S.rb[k < PMAX - 1 ? k + 1 : 0] : 0;
+        inF[k] = k > 0 ? S.rf[k > 0 ? k - 1 : 0] : 0u;
+        inB[k] = k < PMAX - 1 ? S.rb[k < PMAX - 1 ? k + 1 : 0] : 0u;
     }
     [&]<int... K>(std::integer_sequence<int, K...>) {
         ([&] {
             const uint32_t kind = (kinds >> (2 * K)) & 3u;
-            if (kind == kFwd) reg_op<PMAX, OPS, true, K>(S, inF[K], slice[K * 32 + lane], a, x, live);
-            else if (kind == kBwd) reg_op<PMAX, OPS, false, K>(S, inB[K], slice[K * 32 + lane], a, x, live);
+            const uint32_t c = (uint32_t)slice[K * 32 + lane];
+            if (kind == kFwd) reg_op<PMAX, OPS, true, K>(S, inF[K], c, a, x, live);
+            else if (kind == kBwd) reg_op<PMAX, OPS, false, K>(S, inB[K], c, a, x, live);
         }(), ...);
     }(std::make_integer_sequence<int, PMAX>{});
 }
 
-template <int PMAX, bool VEC, bool OPS>
+template <int PMAX, bool OPS>
+__device__ __forceinline__ void run_round(RegState<PMAX> &S, uint64_t w, const int32_t *slice, int lane,
+                                          const EvalArgs &a, int64_t x, bool live) {
+    const uint32_t m = rw_mask(w);
+    switch (rw_pattern(w)) {
+        case kPatAltA: round_alt<PMAX, OPS, false, true>(S, m, slice, lane, a, x, live); break;
+        case kPatAltB: round_alt<PMAX, OPS, false, false>(S, m, slice, lane, a, x, live); break;
+        case kPatAllF: round_all_f<PMAX, OPS, false>(S, m, slice, lane, a, x, live); break;
+        case kPatAllB: round_all_b<PMAX, OPS, false>(S, m, slice, lane, a, x, live); break;
+        case kPatMasked + kPatAltA: round_alt<PMAX, OPS, true, true>(S, m, slice, lane, a, x, live); break;
+        case kPatMasked + kPatAltB: round_alt<PMAX, OPS, true, false>(S, m, slice, lane, a, x, live); break;
+        case kPatMasked + kPatAllF: round_all_f<PMAX, OPS, true>(S, m, slice, lane, a, x, live); break;
+        case kPatMasked + kPatAllB: round_all_b<PMAX, OPS, true>(S, m, slice, lane, a, x, live); break;
+        default: round_generic<PMAX, OPS>(S, rw_kinds(w), slice, lane, a, x, live); break;
+    }
+}
+
+// LT: the vector loader runs from the per-CTA offset table (dynamic shared
+// memory holds the table, then one ring per warp).
+template <int PMAX, bool VEC, bool OPS, bool LT>
 __global__ void __launch_bounds__(128) k_eval_reg(const EvalArgs a) {
     using RG = Ring<PMAX>;
     extern __shared__ __align__(16) int32_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int32_t *ring = smem + warp * RG::kWords;
+    const int lt_words = LT ? ((a.R * PMAX + 3) & ~3) : 0;
+    uint32_t *lt = reinterpret_cast<uint32_t *>(smem);
+    if constexpr (LT) {
+        build_load_table<PMAX>(a, lt);
+        __syncthreads();
+    }
+    int32_t *ring = smem + lt_words + warp * RG::kWords;
     const int64_t inst0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + warp) * 32;
-    if (inst0 >= a.n) return;  // warp-uniform
+    if (inst0 >= a.n) return;  // warp-uniform, after the block barrier
     const int64_t x = inst0 + lane;
     const bool live = x < a.n;
 
     RegState<PMAX> S;
-    uint32_t neg = 0;
+    uint32_t negc = 0;
 #pragma unroll
     for (int k = 0; k < PMAX; ++k) {
-        S.cF[k] = 0;
-        if (a.comm && live && k < a.P - 1) S.cF[k] = a.comm[x * a.c_inst + (int64_t)k * a.c_bnd];
-        neg |= (uint32_t)S.cF[k];
+        int c = 0;
+        if (a.comm && live && k < a.P - 1) c = a.comm[x * a.c_inst + (int64_t)k * a.c_bnd];
+        negc |= (uint32_t)c;
+        S.cF[k] = (uint32_t)c;
         S.fr[k] = 0; S.rf[k] = 0; S.rb[k] = 0; S.busy[k] = 0; S.cnt[k] = 0;
     }
-    S.accE = 0; S.accC = 0;
+    S.flag = 0;
+
+    // loader state
+    const int g = lane & 7;
+    const int64_t x0 = inst0 + 4 * g;
+    const int64_t left = a.n - x0;
+    const uint32_t bytes_in = left <= 0 ? 0u : (left >= 4 ? 16u : (uint32_t)left * 4u);
+    const int32_t *fbase = a.cost_f + (bytes_in ? x0 : 0);
+    const int32_t *bbase = a.cost_b + (bytes_in ? x0 : 0);
+    LoadDesc<PMAX, VEC> ld;
+    auto issue = [&](int rl) {
+        if constexpr (LT) load_round_lt<PMAX>(lt, rl, ring, fbase, bbase, bytes_in, lane);
+        else load_round<PMAX, VEC>(a, rl, ld, ring, inst0, lane);
+    };
 
     const int R = a.R;
-    LoadDesc<PMAX, VEC> ld;
 #pragma unroll 1
     for (int q = 0; q < RG::kAhead; ++q) {
         if (q < R) {
-            fetch_load_desc<PMAX, VEC>(a, q, lane, ld);
-            load_round<PMAX, VEC>(a, q, ld, ring, inst0, lane);
+            if constexpr (!LT) fetch_load_desc<PMAX, VEC>(a, q, lane, ld);
+            issue(q);
         }
         cp_async_commit();
     }
-    if (RG::kAhead < R) fetch_load_desc<PMAX, VEC>(a, RG::kAhead, lane, ld);
+    if constexpr (!LT) {
+        if (RG::kAhead < R) fetch_load_desc<PMAX, VEC>(a, RG::kAhead, lane, ld);
+    }
     uint64_t w = __ldg(a.rw);
 #pragma unroll 1
     for (int r = 0; r < R; ++r) {
         const int rl = r + RG::kAhead;
         if (rl < R) {
-            load_round<PMAX, VEC>(a, rl, ld, ring, inst0, lane);
-            if (rl + 1 < R) fetch_load_desc<PMAX, VEC>(a, rl + 1, lane, ld);
+            issue(rl);
+            if constexpr (!LT) {
+                if (rl + 1 < R) fetch_load_desc<PMAX, VEC>(a, rl + 1, lane, ld);
+            }
         }
         cp_async_commit();
         const uint64_t wnext = r + 1 < R ? __ldg(a.rw + r + 1) : 0ull;
         cp_async_wait<RG::kAhead>();
         __syncwarp();
-        const int32_t *slice = ring + (r % RG::kSlices) * (PMAX * 32);
-        switch (rw_pattern(w)) {
-            case kPatAltA: round_alt<PMAX, OPS, true>(S, slice, lane, a, x, live); break;
-            case kPatAltB: round_alt<PMAX, OPS, false>(S, slice, lane, a, x, live); break;
-            case kPatAllF: round_all_f<PMAX, OPS>(S, slice, lane, a, x, live); break;
-            case kPatAllB: round_all_b<PMAX, OPS>(S, slice, lane, a, x, live); break;
-            default: round_generic<PMAX, OPS>(S, rw_kinds(w), slice, lane, a, x, live); break;
-        }
+        run_round<PMAX, OPS>(S, w, ring + (r % RG::kSlices) * (PMAX * 32), lane, a, x, live);
         w = wnext;
         __syncwarp();
     }
     cp_async_wait<0>();
-    if (live) write_results<PMAX>(a, x, S.fr, S.busy, S.accC | neg, S.accE);
+    if (live) write_results_u<PMAX>(a, x, S.fr, S.busy, S.flag, (negc >> 31) != 0);
 }
 
-template <int PMAX, bool VEC, bool OPS>
+// Largest loader table kept in shared memory (words); bigger plans use the
+// in-loop address computation.
+constexpr int kMaxLtWords = 6144;
+
+template <int PMAX, bool VEC, bool OPS, bool LT>
 static int launch_reg_t(const EvalArgs &a, cudaStream_t st) {
-    constexpr int kWarps = 2;
-    const size_t smem = (size_t)kWarps * Ring<PMAX>::kWords * sizeof(int32_t);
+    constexpr int kWarps = 4;
+    const size_t lt_bytes = LT ? (size_t)((a.R * PMAX + 3) & ~3) * sizeof(uint32_t) : 0;
+    const size_t smem = lt_bytes + (size_t)kWarps * Ring<PMAX>::kWords * sizeof(int32_t);
+    int dev = 0;
+    PPS_CUDA_TRY(cudaGetDevice(&dev));
+    static bool attr_set[64] = {};
+    if (dev < 64 && !attr_set[dev]) {
+        PPS_CUDA_TRY(cudaFuncSetAttribute(k_eval_reg<PMAX, VEC, OPS, LT>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024));
+        attr_set[dev] = true;
+    }
     const int64_t warps = (a.n + 31) / 32;
     const int64_t blocks = (warps + kWarps - 1) / kWarps;
     if (blocks > 0x7FFFFFFF) return PP_ERR_SIZE;
-    k_eval_reg<PMAX, VEC, OPS><<<(unsigned)blocks, kWarps * 32, smem, st>>>(a);
+    k_eval_reg<PMAX, VEC, OPS, LT><<<(unsigned)blocks, kWarps * 32, smem, st>>>(a);
     PPS_CUDA_TRY(cudaGetLastError());
     return PP_OK;
 }
 
 template <int PMAX>
 static int launch_reg_p(const EvalArgs &a, bool vec, bool ops, cudaStream_t st) {
-    if (vec) return ops ? launch_reg_t<PMAX, true, true>(a, st) : launch_reg_t<PMAX, true, false>(a, st);
-    return ops ? launch_reg_t<PMAX, false, true>(a, st) : launch_reg_t<PMAX, false, false>(a, st);
+    // the table path needs 16-byte loads and offsets below 2^30
+    const bool lt = vec && (int64_t)a.R * PMAX <= kMaxLtWords &&
+                    (int64_t)(a.S - 1) * a.s_stage + (int64_t)(a.M - 1) * a.s_mb < ((int64_t)1 << 30);
+    if (lt) return ops ? launch_reg_t<PMAX, true, true, true>(a, st) : launch_reg_t<PMAX, true, false, true>(a, st);
+    if (vec) return ops ? launch_reg_t<PMAX, true, true, false>(a, st) : launch_reg_t<PMAX, true, false, false>(a, st);
+    return ops ? launch_reg_t<PMAX, false, true, false>(a, st) : launch_reg_t<PMAX, false, false, false>(a, st);
 }
 
 int launch_eval_reg(const pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st) {

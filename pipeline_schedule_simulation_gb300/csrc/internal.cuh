@@ -4,7 +4,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/ppsched.h"
+#include "ppsched.h"
 
 namespace pps {
 
@@ -44,10 +44,15 @@ constexpr int kMaxValueSlots = 64;
 //                 kPatAltA  even devices forward, odd devices backward
 //                 kPatAltB  even devices backward, odd devices forward
 //               (the 1F1B steady phase alternates A and B; GPipe's middle
-//               rounds are all-F then all-B); kPatGeneric otherwise.
+//               rounds are all-F then all-B); kPatMasked + one of those when
+//               only some devices run an op but each of them follows the
+//               pattern (warmup and cooldown rounds); kPatGeneric otherwise.
+//   bits 48..63 active-device mask (device k runs an op this round)
 constexpr uint32_t kPatGeneric = 0, kPatAllF = 1, kPatAllB = 2, kPatAltA = 3, kPatAltB = 4;
+constexpr uint32_t kPatMasked = 4;  // kPatMasked + kPatAllF .. kPatMasked + kPatAltB
 __host__ __device__ inline uint32_t rw_kinds(uint64_t w) { return (uint32_t)w; }
 __host__ __device__ inline uint32_t rw_pattern(uint64_t w) { return (uint32_t)(w >> 32) & 0xFFu; }
+__host__ __device__ inline uint32_t rw_mask(uint64_t w) { return (uint32_t)(w >> 48); }
 
 // Width of the device dimension a kernel is compiled for (>= P).
 inline int pmax_for(int P) { return P <= 4 ? 4 : (P <= 8 ? 8 : 16); }

@@ -148,24 +148,27 @@ __global__ void k_desc(const uint32_t *ops, const int32_t *round, int P, int M, 
 __global__ void k_rwords(const uint32_t *desc, int R, int P, int pmax, uint64_t *rw) {
     int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= R) return;
-    uint32_t kinds = 0;
+    uint32_t kinds = 0, mask = 0;
     bool allF = true, allB = true, altA = true, altB = true;
     for (int k = 0; k < pmax; ++k) {
         uint32_t kd = desc_kind(desc[(int64_t)r * pmax + k]);
         kinds |= kd << (2 * k);
+        if (kd == kIdle) continue;
+        mask |= 1u << k;
         allF &= kd == kFwd;
         allB &= kd == kBwd;
         altA &= kd == ((k & 1) ? kBwd : kFwd);
         altB &= kd == ((k & 1) ? kFwd : kBwd);
     }
     uint32_t pat = kPatGeneric;
-    if (P == pmax) {
+    if (mask) {
         if (allF) pat = kPatAllF;
         else if (allB) pat = kPatAllB;
         else if (altA) pat = kPatAltA;
         else if (altB) pat = kPatAltB;
+        if (pat != kPatGeneric && (P != pmax || mask != (1u << pmax) - 1u)) pat += kPatMasked;
     }
-    rw[r] = (uint64_t)kinds | ((uint64_t)pat << 32);
+    rw[r] = (uint64_t)kinds | ((uint64_t)pat << 32) | ((uint64_t)mask << 48);
 }
 
 __global__ void k_peak(const uint32_t *ops, int P, int O, int32_t *peak) {
