@@ -25,12 +25,15 @@ struct EvalArgs {
     const uint32_t *desc;    // [R][PMAX]
     const uint32_t *desc2;   // [R][PMAX] (generic evaluator)
     const uint64_t *rw;      // [R] per-round kind words and patterns
+    const uint4 *seg;        // [nseg] segments
+    int nseg;
     int R, P, M, v, S, O, nslots;
     const int32_t *cost_f, *cost_b;
     int64_t s_inst, s_stage, s_mb;
     const int32_t *comm;
     int64_t c_inst, c_bnd;
     int64_t n;
+    int64_t inst_begin;      // first instance of this launch
     int32_t *makespan, *idle;
     int64_t *bub_num, *bub_den;
     int8_t *status;
@@ -38,12 +41,16 @@ struct EvalArgs {
     int64_t o_inst, o_op;
 };
 
+// Loader-table entry of an idle (round, device) slot.
+constexpr uint32_t kLtIdle = 0xFFFFFFFFu;
+
 // Round slices kept per warp: enough prefetch depth to cover HBM latency
 // while the ring stays at 8 KB per warp.
 template <int PMAX>
 struct Ring {
-    static constexpr int kSlices = PMAX == 4 ? 16 : (PMAX == 8 ? 8 : 4);
-    static constexpr int kAhead = kSlices - 1;
+    static constexpr int kSlices = PMAX == 4 ? 16 : 8;
+    static constexpr int kAhead = kSlices - 1;   // kernels that step one round at a time
+    static constexpr int kAhead2 = kSlices - 2;  // kernels that may step two rounds at once
     static constexpr int kWords = kSlices * PMAX * 32;
 };
 
@@ -138,7 +145,6 @@ __device__ __forceinline__ void load_round(const EvalArgs &a, int rl, const Load
 // (round, device) the element offset of the op's cost row relative to its
 // array, shifted left by one with bit 0 set for a backward op; 0xFFFFFFFF for
 // an idle slot.  Needs every offset below 2^30 (checked on the host).
-constexpr uint32_t kLtIdle = 0xFFFFFFFFu;
 
 template <int PMAX>
 __device__ __forceinline__ void build_load_table(const EvalArgs &a, uint32_t *lt) {

@@ -151,11 +151,19 @@ __device__ __forceinline__ void run_round(RegState<PMAX> &S, uint64_t w, const i
 
 // LT: the vector loader runs from the per-CTA offset table (dynamic shared
 // memory holds the table, then one ring per warp).
+//
+// The kernel walks the plan's segments.  Alternating and all-F / all-B
+// segments are tight loops over static round bodies (two rounds per iteration
+// in the alternating case), so the instance's state stays in the same
+// registers across iterations; warmup and cooldown rounds are dispatched one
+// at a time by their round word.  Copies run D = kAhead2 rounds ahead.
 template <int PMAX, bool VEC, bool OPS, bool LT>
 __global__ void __launch_bounds__(128) k_eval_reg(const EvalArgs a) {
     using RG = Ring<PMAX>;
+    constexpr int D = RG::kAhead2;
     extern __shared__ __align__(16) int32_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
     const int lt_words = LT ? ((a.R * PMAX + 3) & ~3) : 0;
     uint32_t *lt = reinterpret_cast<uint32_t *>(smem);
     if constexpr (LT) {
@@ -163,7 +171,7 @@ __global__ void __launch_bounds__(128) k_eval_reg(const EvalArgs a) {
         __syncthreads();
     }
     int32_t *ring = smem + lt_words + warp * RG::kWords;
-    const int64_t inst0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + warp) * 32;
+    const int64_t inst0 = a.inst_begin + ((int64_t)blockIdx.x * nwarps + warp) * 32;
     if (inst0 >= a.n) return;  // warp-uniform, after the block barrier
     const int64_t x = inst0 + lane;
     const bool live = x < a.n;
@@ -187,53 +195,84 @@ __global__ void __launch_bounds__(128) k_eval_reg(const EvalArgs a) {
     const uint32_t bytes_in = left <= 0 ? 0u : (left >= 4 ? 16u : (uint32_t)left * 4u);
     const int32_t *fbase = a.cost_f + (bytes_in ? x0 : 0);
     const int32_t *bbase = a.cost_b + (bytes_in ? x0 : 0);
-    LoadDesc<PMAX, VEC> ld;
-    auto issue = [&](int rl) {
-        if constexpr (LT) load_round_lt<PMAX>(lt, rl, ring, fbase, bbase, bytes_in, lane);
-        else load_round<PMAX, VEC>(a, rl, ld, ring, inst0, lane);
-    };
-
     const int R = a.R;
-#pragma unroll 1
-    for (int q = 0; q < RG::kAhead; ++q) {
-        if (q < R) {
-            if constexpr (!LT) fetch_load_desc<PMAX, VEC>(a, q, lane, ld);
-            issue(q);
-        }
-        cp_async_commit();
-    }
-    if constexpr (!LT) {
-        if (RG::kAhead < R) fetch_load_desc<PMAX, VEC>(a, RG::kAhead, lane, ld);
-    }
-    uint64_t w = __ldg(a.rw);
-#pragma unroll 1
-    for (int r = 0; r < R; ++r) {
-        const int rl = r + RG::kAhead;
+    auto issue = [&](int rl) {
         if (rl < R) {
-            issue(rl);
-            if constexpr (!LT) {
-                if (rl + 1 < R) fetch_load_desc<PMAX, VEC>(a, rl + 1, lane, ld);
+            if constexpr (LT) {
+                load_round_lt<PMAX>(lt, rl, ring, fbase, bbase, bytes_in, lane);
+            } else {
+                LoadDesc<PMAX, VEC> ld;
+                fetch_load_desc<PMAX, VEC>(a, rl, lane, ld);
+                load_round<PMAX, VEC>(a, rl, ld, ring, inst0, lane);
             }
         }
         cp_async_commit();
-        const uint64_t wnext = r + 1 < R ? __ldg(a.rw + r + 1) : 0ull;
-        cp_async_wait<RG::kAhead>();
+    };
+    auto slice = [&](int r) { return ring + (r % RG::kSlices) * (PMAX * 32); };
+    // one round: its copies D ahead, wait for it, run `body`
+    auto step1 = [&](int r, auto &&body) {
+        issue(r + D);
+        cp_async_wait<D>();
         __syncwarp();
-        run_round<PMAX, OPS>(S, w, ring + (r % RG::kSlices) * (PMAX * 32), lane, a, x, live);
-        w = wnext;
+        body(slice(r));
         __syncwarp();
+    };
+    // two rounds: copies for both, then wait for both
+    auto step2 = [&](int r, auto &&body0, auto &&body1) {
+        issue(r + D);
+        issue(r + D + 1);
+        cp_async_wait<D>();
+        __syncwarp();
+        body0(slice(r));
+        body1(slice(r + 1));
+        __syncwarp();
+    };
+    auto altA = [&](const int32_t *sl) { round_alt<PMAX, OPS, false, true>(S, 0u, sl, lane, a, x, live); };
+    auto altB = [&](const int32_t *sl) { round_alt<PMAX, OPS, false, false>(S, 0u, sl, lane, a, x, live); };
+    auto allF = [&](const int32_t *sl) { round_all_f<PMAX, OPS, false>(S, 0u, sl, lane, a, x, live); };
+    auto allB = [&](const int32_t *sl) { round_all_b<PMAX, OPS, false>(S, 0u, sl, lane, a, x, live); };
+
+#pragma unroll 1
+    for (int q = 0; q < D; ++q) issue(q);
+#pragma unroll 1
+    for (int si = 0; si < a.nseg; ++si) {
+        const uint4 sg = __ldg(a.seg + si);
+        int r = (int)sg.y;
+        const int r1 = (int)sg.z;
+        switch (sg.x) {
+            case kSegAltA:
+#pragma unroll 1
+                for (; r + 1 < r1; r += 2) step2(r, altA, altB);
+                if (r < r1) step1(r, altA);
+                break;
+            case kSegAltB:
+#pragma unroll 1
+                for (; r + 1 < r1; r += 2) step2(r, altB, altA);
+                if (r < r1) step1(r, altB);
+                break;
+            case kSegAllF:
+#pragma unroll 1
+                for (; r < r1; ++r) step1(r, allF);
+                break;
+            case kSegAllB:
+#pragma unroll 1
+                for (; r < r1; ++r) step1(r, allB);
+                break;
+            default: {
+                const uint64_t w = __ldg(a.rw + r);
+                step1(r, [&](const int32_t *sl) { run_round<PMAX, OPS>(S, w, sl, lane, a, x, live); });
+                break;
+            }
+        }
     }
     cp_async_wait<0>();
     if (live) write_results_u<PMAX>(a, x, S.fr, S.busy, S.flag, (negc >> 31) != 0);
 }
 
-// Largest loader table kept in shared memory (words); bigger plans use the
-// in-loop address computation.
-constexpr int kMaxLtWords = 6144;
-
 template <int PMAX, bool VEC, bool OPS, bool LT>
-static int launch_reg_t(const EvalArgs &a, cudaStream_t st) {
+static int launch_reg_t(const EvalArgs &a, int64_t begin, int64_t end, cudaStream_t st) {
     constexpr int kWarps = 4;
+    if (end <= begin) return PP_OK;
     const size_t lt_bytes = LT ? (size_t)((a.R * PMAX + 3) & ~3) * sizeof(uint32_t) : 0;
     const size_t smem = lt_bytes + (size_t)kWarps * Ring<PMAX>::kWords * sizeof(int32_t);
     int dev = 0;
@@ -244,22 +283,34 @@ static int launch_reg_t(const EvalArgs &a, cudaStream_t st) {
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024));
         attr_set[dev] = true;
     }
-    const int64_t warps = (a.n + 31) / 32;
+    const int64_t warps = (end - begin + 31) / 32;
     const int64_t blocks = (warps + kWarps - 1) / kWarps;
     if (blocks > 0x7FFFFFFF) return PP_ERR_SIZE;
-    k_eval_reg<PMAX, VEC, OPS, LT><<<(unsigned)blocks, kWarps * 32, smem, st>>>(a);
+    EvalArgs b = a;
+    b.inst_begin = begin;
+    b.n = end;
+    k_eval_reg<PMAX, VEC, OPS, LT><<<(unsigned)blocks, kWarps * 32, smem, st>>>(b);
     PPS_CUDA_TRY(cudaGetLastError());
     return PP_OK;
 }
 
+template <int PMAX, bool OPS>
+static int launch_reg_o(const EvalArgs &a, bool vec, bool lt, cudaStream_t st) {
+    if (lt) return launch_reg_t<PMAX, true, OPS, true>(a, 0, a.n, st);
+    if (vec) return launch_reg_t<PMAX, true, OPS, false>(a, 0, a.n, st);
+    return launch_reg_t<PMAX, false, OPS, false>(a, 0, a.n, st);
+}
+
+// Largest loader table kept in shared memory (words); bigger plans use the
+// in-loop address computation.
+constexpr int kMaxLtWords = 6144;
+
 template <int PMAX>
 static int launch_reg_p(const EvalArgs &a, bool vec, bool ops, cudaStream_t st) {
-    // the table path needs 16-byte loads and offsets below 2^30
+    // the table path needs 16-byte aligned rows and offsets below 2^30
     const bool lt = vec && (int64_t)a.R * PMAX <= kMaxLtWords &&
                     (int64_t)(a.S - 1) * a.s_stage + (int64_t)(a.M - 1) * a.s_mb < ((int64_t)1 << 30);
-    if (lt) return ops ? launch_reg_t<PMAX, true, true, true>(a, st) : launch_reg_t<PMAX, true, false, true>(a, st);
-    if (vec) return ops ? launch_reg_t<PMAX, true, true, false>(a, st) : launch_reg_t<PMAX, true, false, false>(a, st);
-    return ops ? launch_reg_t<PMAX, false, true, false>(a, st) : launch_reg_t<PMAX, false, false, false>(a, st);
+    return ops ? launch_reg_o<PMAX, true>(a, vec, lt, st) : launch_reg_o<PMAX, false>(a, vec, lt, st);
 }
 
 int launch_eval_reg(const pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st) {
@@ -297,11 +348,13 @@ extern "C" int pp_sched_eval(pp_policy_t policy, int P, int M, int v, const int3
     if (n_instances == 0) return PP_OK;
     EvalArgs a;
     a.desc = plan->d_desc; a.desc2 = plan->d_desc2; a.rw = plan->d_rw;
+    a.seg = plan->d_seg; a.nseg = plan->nseg;
     a.R = plan->R; a.P = P; a.M = M; a.v = v; a.S = plan->S; a.O = plan->O; a.nslots = plan->nslots;
     a.cost_f = cost_f; a.cost_b = cost_b;
     a.s_inst = stride_inst; a.s_stage = stride_stage; a.s_mb = stride_mb;
     a.comm = comm; a.c_inst = comm_stride_inst; a.c_bnd = comm_stride_bnd;
     a.n = n_instances;
+    a.inst_begin = 0;
     a.makespan = makespan; a.idle = idle; a.bub_num = bub_num; a.bub_den = bub_den; a.status = status;
     a.op_start = op_start; a.op_end = op_end; a.o_inst = op_stride_inst; a.o_op = op_stride_op;
     const bool vec = stride_inst == 1 && (reinterpret_cast<uintptr_t>(cost_f) & 15) == 0 &&

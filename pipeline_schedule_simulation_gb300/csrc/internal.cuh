@@ -54,6 +54,13 @@ __host__ __device__ inline uint32_t rw_kinds(uint64_t w) { return (uint32_t)w; }
 __host__ __device__ inline uint32_t rw_pattern(uint64_t w) { return (uint32_t)(w >> 32) & 0xFFu; }
 __host__ __device__ inline uint32_t rw_mask(uint64_t w) { return (uint32_t)(w >> 48); }
 
+// Segments: maximal runs of rounds the register evaluator can run as one
+// tight loop.  One uint4 per segment: {type, first round, end round, 0}.
+//   kSegAltA / kSegAltB  rounds alternate kPatAltA / kPatAltB, starting as named
+//   kSegAllF / kSegAllB  every round is kPatAllF / kPatAllB
+//   kSegRound            one round, dispatched by its round word
+constexpr uint32_t kSegRound = 0, kSegAltA = 1, kSegAltB = 2, kSegAllF = 3, kSegAllB = 4;
+
 // Width of the device dimension a kernel is compiled for (>= P).
 inline int pmax_for(int P) { return P <= 4 ? 4 : (P <= 8 ? 8 : 16); }
 
@@ -72,6 +79,8 @@ struct pp_plan {
     uint32_t *d_desc;   // [R][pmax]
     uint32_t *d_desc2;  // [R][pmax] (generic evaluator), may be null
     uint64_t *d_rw;     // [R] per-round kind words and patterns
+    uint4 *d_seg;       // [nseg] segments (register evaluator)
+    int nseg;
     int32_t *d_peak;    // [P]
     int32_t h_peak[PP_MAX_P];
 };

@@ -171,6 +171,32 @@ __global__ void k_rwords(const uint32_t *desc, int R, int P, int pmax, uint64_t 
     rw[r] = (uint64_t)kinds | ((uint64_t)pat << 32) | ((uint64_t)mask << 48);
 }
 
+// One thread: cut the rounds into segments.  info[6] = segment count.
+__global__ void k_segments(const uint64_t *rw, int R, uint4 *seg, int32_t *info) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    int n = 0, r = 0;
+    while (r < R) {
+        const uint32_t pat = rw_pattern(rw[r]);
+        const int r0 = r;
+        uint32_t type = kSegRound;
+        if (pat == kPatAltA || pat == kPatAltB) {
+            uint32_t expect = pat;
+            while (r < R && rw_pattern(rw[r]) == expect) {
+                ++r;
+                expect = expect == kPatAltA ? kPatAltB : kPatAltA;
+            }
+            type = pat == kPatAltA ? kSegAltA : kSegAltB;
+        } else if (pat == kPatAllF || pat == kPatAllB) {
+            while (r < R && rw_pattern(rw[r]) == pat) ++r;
+            type = pat == kPatAllF ? kSegAllF : kSegAllB;
+        } else {
+            ++r;
+        }
+        seg[n++] = make_uint4(type, (uint32_t)r0, (uint32_t)r, 0u);
+    }
+    info[6] = n;
+}
+
 __global__ void k_peak(const uint32_t *ops, int P, int O, int32_t *peak) {
     int k = threadIdx.x;
     if (k >= P) return;
@@ -272,7 +298,7 @@ static int build_plan(int policy, int P, int M, int v, cudaStream_t st, pp_plan 
     if (rc) return rc;
     const int S = P * v, O = 2 * M * v, pmax = pmax_for(P);
     const int64_t nops = (int64_t)P * O, npos = 2LL * S * M;
-    DevBuf ops, pos, round, info, peak, desc, desc2, slot_of, rw;
+    DevBuf ops, pos, round, info, peak, desc, desc2, slot_of, rw, seg;
     PPS_CUDA_TRY(cudaMalloc(&ops.p, nops * sizeof(uint32_t)));
     PPS_CUDA_TRY(cudaMalloc(&pos.p, npos * sizeof(int32_t)));
     PPS_CUDA_TRY(cudaMalloc(&round.p, nops * sizeof(int32_t)));
@@ -298,6 +324,8 @@ static int build_plan(int policy, int P, int M, int v, cudaStream_t st, pp_plan 
     k_peak<<<1, 32, 0, st>>>(ops.as<uint32_t>(), P, O, peak.as<int32_t>());
     PPS_CUDA_TRY(cudaMalloc(&rw.p, (int64_t)R * sizeof(uint64_t)));
     k_rwords<<<(R + 255) / 256, 256, 0, st>>>(desc.as<uint32_t>(), R, P, pmax, rw.as<uint64_t>());
+    PPS_CUDA_TRY(cudaMalloc(&seg.p, (int64_t)R * sizeof(uint4)));
+    k_segments<<<1, 32, 0, st>>>(rw.as<uint64_t>(), R, seg.as<uint4>(), info.as<int32_t>());
     int reg_ok = 0;
     if (v == 1) {
         k_latest<<<nblk, tpb, 0, st>>>(ops.as<uint32_t>(), pos.as<int32_t>(), round.as<int32_t>(), P, M,
@@ -335,6 +363,8 @@ static int build_plan(int policy, int P, int M, int v, cudaStream_t st, pp_plan 
     p->d_desc = desc.as<uint32_t>(); desc.p = nullptr;
     p->d_desc2 = desc2.as<uint32_t>(); desc2.p = nullptr;
     p->d_rw = rw.as<uint64_t>(); rw.p = nullptr;
+    p->d_seg = seg.as<uint4>(); seg.p = nullptr;
+    p->nseg = h_info[6];
     p->d_peak = peak.as<int32_t>(); peak.p = nullptr;
     *out = p;
     return PP_OK;
@@ -401,6 +431,7 @@ void pp_sched_plan_destroy(pp_plan_t *p) {
     cudaFree(p->d_desc);
     if (p->d_desc2) cudaFree(p->d_desc2);
     cudaFree(p->d_rw);
+    cudaFree(p->d_seg);
     cudaFree(p->d_peak);
     delete p;
 }
