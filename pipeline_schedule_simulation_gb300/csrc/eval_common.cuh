@@ -150,17 +150,33 @@ template <int PMAX>
 __device__ __forceinline__ void build_load_table(const EvalArgs &a, uint32_t *lt) {
     const int total = a.R * PMAX;
     const int s_stage = (int)a.s_stage, s_mb = (int)a.s_mb;
-    for (int e = threadIdx.x; e < total; e += blockDim.x) {
-        const uint32_t d = __ldg(a.desc + e);
-        const uint32_t kind = desc_kind(d);
-        uint32_t v = kLtIdle;
-        if (kind != kIdle) {
-            const int s = (int)desc_chunk(d) * a.P + (e % PMAX);
-            const uint32_t off = (uint32_t)(s * s_stage + (int)desc_mb(d) * s_mb);
-            v = (off << 1) | (kind == kBwd ? 1u : 0u);
+    // four independent loads in flight per thread per pass
+    for (int e0 = threadIdx.x; e0 < total; e0 += 4 * blockDim.x) {
+        uint32_t d[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = e0 + u * blockDim.x;
+            d[u] = e < total ? __ldg(a.desc + e) : 0u;
         }
-        lt[e] = v;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = e0 + u * blockDim.x;
+            if (e >= total) break;
+            const uint32_t kind = desc_kind(d[u]);
+            uint32_t v = kLtIdle;
+            if (kind != kIdle) {
+                const int s = (int)desc_chunk(d[u]) * a.P + (e % PMAX);
+                const uint32_t off = (uint32_t)(s * s_stage + (int)desc_mb(d[u]) * s_mb);
+                v = (off << 1) | (kind == kBwd ? 1u : 0u);
+            }
+            lt[e] = v;
+        }
     }
+}
+
+// Copy n 16-byte words from global to shared memory, all threads of the block.
+__device__ __forceinline__ void stage_words(const uint4 *src, uint4 *dst, int n) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = __ldg(src + i);
 }
 
 // Vector loader driven by the table: lanes 8q..8q+7 copy device 4i+q's row for

@@ -65,6 +65,13 @@ __device__ __forceinline__ void reg_op(RegState<PMAX> &S, uint32_t arr, uint32_t
     }
 }
 
+// Shared-memory words of the per-CTA tables: loader table [R][PMAX] (padded
+// to 16 bytes), round words [R] (padded to 16 bytes), segments [nseg].
+template <int PMAX>
+__host__ __device__ inline int lt_smem_words(int R, int nseg) {
+    return ((R * PMAX + 3) & ~3) + 2 * ((R + 1) & ~1) + 4 * nseg;
+}
+
 template <int PMAX, int K>
 __device__ __forceinline__ uint32_t in_fwd(const RegState<PMAX> &S) { return K > 0 ? S.rf[K > 0 ? K - 1 : 0] : 0u; }
 template <int PMAX, int K>
@@ -149,8 +156,9 @@ __device__ __forceinline__ void run_round(RegState<PMAX> &S, uint64_t w, const i
     }
 }
 
-// LT: the vector loader runs from the per-CTA offset table (dynamic shared
-// memory holds the table, then one ring per warp).
+// LT: the vector loader runs from the per-CTA offset table.  Dynamic shared
+// memory then holds the table, the round words and the segment list (so no
+// global load sits on the warmup / cooldown path), then one ring per warp.
 //
 // The kernel walks the plan's segments.  Alternating and all-F / all-B
 // segments are tight loops over static round bodies (two rounds per iteration
@@ -164,11 +172,20 @@ __global__ void __launch_bounds__(128) k_eval_reg(const EvalArgs a) {
     extern __shared__ __align__(16) int32_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
-    const int lt_words = LT ? ((a.R * PMAX + 3) & ~3) : 0;
+    const int lt_words = LT ? lt_smem_words<PMAX>(a.R, a.nseg) : 0;
     uint32_t *lt = reinterpret_cast<uint32_t *>(smem);
+    const uint64_t *rws = a.rw;
+    const uint4 *segs = a.seg;
     if constexpr (LT) {
+        const int tw = (a.R * PMAX + 3) & ~3;
+        uint64_t *rw_s = reinterpret_cast<uint64_t *>(smem + tw);
+        uint4 *seg_s = reinterpret_cast<uint4 *>(smem + tw + 2 * ((a.R + 1) & ~1));
+        stage_words(a.seg, seg_s, a.nseg);
+        stage_words(reinterpret_cast<const uint4 *>(a.rw), reinterpret_cast<uint4 *>(rw_s), (a.R + 1) / 2);
         build_load_table<PMAX>(a, lt);
         __syncthreads();
+        rws = rw_s;
+        segs = seg_s;
     }
     int32_t *ring = smem + lt_words + warp * RG::kWords;
     const int64_t inst0 = a.inst_begin + ((int64_t)blockIdx.x * nwarps + warp) * 32;
@@ -236,7 +253,7 @@ __global__ void __launch_bounds__(128) k_eval_reg(const EvalArgs a) {
     for (int q = 0; q < D; ++q) issue(q);
 #pragma unroll 1
     for (int si = 0; si < a.nseg; ++si) {
-        const uint4 sg = __ldg(a.seg + si);
+        const uint4 sg = segs[si];
         int r = (int)sg.y;
         const int r1 = (int)sg.z;
         switch (sg.x) {
@@ -259,7 +276,7 @@ __global__ void __launch_bounds__(128) k_eval_reg(const EvalArgs a) {
                 for (; r < r1; ++r) step1(r, allB);
                 break;
             default: {
-                const uint64_t w = __ldg(a.rw + r);
+                const uint64_t w = rws[r];
                 step1(r, [&](const int32_t *sl) { run_round<PMAX, OPS>(S, w, sl, lane, a, x, live); });
                 break;
             }
@@ -273,7 +290,7 @@ template <int PMAX, bool VEC, bool OPS, bool LT>
 static int launch_reg_t(const EvalArgs &a, int64_t begin, int64_t end, cudaStream_t st) {
     constexpr int kWarps = 4;
     if (end <= begin) return PP_OK;
-    const size_t lt_bytes = LT ? (size_t)((a.R * PMAX + 3) & ~3) * sizeof(uint32_t) : 0;
+    const size_t lt_bytes = LT ? (size_t)lt_smem_words<PMAX>(a.R, a.nseg) * sizeof(uint32_t) : 0;
     const size_t smem = lt_bytes + (size_t)kWarps * Ring<PMAX>::kWords * sizeof(int32_t);
     int dev = 0;
     PPS_CUDA_TRY(cudaGetDevice(&dev));
@@ -303,12 +320,12 @@ static int launch_reg_o(const EvalArgs &a, bool vec, bool lt, cudaStream_t st) {
 
 // Largest loader table kept in shared memory (words); bigger plans use the
 // in-loop address computation.
-constexpr int kMaxLtWords = 6144;
+constexpr int kMaxLtWords = 8192;
 
 template <int PMAX>
 static int launch_reg_p(const EvalArgs &a, bool vec, bool ops, cudaStream_t st) {
     // the table path needs 16-byte aligned rows and offsets below 2^30
-    const bool lt = vec && (int64_t)a.R * PMAX <= kMaxLtWords &&
+    const bool lt = vec && (int64_t)lt_smem_words<PMAX>(a.R, a.nseg) <= kMaxLtWords &&
                     (int64_t)(a.S - 1) * a.s_stage + (int64_t)(a.M - 1) * a.s_mb < ((int64_t)1 << 30);
     return ops ? launch_reg_o<PMAX, true>(a, vec, lt, st) : launch_reg_o<PMAX, false>(a, vec, lt, st);
 }

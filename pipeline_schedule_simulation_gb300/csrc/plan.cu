@@ -322,7 +322,9 @@ static int build_plan(int policy, int P, int M, int v, cudaStream_t st, pp_plan 
     k_desc<<<nblk, tpb, 0, st>>>(ops.as<uint32_t>(), round.as<int32_t>(), P, M, v, pmax,
                                  desc.as<uint32_t>());
     k_peak<<<1, 32, 0, st>>>(ops.as<uint32_t>(), P, O, peak.as<int32_t>());
-    PPS_CUDA_TRY(cudaMalloc(&rw.p, (int64_t)R * sizeof(uint64_t)));
+    // one spare word so the table can be copied in 16-byte pieces
+    PPS_CUDA_TRY(cudaMalloc(&rw.p, (int64_t)(R + 1) * sizeof(uint64_t)));
+    PPS_CUDA_TRY(cudaMemsetAsync(rw.p, 0, (int64_t)(R + 1) * sizeof(uint64_t), st));
     k_rwords<<<(R + 255) / 256, 256, 0, st>>>(desc.as<uint32_t>(), R, P, pmax, rw.as<uint64_t>());
     PPS_CUDA_TRY(cudaMalloc(&seg.p, (int64_t)R * sizeof(uint4)));
     k_segments<<<1, 32, 0, st>>>(rw.as<uint64_t>(), R, seg.as<uint4>(), info.as<int32_t>());
