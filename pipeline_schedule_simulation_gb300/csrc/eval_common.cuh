@@ -27,6 +27,8 @@ struct EvalArgs {
     const uint64_t *rw;      // [R] per-round kind words and patterns
     const uint4 *seg;        // [nseg] segments
     int nseg;
+    const uint4 *ktab;       // register evaluator's tables for these strides
+    int ktab_words;
     int R, P, M, v, S, O, nslots;
     const int32_t *cost_f, *cost_b;
     int64_t s_inst, s_stage, s_mb;
@@ -46,12 +48,12 @@ constexpr uint32_t kLtIdle = 0xFFFFFFFFu;
 
 // Round slices kept per warp: enough prefetch depth to cover HBM latency
 // while the ring stays at 8 KB per warp.
-template <int PMAX>
+template <int PMAX, int NI = 1>
 struct Ring {
     static constexpr int kSlices = PMAX == 4 ? 16 : 8;
     static constexpr int kAhead = kSlices - 1;   // kernels that step one round at a time
     static constexpr int kAhead2 = kSlices - 2;  // kernels that may step two rounds at once
-    static constexpr int kWords = kSlices * PMAX * 32;
+    static constexpr int kWords = kSlices * PMAX * NI * 32;
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -141,55 +143,25 @@ __device__ __forceinline__ void load_round(const EvalArgs &a, int rl, const Load
     }
 }
 
-// Loader offset table, built once per CTA in shared memory: for every
-// (round, device) the element offset of the op's cost row relative to its
-// array, shifted left by one with bit 0 set for a backward op; 0xFFFFFFFF for
-// an idle slot.  Needs every offset below 2^30 (checked on the host).
+// Loader table (see k_ktab in plan.cu): for every (round, device) the element
+// offset of the op's cost row relative to its array, shifted left by one with
+// bit 0 set for a backward op; kLtIdle for an idle slot.  Offsets stay below
+// 2^30 (checked on the host).
 
-template <int PMAX>
-__device__ __forceinline__ void build_load_table(const EvalArgs &a, uint32_t *lt) {
-    const int total = a.R * PMAX;
-    const int s_stage = (int)a.s_stage, s_mb = (int)a.s_mb;
-    // four independent loads in flight per thread per pass
-    for (int e0 = threadIdx.x; e0 < total; e0 += 4 * blockDim.x) {
-        uint32_t d[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int e = e0 + u * blockDim.x;
-            d[u] = e < total ? __ldg(a.desc + e) : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int e = e0 + u * blockDim.x;
-            if (e >= total) break;
-            const uint32_t kind = desc_kind(d[u]);
-            uint32_t v = kLtIdle;
-            if (kind != kIdle) {
-                const int s = (int)desc_chunk(d[u]) * a.P + (e % PMAX);
-                const uint32_t off = (uint32_t)(s * s_stage + (int)desc_mb(d[u]) * s_mb);
-                v = (off << 1) | (kind == kBwd ? 1u : 0u);
-            }
-            lt[e] = v;
-        }
-    }
-}
-
-// Copy n 16-byte words from global to shared memory, all threads of the block.
-__device__ __forceinline__ void stage_words(const uint4 *src, uint4 *dst, int n) {
-    for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = __ldg(src + i);
-}
-
-// Vector loader driven by the table: lanes 8q..8q+7 copy device 4i+q's row for
-// the warp's 32 instances, 16 bytes (4 instances) each.
-template <int PMAX>
+// Vector loader driven by the table: a row (one device's cost for the warp's
+// 32*NI instances) takes 8*NI lanes, 16 bytes (4 instances) each; lane copies
+// row 32/(8*NI)*i + lane/(8*NI) for i = 0 .. PMAX*NI/4 - 1.  The slice is laid
+// out [device][instance]; fbase/bbase already point at this lane's instances.
+template <int PMAX, int NI>
 __device__ __forceinline__ void load_round_lt(const uint32_t *lt, int rl, int32_t *ring, const int32_t *fbase,
                                               const int32_t *bbase, uint32_t bytes_in, int lane) {
-    using RG = Ring<PMAX>;
-    int32_t *slice = ring + (rl % RG::kSlices) * (PMAX * 32);
-    const int g = lane & 7;
+    using RG = Ring<PMAX, NI>;
+    constexpr int kLanesPerRow = 8 * NI, kRowsPerInst = 32 / kLanesPerRow;
+    int32_t *slice = ring + (rl % RG::kSlices) * (PMAX * NI * 32);
+    const int g = lane % kLanesPerRow;
 #pragma unroll
-    for (int i = 0; i < PMAX / 4; ++i) {
-        const int k = 4 * i + (lane >> 3);
+    for (int i = 0; i < PMAX / kRowsPerInst; ++i) {
+        const int k = kRowsPerInst * i + lane / kLanesPerRow;
         const uint32_t e = lt[rl * PMAX + k];
         const int32_t *src = (e & 1u) ? bbase : fbase;
         uint32_t nb = 0;
@@ -197,7 +169,7 @@ __device__ __forceinline__ void load_round_lt(const uint32_t *lt, int rl, int32_
             src += e >> 1;
             nb = bytes_in;
         }
-        cp_async16(smem_addr(slice + k * 32 + 4 * g), src, nb);
+        cp_async16(smem_addr(slice + k * (NI * 32) + 4 * g), src, nb);
     }
 }
 
@@ -292,7 +264,7 @@ __device__ __forceinline__ int wrap_add(int x, int y) {
 }
 
 // Launchers (defined in eval_reg.cu / eval_slot.cu).
-int launch_eval_reg(const pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st);
+int launch_eval_reg(pp_plan *plan, EvalArgs &a, bool vec, bool ops, cudaStream_t st);
 int launch_eval_slot(const pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st);
 
 }  // namespace pps

@@ -19,6 +19,12 @@
 
 namespace pps {
 
+#ifndef PPS_REG_NI
+#define PPS_REG_NI 1
+#endif
+// Instances per thread of the table-driven register evaluator.
+constexpr int kRegNI = PPS_REG_NI;
+
 // Overflow and negative-cost detection.  All true ticks are >= 0.  Ticks are
 // carried as uint32 and compared unsigned, and every op ORs its start tick and
 // its cost into one sticky word; the final makespan is ORed in too.  If no cost
@@ -32,51 +38,62 @@ namespace pps {
 // it directly.  So the word's sign bit is set exactly when the instance is
 // flagged; which flag is decided by re-reading the costs (rare path).
 
-// Register state of one instance: per device its free tick, the arrival tick
-// of its latest forward result at device k+1 (rf) and of its latest backward
-// result at device k-1 (rb), its busy ticks, and (per-op output only) its op
-// counter.  cF[k] is the comm of boundary k|k+1; a backward result of device k
-// crosses boundary k-1, whose comm is cF[k-1].
-template <int PMAX>
+// Register state of the NI instances a thread evaluates: per instance and
+// device its free tick, the arrival tick of its latest forward result at
+// device k+1 (rf) and of its latest backward result at device k-1 (rb), its
+// busy ticks, and the comm cF[k] of boundary k|k+1 (a backward result of
+// device k crosses boundary k-1, whose comm is cF[k-1]); per device the op
+// counter of the per-op output (the same for every instance).
+template <int PMAX, int NI>
 struct RegState {
-    uint32_t fr[PMAX], rf[PMAX], rb[PMAX], busy[PMAX], cF[PMAX];
+    uint32_t fr[NI][PMAX], rf[NI][PMAX], rb[NI][PMAX], busy[NI][PMAX], cF[NI][PMAX];
     int cnt[PMAX];
-    uint32_t flag;
+    uint32_t flag[NI];
 };
 
-// One op on device K with input arrival `arr` and cost `c`.
-template <int PMAX, bool OPS, bool FWD, int K>
-__device__ __forceinline__ void reg_op(RegState<PMAX> &S, uint32_t arr, uint32_t c, const EvalArgs &a,
-                                       int64_t x, bool live) {
-    const uint32_t st = max(S.fr[K], arr);
-    const uint32_t en = st + c;
-    S.fr[K] = en;
-    S.busy[K] += c;
-    S.flag |= st | c;
-    if constexpr (FWD) S.rf[K] = en + S.cF[K];
-    else S.rb[K] = en + (K > 0 ? S.cF[K > 0 ? K - 1 : 0] : 0u);
-    if constexpr (OPS) {
-        if (live) {
-            const int64_t off = x * a.o_inst + ((int64_t)K * a.O + S.cnt[K]) * a.o_op;
-            if (a.op_start) a.op_start[off] = (int)st;
-            if (a.op_end) a.op_end[off] = (int)en;
+// Where a thread's instances are: instance i of the thread is x[i].
+template <int NI>
+struct Lanes {
+    int lane;
+    int64_t x[NI];
+    bool live[NI];
+};
+
+// One op on device K for every instance of the thread; its cost for instance
+// i is slice[(K*NI + i)*32 + lane].
+template <int PMAX, int NI, bool OPS, bool FWD, int K>
+__device__ __forceinline__ void reg_op(RegState<PMAX, NI> &S, const uint32_t (&arr)[NI], const int32_t *slice,
+                                       const EvalArgs &a, const Lanes<NI> &L) {
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+        const uint32_t c = (uint32_t)slice[(K * NI + i) * 32 + L.lane];
+        const uint32_t st = max(S.fr[i][K], arr[i]);
+        const uint32_t en = st + c;
+        S.fr[i][K] = en;
+        S.busy[i][K] += c;
+        S.flag[i] |= st | c;
+        if constexpr (FWD) S.rf[i][K] = en + S.cF[i][K];
+        else S.rb[i][K] = en + (K > 0 ? S.cF[i][K > 0 ? K - 1 : 0] : 0u);
+        if constexpr (OPS) {
+            if (L.live[i]) {
+                const int64_t off = L.x[i] * a.o_inst + ((int64_t)K * a.O + S.cnt[K]) * a.o_op;
+                if (a.op_start) a.op_start[off] = (int)st;
+                if (a.op_end) a.op_end[off] = (int)en;
+            }
         }
-        ++S.cnt[K];
     }
+    if constexpr (OPS) ++S.cnt[K];
 }
 
-// Shared-memory words of the per-CTA tables: loader table [R][PMAX] (padded
-// to 16 bytes), round words [R] (padded to 16 bytes), segments [nseg].
-template <int PMAX>
-__host__ __device__ inline int lt_smem_words(int R, int nseg) {
-    return ((R * PMAX + 3) & ~3) + 2 * ((R + 1) & ~1) + 4 * nseg;
+template <int PMAX, int NI, int K>
+__device__ __forceinline__ void in_fwd(const RegState<PMAX, NI> &S, uint32_t (&arr)[NI]) {
+#pragma unroll
+    for (int i = 0; i < NI; ++i) arr[i] = K > 0 ? S.rf[i][K > 0 ? K - 1 : 0] : 0u;
 }
-
-template <int PMAX, int K>
-__device__ __forceinline__ uint32_t in_fwd(const RegState<PMAX> &S) { return K > 0 ? S.rf[K > 0 ? K - 1 : 0] : 0u; }
-template <int PMAX, int K>
-__device__ __forceinline__ uint32_t in_bwd(const RegState<PMAX> &S) {
-    return K < PMAX - 1 ? S.rb[K < PMAX - 1 ? K + 1 : 0] : 0u;
+template <int PMAX, int NI, int K>
+__device__ __forceinline__ void in_bwd(const RegState<PMAX, NI> &S, uint32_t (&arr)[NI]) {
+#pragma unroll
+    for (int i = 0; i < NI; ++i) arr[i] = K < PMAX - 1 ? S.rb[i][K < PMAX - 1 ? K + 1 : 0] : 0u;
 }
 
 // Pattern round bodies.  In the alternating patterns a device's input comes
@@ -84,129 +101,162 @@ __device__ __forceinline__ uint32_t in_bwd(const RegState<PMAX> &S) {
 // unchanged by the round; in all-F (all-B) rounds devices run from the last
 // (first) so each reads its input before the neighbour overwrites it.  MASKED
 // bodies run only the devices whose bit is set.
-template <int PMAX, bool OPS, bool MASKED, bool EVEN_FWD, int K = 0>
-__device__ __forceinline__ void round_alt(RegState<PMAX> &S, uint32_t mask, const int32_t *slice, int lane,
-                                          const EvalArgs &a, int64_t x, bool live) {
+template <int PMAX, int NI, bool OPS, bool MASKED, bool EVEN_FWD, int K = 0>
+__device__ __forceinline__ void round_alt(RegState<PMAX, NI> &S, uint32_t mask, const int32_t *slice,
+                                          const EvalArgs &a, const Lanes<NI> &L) {
     if constexpr (K < PMAX) {
         if (!MASKED || ((mask >> K) & 1u)) {
-            const uint32_t c = (uint32_t)slice[K * 32 + lane];
+            uint32_t arr[NI];
             constexpr bool fwd = ((K & 1) == 0) == EVEN_FWD;
-            if constexpr (fwd) reg_op<PMAX, OPS, true, K>(S, in_fwd<PMAX, K>(S), c, a, x, live);
-            else reg_op<PMAX, OPS, false, K>(S, in_bwd<PMAX, K>(S), c, a, x, live);
+            if constexpr (fwd) {
+                in_fwd<PMAX, NI, K>(S, arr);
+                reg_op<PMAX, NI, OPS, true, K>(S, arr, slice, a, L);
+            } else {
+                in_bwd<PMAX, NI, K>(S, arr);
+                reg_op<PMAX, NI, OPS, false, K>(S, arr, slice, a, L);
+            }
         }
-        round_alt<PMAX, OPS, MASKED, EVEN_FWD, K + 1>(S, mask, slice, lane, a, x, live);
+        round_alt<PMAX, NI, OPS, MASKED, EVEN_FWD, K + 1>(S, mask, slice, a, L);
     }
 }
 
-template <int PMAX, bool OPS, bool MASKED, int K = PMAX - 1>
-__device__ __forceinline__ void round_all_f(RegState<PMAX> &S, uint32_t mask, const int32_t *slice, int lane,
-                                            const EvalArgs &a, int64_t x, bool live) {
+template <int PMAX, int NI, bool OPS, bool MASKED, int K = PMAX - 1>
+__device__ __forceinline__ void round_all_f(RegState<PMAX, NI> &S, uint32_t mask, const int32_t *slice,
+                                            const EvalArgs &a, const Lanes<NI> &L) {
     if constexpr (K >= 0) {
-        if (!MASKED || ((mask >> K) & 1u))
-            reg_op<PMAX, OPS, true, K>(S, in_fwd<PMAX, K>(S), (uint32_t)slice[K * 32 + lane], a, x, live);
-        round_all_f<PMAX, OPS, MASKED, K - 1>(S, mask, slice, lane, a, x, live);
+        if (!MASKED || ((mask >> K) & 1u)) {
+            uint32_t arr[NI];
+            in_fwd<PMAX, NI, K>(S, arr);
+            reg_op<PMAX, NI, OPS, true, K>(S, arr, slice, a, L);
+        }
+        round_all_f<PMAX, NI, OPS, MASKED, K - 1>(S, mask, slice, a, L);
     }
 }
 
-template <int PMAX, bool OPS, bool MASKED, int K = 0>
-__device__ __forceinline__ void round_all_b(RegState<PMAX> &S, uint32_t mask, const int32_t *slice, int lane,
-                                            const EvalArgs &a, int64_t x, bool live) {
+template <int PMAX, int NI, bool OPS, bool MASKED, int K = 0>
+__device__ __forceinline__ void round_all_b(RegState<PMAX, NI> &S, uint32_t mask, const int32_t *slice,
+                                            const EvalArgs &a, const Lanes<NI> &L) {
     if constexpr (K < PMAX) {
-        if (!MASKED || ((mask >> K) & 1u))
-            reg_op<PMAX, OPS, false, K>(S, in_bwd<PMAX, K>(S), (uint32_t)slice[K * 32 + lane], a, x, live);
-        round_all_b<PMAX, OPS, MASKED, K + 1>(S, mask, slice, lane, a, x, live);
+        if (!MASKED || ((mask >> K) & 1u)) {
+            uint32_t arr[NI];
+            in_bwd<PMAX, NI, K>(S, arr);
+            reg_op<PMAX, NI, OPS, false, K>(S, arr, slice, a, L);
+        }
+        round_all_b<PMAX, NI, OPS, MASKED, K + 1>(S, mask, slice, a, L);
     }
 }
 
 // Any other round: inputs are read as of the start of the round, then each
 // device runs its op (or none) by its 2-bit kind.
-template <int PMAX, bool OPS>
-__device__ __forceinline__ void round_generic(RegState<PMAX> &S, uint32_t kinds, const int32_t *slice, int lane,
-                                              const EvalArgs &a, int64_t x, bool live) {
-    uint32_t inF[PMAX], inB[PMAX];
+template <int PMAX, int NI, bool OPS>
+__device__ __forceinline__ void round_generic(RegState<PMAX, NI> &S, uint32_t kinds, const int32_t *slice,
+                                              const EvalArgs &a, const Lanes<NI> &L) {
+    uint32_t inF[PMAX][NI], inB[PMAX][NI];
 #pragma unroll
-    for (int k = 0; k < PMAX; ++k) {
-        inF[k] = k > 0 ? S.rf[k > 0 ? k - 1 : 0] : 0u;
-        inB[k] = k < PMAX - 1 ? S.rb[k < PMAX - 1 ? k + 1 : 0] : 0u;
-    }
+    for (int k = 0; k < PMAX; ++k)
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            inF[k][i] = k > 0 ? S.rf[i][k > 0 ? k - 1 : 0] : 0u;
+            inB[k][i] = k < PMAX - 1 ? S.rb[i][k < PMAX - 1 ? k + 1 : 0] : 0u;
+        }
     [&]<int... K>(std::integer_sequence<int, K...>) {
         ([&] {
             const uint32_t kind = (kinds >> (2 * K)) & 3u;
-            const uint32_t c = (uint32_t)slice[K * 32 + lane];
-            if (kind == kFwd) reg_op<PMAX, OPS, true, K>(S, inF[K], c, a, x, live);
-            else if (kind == kBwd) reg_op<PMAX, OPS, false, K>(S, inB[K], c, a, x, live);
+            if (kind == kFwd) reg_op<PMAX, NI, OPS, true, K>(S, inF[K], slice, a, L);
+            else if (kind == kBwd) reg_op<PMAX, NI, OPS, false, K>(S, inB[K], slice, a, L);
         }(), ...);
     }(std::make_integer_sequence<int, PMAX>{});
 }
 
-template <int PMAX, bool OPS>
-__device__ __forceinline__ void run_round(RegState<PMAX> &S, uint64_t w, const int32_t *slice, int lane,
-                                          const EvalArgs &a, int64_t x, bool live) {
+template <int PMAX, int NI, bool OPS>
+__device__ __forceinline__ void run_round(RegState<PMAX, NI> &S, uint64_t w, const int32_t *slice,
+                                          const EvalArgs &a, const Lanes<NI> &L) {
     const uint32_t m = rw_mask(w);
     switch (rw_pattern(w)) {
-        case kPatAltA: round_alt<PMAX, OPS, false, true>(S, m, slice, lane, a, x, live); break;
-        case kPatAltB: round_alt<PMAX, OPS, false, false>(S, m, slice, lane, a, x, live); break;
-        case kPatAllF: round_all_f<PMAX, OPS, false>(S, m, slice, lane, a, x, live); break;
-        case kPatAllB: round_all_b<PMAX, OPS, false>(S, m, slice, lane, a, x, live); break;
-        case kPatMasked + kPatAltA: round_alt<PMAX, OPS, true, true>(S, m, slice, lane, a, x, live); break;
-        case kPatMasked + kPatAltB: round_alt<PMAX, OPS, true, false>(S, m, slice, lane, a, x, live); break;
-        case kPatMasked + kPatAllF: round_all_f<PMAX, OPS, true>(S, m, slice, lane, a, x, live); break;
-        case kPatMasked + kPatAllB: round_all_b<PMAX, OPS, true>(S, m, slice, lane, a, x, live); break;
-        default: round_generic<PMAX, OPS>(S, rw_kinds(w), slice, lane, a, x, live); break;
+        case kPatAltA: round_alt<PMAX, NI, OPS, false, true>(S, m, slice, a, L); break;
+        case kPatAltB: round_alt<PMAX, NI, OPS, false, false>(S, m, slice, a, L); break;
+        case kPatAllF: round_all_f<PMAX, NI, OPS, false>(S, m, slice, a, L); break;
+        case kPatAllB: round_all_b<PMAX, NI, OPS, false>(S, m, slice, a, L); break;
+        case kPatMasked + kPatAltA: round_alt<PMAX, NI, OPS, true, true>(S, m, slice, a, L); break;
+        case kPatMasked + kPatAltB: round_alt<PMAX, NI, OPS, true, false>(S, m, slice, a, L); break;
+        case kPatMasked + kPatAllF: round_all_f<PMAX, NI, OPS, true>(S, m, slice, a, L); break;
+        case kPatMasked + kPatAllB: round_all_b<PMAX, NI, OPS, true>(S, m, slice, a, L); break;
+        default: round_generic<PMAX, NI, OPS>(S, rw_kinds(w), slice, a, L); break;
     }
 }
 
-// LT: the vector loader runs from the per-CTA offset table.  Dynamic shared
-// memory then holds the table, the round words and the segment list (so no
-// global load sits on the warmup / cooldown path), then one ring per warp.
+// The register evaluator.  A warp covers 32*NI instances (NI per thread).
+// LT: the vector loader runs from the per-CTA offset table (NI may be 2);
+// otherwise the loader computes addresses from the plan's descriptors (NI 1).
+// Dynamic shared memory holds, for LT, the loader table, the round words and
+// the segment list (so no global load sits on the warmup / cooldown path),
+// then one ring of round slices per warp.
 //
 // The kernel walks the plan's segments.  Alternating and all-F / all-B
 // segments are tight loops over static round bodies (two rounds per iteration
-// in the alternating case), so the instance's state stays in the same
+// in the alternating case), so the instances' state stays in the same
 // registers across iterations; warmup and cooldown rounds are dispatched one
-// at a time by their round word.  Copies run D = kAhead2 rounds ahead.
-template <int PMAX, bool VEC, bool OPS, bool LT>
+// at a time by their round word.  Copies run D = kAhead2 rounds ahead, one
+// cp.async group per round; a two-round step commits both rounds' groups and
+// then waits for both.
+template <int PMAX, int NI, bool VEC, bool OPS, bool LT>
 __global__ void __launch_bounds__(128) k_eval_reg(const EvalArgs a) {
-    using RG = Ring<PMAX>;
+    static_assert(NI == 1 || LT, "two instances per thread need the table loader");
+    using RG = Ring<PMAX, NI>;
     constexpr int D = RG::kAhead2;
     extern __shared__ __align__(16) int32_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
-    const int lt_words = LT ? lt_smem_words<PMAX>(a.R, a.nseg) : 0;
+    const int lt_words = LT ? a.ktab_words : 0;
     uint32_t *lt = reinterpret_cast<uint32_t *>(smem);
     const uint64_t *rws = a.rw;
     const uint4 *segs = a.seg;
     if constexpr (LT) {
+        // the block's copy of the precomputed tables, in flight while the
+        // comm values load below
+        for (int i = threadIdx.x; i < a.ktab_words / 4; i += blockDim.x)
+            cp_async16(smem_addr(smem + 4 * i), a.ktab + i, 16u);
+        cp_async_commit();
         const int tw = (a.R * PMAX + 3) & ~3;
-        uint64_t *rw_s = reinterpret_cast<uint64_t *>(smem + tw);
-        uint4 *seg_s = reinterpret_cast<uint4 *>(smem + tw + 2 * ((a.R + 1) & ~1));
-        stage_words(a.seg, seg_s, a.nseg);
-        stage_words(reinterpret_cast<const uint4 *>(a.rw), reinterpret_cast<uint4 *>(rw_s), (a.R + 1) / 2);
-        build_load_table<PMAX>(a, lt);
-        __syncthreads();
-        rws = rw_s;
-        segs = seg_s;
+        rws = reinterpret_cast<const uint64_t *>(smem + tw);
+        segs = reinterpret_cast<const uint4 *>(smem + tw + 2 * ((a.R + 1) & ~1));
     }
     int32_t *ring = smem + lt_words + warp * RG::kWords;
-    const int64_t inst0 = a.inst_begin + ((int64_t)blockIdx.x * nwarps + warp) * 32;
-    if (inst0 >= a.n) return;  // warp-uniform, after the block barrier
-    const int64_t x = inst0 + lane;
-    const bool live = x < a.n;
-
-    RegState<PMAX> S;
-    uint32_t negc = 0;
+    const int64_t inst0 = a.inst_begin + ((int64_t)blockIdx.x * nwarps + warp) * (32 * NI);
+    Lanes<NI> L;
+    L.lane = lane;
 #pragma unroll
-    for (int k = 0; k < PMAX; ++k) {
-        int c = 0;
-        if (a.comm && live && k < a.P - 1) c = a.comm[x * a.c_inst + (int64_t)k * a.c_bnd];
-        negc |= (uint32_t)c;
-        S.cF[k] = (uint32_t)c;
-        S.fr[k] = 0; S.rf[k] = 0; S.rb[k] = 0; S.busy[k] = 0; S.cnt[k] = 0;
+    for (int i = 0; i < NI; ++i) {
+        L.x[i] = inst0 + 32 * i + lane;
+        L.live[i] = L.x[i] < a.n;
     }
-    S.flag = 0;
 
-    // loader state
-    const int g = lane & 7;
+    RegState<PMAX, NI> S;
+    uint32_t negc[NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+        negc[i] = 0;
+        S.flag[i] = 0;
+#pragma unroll
+        for (int k = 0; k < PMAX; ++k) {
+            int c = 0;
+            if (a.comm && L.live[i] && k < a.P - 1) c = a.comm[L.x[i] * a.c_inst + (int64_t)k * a.c_bnd];
+            negc[i] |= (uint32_t)c;
+            S.cF[i][k] = (uint32_t)c;
+            S.fr[i][k] = 0; S.rf[i][k] = 0; S.rb[i][k] = 0; S.busy[i][k] = 0;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < PMAX; ++k) S.cnt[k] = 0;
+    if constexpr (LT) {
+        cp_async_wait<0>();
+        __syncthreads();
+    }
+    if (inst0 >= a.n) return;  // warp-uniform, after the block barrier
+
+    // loader state: lane copies 16 bytes (4 instances) at instance offset 4g
+    // of its row; a row of the warp's 32*NI instances takes 8*NI lanes
+    const int g = lane % (8 * NI);
     const int64_t x0 = inst0 + 4 * g;
     const int64_t left = a.n - x0;
     const uint32_t bytes_in = left <= 0 ? 0u : (left >= 4 ? 16u : (uint32_t)left * 4u);
@@ -216,7 +266,7 @@ __global__ void __launch_bounds__(128) k_eval_reg(const EvalArgs a) {
     auto issue = [&](int rl) {
         if (rl < R) {
             if constexpr (LT) {
-                load_round_lt<PMAX>(lt, rl, ring, fbase, bbase, bytes_in, lane);
+                load_round_lt<PMAX, NI>(lt, rl, ring, fbase, bbase, bytes_in, lane);
             } else {
                 LoadDesc<PMAX, VEC> ld;
                 fetch_load_desc<PMAX, VEC>(a, rl, lane, ld);
@@ -225,7 +275,7 @@ __global__ void __launch_bounds__(128) k_eval_reg(const EvalArgs a) {
         }
         cp_async_commit();
     };
-    auto slice = [&](int r) { return ring + (r % RG::kSlices) * (PMAX * 32); };
+    auto slice = [&](int r) { return ring + (r % RG::kSlices) * (PMAX * NI * 32); };
     // one round: its copies D ahead, wait for it, run `body`
     auto step1 = [&](int r, auto &&body) {
         issue(r + D);
@@ -244,10 +294,10 @@ __global__ void __launch_bounds__(128) k_eval_reg(const EvalArgs a) {
         body1(slice(r + 1));
         __syncwarp();
     };
-    auto altA = [&](const int32_t *sl) { round_alt<PMAX, OPS, false, true>(S, 0u, sl, lane, a, x, live); };
-    auto altB = [&](const int32_t *sl) { round_alt<PMAX, OPS, false, false>(S, 0u, sl, lane, a, x, live); };
-    auto allF = [&](const int32_t *sl) { round_all_f<PMAX, OPS, false>(S, 0u, sl, lane, a, x, live); };
-    auto allB = [&](const int32_t *sl) { round_all_b<PMAX, OPS, false>(S, 0u, sl, lane, a, x, live); };
+    auto altA = [&](const int32_t *sl) { round_alt<PMAX, NI, OPS, false, true>(S, 0u, sl, a, L); };
+    auto altB = [&](const int32_t *sl) { round_alt<PMAX, NI, OPS, false, false>(S, 0u, sl, a, L); };
+    auto allF = [&](const int32_t *sl) { round_all_f<PMAX, NI, OPS, false>(S, 0u, sl, a, L); };
+    auto allB = [&](const int32_t *sl) { round_all_b<PMAX, NI, OPS, false>(S, 0u, sl, a, L); };
 
 #pragma unroll 1
     for (int q = 0; q < D; ++q) issue(q);
@@ -277,64 +327,75 @@ __global__ void __launch_bounds__(128) k_eval_reg(const EvalArgs a) {
                 break;
             default: {
                 const uint64_t w = rws[r];
-                step1(r, [&](const int32_t *sl) { run_round<PMAX, OPS>(S, w, sl, lane, a, x, live); });
+                step1(r, [&](const int32_t *sl) { run_round<PMAX, NI, OPS>(S, w, sl, a, L); });
                 break;
             }
         }
     }
     cp_async_wait<0>();
-    if (live) write_results_u<PMAX>(a, x, S.fr, S.busy, S.flag, (negc >> 31) != 0);
+#pragma unroll
+    for (int i = 0; i < NI; ++i)
+        if (L.live[i]) write_results_u<PMAX>(a, L.x[i], S.fr[i], S.busy[i], S.flag[i], (negc[i] >> 31) != 0);
 }
 
-template <int PMAX, bool VEC, bool OPS, bool LT>
+template <int PMAX, int NI, bool VEC, bool OPS, bool LT>
 static int launch_reg_t(const EvalArgs &a, int64_t begin, int64_t end, cudaStream_t st) {
-    constexpr int kWarps = 4;
+    // two-instance warps hold twice the ring: use two warps per block so the
+    // blocks still spread evenly over the SMs
+    constexpr int kWarps = NI == 1 ? 4 : 2;
     if (end <= begin) return PP_OK;
-    const size_t lt_bytes = LT ? (size_t)lt_smem_words<PMAX>(a.R, a.nseg) * sizeof(uint32_t) : 0;
-    const size_t smem = lt_bytes + (size_t)kWarps * Ring<PMAX>::kWords * sizeof(int32_t);
+    const size_t lt_bytes = LT ? (size_t)a.ktab_words * sizeof(uint32_t) : 0;
+    const size_t smem = lt_bytes + (size_t)kWarps * Ring<PMAX, NI>::kWords * sizeof(int32_t);
     int dev = 0;
     PPS_CUDA_TRY(cudaGetDevice(&dev));
     static bool attr_set[64] = {};
     if (dev < 64 && !attr_set[dev]) {
-        PPS_CUDA_TRY(cudaFuncSetAttribute(k_eval_reg<PMAX, VEC, OPS, LT>,
+        PPS_CUDA_TRY(cudaFuncSetAttribute(k_eval_reg<PMAX, NI, VEC, OPS, LT>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024));
         attr_set[dev] = true;
     }
-    const int64_t warps = (end - begin + 31) / 32;
+    const int64_t warps = (end - begin + 32 * NI - 1) / (32 * NI);
     const int64_t blocks = (warps + kWarps - 1) / kWarps;
     if (blocks > 0x7FFFFFFF) return PP_ERR_SIZE;
     EvalArgs b = a;
     b.inst_begin = begin;
     b.n = end;
-    k_eval_reg<PMAX, VEC, OPS, LT><<<(unsigned)blocks, kWarps * 32, smem, st>>>(b);
+    k_eval_reg<PMAX, NI, VEC, OPS, LT><<<(unsigned)blocks, kWarps * 32, smem, st>>>(b);
     PPS_CUDA_TRY(cudaGetLastError());
     return PP_OK;
 }
 
 template <int PMAX, bool OPS>
 static int launch_reg_o(const EvalArgs &a, bool vec, bool lt, cudaStream_t st) {
-    if (lt) return launch_reg_t<PMAX, true, OPS, true>(a, 0, a.n, st);
-    if (vec) return launch_reg_t<PMAX, true, OPS, false>(a, 0, a.n, st);
-    return launch_reg_t<PMAX, false, OPS, false>(a, 0, a.n, st);
+    if (lt) return launch_reg_t<PMAX, kRegNI, true, OPS, true>(a, 0, a.n, st);
+    if (vec) return launch_reg_t<PMAX, 1, true, OPS, false>(a, 0, a.n, st);
+    return launch_reg_t<PMAX, 1, false, OPS, false>(a, 0, a.n, st);
 }
 
-// Largest loader table kept in shared memory (words); bigger plans use the
-// in-loop address computation.
+// Largest per-CTA table area kept in shared memory (words); bigger plans use
+// the in-loop address computation.
 constexpr int kMaxLtWords = 8192;
 
 template <int PMAX>
-static int launch_reg_p(const EvalArgs &a, bool vec, bool ops, cudaStream_t st) {
+static int launch_reg_p(pp_plan *plan, EvalArgs &a, bool vec, bool ops, cudaStream_t st) {
     // the table path needs 16-byte aligned rows and offsets below 2^30
-    const bool lt = vec && (int64_t)lt_smem_words<PMAX>(a.R, a.nseg) <= kMaxLtWords &&
+    const bool lt = vec && ktab_words(a.R, PMAX, a.nseg) <= kMaxLtWords &&
                     (int64_t)(a.S - 1) * a.s_stage + (int64_t)(a.M - 1) * a.s_mb < ((int64_t)1 << 30);
+    if (lt) {
+        const pp_ktab *t = nullptr;
+        const int rc = kernel_tables(plan, a.s_stage, a.s_mb, st, &t);
+        if (rc) return rc;
+        a.ktab = t->d;
+        a.ktab_words = t->words;
+    }
     return ops ? launch_reg_o<PMAX, true>(a, vec, lt, st) : launch_reg_o<PMAX, false>(a, vec, lt, st);
 }
 
-int launch_eval_reg(const pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st) {
+int launch_eval_reg(pp_plan *plan, EvalArgs &a, bool vec, bool ops, cudaStream_t st) {
     switch (plan->pmax) {
-        case 4: return launch_reg_p<4>(a, vec, ops, st);
-        case 8: return launch_reg_p<8>(a, vec, ops, st);
-        case 16: return launch_reg_p<16>(a, vec, ops, st);
+        case 4: return launch_reg_p<4>(plan, a, vec, ops, st);
+        case 8: return launch_reg_p<8>(plan, a, vec, ops, st);
+        case 16: return launch_reg_p<16>(plan, a, vec, ops, st);
         default: return PP_ERR_INTERNAL;
     }
 }
@@ -357,7 +418,7 @@ extern "C" int pp_sched_eval(pp_policy_t policy, int P, int M, int v, const int3
         comm_stride_bnd < 0)
         return PP_ERR_ARG;
     if ((op_start || op_end) && (op_stride_inst < 0 || op_stride_op < 0)) return PP_ERR_ARG;
-    const pp_plan *plan = nullptr;
+    pp_plan *plan = nullptr;
     rc = cached_plan((int)policy, P, M, v, stream, &plan);
     if (rc) return rc;
     if (peak)
@@ -366,6 +427,7 @@ extern "C" int pp_sched_eval(pp_policy_t policy, int P, int M, int v, const int3
     EvalArgs a;
     a.desc = plan->d_desc; a.desc2 = plan->d_desc2; a.rw = plan->d_rw;
     a.seg = plan->d_seg; a.nseg = plan->nseg;
+    a.ktab = nullptr; a.ktab_words = 0;
     a.R = plan->R; a.P = P; a.M = M; a.v = v; a.S = plan->S; a.O = plan->O; a.nslots = plan->nslots;
     a.cost_f = cost_f; a.cost_b = cost_b;
     a.s_inst = stride_inst; a.s_stage = stride_stage; a.s_mb = stride_mb;

@@ -2,6 +2,9 @@
 #pragma once
 
 #include <cstdint>
+#include <deque>
+#include <mutex>
+
 #include <cuda_runtime.h>
 
 #include "ppsched.h"
@@ -66,6 +69,15 @@ inline int pmax_for(int P) { return P <= 4 ? 4 : (P <= 8 ? 8 : 16); }
 
 }  // namespace pps
 
+// Kernel tables of the register evaluator for one (stride_stage, stride_mb)
+// pair: loader table, round words and segments, contiguous, ready to be copied
+// into shared memory.
+struct pp_ktab {
+    int64_t s_stage, s_mb;
+    uint4 *d;     // words / 4 uint4
+    int words;    // 32-bit words
+};
+
 // The plan object (opaque to callers).
 struct pp_plan {
     int policy, P, M, v, S, O;
@@ -81,6 +93,8 @@ struct pp_plan {
     uint64_t *d_rw;     // [R] per-round kind words and patterns
     uint4 *d_seg;       // [nseg] segments (register evaluator)
     int nseg;
+    std::mutex ktab_mu; // guards ktabs
+    std::deque<pp_ktab> ktabs;   // per stride pair, built on first use (stable addresses)
     int32_t *d_peak;    // [P]
     int32_t h_peak[PP_MAX_P];
 };
@@ -92,10 +106,21 @@ int cuda_status(cudaError_t e);
 
 // Plan cache used by the evaluation entry points: returns the plan of the
 // shape on the current device, building it on first use.
-int cached_plan(int policy, int P, int M, int v, cudaStream_t stream, const pp_plan **out);
+int cached_plan(int policy, int P, int M, int v, cudaStream_t stream, pp_plan **out);
 
 // Argument validation shared by plan construction and evaluation.
 int check_shape(int policy, int P, int M, int v);
+
+// Shared-memory words of the register evaluator's per-block tables: loader
+// table [R][pmax] (padded to 16 bytes), round words [R] (padded to 16 bytes),
+// segments [nseg].
+__host__ __device__ inline int ktab_words(int R, int pmax, int nseg) {
+    return ((R * pmax + 3) & ~3) + 2 * ((R + 1) & ~1) + 4 * nseg;
+}
+
+// The kernel tables of `plan` for the given strides, built (allocating device
+// memory and synchronizing `stream`) the first time a stride pair is seen.
+int kernel_tables(pp_plan *plan, int64_t s_stage, int64_t s_mb, cudaStream_t stream, const pp_ktab **out);
 
 }  // namespace pps
 

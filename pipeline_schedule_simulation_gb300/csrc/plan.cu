@@ -269,6 +269,39 @@ __global__ void k_slots(const uint32_t *desc, int R, int P, int M, int v, int pm
     info[3] = nmax;
 }
 
+// Fill the register evaluator's tables for one stride pair: loader table
+// entries (element offset of the op's cost row, shifted left by one, bit 0 set
+// for a backward op; all ones for an idle slot), then the round words, then
+// the segments.
+__global__ void k_ktab(const uint32_t *desc, const uint64_t *rw, const uint4 *seg, int R, int P, int pmax,
+                       int nseg, int s_stage, int s_mb, uint32_t *out) {
+    const int tw = (R * pmax + 3) & ~3;
+    const int rw_words = 2 * ((R + 1) & ~1);
+    const int total = tw + rw_words + 4 * nseg;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
+        uint32_t v = 0;
+        if (e < R * pmax) {
+            const uint32_t d = desc[e];
+            const uint32_t kind = desc_kind(d);
+            v = 0xFFFFFFFFu;
+            if (kind != kIdle) {
+                const int st = (int)desc_chunk(d) * P + (e % pmax);
+                const uint32_t off = (uint32_t)(st * s_stage + (int)desc_mb(d) * s_mb);
+                v = (off << 1) | (kind == kBwd ? 1u : 0u);
+            }
+        } else if (e >= tw && e < tw + rw_words) {
+            const int q = e - tw;
+            if (q / 2 < R) v = (q & 1) ? (uint32_t)(rw[q / 2] >> 32) : (uint32_t)rw[q / 2];
+        } else if (e >= tw + rw_words) {
+            const int q = e - tw - rw_words;
+            const uint4 sg = seg[q / 4];
+            const int c = q % 4;
+            v = c == 0 ? sg.x : (c == 1 ? sg.y : (c == 2 ? sg.z : sg.w));
+        }
+        out[e] = v;
+    }
+}
+
 struct DevBuf {
     void *p = nullptr;
     ~DevBuf() { if (p) cudaFree(p); }
@@ -372,12 +405,35 @@ static int build_plan(int policy, int P, int M, int v, cudaStream_t st, pp_plan 
     return PP_OK;
 }
 
+int kernel_tables(pp_plan *plan, int64_t s_stage, int64_t s_mb, cudaStream_t stream, const pp_ktab **out) {
+    std::lock_guard<std::mutex> lk(plan->ktab_mu);
+    for (const pp_ktab &t : plan->ktabs)
+        if (t.s_stage == s_stage && t.s_mb == s_mb) { *out = &t; return PP_OK; }
+    pp_ktab t;
+    t.s_stage = s_stage;
+    t.s_mb = s_mb;
+    t.words = ktab_words(plan->R, plan->pmax, plan->nseg);
+    PPS_CUDA_TRY(cudaMalloc(&t.d, (size_t)t.words * sizeof(uint32_t)));
+    const int blocks = (t.words + 255) / 256;
+    k_ktab<<<blocks, 256, 0, stream>>>(plan->d_desc, plan->d_rw, plan->d_seg, plan->R, plan->P, plan->pmax,
+                                       plan->nseg, (int)s_stage, (int)s_mb, reinterpret_cast<uint32_t *>(t.d));
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) {
+        cudaFree(t.d);
+        return cuda_status(e);
+    }
+    plan->ktabs.push_back(t);
+    *out = &plan->ktabs.back();
+    return PP_OK;
+}
+
 namespace {
 std::mutex g_cache_mu;
 std::map<std::tuple<int, int, int, int, int>, pp_plan *> g_cache;
 }  // namespace
 
-int cached_plan(int policy, int P, int M, int v, cudaStream_t stream, const pp_plan **out) {
+int cached_plan(int policy, int P, int M, int v, cudaStream_t stream, pp_plan **out) {
     int dev = 0;
     PPS_CUDA_TRY(cudaGetDevice(&dev));
     auto key = std::make_tuple(dev, policy, P, M, v);
@@ -434,6 +490,7 @@ void pp_sched_plan_destroy(pp_plan_t *p) {
     if (p->d_desc2) cudaFree(p->d_desc2);
     cudaFree(p->d_rw);
     cudaFree(p->d_seg);
+    for (pp_ktab &t : p->ktabs) cudaFree(t.d);
     cudaFree(p->d_peak);
     delete p;
 }

@@ -248,7 +248,7 @@ extern "C" int pp_sched_partition_search(const int32_t *layer_tf, const int32_t 
     if (P > PP_MAX_P || L > kMaxL || M > PP_MAX_MV || n_cand >= (int64_t)1 << 32) return PP_ERR_SIZE;
     const uint64_t ncomb = host_binom(L - 1, P - 1);
     if (ncomb == ~0ull || ncomb == 0) return PP_ERR_SIZE;
-    const pp_plan *plan = nullptr;
+    pp_plan *plan = nullptr;
     int rc = cached_plan(PP_1F1B, P, M, 1, stream, &plan);
     if (rc) return rc;
     if (!plan->reg_ok) return PP_ERR_INTERNAL;
