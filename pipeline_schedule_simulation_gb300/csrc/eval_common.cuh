@@ -215,6 +215,50 @@ __device__ __forceinline__ void write_results_u(const EvalArgs &a, int64_t x, co
     }
 }
 
+// Warp-cooperative version of write_results_u for the warp's 32 instances
+// starting at x0 (this lane's instance is x0 + lane): the [n][P] idle block of
+// the warp is contiguous, so it is staged through `scratch` (32*P words of the
+// warp's own shared memory, free at this point) and written with consecutive
+// lanes on consecutive words.  Called by all 32 lanes.
+template <int PMAX>
+__device__ __forceinline__ void write_results_warp(const EvalArgs &a, int64_t x0, int lane,
+                                                   const uint32_t (&fr)[PMAX], const uint32_t (&busy)[PMAX],
+                                                   uint32_t flag, bool neg_comm, int32_t *scratch) {
+    const int64_t x = x0 + lane;
+    const bool live = x < a.n;
+    uint32_t mk = 0;
+#pragma unroll
+    for (int k = 0; k < PMAX; ++k) mk = max(mk, fr[k]);
+    flag |= mk;
+    int64_t num = 0;
+#pragma unroll
+    for (int k = 0; k < PMAX; ++k) {
+        if (k < a.P) {
+            const int idle = (int)(mk - busy[k]);
+            num += idle;
+            scratch[lane * a.P + k] = idle;
+        }
+    }
+    if (live) {
+        if (a.makespan) a.makespan[x] = (int)mk;
+        if (a.bub_num) a.bub_num[x] = num;
+        if (a.bub_den) a.bub_den[x] = (int64_t)a.P * (int)mk;
+        if (a.status) {
+            int8_t st = PP_ST_OK;
+            if (neg_comm) st = PP_ST_NEG_COST;
+            else if (flag >> 31) st = any_negative_cost(a, x) ? PP_ST_NEG_COST : PP_ST_OVERFLOW;
+            a.status[x] = st;
+        }
+    }
+    __syncwarp();
+    if (a.idle) {
+        const int64_t valid = (a.n - x0 < 32 ? a.n - x0 : 32) * a.P;
+        int32_t *dst = a.idle + x0 * a.P;
+        for (int w = lane; w < valid; w += 32) dst[w] = scratch[w];
+    }
+    __syncwarp();
+}
+
 // Load the round's descriptors (identical for every lane of the warp).
 template <int PMAX>
 __device__ __forceinline__ void load_desc(const uint32_t *row, uint32_t (&d)[PMAX]) {

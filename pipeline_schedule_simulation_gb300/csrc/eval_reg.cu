@@ -333,9 +333,11 @@ __global__ void __launch_bounds__(128) k_eval_reg(const EvalArgs a) {
         }
     }
     cp_async_wait<0>();
+    __syncwarp();  // the ring is free: stage the idle block through it
 #pragma unroll
     for (int i = 0; i < NI; ++i)
-        if (L.live[i]) write_results_u<PMAX>(a, L.x[i], S.fr[i], S.busy[i], S.flag[i], (negc[i] >> 31) != 0);
+        write_results_warp<PMAX>(a, inst0 + 32 * i, lane, S.fr[i], S.busy[i], S.flag[i], (negc[i] >> 31) != 0,
+                                 ring);
 }
 
 template <int PMAX, int NI, bool VEC, bool OPS, bool LT>
