@@ -44,6 +44,39 @@ def algorithmic_bytes(n, P_=P, M_=M):
     return costs + comm + outs
 
 
+KERNEL_SOURCES = ("pipeline_schedule_simulation_gb300/csrc/eval_reg.cu",
+                  "pipeline_schedule_simulation_gb300/csrc/eval_common.cuh",
+                  "pipeline_schedule_simulation_gb300/csrc/internal.cuh")
+PROFILE = os.path.join(ROOT, "profiles", "eval_reg_1f1b_P8_M64_n65536.md")
+
+
+def kernel_source_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic():
+    """DRAM bytes (read + write) per launch of the evaluator from the committed
+    ncu summary, or None when the kernel sources changed since that capture."""
+    try:
+        fields = {}
+        with open(PROFILE) as f:
+            for line in f:
+                line = line.strip().lstrip("-* ")
+                if line.startswith(("traffic_bytes_per_launch:", "kernel_source_sha256:")):
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip().strip("` ")
+        if fields.get("kernel_source_sha256") != kernel_source_sha():
+            return None
+        return int(fields["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -189,7 +222,7 @@ def reference_arm(args):
     if rank != 0:
         return 0
     import pipeline_schedule_simulation_gb300.workloads as W
-    batch = W.config3(n=args.n)
+    batch = W.hetero_1f1b(n=args.n)
     threads = os.cpu_count() or 1
     per_step = None
     times = []
@@ -235,7 +268,7 @@ def main():
         if world > 1:
             dist.barrier()
 
-    batch = W.config3(n=args.n, seed=3 + rank)
+    batch = W.hetero_1f1b(n=args.n, seed=3 + rank)
     n = batch.n
     dev = lambda a: torch.from_numpy(a).cuda()  # noqa: E731
     cf, cb, cm = dev(batch.cost_f), dev(batch.cost_b), dev(batch.comm)
@@ -328,9 +361,9 @@ def main():
                        "l2": f"inputs {2 * P * M * n * 4 / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB, no flush",
                        "parallelism": f"instance-sharded x{world}"},
             "gpu_launches": K,
-            "roofline": {"bound": "hbm", "kernel": "k_eval_reg<8,true,false>", "achieved": achieved,
+            "roofline": {"bound": "hbm", "kernel": "k_eval_reg<8,1,true,false,true>", "achieved": achieved,
                          "peak": peak_gbs, "unit": "GB/s", "frac": achieved / peak_gbs,
-                         "peak_source": peak_src, "traffic": None,
+                         "peak_source": peak_src, "traffic": profiled_traffic(),
                          "algorithmic_bytes_per_launch": abytes, "avg_launch_us": kavg * 1e6},
             "instances_per_s": world * n * K / elapsed,
             "clocks": sampler.summary(),
@@ -364,7 +397,7 @@ def secondary(B, W, torch, stream):
         return a.elapsed_time(b) / 1e3 / reps
 
     # per-op start/end stored (instance-minor op layout)
-    b3 = W.config3(n=N_INST)
+    b3 = W.hetero_1f1b(n=N_INST)
     cf, cb, cm = (torch.from_numpy(x).cuda() for x in (b3.cost_f, b3.cost_b, b3.comm))
     O = 2 * M
     ops_out = {"op_start": torch.empty((P, O, N_INST), dtype=torch.int32, device="cuda"),
@@ -374,13 +407,13 @@ def secondary(B, W, torch, stream):
     out["1f1b_P8_M64_with_op_times"] = {"op_times_per_s": 2 * P * M * N_INST / t, "ms": t * 1e3}
     del ops_out, cf, cb, cm
     for v in (2, 4):
-        il, base = W.config4(v)
+        il, base = W.interleaved_vs_1f1b(v)
         for tag, bt in (("interleaved", il), ("1f1b_equal_work", base)):
             f, g, c = (torch.from_numpy(x).cuda() for x in (bt.cost_f, bt.cost_b, bt.comm))
             t = timed(lambda: B.evaluate(bt.policy, bt.P, bt.M, bt.v, f, g, bt.strides, bt.n, comm=c,
                                          comm_strides=bt.comm_strides, stream=stream), 20)
             out[f"{tag}_P8_v{v}_M128_n16384"] = {"op_times_per_s": bt.op_times / t, "ms": t * 1e3}
-    p = W.config5()
+    p = W.layer_split()
     lt, lb, la = (torch.from_numpy(x).cuda() for x in (p.layer_tf, p.layer_tb, p.layer_act))
     res = {}
     t = timed(lambda: res.update(B.partition_search(lt, lb, la, p.P, p.M, p.comm, p.cap, p.seed, 0,

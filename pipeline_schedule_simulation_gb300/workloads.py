@@ -55,7 +55,7 @@ def uniform_batch(policy, P, M, v, tf, tb, comm):
     return Batch(policy, P, M, v, n, tf, tb, (1, 0, 0), cm, (1, 0))
 
 
-def config1():
+def worked_examples():
     """Single instances: P=4, M=8, t_f=1, t_b=2, comm 0 (GPipe and 1F1B), and the
     two-stage, four-microbatch worked case with t_f = t_b = 1."""
     out = []
@@ -65,7 +65,7 @@ def config1():
     return out
 
 
-def config2_shapes():
+def sweep_shapes():
     """The closed-form sweep's shapes: P in 2..16 x M in 1..128 for GPipe and 1F1B,
     interleaved v=2 where P divides M."""
     shapes = []
@@ -78,7 +78,7 @@ def config2_shapes():
     return shapes
 
 
-def config2_batch(policy, P, M, v):
+def sweep_batch(policy, P, M, v):
     """All 16 combinations of t_f in {1..4}, t_b in {t_f, 2 t_f}, comm in {0, 1}
     for one shape, one instance each."""
     tf, tb, cm = [], [], []
@@ -89,7 +89,7 @@ def config2_batch(policy, P, M, v):
     return uniform_batch(policy, P, M, v, tf, tb, cm)
 
 
-def config3(n=65536, seed=3, P=8, M=64):
+def hetero_1f1b(n=65536, seed=3, P=8, M=64):
     """Heterogeneous 1F1B batch: per (instance, stage, microbatch) t_f ~ U[80,120],
     t_b ~ U[160,240]; comm ~ U[2,8] per (instance, boundary)."""
     rng = _rng(seed)
@@ -100,7 +100,7 @@ def config3(n=65536, seed=3, P=8, M=64):
                  cm.reshape(-1), (1, n), meta={"workload": f"1f1b_hetero_P{P}_M{M}_n{n}"})
 
 
-def config4(v, n=16384, seed=4, P=8, M=128):
+def interleaved_vs_1f1b(v, n=16384, seed=4, P=8, M=128):
     """Interleaved batch: per (instance, virtual stage) t_f ~ U[40,60],
     t_b = 2 t_f + U[-5,5], comm = 3, costs broadcast over microbatches
     (stride_mb = 0).  Also returns the 1F1B batch with the same total work per
@@ -133,7 +133,7 @@ class SearchProblem:
     n_cand: int
 
 
-def config5(seed=5, L=80, P=8, M=128, n_cand=1 << 20):
+def layer_split(seed=5, L=80, P=8, M=128, n_cand=1 << 20):
     """80-layer model: per-layer t_f = u ~ U[90,110] ticks, the embedding layer
     (layer 0) floor(1.5 u), the output projection (layer L-1) 3u, t_b = 2 t_f;
     activation bytes ~ U[200,300] * 10^6; cap 80 * 10^9 bytes; comm 0."""

@@ -16,12 +16,12 @@ def B():
     return binding
 
 
-def test_config1_every_op(orc, B):
-    for batch in W.config1():
+def test_worked_examples_every_op(orc, B):
+    for batch in W.worked_examples():
         g = run_gpu(batch, op_times=True)
         r = run_oracle(orc, batch, op_times=True)
         assert_same(g, r, op_times=True)
-    # the worked 2x4 tables end in 10 units; config 1 in 33 with bubble 36/132
+    # the worked 2x4 tables end in 10 units; P=4 M=8 t_f=1 t_b=2 in 33 with bubble 36/132
     g = run_gpu(W.uniform_batch(W.ONEF1B, 4, 8, 1, [1], [2], [0]))
     assert g["makespan"][0] == 33 and g["bub_num"][0] == 36 and g["bub_den"][0] == 132
     assert list(g["peak"]) == [4, 3, 2, 1]
@@ -95,12 +95,12 @@ def test_status_negative_and_overflow(orc, B):
     assert_same(g, r)
 
 
-def test_config2_closed_form_sweep(orc, B):
+def test_closed_form_sweep(orc, B):
     """Every shape of the closed-form sweep (GPipe, 1F1B, interleaved v=2):
     bit-exact against the oracle and equal to the pages' closed forms."""
     from fractions import Fraction
-    for policy, P, M, v in W.config2_shapes():
-        batch = W.config2_batch(policy, P, M, v)
+    for policy, P, M, v in W.sweep_shapes():
+        batch = W.sweep_batch(policy, P, M, v)
         g = run_gpu(batch)
         tf = batch.cost_f
         tb = batch.cost_b
@@ -120,11 +120,11 @@ def test_config2_closed_form_sweep(orc, B):
             assert_same(g, r)
 
 
-def test_config3_full_batch_sampled(orc, B):
+def test_hetero_1f1b_full_batch_sampled(orc, B):
     """65,536 heterogeneous 1F1B instances (P=8, M=64) in the benchmark's
     launch configuration; 600 sampled instances re-derived by the oracle, and
     invariants that hold for every instance."""
-    batch = W.config3()
+    batch = W.hetero_1f1b()
     g = run_gpu(batch)
     rng = np.random.default_rng(0)
     sel = np.unique(np.concatenate([rng.choice(batch.n, 600, replace=False), [0, 31, 32, batch.n - 1]]))
@@ -144,8 +144,8 @@ def test_config3_full_batch_sampled(orc, B):
 
 
 @pytest.mark.parametrize("v", [2, 4])
-def test_config4_interleaved_sampled(orc, B, v):
-    il, base = W.config4(v)
+def test_interleaved_batches_sampled(orc, B, v):
+    il, base = W.interleaved_vs_1f1b(v)
     for batch in (il, base):
         g = run_gpu(batch)
         sel = np.unique(np.random.default_rng(v).choice(batch.n, 96, replace=False))
@@ -156,7 +156,7 @@ def test_config4_interleaved_sampled(orc, B, v):
 
 def test_split_call_equals_whole(orc, B):
     """Sharding by instance range (one GPU, two calls) gives the same numbers."""
-    batch = W.config3(n=4096)
+    batch = W.hetero_1f1b(n=4096)
     whole = run_gpu(batch)
     import torch
     cf, cb, cm = to_dev(batch.cost_f), to_dev(batch.cost_b), to_dev(batch.comm)
@@ -173,7 +173,7 @@ def test_split_call_equals_whole(orc, B):
 
 def test_host_entry_end_to_end(B):
     import torch
-    batch = W.config3(n=1000)
+    batch = W.hetero_1f1b(n=1000)
     ref = run_gpu(batch)
     host, h2d, d2h = B.evaluate_host(batch.policy, 8, 64, 1, torch.from_numpy(batch.cost_f).pin_memory(),
                                      torch.from_numpy(batch.cost_b).pin_memory(), batch.strides, batch.n,

@@ -47,11 +47,11 @@ def test_nothing_feasible(B):
     assert (g["best_cuts"] == -1).all() and (g["all_makespan"] == -1).all()
 
 
-def test_config5_full(orc, B):
+def test_layer_split_full(orc, B):
     """1,048,576 candidates of the 80-layer model at P=8, M=128: the winner is
     the lowest-index minimum of all makespans; the oracle re-scores the winner,
     its stage split and 200 sampled candidates."""
-    p = W.config5()
+    p = W.layer_split()
     g = _gpu_search(B, p, 0, p.n_cand)
     mk = g["all_makespan"]
     feas = mk >= 0
@@ -71,7 +71,7 @@ def test_config5_full(orc, B):
 
 def test_split_ranges_reduce_to_whole(B):
     from pipeline_schedule_simulation_gb300.sharding import best_of
-    p = W.config5(n_cand=1 << 16)
+    p = W.layer_split(n_cand=1 << 16)
     whole = _gpu_search(B, p, 0, p.n_cand, all_mk=False)
     parts = []
     for lo, hi in ((0, 30000), (30000, 1 << 16)):

@@ -95,7 +95,7 @@ def test_lpnh_30_4_percent(orc):
         assert round(100 * num / den, 1) == 30.4
 
 
-def test_config1_values(orc):
+def test_p4_m8_tf1_tb2_values(orc):
     # P=4, M=8, t_f=1, t_b=2: (M+P-1)(t_f+t_b) = 33, busy 24 per stage, bubble 3/11.
     for policy in ("gpipe", "1f1b"):
         r = orc.evaluate(policy, 4, 8, 1, 1, 2, method=2)

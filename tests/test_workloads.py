@@ -4,9 +4,9 @@ import numpy as np
 import pipeline_schedule_simulation_gb300.workloads as W
 
 
-def test_config3_ranges_and_determinism():
-    a = W.config3(n=2048)
-    b = W.config3(n=2048)
+def test_hetero_1f1b_ranges_and_determinism():
+    a = W.hetero_1f1b(n=2048)
+    b = W.hetero_1f1b(n=2048)
     assert np.array_equal(a.cost_f, b.cost_f) and np.array_equal(a.comm, b.comm)
     assert a.cost_f.min() >= 80 and a.cost_f.max() <= 120
     assert a.cost_b.min() >= 160 and a.cost_b.max() <= 240
@@ -16,8 +16,8 @@ def test_config3_ranges_and_determinism():
     assert a.cost_f.max() == 120 and a.comm.max() == 8
 
 
-def test_config4_equal_work():
-    il, base = W.config4(2, n=512)
+def test_interleaved_equal_work():
+    il, base = W.interleaved_vs_1f1b(2, n=512)
     tf = il.cost_f.reshape(16, 512)
     assert tf.min() >= 40 and tf.max() <= 60
     tb = il.cost_b.reshape(16, 512)
@@ -26,8 +26,8 @@ def test_config4_equal_work():
     assert il.strides == (1, 512, 0)
 
 
-def test_config5_layers():
-    p = W.config5()
+def test_layer_split_layers():
+    p = W.layer_split()
     assert p.layer_tf.shape == (80,)
     assert 135 <= p.layer_tf[0] <= 165 and 270 <= p.layer_tf[79] <= 330
     assert np.all((p.layer_tf[1:79] >= 90) & (p.layer_tf[1:79] <= 110))
@@ -36,10 +36,10 @@ def test_config5_layers():
     assert p.cap == 80 * 10**9 and p.n_cand == 1 << 20
 
 
-def test_config2_shapes():
-    shapes = W.config2_shapes()
+def test_sweep_shapes():
+    shapes = W.sweep_shapes()
     assert len([s for s in shapes if s[0] == W.GPIPE]) == 15 * 128
     il = [s for s in shapes if s[0] == W.INTERLEAVED]
     assert all(M % P == 0 and v == 2 for _, P, M, v in il)
-    b = W.config2_batch(W.ONEF1B, 4, 8, 1)
+    b = W.sweep_batch(W.ONEF1B, 4, 8, 1)
     assert b.n == 16 and b.strides == (1, 0, 0)
