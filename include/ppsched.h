@@ -184,6 +184,32 @@ int pp_sched_partition_search(const int32_t *layer_tf, const int32_t *layer_tb,
                               int64_t *best_idx, int32_t *best_makespan, int32_t *best_cuts,
                               int32_t *all_makespan, cudaStream_t stream);
 
+/* pp_sched_eval for GPipe and 1F1B that allocates no device memory.  (This
+ * entry point has no counterpart on the pages; it exists for callers that
+ * cannot let a library call cudaMalloc, e.g. code whose device memory belongs to
+ * another allocator or that must not grow its device footprint while running.)
+ *
+ * Same arguments and results as pp_sched_eval with v = 1 and no per-op times.
+ * The schedule tables are built in one array of 4 MiB that the library reserves
+ * at file scope on every GPU that loads it and keeps until the process exits.
+ *   - The first call on a device looks up that array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - A call whose shape (policy, P, M) or stride pair differs from the previous
+ *     call on the device rebuilds the tables in the array and synchronizes
+ *     `stream`; a repeated shape and stride pair reuses them and just launches.
+ *   - Every call shares the array: calls that overlap on the GPU (other streams,
+ *     other threads) race; serialize them.
+ *   - Shapes whose tables do not fit in the array return PP_ERR_SIZE;
+ *     PP_INTERLEAVED_1F1B returns PP_ERR_ARG.
+ * Inputs, outputs and strides: as pp_sched_eval.  Errors: as pp_sched_eval. */
+int pp_sched_eval_noalloc(pp_policy_t policy, int P, int M,
+                          const int32_t *cost_f, const int32_t *cost_b,
+                          int64_t stride_inst, int64_t stride_stage, int64_t stride_mb,
+                          const int32_t *comm, int64_t comm_stride_inst, int64_t comm_stride_bnd,
+                          int64_t n_instances,
+                          int32_t *makespan, int32_t *idle, int64_t *bub_num, int64_t *bub_den,
+                          int32_t *peak, int8_t *status, cudaStream_t stream);
+
 /* Human-readable name of a PP_ERR_* return code. */
 const char *pp_sched_status_str(int code);
 

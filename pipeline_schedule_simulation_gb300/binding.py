@@ -21,7 +21,7 @@ ST_OK, ST_NEG_COST, ST_OVERFLOW = 0, 1, 2
 
 EXPORTS = ("pp_sched_plan", "pp_sched_plan_info", "pp_sched_plan_ops", "pp_sched_plan_destroy",
            "pp_sched_eval", "pp_sched_partition_search", "pp_sched_status_str",
-           "pp_sched_cache_clear")
+           "pp_sched_cache_clear", "pp_sched_eval_noalloc")
 
 
 class PPSchedError(RuntimeError):
@@ -54,6 +54,9 @@ def _load():
     lib.pp_sched_partition_search.restype = i32
     lib.pp_sched_status_str.argtypes = [i32]
     lib.pp_sched_status_str.restype = ctypes.c_char_p
+    lib.pp_sched_eval_noalloc.argtypes = [i32, i32, i32, vp, vp, i64, i64, i64, vp, i64, i64, i64,
+                                          vp, vp, vp, vp, vp, vp, vp]
+    lib.pp_sched_eval_noalloc.restype = i32
     lib.pp_sched_cache_clear.argtypes = []
     lib.pp_sched_cache_clear.restype = None
     return lib

@@ -309,6 +309,8 @@ __device__ __forceinline__ int wrap_add(int x, int y) {
 
 // Launchers (defined in eval_reg.cu / eval_slot.cu).
 int launch_eval_reg(pp_plan *plan, EvalArgs &a, bool vec, bool ops, cudaStream_t st);
+bool reg_table_path(int pmax, const EvalArgs &a, bool vec);
+int launch_eval_reg_tables(int pmax, const EvalArgs &a, bool vec, bool ops, cudaStream_t st);
 int launch_eval_slot(const pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st);
 
 }  // namespace pps

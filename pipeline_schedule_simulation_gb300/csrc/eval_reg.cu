@@ -402,6 +402,23 @@ int launch_eval_reg(pp_plan *plan, EvalArgs &a, bool vec, bool ops, cudaStream_t
     }
 }
 
+// Launch the register evaluator on tables the caller already built (the
+// entry point that allocates nothing): the table path when a.ktab is set.
+bool reg_table_path(int pmax, const EvalArgs &a, bool vec) {
+    return vec && ktab_words(a.R, pmax, a.nseg) <= kMaxLtWords &&
+           (int64_t)(a.S - 1) * a.s_stage + (int64_t)(a.M - 1) * a.s_mb < ((int64_t)1 << 30);
+}
+
+int launch_eval_reg_tables(int pmax, const EvalArgs &a, bool vec, bool ops, cudaStream_t st) {
+    const bool lt = a.ktab != nullptr;
+    switch (pmax) {
+        case 4: return ops ? launch_reg_o<4, true>(a, vec, lt, st) : launch_reg_o<4, false>(a, vec, lt, st);
+        case 8: return ops ? launch_reg_o<8, true>(a, vec, lt, st) : launch_reg_o<8, false>(a, vec, lt, st);
+        case 16: return ops ? launch_reg_o<16, true>(a, vec, lt, st) : launch_reg_o<16, false>(a, vec, lt, st);
+        default: return PP_ERR_INTERNAL;
+    }
+}
+
 }  // namespace pps
 
 extern "C" int pp_sched_eval(pp_policy_t policy, int P, int M, int v, const int32_t *cost_f,

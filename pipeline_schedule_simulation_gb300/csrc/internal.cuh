@@ -122,6 +122,27 @@ __host__ __device__ inline int ktab_words(int R, int pmax, int nseg) {
 // memory and synchronizing `stream`) the first time a stride pair is seen.
 int kernel_tables(pp_plan *plan, int64_t s_stage, int64_t s_mb, cudaStream_t stream, const pp_ktab **out);
 
+// A GPipe / 1F1B plan laid out in device memory the caller provides (used by
+// the entry point that allocates nothing).  Every table lives in `region`.
+struct ScratchPlan {
+    uint32_t *region;
+    int64_t region_words, used_words;
+    int policy, P, M, R, pmax, nseg;
+    uint32_t *desc;
+    uint64_t *rw;
+    uint4 *seg;
+    int32_t *peak;
+    uint32_t *ktab;  // kernel tables for one stride pair, or null
+    int ktab_words;
+};
+
+// Build the plan of (policy, P, M) for GPipe or 1F1B into `region` (device
+// words).  Synchronizes `stream` twice; PP_ERR_SIZE if the region is too small.
+int plan_into(int policy, int P, int M, uint32_t *region, int64_t region_words, cudaStream_t stream,
+              ScratchPlan *sp);
+// Append the kernel tables for one stride pair to the plan's region.
+int ktab_into(ScratchPlan *sp, int64_t s_stage, int64_t s_mb, cudaStream_t stream);
+
 }  // namespace pps
 
 #define PPS_CUDA_TRY(expr)                                  \

@@ -428,6 +428,72 @@ int kernel_tables(pp_plan *plan, int64_t s_stage, int64_t s_mb, cudaStream_t str
     return PP_OK;
 }
 
+int plan_into(int policy, int P, int M, uint32_t *region, int64_t region_words, cudaStream_t st,
+              ScratchPlan *sp) {
+    if (policy != PP_GPIPE && policy != PP_1F1B) return PP_ERR_ARG;
+    int rc = check_shape(policy, P, M, 1);
+    if (rc) return rc;
+    const int O = 2 * M, pmax = pmax_for(P);
+    const int64_t nops = (int64_t)P * O, npos = 2LL * P * M;
+    auto pad4 = [](int64_t w) { return (w + 3) & ~(int64_t)3; };
+    int64_t off = 0;
+    auto take = [&](int64_t w) {
+        uint32_t *p = region + off;
+        off += pad4(w);
+        return p;
+    };
+    if (pad4(8) + pad4(P) + 2 * pad4(nops) + pad4(npos) > region_words) return PP_ERR_SIZE;
+    int32_t *info = reinterpret_cast<int32_t *>(take(8));
+    int32_t *peak = reinterpret_cast<int32_t *>(take(P));
+    uint32_t *ops = take(nops);
+    int32_t *round = reinterpret_cast<int32_t *>(take(nops));
+    int32_t *pos = reinterpret_cast<int32_t *>(take(npos));
+    PPS_CUDA_TRY(cudaMemsetAsync(info, 0, 8 * sizeof(int32_t), st));
+    const int tpb = 256;
+    const unsigned nblk = (unsigned)((nops + tpb - 1) / tpb);
+    k_order<<<nblk, tpb, 0, st>>>(policy, P, M, 1, ops, pos);
+    k_rounds<<<1, 32, 0, st>>>(ops, pos, P, M, 1, round, info);
+    PPS_CUDA_TRY(cudaGetLastError());
+    int32_t h_info[8];
+    PPS_CUDA_TRY(cudaMemcpyAsync(h_info, info, sizeof(h_info), cudaMemcpyDeviceToHost, st));
+    PPS_CUDA_TRY(cudaStreamSynchronize(st));
+    if (h_info[1]) return PP_ERR_DEADLOCK;
+    const int R = h_info[0];
+    if (R < 1) return PP_ERR_INTERNAL;
+    if (off + pad4((int64_t)R * pmax) + pad4(2LL * (R + 1)) + pad4(4LL * R) > region_words) return PP_ERR_SIZE;
+    uint32_t *desc = take((int64_t)R * pmax);
+    uint64_t *rw = reinterpret_cast<uint64_t *>(take(2LL * (R + 1)));
+    uint4 *seg = reinterpret_cast<uint4 *>(take(4LL * R));
+    PPS_CUDA_TRY(cudaMemsetAsync(desc, 0, (int64_t)R * pmax * sizeof(uint32_t), st));
+    PPS_CUDA_TRY(cudaMemsetAsync(rw, 0, (int64_t)(R + 1) * sizeof(uint64_t), st));
+    k_desc<<<nblk, tpb, 0, st>>>(ops, round, P, M, 1, pmax, desc);
+    k_peak<<<1, 32, 0, st>>>(ops, P, O, peak);
+    k_rwords<<<(R + 255) / 256, 256, 0, st>>>(desc, R, P, pmax, rw);
+    k_segments<<<1, 32, 0, st>>>(rw, R, seg, info);
+    k_latest<<<nblk, tpb, 0, st>>>(ops, pos, round, P, M, info);
+    PPS_CUDA_TRY(cudaGetLastError());
+    PPS_CUDA_TRY(cudaMemcpyAsync(h_info, info, sizeof(h_info), cudaMemcpyDeviceToHost, st));
+    PPS_CUDA_TRY(cudaStreamSynchronize(st));
+    if (h_info[2]) return PP_ERR_INTERNAL;  // the register evaluator would not apply
+    sp->region = region; sp->region_words = region_words; sp->used_words = off;
+    sp->policy = policy; sp->P = P; sp->M = M; sp->R = R; sp->pmax = pmax; sp->nseg = h_info[6];
+    sp->desc = desc; sp->rw = rw; sp->seg = seg; sp->peak = peak;
+    sp->ktab = nullptr; sp->ktab_words = 0;
+    return PP_OK;
+}
+
+int ktab_into(ScratchPlan *sp, int64_t s_stage, int64_t s_mb, cudaStream_t st) {
+    const int words = ktab_words(sp->R, sp->pmax, sp->nseg);
+    if (sp->used_words + words > sp->region_words) return PP_ERR_SIZE;
+    uint32_t *out = sp->region + sp->used_words;
+    k_ktab<<<(words + 255) / 256, 256, 0, st>>>(sp->desc, sp->rw, sp->seg, sp->R, sp->P, sp->pmax, sp->nseg,
+                                                (int)s_stage, (int)s_mb, out);
+    PPS_CUDA_TRY(cudaGetLastError());
+    sp->ktab = out;
+    sp->ktab_words = words;
+    return PP_OK;
+}
+
 namespace {
 std::mutex g_cache_mu;
 std::map<std::tuple<int, int, int, int, int>, pp_plan *> g_cache;
