@@ -38,6 +38,9 @@ __global__ void __launch_bounds__(128) k_eval_slot(const EvalArgs a) {
     for (int k = 0; k < PMAX; ++k) { fr[k] = 0; busy[k] = 0; cnt[k] = 0; }
     uint32_t accE = 0, accC = 0;
 
+    // Descriptors are loaded one round before they are used (the loader's for
+    // round r+kAhead+1, the compute's for round r+1), so no global load sits
+    // on the critical path of a round.
     const int R = a.R;
     LoadDesc<PMAX, VEC> ld;
 #pragma unroll 1
@@ -48,16 +51,24 @@ __global__ void __launch_bounds__(128) k_eval_slot(const EvalArgs a) {
         }
         cp_async_commit();
     }
+    if (RG::kAhead < R) fetch_load_desc<PMAX, VEC>(a, RG::kAhead, lane, ld);
+    uint32_t dn[PMAX], d2n[PMAX];
+    load_desc<PMAX>(a.desc, dn);
+    load_desc<PMAX>(a.desc2, d2n);
 #pragma unroll 1
     for (int r = 0; r < R; ++r) {
         if (r + RG::kAhead < R) {
-            fetch_load_desc<PMAX, VEC>(a, r + RG::kAhead, lane, ld);
             load_round<PMAX, VEC>(a, r + RG::kAhead, ld, ring, inst0, lane);
+            if (r + RG::kAhead + 1 < R) fetch_load_desc<PMAX, VEC>(a, r + RG::kAhead + 1, lane, ld);
         }
         cp_async_commit();
         uint32_t d[PMAX], d2[PMAX];
-        load_desc<PMAX>(a.desc + (int64_t)r * PMAX, d);
-        load_desc<PMAX>(a.desc2 + (int64_t)r * PMAX, d2);
+#pragma unroll
+        for (int k = 0; k < PMAX; ++k) { d[k] = dn[k]; d2[k] = d2n[k]; }
+        if (r + 1 < R) {
+            load_desc<PMAX>(a.desc + (int64_t)(r + 1) * PMAX, dn);
+            load_desc<PMAX>(a.desc2 + (int64_t)(r + 1) * PMAX, d2n);
+        }
         cp_async_wait<RG::kAhead>();
         __syncwarp();
         const int32_t *slice = ring + (r % RG::kSlices) * (PMAX * 32);
