@@ -307,10 +307,12 @@ __device__ __forceinline__ int wrap_add(int x, int y) {
     return static_cast<int>(static_cast<uint32_t>(x) + static_cast<uint32_t>(y));
 }
 
-// Launchers (defined in eval_reg.cu / eval_slot.cu).
+// Launchers (defined in eval_reg.cu / eval_slot.cu / eval_lane.cu).
 int launch_eval_reg(pp_plan *plan, EvalArgs &a, bool vec, bool ops, cudaStream_t st);
 bool reg_table_path(int pmax, const EvalArgs &a, bool vec);
 int launch_eval_reg_tables(int pmax, const EvalArgs &a, bool vec, bool ops, cudaStream_t st);
 int launch_eval_slot(const pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st);
+bool lane_path(const pp_plan *plan, const EvalArgs &a);
+int launch_eval_lane(pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st);
 
 }  // namespace pps

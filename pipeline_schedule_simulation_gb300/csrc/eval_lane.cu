@@ -1,0 +1,371 @@
+// eval_lane.cu -- the lane-per-device evaluator (interleaved 1F1B).
+//
+// Interleaved 1F1B ("2. 1F1B" §6.1; "Pipeline scheduling" (M040) §06: device
+// k holds the virtual stages k, k+P, ...) can keep several results of one
+// kind in flight between two devices, so an op finds its input through the
+// plan's value slots rather than a fixed register.  Its cost tables are small
+// (a few MB), so the evaluation is bound by instruction issue and latency,
+// not by HBM.  This kernel therefore gives every (instance, device) pair its
+// own lane: a warp holds 32/PMAX instances, lane = device * (32/PMAX) +
+// instance, and in each wavefront round every lane runs at most one op.
+// Ops of one round are independent, so all lanes of a round run in parallel
+// and one __syncwarp per round publishes the round's results.
+//
+// Per warp, in shared memory, every row is 32 words with column = lane:
+//   ring   kSlices rows  cost of this lane's op, filled kAhead rounds ahead
+//   val    nslots rows + a zero row + a scratch row: an op's end tick is
+//          written into its consumer device's column of its value slot
+//   ctab   2v rows + a zero row: the comm latency on the input edge of this
+//          lane's ops, row 2c for a forward of chunk c (boundary s-1|s) and
+//          row 2c+1 for a backward (boundary s|s+1)
+// An op without an input reads the zero rows, an op without a consumer
+// writes the scratch row, and an idle slot runs as a zero-cost op, so the
+// round body has no branch.
+//
+// The per-(round, device) table (built once per plan and stride pair by
+// k_ltab) is streamed through the CTA in blocks of kBR rounds, double
+// buffered with cp.async and published with one __syncthreads per block.
+// Entry (round r, device k):
+//   cw.x  low 16 bits: byte offset of the input slot cell (row*128 + column)
+//         high 16 bits: byte offset of the output slot cell
+//   cw.y  low 16 bits: byte offset of the comm cell; bit 31: op is not idle
+//   lt    loader entry of round r + kAhead (offset << 1 | is-backward, or
+//         kLtIdle), so the loader never needs the next block
+#include "eval_common.cuh"
+
+namespace pps {
+
+template <int PMAX>
+struct LaneGeom {
+    static constexpr int kIPW = 32 / PMAX;              // instances per warp
+    static constexpr int kSlices = 8;                   // cost ring rows
+    static constexpr int kAhead = kSlices - 2;          // rounds loaded ahead
+    static constexpr int kBR = 512 / PMAX;              // rounds per table block
+    static constexpr int kBlockWords = 3 * kBR * PMAX;  // cw (2 words) + lt per entry
+    static constexpr int kHeadWords = (kAhead * PMAX + 3) & ~3;
+    static constexpr int kCopy = kIPW < 4 ? kIPW : 4;   // instances per loader copy (vector path)
+    static_assert(kBR > kAhead, "a table block must outlast the loader's lead");
+};
+
+constexpr uint32_t kLaneActive = 0x80000000u;
+
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+// Loader entry of (round r, device k): the element offset of the op's cost
+// row, shifted left by one, bit 0 set for a backward op; kLtIdle for an idle
+// slot or a round past the end.
+__device__ __forceinline__ uint32_t lane_lt(const uint32_t *desc, int R, int P, int pmax, int r, int k,
+                                            int s_stage, int s_mb) {
+    if (r >= R) return kLtIdle;
+    const uint32_t d = desc[(int64_t)r * pmax + k];
+    const uint32_t kind = desc_kind(d);
+    if (kind == kIdle) return kLtIdle;
+    const int s = (int)desc_chunk(d) * P + k;
+    const uint32_t off = (uint32_t)(s * s_stage + (int)desc_mb(d) * s_mb);
+    return (off << 1) | (kind == kBwd ? 1u : 0u);
+}
+
+// Table of the lane evaluator for one stride pair: head (loader entries of
+// rounds 0 .. kAhead-1), then ceil(R / kBR) blocks laid out as described at
+// the top of the file.
+template <int PMAX>
+__global__ void k_ltab(const uint32_t *desc, const uint32_t *desc2, int R, int P, int v, int nslots,
+                       int s_stage, int s_mb, int nblocks, uint32_t *out) {
+    using G = LaneGeom<PMAX>;
+    const int64_t total = G::kHeadWords + (int64_t)nblocks * G::kBlockWords;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        uint32_t w = kLtIdle;
+        if (e < G::kHeadWords) {
+            const int q = (int)e;
+            if (q < G::kAhead * PMAX) w = lane_lt(desc, R, P, PMAX, q / PMAX, q % PMAX, s_stage, s_mb);
+        } else {
+            const int64_t e2 = e - G::kHeadWords;
+            const int b = (int)(e2 / G::kBlockWords);
+            const int o = (int)(e2 % G::kBlockWords);
+            if (o < 2 * G::kBR * PMAX) {
+                const int idx = o >> 1, q = idx / PMAX, k = idx % PMAX, r = b * G::kBR + q;
+                const uint32_t col = (uint32_t)(k * G::kIPW * 4);
+                const uint32_t zero = (uint32_t)nslots * 128u + col;
+                const uint32_t scratch = (uint32_t)(nslots + 1) * 128u + col;
+                uint32_t rd = zero, wr = scratch, cm = (uint32_t)(2 * v) * 128u + col, act = 0;
+                if (r < R) {
+                    const uint32_t d = desc[(int64_t)r * PMAX + k];
+                    const uint32_t kind = desc_kind(d);
+                    if (kind != kIdle) {
+                        act = kLaneActive;
+                        const uint32_t d2 = desc2[(int64_t)r * PMAX + k];
+                        const uint32_t rs = d2_rslot(d2), ws = d2_wslot(d2);
+                        if (rs != kNoSlot) {
+                            rd = rs * 128u + col;
+                            cm = (2u * desc_chunk(d) + (kind == kBwd ? 1u : 0u)) * 128u + col;
+                        }
+                        if (ws != kNoSlot) {
+                            const int kc = kind == kFwd ? (k + 1) % P : (k + P - 1) % P;
+                            wr = ws * 128u + (uint32_t)(kc * G::kIPW * 4);
+                        }
+                    }
+                }
+                w = (o & 1) ? (cm | act) : (rd | (wr << 16));
+            } else {
+                const int idx = o - 2 * G::kBR * PMAX, q = idx / PMAX, k = idx % PMAX;
+                w = lane_lt(desc, R, P, PMAX, b * G::kBR + q + G::kAhead, k, s_stage, s_mb);
+            }
+        }
+        out[e] = w;
+    }
+}
+
+// Issue this lane's share of the copies of one round's costs into ring row
+// `slice` (layout [device][instance] = column lane).  Vector path: the lanes
+// of instance 0, 4, ... copy kCopy consecutive instances each; scalar path:
+// every lane copies its own word.
+template <int PMAX, bool VEC>
+__device__ __forceinline__ void lane_load(const EvalArgs &a, uint32_t lt, uint32_t *slice, int lane, int j,
+                                          int64_t x) {
+    using G = LaneGeom<PMAX>;
+    if constexpr (VEC) {
+        if (j % G::kCopy != 0) return;
+        const int64_t left = a.n - x;
+        const int32_t *src = a.cost_f;
+        uint32_t nb = 0;
+        if (lt != kLtIdle && left > 0) {
+            src = ((lt & 1u) ? a.cost_b : a.cost_f) + (lt >> 1) + x;
+            nb = (uint32_t)(left < G::kCopy ? left : G::kCopy) * 4u;
+        }
+        if constexpr (G::kCopy == 4) cp_async16(smem_addr(slice + lane), src, nb);
+        else cp_async8(smem_addr(slice + lane), src, nb);
+    } else {
+        const int32_t *src = a.cost_f;
+        uint32_t nb = 0;
+        if (lt != kLtIdle && x < a.n) {
+            src = ((lt & 1u) ? a.cost_b : a.cost_f) + (lt >> 1) + x * a.s_inst;
+            nb = 4;
+        }
+        cp_async4(smem_addr(slice + lane), src, nb);
+    }
+}
+
+// Copy table block `b` into `dst` (all threads of the CTA; joins the caller's
+// next commit group).
+template <int PMAX>
+__device__ __forceinline__ void lane_copy_block(const uint4 *blocks, int b, uint32_t *dst) {
+    using G = LaneGeom<PMAX>;
+    const uint4 *src = blocks + (int64_t)b * (G::kBlockWords / 4);
+    for (int i = threadIdx.x; i < G::kBlockWords / 4; i += blockDim.x) cp_async16(smem_addr(dst + 4 * i), src + i, 16);
+}
+
+template <int PMAX, bool VEC, bool OPS>
+__global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4 *tab, int nblocks) {
+    using G = LaneGeom<PMAX>;
+    extern __shared__ __align__(16) uint32_t lsm[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int j = lane % G::kIPW, k = lane / G::kIPW;
+    const int rows = G::kSlices + a.nslots + 2 + 2 * a.v + 1;
+    uint32_t *ring = lsm + 2 * G::kBlockWords + warp * rows * 32;
+    uint32_t *val = ring + G::kSlices * 32;
+    uint32_t *ctab = val + (a.nslots + 2) * 32;
+    const int64_t inst0 = ((int64_t)blockIdx.x * nwarps + warp) * G::kIPW;
+    const int64_t x = inst0 + j;
+    const bool live = x < a.n;
+    const uint4 *blocks = tab + G::kHeadWords / 4;
+    const int R = a.R;
+
+    // every warp stays to the end: the table blocks are shared by the CTA
+    lane_copy_block<PMAX>(blocks, 0, lsm);
+    cp_async_commit();
+    const uint32_t *head = reinterpret_cast<const uint32_t *>(tab);
+#pragma unroll 1
+    for (int q = 0; q < G::kAhead; ++q) {
+        lane_load<PMAX, VEC>(a, __ldg(head + q * PMAX + k), ring + q * 32, lane, j, x);
+        cp_async_commit();
+    }
+    uint32_t ncomm = 0;
+#pragma unroll 1
+    for (int cr = 0; cr < 2 * a.v; ++cr) {
+        const int s = (cr >> 1) * a.P + k;
+        const int bnd = (cr & 1) ? s : s - 1;
+        int32_t c = 0;
+        if (a.comm && live && k < a.P && bnd >= 0 && bnd < a.S - 1) c = a.comm[x * a.c_inst + (int64_t)bnd * a.c_bnd];
+        ncomm |= (uint32_t)c;
+        ctab[cr * 32 + lane] = (uint32_t)c;
+    }
+    ctab[2 * a.v * 32 + lane] = 0;
+    val[a.nslots * 32 + lane] = 0;
+    cp_async_wait<G::kAhead>();
+    __syncthreads();
+
+    const char *vrd = reinterpret_cast<const char *>(val + j);
+    char *vwr = reinterpret_cast<char *>(val + j);
+    const char *crd = reinterpret_cast<const char *>(ctab + j);
+    uint32_t fr = 0, busy = 0, flag = 0;
+    int cnt = 0;
+#pragma unroll 1
+    for (int b = 0; b < nblocks; ++b) {
+        const uint32_t *tbl = lsm + (b & 1) * G::kBlockWords;
+        if (b + 1 < nblocks) lane_copy_block<PMAX>(blocks, b + 1, lsm + ((b + 1) & 1) * G::kBlockWords);
+        const uint2 *cw = reinterpret_cast<const uint2 *>(tbl) + k;
+        const uint32_t *lt = tbl + 2 * G::kBR * PMAX + k;
+        const int r0 = b * G::kBR, n_r = min(R - r0, G::kBR);
+#pragma unroll 2
+        for (int q = 0; q < n_r; ++q) {
+            const int r = r0 + q;
+            const uint2 e = cw[q * PMAX];
+            lane_load<PMAX, VEC>(a, lt[q * PMAX], ring + ((unsigned)(r + G::kAhead) % G::kSlices) * 32, lane, j, x);
+            cp_async_commit();
+            cp_async_wait<G::kAhead>();
+            __syncwarp();
+            const uint32_t c = ring[((unsigned)r % G::kSlices) * 32 + lane];
+            const uint32_t arr = *reinterpret_cast<const uint32_t *>(vrd + (e.x & 0xFFFFu)) +
+                                 *reinterpret_cast<const uint32_t *>(crd + (e.y & 0xFFFFu));
+            const uint32_t st = max(fr, arr);
+            const uint32_t en = st + c;
+            flag |= st | c;
+            busy += c;
+            fr = en;
+            *reinterpret_cast<uint32_t *>(vwr + (e.x >> 16)) = en;
+            if constexpr (OPS) {
+                if (e.y & kLaneActive) {
+                    if (live) {
+                        const int64_t off = x * a.o_inst + ((int64_t)k * a.O + cnt) * a.o_op;
+                        if (a.op_start) a.op_start[off] = (int32_t)st;
+                        if (a.op_end) a.op_end[off] = (int32_t)en;
+                    }
+                    ++cnt;
+                }
+            }
+        }
+        __syncthreads();
+    }
+    cp_async_wait<0>();
+
+    // Per-instance reductions over the instance's PMAX lanes ("2. 1F1B" §4.3
+    // and M040 §04: the window is the last end tick, a stage's idle time is
+    // the window minus its busy time, the bubble is total idle over P
+    // windows).  `flag` holds the sign bits of every start tick and cost: it
+    // is clear exactly when no cost is negative and every tick fits in int32.
+    uint32_t mk = fr;
+#pragma unroll
+    for (int m = G::kIPW; m < 32; m <<= 1) {
+        mk = max(mk, __shfl_xor_sync(0xFFFFFFFFu, mk, m));
+        flag |= __shfl_xor_sync(0xFFFFFFFFu, flag, m);
+        ncomm |= __shfl_xor_sync(0xFFFFFFFFu, ncomm, m);
+    }
+    flag |= mk;
+    const int idle = k < a.P ? (int)(mk - busy) : 0;
+    int64_t num = idle;
+#pragma unroll
+    for (int m = G::kIPW; m < 32; m <<= 1) num += __shfl_xor_sync(0xFFFFFFFFu, num, m);
+    if (!live) return;
+    if (a.idle && k < a.P) a.idle[x * a.P + k] = idle;
+    if (k == 0) {
+        if (a.makespan) a.makespan[x] = (int)mk;
+        if (a.bub_num) a.bub_num[x] = num;
+        if (a.bub_den) a.bub_den[x] = (int64_t)a.P * (int)mk;
+        if (a.status) {
+            int8_t st = PP_ST_OK;
+            if (ncomm >> 31) st = PP_ST_NEG_COST;
+            else if (flag >> 31) st = any_negative_cost(a, x) ? PP_ST_NEG_COST : PP_ST_OVERFLOW;
+            a.status[x] = st;
+        }
+    }
+}
+
+namespace {
+
+template <int PMAX>
+int lane_tables_t(pp_plan *plan, int64_t s_stage, int64_t s_mb, cudaStream_t stream, const pp_ktab **out) {
+    using G = LaneGeom<PMAX>;
+    std::lock_guard<std::mutex> lk(plan->ktab_mu);
+    for (const pp_ktab &t : plan->ltabs)
+        if (t.s_stage == s_stage && t.s_mb == s_mb) { *out = &t; return PP_OK; }
+    const int nblocks = (plan->R + G::kBR - 1) / G::kBR;
+    pp_ktab t;
+    t.s_stage = s_stage;
+    t.s_mb = s_mb;
+    t.words = G::kHeadWords + nblocks * G::kBlockWords;
+    PPS_CUDA_TRY(cudaMalloc(&t.d, (size_t)t.words * sizeof(uint32_t)));
+    const int blocks = (t.words + 255) / 256;
+    k_ltab<PMAX><<<blocks, 256, 0, stream>>>(plan->d_desc, plan->d_desc2, plan->R, plan->P, plan->v,
+                                             plan->nslots, (int)s_stage, (int)s_mb, nblocks,
+                                             reinterpret_cast<uint32_t *>(t.d));
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) {
+        cudaFree(t.d);
+        return cuda_status(e);
+    }
+    plan->ltabs.push_back(t);
+    *out = &plan->ltabs.back();
+    return PP_OK;
+}
+
+constexpr size_t kLaneSmemLimit = 227 * 1024;
+
+template <int PMAX>
+size_t lane_smem(const EvalArgs &a, int warps) {
+    using G = LaneGeom<PMAX>;
+    const size_t rows = (size_t)G::kSlices + a.nslots + 2 + 2 * a.v + 1;
+    return 2 * (size_t)G::kBlockWords * 4 + (size_t)warps * rows * 32 * 4;
+}
+
+template <int PMAX, bool VEC, bool OPS>
+int launch_lane_t(const EvalArgs &a, const pp_ktab *t, cudaStream_t st) {
+    using G = LaneGeom<PMAX>;
+    const int warps = lane_smem<PMAX>(a, 8) <= 100 * 1024 ? 8 : 4;
+    const size_t smem = lane_smem<PMAX>(a, warps);
+    int dev = 0;
+    PPS_CUDA_TRY(cudaGetDevice(&dev));
+    static bool attr_set[64] = {};
+    if (dev < 64 && !attr_set[dev]) {
+        PPS_CUDA_TRY(cudaFuncSetAttribute(k_eval_lane<PMAX, VEC, OPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)kLaneSmemLimit));
+        attr_set[dev] = true;
+    }
+    const int64_t nw = (a.n + G::kIPW - 1) / G::kIPW;
+    const int64_t grid = (nw + warps - 1) / warps;
+    if (grid > 0x7FFFFFFF) return PP_ERR_SIZE;
+    const int nblocks = (a.R + G::kBR - 1) / G::kBR;
+    k_eval_lane<PMAX, VEC, OPS><<<(unsigned)grid, warps * 32, smem, st>>>(a, t->d, nblocks);
+    PPS_CUDA_TRY(cudaGetLastError());
+    return PP_OK;
+}
+
+template <int PMAX>
+int launch_lane_p(pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st) {
+    const pp_ktab *t = nullptr;
+    const int rc = lane_tables_t<PMAX>(plan, a.s_stage, a.s_mb, st, &t);
+    if (rc) return rc;
+    if (vec) return ops ? launch_lane_t<PMAX, true, true>(a, t, st) : launch_lane_t<PMAX, true, false>(a, t, st);
+    return ops ? launch_lane_t<PMAX, false, true>(a, t, st) : launch_lane_t<PMAX, false, false>(a, t, st);
+}
+
+}  // namespace
+
+// The lane evaluator applies when the plan has value slots, every cost-row
+// offset fits the loader table (below 2^30 elements) and a 4-warp CTA fits in
+// shared memory.
+bool lane_path(const pp_plan *plan, const EvalArgs &a) {
+    if (!plan->d_desc2) return false;
+    if ((int64_t)(a.S - 1) * a.s_stage + (int64_t)(a.M - 1) * a.s_mb >= ((int64_t)1 << 30)) return false;
+    switch (plan->pmax) {
+        case 4: return lane_smem<4>(a, 4) <= kLaneSmemLimit;
+        case 8: return lane_smem<8>(a, 4) <= kLaneSmemLimit;
+        case 16: return lane_smem<16>(a, 4) <= kLaneSmemLimit;
+        default: return false;
+    }
+}
+
+int launch_eval_lane(pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st) {
+    switch (plan->pmax) {
+        case 4: return launch_lane_p<4>(plan, a, vec, ops, st);
+        case 8: return launch_lane_p<8>(plan, a, vec, ops, st);
+        case 16: return launch_lane_p<16>(plan, a, vec, ops, st);
+        default: return PP_ERR_INTERNAL;
+    }
+}
+
+}  // namespace pps

@@ -461,5 +461,6 @@ extern "C" int pp_sched_eval(pp_policy_t policy, int P, int M, int v, const int3
                      (int64_t)(plan->S - 1) * stride_stage + (int64_t)(M - 1) * stride_mb < ((int64_t)1 << 31);
     const bool ops = op_start || op_end;
     if (plan->reg_ok) return launch_eval_reg(plan, a, vec, ops, stream);
+    if (lane_path(plan, a)) return launch_eval_lane(plan, a, vec, ops, stream);
     return launch_eval_slot(plan, a, vec, ops, stream);
 }

@@ -95,6 +95,7 @@ struct pp_plan {
     int nseg;
     std::mutex ktab_mu; // guards ktabs
     std::deque<pp_ktab> ktabs;   // per stride pair, built on first use (stable addresses)
+    std::deque<pp_ktab> ltabs;   // lane evaluator's tables, per stride pair (guarded by ktab_mu)
     int32_t *d_peak;    // [P]
     int32_t h_peak[PP_MAX_P];
 };

@@ -557,6 +557,7 @@ void pp_sched_plan_destroy(pp_plan_t *p) {
     cudaFree(p->d_rw);
     cudaFree(p->d_seg);
     for (pp_ktab &t : p->ktabs) cudaFree(t.d);
+    for (pp_ktab &t : p->ltabs) cudaFree(t.d);
     cudaFree(p->d_peak);
     delete p;
 }

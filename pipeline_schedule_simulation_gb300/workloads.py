@@ -148,8 +148,11 @@ def layer_split(seed=5, L=80, P=8, M=128, n_cand=1 << 20):
 
 
 def random_batch(policy, P, M, v, n, seed, lo=0, hi=9, comm_hi=4, layout="inst_minor",
-                 stride_mb_zero=False):
-    """Small random instances for parity tests (any policy/shape/layout)."""
+                 stride_mb_zero=False, pad_to=1):
+    """Small random instances for parity tests (any policy/shape/layout).
+
+    With the instance-minor layout each (stage, microbatch) row holds n
+    instances padded to a multiple of `pad_to` elements (the pad is zero)."""
     rng = _rng(seed)
     S = P * v
     Mx = 1 if stride_mb_zero else M
@@ -157,9 +160,13 @@ def random_batch(policy, P, M, v, n, seed, lo=0, hi=9, comm_hi=4, layout="inst_m
     cb = rng.integers(lo, hi, size=(n, S, Mx), dtype=np.int32, endpoint=True)
     cm = rng.integers(0, comm_hi, size=(n, max(S - 1, 1)), dtype=np.int32, endpoint=True)
     if layout == "inst_minor":
-        cfa = np.ascontiguousarray(np.transpose(cf, (1, 2, 0))).reshape(-1)
-        cba = np.ascontiguousarray(np.transpose(cb, (1, 2, 0))).reshape(-1)
-        st = (1, Mx * n, 0 if stride_mb_zero else n)
+        pitch = -(-n // pad_to) * pad_to if n else 0
+        rows_f = np.zeros((S, Mx, pitch), np.int32)
+        rows_b = np.zeros((S, Mx, pitch), np.int32)
+        rows_f[:, :, :n] = np.transpose(cf, (1, 2, 0))
+        rows_b[:, :, :n] = np.transpose(cb, (1, 2, 0))
+        cfa, cba = rows_f.reshape(-1), rows_b.reshape(-1)
+        st = (1, Mx * pitch, 0 if stride_mb_zero else pitch)
         cma = np.ascontiguousarray(cm.T).reshape(-1)
         cst = (1, n)
     else:

@@ -66,6 +66,69 @@ def test_random_batches(orc, B, policy, P, M, v, layout):
         assert_same(g, r, op_times=True)
 
 
+VEC_SHAPES = [
+    (W.INTERLEAVED, 8, 16, 2), (W.INTERLEAVED, 4, 8, 3), (W.INTERLEAVED, 16, 32, 2),
+    (W.INTERLEAVED, 2, 4, 4), (W.INTERLEAVED, 3, 6, 2), (W.ONEF1B, 8, 12, 1), (W.GPIPE, 4, 8, 1),
+]
+
+
+@pytest.mark.parametrize("policy,P,M,v", VEC_SHAPES)
+def test_vector_rows_ragged_tail(orc, B, policy, P, M, v):
+    """Instance-minor rows padded to 16 bytes take the vector loaders; n
+    leaves a last copy that covers fewer instances than its width."""
+    for n, seed in ((77, 5), (161, 6), (3, 7)):
+        batch = W.random_batch(policy, P, M, v, n, seed=seed + P + M, hi=12, comm_hi=5, pad_to=4)
+        assert batch.strides[1] % 4 == 0 and batch.strides[2] % 4 == 0
+        g = run_gpu(batch, op_times=True)
+        r = run_oracle(orc, batch, op_times=True)
+        assert_same(g, r, op_times=True)
+
+
+def test_status_interleaved(orc, B):
+    P, M, v, n = 4, 8, 2, 70
+    S = P * v
+    batch = W.random_batch(W.INTERLEAVED, P, M, v, n, seed=9, layout="inst_major")
+    cf = batch.cost_f.reshape(n, S, M)
+    cb = batch.cost_b.reshape(n, S, M)
+    cf[3, 5, 2] = -1
+    cb[10, 0, 0] = 2**31 - 1
+    cf[11, 7, 7] = 2**30
+    cb[11, 2, 3] = 2**30
+    batch.comm.reshape(n, S - 1)[20, 4] = -4
+    batch.comm.reshape(n, S - 1)[21, 6] = 2**31 - 2
+    g = run_gpu(batch)
+    r = run_oracle(orc, batch)
+    assert g["status"][3] == B.ST_NEG_COST and g["status"][20] == B.ST_NEG_COST
+    assert g["status"][10] == B.ST_OVERFLOW and g["status"][21] == B.ST_OVERFLOW
+    assert_same(g, r)
+
+
+def test_generic_evaluator_wide_strides(orc, B):
+    """Cost rows more than 2^30 elements apart are beyond the lane
+    evaluator's loader table, so interleaved instances run on the generic
+    slot evaluator: same numbers.  Forward and backward costs share one
+    sparse 8 GB buffer (backward rows sit n*M elements after forward rows)."""
+    import torch
+    P, M, v, n = 8, 8, 4, 40
+    S = P * v
+    compact = W.random_batch(W.INTERLEAVED, P, M, v, n, seed=12, hi=12, comm_hi=5, layout="inst_major")
+    si, ss, sm = M, 1 << 26, 1
+    assert (S - 1) * ss >= 1 << 30
+    x, s, m = np.meshgrid(np.arange(n), np.arange(S), np.arange(M), indexing="ij")
+    idx = (x * si + s * ss + m * sm).reshape(-1)
+    buf = torch.empty(int(idx.max()) + n * M + 1, dtype=torch.int32, device="cuda")
+    buf[torch.from_numpy(idx).cuda()] = to_dev(compact.cost_f.reshape(-1))
+    buf[torch.from_numpy(idx + n * M).cuda()] = to_dev(compact.cost_b.reshape(-1))
+    out = B.evaluate(W.INTERLEAVED, P, M, v, buf, buf[n * M:], (si, ss, sm), n, comm=to_dev(compact.comm),
+                     comm_strides=compact.comm_strides, op_times=True)
+    torch.cuda.synchronize()
+    g = {k: t.cpu().numpy() for k, t in out.items()}
+    del buf, out
+    torch.cuda.empty_cache()
+    r = run_oracle(orc, compact, op_times=True)
+    assert_same(g, r, op_times=True)
+
+
 def test_zero_costs_and_empty(orc, B):
     batch = W.random_batch(W.ONEF1B, 4, 6, 1, 40, seed=3, lo=0, hi=0, comm_hi=0)
     g = run_gpu(batch)
