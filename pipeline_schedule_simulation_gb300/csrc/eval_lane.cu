@@ -29,8 +29,9 @@
 //   cw.x  low 16 bits: byte offset of the input slot cell (row*128 + column)
 //         high 16 bits: byte offset of the output slot cell
 //   cw.y  low 16 bits: byte offset of the comm cell; bit 31: op is not idle
-//   lt    loader entry of round r + kAhead (offset << 1 | is-backward, or
-//         kLtIdle), so the loader never needs the next block
+//   lt    loader entry of round r + kAhead: byte offset of the op's cost
+//         row | 1 for a backward op, or kLtIdle; shifted by kAhead rounds so
+//         the loader never needs the next block
 #include "eval_common.cuh"
 
 namespace pps {
@@ -45,18 +46,14 @@ struct LaneGeom {
     static constexpr int kHeadWords = (kAhead * PMAX + 3) & ~3;
     static constexpr int kCopy = kIPW < 4 ? kIPW : 4;   // instances per loader copy (vector path)
     static_assert(kBR > kAhead, "a table block must outlast the loader's lead");
+    static_assert(kSlices == 8 && kBR % kSlices == 0, "the round loop is unrolled by the ring size");
 };
 
 constexpr uint32_t kLaneActive = 0x80000000u;
 
-__device__ __forceinline__ void cp_async8(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-
-// Loader entry of (round r, device k): the element offset of the op's cost
-// row, shifted left by one, bit 0 set for a backward op; kLtIdle for an idle
-// slot or a round past the end.
+// Loader entry of (round r, device k): the byte offset of the op's cost row
+// (element offsets stay below 2^30, checked on the host), bit 0 set for a
+// backward op; kLtIdle for an idle slot or a round past the end.
 __device__ __forceinline__ uint32_t lane_lt(const uint32_t *desc, int R, int P, int pmax, int r, int k,
                                             int s_stage, int s_mb) {
     if (r >= R) return kLtIdle;
@@ -65,7 +62,7 @@ __device__ __forceinline__ uint32_t lane_lt(const uint32_t *desc, int R, int P, 
     if (kind == kIdle) return kLtIdle;
     const int s = (int)desc_chunk(d) * P + k;
     const uint32_t off = (uint32_t)(s * s_stage + (int)desc_mb(d) * s_mb);
-    return (off << 1) | (kind == kBwd ? 1u : 0u);
+    return (off << 2) | (kind == kBwd ? 1u : 0u);
 }
 
 // Table of the lane evaluator for one stride pair: head (loader entries of
@@ -119,35 +116,50 @@ __global__ void k_ltab(const uint32_t *desc, const uint32_t *desc2, int R, int P
     }
 }
 
-// Issue this lane's share of the copies of one round's costs into ring row
-// `slice` (layout [device][instance] = column lane).  Vector path: the lanes
-// of instance 0, 4, ... copy kCopy consecutive instances each; scalar path:
-// every lane copies its own word.
+// This lane's share of the cost copies.  Vector path: the lanes of instance
+// 0, 4, ... of each device copy kCopy consecutive instances (16 or 8 bytes);
+// scalar path: every lane copies its own word.  The copy lands in ring row
+// `dst` at column lane (layout [device][instance]).  Everything but the row
+// offset is fixed per lane, so a round costs a select, an add and one
+// predicated cp.async.
 template <int PMAX, bool VEC>
-__device__ __forceinline__ void lane_load(const EvalArgs &a, uint32_t lt, uint32_t *slice, int lane, int j,
-                                          int64_t x) {
-    using G = LaneGeom<PMAX>;
-    if constexpr (VEC) {
-        if (j % G::kCopy != 0) return;
+struct LaneLoader {
+    const char *fb, *bb;  // this lane's first element in cost_f / cost_b
+    uint32_t bytes;       // bytes copied for a non-idle op (0 past the last instance)
+    uint32_t on;          // this lane issues copies
+
+    __device__ __forceinline__ LaneLoader(const EvalArgs &a, int j, int64_t x) {
+        using G = LaneGeom<PMAX>;
         const int64_t left = a.n - x;
-        const int32_t *src = a.cost_f;
-        uint32_t nb = 0;
-        if (lt != kLtIdle && left > 0) {
-            src = ((lt & 1u) ? a.cost_b : a.cost_f) + (lt >> 1) + x;
-            nb = (uint32_t)(left < G::kCopy ? left : G::kCopy) * 4u;
+        const int64_t e0 = left > 0 ? (VEC ? x : x * a.s_inst) : 0;
+        fb = reinterpret_cast<const char *>(a.cost_f + e0);
+        bb = reinterpret_cast<const char *>(a.cost_b + e0);
+        if constexpr (VEC) {
+            on = (j % G::kCopy) == 0;
+            bytes = left <= 0 ? 0u : (uint32_t)(left < G::kCopy ? left : G::kCopy) * 4u;
+        } else {
+            on = 1;
+            bytes = left > 0 ? 4u : 0u;
         }
-        if constexpr (G::kCopy == 4) cp_async16(smem_addr(slice + lane), src, nb);
-        else cp_async8(smem_addr(slice + lane), src, nb);
-    } else {
-        const int32_t *src = a.cost_f;
-        uint32_t nb = 0;
-        if (lt != kLtIdle && x < a.n) {
-            src = ((lt & 1u) ? a.cost_b : a.cost_f) + (lt >> 1) + x * a.s_inst;
-            nb = 4;
-        }
-        cp_async4(smem_addr(slice + lane), src, nb);
     }
-}
+
+    __device__ __forceinline__ void issue(uint32_t lt, uint32_t dst) const {
+        using G = LaneGeom<PMAX>;
+        const bool idle = lt == kLtIdle;
+        const char *src = ((lt & 1u) ? bb : fb) + (idle ? 0u : (lt & ~3u));
+        const uint32_t nb = idle ? 0u : bytes;
+        if constexpr (VEC && G::kCopy == 4)
+            asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %3, 0;\n"
+                         " @p cp.async.cg.shared.global [%0], [%1], 16, %2;\n}\n" ::"r"(dst), "l"(src), "r"(nb),
+                         "r"(on) : "memory");
+        else if constexpr (VEC)
+            asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %3, 0;\n"
+                         " @p cp.async.ca.shared.global [%0], [%1], 8, %2;\n}\n" ::"r"(dst), "l"(src), "r"(nb),
+                         "r"(on) : "memory");
+        else
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(nb) : "memory");
+    }
+};
 
 // Copy table block `b` into `dst` (all threads of the CTA; joins the caller's
 // next commit group).
@@ -178,9 +190,11 @@ __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4
     lane_copy_block<PMAX>(blocks, 0, lsm);
     cp_async_commit();
     const uint32_t *head = reinterpret_cast<const uint32_t *>(tab);
+    const LaneLoader<PMAX, VEC> ld(a, j, x);
+    const uint32_t ring_s = smem_addr(ring + lane);
 #pragma unroll 1
     for (int q = 0; q < G::kAhead; ++q) {
-        lane_load<PMAX, VEC>(a, __ldg(head + q * PMAX + k), ring + q * 32, lane, j, x);
+        ld.issue(__ldg(head + q * PMAX + k), ring_s + q * 128);
         cp_async_commit();
     }
     uint32_t ncomm = 0;
@@ -209,16 +223,17 @@ __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4
         if (b + 1 < nblocks) lane_copy_block<PMAX>(blocks, b + 1, lsm + ((b + 1) & 1) * G::kBlockWords);
         const uint2 *cw = reinterpret_cast<const uint2 *>(tbl) + k;
         const uint32_t *lt = tbl + 2 * G::kBR * PMAX + k;
-        const int r0 = b * G::kBR, n_r = min(R - r0, G::kBR);
-#pragma unroll 2
-        for (int q = 0; q < n_r; ++q) {
-            const int r = r0 + q;
+        const int n_r = min(R - b * G::kBR, G::kBR);
+        // one round: the loader runs kAhead rounds ahead into ring row nxt,
+        // the op reads its cost from row cur (rows are round mod kSlices; a
+        // block starts at a multiple of kSlices)
+        auto round = [&](int q, int cur, int nxt) {
             const uint2 e = cw[q * PMAX];
-            lane_load<PMAX, VEC>(a, lt[q * PMAX], ring + ((unsigned)(r + G::kAhead) % G::kSlices) * 32, lane, j, x);
+            ld.issue(lt[q * PMAX], ring_s + nxt * 128);
             cp_async_commit();
             cp_async_wait<G::kAhead>();
             __syncwarp();
-            const uint32_t c = ring[((unsigned)r % G::kSlices) * 32 + lane];
+            const uint32_t c = ring[cur * 32 + lane];
             const uint32_t arr = *reinterpret_cast<const uint32_t *>(vrd + (e.x & 0xFFFFu)) +
                                  *reinterpret_cast<const uint32_t *>(crd + (e.y & 0xFFFFu));
             const uint32_t st = max(fr, arr);
@@ -237,7 +252,15 @@ __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4
                     ++cnt;
                 }
             }
+        };
+        int q = 0;
+#pragma unroll 1
+        for (; q + G::kSlices <= n_r; q += G::kSlices) {
+#pragma unroll
+            for (int i = 0; i < G::kSlices; ++i) round(q + i, i, (i + G::kAhead) % G::kSlices);
         }
+#pragma unroll 1
+        for (; q < n_r; ++q) round(q, q % G::kSlices, (q + G::kAhead) % G::kSlices);
         __syncthreads();
     }
     cp_async_wait<0>();
