@@ -70,7 +70,7 @@ __device__ __forceinline__ uint32_t lane_lt(const uint32_t *desc, int R, int P, 
 // the top of the file.
 template <int PMAX>
 __global__ void k_ltab(const uint32_t *desc, const uint32_t *desc2, int R, int P, int v, int nslots,
-                       int s_stage, int s_mb, int nblocks, uint32_t *out) {
+                       int s_stage, int s_mb, int nblocks, uint32_t row_bytes, uint32_t *out) {
     using G = LaneGeom<PMAX>;
     const int64_t total = G::kHeadWords + (int64_t)nblocks * G::kBlockWords;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
@@ -86,9 +86,9 @@ __global__ void k_ltab(const uint32_t *desc, const uint32_t *desc2, int R, int P
             if (o < 2 * G::kBR * PMAX) {
                 const int idx = o >> 1, q = idx / PMAX, k = idx % PMAX, r = b * G::kBR + q;
                 const uint32_t col = (uint32_t)(k * G::kIPW * 4);
-                const uint32_t zero = (uint32_t)nslots * 128u + col;
-                const uint32_t scratch = (uint32_t)(nslots + 1) * 128u + col;
-                uint32_t rd = zero, wr = scratch, cm = (uint32_t)(2 * v) * 128u + col, act = 0;
+                const uint32_t zero = (uint32_t)nslots * row_bytes + col;
+                const uint32_t scratch = (uint32_t)(nslots + 1) * row_bytes + col;
+                uint32_t rd = zero, wr = scratch, cm = (uint32_t)(2 * v) * row_bytes + col, act = 0;
                 if (r < R) {
                     const uint32_t d = desc[(int64_t)r * PMAX + k];
                     const uint32_t kind = desc_kind(d);
@@ -97,12 +97,12 @@ __global__ void k_ltab(const uint32_t *desc, const uint32_t *desc2, int R, int P
                         const uint32_t d2 = desc2[(int64_t)r * PMAX + k];
                         const uint32_t rs = d2_rslot(d2), ws = d2_wslot(d2);
                         if (rs != kNoSlot) {
-                            rd = rs * 128u + col;
-                            cm = (2u * desc_chunk(d) + (kind == kBwd ? 1u : 0u)) * 128u + col;
+                            rd = rs * row_bytes + col;
+                            cm = (2u * desc_chunk(d) + (kind == kBwd ? 1u : 0u)) * row_bytes + col;
                         }
                         if (ws != kNoSlot) {
                             const int kc = kind == kFwd ? (k + 1) % P : (k + P - 1) % P;
-                            wr = ws * 128u + (uint32_t)(kc * G::kIPW * 4);
+                            wr = ws * row_bytes + (uint32_t)(kc * G::kIPW * 4);
                         }
                     }
                 }
@@ -116,30 +116,31 @@ __global__ void k_ltab(const uint32_t *desc, const uint32_t *desc2, int R, int P
     }
 }
 
-// This lane's share of the cost copies.  Vector path: the lanes of instance
-// 0, 4, ... of each device copy kCopy consecutive instances (16 or 8 bytes);
-// scalar path: every lane copies its own word.  The copy lands in ring row
-// `dst` at column lane (layout [device][instance]).  Everything but the row
-// offset is fixed per lane, so a round costs a select, an add and one
-// predicated cp.async.
-template <int PMAX, bool VEC>
+// This lane's share of the cost copies, for each of its NI instances.
+// Vector path: the lanes of instance 0, 4, ... of each device copy kCopy
+// consecutive instances (16 or 8 bytes); scalar path: every lane copies its
+// own word.  Instance set i lands in ring row `dst` at column 32*i + lane
+// (layout [device][instance]).  Everything but the row offset is fixed per
+// lane, so a round costs a select, an add and one predicated cp.async per set.
+template <int PMAX, int NI, bool VEC>
 struct LaneLoader {
-    const char *fb, *bb;  // this lane's first element in cost_f / cost_b
-    uint32_t bytes;       // bytes copied for a non-idle op (0 past the last instance)
-    uint32_t on;          // this lane issues copies
+    const char *fb, *bb;   // this lane's first element of set 0 in cost_f / cost_b
+    int64_t step[NI];      // byte distance from set 0 to set i (0 where set i copies nothing)
+    uint32_t bytes[NI];    // bytes copied for a non-idle op (0 past the last instance)
+    uint32_t on;           // this lane issues copies
 
-    __device__ __forceinline__ LaneLoader(const EvalArgs &a, int j, int64_t x) {
+    __device__ __forceinline__ LaneLoader(const EvalArgs &a, int j, int64_t x0) {
         using G = LaneGeom<PMAX>;
-        const int64_t left = a.n - x;
-        const int64_t e0 = left > 0 ? (VEC ? x : x * a.s_inst) : 0;
+        const int64_t e0 = x0 < a.n ? (VEC ? x0 : x0 * a.s_inst) : 0;
         fb = reinterpret_cast<const char *>(a.cost_f + e0);
         bb = reinterpret_cast<const char *>(a.cost_b + e0);
-        if constexpr (VEC) {
-            on = (j % G::kCopy) == 0;
-            bytes = left <= 0 ? 0u : (uint32_t)(left < G::kCopy ? left : G::kCopy) * 4u;
-        } else {
-            on = 1;
-            bytes = left > 0 ? 4u : 0u;
+        on = VEC ? (j % G::kCopy) == 0 : 1;
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            const int64_t left = a.n - (x0 + i * G::kIPW);
+            const int64_t per = VEC ? G::kCopy : 1;
+            bytes[i] = left <= 0 ? 0u : (uint32_t)(left < per ? left : per) * 4u;
+            step[i] = bytes[i] ? (int64_t)i * G::kIPW * (VEC ? 1 : a.s_inst) * 4 : 0;
         }
     }
 
@@ -147,17 +148,22 @@ struct LaneLoader {
         using G = LaneGeom<PMAX>;
         const bool idle = lt == kLtIdle;
         const char *src = ((lt & 1u) ? bb : fb) + (idle ? 0u : (lt & ~3u));
-        const uint32_t nb = idle ? 0u : bytes;
-        if constexpr (VEC && G::kCopy == 4)
-            asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %3, 0;\n"
-                         " @p cp.async.cg.shared.global [%0], [%1], 16, %2;\n}\n" ::"r"(dst), "l"(src), "r"(nb),
-                         "r"(on) : "memory");
-        else if constexpr (VEC)
-            asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %3, 0;\n"
-                         " @p cp.async.ca.shared.global [%0], [%1], 8, %2;\n}\n" ::"r"(dst), "l"(src), "r"(nb),
-                         "r"(on) : "memory");
-        else
-            asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(nb) : "memory");
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            const char *s = src + step[i];
+            const uint32_t nb = idle ? 0u : bytes[i];
+            const uint32_t d = dst + 128 * i;
+            if constexpr (VEC && G::kCopy == 4)
+                asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %3, 0;\n"
+                             " @p cp.async.cg.shared.global [%0], [%1], 16, %2;\n}\n" ::"r"(d), "l"(s), "r"(nb),
+                             "r"(on) : "memory");
+            else if constexpr (VEC)
+                asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %3, 0;\n"
+                             " @p cp.async.ca.shared.global [%0], [%1], 8, %2;\n}\n" ::"r"(d), "l"(s), "r"(nb),
+                             "r"(on) : "memory");
+            else
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(d), "l"(s), "r"(nb) : "memory");
+        }
     }
 };
 
@@ -170,19 +176,22 @@ __device__ __forceinline__ void lane_copy_block(const uint4 *blocks, int b, uint
     for (int i = threadIdx.x; i < G::kBlockWords / 4; i += blockDim.x) cp_async16(smem_addr(dst + 4 * i), src + i, 16);
 }
 
-template <int PMAX, bool VEC, bool OPS>
+// NI instance sets per lane: a warp holds NI * 32/PMAX instances; every row
+// of the warp's shared memory is 32*NI words, set i in words 32i .. 32i+31,
+// so the second set of a row sits at a fixed +128 bytes.
+template <int PMAX, int NI, bool VEC, bool OPS>
 __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4 *tab, int nblocks) {
     using G = LaneGeom<PMAX>;
+    constexpr int kRow = 32 * NI;  // words per row
     extern __shared__ __align__(16) uint32_t lsm[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const int j = lane % G::kIPW, k = lane / G::kIPW;
     const int rows = G::kSlices + a.nslots + 2 + 2 * a.v + 1;
-    uint32_t *ring = lsm + 2 * G::kBlockWords + warp * rows * 32;
-    uint32_t *val = ring + G::kSlices * 32;
-    uint32_t *ctab = val + (a.nslots + 2) * 32;
-    const int64_t inst0 = ((int64_t)blockIdx.x * nwarps + warp) * G::kIPW;
-    const int64_t x = inst0 + j;
-    const bool live = x < a.n;
+    uint32_t *ring = lsm + 2 * G::kBlockWords + warp * rows * kRow;
+    uint32_t *val = ring + G::kSlices * kRow;
+    uint32_t *ctab = val + (a.nslots + 2) * kRow;
+    const int64_t inst0 = ((int64_t)blockIdx.x * nwarps + warp) * (G::kIPW * NI);
+    const int64_t x0 = inst0 + j;  // set i holds instance x0 + i * kIPW
     const uint4 *blocks = tab + G::kHeadWords / 4;
     const int R = a.R;
 
@@ -190,32 +199,40 @@ __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4
     lane_copy_block<PMAX>(blocks, 0, lsm);
     cp_async_commit();
     const uint32_t *head = reinterpret_cast<const uint32_t *>(tab);
-    const LaneLoader<PMAX, VEC> ld(a, j, x);
+    const LaneLoader<PMAX, NI, VEC> ld(a, j, x0);
     const uint32_t ring_s = smem_addr(ring + lane);
 #pragma unroll 1
     for (int q = 0; q < G::kAhead; ++q) {
-        ld.issue(__ldg(head + q * PMAX + k), ring_s + q * 128);
+        ld.issue(__ldg(head + q * PMAX + k), ring_s + q * kRow * 4);
         cp_async_commit();
     }
-    uint32_t ncomm = 0;
+    uint32_t ncomm[NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+        const int64_t x = x0 + i * G::kIPW;
+        ncomm[i] = 0;
 #pragma unroll 1
-    for (int cr = 0; cr < 2 * a.v; ++cr) {
-        const int s = (cr >> 1) * a.P + k;
-        const int bnd = (cr & 1) ? s : s - 1;
-        int32_t c = 0;
-        if (a.comm && live && k < a.P && bnd >= 0 && bnd < a.S - 1) c = a.comm[x * a.c_inst + (int64_t)bnd * a.c_bnd];
-        ncomm |= (uint32_t)c;
-        ctab[cr * 32 + lane] = (uint32_t)c;
+        for (int cr = 0; cr < 2 * a.v; ++cr) {
+            const int s = (cr >> 1) * a.P + k;
+            const int bnd = (cr & 1) ? s : s - 1;
+            int32_t c = 0;
+            if (a.comm && x < a.n && k < a.P && bnd >= 0 && bnd < a.S - 1)
+                c = a.comm[x * a.c_inst + (int64_t)bnd * a.c_bnd];
+            ncomm[i] |= (uint32_t)c;
+            ctab[cr * kRow + 32 * i + lane] = (uint32_t)c;
+        }
+        ctab[2 * a.v * kRow + 32 * i + lane] = 0;
+        val[a.nslots * kRow + 32 * i + lane] = 0;
     }
-    ctab[2 * a.v * 32 + lane] = 0;
-    val[a.nslots * 32 + lane] = 0;
     cp_async_wait<G::kAhead>();
     __syncthreads();
 
     const char *vrd = reinterpret_cast<const char *>(val + j);
     char *vwr = reinterpret_cast<char *>(val + j);
     const char *crd = reinterpret_cast<const char *>(ctab + j);
-    uint32_t fr = 0, busy = 0, flag = 0;
+    uint32_t fr[NI], busy[NI], flag[NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) { fr[i] = 0; busy[i] = 0; flag[i] = 0; }
     int cnt = 0;
 #pragma unroll 1
     for (int b = 0; b < nblocks; ++b) {
@@ -229,29 +246,34 @@ __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4
         // block starts at a multiple of kSlices)
         auto round = [&](int q, int cur, int nxt) {
             const uint2 e = cw[q * PMAX];
-            ld.issue(lt[q * PMAX], ring_s + nxt * 128);
+            ld.issue(lt[q * PMAX], ring_s + nxt * kRow * 4);
             cp_async_commit();
             cp_async_wait<G::kAhead>();
             __syncwarp();
-            const uint32_t c = ring[cur * 32 + lane];
-            const uint32_t arr = *reinterpret_cast<const uint32_t *>(vrd + (e.x & 0xFFFFu)) +
-                                 *reinterpret_cast<const uint32_t *>(crd + (e.y & 0xFFFFu));
-            const uint32_t st = max(fr, arr);
-            const uint32_t en = st + c;
-            flag |= st | c;
-            busy += c;
-            fr = en;
-            *reinterpret_cast<uint32_t *>(vwr + (e.x >> 16)) = en;
-            if constexpr (OPS) {
-                if (e.y & kLaneActive) {
-                    if (live) {
+            const char *vr = vrd + (e.x & 0xFFFFu);
+            const char *cr = crd + (e.y & 0xFFFFu);
+            char *vw = vwr + (e.x >> 16);
+#pragma unroll
+            for (int i = 0; i < NI; ++i) {
+                const uint32_t c = ring[cur * kRow + 32 * i + lane];
+                const uint32_t arr = *reinterpret_cast<const uint32_t *>(vr + 128 * i) +
+                                     *reinterpret_cast<const uint32_t *>(cr + 128 * i);
+                const uint32_t st = max(fr[i], arr);
+                const uint32_t en = st + c;
+                flag[i] |= st | c;
+                busy[i] += c;
+                fr[i] = en;
+                *reinterpret_cast<uint32_t *>(vw + 128 * i) = en;
+                if constexpr (OPS) {
+                    const int64_t x = x0 + i * G::kIPW;
+                    if ((e.y & kLaneActive) && x < a.n) {
                         const int64_t off = x * a.o_inst + ((int64_t)k * a.O + cnt) * a.o_op;
                         if (a.op_start) a.op_start[off] = (int32_t)st;
                         if (a.op_end) a.op_end[off] = (int32_t)en;
                     }
-                    ++cnt;
                 }
             }
+            if constexpr (OPS) cnt += (e.y & kLaneActive) ? 1 : 0;
         };
         int q = 0;
 #pragma unroll 1
@@ -270,50 +292,55 @@ __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4
     // the window minus its busy time, the bubble is total idle over P
     // windows).  `flag` holds the sign bits of every start tick and cost: it
     // is clear exactly when no cost is negative and every tick fits in int32.
-    uint32_t mk = fr;
 #pragma unroll
-    for (int m = G::kIPW; m < 32; m <<= 1) {
-        mk = max(mk, __shfl_xor_sync(0xFFFFFFFFu, mk, m));
-        flag |= __shfl_xor_sync(0xFFFFFFFFu, flag, m);
-        ncomm |= __shfl_xor_sync(0xFFFFFFFFu, ncomm, m);
-    }
-    flag |= mk;
-    const int idle = k < a.P ? (int)(mk - busy) : 0;
-    int64_t num = idle;
+    for (int i = 0; i < NI; ++i) {
+        const int64_t x = x0 + i * G::kIPW;
+        uint32_t mk = fr[i], fl = flag[i], nc = ncomm[i];
 #pragma unroll
-    for (int m = G::kIPW; m < 32; m <<= 1) num += __shfl_xor_sync(0xFFFFFFFFu, num, m);
-    if (!live) return;
-    if (a.idle && k < a.P) a.idle[x * a.P + k] = idle;
-    if (k == 0) {
-        if (a.makespan) a.makespan[x] = (int)mk;
-        if (a.bub_num) a.bub_num[x] = num;
-        if (a.bub_den) a.bub_den[x] = (int64_t)a.P * (int)mk;
-        if (a.status) {
-            int8_t st = PP_ST_OK;
-            if (ncomm >> 31) st = PP_ST_NEG_COST;
-            else if (flag >> 31) st = any_negative_cost(a, x) ? PP_ST_NEG_COST : PP_ST_OVERFLOW;
-            a.status[x] = st;
+        for (int m = G::kIPW; m < 32; m <<= 1) {
+            mk = max(mk, __shfl_xor_sync(0xFFFFFFFFu, mk, m));
+            fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, m);
+            nc |= __shfl_xor_sync(0xFFFFFFFFu, nc, m);
+        }
+        fl |= mk;
+        const int idle = k < a.P ? (int)(mk - busy[i]) : 0;
+        int64_t num = idle;
+#pragma unroll
+        for (int m = G::kIPW; m < 32; m <<= 1) num += __shfl_xor_sync(0xFFFFFFFFu, num, m);
+        if (x >= a.n) continue;
+        if (a.idle && k < a.P) a.idle[x * a.P + k] = idle;
+        if (k == 0) {
+            if (a.makespan) a.makespan[x] = (int)mk;
+            if (a.bub_num) a.bub_num[x] = num;
+            if (a.bub_den) a.bub_den[x] = (int64_t)a.P * (int)mk;
+            if (a.status) {
+                int8_t st = PP_ST_OK;
+                if (nc >> 31) st = PP_ST_NEG_COST;
+                else if (fl >> 31) st = any_negative_cost(a, x) ? PP_ST_NEG_COST : PP_ST_OVERFLOW;
+                a.status[x] = st;
+            }
         }
     }
 }
 
 namespace {
 
-template <int PMAX>
+template <int PMAX, int NI>
 int lane_tables_t(pp_plan *plan, int64_t s_stage, int64_t s_mb, cudaStream_t stream, const pp_ktab **out) {
     using G = LaneGeom<PMAX>;
     std::lock_guard<std::mutex> lk(plan->ktab_mu);
     for (const pp_ktab &t : plan->ltabs)
-        if (t.s_stage == s_stage && t.s_mb == s_mb) { *out = &t; return PP_OK; }
+        if (t.s_stage == s_stage && t.s_mb == s_mb && t.variant == NI) { *out = &t; return PP_OK; }
     const int nblocks = (plan->R + G::kBR - 1) / G::kBR;
     pp_ktab t;
     t.s_stage = s_stage;
     t.s_mb = s_mb;
+    t.variant = NI;
     t.words = G::kHeadWords + nblocks * G::kBlockWords;
     PPS_CUDA_TRY(cudaMalloc(&t.d, (size_t)t.words * sizeof(uint32_t)));
     const int blocks = (t.words + 255) / 256;
     k_ltab<PMAX><<<blocks, 256, 0, stream>>>(plan->d_desc, plan->d_desc2, plan->R, plan->P, plan->v,
-                                             plan->nslots, (int)s_stage, (int)s_mb, nblocks,
+                                             plan->nslots, (int)s_stage, (int)s_mb, nblocks, 128 * NI,
                                              reinterpret_cast<uint32_t *>(t.d));
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
@@ -329,41 +356,54 @@ int lane_tables_t(pp_plan *plan, int64_t s_stage, int64_t s_mb, cudaStream_t str
 constexpr size_t kLaneSmemLimit = 227 * 1024;
 
 template <int PMAX>
-size_t lane_smem(const EvalArgs &a, int warps) {
+size_t lane_smem(const EvalArgs &a, int warps, int ni) {
     using G = LaneGeom<PMAX>;
     const size_t rows = (size_t)G::kSlices + a.nslots + 2 + 2 * a.v + 1;
-    return 2 * (size_t)G::kBlockWords * 4 + (size_t)warps * rows * 32 * 4;
+    return 2 * (size_t)G::kBlockWords * 4 + (size_t)warps * rows * 32 * ni * 4;
 }
 
-template <int PMAX, bool VEC, bool OPS>
+// Two instance sets per lane halve the per-op share of the table reads, the
+// loop and the warp barrier; they are used once the batch still gives the
+// GPU about eight such warps per SM.
+constexpr int64_t kLaneWarpsForTwoSets = 152 * 8;
+
+template <int PMAX, int NI, bool VEC, bool OPS>
 int launch_lane_t(const EvalArgs &a, const pp_ktab *t, cudaStream_t st) {
     using G = LaneGeom<PMAX>;
-    const int warps = lane_smem<PMAX>(a, 8) <= 100 * 1024 ? 8 : 4;
-    const size_t smem = lane_smem<PMAX>(a, warps);
+    const int warps = lane_smem<PMAX>(a, 8, NI) <= 100 * 1024 ? 8 : 4;
+    const size_t smem = lane_smem<PMAX>(a, warps, NI);
     int dev = 0;
     PPS_CUDA_TRY(cudaGetDevice(&dev));
     static bool attr_set[64] = {};
     if (dev < 64 && !attr_set[dev]) {
-        PPS_CUDA_TRY(cudaFuncSetAttribute(k_eval_lane<PMAX, VEC, OPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)kLaneSmemLimit));
+        PPS_CUDA_TRY(cudaFuncSetAttribute(k_eval_lane<PMAX, NI, VEC, OPS>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLaneSmemLimit));
         attr_set[dev] = true;
     }
-    const int64_t nw = (a.n + G::kIPW - 1) / G::kIPW;
+    const int64_t nw = (a.n + G::kIPW * NI - 1) / (G::kIPW * NI);
     const int64_t grid = (nw + warps - 1) / warps;
     if (grid > 0x7FFFFFFF) return PP_ERR_SIZE;
     const int nblocks = (a.R + G::kBR - 1) / G::kBR;
-    k_eval_lane<PMAX, VEC, OPS><<<(unsigned)grid, warps * 32, smem, st>>>(a, t->d, nblocks);
+    k_eval_lane<PMAX, NI, VEC, OPS><<<(unsigned)grid, warps * 32, smem, st>>>(a, t->d, nblocks);
     PPS_CUDA_TRY(cudaGetLastError());
     return PP_OK;
 }
 
+template <int PMAX, int NI>
+int launch_lane_n(pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st) {
+    const pp_ktab *t = nullptr;
+    const int rc = lane_tables_t<PMAX, NI>(plan, a.s_stage, a.s_mb, st, &t);
+    if (rc) return rc;
+    if (vec)
+        return ops ? launch_lane_t<PMAX, NI, true, true>(a, t, st) : launch_lane_t<PMAX, NI, true, false>(a, t, st);
+    return ops ? launch_lane_t<PMAX, NI, false, true>(a, t, st) : launch_lane_t<PMAX, NI, false, false>(a, t, st);
+}
+
 template <int PMAX>
 int launch_lane_p(pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st) {
-    const pp_ktab *t = nullptr;
-    const int rc = lane_tables_t<PMAX>(plan, a.s_stage, a.s_mb, st, &t);
-    if (rc) return rc;
-    if (vec) return ops ? launch_lane_t<PMAX, true, true>(a, t, st) : launch_lane_t<PMAX, true, false>(a, t, st);
-    return ops ? launch_lane_t<PMAX, false, true>(a, t, st) : launch_lane_t<PMAX, false, false>(a, t, st);
+    using G = LaneGeom<PMAX>;
+    const bool two = a.n / (2 * G::kIPW) >= kLaneWarpsForTwoSets && lane_smem<PMAX>(a, 4, 2) <= kLaneSmemLimit;
+    return two ? launch_lane_n<PMAX, 2>(plan, a, vec, ops, st) : launch_lane_n<PMAX, 1>(plan, a, vec, ops, st);
 }
 
 }  // namespace
@@ -375,9 +415,9 @@ bool lane_path(const pp_plan *plan, const EvalArgs &a) {
     if (!plan->d_desc2) return false;
     if ((int64_t)(a.S - 1) * a.s_stage + (int64_t)(a.M - 1) * a.s_mb >= ((int64_t)1 << 30)) return false;
     switch (plan->pmax) {
-        case 4: return lane_smem<4>(a, 4) <= kLaneSmemLimit;
-        case 8: return lane_smem<8>(a, 4) <= kLaneSmemLimit;
-        case 16: return lane_smem<16>(a, 4) <= kLaneSmemLimit;
+        case 4: return lane_smem<4>(a, 4, 1) <= kLaneSmemLimit;
+        case 8: return lane_smem<8>(a, 4, 1) <= kLaneSmemLimit;
+        case 16: return lane_smem<16>(a, 4, 1) <= kLaneSmemLimit;
         default: return false;
     }
 }

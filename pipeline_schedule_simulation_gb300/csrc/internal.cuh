@@ -74,8 +74,9 @@ inline int pmax_for(int P) { return P <= 4 ? 4 : (P <= 8 ? 8 : 16); }
 // into shared memory.
 struct pp_ktab {
     int64_t s_stage, s_mb;
-    uint4 *d;     // words / 4 uint4
-    int words;    // 32-bit words
+    uint4 *d;         // words / 4 uint4
+    int words;        // 32-bit words
+    int variant = 0;  // layout variant (lane evaluator: instance sets per lane)
 };
 
 // The plan object (opaque to callers).

@@ -84,6 +84,18 @@ def test_vector_rows_ragged_tail(orc, B, policy, P, M, v):
         assert_same(g, r, op_times=True)
 
 
+@pytest.mark.parametrize("P,M,v,n", [(4, 4, 2, 19456 + 37), (8, 8, 2, 9728 + 13), (16, 16, 2, 4864 + 3),
+                                     (3, 6, 3, 19456 + 5)])
+@pytest.mark.parametrize("layout", ["inst_minor", "inst_major"])
+def test_interleaved_two_sets_per_lane(orc, B, P, M, v, n, layout):
+    """Batches large enough for the lane evaluator's two-instance-set layout
+    (about eight warps per SM), with a ragged last warp, every op time."""
+    batch = W.random_batch(W.INTERLEAVED, P, M, v, n, seed=P * 100 + M, hi=30, comm_hi=6, layout=layout, pad_to=4)
+    g = run_gpu(batch, op_times=True)
+    r = run_oracle(orc, batch, op_times=True)
+    assert_same(g, r, op_times=True)
+
+
 def test_status_interleaved(orc, B):
     P, M, v, n = 4, 8, 2, 70
     S = P * v
