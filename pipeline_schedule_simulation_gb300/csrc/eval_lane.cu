@@ -11,10 +11,13 @@
 // Ops of one round are independent, so all lanes of a round run in parallel
 // and one __syncwarp per round publishes the round's results.
 //
-// Per warp, in shared memory, every row is 32 words with column = lane:
+// Per warp, in shared memory, every row is 32 words per instance set (see
+// k_eval_lane) with column = lane:
 //   ring   kSlices rows  cost of this lane's op, filled kAhead rounds ahead
 //   val    nslots rows + a zero row + a scratch row: an op's end tick is
-//          written into its consumer device's column of its value slot
+//          written into its consumer device's column of its value slot;
+//          slots are coloured per consumer device (k_cslots), so nslots is
+//          the most inputs one device has in flight, not the plan's total
 //   ctab   2v rows + a zero row: the comm latency on the input edge of this
 //          lane's ops, row 2c for a forward of chunk c (boundary s-1|s) and
 //          row 2c+1 for a backward (boundary s|s+1)
@@ -25,13 +28,16 @@
 // The per-(round, device) table (built once per plan and stride pair by
 // k_ltab) is streamed through the CTA in blocks of kBR rounds, double
 // buffered with cp.async and published with one __syncthreads per block.
-// Entry (round r, device k):
-//   cw.x  low 16 bits: byte offset of the input slot cell (row*128 + column)
-//         high 16 bits: byte offset of the output slot cell
-//   cw.y  low 16 bits: byte offset of the comm cell; bit 31: op is not idle
-//   lt    loader entry of round r + kAhead: byte offset of the op's cost
-//         row | 1 for a backward op, or kLtIdle; shifted by kAhead rounds so
-//         the loader never needs the next block
+// Entry (round r, device k), one uint4 read by the device's lanes at once:
+//   x  byte offset of the input slot cell (row * row bytes + column)
+//   y  byte offset of the comm cell
+//   z  byte offset of the output slot cell; bit 31 set when the op is not idle
+//   w  loader entry of round r + kAhead: byte offset of the op's cost row
+//      | 1 for a backward op, or kLtIdle; shifted by kAhead rounds so the
+//      loader never needs the next block
+#include <algorithm>
+#include <climits>
+
 #include "eval_common.cuh"
 
 namespace pps {
@@ -42,7 +48,7 @@ struct LaneGeom {
     static constexpr int kSlices = 8;                   // cost ring rows
     static constexpr int kAhead = kSlices - 2;          // rounds loaded ahead
     static constexpr int kBR = 512 / PMAX;              // rounds per table block
-    static constexpr int kBlockWords = 3 * kBR * PMAX;  // cw (2 words) + lt per entry
+    static constexpr int kBlockWords = 4 * kBR * PMAX;  // one uint4 per entry
     static constexpr int kHeadWords = (kAhead * PMAX + 3) & ~3;
     static constexpr int kCopy = kIPW < 4 ? kIPW : 4;   // instances per loader copy (vector path)
     static_assert(kBR > kAhead, "a table block must outlast the loader's lead");
@@ -69,7 +75,7 @@ __device__ __forceinline__ uint32_t lane_lt(const uint32_t *desc, int R, int P, 
 // rounds 0 .. kAhead-1), then ceil(R / kBR) blocks laid out as described at
 // the top of the file.
 template <int PMAX>
-__global__ void k_ltab(const uint32_t *desc, const uint32_t *desc2, int R, int P, int v, int nslots,
+__global__ void k_ltab(const uint32_t *desc, const uint8_t *lrd, const uint8_t *lwr, int R, int P, int v, int nslots,
                        int s_stage, int s_mb, int nblocks, uint32_t row_bytes, uint32_t *out) {
     using G = LaneGeom<PMAX>;
     const int64_t total = G::kHeadWords + (int64_t)nblocks * G::kBlockWords;
@@ -83,19 +89,20 @@ __global__ void k_ltab(const uint32_t *desc, const uint32_t *desc2, int R, int P
             const int64_t e2 = e - G::kHeadWords;
             const int b = (int)(e2 / G::kBlockWords);
             const int o = (int)(e2 % G::kBlockWords);
-            if (o < 2 * G::kBR * PMAX) {
-                const int idx = o >> 1, q = idx / PMAX, k = idx % PMAX, r = b * G::kBR + q;
+            const int idx = o >> 2, q = idx / PMAX, k = idx % PMAX, r = b * G::kBR + q;
+            if ((o & 3) == 3) {
+                w = lane_lt(desc, R, P, PMAX, r + G::kAhead, k, s_stage, s_mb);
+            } else {
                 const uint32_t col = (uint32_t)(k * G::kIPW * 4);
-                const uint32_t zero = (uint32_t)nslots * row_bytes + col;
-                const uint32_t scratch = (uint32_t)(nslots + 1) * row_bytes + col;
-                uint32_t rd = zero, wr = scratch, cm = (uint32_t)(2 * v) * row_bytes + col, act = 0;
+                uint32_t rd = (uint32_t)nslots * row_bytes + col;           // zero row
+                uint32_t wr = (uint32_t)(nslots + 1) * row_bytes + col;     // scratch row
+                uint32_t cm = (uint32_t)(2 * v) * row_bytes + col, act = 0;  // zero comm row
                 if (r < R) {
                     const uint32_t d = desc[(int64_t)r * PMAX + k];
                     const uint32_t kind = desc_kind(d);
                     if (kind != kIdle) {
                         act = kLaneActive;
-                        const uint32_t d2 = desc2[(int64_t)r * PMAX + k];
-                        const uint32_t rs = d2_rslot(d2), ws = d2_wslot(d2);
+                        const uint32_t rs = lrd[(int64_t)r * PMAX + k], ws = lwr[(int64_t)r * PMAX + k];
                         if (rs != kNoSlot) {
                             rd = rs * row_bytes + col;
                             cm = (2u * desc_chunk(d) + (kind == kBwd ? 1u : 0u)) * row_bytes + col;
@@ -106,53 +113,69 @@ __global__ void k_ltab(const uint32_t *desc, const uint32_t *desc2, int R, int P
                         }
                     }
                 }
-                w = (o & 1) ? (cm | act) : (rd | (wr << 16));
-            } else {
-                const int idx = o - 2 * G::kBR * PMAX, q = idx / PMAX, k = idx % PMAX;
-                w = lane_lt(desc, R, P, PMAX, b * G::kBR + q + G::kAhead, k, s_stage, s_mb);
+                w = (o & 3) == 0 ? rd : ((o & 3) == 1 ? cm : (wr | act));
             }
         }
         out[e] = w;
     }
 }
 
-// This lane's share of the cost copies, for each of its NI instances.
-// Vector path: the lanes of instance 0, 4, ... of each device copy kCopy
-// consecutive instances (16 or 8 bytes); scalar path: every lane copies its
-// own word.  Instance set i lands in ring row `dst` at column 32*i + lane
-// (layout [device][instance]).  Everything but the row offset is fixed per
-// lane, so a round costs a select, an add and one predicated cp.async per set.
+// This lane's share of a round's cost copies.  Vector path: a device row of
+// the warp holds NI * 32/PMAX consecutive instances per set, copied in
+// pieces of kCopy instances (16 or 8 bytes) by the device's first lanes, one
+// piece each.  Scalar path: every lane copies its own word of each set.  Set
+// i lands in the ring row at column 32*i + lane (layout [device][instance]).
+// Everything but the row offset is fixed per lane, so a round costs a select,
+// an add and one predicated cp.async per copy.
 template <int PMAX, int NI, bool VEC>
 struct LaneLoader {
-    const char *fb, *bb;   // this lane's first element of set 0 in cost_f / cost_b
-    int64_t step[NI];      // byte distance from set 0 to set i (0 where set i copies nothing)
-    uint32_t bytes[NI];    // bytes copied for a non-idle op (0 past the last instance)
+    static constexpr int kN = VEC ? 1 : NI;  // copies per lane and round
+    const char *fb, *bb;   // this lane's first source element in cost_f / cost_b
+    int64_t step[kN];      // byte distance from copy 0's source to copy i's (0 if it copies nothing)
+    uint32_t bytes[kN];    // bytes of a non-idle op's copy (0 past the last instance)
+    uint32_t doff[kN];     // byte offset of the copy in the ring row
     uint32_t on;           // this lane issues copies
 
-    __device__ __forceinline__ LaneLoader(const EvalArgs &a, int j, int64_t x0) {
+    __device__ __forceinline__ LaneLoader(const EvalArgs &a, int lane, int j, int k, int64_t inst0) {
         using G = LaneGeom<PMAX>;
-        const int64_t e0 = x0 < a.n ? (VEC ? x0 : x0 * a.s_inst) : 0;
-        fb = reinterpret_cast<const char *>(a.cost_f + e0);
-        bb = reinterpret_cast<const char *>(a.cost_b + e0);
-        on = VEC ? (j % G::kCopy) == 0 : 1;
+        if constexpr (VEC) {
+            constexpr int kPerSet = G::kIPW / G::kCopy;
+            const int set = j / kPerSet, piece = j % kPerSet;
+            on = j < NI * kPerSet;
+            const int64_t xi = inst0 + set * G::kIPW + piece * G::kCopy;
+            const int64_t left = a.n - xi;
+            const int64_t e0 = on && left > 0 ? xi : 0;
+            fb = reinterpret_cast<const char *>(a.cost_f + e0);
+            bb = reinterpret_cast<const char *>(a.cost_b + e0);
+            bytes[0] = !on || left <= 0 ? 0u : (uint32_t)(left < G::kCopy ? left : G::kCopy) * 4u;
+            step[0] = 0;
+            doff[0] = (uint32_t)(set * 32 + k * G::kIPW + piece * G::kCopy) * 4u;
+        } else {
+            const int64_t x0 = inst0 + j;
+            const int64_t e0 = x0 < a.n ? x0 * a.s_inst : 0;
+            fb = reinterpret_cast<const char *>(a.cost_f + e0);
+            bb = reinterpret_cast<const char *>(a.cost_b + e0);
+            on = 1;
 #pragma unroll
-        for (int i = 0; i < NI; ++i) {
-            const int64_t left = a.n - (x0 + i * G::kIPW);
-            const int64_t per = VEC ? G::kCopy : 1;
-            bytes[i] = left <= 0 ? 0u : (uint32_t)(left < per ? left : per) * 4u;
-            step[i] = bytes[i] ? (int64_t)i * G::kIPW * (VEC ? 1 : a.s_inst) * 4 : 0;
+            for (int i = 0; i < NI; ++i) {
+                const bool in = x0 + i * G::kIPW < a.n;
+                bytes[i] = in ? 4u : 0u;
+                step[i] = in ? (int64_t)i * G::kIPW * a.s_inst * 4 : 0;
+                doff[i] = (uint32_t)(32 * i + lane) * 4u;
+            }
         }
     }
 
-    __device__ __forceinline__ void issue(uint32_t lt, uint32_t dst) const {
+    // lt: the loader entry of the round; row: shared address of the ring row
+    __device__ __forceinline__ void issue(uint32_t lt, uint32_t row) const {
         using G = LaneGeom<PMAX>;
         const bool idle = lt == kLtIdle;
         const char *src = ((lt & 1u) ? bb : fb) + (idle ? 0u : (lt & ~3u));
 #pragma unroll
-        for (int i = 0; i < NI; ++i) {
+        for (int i = 0; i < kN; ++i) {
             const char *s = src + step[i];
             const uint32_t nb = idle ? 0u : bytes[i];
-            const uint32_t d = dst + 128 * i;
+            const uint32_t d = row + doff[i];
             if constexpr (VEC && G::kCopy == 4)
                 asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %3, 0;\n"
                              " @p cp.async.cg.shared.global [%0], [%1], 16, %2;\n}\n" ::"r"(d), "l"(s), "r"(nb),
@@ -199,8 +222,8 @@ __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4
     lane_copy_block<PMAX>(blocks, 0, lsm);
     cp_async_commit();
     const uint32_t *head = reinterpret_cast<const uint32_t *>(tab);
-    const LaneLoader<PMAX, NI, VEC> ld(a, j, x0);
-    const uint32_t ring_s = smem_addr(ring + lane);
+    const LaneLoader<PMAX, NI, VEC> ld(a, lane, j, k, inst0);
+    const uint32_t ring_s = smem_addr(ring);
 #pragma unroll 1
     for (int q = 0; q < G::kAhead; ++q) {
         ld.issue(__ldg(head + q * PMAX + k), ring_s + q * kRow * 4);
@@ -238,21 +261,20 @@ __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4
     for (int b = 0; b < nblocks; ++b) {
         const uint32_t *tbl = lsm + (b & 1) * G::kBlockWords;
         if (b + 1 < nblocks) lane_copy_block<PMAX>(blocks, b + 1, lsm + ((b + 1) & 1) * G::kBlockWords);
-        const uint2 *cw = reinterpret_cast<const uint2 *>(tbl) + k;
-        const uint32_t *lt = tbl + 2 * G::kBR * PMAX + k;
+        const uint4 *ent = reinterpret_cast<const uint4 *>(tbl) + k;
         const int n_r = min(R - b * G::kBR, G::kBR);
         // one round: the loader runs kAhead rounds ahead into ring row nxt,
         // the op reads its cost from row cur (rows are round mod kSlices; a
         // block starts at a multiple of kSlices)
         auto round = [&](int q, int cur, int nxt) {
-            const uint2 e = cw[q * PMAX];
-            ld.issue(lt[q * PMAX], ring_s + nxt * kRow * 4);
+            const uint4 e = ent[q * PMAX];
+            ld.issue(e.w, ring_s + nxt * kRow * 4);
             cp_async_commit();
             cp_async_wait<G::kAhead>();
             __syncwarp();
-            const char *vr = vrd + (e.x & 0xFFFFu);
-            const char *cr = crd + (e.y & 0xFFFFu);
-            char *vw = vwr + (e.x >> 16);
+            const char *vr = vrd + e.x;
+            const char *cr = crd + e.y;
+            char *vw = vwr + (e.z & ~kLaneActive);
 #pragma unroll
             for (int i = 0; i < NI; ++i) {
                 const uint32_t c = ring[cur * kRow + 32 * i + lane];
@@ -266,14 +288,14 @@ __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4
                 *reinterpret_cast<uint32_t *>(vw + 128 * i) = en;
                 if constexpr (OPS) {
                     const int64_t x = x0 + i * G::kIPW;
-                    if ((e.y & kLaneActive) && x < a.n) {
+                    if ((e.z & kLaneActive) && x < a.n) {
                         const int64_t off = x * a.o_inst + ((int64_t)k * a.O + cnt) * a.o_op;
                         if (a.op_start) a.op_start[off] = (int32_t)st;
                         if (a.op_end) a.op_end[off] = (int32_t)en;
                     }
                 }
             }
-            if constexpr (OPS) cnt += (e.y & kLaneActive) ? 1 : 0;
+            if constexpr (OPS) cnt += (e.z & kLaneActive) ? 1 : 0;
         };
         int q = 0;
 #pragma unroll 1
@@ -339,8 +361,9 @@ int lane_tables_t(pp_plan *plan, int64_t s_stage, int64_t s_mb, cudaStream_t str
     t.words = G::kHeadWords + nblocks * G::kBlockWords;
     PPS_CUDA_TRY(cudaMalloc(&t.d, (size_t)t.words * sizeof(uint32_t)));
     const int blocks = (t.words + 255) / 256;
-    k_ltab<PMAX><<<blocks, 256, 0, stream>>>(plan->d_desc, plan->d_desc2, plan->R, plan->P, plan->v,
-                                             plan->nslots, (int)s_stage, (int)s_mb, nblocks, 128 * NI,
+    const int64_t cells = (int64_t)plan->R * PMAX;
+    k_ltab<PMAX><<<blocks, 256, 0, stream>>>(plan->d_desc, plan->d_lslot, plan->d_lslot + cells, plan->R, plan->P,
+                                             plan->v, plan->nlslots, (int)s_stage, (int)s_mb, nblocks, 128 * NI,
                                              reinterpret_cast<uint32_t *>(t.d));
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
@@ -367,11 +390,49 @@ size_t lane_smem(const EvalArgs &a, int warps, int ni) {
 // GPU about eight such warps per SM.
 constexpr int64_t kLaneWarpsForTwoSets = 152 * 8;
 
+// SMs of the current device (cached per device).
+int sm_count(int dev) {
+    static int cached[64] = {};
+    if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+        (void)cudaGetLastError();
+        n = 1;
+    }
+    if (dev >= 0 && dev < 64) cached[dev] = n;
+    return n;
+}
+
+// Warps per CTA: every CTA copies the whole table, so larger CTAs are
+// cheaper, but a batch of a few thousand warps is one wave of CTAs and the
+// busiest SM sets the time.  Take the size (8, 4 or 2 warps) whose busiest
+// SM holds the fewest warps with every CTA resident at once, the larger size
+// on a tie; with more than one wave, the largest size that fits.
+template <int PMAX, int NI, bool VEC, bool OPS>
+int lane_warps(const EvalArgs &a, int64_t warps_total, int sms) {
+    int best = 0;
+    int64_t best_load = 0;
+    for (int w = 8; w >= 2; w >>= 1) {
+        const size_t smem = lane_smem<PMAX>(a, w, NI);
+        if (smem > kLaneSmemLimit) continue;
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_eval_lane<PMAX, NI, VEC, OPS>, w * 32, smem) !=
+            cudaSuccess) {
+            (void)cudaGetLastError();
+            continue;
+        }
+        if (per_sm < 1) continue;
+        const int64_t ctas = (warps_total + w - 1) / w;
+        const int64_t need = (ctas + sms - 1) / sms;  // CTAs on the busiest SM
+        const int64_t load = need > per_sm ? INT64_MAX : need * w;
+        if (!best || load < best_load) { best = w; best_load = load; }
+    }
+    return best;
+}
+
 template <int PMAX, int NI, bool VEC, bool OPS>
 int launch_lane_t(const EvalArgs &a, const pp_ktab *t, cudaStream_t st) {
     using G = LaneGeom<PMAX>;
-    const int warps = lane_smem<PMAX>(a, 8, NI) <= 100 * 1024 ? 8 : 4;
-    const size_t smem = lane_smem<PMAX>(a, warps, NI);
     int dev = 0;
     PPS_CUDA_TRY(cudaGetDevice(&dev));
     static bool attr_set[64] = {};
@@ -381,6 +442,9 @@ int launch_lane_t(const EvalArgs &a, const pp_ktab *t, cudaStream_t st) {
         attr_set[dev] = true;
     }
     const int64_t nw = (a.n + G::kIPW * NI - 1) / (G::kIPW * NI);
+    const int warps = lane_warps<PMAX, NI, VEC, OPS>(a, nw, sm_count(dev));
+    if (!warps) return PP_ERR_SIZE;
+    const size_t smem = lane_smem<PMAX>(a, warps, NI);
     const int64_t grid = (nw + warps - 1) / warps;
     if (grid > 0x7FFFFFFF) return PP_ERR_SIZE;
     const int nblocks = (a.R + G::kBR - 1) / G::kBR;
@@ -402,27 +466,31 @@ int launch_lane_n(pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStre
 template <int PMAX>
 int launch_lane_p(pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st) {
     using G = LaneGeom<PMAX>;
-    const bool two = a.n / (2 * G::kIPW) >= kLaneWarpsForTwoSets && lane_smem<PMAX>(a, 4, 2) <= kLaneSmemLimit;
+    const bool two = a.n / (2 * G::kIPW) >= kLaneWarpsForTwoSets && lane_smem<PMAX>(a, 2, 2) <= kLaneSmemLimit;
     return two ? launch_lane_n<PMAX, 2>(plan, a, vec, ops, st) : launch_lane_n<PMAX, 1>(plan, a, vec, ops, st);
 }
 
 }  // namespace
 
 // The lane evaluator applies when the plan has value slots, every cost-row
-// offset fits the loader table (below 2^30 elements) and a 4-warp CTA fits in
+// offset fits the loader table (below 2^30 elements) and a 2-warp CTA fits in
 // shared memory.
-bool lane_path(const pp_plan *plan, const EvalArgs &a) {
-    if (!plan->d_desc2) return false;
+bool lane_path(const pp_plan *plan, const EvalArgs &args) {
+    if (!plan->d_lslot) return false;
+    EvalArgs a = args;
+    a.nslots = plan->nlslots;
     if ((int64_t)(a.S - 1) * a.s_stage + (int64_t)(a.M - 1) * a.s_mb >= ((int64_t)1 << 30)) return false;
     switch (plan->pmax) {
-        case 4: return lane_smem<4>(a, 4, 1) <= kLaneSmemLimit;
-        case 8: return lane_smem<8>(a, 4, 1) <= kLaneSmemLimit;
-        case 16: return lane_smem<16>(a, 4, 1) <= kLaneSmemLimit;
+        case 4: return lane_smem<4>(a, 2, 1) <= kLaneSmemLimit;
+        case 8: return lane_smem<8>(a, 2, 1) <= kLaneSmemLimit;
+        case 16: return lane_smem<16>(a, 2, 1) <= kLaneSmemLimit;
         default: return false;
     }
 }
 
-int launch_eval_lane(pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st) {
+int launch_eval_lane(pp_plan *plan, const EvalArgs &args, bool vec, bool ops, cudaStream_t st) {
+    EvalArgs a = args;
+    a.nslots = plan->nlslots;  // the lane evaluator's rows hold per-consumer slots
     switch (plan->pmax) {
         case 4: return launch_lane_p<4>(plan, a, vec, ops, st);
         case 8: return launch_lane_p<8>(plan, a, vec, ops, st);

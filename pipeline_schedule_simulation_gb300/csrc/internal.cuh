@@ -85,12 +85,14 @@ struct pp_plan {
     int R;              // rounds
     int pmax;           // row width of the per-round tables
     int nslots;         // value slots of the generic evaluator
+    int nlslots;        // per-consumer value slots of the lane evaluator
     int reg_ok;         // 1 if the register evaluator applies
     int device;         // CUDA device the tables live on
     uint32_t *d_ops;    // [P][O] packed ops (PP_OP_* layout)
     int32_t *d_round;   // [P][O] wavefront round of each op
     uint32_t *d_desc;   // [R][pmax]
     uint32_t *d_desc2;  // [R][pmax] (generic evaluator), may be null
+    uint8_t *d_lslot;   // [2][R][pmax] lane evaluator's local read / write slots (with d_desc2)
     uint64_t *d_rw;     // [R] per-round kind words and patterns
     uint4 *d_seg;       // [nseg] segments (register evaluator)
     int nseg;

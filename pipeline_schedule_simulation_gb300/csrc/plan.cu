@@ -269,6 +269,61 @@ __global__ void k_slots(const uint32_t *desc, int R, int P, int M, int v, int pm
     info[3] = nmax;
 }
 
+// Per-consumer value slots for the lane evaluator.  Every in-flight result
+// has one consumer op, on device (k+1) mod P for a forward and (k-1) mod P
+// for a backward.  The lane evaluator keeps a result in its consumer
+// device's column, so results with different consumers never share a cell
+// and each consumer device colours only its own inputs; that needs far fewer
+// rows than the plan-wide colouring of k_slots.  One warp, lane kc colours
+// the inputs of device kc in round order, mapping each in-flight result
+// from its plan-wide slot (unique while it is in flight) to a local one, and
+// frees a local slot at the end of the round that consumes it.  Writes
+// lrd[r][k] (local slot read by op (r,k)) for k = kc, lwr[r][k] (local slot
+// op (r,k) writes) for producers whose consumer is kc; 0xFF where none.
+// info[7] = local slots used (the maximum over devices), -1 on exhaustion.
+__global__ void k_cslots(const uint32_t *desc, const uint32_t *desc2, int R, int P, int pmax, uint8_t *lrd,
+                         uint8_t *lwr, int32_t *info) {
+    __shared__ uint8_t loc[32][kMaxValueSlots];
+    const int kc = threadIdx.x;
+    uint64_t used = 0;
+    int nmax = 0;
+    bool bad = false;
+    if (kc < P) {
+        for (int r = 0; r < R && !bad; ++r) {
+            uint64_t freed = 0;
+            const int64_t row = (int64_t)r * pmax;
+            uint8_t rd = 0xFF;
+            if (desc_kind(desc[row + kc]) != kIdle) {
+                const uint32_t rs = d2_rslot(desc2[row + kc]);
+                if (rs != kNoSlot) {
+                    rd = loc[kc][rs];
+                    freed |= 1ull << rd;
+                }
+            }
+            lrd[row + kc] = rd;
+            for (int k = 0; k < P; ++k) {
+                const uint32_t kind = desc_kind(desc[row + k]);
+                if (kind == kIdle) continue;
+                const uint32_t ws = d2_wslot(desc2[row + k]);
+                if (ws == kNoSlot) continue;
+                const int cons = kind == kFwd ? (k + 1) % P : (k + P - 1) % P;
+                if (cons != kc) continue;
+                if (used == ~0ull) { bad = true; break; }
+                const int b = __ffsll((long long)~used) - 1;
+                used |= 1ull << b;
+                nmax = max(nmax, b + 1);
+                loc[kc][ws] = (uint8_t)b;
+                lwr[row + k] = (uint8_t)b;
+            }
+            used &= ~freed;
+        }
+    }
+    const unsigned any_bad = __ballot_sync(0xFFFFFFFFu, bad);
+#pragma unroll
+    for (int m = 16; m; m >>= 1) nmax = max(nmax, __shfl_xor_sync(0xFFFFFFFFu, nmax, m));
+    if (threadIdx.x == 0) info[7] = any_bad ? -1 : nmax;
+}
+
 // Fill the register evaluator's tables for one stride pair: loader table
 // entries (element offset of the op's cost row, shifted left by one, bit 0 set
 // for a backward op; all ones for an idle slot), then the round words, then
@@ -331,7 +386,7 @@ static int build_plan(int policy, int P, int M, int v, cudaStream_t st, pp_plan 
     if (rc) return rc;
     const int S = P * v, O = 2 * M * v, pmax = pmax_for(P);
     const int64_t nops = (int64_t)P * O, npos = 2LL * S * M;
-    DevBuf ops, pos, round, info, peak, desc, desc2, slot_of, rw, seg;
+    DevBuf ops, pos, round, info, peak, desc, desc2, slot_of, rw, seg, lslot;
     PPS_CUDA_TRY(cudaMalloc(&ops.p, nops * sizeof(uint32_t)));
     PPS_CUDA_TRY(cudaMalloc(&pos.p, npos * sizeof(int32_t)));
     PPS_CUDA_TRY(cudaMalloc(&round.p, nops * sizeof(int32_t)));
@@ -370,7 +425,7 @@ static int build_plan(int policy, int P, int M, int v, cudaStream_t st, pp_plan 
         PPS_CUDA_TRY(cudaStreamSynchronize(st));
         reg_ok = h_info[2] == 0;
     }
-    int nslots = 0;
+    int nslots = 0, nlslots = 0;
     if (!reg_ok) {
         PPS_CUDA_TRY(cudaMalloc(&desc2.p, (int64_t)R * pmax * sizeof(uint32_t)));
         PPS_CUDA_TRY(cudaMalloc(&slot_of.p, npos * sizeof(int32_t)));
@@ -383,10 +438,21 @@ static int build_plan(int policy, int P, int M, int v, cudaStream_t st, pp_plan 
         if (h_info[5]) return PP_ERR_INTERNAL;
         if (h_info[4]) return PP_ERR_SIZE;
         nslots = h_info[3];
+        // per-consumer slots of the lane evaluator: lrd then lwr, [R][pmax] bytes each
+        const int64_t cells = (int64_t)R * pmax;
+        PPS_CUDA_TRY(cudaMalloc(&lslot.p, 2 * cells));
+        PPS_CUDA_TRY(cudaMemsetAsync(lslot.p, 0xFF, 2 * cells, st));
+        k_cslots<<<1, 32, 0, st>>>(desc.as<uint32_t>(), desc2.as<uint32_t>(), R, P, pmax, lslot.as<uint8_t>(),
+                                   lslot.as<uint8_t>() + cells, info.as<int32_t>());
+        PPS_CUDA_TRY(cudaGetLastError());
+        PPS_CUDA_TRY(cudaMemcpyAsync(h_info, info.p, sizeof(h_info), cudaMemcpyDeviceToHost, st));
+        PPS_CUDA_TRY(cudaStreamSynchronize(st));
+        if (h_info[7] < 0) return PP_ERR_INTERNAL;
+        nlslots = h_info[7];
     }
     pp_plan *p = new pp_plan();
     p->policy = policy; p->P = P; p->M = M; p->v = v; p->S = S; p->O = O;
-    p->R = R; p->pmax = pmax; p->nslots = nslots; p->reg_ok = reg_ok;
+    p->R = R; p->pmax = pmax; p->nslots = nslots; p->nlslots = nlslots; p->reg_ok = reg_ok;
     PPS_CUDA_TRY(cudaGetDevice(&p->device));
     if (cudaMemcpyAsync(p->h_peak, peak.p, P * sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
         cudaStreamSynchronize(st) != cudaSuccess) {
@@ -397,6 +463,7 @@ static int build_plan(int policy, int P, int M, int v, cudaStream_t st, pp_plan 
     p->d_round = round.as<int32_t>(); round.p = nullptr;
     p->d_desc = desc.as<uint32_t>(); desc.p = nullptr;
     p->d_desc2 = desc2.as<uint32_t>(); desc2.p = nullptr;
+    p->d_lslot = lslot.as<uint8_t>(); lslot.p = nullptr;
     p->d_rw = rw.as<uint64_t>(); rw.p = nullptr;
     p->d_seg = seg.as<uint4>(); seg.p = nullptr;
     p->nseg = h_info[6];
@@ -554,6 +621,7 @@ void pp_sched_plan_destroy(pp_plan_t *p) {
     cudaFree(p->d_round);
     cudaFree(p->d_desc);
     if (p->d_desc2) cudaFree(p->d_desc2);
+    if (p->d_lslot) cudaFree(p->d_lslot);
     cudaFree(p->d_rw);
     cudaFree(p->d_seg);
     for (pp_ktab &t : p->ktabs) cudaFree(t.d);
