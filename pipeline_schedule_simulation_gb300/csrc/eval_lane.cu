@@ -190,6 +190,22 @@ struct LaneLoader {
     }
 };
 
+// Shared-memory accesses by 32-bit shared-window address.
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.u32 [%0], %1;\n" ::"r"(addr), "r"(v) : "memory");
+}
+
 // Copy table block `b` into `dst` (all threads of the CTA; joins the caller's
 // next commit group).
 template <int PMAX>
@@ -250,42 +266,41 @@ __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4
     cp_async_wait<G::kAhead>();
     __syncthreads();
 
-    const char *vrd = reinterpret_cast<const char *>(val + j);
-    char *vwr = reinterpret_cast<char *>(val + j);
-    const char *crd = reinterpret_cast<const char *>(ctab + j);
+    const uint32_t val_s = smem_addr(val + j), ctab_s = smem_addr(ctab + j), cost_s = smem_addr(ring + lane);
     uint32_t fr[NI], busy[NI], flag[NI];
 #pragma unroll
     for (int i = 0; i < NI; ++i) { fr[i] = 0; busy[i] = 0; flag[i] = 0; }
     int cnt = 0;
 #pragma unroll 1
     for (int b = 0; b < nblocks; ++b) {
-        const uint32_t *tbl = lsm + (b & 1) * G::kBlockWords;
         if (b + 1 < nblocks) lane_copy_block<PMAX>(blocks, b + 1, lsm + ((b + 1) & 1) * G::kBlockWords);
-        const uint4 *ent = reinterpret_cast<const uint4 *>(tbl) + k;
+        const uint32_t ent_s = smem_addr(lsm + (b & 1) * G::kBlockWords) + k * 16;
         const int n_r = min(R - b * G::kBR, G::kBR);
-        // one round: the loader runs kAhead rounds ahead into ring row nxt,
+        // One round: the loader runs kAhead rounds ahead into ring row nxt,
         // the op reads its cost from row cur (rows are round mod kSlices; a
-        // block starts at a multiple of kSlices)
+        // block starts at a multiple of kSlices).  The next round's entry is
+        // read one round early; past the block's last round that read lands
+        // in the other table buffer or the first warp's ring (still inside
+        // the CTA's shared memory) and is discarded.
+        uint4 nx = lds128(ent_s);
         auto round = [&](int q, int cur, int nxt) {
-            const uint4 e = ent[q * PMAX];
+            const uint4 e = nx;
+            nx = lds128(ent_s + (q + 1) * PMAX * 16);
             ld.issue(e.w, ring_s + nxt * kRow * 4);
             cp_async_commit();
             cp_async_wait<G::kAhead>();
             __syncwarp();
-            const char *vr = vrd + e.x;
-            const char *cr = crd + e.y;
-            char *vw = vwr + (e.z & ~kLaneActive);
+            const uint32_t vr = val_s + e.x, cr = ctab_s + e.y, vw = val_s + (e.z & ~kLaneActive);
 #pragma unroll
             for (int i = 0; i < NI; ++i) {
-                const uint32_t c = ring[cur * kRow + 32 * i + lane];
-                const uint32_t arr = *reinterpret_cast<const uint32_t *>(vr + 128 * i) +
-                                     *reinterpret_cast<const uint32_t *>(cr + 128 * i);
+                const uint32_t c = lds32(cost_s + (cur * kRow + 32 * i) * 4);
+                const uint32_t arr = lds32(vr + 128 * i) + lds32(cr + 128 * i);
                 const uint32_t st = max(fr[i], arr);
                 const uint32_t en = st + c;
                 flag[i] |= st | c;
                 busy[i] += c;
                 fr[i] = en;
-                *reinterpret_cast<uint32_t *>(vw + 128 * i) = en;
+                sts32(vw + 128 * i, en);
                 if constexpr (OPS) {
                     const int64_t x = x0 + i * G::kIPW;
                     if ((e.z & kLaneActive) && x < a.n) {
