@@ -25,12 +25,12 @@ _SRC = os.path.join(_HERE, "ppsim_oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libppsim_oracle.so")
 
-GPIPE, ONEF1B, INTERLEAVED = 0, 1, 2
-POLICIES = {"gpipe": GPIPE, "1f1b": ONEF1B, "interleaved": INTERLEAVED}
-F, B = 0, 1
+GPIPE, ONEF1B, INTERLEAVED, ZB1P, ZB2P = 0, 1, 2, 3, 4
+POLICIES = {"gpipe": GPIPE, "1f1b": ONEF1B, "interleaved": INTERLEAVED, "zb1p": ZB1P, "zb2p": ZB2P}
+F, B, W = 0, 1, 2
 
 OK, ERR_ARG, ERR_DIVISIBILITY, ERR_DEADLOCK, ERR_INVARIANT, ERR_NOMEM = 0, 1, 2, 5, 6, 7
-ST_OK, ST_NEG_COST, ST_OVERFLOW = 0, 1, 2
+ST_OK, ST_NEG_COST, ST_OVERFLOW, ST_ZERO_COST = 0, 1, 2, 3
 
 _lock = threading.Lock()
 _lib = None
@@ -80,6 +80,11 @@ def _bind(lib):
     lib.orc_binom.restype = c_u64
     lib.orc_splitmix64.argtypes = [c_u64]
     lib.orc_splitmix64.restype = c_u64
+    lib.orc_zb_inst.argtypes = [c_int, c_int, c_int, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.orc_zb_inst.restype = c_int
+    lib.orc_zb_batch.argtypes = [c_int, c_int, c_int, c_i64, vp, vp, vp, c_i64, c_i64, c_i64,
+                                 vp, c_i64, c_i64, vp, vp, vp, vp, vp, vp, vp, vp, c_int]
+    lib.orc_zb_batch.restype = c_int
     del i32p, i64p
     return lib
 
@@ -233,3 +238,62 @@ def binom(n, k, lib=None):
 
 def splitmix64(state, lib=None):
     return int((lib or load()).orc_splitmix64(ctypes.c_uint64(state & (2**64 - 1))))
+
+
+def zb_evaluate(policy, P, M, tf, tb, tw, comm=None, lib=None):
+    """One Zero Bubble instance (ZB1P or ZB2P).
+
+    tf, tb: [P][M] costs >= 1, tw: [P][M] costs >= 0 (scalars broadcast);
+    comm: [P-1] or None.  Returns start, end ([P][3][M]: device, kind F/B/W, microbatch),
+    makespan, busy, idle, bub (num, den) and peak (held microbatches, +1 at F,
+    -1 at W).  Raises OracleError on a cost out of range or a failed validity
+    check.
+    Parity: pinned by hand-derived worked examples, the W-free reduction to
+    1F1B and to the explicit-order evaluator, and an independent tick-stepped
+    simulation (tests/test_oracle_pins.py)."""
+    lib = lib or load()
+    full = lambda a: np.ascontiguousarray(np.broadcast_to(np.asarray(a, np.int64), (P, M)))
+    tf, tb, tw = full(tf), full(tb), full(tw)
+    cm = None if comm is None else np.ascontiguousarray(np.broadcast_to(np.asarray(comm, np.int64), (max(P - 1, 1),)))
+    start = np.zeros((P, 3, M), np.int64)
+    end = np.zeros((P, 3, M), np.int64)
+    mk = np.zeros(1, np.int64)
+    busy = np.zeros(P, np.int64)
+    idle = np.zeros(P, np.int64)
+    bub = np.zeros(2, np.int64)
+    peak = np.zeros(P, np.int32)
+    rc = lib.orc_zb_inst(_policy(policy), P, M, _ptr(tf), _ptr(tb), _ptr(tw), _ptr(cm), _ptr(start), _ptr(end),
+                         _ptr(mk), _ptr(busy), _ptr(idle), _ptr(bub), _ptr(peak))
+    if rc != OK:
+        raise OracleError(rc, "zb_evaluate")
+    return dict(start=start, end=end, makespan=int(mk[0]), busy=busy, idle=idle,
+                bub=(int(bub[0]), int(bub[1])), peak=peak)
+
+
+def zb_batch(policy, P, M, cost_f, cost_b, cost_w, strides, comm=None, comm_strides=(0, 0), n=None,
+             op_times=False, nthreads=1, lib=None):
+    """Zero Bubble batch with the library's input conventions (int32 costs
+    through element strides shared by F, B and W; comm [inst][boundary]).
+    Returns makespan, idle [n][P], bub_num, bub_den, peak [n][P], status and
+    optionally op_start / op_end [n][P][3][M]."""
+    lib = lib or load()
+    cf = np.ascontiguousarray(cost_f, np.int32)
+    cb = np.ascontiguousarray(cost_b, np.int32)
+    cw = np.ascontiguousarray(cost_w, np.int32)
+    cm = None if comm is None else np.ascontiguousarray(comm, np.int32)
+    out = dict(makespan=np.zeros(n, np.int64), idle=np.zeros((n, P), np.int64),
+               bub_num=np.zeros(n, np.int64), bub_den=np.zeros(n, np.int64),
+               peak=np.zeros((n, P), np.int32), status=np.zeros(n, np.int8))
+    os_ = oe = None
+    if op_times:
+        os_ = np.zeros((n, P, 3, M), np.int64)
+        oe = np.zeros((n, P, 3, M), np.int64)
+    rc = lib.orc_zb_batch(_policy(policy), P, M, n, _ptr(cf), _ptr(cb), _ptr(cw), strides[0], strides[1],
+                          strides[2], _ptr(cm), comm_strides[0], comm_strides[1],
+                          _ptr(out["makespan"]), _ptr(out["idle"]), _ptr(out["bub_num"]), _ptr(out["bub_den"]),
+                          _ptr(out["peak"]), _ptr(out["status"]), _ptr(os_), _ptr(oe), nthreads)
+    if rc != OK:
+        raise OracleError(rc, "zb_batch")
+    if op_times:
+        out["op_start"], out["op_end"] = os_, oe
+    return out

@@ -900,3 +900,390 @@ int orc_search(const int32_t *layer_tf, const int32_t *layer_tb, const int64_t *
  * textbook values */
 uint64_t orc_binom(int n, int k) { return binom(n, k); }
 uint64_t orc_splitmix64(uint64_t state) { return splitmix64_at(state); }
+
+/* ------------------------------------------------------------------------- */
+/* Zero Bubble (ZB1P / ZB2P): the backward split into B and W                  */
+/* ------------------------------------------------------------------------- */
+/*
+ * [GPipe->ZB] "Zero Bubble" and "ZB1P and ZB2P"; [1F1B] §6.2.  A microbatch's
+ * backward splits into B (the input gradient, which the previous stage waits
+ * for) and W (the weight gradient, needed only before the parameter update:
+ * no cross-stage dependency).  W(s,i) runs on stage s's device after B(s,i).
+ * The schedule keeps 1F1B's order of F and B and places W greedily: when the
+ * next F or B cannot start because its input has not arrived, the device runs
+ * a W that is ready instead; a device holds at most L microbatches whose F has
+ * run and whose W has not, so an F that would exceed L waits for a W.
+ *
+ * Readings (the pages state the rules loosely; each is in the design notes):
+ *   - F/B order: F^w (B F)^(M-w) B^w as in 1F1B, with w = min(P-k, M) for
+ *     ZB1P and w = min(2(P-k), M) for ZB2P (more forwards in the warmup, about
+ *     twice the activation budget).
+ *   - L = P for ZB1P and 2P for ZB2P, on every device.
+ *   - A device that becomes free at tick t decides:
+ *       1. if its next F/B op X is an F and it holds L microbatches, it runs
+ *          the oldest pending W;
+ *       2. else if X's input has arrived by t, it runs X at t;
+ *       3. else if a W is pending, it runs the oldest pending W at t;
+ *       4. else it waits and runs X when X's input arrives.
+ *     With no F/B op left it runs its pending W's, oldest first.
+ *   - Pending W's run in the order of their B's.
+ *   - Every F and B cost is at least 1 tick (a W may take 0).  Then whether
+ *     an input has arrived by t depends on the costs alone, not on the order
+ *     in which simultaneous decisions are taken: an F or B placed at t or
+ *     later cannot end by t, and a W feeds no other device.  An instance with
+ *     an F or B cost below 1 is flagged ORC_ST_ZERO_COST.
+ *   - comm is the latency on F and B edges as in the other schedules; W has
+ *     no cross-stage edge.
+ *   - Held activations: +1 at F, -1 at W (a microbatch's saved data is
+ *     released when its W is done); the peak is over the device's op order.
+ * Op times are laid out [P][3][M]: device, kind (F, B, W), microbatch.
+ */
+#define ORC_ZB1P 3
+#define ORC_ZB2P 4
+#define ORC_W 2
+#define ORC_ST_ZERO_COST 3
+
+static int zb_warmup(int policy, int P, int M, int k)
+{
+    int w = policy == ORC_ZB2P ? 2 * (P - k) : P - k;
+#if ORC_MUTANT == 10  /* mistake: ZB2P keeps 1F1B's warmup */
+    w = P - k;
+#endif
+    return w < M ? w : M;
+}
+
+typedef struct {
+    int P, M, L;
+    const int64_t *tf, *tb, *tw, *comm;   /* costs [P][M], comm [P-1] or NULL */
+    int *kind, *mb;                       /* F/B order [P][2M] */
+    int *pos, *nf, *nb, *nw, *held, *state, *border;   /* border [P][M]: mb of the i-th B */
+    int64_t *t_free;
+    int64_t *start, *end;                 /* [P][3][M] */
+    int64_t *busy;
+    int *peak;
+} zb_sim;
+
+#define ZB_AT(z, k, kd, m) ((((k) * 3) + (kd)) * (z)->M + (m))
+
+/* Arrival tick of the input of F/B op (kd, m) on device k: 0 without an input
+ * edge, -1 while its producer is not placed. */
+static int64_t zb_arrival(const zb_sim *z, int k, int kd, int m)
+{
+    if (kd == ORC_F) {
+        if (k == 0) return 0;
+        int64_t e = z->end[ZB_AT(z, k - 1, ORC_F, m)];
+        return e < 0 ? -1 : e + (z->comm ? z->comm[k - 1] : 0);
+    }
+    /* B(k,m) also needs F(k,m), which precedes it on the same device */
+    if (k == z->P - 1) return z->end[ZB_AT(z, k, ORC_F, m)];
+    int64_t e = z->end[ZB_AT(z, k + 1, ORC_B, m)];
+    return e < 0 ? -1 : e + (z->comm ? z->comm[k] : 0);
+}
+
+static void zb_place(zb_sim *z, int k, int kd, int m, int64_t s)
+{
+    int64_t c = kd == ORC_F ? z->tf[k * z->M + m] : (kd == ORC_B ? z->tb[k * z->M + m] : z->tw[k * z->M + m]);
+    z->start[ZB_AT(z, k, kd, m)] = s;
+    z->end[ZB_AT(z, k, kd, m)] = s + c;
+    z->t_free[k] = s + c;
+    z->busy[k] += c;
+    if (kd == ORC_F) {
+        z->nf[k]++;
+        z->held[k]++;
+        if (z->held[k] > z->peak[k]) z->peak[k] = z->held[k];
+    } else if (kd == ORC_B) {
+        z->border[k * z->M + z->nb[k]] = m;
+        z->nb[k]++;
+    } else {
+        z->nw[k]++;
+        z->held[k]--;
+    }
+    if (kd != ORC_W) z->pos[k]++;
+}
+
+static void zb_place_w(zb_sim *z, int k, int64_t s)
+{
+    zb_place(z, k, ORC_W, z->border[k * z->M + z->nw[k]], s);
+}
+
+/* A waiting device runs its next F/B op once the op's input is placed. */
+static void zb_wake(zb_sim *z)
+{
+    int again = 1;
+    while (again) {
+        again = 0;
+        for (int d = 0; d < z->P; ++d) {
+            if (z->state[d] != 1) continue;
+            int j = d * 2 * z->M + z->pos[d];
+            int64_t arr = zb_arrival(z, d, z->kind[j], z->mb[j]);
+            if (arr < 0) continue;
+            z->state[d] = 0;
+            zb_place(z, d, z->kind[j], z->mb[j], arr > z->t_free[d] ? arr : z->t_free[d]);
+            again = 1;
+        }
+    }
+}
+
+/* Validity of a finished ZB schedule: per device no overlap and end = start +
+ * cost; F/B in their order; every input arrived before use; W after its B;
+ * at most L held. */
+static int zb_check(const zb_sim *z)
+{
+    int P = z->P, M = z->M;
+    for (int k = 0; k < P; ++k) {
+        if (z->peak[k] > z->L) return ORC_ERR_INVARIANT;
+        /* no overlap: sort this device's 3M ops by (start, end) (insertion
+         * sort; a W of zero cost sorts before an op starting at its tick) */
+        int n = 3 * M;
+        int *ix = (int *)malloc((size_t)n * sizeof(int));
+        if (!ix) return ORC_ERR_NOMEM;
+        for (int q = 0; q < n; ++q) ix[q] = k * n + q;
+        for (int a = 1; a < n; ++a) {
+            int v = ix[a], b = a - 1;
+            while (b >= 0 && (z->start[ix[b]] > z->start[v] ||
+                              (z->start[ix[b]] == z->start[v] && z->end[ix[b]] > z->end[v]))) {
+                ix[b + 1] = ix[b];
+                --b;
+            }
+            ix[b + 1] = v;
+        }
+        int bad = 0;
+        for (int a = 0; a + 1 < n; ++a)
+            if (z->end[ix[a]] > z->start[ix[a + 1]]) bad = 1;
+        free(ix);
+        if (bad) return ORC_ERR_INVARIANT;
+        for (int j = 0; j + 1 < 2 * M; ++j) {
+            int a = k * 2 * M + j;
+            if (z->start[ZB_AT(z, k, z->kind[a], z->mb[a])] > z->start[ZB_AT(z, k, z->kind[a + 1], z->mb[a + 1])])
+                return ORC_ERR_INVARIANT;
+        }
+        for (int m = 0; m < M; ++m) {
+            int64_t c[3] = { z->tf[k * M + m], z->tb[k * M + m], z->tw[k * M + m] };
+            for (int kd = 0; kd < 3; ++kd)
+                if (z->start[ZB_AT(z, k, kd, m)] < 0 || z->end[ZB_AT(z, k, kd, m)] != z->start[ZB_AT(z, k, kd, m)] + c[kd])
+                    return ORC_ERR_INVARIANT;
+            if (k > 0 && z->start[ZB_AT(z, k, ORC_F, m)] < z->end[ZB_AT(z, k - 1, ORC_F, m)] + (z->comm ? z->comm[k - 1] : 0))
+                return ORC_ERR_INVARIANT;
+            if (z->start[ZB_AT(z, k, ORC_B, m)] < z->end[ZB_AT(z, k, ORC_F, m)]) return ORC_ERR_INVARIANT;
+            if (k < P - 1 && z->start[ZB_AT(z, k, ORC_B, m)] < z->end[ZB_AT(z, k + 1, ORC_B, m)] + (z->comm ? z->comm[k] : 0))
+                return ORC_ERR_INVARIANT;
+            if (z->start[ZB_AT(z, k, ORC_W, m)] < z->end[ZB_AT(z, k, ORC_B, m)]) return ORC_ERR_INVARIANT;
+        }
+    }
+    return ORC_OK;
+}
+
+/* One ZB instance.  tf/tb [P][M] (every cost >= 1), tw [P][M] (>= 0), comm
+ * [P-1] or NULL.  Outputs: start/end [P][3][M], makespan, busy[P], idle[P],
+ * bub (num, den), peak[P].  Returns ORC_OK, ORC_ERR_ARG (policy, shape or a
+ * cost out of range),
+ * ORC_ERR_DEADLOCK, ORC_ERR_INVARIANT or ORC_ERR_NOMEM. */
+int orc_zb_inst(int policy, int P, int M, const int64_t *tf, const int64_t *tb, const int64_t *tw,
+                const int64_t *comm, int64_t *start, int64_t *end, int64_t *makespan,
+                int64_t *busy, int64_t *idle, int64_t *bub, int *peak)
+{
+    if ((policy != ORC_ZB1P && policy != ORC_ZB2P) || P < 1 || M < 1) return ORC_ERR_ARG;
+    for (int q = 0; q < P * M; ++q)
+        if (tf[q] < 1 || tb[q] < 1 || tw[q] < 0) return ORC_ERR_ARG;
+    zb_sim z;
+    memset(&z, 0, sizeof(z));
+    z.P = P; z.M = M; z.L = policy == ORC_ZB1P ? P : 2 * P;
+    z.tf = tf; z.tb = tb; z.tw = tw; z.comm = comm;
+    z.start = start; z.end = end; z.busy = busy; z.peak = peak;
+    int O = 2 * M, rc = ORC_OK;
+    z.kind = (int *)malloc((size_t)P * O * sizeof(int));
+    z.mb = (int *)malloc((size_t)P * O * sizeof(int));
+    z.border = (int *)malloc((size_t)P * M * sizeof(int));
+    z.pos = (int *)calloc((size_t)P, sizeof(int));
+    z.nf = (int *)calloc((size_t)P, sizeof(int));
+    z.nb = (int *)calloc((size_t)P, sizeof(int));
+    z.nw = (int *)calloc((size_t)P, sizeof(int));
+    z.held = (int *)calloc((size_t)P, sizeof(int));
+    z.state = (int *)calloc((size_t)P, sizeof(int));
+    z.t_free = (int64_t *)calloc((size_t)P, sizeof(int64_t));
+    if (!z.kind || !z.mb || !z.border || !z.pos || !z.nf || !z.nb || !z.nw || !z.held || !z.state || !z.t_free) {
+        rc = ORC_ERR_NOMEM;
+        goto out;
+    }
+    for (int k = 0; k < P; ++k) {
+        int w = zb_warmup(policy, P, M, k), n = 0, *kd = z.kind + k * O, *mb = z.mb + k * O;
+        for (int i = 0; i < w; ++i) { kd[n] = ORC_F; mb[n] = i; ++n; }
+        for (int q = 0; q < M - w; ++q) {
+            kd[n] = ORC_B; mb[n] = q; ++n;
+            kd[n] = ORC_F; mb[n] = w + q; ++n;
+        }
+        for (int i = M - w; i < M; ++i) { kd[n] = ORC_B; mb[n] = i; ++n; }
+        busy[k] = 0;
+        peak[k] = 0;
+    }
+    for (int q = 0; q < 3 * P * M; ++q) { start[q] = -1; end[q] = -1; }
+
+    for (;;) {
+        /* the free device with the smallest tick decides (then the lowest index) */
+        int k = -1, waiting = 0, left = 0;
+        for (int d = 0; d < P; ++d) {
+            if (z.state[d] == 2) continue;
+            left = 1;
+            if (z.state[d] == 1) { waiting = 1; continue; }
+            if (k < 0 || z.t_free[d] < z.t_free[k]) k = d;
+        }
+        if (!left) break;
+        if (k < 0) { rc = waiting ? ORC_ERR_DEADLOCK : ORC_ERR_INVARIANT; goto out; }
+        int64_t t = z.t_free[k];
+        int pend = z.nw[k] < z.nb[k];
+        if (z.pos[k] == O) {
+            if (pend) zb_place_w(&z, k, t);
+            else z.state[k] = 2;
+            continue;
+        }
+        int j = k * O + z.pos[k];
+        int xk = z.kind[j], xm = z.mb[j];
+#if ORC_MUTANT == 11  /* mistake: an F is admitted with L microbatches already held */
+        if (xk == ORC_F && z.nf[k] - z.nw[k] > z.L) {
+#else
+        if (xk == ORC_F && z.nf[k] - z.nw[k] >= z.L) {
+#endif
+            if (!pend) { rc = ORC_ERR_INVARIANT; goto out; }
+            zb_place_w(&z, k, t);
+            continue;
+        }
+        int64_t arr = zb_arrival(&z, k, xk, xm);
+#if ORC_MUTANT == 9   /* mistake: a pending W goes before a ready F/B */
+        if (pend) zb_place_w(&z, k, t);
+        else if (arr >= 0 && arr <= t) zb_place(&z, k, xk, xm, t);
+#else
+        if (arr >= 0 && arr <= t) zb_place(&z, k, xk, xm, t);
+        else if (pend) zb_place_w(&z, k, t);
+#endif
+        else if (arr >= 0) zb_place(&z, k, xk, xm, arr);
+        else z.state[k] = 1;
+        zb_wake(&z);
+    }
+    rc = zb_check(&z);
+    if (rc) goto out;
+    {
+        int64_t mk = 0, num = 0;
+        for (int q = 0; q < 3 * P * M; ++q) if (end[q] > mk) mk = end[q];
+        for (int k = 0; k < P; ++k) { idle[k] = mk - busy[k]; num += idle[k]; }
+        *makespan = mk;
+        bub[0] = num;
+        bub[1] = (int64_t)P * mk;
+    }
+out:
+    free(z.kind); free(z.mb); free(z.border); free(z.pos); free(z.nf); free(z.nb); free(z.nw);
+    free(z.held); free(z.state); free(z.t_free);
+    return rc;
+}
+
+typedef struct {
+    int policy, P, M;
+    const int32_t *cost_f, *cost_b, *cost_w;
+    int64_t cs_inst, cs_stage, cs_mb;
+    const int32_t *comm;
+    int64_t ms_inst, ms_bnd;
+    int64_t *makespan, *idle, *bub_num, *bub_den;
+    int32_t *peak;                       /* [n][P] */
+    int8_t *status;
+    int64_t *op_start, *op_end;          /* [n][P][3][M] or NULL */
+    int64_t lo, hi;
+    int rc;
+} orc_zb_job;
+
+static void *zb_worker(void *arg)
+{
+    orc_zb_job *jb = (orc_zb_job *)arg;
+    int P = jb->P, M = jb->M, n3 = 3 * P * M;
+    int64_t *tf = (int64_t *)malloc((size_t)P * M * sizeof(int64_t));
+    int64_t *tb = (int64_t *)malloc((size_t)P * M * sizeof(int64_t));
+    int64_t *tw = (int64_t *)malloc((size_t)P * M * sizeof(int64_t));
+    int64_t *cm = (int64_t *)malloc((size_t)(P > 1 ? P - 1 : 1) * sizeof(int64_t));
+    int64_t *st = (int64_t *)malloc((size_t)n3 * sizeof(int64_t));
+    int64_t *en = (int64_t *)malloc((size_t)n3 * sizeof(int64_t));
+    int64_t *busy = (int64_t *)malloc((size_t)P * sizeof(int64_t));
+    int64_t *idle = (int64_t *)malloc((size_t)P * sizeof(int64_t));
+    int *peak = (int *)malloc((size_t)P * sizeof(int));
+    jb->rc = ORC_OK;
+    if (!tf || !tb || !tw || !cm || !st || !en || !busy || !idle || !peak) { jb->rc = ORC_ERR_NOMEM; goto out; }
+    for (int64_t x = jb->lo; x < jb->hi; ++x) {
+        int neg = 0, zero = 0;
+        for (int s = 0; s < P; ++s)
+            for (int i = 0; i < M; ++i) {
+                int64_t off = x * jb->cs_inst + s * jb->cs_stage + i * jb->cs_mb;
+                int q = s * M + i;
+                tf[q] = jb->cost_f[off];
+                tb[q] = jb->cost_b[off];
+                tw[q] = jb->cost_w[off];
+                if (tf[q] < 0 || tb[q] < 0 || tw[q] < 0) neg = 1;
+                if (tf[q] < 1 || tb[q] < 1) zero = 1;
+            }
+        for (int b = 0; b < P - 1; ++b) {
+            cm[b] = jb->comm ? jb->comm[x * jb->ms_inst + b * jb->ms_bnd] : 0;
+            if (cm[b] < 0) neg = 1;
+        }
+        int64_t mk = 0, bub[2] = {0, 0};
+        int8_t status = neg ? ORC_ST_NEG_COST : (zero ? ORC_ST_ZERO_COST : ORC_ST_OK);
+        if (status == ORC_ST_OK) {
+            int rc = orc_zb_inst(jb->policy, P, M, tf, tb, tw, cm, st, en, &mk, busy, idle, bub, peak);
+            if (rc) { jb->rc = rc; goto out; }
+            if (mk > ORC_INT32_MAX) status = ORC_ST_OVERFLOW;
+        } else {
+            for (int q = 0; q < n3; ++q) { st[q] = 0; en[q] = 0; }
+            for (int d = 0; d < P; ++d) { idle[d] = 0; peak[d] = 0; }
+        }
+        if (jb->status) jb->status[x] = status;
+        jb->makespan[x] = mk;
+        for (int d = 0; d < P; ++d) {
+            jb->idle[x * P + d] = idle[d];
+            if (jb->peak) jb->peak[x * P + d] = peak[d];
+        }
+        jb->bub_num[x] = bub[0];
+        jb->bub_den[x] = bub[1];
+        if (jb->op_start)
+            for (int q = 0; q < n3; ++q) {
+                jb->op_start[x * n3 + q] = st[q];
+                jb->op_end[x * n3 + q] = en[q];
+            }
+    }
+out:
+    free(tf); free(tb); free(tw); free(cm); free(st); free(en); free(busy); free(idle); free(peak);
+    return NULL;
+}
+
+/* Evaluate n ZB instances.  Costs are int32 [inst][stage][mb] through element
+ * strides (the same for F, B and W); comm int32 [inst][boundary] or NULL.
+ * Outputs: int64 makespan[n], idle[n][P], bub_num[n], bub_den[n]; int32
+ * peak[n][P] (may be NULL); int8 status[n]; optional int64 op times
+ * [n][P][3][M].  Instances with a negative cost or comm (ORC_ST_NEG_COST) or an
+ * F or B cost below 1 (ORC_ST_ZERO_COST) are not evaluated (outputs 0). */
+int orc_zb_batch(int policy, int P, int M, int64_t n,
+                 const int32_t *cost_f, const int32_t *cost_b, const int32_t *cost_w,
+                 int64_t cs_inst, int64_t cs_stage, int64_t cs_mb,
+                 const int32_t *comm, int64_t ms_inst, int64_t ms_bnd,
+                 int64_t *makespan, int64_t *idle, int64_t *bub_num, int64_t *bub_den,
+                 int32_t *peak, int8_t *status, int64_t *op_start, int64_t *op_end, int nthreads)
+{
+    if ((policy != ORC_ZB1P && policy != ORC_ZB2P) || P < 1 || M < 1 || n < 0) return ORC_ERR_ARG;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if ((int64_t)nthreads > n) nthreads = n > 0 ? (int)n : 1;
+    orc_zb_job jobs[256];
+    pthread_t th[256];
+    for (int t = 0; t < nthreads; ++t) {
+        orc_zb_job *jb = &jobs[t];
+        jb->policy = policy; jb->P = P; jb->M = M;
+        jb->cost_f = cost_f; jb->cost_b = cost_b; jb->cost_w = cost_w;
+        jb->cs_inst = cs_inst; jb->cs_stage = cs_stage; jb->cs_mb = cs_mb;
+        jb->comm = comm; jb->ms_inst = ms_inst; jb->ms_bnd = ms_bnd;
+        jb->makespan = makespan; jb->idle = idle; jb->bub_num = bub_num; jb->bub_den = bub_den;
+        jb->peak = peak; jb->status = status; jb->op_start = op_start; jb->op_end = op_end;
+        jb->lo = n * t / nthreads; jb->hi = n * (t + 1) / nthreads;
+        jb->rc = ORC_OK;
+    }
+    if (nthreads == 1) zb_worker(&jobs[0]);
+    else {
+        for (int t = 0; t < nthreads; ++t) pthread_create(&th[t], NULL, zb_worker, &jobs[t]);
+        for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+    }
+    for (int t = 0; t < nthreads; ++t) if (jobs[t].rc) return jobs[t].rc;
+    return ORC_OK;
+}

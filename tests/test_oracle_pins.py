@@ -307,6 +307,9 @@ MUTANTS = {
     6: "bubble over ideal time",
     7: "splitmix64 shift mistyped",
     8: "unranking off by one",
+    9: "ZB runs a pending W before a ready F/B",
+    10: "ZB2P keeps 1F1B's warmup",
+    11: "ZB admits an F at the activation limit",
 }
 
 
@@ -360,12 +363,33 @@ def _pin_suite(orc, lib):
                 return False
         return True
 
+    def zb():
+        from test_oracle_zb import zb_tick_sim
+        for policy, fx in (("zb1p", "zb1p_p2m2_unit.txt"), ("zb2p", "zb2p_p2m2_unit.txt")):
+            g = read_golden(fx)
+            r = orc.zb_evaluate(policy, 2, 2, 1, 1, 1, lib=lib)
+            if r["makespan"] != int(g["makespan"][0]) or r["bub"] != tuple(int(x) for x in g["bubble"]):
+                return False
+        rng = np.random.default_rng(21)
+        for policy in ("zb1p", "zb2p"):
+            for P, M in ((2, 4), (3, 6), (4, 9)):
+                tf = rng.integers(1, 4, size=(P, M))
+                tb = rng.integers(1, 4, size=(P, M))
+                tw = rng.integers(3, 9, size=(P, M))
+                cm = rng.integers(0, 3, size=P - 1)
+                r = orc.zb_evaluate(policy, P, M, tf, tb, tw, cm, lib=lib)
+                S, _, _ = zb_tick_sim(policy, P, M, tf, tb, tw, cm)
+                if not np.array_equal(r["start"], S):
+                    return False
+        return True
+
     check("tables", tables)
     check("closed", closed)
     check("comm", comm)
     check("phases", phases)
     check("splitmix", sm)
     check("unrank", unrank)
+    check("zb", zb)
     return failed
 
 
