@@ -1,7 +1,8 @@
 /*
  * ppsched.h -- C ABI of libppsched, a GB300 (sm_103a) batched evaluator of
  * pipeline-parallel training schedules: GPipe, synchronous 1F1B
- * (PipeDream-Flush) and interleaved 1F1B.
+ * (PipeDream-Flush), interleaved 1F1B and the Zero Bubble schedules ZB1P and
+ * ZB2P.
  *
  * Sources, by page title and section (short names in brackets):
  *   [1F1B]      "2. 1F1B" (sgdbs.github.io, AI_Infra / 2.PipelineParallel / OneF1B)
@@ -61,11 +62,16 @@ extern "C" {
  *    (j mod Pv)/P of microbatch (j/(Pv))*P + j mod P, backward j is chunk
  *    v-1-(j mod Pv)/P of the same microbatch.  Requires M % P == 0 ([M040] §06).
  *    The pages give the bubble, (P-1)/(vM+P-1) ([1F1B] §6.1), not the order; this
- *    order is the Megatron interleaved schedule they refer to. */
+ *    order is the Megatron interleaved schedule they refer to.
+ *  PP_ZB1P, PP_ZB2P (Zero Bubble; only through pp_sched_eval_zb): the backward
+ *    splits into B (input gradient) and W (weight gradient, no cross-stage
+ *    edge); see pp_sched_eval_zb ([GPipe->ZB] "Zero Bubble", "ZB1P and ZB2P"). */
 typedef enum {
     PP_GPIPE = 0,
     PP_1F1B = 1,
-    PP_INTERLEAVED_1F1B = 2
+    PP_INTERLEAVED_1F1B = 2,
+    PP_ZB1P = 3,
+    PP_ZB2P = 4
 } pp_policy_t;
 
 /* Return codes. */
@@ -84,6 +90,7 @@ typedef enum {
 #define PP_ST_OK 0
 #define PP_ST_NEG_COST 1       /* some cost or comm of the instance is negative */
 #define PP_ST_OVERFLOW 2       /* some tick would exceed INT32_MAX (detected, not wrapped) */
+#define PP_ST_ZERO_COST 3      /* Zero Bubble only: some F or B cost is below 1 tick */
 
 /* Limits. */
 #define PP_MAX_P 16            /* devices */
@@ -216,6 +223,50 @@ const char *pp_sched_status_str(int code);
 /* Free every cached plan of the calling process (all devices).  Not safe while
  * evaluations are in flight. */
 void pp_sched_cache_clear(void);
+
+/* Evaluate n_instances Zero Bubble schedule instances (policy PP_ZB1P or
+ * PP_ZB2P, one stage per device).  [GPipe->ZB] "Zero Bubble" and "ZB1P and
+ * ZB2P"; [1F1B] §6.2.  The backward of microbatch i on stage k splits into
+ * B(k,i), which stage k-1 waits for, and W(k,i), which only needs B(k,i) on
+ * the same device.  The op order depends on the costs, so there is no plan:
+ *   - F and B keep 1F1B's order F^w (B F)^(M-w) B^w with w = min(P-k, M)
+ *     (ZB1P) or min(2(P-k), M) (ZB2P: twice the warmup);
+ *   - a device holds at most L = P (ZB1P) or 2P (ZB2P) microbatches whose F
+ *     has run and whose W has not;
+ *   - a device that becomes free at tick t runs, in this order of preference:
+ *     the oldest pending W if its next F/B op is an F and it holds L; that
+ *     F/B op if its input has arrived by t; the oldest pending W; else it
+ *     waits for the F/B op's input.  With no F/B op left it runs its pending
+ *     W's, oldest first.
+ * These rules are stated loosely on the pages; the library takes this reading.
+ * F and B costs must be at least 1 tick (W may be 0) so that "arrived by t"
+ * depends on the costs alone; an instance with an F or B cost below 1 gets
+ * PP_ST_ZERO_COST.
+ *
+ * Inputs (device, int32): cost_f, cost_b, cost_w of (instance x, stage k,
+ *   microbatch i) at x*stride_inst + k*stride_stage + i*stride_mb (strides may
+ *   be 0); comm [instance][boundary] through its strides, NULL means 0.
+ * Outputs (device; each may be NULL):
+ *   makespan [n], idle [n][P], bub_num [n], bub_den [n]  as pp_sched_eval
+ *   peak [n][P]      most microbatches held at once per device (+1 at F, -1 at
+ *                    W); it depends on the costs, hence per instance
+ *   op_start, op_end each op's start / end tick at element offset
+ *                    x*op_stride_inst + ((k*3 + kind)*M + i)*op_stride_op with
+ *                    kind 0 = F, 1 = B, 2 = W
+ *   status [n]       PP_ST_* (negative cost or comm first, then a zero F/B
+ *                    cost, then overflow)
+ * Limits: 1 <= P <= PP_MAX_P, 1 <= M <= PP_MAX_MV.
+ * Errors: PP_ERR_ARG (policy, shape, NULL cost pointer with n > 0, negative
+ * stride or n), PP_ERR_SIZE, PP_ERR_CUDA.  Allocates nothing; asynchronous. */
+int pp_sched_eval_zb(pp_policy_t policy, int P, int M,
+                     const int32_t *cost_f, const int32_t *cost_b, const int32_t *cost_w,
+                     int64_t stride_inst, int64_t stride_stage, int64_t stride_mb,
+                     const int32_t *comm, int64_t comm_stride_inst, int64_t comm_stride_bnd,
+                     int64_t n_instances,
+                     int32_t *makespan, int32_t *idle, int64_t *bub_num, int64_t *bub_den,
+                     int32_t *peak,
+                     int32_t *op_start, int32_t *op_end, int64_t op_stride_inst, int64_t op_stride_op,
+                     int8_t *status, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -13,15 +13,15 @@ import torch
 
 from . import build_lib
 
-GPIPE, ONEF1B, INTERLEAVED = 0, 1, 2
-POLICIES = {"gpipe": GPIPE, "1f1b": ONEF1B, "interleaved": INTERLEAVED}
+GPIPE, ONEF1B, INTERLEAVED, ZB1P, ZB2P = 0, 1, 2, 3, 4
+POLICIES = {"gpipe": GPIPE, "1f1b": ONEF1B, "interleaved": INTERLEAVED, "zb1p": ZB1P, "zb2p": ZB2P}
 
 PP_OK, PP_ERR_ARG, PP_ERR_DIVISIBILITY, PP_ERR_SIZE, PP_ERR_CUDA, PP_ERR_DEADLOCK, PP_ERR_INTERNAL = range(7)
-ST_OK, ST_NEG_COST, ST_OVERFLOW = 0, 1, 2
+ST_OK, ST_NEG_COST, ST_OVERFLOW, ST_ZERO_COST = 0, 1, 2, 3
 
 EXPORTS = ("pp_sched_plan", "pp_sched_plan_info", "pp_sched_plan_ops", "pp_sched_plan_destroy",
            "pp_sched_eval", "pp_sched_partition_search", "pp_sched_status_str",
-           "pp_sched_cache_clear", "pp_sched_eval_noalloc")
+           "pp_sched_cache_clear", "pp_sched_eval_noalloc", "pp_sched_eval_zb")
 
 
 class PPSchedError(RuntimeError):
@@ -57,6 +57,9 @@ def _load():
     lib.pp_sched_eval_noalloc.argtypes = [i32, i32, i32, vp, vp, i64, i64, i64, vp, i64, i64, i64,
                                           vp, vp, vp, vp, vp, vp, vp]
     lib.pp_sched_eval_noalloc.restype = i32
+    lib.pp_sched_eval_zb.argtypes = [i32, i32, i32, vp, vp, vp, i64, i64, i64, vp, i64, i64, i64,
+                                     vp, vp, vp, vp, vp, vp, vp, i64, i64, vp, vp]
+    lib.pp_sched_eval_zb.restype = i32
     lib.pp_sched_cache_clear.argtypes = []
     lib.pp_sched_cache_clear.restype = None
     return lib
@@ -165,6 +168,48 @@ def evaluate(policy, P, M, v, cost_f, cost_b, strides, n, comm=None, comm_stride
                            _ptr(mk), _ptr(idle), _ptr(bn), _ptr(bd), _ptr(pk), _ptr(os_), _ptr(oe),
                            op_strides[0], op_strides[1], _ptr(stt), _stream(stream))
     _check(rc, "pp_sched_eval")
+    return out
+
+
+def evaluate_zb(policy, P, M, cost_f, cost_b, cost_w, strides, n, comm=None, comm_strides=(0, 0),
+                outputs=("makespan", "idle", "bub_num", "bub_den", "peak", "status"),
+                op_times=False, op_strides=None, out=None, stream=None):
+    """Call pp_sched_eval_zb (ZB1P / ZB2P) on DEVICE tensors.
+
+    cost_f / cost_b / cost_w share the element strides (inst, stage, mb).
+    Returns a dict of CUDA tensors; `peak` is per instance [n][P].  op_times
+    adds op_start / op_end [n][P][3][M] (kind 0 = F, 1 = B, 2 = W), or through
+    op_strides = (inst, op)."""
+    pol = _policy(policy)
+    dev = cost_f.device
+    out = dict(out or {})
+
+    def want(name, shape, dtype):
+        if name in out:
+            return out[name]
+        t = torch.empty(shape, dtype=dtype, device=dev)
+        out[name] = t
+        return t
+
+    mk = want("makespan", (n,), torch.int32) if "makespan" in outputs else None
+    idle = want("idle", (n, P), torch.int32) if "idle" in outputs else None
+    bn = want("bub_num", (n,), torch.int64) if "bub_num" in outputs else None
+    bd = want("bub_den", (n,), torch.int64) if "bub_den" in outputs else None
+    pk = want("peak", (n, P), torch.int32) if "peak" in outputs else None
+    stt = want("status", (n,), torch.int8) if "status" in outputs else None
+    os_ = oe = None
+    if op_times:
+        os_ = want("op_start", (n, P, 3, M), torch.int32)
+        oe = want("op_end", (n, P, 3, M), torch.int32)
+        if op_strides is None:
+            op_strides = (P * 3 * M, 1)
+    else:
+        op_strides = (0, 0)
+    rc = LIB.pp_sched_eval_zb(pol, P, M, _ptr(cost_f), _ptr(cost_b), _ptr(cost_w), strides[0], strides[1],
+                              strides[2], _ptr(comm), comm_strides[0], comm_strides[1], n,
+                              _ptr(mk), _ptr(idle), _ptr(bn), _ptr(bd), _ptr(pk), _ptr(os_), _ptr(oe),
+                              op_strides[0], op_strides[1], _ptr(stt), _stream(stream))
+    _check(rc, "pp_sched_eval_zb")
     return out
 
 

@@ -14,7 +14,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-GPIPE, ONEF1B, INTERLEAVED = 0, 1, 2
+GPIPE, ONEF1B, INTERLEAVED, ZB1P, ZB2P = 0, 1, 2, 3, 4
 
 
 @dataclass
@@ -31,6 +31,7 @@ class Batch:
     comm: np.ndarray | None       # int32, flat buffer indexed through `comm_strides`
     comm_strides: tuple = (0, 0)  # element strides (inst, boundary)
     meta: dict = field(default_factory=dict)
+    cost_w: np.ndarray | None = None  # Zero Bubble only: W costs, same strides as cost_f
 
     @property
     def S(self):
@@ -38,7 +39,7 @@ class Batch:
 
     @property
     def op_times(self):
-        return 2 * self.P * self.M * self.v * self.n
+        return (3 if self.cost_w is not None else 2) * self.P * self.M * self.v * self.n
 
 
 def _rng(seed):
@@ -175,3 +176,43 @@ def random_batch(policy, P, M, v, n, seed, lo=0, hi=9, comm_hi=4, layout="inst_m
         cma = cm.reshape(-1)
         cst = (max(S - 1, 1), 1)
     return Batch(policy, P, M, v, n, cfa, cba, st, cma, cst)
+
+
+def hetero_zb(policy=ZB1P, n=65536, seed=6, P=8, M=64):
+    """Heterogeneous Zero Bubble batch: the 1F1B batch's t_b ~ U[160,240] split
+    into B ~ U[80,120] and W ~ U[80,120]; t_f ~ U[80,120]; comm ~ U[2,8];
+    instance-minor layout."""
+    rng = _rng(seed)
+    cf = rng.integers(80, 120, size=(P, M, n), dtype=np.int32, endpoint=True)
+    cb = rng.integers(80, 120, size=(P, M, n), dtype=np.int32, endpoint=True)
+    cw = rng.integers(80, 120, size=(P, M, n), dtype=np.int32, endpoint=True)
+    cm = rng.integers(2, 8, size=(max(P - 1, 1), n), dtype=np.int32, endpoint=True)
+    name = "zb1p" if policy == ZB1P else "zb2p"
+    return Batch(policy, P, M, 1, n, cf.reshape(-1), cb.reshape(-1), (1, M * n, n), cm.reshape(-1), (1, n),
+                 meta={"workload": f"{name}_hetero_P{P}_M{M}_n{n}"}, cost_w=cw.reshape(-1))
+
+
+def random_zb(policy, P, M, n, seed, lo=1, hi=9, w_lo=0, w_hi=9, comm_hi=4, layout="inst_minor", pad_to=1):
+    """Small random Zero Bubble instances for parity tests (F, B in [lo, hi],
+    W in [w_lo, w_hi], comm in [0, comm_hi])."""
+    rng = _rng(seed)
+    cf = rng.integers(lo, hi, size=(n, P, M), dtype=np.int32, endpoint=True)
+    cb = rng.integers(lo, hi, size=(n, P, M), dtype=np.int32, endpoint=True)
+    cw = rng.integers(w_lo, w_hi, size=(n, P, M), dtype=np.int32, endpoint=True)
+    cm = rng.integers(0, comm_hi, size=(n, max(P - 1, 1)), dtype=np.int32, endpoint=True)
+    if layout == "inst_minor":
+        pitch = -(-n // pad_to) * pad_to if n else 0
+        arrs = []
+        for c in (cf, cb, cw):
+            rows = np.zeros((P, M, pitch), np.int32)
+            rows[:, :, :n] = np.transpose(c, (1, 2, 0))
+            arrs.append(rows.reshape(-1))
+        st = (1, M * pitch, pitch)
+        cma = np.ascontiguousarray(cm.T).reshape(-1)
+        cst = (1, n)
+    else:
+        arrs = [c.reshape(-1) for c in (cf, cb, cw)]
+        st = (P * M, M, 1)
+        cma = cm.reshape(-1)
+        cst = (max(P - 1, 1), 1)
+    return Batch(policy, P, M, 1, n, arrs[0], arrs[1], st, cma, cst, cost_w=arrs[2])

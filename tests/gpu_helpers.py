@@ -56,3 +56,40 @@ def assert_same(gpu, ref, select=None, op_times=False):
     if op_times:
         assert np.array_equal(g["op_start"][ok], ref["op_start"][ok])
         assert np.array_equal(g["op_end"][ok], ref["op_end"][ok])
+
+
+def run_gpu_zb(batch, op_times=False):
+    from pipeline_schedule_simulation_gb300 import binding as B
+    out = B.evaluate_zb(batch.policy, batch.P, batch.M, to_dev(batch.cost_f), to_dev(batch.cost_b),
+                        to_dev(batch.cost_w), batch.strides, batch.n, comm=to_dev(batch.comm),
+                        comm_strides=batch.comm_strides, op_times=op_times)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def run_oracle_zb(orc, batch, op_times=False, nthreads=8, select=None):
+    """Oracle outputs of a Zero Bubble batch, for all instances or `select`."""
+    if select is None:
+        return orc.zb_batch(batch.policy, batch.P, batch.M, batch.cost_f, batch.cost_b, batch.cost_w,
+                            batch.strides, comm=batch.comm, comm_strides=batch.comm_strides, n=batch.n,
+                            op_times=op_times, nthreads=nthreads)
+    P, M = batch.P, batch.M
+    si, ss, sm = batch.strides
+    idx = np.asarray(select, np.int64)
+    off = idx[:, None, None] * si + np.arange(P)[None, :, None] * ss + np.arange(M)[None, None, :] * sm
+    ci, cbd = batch.comm_strides
+    cm = batch.comm[idx[:, None] * ci + np.arange(max(P - 1, 1))[None, :] * cbd].astype(np.int32)
+    return orc.zb_batch(batch.policy, P, M, batch.cost_f[off].astype(np.int32), batch.cost_b[off].astype(np.int32),
+                        batch.cost_w[off].astype(np.int32), (P * M, M, 1), comm=cm,
+                        comm_strides=(max(P - 1, 1), 1), n=len(idx), op_times=op_times, nthreads=nthreads)
+
+
+def assert_same_zb(gpu, ref, select=None, op_times=False):
+    ok = ref["status"] == 0
+    g = {k: (v if select is None else v[np.asarray(select)]) for k, v in gpu.items()}
+    assert np.array_equal(g["status"], ref["status"])
+    for key in ("makespan", "idle", "bub_num", "bub_den", "peak"):
+        assert np.array_equal(g[key][ok], ref[key][ok]), key
+    if op_times:
+        assert np.array_equal(g["op_start"][ok], ref["op_start"][ok])
+        assert np.array_equal(g["op_end"][ok], ref["op_end"][ok])
