@@ -413,6 +413,17 @@ def secondary(B, W, torch, stream):
             t = timed(lambda: B.evaluate(bt.policy, bt.P, bt.M, bt.v, f, g, bt.strides, bt.n, comm=c,
                                          comm_strides=bt.comm_strides, stream=stream), 20)
             out[f"{tag}_P8_v{v}_M128_n16384"] = {"op_times_per_s": bt.op_times / t, "ms": t * 1e3}
+    for pol, name in ((W.ZB1P, "zb1p"), (W.ZB2P, "zb2p")):
+        bz = W.hetero_zb(pol, n=N_INST)
+        f, g, w, c = (torch.from_numpy(x).cuda() for x in (bz.cost_f, bz.cost_b, bz.cost_w, bz.comm))
+        zout = {}
+        zout.update(B.evaluate_zb(pol, P, M, f, g, w, bz.strides, N_INST, comm=c, comm_strides=bz.comm_strides,
+                                  stream=stream))
+        t = timed(lambda: B.evaluate_zb(pol, P, M, f, g, w, bz.strides, N_INST, comm=c,
+                                        comm_strides=bz.comm_strides, out=zout, stream=stream), 10)
+        out[f"{name}_P8_M64_n{N_INST}"] = {"op_times_per_s": bz.op_times / t, "ms": t * 1e3,
+                                           "mean_makespan": float(zout["makespan"].float().mean().item())}
+        del f, g, w, c, zout
     p = W.layer_split()
     lt, lb, la = (torch.from_numpy(x).cuda() for x in (p.layer_tf, p.layer_tb, p.layer_act))
     res = {}

@@ -17,9 +17,10 @@
 // fix: its next F/B op's input has been placed (the arrival tick is known), or
 // the producer device's current free tick proves the input cannot arrive by
 // the decision tick (an F or B costs at least one tick, so a producer op not
-// placed yet ends after the producer's free tick).  Otherwise the lane waits a
-// step.  Every decision is the one the rules fix, so the result does not
-// depend on the order of the steps.  While an instance is unfinished, some
+// placed yet ends after the producer's free tick plus the costs of the
+// producer's ops up to and including it).  Otherwise the lane waits a step.
+// Every decision is the one the rules fix, so the result does not depend on
+// the order of the steps.  While an instance is unfinished, some
 // device of it places an op in every step: following "waits for the input of"
 // from any waiting device walks the acyclic dependency graph back to an op
 // whose input is known.  An instance therefore takes at most 3*P*M + 1 steps.
@@ -27,8 +28,10 @@
 // Per warp, in shared memory ([row][lane], conflict-free):
 //   cost rings  [3 kinds][kRing]: the costs of the next microbatches of each
 //               kind, copied by cp.async kAheadC microbatches ahead; each step
-//               commits one group, and a lane consumes at most one op per step,
-//               so a copy is kAheadC steps old when its row is read
+//               commits one group and a lane consumes at most one op per step,
+//               so the copy of a kind's next microbatch was issued at least
+//               kAheadC - 1 steps ago: each step first waits for every group
+//               but the last kAheadC - 2
 //   arrival rings [2][kQ]: the arrival tick of F(k-1, i) at row i mod kQ of
 //               the first ring (written by lane k-1) and of B(k+1, i) in the
 //               second (written by lane k+1).  At most 2P results of a kind
@@ -109,86 +112,83 @@ __global__ void __launch_bounds__(128) k_eval_zb(const EvalArgs a, const int32_t
     uint32_t t = 0, busy = 0, flag = 0, zero = 0;
     int nf = 0, nb = 0, nw = 0, held = 0, peak = 0;
     bool done = !dev;
-    int nfL = 0, nbR = 0;     // the neighbours' counts after the previous step
-    uint32_t tL = 0, tR = 0;  // and their free ticks
+    // After each step every lane publishes its counts and two lower bounds:
+    // lbF, the earliest end of its next F, and lbB, of its next B (its free
+    // tick plus the costs of the ops its order puts before them).  A consumer
+    // whose input is not placed yet knows the producer's next op of that kind
+    // is exactly the one it waits for.
+    int nfL = 0, nbR = 0;
+    uint32_t lbL = 0, lbR = 0;
     const int max_steps = 3 * P * M + 2;
     bool capped = true;
 #pragma unroll 1
     for (int step = 0; step < max_steps; ++step) {
-        cp_async_wait<G::kAheadC - 1>();
+        cp_async_wait<G::kAheadC - 2>();
         __syncwarp();
-        int kind = -1, m = 0;
+        // ---- decide (every lane evaluates the rules; no divergent paths)
+        const bool pend = nw < nb;
+        const int p = nf + nb;
+        const bool haveX = p < 2 * M;
+        const int q = p - w;
+        const bool isF = q < 0 || (q < 2 * (M - w) && (q & 1));  // order F^w (B F)^(M-w) B^w
+        const int mx = isF ? nf : nb;
+        const uint32_t arrF = k == 0 ? 0u : fring[(mx % G::kQ) * 32 + lane];
+        const uint32_t arrB = k == P - 1 ? 0u : bring[(mx % G::kQ) * 32 + lane];
+        const bool known = isF ? (k == 0 || nfL > nf) : (k == P - 1 || nbR > nb);
+        const uint32_t arr = isF ? arrF : arrB;
+        // the input has not arrived by t: known and later, or provably later
+        const uint32_t lower = isF ? lbL + cmL : lbR + cmR;
+        const bool late = known ? arr > t : lower > t;
+        const int kX = isF ? kZbF : kZbB;
+        int kind = -1;
         uint32_t s = t;
         if (!done) {
-            const bool pend = nw < nb;
-            const int p = nf + nb;
-            if (p == 2 * M) {
-                if (pend) kind = kZbW;
-                else done = true;
-            } else {
-                // the next F/B op: F^w (B F)^(M-w) B^w
-                const int q = p - w;
-                const bool isF = q < 0 || (q < 2 * (M - w) && (q & 1));
-                if (isF && nf - nw >= L) {
-                    kind = kZbW;
-                } else {
-                    const int mx = isF ? nf : nb;
-                    bool known;
-                    uint32_t arr = 0;
-                    if (isF) {
-                        known = k == 0 || nfL > nf;
-                        if (k > 0 && known) arr = fring[(mx % G::kQ) * 32 + lane];
-                    } else {
-                        known = k == P - 1 || nbR > nb;
-                        if (k < P - 1 && known) arr = bring[(mx % G::kQ) * 32 + lane];
-                    }
-                    if (known) {
-                        if (arr <= t) kind = isF ? kZbF : kZbB;
-                        else if (pend) kind = kZbW;
-                        else { kind = isF ? kZbF : kZbB; s = arr; }
-                    } else if (pend) {
-                        // the producer op is not placed: it starts at or after the
-                        // producer's free tick and lasts at least one tick
-                        const uint64_t lower = (uint64_t)(isF ? tL : tR) + 1u + (isF ? cmL : cmR);
-                        if (lower > t) kind = kZbW;
-                    }
-                    if (kind == kZbF || kind == kZbB) m = mx;
-                }
-            }
-            if (kind == kZbW) m = nw;  // W's run in the order of their B's: microbatch order
+            if (!haveX) kind = pend ? kZbW : -1;
+            else if (isF && nf - nw >= L) kind = kZbW;
+            else if (known && !late) kind = kX;
+            else if (late && pend) kind = kZbW;
+            else if (known) { kind = kX; s = arr; }
         }
-        if (kind >= 0) {
-            const uint32_t c = cring[(kind * G::kRing + m % G::kRing) * 32 + lane];
-            const uint32_t e = s + c;
+        done = done || (!haveX && !pend);
+        // ---- place (predicated on kind >= 0)
+        const bool act = kind >= 0;
+        const int m = kind == kZbW ? nw : mx;
+        const int kr = act ? kind : 0;
+        const uint32_t c = cring[(kr * G::kRing + m % G::kRing) * 32 + lane];
+        const uint32_t e = s + c;
+        if (act) {
             flag |= s | c;
-            if (kind != kZbW && c == 0) zero = 1;
+            zero |= (kind != kZbW && c == 0) ? 1u : 0u;
             busy += c;
             t = e;
             fetch(kind, m + G::kAheadC);
-            if (kind == kZbF) {
-                ++nf;
-                ++held;
-                peak = max(peak, held);
-                if (k + 1 < P) fring[(m % G::kQ) * 32 + lane + G::kIPW] = e + cmR;
-            } else if (kind == kZbB) {
-                ++nb;
-                if (k > 0) bring[(m % G::kQ) * 32 + lane - G::kIPW] = e + cmL;
-            } else {
-                ++nw;
-                --held;
-            }
+            if (kind == kZbF && k + 1 < P) fring[(m % G::kQ) * 32 + lane + G::kIPW] = e + cmR;
+            if (kind == kZbB && k > 0) bring[(m % G::kQ) * 32 + lane - G::kIPW] = e + cmL;
             if constexpr (OPS) {
                 const int64_t off = x * a.o_inst + ((int64_t)(k * 3 + kind) * M + m) * a.o_op;
                 if (a.op_start) a.op_start[off] = (int32_t)s;
                 if (a.op_end) a.op_end[off] = (int32_t)e;
             }
         }
+        nf += kind == kZbF;
+        nb += kind == kZbB;
+        nw += kind == kZbW;
+        held += (kind == kZbF) - (kind == kZbW);
+        peak = max(peak, held);
+        // ---- publish
+        const int p2 = nf + nb, q2 = p2 - w;
+        const bool nextF = q2 < 0 || (q2 < 2 * (M - w) && (q2 & 1));
+        const uint32_t cF = nf < M ? cring[(kZbF * G::kRing + nf % G::kRing) * 32 + lane] : 0u;
+        const uint32_t cB = nb < M ? cring[(kZbB * G::kRing + nb % G::kRing) * 32 + lane] : 0u;
+        const bool moreX = p2 < 2 * M;
+        const uint32_t lbF = t + ((moreX && !nextF) ? cB : 0u) + cF;
+        const uint32_t lbB = t + ((moreX && nextF) ? cF : 0u) + cB;
         cp_async_commit();
         __syncwarp();
         nfL = __shfl_up_sync(0xFFFFFFFFu, nf, G::kIPW);
         nbR = __shfl_down_sync(0xFFFFFFFFu, nb, G::kIPW);
-        tL = __shfl_up_sync(0xFFFFFFFFu, t, G::kIPW);
-        tR = __shfl_down_sync(0xFFFFFFFFu, t, G::kIPW);
+        lbL = __shfl_up_sync(0xFFFFFFFFu, lbF, G::kIPW);
+        lbR = __shfl_down_sync(0xFFFFFFFFu, lbB, G::kIPW);
         if (__all_sync(0xFFFFFFFFu, done)) { capped = false; break; }
     }
     cp_async_wait<0>();
