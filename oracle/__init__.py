@@ -74,6 +74,11 @@ def _bind(lib):
     lib.orc_search.argtypes = [vp, vp, vp, c_int, c_int, c_int, ctypes.c_int32, c_i64, c_u64,
                                c_i64, c_i64, vp, vp, vp, vp, c_int]
     lib.orc_search.restype = c_int
+    lib.orc_search_ranks.argtypes = [vp, vp, vp, c_int, c_int, c_int, ctypes.c_int32, c_i64,
+                                     c_i64, c_i64, vp, vp, vp, vp, c_int]
+    lib.orc_search_ranks.restype = c_int
+    lib.orc_rank_split.argtypes = [c_u64, c_int, c_int, vp]
+    lib.orc_rank_split.restype = None
     lib.orc_candidate_split.argtypes = [c_u64, c_i64, c_int, c_int, vp]
     lib.orc_candidate_split.restype = None
     lib.orc_binom.argtypes = [c_int, c_int]
@@ -230,6 +235,33 @@ def search(layer_tf, layer_tb, layer_act, P, M, comm, cap, seed, c_lo, c_hi, nth
     if rc != OK:
         raise OracleError(rc, "search")
     return dict(all_makespan=all_mk, best_idx=int(bi[0]), best_makespan=int(bm[0]), first=first)
+
+
+def search_ranks(layer_tf, layer_tb, layer_act, P, M, comm, cap, r_lo, r_hi, nthreads=1, lib=None):
+    """Exhaustive search over the splits of colex ranks [r_lo, r_hi); returns
+    dict(all_makespan, best_idx (a rank), best_makespan, first) -- see
+    orc_search_ranks."""
+    lib = lib or load()
+    ltf = np.ascontiguousarray(layer_tf, np.int32)
+    ltb = np.ascontiguousarray(layer_tb, np.int32)
+    lact = np.ascontiguousarray(layer_act, np.int64)
+    L = ltf.shape[0]
+    all_mk = np.zeros(r_hi - r_lo, np.int32)
+    bi = np.zeros(1, np.int64)
+    bm = np.zeros(1, np.int64)
+    first = np.zeros(P + 1, np.int32)
+    rc = lib.orc_search_ranks(_ptr(ltf), _ptr(ltb), _ptr(lact), L, P, M, comm, cap, r_lo, r_hi, _ptr(all_mk),
+                              _ptr(bi), _ptr(bm), _ptr(first), nthreads)
+    if rc != OK:
+        raise OracleError(rc, "search_ranks")
+    return dict(all_makespan=all_mk, best_idx=int(bi[0]), best_makespan=int(bm[0]), first=first)
+
+
+def rank_split(r, L, P, lib=None):
+    """Stage starts [P+1] of the split of colex rank r."""
+    first = np.zeros(P + 1, np.int32)
+    (lib or load()).orc_rank_split(ctypes.c_uint64(r), L, P, _ptr(first))
+    return first
 
 
 def binom(n, k, lib=None):

@@ -771,6 +771,20 @@ static void unrank_colex(uint64_t r, int N, int K, int *x)
     }
 }
 
+/* The split of colex rank r in [0, C(L-1, P-1)): the P-1 cut positions
+ * x_1 < ... < x_{P-1} in [0, L-1) of rank r; stage t starts at layer x_t + 1
+ * (stage 0 at layer 0).  Writes first[P+1], first[P] = L.  Ranks 0 .. C-1
+ * enumerate every contiguous split once (the exhaustive search). */
+void orc_rank_split(uint64_t r, int L, int P, int *first)
+{
+    int K = P - 1;
+    int x[64];
+    unrank_colex(r, L - 1, K, x);
+    first[0] = 0;
+    for (int t = 1; t <= K; ++t) first[t] = x[t - 1] + 1;
+    first[P] = L;
+}
+
 /* Candidate c's contiguous split of L layers into P non-empty stages: draw
  * u = splitmix64(seed + c), rank = u mod C(L-1, P-1), unrank it to the P-1 cut
  * positions x_1 < ... < x_{P-1} in [0, L-1); stage t starts at layer
@@ -780,14 +794,8 @@ static void unrank_colex(uint64_t r, int N, int K, int *x)
  * [M040] §05; [lpnh]: 80 layers into 8 stages). */
 void orc_candidate_split(uint64_t seed, int64_t c, int L, int P, int *first)
 {
-    int K = P - 1;
-    int x[64];
-    uint64_t total = binom(L - 1, K);
-    uint64_t r = splitmix64_at(seed + (uint64_t)c) % total;
-    unrank_colex(r, L - 1, K, x);
-    first[0] = 0;
-    for (int t = 1; t <= K; ++t) first[t] = x[t - 1] + 1;
-    first[P] = L;
+    uint64_t total = binom(L - 1, P - 1);
+    orc_rank_split((uint64_t)(splitmix64_at(seed + (uint64_t)c) % total), L, P, first);
 }
 
 typedef struct {
@@ -797,6 +805,7 @@ typedef struct {
     int32_t *all_mk;
     int64_t best_idx; int64_t best_mk;
     const int *kind, *chunk, *mb; const int *peak;
+    int exhaustive;             /* candidate c is colex rank c instead of a seeded draw */
     int rc;
 } orc_search_job;
 
@@ -816,7 +825,8 @@ static void *search_worker(void *arg)
     jb->best_idx = -1; jb->best_mk = -1; jb->rc = ORC_OK;
     for (int b = 0; b < P; ++b) cm[b] = jb->comm;
     for (int64_t c = jb->lo; c < jb->hi; ++c) {
-        orc_candidate_split(jb->seed, c, jb->L, P, first);
+        if (jb->exhaustive) orc_rank_split((uint64_t)c, jb->L, P, first);
+        else orc_candidate_split(jb->seed, c, jb->L, P, first);
         int rejected = 0;
         for (int k = 0; k < P; ++k) {
             int64_t sf = 0, sb = 0, sa = 0;
@@ -847,13 +857,14 @@ static void *search_worker(void *arg)
  * rejected, -2 if it overflows int32.  best = argmin (makespan, index) over the
  * range; best_idx = -1 when nothing is feasible.  first_best[P+1] gets the
  * winner's stage starts.  Returns ORC_OK or an ORC_ERR_* code. */
-int orc_search(const int32_t *layer_tf, const int32_t *layer_tb, const int64_t *layer_act,
-               int L, int P, int M, int32_t comm, int64_t cap, uint64_t seed,
-               int64_t c_lo, int64_t c_hi, int32_t *all_mk,
-               int64_t *best_idx, int64_t *best_mk, int *first_best, int nthreads)
+static int search_impl(const int32_t *layer_tf, const int32_t *layer_tb, const int64_t *layer_act,
+                       int L, int P, int M, int32_t comm, int64_t cap, uint64_t seed, int exhaustive,
+                       int64_t c_lo, int64_t c_hi, int32_t *all_mk,
+                       int64_t *best_idx, int64_t *best_mk, int *first_best, int nthreads)
 {
     if (P < 1 || P > 64 || L < P || M < 1 || c_lo < 0 || c_hi < c_lo) return ORC_ERR_ARG;
     if (binom(L - 1, P - 1) == UINT64_MAX) return ORC_ERR_ARG;
+    if (exhaustive && (uint64_t)c_hi > binom(L - 1, P - 1)) return ORC_ERR_ARG;
     int O = 2 * M;
     int *kind = (int *)malloc((size_t)P * O * sizeof(int));
     int *chunk = (int *)malloc((size_t)P * O * sizeof(int));
@@ -874,6 +885,7 @@ int orc_search(const int32_t *layer_tf, const int32_t *layer_tb, const int64_t *
         jb->lo = c_lo + n * t / nthreads; jb->hi = c_lo + n * (t + 1) / nthreads;
         jb->all_mk = all_mk ? all_mk + (jb->lo - c_lo) : NULL;
         jb->kind = kind; jb->chunk = chunk; jb->mb = mbv; jb->peak = pk;
+        jb->exhaustive = exhaustive;
     }
     if (nthreads == 1) search_worker(&jobs[0]);
     else {
@@ -889,11 +901,33 @@ int orc_search(const int32_t *layer_tf, const int32_t *layer_tb, const int64_t *
         }
     }
     if (first_best) {
-        if (*best_idx >= 0) orc_candidate_split(seed, *best_idx, L, P, first_best);
-        else for (int t = 0; t <= P; ++t) first_best[t] = -1;
+        if (*best_idx < 0) for (int t = 0; t <= P; ++t) first_best[t] = -1;
+        else if (exhaustive) orc_rank_split((uint64_t)*best_idx, L, P, first_best);
+        else orc_candidate_split(seed, *best_idx, L, P, first_best);
     }
     free(kind); free(chunk); free(mbv); free(pk);
     return rc;
+}
+
+int orc_search(const int32_t *layer_tf, const int32_t *layer_tb, const int64_t *layer_act,
+               int L, int P, int M, int32_t comm, int64_t cap, uint64_t seed,
+               int64_t c_lo, int64_t c_hi, int32_t *all_mk,
+               int64_t *best_idx, int64_t *best_mk, int *first_best, int nthreads)
+{
+    return search_impl(layer_tf, layer_tb, layer_act, L, P, M, comm, cap, seed, 0, c_lo, c_hi, all_mk,
+                       best_idx, best_mk, first_best, nthreads);
+}
+
+/* The exhaustive search ([lpnh]'s 80-layer split, every contiguous split):
+ * as orc_search, but candidate c is the split of colex rank c, for ranks
+ * [r_lo, r_hi) within [0, C(L-1, P-1)). */
+int orc_search_ranks(const int32_t *layer_tf, const int32_t *layer_tb, const int64_t *layer_act,
+                     int L, int P, int M, int32_t comm, int64_t cap,
+                     int64_t r_lo, int64_t r_hi, int32_t *all_mk,
+                     int64_t *best_idx, int64_t *best_mk, int *first_best, int nthreads)
+{
+    return search_impl(layer_tf, layer_tb, layer_act, L, P, M, comm, cap, 0, 1, r_lo, r_hi, all_mk,
+                       best_idx, best_mk, first_best, nthreads);
 }
 
 /* exposed for tests: C(n, k) and the raw generator, to pin them against

@@ -298,6 +298,43 @@ def test_search_finds_global_optimum_small(orc):
     assert tight["best_idx"] == -1 and (tight["all_makespan"] == -1).all()
 
 
+def test_exhaustive_search_covers_every_split(orc):
+    """Ranks 0 .. C(L-1, P-1)-1 enumerate every contiguous split exactly once,
+    rank r being the colex rank sum_i C(x_i, i) of its cut positions (the
+    combinatorial number system), and every split is scored as a direct
+    1F1B evaluation of its stage sums would score it."""
+    rng = np.random.default_rng(19)
+    L, P, M, comm = 10, 4, 5, 1
+    ltf = rng.integers(3, 12, L).astype(np.int32)
+    ltb = rng.integers(5, 25, L).astype(np.int32)
+    lact = rng.integers(1, 5, L).astype(np.int64)
+    total = math.comb(L - 1, P - 1)
+    cap = 30
+    res = orc.search_ranks(ltf, ltb, lact, P, M, comm, cap, 0, total)
+    seen = set()
+    for r in range(total):
+        first = [int(v) for v in orc.rank_split(r, L, P)]
+        x = [f - 1 for f in first[1:P]]
+        assert sum(math.comb(xi, i + 1) for i, xi in enumerate(x)) == r
+        seen.add(tuple(first[1:P]))
+        tf = [int(ltf[first[k]:first[k + 1]].sum()) for k in range(P)]
+        tb = [int(ltb[first[k]:first[k + 1]].sum()) for k in range(P)]
+        act = [int(lact[first[k]:first[k + 1]].sum()) for k in range(P)]
+        if any(min(P - k, M) * act[k] > cap for k in range(P)):
+            assert res["all_makespan"][r] == -1
+            continue
+        ev = orc.evaluate("1f1b", P, M, 1, np.repeat(np.array(tf)[:, None], M, 1),
+                          np.repeat(np.array(tb)[:, None], M, 1), comm)
+        assert res["all_makespan"][r] == ev["makespan"]
+    assert seen == set(itertools.combinations(range(1, L), P - 1))
+    feas = res["all_makespan"] >= 0
+    assert feas.any() and not feas.all()
+    best = int(res["all_makespan"][feas].min())
+    assert res["best_makespan"] == best
+    assert res["best_idx"] == int(np.nonzero(res["all_makespan"] == best)[0][0])
+    assert list(res["first"]) == [int(v) for v in orc.rank_split(res["best_idx"], L, P)]
+
+
 MUTANTS = {
     1: "forward edges carry no comm",
     2: "1F1B warmup off by one",
