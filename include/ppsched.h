@@ -191,6 +191,22 @@ int pp_sched_partition_search(const int32_t *layer_tf, const int32_t *layer_tb,
                               int64_t *best_idx, int32_t *best_makespan, int32_t *best_cuts,
                               int32_t *all_makespan, cudaStream_t stream);
 
+/* The exhaustive form of pp_sched_partition_search: scores the splits of colex
+ * ranks rank_begin .. rank_begin + n_ranks - 1, every contiguous split of L
+ * layers into P stages having one rank in [0, C(L-1, P-1)) (the cut positions
+ * x_1 < ... < x_{P-1} of rank r satisfy r = sum_i C(x_i, i)).  Scoring, cap,
+ * outputs and errors as pp_sched_partition_search, with best_rank in place of
+ * best_idx (the winning rank; ties go to the lower rank; -1 if nothing is
+ * feasible) and all_makespan indexed by rank - rank_begin.  A whole search is
+ * rank_begin = 0, n_ranks = C(L-1, P-1) (2,898,753,715 for 80 layers into 8
+ * stages); disjoint rank ranges reduce by (makespan, rank).
+ * Extra error: PP_ERR_ARG if rank_begin + n_ranks > C(L-1, P-1). */
+int pp_sched_partition_search_ranks(const int32_t *layer_tf, const int32_t *layer_tb,
+                                    const int64_t *layer_act, int L, int P, int M, int32_t comm,
+                                    int64_t act_cap, int64_t rank_begin, int64_t n_ranks,
+                                    int64_t *best_rank, int32_t *best_makespan, int32_t *best_cuts,
+                                    int32_t *all_makespan, cudaStream_t stream);
+
 /* pp_sched_eval for GPipe and 1F1B that allocates no device memory.  (This
  * entry point has no counterpart on the pages; it exists for callers that
  * cannot let a library call cudaMalloc, e.g. code whose device memory belongs to

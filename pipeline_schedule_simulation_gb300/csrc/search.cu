@@ -21,7 +21,9 @@ namespace {
 constexpr int kMaxL = 256;
 
 struct SearchArgs {
-    const uint32_t *desc;  // 1F1B plan [R][PMAX]
+    const uint64_t *rw;    // 1F1B plan: per-round kind words
+    const uint4 *seg;      // and segments
+    int nseg;
     int R, P, M, L;
     const int32_t *ltf, *ltb;
     const int64_t *lact;
@@ -101,7 +103,106 @@ __device__ __forceinline__ void unrank(const SearchArgs &a, const Tables &t, uin
     for (int i = 1; i <= PMAX; ++i) if (i >= a.P) first[i] = a.L;
 }
 
+// 1F1B max-plus recurrence of one candidate.  Stage costs are the same for
+// every microbatch, so they stay in registers; the plan's rounds are walked
+// segment by segment: the steady state alternates static rounds in which the
+// even devices run F and the odd ones B (or the reverse), the warmup and
+// cooldown rounds run from their kind words.  The input of an op is the
+// latest result of its kind on the neighbouring device (the plan checks that
+// this holds for 1F1B).  `acc` collects the sign bits of every end tick and
+// arrival (an int32 overflow or a negative stage sum sets it).
 template <int PMAX>
+struct SState {
+    int fr[PMAX], rf[PMAX], rb[PMAX];
+    uint32_t acc;
+};
+
+template <int PMAX>
+__device__ __forceinline__ void s_op_f(SState<PMAX> &S, int k, int arr, int c, int cm) {
+    const int st = max(S.fr[k], arr);
+    const int en = (int)((uint32_t)st + (uint32_t)c);
+    S.fr[k] = en;
+    S.acc |= (uint32_t)en | (uint32_t)arr;
+    S.rf[k] = (int)((uint32_t)en + (uint32_t)cm);
+}
+
+template <int PMAX>
+__device__ __forceinline__ void s_op_b(SState<PMAX> &S, int k, int arr, int c, int cm) {
+    const int st = max(S.fr[k], arr);
+    const int en = (int)((uint32_t)st + (uint32_t)c);
+    S.fr[k] = en;
+    S.acc |= (uint32_t)en | (uint32_t)arr;
+    S.rb[k] = (int)((uint32_t)en + (uint32_t)cm);
+}
+
+// Alternating round: F on devices of parity FP, B on the others.  An F reads
+// rf of a device that runs B this round and a B reads rb of a device that runs
+// F, so no input is overwritten within the round.
+template <int PMAX, int FP>
+__device__ __forceinline__ void s_alt(SState<PMAX> &S, const int (&cf)[PMAX], const int (&cb)[PMAX], int comm) {
+#pragma unroll
+    for (int k = 0; k < PMAX; ++k) {
+        if ((k & 1) == FP) s_op_f<PMAX>(S, k, k > 0 ? S.rf[k > 0 ? k - 1 : 0] : 0, cf[k], k < PMAX - 1 ? comm : 0);
+        else s_op_b<PMAX>(S, k, k < PMAX - 1 ? S.rb[k < PMAX - 1 ? k + 1 : 0] : 0, cb[k], k > 0 ? comm : 0);
+    }
+}
+
+// Any round, from its kind word (2 bits per device).
+template <int PMAX>
+__device__ __forceinline__ void s_round(SState<PMAX> &S, uint32_t kinds, const int (&cf)[PMAX],
+                                        const int (&cb)[PMAX], int P, int comm) {
+    int rf0[PMAX], rb0[PMAX];
+#pragma unroll
+    for (int k = 0; k < PMAX; ++k) { rf0[k] = S.rf[k]; rb0[k] = S.rb[k]; }
+#pragma unroll
+    for (int k = 0; k < PMAX; ++k) {
+        const uint32_t kind = (kinds >> (2 * k)) & 3u;
+        if (kind == kFwd) s_op_f<PMAX>(S, k, k > 0 ? rf0[k > 0 ? k - 1 : 0] : 0, cf[k], k < P - 1 ? comm : 0);
+        else if (kind == kBwd) s_op_b<PMAX>(S, k, k < PMAX - 1 ? rb0[k < PMAX - 1 ? k + 1 : 0] : 0, cb[k], k > 0 ? comm : 0);
+    }
+}
+
+template <int PMAX>
+__device__ __forceinline__ int eval_1f1b(const SearchArgs &a, SState<PMAX> &S, const int (&cf)[PMAX],
+                                         const int (&cb)[PMAX]) {
+#pragma unroll
+    for (int k = 0; k < PMAX; ++k) { S.fr[k] = 0; S.rf[k] = 0; S.rb[k] = 0; }
+#pragma unroll 1
+    for (int si = 0; si < a.nseg; ++si) {
+        const uint4 sg = __ldg(a.seg + si);
+        int r = (int)sg.y;
+        const int r1 = (int)sg.z;
+        if (sg.x == kSegAltA || sg.x == kSegAltB) {
+            const bool a_first = sg.x == kSegAltA;
+#pragma unroll 1
+            for (; r + 1 < r1; r += 2) {
+                if (a_first) { s_alt<PMAX, 0>(S, cf, cb, a.comm); s_alt<PMAX, 1>(S, cf, cb, a.comm); }
+                else { s_alt<PMAX, 1>(S, cf, cb, a.comm); s_alt<PMAX, 0>(S, cf, cb, a.comm); }
+            }
+            if (r < r1) {
+                if (a_first) s_alt<PMAX, 0>(S, cf, cb, a.comm);
+                else s_alt<PMAX, 1>(S, cf, cb, a.comm);
+            }
+        } else {
+#pragma unroll 1
+            for (; r < r1; ++r) s_round<PMAX>(S, rw_kinds(__ldg(a.rw + r)), cf, cb, a.P, a.comm);
+        }
+    }
+    int mk = 0;
+#pragma unroll
+    for (int k = 0; k < PMAX; ++k) mk = max(mk, S.fr[k]);
+    return mk;
+}
+
+// The candidate's rank: a seeded draw (SplitMix64 of seed + index, mod the
+// number of splits) or, for the exhaustive search, the index itself.
+template <bool EXH>
+__device__ __forceinline__ uint64_t cand_rank(const SearchArgs &a, int64_t ci) {
+    if constexpr (EXH) return (uint64_t)(a.begin + ci);
+    return splitmix64(a.seed + (uint64_t)(a.begin + ci)) % a.ncomb;
+}
+
+template <int PMAX, bool EXH>
 __global__ void __launch_bounds__(256) k_search(const SearchArgs a) {
     __shared__ Tables t;
     build_tables(a, t);
@@ -112,9 +213,8 @@ __global__ void __launch_bounds__(256) k_search(const SearchArgs a) {
         const bool live = ci < a.n;
         int mk = -1;
         if (live) {
-            const uint64_t u = splitmix64(a.seed + (uint64_t)(a.begin + ci));
             int first[PMAX + 1];
-            unrank<PMAX>(a, t, u % a.ncomb, first);
+            unrank<PMAX>(a, t, cand_rank<EXH>(a, ci), first);
             int cf[PMAX], cb[PMAX];
             bool ok = true;
             uint32_t big = 0;
@@ -131,41 +231,10 @@ __global__ void __launch_bounds__(256) k_search(const SearchArgs a) {
                 }
             }
             if (ok) {
-                // 1F1B max-plus recurrence over the plan's rounds (see eval_reg.cu)
-                int fr[PMAX], rf[PMAX], rb[PMAX];
-#pragma unroll
-                for (int k = 0; k < PMAX; ++k) { fr[k] = 0; rf[k] = 0; rb[k] = 0; }
-                uint32_t acc = big | (uint32_t)a.comm;
-                for (int r = 0; r < a.R; ++r) {
-                    const uint4 *row = reinterpret_cast<const uint4 *>(a.desc + (int64_t)r * PMAX);
-                    uint32_t d[PMAX];
-#pragma unroll
-                    for (int i = 0; i < PMAX / 4; ++i) {
-                        const uint4 q = __ldg(row + i);
-                        d[4 * i] = q.x; d[4 * i + 1] = q.y; d[4 * i + 2] = q.z; d[4 * i + 3] = q.w;
-                    }
-                    int rf0[PMAX], rb0[PMAX];
-#pragma unroll
-                    for (int k = 0; k < PMAX; ++k) { rf0[k] = rf[k]; rb0[k] = rb[k]; }
-#pragma unroll
-                    for (int k = 0; k < PMAX; ++k) {
-                        const uint32_t kind = desc_kind(d[k]);
-                        if (kind == kIdle) continue;
-                        int arr, c;
-                        if (kind == kFwd) { arr = k > 0 ? rf0[k > 0 ? k - 1 : 0] : 0; c = cf[k]; }
-                        else { arr = k < PMAX - 1 ? rb0[k < PMAX - 1 ? k + 1 : 0] : 0; c = cb[k]; }
-                        const int st = max(fr[k], arr);
-                        const int en = (int)((uint32_t)st + (uint32_t)c);
-                        fr[k] = en;
-                        acc |= (uint32_t)en | (uint32_t)arr;
-                        const int out = (int)((uint32_t)en + (uint32_t)((kind == kFwd ? k < a.P - 1 : k > 0) ? a.comm : 0));
-                        if (kind == kFwd) rf[k] = out; else rb[k] = out;
-                    }
-                }
-                mk = 0;
-#pragma unroll
-                for (int k = 0; k < PMAX; ++k) mk = max(mk, fr[k]);
-                if (acc >> 31) mk = -2;
+                SState<PMAX> S;
+                S.acc = big | (uint32_t)a.comm;
+                mk = eval_1f1b<PMAX>(a, S, cf, cb);
+                if (S.acc >> 31) mk = -2;
             }
             if (a.all_mk) a.all_mk[ci] = mk;
         }
@@ -180,7 +249,7 @@ __global__ void __launch_bounds__(256) k_search(const SearchArgs a) {
     }
 }
 
-template <int PMAX>
+template <int PMAX, bool EXH>
 __global__ void k_search_finish(const SearchArgs a, int64_t *best_idx, int32_t *best_mk, int32_t *best_cuts) {
     __shared__ Tables t;
     build_tables(a, t);
@@ -195,9 +264,8 @@ __global__ void k_search_finish(const SearchArgs a, int64_t *best_idx, int32_t *
     const int64_t ci = (int64_t)(key & 0xFFFFFFFFull);
     const int mk = (int)(key >> 32);
     if (best_cuts) {
-        const uint64_t u = splitmix64(a.seed + (uint64_t)(a.begin + ci));
         int first[PMAX + 1];
-        unrank<PMAX>(a, t, u % a.ncomb, first);
+        unrank<PMAX>(a, t, cand_rank<EXH>(a, ci), first);
         for (int k = 1; k < a.P; ++k) best_cuts[k - 1] = first[k];
     }
     if (best_mk) *best_mk = mk;
@@ -215,19 +283,19 @@ uint64_t host_binom(int n, int k) {
     return (uint64_t)acc;
 }
 
-template <int PMAX>
+template <int PMAX, bool EXH>
 int run_search(SearchArgs &a, int64_t *best_idx, int32_t *best_mk, int32_t *best_cuts, cudaStream_t st) {
     int dev = 0, sms = 0, per_sm = 0;
     PPS_CUDA_TRY(cudaGetDevice(&dev));
     PPS_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    PPS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_search<PMAX>, 256, 0));
+    PPS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_search<PMAX, EXH>, 256, 0));
     if (per_sm < 1) per_sm = 1;
     int64_t want = (a.n + 255) / 256;
     int64_t grid = (int64_t)sms * per_sm;
     if (want < grid) grid = want;
     if (grid < 1) grid = 1;
-    if (a.n > 0) k_search<PMAX><<<(unsigned)grid, 256, 0, st>>>(a);
-    k_search_finish<PMAX><<<1, 64, 0, st>>>(a, best_idx, best_mk, best_cuts);
+    if (a.n > 0) k_search<PMAX, EXH><<<(unsigned)grid, 256, 0, st>>>(a);
+    k_search_finish<PMAX, EXH><<<1, 64, 0, st>>>(a, best_idx, best_mk, best_cuts);
     PPS_CUDA_TRY(cudaGetLastError());
     return PP_OK;
 }
@@ -236,34 +304,60 @@ int run_search(SearchArgs &a, int64_t *best_idx, int32_t *best_mk, int32_t *best
 
 }  // namespace pps
 
-extern "C" int pp_sched_partition_search(const int32_t *layer_tf, const int32_t *layer_tb,
-                                         const int64_t *layer_act, int L, int P, int M, int32_t comm,
-                                         int64_t act_cap, uint64_t seed, int64_t cand_begin,
-                                         int64_t n_cand, int64_t *best_idx, int32_t *best_makespan,
-                                         int32_t *best_cuts, int32_t *all_makespan, cudaStream_t stream) {
-    using namespace pps;
+namespace pps {
+namespace {
+
+int search_entry(const int32_t *layer_tf, const int32_t *layer_tb, const int64_t *layer_act, int L, int P, int M,
+                 int32_t comm, int64_t act_cap, uint64_t seed, bool exhaustive, int64_t begin, int64_t n,
+                 int64_t *best_idx, int32_t *best_makespan, int32_t *best_cuts, int32_t *all_makespan,
+                 cudaStream_t stream) {
     if (!layer_tf || !layer_tb || !layer_act || !best_idx) return PP_ERR_ARG;
-    if (P < 1 || M < 1 || L < P || n_cand < 0 || cand_begin < 0 || comm < 0) return PP_ERR_ARG;
+    if (P < 1 || M < 1 || L < P || n < 0 || begin < 0 || comm < 0) return PP_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(best_idx) & 7) != 0) return PP_ERR_ARG;
-    if (P > PP_MAX_P || L > kMaxL || M > PP_MAX_MV || n_cand >= (int64_t)1 << 32) return PP_ERR_SIZE;
+    if (P > PP_MAX_P || L > kMaxL || M > PP_MAX_MV || n >= (int64_t)1 << 32) return PP_ERR_SIZE;
     const uint64_t ncomb = host_binom(L - 1, P - 1);
     if (ncomb == ~0ull || ncomb == 0) return PP_ERR_SIZE;
+    if (exhaustive && (uint64_t)begin + (uint64_t)n > ncomb) return PP_ERR_ARG;
     pp_plan *plan = nullptr;
     int rc = cached_plan(PP_1F1B, P, M, 1, stream, &plan);
     if (rc) return rc;
     if (!plan->reg_ok) return PP_ERR_INTERNAL;
     SearchArgs a;
-    a.desc = plan->d_desc; a.R = plan->R; a.P = P; a.M = M; a.L = L;
+    a.rw = plan->d_rw; a.seg = plan->d_seg; a.nseg = plan->nseg; a.R = plan->R; a.P = P; a.M = M; a.L = L;
     a.ltf = layer_tf; a.ltb = layer_tb; a.lact = layer_act;
-    a.comm = comm; a.cap = act_cap; a.seed = seed; a.begin = cand_begin; a.n = n_cand; a.ncomb = ncomb;
+    a.comm = comm; a.cap = act_cap; a.seed = seed; a.begin = begin; a.n = n; a.ncomb = ncomb;
     for (int k = 0; k < PP_MAX_P; ++k) a.peak[k] = k < P ? plan->h_peak[k] : 0;
     a.all_mk = all_makespan;
     a.key = reinterpret_cast<unsigned long long *>(best_idx);
     PPS_CUDA_TRY(cudaMemsetAsync(best_idx, 0xFF, sizeof(int64_t), stream));
     switch (plan->pmax) {
-        case 4: return run_search<4>(a, best_idx, best_makespan, best_cuts, stream);
-        case 8: return run_search<8>(a, best_idx, best_makespan, best_cuts, stream);
-        case 16: return run_search<16>(a, best_idx, best_makespan, best_cuts, stream);
+        case 4: return exhaustive ? run_search<4, true>(a, best_idx, best_makespan, best_cuts, stream)
+                                  : run_search<4, false>(a, best_idx, best_makespan, best_cuts, stream);
+        case 8: return exhaustive ? run_search<8, true>(a, best_idx, best_makespan, best_cuts, stream)
+                                  : run_search<8, false>(a, best_idx, best_makespan, best_cuts, stream);
+        case 16: return exhaustive ? run_search<16, true>(a, best_idx, best_makespan, best_cuts, stream)
+                                   : run_search<16, false>(a, best_idx, best_makespan, best_cuts, stream);
         default: return PP_ERR_INTERNAL;
     }
+}
+
+}  // namespace
+}  // namespace pps
+
+extern "C" int pp_sched_partition_search(const int32_t *layer_tf, const int32_t *layer_tb,
+                                         const int64_t *layer_act, int L, int P, int M, int32_t comm,
+                                         int64_t act_cap, uint64_t seed, int64_t cand_begin,
+                                         int64_t n_cand, int64_t *best_idx, int32_t *best_makespan,
+                                         int32_t *best_cuts, int32_t *all_makespan, cudaStream_t stream) {
+    return pps::search_entry(layer_tf, layer_tb, layer_act, L, P, M, comm, act_cap, seed, false, cand_begin,
+                             n_cand, best_idx, best_makespan, best_cuts, all_makespan, stream);
+}
+
+extern "C" int pp_sched_partition_search_ranks(const int32_t *layer_tf, const int32_t *layer_tb,
+                                               const int64_t *layer_act, int L, int P, int M, int32_t comm,
+                                               int64_t act_cap, int64_t rank_begin, int64_t n_ranks,
+                                               int64_t *best_rank, int32_t *best_makespan, int32_t *best_cuts,
+                                               int32_t *all_makespan, cudaStream_t stream) {
+    return pps::search_entry(layer_tf, layer_tb, layer_act, L, P, M, comm, act_cap, 0, true, rank_begin, n_ranks,
+                             best_rank, best_makespan, best_cuts, all_makespan, stream);
 }

@@ -78,3 +78,72 @@ def test_split_ranges_reduce_to_whole(B):
         g = _gpu_search(B, p, lo, hi - lo, all_mk=False)
         parts.append((int(g["best_makespan"][0]), int(g["best_idx"][0])))
     assert best_of(parts) == (int(whole["best_makespan"][0]), int(whole["best_idx"][0]))
+
+
+@pytest.mark.parametrize("L,P,M,comm,cap", [(10, 4, 5, 1, 30), (20, 5, 10, 2, 10**12), (12, 1, 4, 0, 10**9),
+                                            (18, 8, 16, 1, 60), (20, 16, 20, 0, 10**12), (30, 3, 7, 3, 10**12)])
+def test_exhaustive_small_exact(orc, B, L, P, M, comm, cap):
+    """Every split of small problems, ranks split over two calls: makespans
+    bit-exact, best rank and cuts as the oracle's exhaustive search."""
+    import math
+    rng = np.random.default_rng(L * 7 + P)
+    ltf = rng.integers(1, 20, L).astype(np.int32)
+    ltb = rng.integers(1, 40, L).astype(np.int32)
+    lact = rng.integers(1, 4, L).astype(np.int64)
+    total = math.comb(L - 1, P - 1)
+    half = total // 2
+    got, parts = [], []
+    for lo, hi in ((0, half), (half, total)):
+        g = B.partition_search_ranks(to_dev(ltf), to_dev(ltb), to_dev(lact), P, M, comm, cap, lo, hi - lo,
+                                     all_makespan=True)
+        torch.cuda.synchronize()
+        got.append(g["all_makespan"].cpu().numpy())
+        parts.append((int(g["best_makespan"].item()), int(g["best_idx"].item())))
+    allmk = np.concatenate(got)
+    r = orc.search_ranks(ltf, ltb, lact, P, M, comm, cap, 0, total, nthreads=8)
+    assert np.array_equal(allmk, r["all_makespan"])
+    from pipeline_schedule_simulation_gb300.sharding import best_of
+    feas = [p for p in parts if p[1] >= 0]
+    if r["best_idx"] >= 0:
+        assert best_of(feas) == (r["best_makespan"], r["best_idx"])
+    whole = B.partition_search_ranks(to_dev(ltf), to_dev(ltb), to_dev(lact), P, M, comm, cap, 0, total)
+    torch.cuda.synchronize()
+    assert int(whole["best_idx"].item()) == r["best_idx"]
+    assert int(whole["best_makespan"].item()) == r["best_makespan"]
+    if P > 1 and r["best_idx"] >= 0:
+        assert list(whole["best_cuts"].cpu().numpy()) == list(r["first"][1:P])
+
+
+def test_exhaustive_layer_split_full(orc, B):
+    """All 2,898,753,715 splits of the 80-layer model into 8 stages at M=128:
+    the winner and 20 sampled rank windows re-scored by the oracle; two halves
+    reduce to the whole; no split beats the seeded search's best."""
+    import math
+    p = W.layer_split()
+    total = math.comb(len(p.layer_tf) - 1, p.P - 1)
+    assert total == 2_898_753_715
+    args = (to_dev(p.layer_tf), to_dev(p.layer_tb), to_dev(p.layer_act), p.P, p.M, p.comm, p.cap)
+    whole = B.partition_search_ranks(*args, 0, total)
+    torch.cuda.synchronize()
+    best, mk = int(whole["best_idx"].item()), int(whole["best_makespan"].item())
+    assert best >= 0
+    r = orc.search_ranks(p.layer_tf, p.layer_tb, p.layer_act, p.P, p.M, p.comm, p.cap, best, best + 1)
+    assert r["best_makespan"] == mk
+    assert list(whole["best_cuts"].cpu().numpy()) == list(r["first"][1:p.P])
+    seeded = B.partition_search(*args, p.seed, 0, p.n_cand)
+    torch.cuda.synchronize()
+    assert mk <= int(seeded["best_makespan"].item())
+    rng = np.random.default_rng(77)
+    for lo in rng.integers(0, total - 16, 20):
+        g = B.partition_search_ranks(*args, int(lo), 16, all_makespan=True)
+        torch.cuda.synchronize()
+        rs = orc.search_ranks(p.layer_tf, p.layer_tb, p.layer_act, p.P, p.M, p.comm, p.cap, int(lo), int(lo) + 16)
+        assert np.array_equal(g["all_makespan"].cpu().numpy(), rs["all_makespan"])
+    half = total // 2
+    parts = []
+    for lo, hi in ((0, half), (half, total)):
+        g = B.partition_search_ranks(*args, lo, hi - lo)
+        torch.cuda.synchronize()
+        parts.append((int(g["best_makespan"].item()), int(g["best_idx"].item())))
+    from pipeline_schedule_simulation_gb300.sharding import best_of
+    assert best_of([q for q in parts if q[1] >= 0]) == (mk, best)
