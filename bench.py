@@ -15,6 +15,7 @@ the data path); the slowest rank's time is reported.
 from __future__ import annotations
 
 import argparse
+import math
 import ctypes
 import json
 import os
@@ -433,6 +434,14 @@ def secondary(B, W, torch, stream):
         "candidates_per_s": p.n_cand / t, "ms": t * 1e3,
         "best_idx": int(res["best_idx"].item()), "best_makespan": int(res["best_makespan"].item()),
         "best_cuts": res["best_cuts"].cpu().tolist()}
+    total = math.comb(len(p.layer_tf) - 1, p.P - 1)
+    ex = {}
+    t = timed(lambda: ex.update(B.partition_search_ranks(lt, lb, la, p.P, p.M, p.comm, p.cap, 0, total,
+                                                         stream=stream)), 3)
+    out["partition_search_exhaustive_L80_P8_M128"] = {
+        "splits": total, "splits_per_s": total / t, "ms": t * 1e3,
+        "best_rank": int(ex["best_idx"].item()), "best_makespan": int(ex["best_makespan"].item()),
+        "best_cuts": ex["best_cuts"].cpu().tolist()}
     return out
 
 
