@@ -77,6 +77,9 @@ def _bind(lib):
     lib.orc_search_ranks.argtypes = [vp, vp, vp, c_int, c_int, c_int, ctypes.c_int32, c_i64,
                                      c_i64, c_i64, vp, vp, vp, vp, c_int]
     lib.orc_search_ranks.restype = c_int
+    lib.orc_search_interleaved.argtypes = [vp, vp, vp, c_int, c_int, c_int, c_int, ctypes.c_int32, c_i64, c_u64,
+                                           c_i64, c_i64, vp, vp, vp, vp, c_int]
+    lib.orc_search_interleaved.restype = c_int
     lib.orc_rank_split.argtypes = [c_u64, c_int, c_int, vp]
     lib.orc_rank_split.restype = None
     lib.orc_candidate_split.argtypes = [c_u64, c_i64, c_int, c_int, vp]
@@ -254,6 +257,27 @@ def search_ranks(layer_tf, layer_tb, layer_act, P, M, comm, cap, r_lo, r_hi, nth
                               _ptr(bi), _ptr(bm), _ptr(first), nthreads)
     if rc != OK:
         raise OracleError(rc, "search_ranks")
+    return dict(all_makespan=all_mk, best_idx=int(bi[0]), best_makespan=int(bm[0]), first=first)
+
+
+def search_interleaved(layer_tf, layer_tb, layer_act, P, v, M, comm, cap, seed, c_lo, c_hi, nthreads=1, lib=None):
+    """Seeded search over interleaved layouts (S = P*v contiguous ranges);
+    returns dict(all_makespan, best_idx, best_makespan, first [S+1]) -- see
+    orc_search_interleaved."""
+    lib = lib or load()
+    ltf = np.ascontiguousarray(layer_tf, np.int32)
+    ltb = np.ascontiguousarray(layer_tb, np.int32)
+    lact = np.ascontiguousarray(layer_act, np.int64)
+    L = ltf.shape[0]
+    all_mk = np.zeros(c_hi - c_lo, np.int32)
+    bi = np.zeros(1, np.int64)
+    bm = np.zeros(1, np.int64)
+    first = np.zeros(P * v + 1, np.int32)
+    rc = lib.orc_search_interleaved(_ptr(ltf), _ptr(ltb), _ptr(lact), L, P, v, M, comm, cap,
+                                    ctypes.c_uint64(seed & (2**64 - 1)), c_lo, c_hi, _ptr(all_mk),
+                                    _ptr(bi), _ptr(bm), _ptr(first), nthreads)
+    if rc != OK:
+        raise OracleError(rc, "search_interleaved")
     return dict(all_makespan=all_mk, best_idx=int(bi[0]), best_makespan=int(bm[0]), first=first)
 
 

@@ -800,7 +800,7 @@ void orc_candidate_split(uint64_t seed, int64_t c, int L, int P, int *first)
 
 typedef struct {
     const int32_t *ltf, *ltb; const int64_t *lact;
-    int L, P, M; int32_t comm; int64_t cap; uint64_t seed;
+    int L, P, M, v; int32_t comm; int64_t cap; uint64_t seed;
     int64_t lo, hi;
     int32_t *all_mk;
     int64_t best_idx; int64_t best_mk;
@@ -812,32 +812,45 @@ typedef struct {
 static void *search_worker(void *arg)
 {
     orc_search_job *jb = (orc_search_job *)arg;
-    int P = jb->P, M = jb->M, O = 2 * M;
+    int P = jb->P, M = jb->M, v = jb->v, S = P * v, O = 2 * M * v;
     int first[65];
-    int64_t *tf = (int64_t *)malloc((size_t)P * M * sizeof(int64_t));
-    int64_t *tb = (int64_t *)malloc((size_t)P * M * sizeof(int64_t));
-    int64_t *cm = (int64_t *)malloc((size_t)P * sizeof(int64_t));
+    int64_t *tf = (int64_t *)malloc((size_t)S * M * sizeof(int64_t));
+    int64_t *tb = (int64_t *)malloc((size_t)S * M * sizeof(int64_t));
+    int64_t *act = (int64_t *)malloc((size_t)S * sizeof(int64_t));
+    int64_t *cm = (int64_t *)malloc((size_t)S * sizeof(int64_t));
     int64_t *st = (int64_t *)malloc((size_t)P * O * sizeof(int64_t));
     int64_t *en = (int64_t *)malloc((size_t)P * O * sizeof(int64_t));
     int64_t *busy = (int64_t *)malloc((size_t)P * sizeof(int64_t));
     int64_t *idle = (int64_t *)malloc((size_t)P * sizeof(int64_t));
     int *pk = (int *)malloc((size_t)P * sizeof(int));
     jb->best_idx = -1; jb->best_mk = -1; jb->rc = ORC_OK;
-    for (int b = 0; b < P; ++b) cm[b] = jb->comm;
+    for (int b = 0; b < S; ++b) cm[b] = jb->comm;
     for (int64_t c = jb->lo; c < jb->hi; ++c) {
-        if (jb->exhaustive) orc_rank_split((uint64_t)c, jb->L, P, first);
-        else orc_candidate_split(jb->seed, c, jb->L, P, first);
-        int rejected = 0;
-        for (int k = 0; k < P; ++k) {
+        if (jb->exhaustive) orc_rank_split((uint64_t)c, jb->L, S, first);
+        else orc_candidate_split(jb->seed, c, jb->L, S, first);
+        for (int s = 0; s < S; ++s) {
             int64_t sf = 0, sb = 0, sa = 0;
-            for (int l = first[k]; l < first[k + 1]; ++l) { sf += jb->ltf[l]; sb += jb->ltb[l]; sa += jb->lact[l]; }
-            /* peak bytes on stage k = held activations x bytes per activation */
-            if ((int64_t)jb->peak[k] * sa > jb->cap) rejected = 1;
-            for (int i = 0; i < M; ++i) { tf[k * M + i] = sf; tb[k * M + i] = sb; }
+            for (int l = first[s]; l < first[s + 1]; ++l) { sf += jb->ltf[l]; sb += jb->ltb[l]; sa += jb->lact[l]; }
+            act[s] = sa;
+            for (int i = 0; i < M; ++i) { tf[s * M + i] = sf; tb[s * M + i] = sb; }
+        }
+        /* peak bytes held on device d: the ledger of [1F1B] §4.1 weighted by
+         * the bytes of the chunk each op belongs to (+ at F, - at B), at its
+         * running maximum; with one chunk per device this is the peak count
+         * times the stage's bytes */
+        int rejected = 0;
+        for (int d = 0; d < P && !rejected; ++d) {
+            int64_t held = 0, top = 0;
+            for (int j = 0; j < O; ++j) {
+                int s = jb->chunk[d * O + j] * P + d;
+                held += jb->kind[d * O + j] == ORC_F ? act[s] : -act[s];
+                if (held > top) top = held;
+            }
+            if (top > jb->cap) rejected = 1;
         }
         int64_t mk = -1, bub[2];
         if (!rejected) {
-            int rc = orc_eval_explicit(P, M, 1, jb->kind, jb->chunk, jb->mb, tf, tb, cm, 0,
+            int rc = orc_eval_explicit(P, M, v, jb->kind, jb->chunk, jb->mb, tf, tb, cm, 0,
                                        st, en, &mk, busy, idle, bub, pk);
             if (rc) { jb->rc = rc; break; }
             if (mk > ORC_INT32_MAX) mk = -2;
@@ -845,7 +858,7 @@ static void *search_worker(void *arg)
         if (jb->all_mk) jb->all_mk[c - jb->lo] = (int32_t)mk;
         if (mk >= 0 && (jb->best_idx < 0 || mk < jb->best_mk)) { jb->best_mk = mk; jb->best_idx = c; }
     }
-    free(tf); free(tb); free(cm); free(st); free(en); free(busy); free(idle); free(pk);
+    free(tf); free(tb); free(act); free(cm); free(st); free(en); free(busy); free(idle); free(pk);
     return NULL;
 }
 
@@ -858,19 +871,22 @@ static void *search_worker(void *arg)
  * range; best_idx = -1 when nothing is feasible.  first_best[P+1] gets the
  * winner's stage starts.  Returns ORC_OK or an ORC_ERR_* code. */
 static int search_impl(const int32_t *layer_tf, const int32_t *layer_tb, const int64_t *layer_act,
-                       int L, int P, int M, int32_t comm, int64_t cap, uint64_t seed, int exhaustive,
+                       int L, int P, int v, int M, int32_t comm, int64_t cap, uint64_t seed, int exhaustive,
                        int64_t c_lo, int64_t c_hi, int32_t *all_mk,
                        int64_t *best_idx, int64_t *best_mk, int *first_best, int nthreads)
 {
-    if (P < 1 || P > 64 || L < P || M < 1 || c_lo < 0 || c_hi < c_lo) return ORC_ERR_ARG;
-    if (binom(L - 1, P - 1) == UINT64_MAX) return ORC_ERR_ARG;
-    if (exhaustive && (uint64_t)c_hi > binom(L - 1, P - 1)) return ORC_ERR_ARG;
-    int O = 2 * M;
+    int S = P * v;
+    if (P < 1 || v < 1 || S > 64 || L < S || M < 1 || c_lo < 0 || c_hi < c_lo) return ORC_ERR_ARG;
+    if (v > 1 && M % P != 0) return ORC_ERR_DIVISIBILITY;
+    if (binom(L - 1, S - 1) == UINT64_MAX) return ORC_ERR_ARG;
+    if (exhaustive && (uint64_t)c_hi > binom(L - 1, S - 1)) return ORC_ERR_ARG;
+    int O = 2 * M * v;
     int *kind = (int *)malloc((size_t)P * O * sizeof(int));
     int *chunk = (int *)malloc((size_t)P * O * sizeof(int));
     int *mbv = (int *)malloc((size_t)P * O * sizeof(int));
     int *pk = (int *)malloc((size_t)P * sizeof(int));
-    for (int d = 0; d < P; ++d) orc_order(ORC_1F1B, P, M, 1, d, kind + d * O, chunk + d * O, mbv + d * O);
+    for (int d = 0; d < P; ++d)
+        orc_order(v > 1 ? ORC_INTERLEAVED : ORC_1F1B, P, M, v, d, kind + d * O, chunk + d * O, mbv + d * O);
     orc_peak(P, O, kind, pk);
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;
@@ -881,7 +897,7 @@ static int search_impl(const int32_t *layer_tf, const int32_t *layer_tb, const i
     for (int t = 0; t < nthreads; ++t) {
         orc_search_job *jb = &jobs[t];
         jb->ltf = layer_tf; jb->ltb = layer_tb; jb->lact = layer_act;
-        jb->L = L; jb->P = P; jb->M = M; jb->comm = comm; jb->cap = cap; jb->seed = seed;
+        jb->L = L; jb->P = P; jb->M = M; jb->v = v; jb->comm = comm; jb->cap = cap; jb->seed = seed;
         jb->lo = c_lo + n * t / nthreads; jb->hi = c_lo + n * (t + 1) / nthreads;
         jb->all_mk = all_mk ? all_mk + (jb->lo - c_lo) : NULL;
         jb->kind = kind; jb->chunk = chunk; jb->mb = mbv; jb->peak = pk;
@@ -901,9 +917,9 @@ static int search_impl(const int32_t *layer_tf, const int32_t *layer_tb, const i
         }
     }
     if (first_best) {
-        if (*best_idx < 0) for (int t = 0; t <= P; ++t) first_best[t] = -1;
-        else if (exhaustive) orc_rank_split((uint64_t)*best_idx, L, P, first_best);
-        else orc_candidate_split(seed, *best_idx, L, P, first_best);
+        if (*best_idx < 0) for (int t = 0; t <= S; ++t) first_best[t] = -1;
+        else if (exhaustive) orc_rank_split((uint64_t)*best_idx, L, S, first_best);
+        else orc_candidate_split(seed, *best_idx, L, S, first_best);
     }
     free(kind); free(chunk); free(mbv); free(pk);
     return rc;
@@ -914,7 +930,23 @@ int orc_search(const int32_t *layer_tf, const int32_t *layer_tb, const int64_t *
                int64_t c_lo, int64_t c_hi, int32_t *all_mk,
                int64_t *best_idx, int64_t *best_mk, int *first_best, int nthreads)
 {
-    return search_impl(layer_tf, layer_tb, layer_act, L, P, M, comm, cap, seed, 0, c_lo, c_hi, all_mk,
+    return search_impl(layer_tf, layer_tb, layer_act, L, P, 1, M, comm, cap, seed, 0, c_lo, c_hi, all_mk,
+                       best_idx, best_mk, first_best, nthreads);
+}
+
+/* The search over interleaved layouts ([M040] §06: a device holds several
+ * virtual stages; §05: split by measured cost and activation): each candidate
+ * splits the L layers into S = P*v contiguous non-empty ranges (seeded draw of
+ * a colex rank of C(L-1, S-1)); range s is virtual stage s, chunk s / P of
+ * device s mod P.  Scored under interleaved 1F1B with M microbatches (M % P ==
+ * 0); rejected when a device's peak held bytes (the chunk-weighted ledger)
+ * exceeds `cap`.  first_best gets S+1 range starts. */
+int orc_search_interleaved(const int32_t *layer_tf, const int32_t *layer_tb, const int64_t *layer_act,
+                           int L, int P, int v, int M, int32_t comm, int64_t cap, uint64_t seed,
+                           int64_t c_lo, int64_t c_hi, int32_t *all_mk,
+                           int64_t *best_idx, int64_t *best_mk, int *first_best, int nthreads)
+{
+    return search_impl(layer_tf, layer_tb, layer_act, L, P, v, M, comm, cap, seed, 0, c_lo, c_hi, all_mk,
                        best_idx, best_mk, first_best, nthreads);
 }
 
@@ -926,7 +958,7 @@ int orc_search_ranks(const int32_t *layer_tf, const int32_t *layer_tb, const int
                      int64_t r_lo, int64_t r_hi, int32_t *all_mk,
                      int64_t *best_idx, int64_t *best_mk, int *first_best, int nthreads)
 {
-    return search_impl(layer_tf, layer_tb, layer_act, L, P, M, comm, cap, 0, 1, r_lo, r_hi, all_mk,
+    return search_impl(layer_tf, layer_tb, layer_act, L, P, 1, M, comm, cap, 0, 1, r_lo, r_hi, all_mk,
                        best_idx, best_mk, first_best, nthreads);
 }
 

@@ -335,6 +335,48 @@ def test_exhaustive_search_covers_every_split(orc):
     assert list(res["first"]) == [int(v) for v in orc.rank_split(res["best_idx"], L, P)]
 
 
+def test_interleaved_search_scores_layouts(orc):
+    """Each candidate splits the layers into P*v contiguous ranges (virtual
+    stage s on device s mod P); its score equals a direct interleaved
+    evaluation of the range sums, and it is rejected exactly when a device's
+    chunk-weighted held bytes peak above the cap.  With v = 1 the search is
+    the 1F1B search."""
+    rng = np.random.default_rng(23)
+    L, P, v, M, comm = 14, 3, 2, 6, 1
+    S = P * v
+    ltf = rng.integers(3, 12, L).astype(np.int32)
+    ltb = rng.integers(5, 25, L).astype(np.int32)
+    lact = rng.integers(1, 5, L).astype(np.int64)
+    cap = 40
+    res = orc.search_interleaved(ltf, ltb, lact, P, v, M, comm, cap, 99, 0, 120)
+    kind, chunk, _ = orc.order("interleaved", P, M, v)
+    rejected = 0
+    for c in range(120):
+        first = [int(x) for x in orc.candidate_split(99, c, L, S)]
+        tf = [int(ltf[first[s]:first[s + 1]].sum()) for s in range(S)]
+        tb = [int(ltb[first[s]:first[s + 1]].sum()) for s in range(S)]
+        act = [int(lact[first[s]:first[s + 1]].sum()) for s in range(S)]
+        top = []
+        for d in range(P):
+            held, hi = 0, 0
+            for j in range(kind.shape[1]):
+                a = act[chunk[d, j] * P + d]
+                held += a if kind[d, j] == 0 else -a
+                hi = max(hi, held)
+            top.append(hi)
+        if max(top) > cap:
+            rejected += 1
+            assert res["all_makespan"][c] == -1
+            continue
+        ev = orc.evaluate("interleaved", P, M, v, np.repeat(np.array(tf)[:, None], M, 1),
+                          np.repeat(np.array(tb)[:, None], M, 1), comm)
+        assert res["all_makespan"][c] == ev["makespan"]
+    assert 0 < rejected < 120
+    one = orc.search_interleaved(ltf, ltb, lact, P, 1, M, comm, cap, 99, 0, 50)
+    base = orc.search(ltf, ltb, lact, P, M, comm, cap, 99, 0, 50)
+    assert np.array_equal(one["all_makespan"], base["all_makespan"])
+
+
 MUTANTS = {
     1: "forward edges carry no comm",
     2: "1F1B warmup off by one",
