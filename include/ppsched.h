@@ -207,6 +207,31 @@ int pp_sched_partition_search_ranks(const int32_t *layer_tf, const int32_t *laye
                                     int64_t *best_rank, int32_t *best_makespan, int32_t *best_cuts,
                                     int32_t *all_makespan, cudaStream_t stream);
 
+/* The partition search over interleaved layouts ([M040] §06: a device holds
+ * several virtual stages; §05: split by measured cost and activation).  Each
+ * candidate c in [cand_begin, cand_begin + n_cand) cuts the L layers into
+ * S = P*v contiguous non-empty ranges: u = SplitMix64(seed + c),
+ * r = u mod C(L-1, S-1), unranked in colex order as pp_sched_partition_search
+ * does with S-1 cuts; range s is virtual stage s (chunk s / P of device
+ * s mod P).  A candidate is rejected when some device's held activation bytes
+ * peak above act_cap (the [1F1B] §4.1 ledger over the interleaved order, +
+ * the bytes of the op's range at F, - at B); the others are scored under
+ * PP_INTERLEAVED_1F1B with M microbatches, every boundary with latency `comm`.
+ * Outputs as pp_sched_partition_search; best_cuts has S-1 entries (first layer
+ * of ranges 1..S-1).
+ * Memory: the candidates are scored in chunks of up to 262,144 through a
+ * scratch cost table the library allocates on a device's first call (about
+ * 2 MB per virtual stage) and keeps; calls on one device share it, so calls
+ * that overlap on the GPU must be serialized.  The first call for a shape also
+ * builds its plan.
+ * Limits: v >= 2, P*v <= PP_MAX_S, M % P == 0, S <= L <= 256, n_cand < 2^32.
+ * Errors: PP_ERR_ARG, PP_ERR_DIVISIBILITY, PP_ERR_SIZE, PP_ERR_CUDA. */
+int pp_sched_partition_search_interleaved(const int32_t *layer_tf, const int32_t *layer_tb,
+                                          const int64_t *layer_act, int L, int P, int v, int M, int32_t comm,
+                                          int64_t act_cap, uint64_t seed, int64_t cand_begin, int64_t n_cand,
+                                          int64_t *best_idx, int32_t *best_makespan, int32_t *best_cuts,
+                                          int32_t *all_makespan, cudaStream_t stream);
+
 /* pp_sched_eval for GPipe and 1F1B that allocates no device memory.  (This
  * entry point has no counterpart on the pages; it exists for callers that
  * cannot let a library call cudaMalloc, e.g. code whose device memory belongs to

@@ -22,7 +22,7 @@ ST_OK, ST_NEG_COST, ST_OVERFLOW, ST_ZERO_COST = 0, 1, 2, 3
 EXPORTS = ("pp_sched_plan", "pp_sched_plan_info", "pp_sched_plan_ops", "pp_sched_plan_destroy",
            "pp_sched_eval", "pp_sched_partition_search", "pp_sched_status_str",
            "pp_sched_cache_clear", "pp_sched_eval_noalloc", "pp_sched_eval_zb",
-           "pp_sched_partition_search_ranks")
+           "pp_sched_partition_search_ranks", "pp_sched_partition_search_interleaved")
 
 
 class PPSchedError(RuntimeError):
@@ -56,6 +56,9 @@ def _load():
     lib.pp_sched_partition_search_ranks.argtypes = [vp, vp, vp, i32, i32, i32, ctypes.c_int32, i64, i64, i64,
                                                     vp, vp, vp, vp, vp]
     lib.pp_sched_partition_search_ranks.restype = i32
+    lib.pp_sched_partition_search_interleaved.argtypes = [vp, vp, vp, i32, i32, i32, i32, ctypes.c_int32, i64, u64,
+                                                          i64, i64, vp, vp, vp, vp, vp]
+    lib.pp_sched_partition_search_interleaved.restype = i32
     lib.pp_sched_status_str.argtypes = [i32]
     lib.pp_sched_status_str.restype = ctypes.c_char_p
     lib.pp_sched_eval_noalloc.argtypes = [i32, i32, i32, vp, vp, i64, i64, i64, vp, i64, i64, i64,
@@ -299,6 +302,27 @@ def partition_search_ranks(layer_tf, layer_tb, layer_act, P, M, comm, cap, rank_
                                              int(comm), int(cap), int(rank_begin), int(n_ranks), _ptr(bi),
                                              _ptr(bm), _ptr(bc) if P > 1 else None, _ptr(am), _stream(stream))
     _check(rc, "pp_sched_partition_search_ranks")
+    return out
+
+
+def partition_search_interleaved(layer_tf, layer_tb, layer_act, P, v, M, comm, cap, seed, cand_begin, n_cand,
+                                 all_makespan=False, out=None, stream=None):
+    """Call pp_sched_partition_search_interleaved (S = P*v ranges).  Returns
+    dict(best_idx, best_makespan, best_cuts int32[S-1], all_makespan)."""
+    dev = layer_tf.device
+    out = dict(out or {})
+    bi = out.setdefault("best_idx", torch.empty(1, dtype=torch.int64, device=dev))
+    bm = out.setdefault("best_makespan", torch.empty(1, dtype=torch.int32, device=dev))
+    bc = out.setdefault("best_cuts", torch.empty(P * v - 1, dtype=torch.int32, device=dev))
+    am = None
+    if all_makespan:
+        am = out.setdefault("all_makespan", torch.empty(n_cand, dtype=torch.int32, device=dev))
+    L = layer_tf.numel()
+    rc = LIB.pp_sched_partition_search_interleaved(_ptr(layer_tf), _ptr(layer_tb), _ptr(layer_act), L, P, v, M,
+                                                   int(comm), int(cap), ctypes.c_uint64(seed & (2**64 - 1)),
+                                                   int(cand_begin), int(n_cand), _ptr(bi), _ptr(bm), _ptr(bc),
+                                                   _ptr(am), _stream(stream))
+    _check(rc, "pp_sched_partition_search_interleaved")
     return out
 
 

@@ -1,0 +1,299 @@
+// search_ilv.cu -- the partition search over interleaved layouts
+// (pp_sched_partition_search_interleaved).
+//
+// "Pipeline scheduling" (M040) §06: one device can hold several virtual
+// stages (segments 0..3 in order, device A holding 0 and 2, B holding 1 and
+// 3); §05: split by measured computation and activation.  A candidate cuts the
+// L layers into S = P*v contiguous non-empty ranges (a seeded draw of a colex
+// rank, as the 1F1B search); range s is virtual stage s, chunk s / P of device
+// s mod P.  It is rejected when a device's held activation bytes -- the
+// ledger of "2. 1F1B" §4.1 weighted by the bytes of each op's chunk -- peak
+// above the cap, and otherwise scored by its interleaved 1F1B makespan.
+//
+// The candidates of a call are processed in chunks of up to kChunk: one
+// kernel draws each candidate's split, writes its virtual stages' costs into a
+// scratch cost table laid out [S][chunk] (the evaluator's instance-minor
+// layout, costs the same for every microbatch) and runs the byte ledger; the
+// interleaved evaluator scores the chunk; a third kernel combines the results
+// and reduces (makespan, candidate) with one 64-bit atomicMin per warp into the
+// caller's best_idx word.  The scratch table is allocated on a device's first
+// call and kept (grown when a call needs more).
+#include <algorithm>
+#include <mutex>
+
+#include "eval_common.cuh"
+
+namespace pps {
+namespace {
+
+constexpr int kIlvMaxL = 256;
+constexpr int kChunk = 1 << 18;
+
+struct IlvArgs {
+    const int32_t *ltf, *ltb;
+    const int64_t *lact;
+    int L, P, v, S, M, O;
+    int64_t cap;
+    uint64_t seed;
+    int64_t begin;
+    uint64_t ncomb;        // C(L-1, S-1)
+    const uint32_t *ops;   // plan: [P][O] packed ops (kind bit 31, chunk bits 24..30)
+    int32_t *cf, *cb;      // scratch [S][cn]
+    int8_t *flag;          // scratch [cn]: 0 feasible, 1 over the cap, 2 a stage sum out of int32
+    int cn;                // stride of the scratch tables
+};
+
+__device__ __forceinline__ uint64_t ilv_splitmix64(uint64_t s) {
+    // SplitMix64 (Steele, Lea & Flood, OOPSLA 2014)
+    uint64_t z = s + 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+__device__ uint64_t ilv_binom(int n, int i) {
+    if (i < 0 || i > n) return 0;
+    if (i > n - i) i = n - i;
+    unsigned __int128 acc = 1;
+    for (int t = 1; t <= i; ++t) {
+        acc = acc * (unsigned)(n - i + t) / (unsigned)t;
+        if (acc > (unsigned __int128)0xFFFFFFFFFFFFFFFFull) return ~0ull;
+    }
+    return (uint64_t)acc;
+}
+
+// Dynamic shared memory: prefix sums of the layer costs and bytes, then
+// C(n, i) for n < L, i < S.
+struct IlvTables {
+    int64_t *pre_tf, *pre_tb, *pre_act;
+    uint64_t *C;  // [L][S]
+};
+
+__device__ IlvTables ilv_tables(const IlvArgs &a, unsigned char *smem) {
+    IlvTables t;
+    t.pre_tf = reinterpret_cast<int64_t *>(smem);
+    t.pre_tb = t.pre_tf + (a.L + 1);
+    t.pre_act = t.pre_tb + (a.L + 1);
+    t.C = reinterpret_cast<uint64_t *>(t.pre_act + (a.L + 1));
+    for (int e = threadIdx.x; e < a.L * a.S; e += blockDim.x) t.C[e] = ilv_binom(e / a.S, e % a.S);
+    if (threadIdx.x == 0) {
+        int64_t f = 0, b = 0, c = 0;
+        t.pre_tf[0] = t.pre_tb[0] = t.pre_act[0] = 0;
+        for (int l = 0; l < a.L; ++l) {
+            f += a.ltf[l]; b += a.ltb[l]; c += a.lact[l];
+            t.pre_tf[l + 1] = f; t.pre_tb[l + 1] = b; t.pre_act[l + 1] = c;
+        }
+    }
+    __syncthreads();
+    return t;
+}
+
+size_t ilv_smem(int L, int S) { return (size_t)3 * (L + 1) * sizeof(int64_t) + (size_t)L * S * sizeof(uint64_t); }
+
+// Colex unranking of r into S-1 cut positions; first[s] = first layer of
+// range s (first[0] = 0, first[S] = L).
+__device__ void ilv_unrank(const IlvArgs &a, const IlvTables &t, uint64_t r, int *first) {
+    int hi = a.L - 2;
+    for (int i = a.S - 1; i >= 1; --i) {
+        int c = hi;
+        while (c >= i && t.C[c * a.S + i] > r) --c;
+        r -= t.C[c * a.S + i];
+        first[i] = c + 1;
+        hi = c - 1;
+    }
+    first[0] = 0;
+    first[a.S] = a.L;
+}
+
+__global__ void __launch_bounds__(256) k_ilv_cands(const IlvArgs a, int64_t chunk0, int nchunk) {
+    extern __shared__ __align__(16) unsigned char ilv_sm[];
+    const IlvTables t = ilv_tables(a, ilv_sm);
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nchunk; i += gridDim.x * blockDim.x) {
+        int first[PP_MAX_S + 1];
+        int64_t act[PP_MAX_S];
+        const uint64_t r = ilv_splitmix64(a.seed + (uint64_t)(a.begin + chunk0 + i)) % a.ncomb;
+        ilv_unrank(a, t, r, first);
+        int8_t fl = 0;
+        for (int s = 0; s < a.S; ++s) {
+            const int64_t sf = t.pre_tf[first[s + 1]] - t.pre_tf[first[s]];
+            const int64_t sb = t.pre_tb[first[s + 1]] - t.pre_tb[first[s]];
+            act[s] = t.pre_act[first[s + 1]] - t.pre_act[first[s]];
+            if (sf < 0 || sb < 0 || sf > 0x7FFFFFFF || sb > 0x7FFFFFFF) fl = 2;
+            a.cf[(int64_t)s * a.cn + i] = (int32_t)sf;
+            a.cb[(int64_t)s * a.cn + i] = (int32_t)sb;
+        }
+        // held bytes per device: + the chunk's bytes at F, - at B, running max
+        for (int d = 0; d < a.P && fl == 0; ++d) {
+            int64_t held = 0, top = 0;
+            const uint32_t *row = a.ops + (int64_t)d * a.O;
+            for (int j = 0; j < a.O; ++j) {
+                const uint32_t op = __ldg(row + j);
+                const int64_t b = act[((op >> 24) & 0x7Fu) * a.P + d];
+                held += (op >> 31) ? -b : b;
+                top = max(top, held);
+            }
+            if (top > a.cap) fl = 1;
+        }
+        a.flag[i] = fl;
+    }
+}
+
+__global__ void __launch_bounds__(256) k_ilv_select(const int32_t *mk, const int8_t *status, const int8_t *flag,
+                                                    int nchunk, int64_t chunk0, int32_t *all_mk,
+                                                    unsigned long long *key) {
+    const int lane = threadIdx.x & 31;
+    for (int base = blockIdx.x * blockDim.x; base < nchunk; base += gridDim.x * blockDim.x) {
+        const int i = base + threadIdx.x;
+        int m = -1;
+        if (i < nchunk) {
+            const int8_t f = flag[i];
+            m = f == 1 ? -1 : ((f == 2 || status[i] != PP_ST_OK) ? -2 : mk[i]);
+            if (all_mk) all_mk[chunk0 + i] = m;
+        }
+        unsigned long long k = ~0ull;
+        if (i < nchunk && m >= 0) k = ((unsigned long long)(uint32_t)m << 32) | (uint32_t)(chunk0 + i);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, k, o);
+            k = other < k ? other : k;
+        }
+        if (lane == 0 && k != ~0ull) atomicMin(key, k);
+    }
+}
+
+__global__ void k_ilv_finish(const IlvArgs a, const unsigned long long *key, int64_t *best_idx, int32_t *best_mk,
+                             int32_t *best_cuts) {
+    extern __shared__ __align__(16) unsigned char ilv_sm[];
+    const IlvTables t = ilv_tables(a, ilv_sm);
+    if (threadIdx.x != 0) return;
+    const unsigned long long k = *key;
+    if (k == ~0ull) {
+        *best_idx = -1;
+        if (best_mk) *best_mk = -1;
+        if (best_cuts) for (int s = 0; s + 1 < a.S; ++s) best_cuts[s] = -1;
+        return;
+    }
+    const int64_t ci = (int64_t)(k & 0xFFFFFFFFull);
+    if (best_cuts) {
+        int first[PP_MAX_S + 1];
+        ilv_unrank(a, t, ilv_splitmix64(a.seed + (uint64_t)(a.begin + ci)) % a.ncomb, first);
+        for (int s = 1; s < a.S; ++s) best_cuts[s - 1] = first[s];
+    }
+    if (best_mk) *best_mk = (int)(k >> 32);
+    *best_idx = a.begin + ci;
+}
+
+uint64_t ilv_host_binom(int n, int k) {
+    if (k < 0 || k > n) return 0;
+    if (k > n - k) k = n - k;
+    unsigned __int128 acc = 1;
+    for (int t = 1; t <= k; ++t) {
+        acc = acc * (unsigned)(n - k + t) / (unsigned)t;
+        if (acc > (unsigned __int128)0xFFFFFFFFFFFFFFFFull) return ~0ull;
+    }
+    return (uint64_t)acc;
+}
+
+// Per-device scratch: cost tables [S][cn] x 2, makespan, status, flag, comm.
+struct IlvScratch {
+    void *p = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_ilv_mu;
+IlvScratch g_ilv[64];
+
+int ilv_scratch(size_t need, void **out) {
+    int dev = 0;
+    PPS_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return PP_ERR_SIZE;
+    IlvScratch &s = g_ilv[dev];
+    if (s.bytes < need) {
+        if (s.p) PPS_CUDA_TRY(cudaFree(s.p));
+        s.p = nullptr;
+        s.bytes = 0;
+        PPS_CUDA_TRY(cudaMalloc(&s.p, need));
+        s.bytes = need;
+    }
+    *out = s.p;
+    return PP_OK;
+}
+
+}  // namespace
+}  // namespace pps
+
+extern "C" int pp_sched_partition_search_interleaved(const int32_t *layer_tf, const int32_t *layer_tb,
+                                                     const int64_t *layer_act, int L, int P, int v, int M,
+                                                     int32_t comm, int64_t act_cap, uint64_t seed,
+                                                     int64_t cand_begin, int64_t n_cand, int64_t *best_idx,
+                                                     int32_t *best_makespan, int32_t *best_cuts,
+                                                     int32_t *all_makespan, cudaStream_t stream) {
+    using namespace pps;
+    if (!layer_tf || !layer_tb || !layer_act || !best_idx) return PP_ERR_ARG;
+    if (P < 1 || v < 2 || M < 1 || n_cand < 0 || cand_begin < 0 || comm < 0) return PP_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(best_idx) & 7) != 0) return PP_ERR_ARG;
+    const int S = P * v;
+    if (P > PP_MAX_P || S > PP_MAX_S || L > kIlvMaxL || (int64_t)M * v > PP_MAX_MV || n_cand >= (int64_t)1 << 32)
+        return PP_ERR_SIZE;
+    if (L < S) return PP_ERR_ARG;
+    if (M % P != 0) return PP_ERR_DIVISIBILITY;
+    const uint64_t ncomb = ilv_host_binom(L - 1, S - 1);
+    if (ncomb == ~0ull || ncomb == 0) return PP_ERR_SIZE;
+    pp_plan *plan = nullptr;
+    int rc = cached_plan(PP_INTERLEAVED_1F1B, P, M, v, stream, &plan);
+    if (rc) return rc;
+
+    std::lock_guard<std::mutex> lk(g_ilv_mu);
+    const int cn = (int)std::min<int64_t>(kChunk, std::max<int64_t>(32, (n_cand + 31) / 32 * 32));
+    const size_t cost_bytes = (size_t)S * cn * sizeof(int32_t);
+    const size_t need = 2 * cost_bytes + (size_t)cn * (sizeof(int32_t) + 2) + 256;
+    void *scratch = nullptr;
+    rc = ilv_scratch(need, &scratch);
+    if (rc) return rc;
+    unsigned char *base = static_cast<unsigned char *>(scratch);
+    int32_t *cf = reinterpret_cast<int32_t *>(base);
+    int32_t *cb = reinterpret_cast<int32_t *>(base + cost_bytes);
+    int32_t *mk = reinterpret_cast<int32_t *>(base + 2 * cost_bytes);
+    int32_t *dcomm = mk + cn;  // one word, broadcast to every instance and boundary
+    int8_t *st = reinterpret_cast<int8_t *>(dcomm + 4);
+    int8_t *flag = st + cn;
+
+    IlvArgs a;
+    a.ltf = layer_tf; a.ltb = layer_tb; a.lact = layer_act;
+    a.L = L; a.P = P; a.v = v; a.S = S; a.M = M; a.O = plan->O;
+    a.cap = act_cap; a.seed = seed; a.begin = cand_begin; a.ncomb = ncomb;
+    a.ops = plan->d_ops; a.cf = cf; a.cb = cb; a.flag = flag; a.cn = cn;
+    const size_t smem = ilv_smem(L, S);
+    static bool attr_set[64] = {};
+    int dev = 0;
+    PPS_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 64 && !attr_set[dev]) {
+        PPS_CUDA_TRY(cudaFuncSetAttribute(k_ilv_cands, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
+        PPS_CUDA_TRY(cudaFuncSetAttribute(k_ilv_finish, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
+        attr_set[dev] = true;
+    }
+    unsigned long long *key = reinterpret_cast<unsigned long long *>(best_idx);
+    PPS_CUDA_TRY(cudaMemsetAsync(best_idx, 0xFF, sizeof(int64_t), stream));
+    PPS_CUDA_TRY(cudaMemcpyAsync(dcomm, &comm, sizeof(int32_t), cudaMemcpyHostToDevice, stream));
+
+    EvalArgs e{};
+    e.desc = plan->d_desc; e.desc2 = plan->d_desc2; e.rw = plan->d_rw; e.seg = plan->d_seg; e.nseg = plan->nseg;
+    e.R = plan->R; e.P = P; e.M = M; e.v = v; e.S = S; e.O = plan->O; e.nslots = plan->nslots;
+    e.cost_f = cf; e.cost_b = cb; e.s_inst = 1; e.s_stage = cn; e.s_mb = 0;
+    e.comm = dcomm; e.c_inst = 0; e.c_bnd = 0;
+    e.makespan = mk; e.status = st;
+    for (int64_t c0 = 0; c0 < n_cand; c0 += cn) {
+        const int nc = (int)std::min<int64_t>(cn, n_cand - c0);
+        const unsigned blocks = (unsigned)((nc + 255) / 256);
+        k_ilv_cands<<<blocks, 256, smem, stream>>>(a, c0, nc);
+        PPS_CUDA_TRY(cudaGetLastError());
+        e.n = nc;
+        rc = lane_path(plan, e) ? launch_eval_lane(plan, e, true, false, stream)
+                                : launch_eval_slot(plan, e, true, false, stream);
+        if (rc) return rc;
+        k_ilv_select<<<blocks, 256, 0, stream>>>(mk, st, flag, nc, c0, all_makespan, key);
+        PPS_CUDA_TRY(cudaGetLastError());
+    }
+    k_ilv_finish<<<1, 64, smem, stream>>>(a, key, best_idx, best_makespan, best_cuts);
+    PPS_CUDA_TRY(cudaGetLastError());
+    return PP_OK;
+}

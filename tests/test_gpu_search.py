@@ -147,3 +147,75 @@ def test_exhaustive_layer_split_full(orc, B):
         parts.append((int(g["best_makespan"].item()), int(g["best_idx"].item())))
     from pipeline_schedule_simulation_gb300.sharding import best_of
     assert best_of([q for q in parts if q[1] >= 0]) == (mk, best)
+
+
+@pytest.mark.parametrize("L,P,v,M,comm,cap", [(14, 3, 2, 6, 1, 40), (20, 4, 2, 8, 2, 10**12), (24, 2, 4, 4, 0, 60),
+                                              (40, 8, 2, 16, 1, 10**12), (70, 16, 3, 16, 2, 10**12)])
+def test_interleaved_search_exact(orc, B, L, P, v, M, comm, cap):
+    """Seeded interleaved layouts: every makespan (rejected, scored) and the
+    winner equal the oracle's."""
+    rng = np.random.default_rng(L + 3 * P + v)
+    ltf = rng.integers(1, 20, L).astype(np.int32)
+    ltb = rng.integers(1, 40, L).astype(np.int32)
+    lact = rng.integers(1, 4, L).astype(np.int64)
+    n = 1500
+    g = B.partition_search_interleaved(to_dev(ltf), to_dev(ltb), to_dev(lact), P, v, M, comm, cap, 4321, 0, n,
+                                       all_makespan=True)
+    torch.cuda.synchronize()
+    r = orc.search_interleaved(ltf, ltb, lact, P, v, M, comm, cap, 4321, 0, n, nthreads=8)
+    assert np.array_equal(g["all_makespan"].cpu().numpy(), r["all_makespan"])
+    assert int(g["best_idx"].item()) == r["best_idx"]
+    assert int(g["best_makespan"].item()) == r["best_makespan"]
+    if r["best_idx"] >= 0:
+        assert list(g["best_cuts"].cpu().numpy()) == list(r["first"][1:P * v])
+
+
+def test_interleaved_search_chunks_and_ranges(orc, B):
+    """More candidates than one scratch chunk (262,144): sampled makespans
+    against the oracle, and two ranges reduce to the whole."""
+    rng = np.random.default_rng(5)
+    L, P, v, M = 30, 2, 2, 4
+    ltf = rng.integers(1, 30, L).astype(np.int32)
+    ltb = rng.integers(1, 60, L).astype(np.int32)
+    lact = rng.integers(1, 4, L).astype(np.int64)
+    n = 600_000
+    cap = 100
+    args = (to_dev(ltf), to_dev(ltb), to_dev(lact), P, v, M, 1, cap, 77)
+    whole = B.partition_search_interleaved(*args, 0, n, all_makespan=True)
+    torch.cuda.synchronize()
+    mk = whole["all_makespan"].cpu().numpy()
+    for lo in (0, 262_140, 524_280, n - 40):
+        r = orc.search_interleaved(ltf, ltb, lact, P, v, M, 1, cap, 77, lo, lo + 40)
+        assert np.array_equal(mk[lo:lo + 40], r["all_makespan"])
+    feas = mk >= 0
+    assert feas.any() and not feas.all()
+    best = int(whole["best_idx"].item())
+    assert mk[best] == mk[feas].min() == int(whole["best_makespan"].item())
+    assert best == int(np.nonzero(mk == mk[feas].min())[0][0])
+    parts = []
+    for lo, hi in ((0, 250_000), (250_000, n)):
+        g = B.partition_search_interleaved(*args, lo, hi - lo)
+        torch.cuda.synchronize()
+        parts.append((int(g["best_makespan"].item()), int(g["best_idx"].item())))
+    from pipeline_schedule_simulation_gb300.sharding import best_of
+    assert best_of(parts) == (int(whole["best_makespan"].item()), best)
+
+
+def test_interleaved_search_layer_split(orc, B):
+    """The 80-layer model as 16 virtual stages (P=8, v=2, M=128), 65,536
+    layouts: the winner and 40 sampled layouts re-scored by the oracle."""
+    p = W.layer_split()
+    args = (to_dev(p.layer_tf), to_dev(p.layer_tb), to_dev(p.layer_act), p.P, 2, p.M, p.comm, p.cap, p.seed)
+    g = B.partition_search_interleaved(*args, 0, 1 << 16, all_makespan=True)
+    torch.cuda.synchronize()
+    mk = g["all_makespan"].cpu().numpy()
+    best = int(g["best_idx"].item())
+    assert best >= 0 and mk[best] == mk[mk >= 0].min()
+    r = orc.search_interleaved(p.layer_tf, p.layer_tb, p.layer_act, p.P, 2, p.M, p.comm, p.cap, p.seed,
+                               best, best + 1)
+    assert r["best_makespan"] == int(g["best_makespan"].item())
+    assert list(g["best_cuts"].cpu().numpy()) == list(r["first"][1:16])
+    for lo in np.random.default_rng(3).choice((1 << 16) - 8, 5, replace=False):
+        rs = orc.search_interleaved(p.layer_tf, p.layer_tb, p.layer_act, p.P, 2, p.M, p.comm, p.cap, p.seed,
+                                    int(lo), int(lo) + 8, nthreads=8)
+        assert np.array_equal(mk[lo:lo + 8], rs["all_makespan"])
