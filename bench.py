@@ -438,6 +438,13 @@ def secondary(B, W, torch, stream):
     ex = {}
     t = timed(lambda: ex.update(B.partition_search_ranks(lt, lb, la, p.P, p.M, p.comm, p.cap, 0, total,
                                                          stream=stream)), 3)
+    il = {}
+    n_il = 1 << 20
+    t = timed(lambda: il.update(B.partition_search_interleaved(lt, lb, la, p.P, 2, p.M, p.comm, p.cap, p.seed, 0,
+                                                               n_il, stream=stream)), 3)
+    out["partition_search_interleaved_L80_P8_v2_M128_1M"] = {
+        "candidates_per_s": n_il / t, "ms": t * 1e3, "op_times_per_candidate": 2 * p.P * p.M * 2,
+        "best_idx": int(il["best_idx"].item()), "best_makespan": int(il["best_makespan"].item())}
     out["partition_search_exhaustive_L80_P8_M128"] = {
         "splits": total, "splits_per_s": total / t, "ms": t * 1e3,
         "best_rank": int(ex["best_idx"].item()), "best_makespan": int(ex["best_makespan"].item()),
