@@ -63,6 +63,9 @@ extern "C" {
  *    v-1-(j mod Pv)/P of the same microbatch.  Requires M % P == 0 ([M040] §06).
  *    The pages give the bubble, (P-1)/(vM+P-1) ([1F1B] §6.1), not the order; this
  *    order is the Megatron interleaved schedule they refer to.
+ *  PP_GPIPE_FIFO: GPipe with the backwards in first-in-first-out order, B of
+ *    microbatches 0..M-1 (the variant of [M040] §02's last-in-first-out table;
+ *    the same makespan at uniform costs, other op times).
  *  PP_ZB1P, PP_ZB2P (Zero Bubble; only through pp_sched_eval_zb): the backward
  *    splits into B (input gradient) and W (weight gradient, no cross-stage
  *    edge); see pp_sched_eval_zb ([GPipe->ZB] "Zero Bubble", "ZB1P and ZB2P"). */
@@ -71,7 +74,8 @@ typedef enum {
     PP_1F1B = 1,
     PP_INTERLEAVED_1F1B = 2,
     PP_ZB1P = 3,
-    PP_ZB2P = 4
+    PP_ZB2P = 4,
+    PP_GPIPE_FIFO = 5
 } pp_policy_t;
 
 /* Return codes. */

@@ -25,8 +25,9 @@ _SRC = os.path.join(_HERE, "ppsim_oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libppsim_oracle.so")
 
-GPIPE, ONEF1B, INTERLEAVED, ZB1P, ZB2P = 0, 1, 2, 3, 4
-POLICIES = {"gpipe": GPIPE, "1f1b": ONEF1B, "interleaved": INTERLEAVED, "zb1p": ZB1P, "zb2p": ZB2P}
+GPIPE, ONEF1B, INTERLEAVED, ZB1P, ZB2P, GPIPE_FIFO = 0, 1, 2, 3, 4, 5
+POLICIES = {"gpipe": GPIPE, "1f1b": ONEF1B, "interleaved": INTERLEAVED, "zb1p": ZB1P, "zb2p": ZB2P,
+            "gpipe_fifo": GPIPE_FIFO}
 F, B, W = 0, 1, 2
 
 OK, ERR_ARG, ERR_DIVISIBILITY, ERR_DEADLOCK, ERR_INVARIANT, ERR_NOMEM = 0, 1, 2, 5, 6, 7
@@ -69,6 +70,12 @@ def _bind(lib):
     lib.orc_eval_batch.argtypes = [c_int, c_int, c_int, c_int, c_i64, vp, vp, c_i64, c_i64, c_i64,
                                    vp, c_i64, c_i64, vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int]
     lib.orc_eval_batch.restype = c_int
+    lib.orc_eval_batch_fb.argtypes = [c_int, c_int, c_int, c_int, c_i64, vp, vp, c_i64, c_i64, c_i64,
+                                      vp, vp, c_i64, c_i64, vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int]
+    lib.orc_eval_batch_fb.restype = c_int
+    lib.orc_eval_explicit_fb.argtypes = [c_int, c_int, c_int, vp, vp, vp, vp, vp, vp, vp, c_int,
+                                         vp, vp, vp, vp, vp, vp, vp]
+    lib.orc_eval_explicit_fb.restype = c_int
     lib.orc_bruteforce.argtypes = [c_int, c_int, vp]
     lib.orc_bruteforce.restype = c_int
     lib.orc_search.argtypes = [vp, vp, vp, c_int, c_int, c_int, ctypes.c_int32, c_i64, c_u64,
@@ -130,10 +137,11 @@ def order(policy, P, M, v=1, lib=None):
     return kind, chunk, mb
 
 
-def eval_explicit(P, M, v, kind, chunk, mb, tf, tb, comm=None, method=2, lib=None):
+def eval_explicit(P, M, v, kind, chunk, mb, tf, tb, comm=None, method=2, lib=None, comm_b=None):
     """Evaluate one instance with an explicit order.
 
-    tf, tb: [S][M] costs; comm: [S-1] or None.  method 0 = event simulation,
+    tf, tb: [S][M] costs; comm: [S-1] or None; comm_b: [S-1] latency of the
+    backward edges (None: the same as comm).  method 0 = event simulation,
     1 = longest path, 2 = both (must agree).  Returns a dict with start, end
     ([P][O]), makespan, busy, idle, bub (num, den), peak; raises OracleError on
     deadlock or a failed validity check.
@@ -146,6 +154,8 @@ def eval_explicit(P, M, v, kind, chunk, mb, tf, tb, comm=None, method=2, lib=Non
     tf = np.ascontiguousarray(np.broadcast_to(np.asarray(tf, np.int64), (S, M)))
     tb = np.ascontiguousarray(np.broadcast_to(np.asarray(tb, np.int64), (S, M)))
     cm = None if comm is None else np.ascontiguousarray(np.broadcast_to(np.asarray(comm, np.int64), (max(S - 1, 1),)))
+    cmb = None if comm_b is None else np.ascontiguousarray(
+        np.broadcast_to(np.asarray(comm_b, np.int64), (max(S - 1, 1),)))
     start = np.zeros((P, O), np.int64)
     end = np.zeros((P, O), np.int64)
     mk = np.zeros(1, np.int64)
@@ -153,33 +163,35 @@ def eval_explicit(P, M, v, kind, chunk, mb, tf, tb, comm=None, method=2, lib=Non
     idle = np.zeros(P, np.int64)
     bub = np.zeros(2, np.int64)
     peak = np.zeros(P, np.int32)
-    rc = lib.orc_eval_explicit(P, M, v, _ptr(kind), _ptr(chunk), _ptr(mb), _ptr(tf), _ptr(tb),
-                               _ptr(cm), method, _ptr(start), _ptr(end), _ptr(mk), _ptr(busy),
-                               _ptr(idle), _ptr(bub), _ptr(peak))
+    rc = lib.orc_eval_explicit_fb(P, M, v, _ptr(kind), _ptr(chunk), _ptr(mb), _ptr(tf), _ptr(tb),
+                                  _ptr(cm), _ptr(cmb), method, _ptr(start), _ptr(end), _ptr(mk), _ptr(busy),
+                                  _ptr(idle), _ptr(bub), _ptr(peak))
     if rc != OK:
         raise OracleError(rc, "eval_explicit")
     return dict(start=start, end=end, makespan=int(mk[0]), busy=busy, idle=idle,
                 bub=(int(bub[0]), int(bub[1])), peak=peak)
 
 
-def evaluate(policy, P, M, v, tf, tb, comm=None, method=2, lib=None):
+def evaluate(policy, P, M, v, tf, tb, comm=None, method=2, lib=None, comm_b=None):
     """Generate the policy's order and evaluate one instance (see eval_explicit)."""
     kind, chunk, mb = order(policy, P, M, v, lib=lib)
-    r = eval_explicit(P, M, v, kind, chunk, mb, tf, tb, comm, method, lib=lib)
+    r = eval_explicit(P, M, v, kind, chunk, mb, tf, tb, comm, method, lib=lib, comm_b=comm_b)
     r.update(kind=kind, chunk=chunk, mb=mb)
     return r
 
 
 def eval_batch(policy, P, M, v, cost_f, cost_b, strides, comm=None, comm_strides=(0, 0), n=None,
-               op_times=False, method=0, nthreads=1, lib=None):
+               op_times=False, method=0, nthreads=1, lib=None, comm_b=None):
     """Evaluate n instances.  cost_f/cost_b are flat int32 buffers indexed by
     element strides (inst, stage, mb); comm a flat int32 buffer indexed by
-    (inst, boundary) strides or None.  Returns dict of numpy outputs."""
+    (inst, boundary) strides or None; comm_b the backward edges' latency with
+    comm's strides (None: the same as comm).  Returns dict of numpy outputs."""
     lib = lib or load()
     S, O = P * v, 2 * M * v
     cost_f = np.ascontiguousarray(cost_f, np.int32).reshape(-1)
     cost_b = np.ascontiguousarray(cost_b, np.int32).reshape(-1)
     cm = None if comm is None else np.ascontiguousarray(comm, np.int32).reshape(-1)
+    cmb = None if comm_b is None else np.ascontiguousarray(comm_b, np.int32).reshape(-1)
     if n is None:
         raise ValueError("n required")
     out = dict(
@@ -189,9 +201,9 @@ def eval_batch(policy, P, M, v, cost_f, cost_b, strides, comm=None, comm_strides
     if op_times:
         out["op_start"] = np.zeros((n, P, O), np.int64)
         out["op_end"] = np.zeros((n, P, O), np.int64)
-    rc = lib.orc_eval_batch(_policy(policy), P, M, v, n, _ptr(cost_f), _ptr(cost_b),
-                            strides[0], strides[1], strides[2], _ptr(cm), comm_strides[0],
-                            comm_strides[1], _ptr(out["makespan"]), _ptr(out["idle"]),
+    rc = lib.orc_eval_batch_fb(_policy(policy), P, M, v, n, _ptr(cost_f), _ptr(cost_b),
+                               strides[0], strides[1], strides[2], _ptr(cm), _ptr(cmb), comm_strides[0],
+                               comm_strides[1], _ptr(out["makespan"]), _ptr(out["idle"]),
                             _ptr(out["bub_num"]), _ptr(out["bub_den"]), _ptr(out["peak"]),
                             _ptr(out["status"]), _ptr(out.get("op_start")), _ptr(out.get("op_end")),
                             method, nthreads)

@@ -55,6 +55,7 @@
 #define ORC_GPIPE 0
 #define ORC_1F1B 1
 #define ORC_INTERLEAVED 2
+#define ORC_GPIPE_FIFO 5
 
 #define ORC_F 0
 #define ORC_B 1
@@ -99,6 +100,13 @@ int orc_order(int policy, int P, int M, int v, int k, int *kind, int *chunk, int
 #else
         for (int i = M - 1; i >= 0; --i) { kind[n] = ORC_B; chunk[n] = 0; mb[n] = i; ++n; }
 #endif
+        return n;
+    }
+    if (policy == ORC_GPIPE_FIFO) {
+        /* the first-in-first-out variant of [M040] §02: backwards A..D */
+        if (v != 1) return -ORC_ERR_ARG;
+        for (int i = 0; i < M; ++i) { kind[n] = ORC_F; chunk[n] = 0; mb[n] = i; ++n; }
+        for (int i = 0; i < M; ++i) { kind[n] = ORC_B; chunk[n] = 0; mb[n] = i; ++n; }
         return n;
     }
     if (policy == ORC_1F1B) {
@@ -152,6 +160,7 @@ typedef struct {
     const int *kind, *chunk, *mb;   /* [P][O] op order */
     const int64_t *tf, *tb;     /* [S][M] costs of this instance */
     const int64_t *comm;        /* [S-1] edge latency (may be NULL: all 0) */
+    const int64_t *comm_b;      /* [S-1] latency of backward edges, NULL: the same as comm */
 } orc_inst;
 
 static int64_t op_cost(const orc_inst *in, int dev, int j)
@@ -165,6 +174,16 @@ static int64_t op_cost(const orc_inst *in, int dev, int j)
 static int64_t edge_comm(const orc_inst *in, int b)
 {
     return in->comm ? in->comm[b] : 0;
+}
+
+/* Backward edges may have their own latency ([M040] §05: a forward boundary
+ * carries the hidden activations, a backward one the activation gradients). */
+static int64_t edge_comm_b(const orc_inst *in, int b)
+{
+#if ORC_MUTANT == 12  /* mistake: backward edges take the forward latency */
+    return edge_comm(in, b);
+#endif
+    return in->comm_b ? in->comm_b[b] : edge_comm(in, b);
 }
 
 /* Locate every op (kind, s, i): pos[(kind*S + s)*M + i] = dev*O + j, or -1.
@@ -209,7 +228,7 @@ static int deps_of(const orc_inst *in, const int *pos, int dev, int j, int *dop,
 #endif
     } else {
 #if ORC_MUTANT != 4   /* mutant 4's mistake: B ignores the downstream gradient */
-        if (s < S - 1) { dop[nd] = pos[((int64_t)ORC_B * S + (s + 1)) * M + i]; dlat[nd] = edge_comm(in, s); ++nd; }
+        if (s < S - 1) { dop[nd] = pos[((int64_t)ORC_B * S + (s + 1)) * M + i]; dlat[nd] = edge_comm_b(in, s); ++nd; }
 #endif
         dop[nd] = pos[((int64_t)ORC_F * S + s) * M + i]; dlat[nd] = 0; ++nd;
     }
@@ -443,13 +462,29 @@ static int check_inst(const orc_inst *in, const int *pos, const int64_t *start, 
  * method 0: discrete-event simulation; 1: longest path; 2: both, and compare.
  * Outputs: start/end [P][O], makespan, busy[P], idle[P], bub (num, den), peak[P].
  * Returns ORC_OK, ORC_ERR_DEADLOCK, ORC_ERR_INVARIANT or ORC_ERR_NOMEM. */
+int orc_eval_explicit_fb(int P, int M, int v, const int *kind, const int *chunk, const int *mb,
+                         const int64_t *tf, const int64_t *tb, const int64_t *comm, const int64_t *comm_b,
+                         int method, int64_t *start, int64_t *end, int64_t *makespan, int64_t *busy,
+                         int64_t *idle, int64_t *bub, int *peak);
+
 int orc_eval_explicit(int P, int M, int v, const int *kind, const int *chunk, const int *mb,
                       const int64_t *tf, const int64_t *tb, const int64_t *comm, int method,
                       int64_t *start, int64_t *end, int64_t *makespan, int64_t *busy,
                       int64_t *idle, int64_t *bub, int *peak)
 {
+    return orc_eval_explicit_fb(P, M, v, kind, chunk, mb, tf, tb, comm, NULL, method, start, end, makespan,
+                                busy, idle, bub, peak);
+}
+
+/* As orc_eval_explicit, with a separate latency comm_b [S-1] on the backward
+ * edges (NULL: the same as comm). */
+int orc_eval_explicit_fb(int P, int M, int v, const int *kind, const int *chunk, const int *mb,
+                         const int64_t *tf, const int64_t *tb, const int64_t *comm, const int64_t *comm_b,
+                         int method, int64_t *start, int64_t *end, int64_t *makespan, int64_t *busy,
+                         int64_t *idle, int64_t *bub, int *peak)
+{
     if (P < 1 || M < 1 || v < 1) return ORC_ERR_ARG;
-    orc_inst in = { P, M, v, P * v, 2 * M * v, kind, chunk, mb, tf, tb, comm };
+    orc_inst in = { P, M, v, P * v, 2 * M * v, kind, chunk, mb, tf, tb, comm, comm_b };
     int total = P * in.O;
     int *pos = (int *)malloc((size_t)2 * in.S * M * sizeof(int));
     int64_t *s2 = (int64_t *)malloc((size_t)total * sizeof(int64_t));
@@ -502,7 +537,7 @@ typedef struct {
     int64_t n;
     const int32_t *cost_f, *cost_b;
     int64_t cs_inst, cs_stage, cs_mb;
-    const int32_t *comm;
+    const int32_t *comm, *comm_b;
     int64_t ms_inst, ms_bnd;
     int64_t *makespan, *idle, *bub_num, *bub_den;   /* idle [n][P] */
     int8_t *status;
@@ -520,13 +555,14 @@ static void *batch_worker(void *arg)
     int64_t *tf = (int64_t *)malloc((size_t)S * M * sizeof(int64_t));
     int64_t *tb = (int64_t *)malloc((size_t)S * M * sizeof(int64_t));
     int64_t *cm = (int64_t *)malloc((size_t)(S > 1 ? S - 1 : 1) * sizeof(int64_t));
+    int64_t *cmb = (int64_t *)malloc((size_t)(S > 1 ? S - 1 : 1) * sizeof(int64_t));
     int64_t *st = (int64_t *)malloc((size_t)P * O * sizeof(int64_t));
     int64_t *en = (int64_t *)malloc((size_t)P * O * sizeof(int64_t));
     int64_t *busy = (int64_t *)malloc((size_t)P * sizeof(int64_t));
     int64_t *idle = (int64_t *)malloc((size_t)P * sizeof(int64_t));
     int *peak = (int *)malloc((size_t)P * sizeof(int));
     jb->rc = ORC_OK;
-    if (!tf || !tb || !cm || !st || !en || !busy || !idle || !peak) { jb->rc = ORC_ERR_NOMEM; goto out; }
+    if (!tf || !tb || !cm || !cmb || !st || !en || !busy || !idle || !peak) { jb->rc = ORC_ERR_NOMEM; goto out; }
     for (int64_t x = jb->lo; x < jb->hi; ++x) {
         int neg = 0;
         for (int s = 0; s < S; ++s)
@@ -538,13 +574,14 @@ static void *batch_worker(void *arg)
             }
         for (int b = 0; b < S - 1; ++b) {
             cm[b] = jb->comm ? jb->comm[x * jb->ms_inst + b * jb->ms_bnd] : 0;
-            if (cm[b] < 0) neg = 1;
+            cmb[b] = jb->comm_b ? jb->comm_b[x * jb->ms_inst + b * jb->ms_bnd] : cm[b];
+            if (cm[b] < 0 || cmb[b] < 0) neg = 1;
         }
         int64_t mk = 0, bub[2] = {0, 0};
         int rc = ORC_OK;
         if (!neg)
-            rc = orc_eval_explicit(P, M, v, jb->kind, jb->chunk, jb->mb, tf, tb, cm, jb->method,
-                                   st, en, &mk, busy, idle, bub, peak);
+            rc = orc_eval_explicit_fb(P, M, v, jb->kind, jb->chunk, jb->mb, tf, tb, cm, cmb, jb->method,
+                                      st, en, &mk, busy, idle, bub, peak);
         if (rc) { jb->rc = rc; goto out; }
         int8_t status = ORC_ST_OK;
         if (neg) status = ORC_ST_NEG_COST;
@@ -563,7 +600,7 @@ static void *batch_worker(void *arg)
             }
     }
 out:
-    free(tf); free(tb); free(cm); free(st); free(en); free(busy); free(idle); free(peak);
+    free(tf); free(tb); free(cm); free(cmb); free(st); free(en); free(busy); free(idle); free(peak);
     return NULL;
 }
 
@@ -573,6 +610,14 @@ out:
  * bub_den[n]), int8 status[n], int32 peak[P], and optionally int64 op times
  * [n][P][O].  Instances are split statically over `nthreads` threads.
  * Returns ORC_OK or an ORC_ERR_* code. */
+int orc_eval_batch_fb(int policy, int P, int M, int v, int64_t n,
+                      const int32_t *cost_f, const int32_t *cost_b,
+                      int64_t cs_inst, int64_t cs_stage, int64_t cs_mb,
+                      const int32_t *comm, const int32_t *comm_b, int64_t ms_inst, int64_t ms_bnd,
+                      int64_t *makespan, int64_t *idle, int64_t *bub_num, int64_t *bub_den,
+                      int32_t *peak, int8_t *status, int64_t *op_start, int64_t *op_end,
+                      int method, int nthreads);
+
 int orc_eval_batch(int policy, int P, int M, int v, int64_t n,
                    const int32_t *cost_f, const int32_t *cost_b,
                    int64_t cs_inst, int64_t cs_stage, int64_t cs_mb,
@@ -580,6 +625,21 @@ int orc_eval_batch(int policy, int P, int M, int v, int64_t n,
                    int64_t *makespan, int64_t *idle, int64_t *bub_num, int64_t *bub_den,
                    int32_t *peak, int8_t *status, int64_t *op_start, int64_t *op_end,
                    int method, int nthreads)
+{
+    return orc_eval_batch_fb(policy, P, M, v, n, cost_f, cost_b, cs_inst, cs_stage, cs_mb, comm, NULL, ms_inst,
+                             ms_bnd, makespan, idle, bub_num, bub_den, peak, status, op_start, op_end, method,
+                             nthreads);
+}
+
+/* As orc_eval_batch, with a separate latency comm_b on the backward edges
+ * (same strides as comm; NULL: the same as comm). */
+int orc_eval_batch_fb(int policy, int P, int M, int v, int64_t n,
+                      const int32_t *cost_f, const int32_t *cost_b,
+                      int64_t cs_inst, int64_t cs_stage, int64_t cs_mb,
+                      const int32_t *comm, const int32_t *comm_b, int64_t ms_inst, int64_t ms_bnd,
+                      int64_t *makespan, int64_t *idle, int64_t *bub_num, int64_t *bub_den,
+                      int32_t *peak, int8_t *status, int64_t *op_start, int64_t *op_end,
+                      int method, int nthreads)
 {
     if (P < 1 || M < 1 || v < 1 || n < 0) return ORC_ERR_ARG;
     if (policy != ORC_INTERLEAVED && v != 1) return ORC_ERR_ARG;
@@ -606,7 +666,7 @@ int orc_eval_batch(int policy, int P, int M, int v, int64_t n,
         jb->policy = policy; jb->P = P; jb->M = M; jb->v = v; jb->n = n;
         jb->cost_f = cost_f; jb->cost_b = cost_b;
         jb->cs_inst = cs_inst; jb->cs_stage = cs_stage; jb->cs_mb = cs_mb;
-        jb->comm = comm; jb->ms_inst = ms_inst; jb->ms_bnd = ms_bnd;
+        jb->comm = comm; jb->comm_b = comm_b; jb->ms_inst = ms_inst; jb->ms_bnd = ms_bnd;
         jb->makespan = makespan; jb->idle = idle; jb->bub_num = bub_num; jb->bub_den = bub_den;
         jb->status = status; jb->op_start = op_start; jb->op_end = op_end;
         jb->method = method; jb->kind = kind; jb->chunk = chunk; jb->mb = mbv;

@@ -13,8 +13,9 @@ import torch
 
 from . import build_lib
 
-GPIPE, ONEF1B, INTERLEAVED, ZB1P, ZB2P = 0, 1, 2, 3, 4
-POLICIES = {"gpipe": GPIPE, "1f1b": ONEF1B, "interleaved": INTERLEAVED, "zb1p": ZB1P, "zb2p": ZB2P}
+GPIPE, ONEF1B, INTERLEAVED, ZB1P, ZB2P, GPIPE_FIFO = 0, 1, 2, 3, 4, 5
+POLICIES = {"gpipe": GPIPE, "1f1b": ONEF1B, "interleaved": INTERLEAVED, "zb1p": ZB1P, "zb2p": ZB2P,
+            "gpipe_fifo": GPIPE_FIFO}
 
 PP_OK, PP_ERR_ARG, PP_ERR_DIVISIBILITY, PP_ERR_SIZE, PP_ERR_CUDA, PP_ERR_DEADLOCK, PP_ERR_INTERNAL = range(7)
 ST_OK, ST_NEG_COST, ST_OVERFLOW, ST_ZERO_COST = 0, 1, 2, 3

@@ -35,7 +35,7 @@ constexpr uint32_t kOpB = 0x80000000u;  // PP_OP kind bit
 
 // The op at position j of device k, as a PP_OP-packed word.  Rules:
 //  GPipe: "Pipeline scheduling" (M040) §02 -- all F, then B from the last
-//    microbatch back to the first.
+//    microbatch back to the first (GPipe FIFO: B from the first to the last).
 //  1F1B: "2. 1F1B" §2.3 and §3.2 -- P-k forwards (at most M), then B,F pairs
 //    with the oldest outstanding backward first, then the remaining B.
 //  Interleaved: device k holds chunks c (virtual stage c*P+k); warmup
@@ -47,6 +47,9 @@ __device__ uint32_t op_at(int policy, int P, int M, int v, int k, int j) {
     auto B = [](uint32_t c, uint32_t i) { return kOpB | (c << 24) | i; };
     if (policy == PP_GPIPE) {
         return j < M ? F(0, j) : B(0, 2 * M - 1 - j);
+    }
+    if (policy == PP_GPIPE_FIFO) {
+        return j < M ? F(0, j) : B(0, j - M);
     }
     if (policy == PP_1F1B) {
         int w = min(P - k, M);
@@ -372,7 +375,8 @@ int cuda_status(cudaError_t e) {
 }
 
 int check_shape(int policy, int P, int M, int v) {
-    if (policy < PP_GPIPE || policy > PP_INTERLEAVED_1F1B) return PP_ERR_ARG;
+    if (policy != PP_GPIPE && policy != PP_1F1B && policy != PP_INTERLEAVED_1F1B && policy != PP_GPIPE_FIFO)
+        return PP_ERR_ARG;
     if (P < 1 || M < 1 || v < 1) return PP_ERR_ARG;
     if (policy != PP_INTERLEAVED_1F1B && v != 1) return PP_ERR_ARG;
     if (policy == PP_INTERLEAVED_1F1B && v < 2) return PP_ERR_ARG;

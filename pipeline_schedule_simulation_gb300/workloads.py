@@ -14,7 +14,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-GPIPE, ONEF1B, INTERLEAVED, ZB1P, ZB2P = 0, 1, 2, 3, 4
+GPIPE, ONEF1B, INTERLEAVED, ZB1P, ZB2P, GPIPE_FIFO = 0, 1, 2, 3, 4, 5
 
 
 @dataclass

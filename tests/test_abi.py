@@ -46,7 +46,10 @@ def test_host_argument_errors_without_gpu():
     def ev(pol, P, M, v, n=4, f=1, b=1, si=1):
         return L.pp_sched_eval(pol, P, M, v, f, b, si, 0, 0, nul, 0, 0, n, nul, nul, nul, nul,
                                nul, nul, nul, 0, 0, nul, nul)
-    assert ev(5, 4, 8, 1) == B.PP_ERR_ARG           # unknown policy
+    assert ev(9, 4, 8, 1) == B.PP_ERR_ARG           # unknown policy
+    assert ev(B.ZB1P, 4, 8, 1) == B.PP_ERR_ARG      # Zero Bubble needs pp_sched_eval_zb
+    assert ev(B.ZB2P, 4, 8, 1) == B.PP_ERR_ARG
+    assert ev(B.GPIPE_FIFO, 4, 8, 2) == B.PP_ERR_ARG   # v != 1 for GPipe FIFO
     assert ev(B.ONEF1B, 0, 8, 1) == B.PP_ERR_ARG    # P < 1
     assert ev(B.ONEF1B, 4, 0, 1) == B.PP_ERR_ARG    # M < 1
     assert ev(B.ONEF1B, 4, 8, 2) == B.PP_ERR_ARG    # v != 1 for 1F1B

@@ -51,6 +51,7 @@ SHAPES = [
     (W.GPIPE, 8, 64, 1), (W.ONEF1B, 12, 20, 1), (W.ONEF1B, 16, 40, 1), (W.GPIPE, 16, 9, 1),
     (W.INTERLEAVED, 2, 4, 2), (W.INTERLEAVED, 4, 8, 2), (W.INTERLEAVED, 3, 9, 3),
     (W.INTERLEAVED, 8, 16, 4), (W.INTERLEAVED, 16, 32, 2), (W.INTERLEAVED, 1, 3, 5),
+    (W.GPIPE_FIFO, 1, 4, 1), (W.GPIPE_FIFO, 3, 7, 1), (W.GPIPE_FIFO, 8, 16, 1), (W.GPIPE_FIFO, 16, 5, 1),
 ]
 
 

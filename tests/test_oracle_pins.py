@@ -377,6 +377,53 @@ def test_interleaved_search_scores_layouts(orc):
     assert np.array_equal(one["all_makespan"], base["all_makespan"])
 
 
+def test_gpipe_fifo_variant(orc):
+    """GPipe with first-in-first-out backwards: the same makespan as GPipe's
+    last-in-first-out order at costs uniform over microbatches (R1), other op
+    times, the same peak M; both evaluators agree on heterogeneous costs."""
+    for P, M in ((2, 4), (4, 8), (5, 3), (8, 16)):
+        for tf, tb in ((1, 1), (1, 2), (3, 5)):
+            fifo = orc.evaluate("gpipe_fifo", P, M, 1, tf, tb)
+            lifo = orc.evaluate("gpipe", P, M, 1, tf, tb)
+            assert fifo["makespan"] == lifo["makespan"] == (M + P - 1) * (tf + tb)
+            assert list(fifo["peak"]) == [M] * P
+            # same ticks per position, other microbatches at them: B of
+            # microbatch 0 runs first under FIFO and last under LIFO
+            assert np.array_equal(fifo["start"], lifo["start"])
+            if M > 1:
+                assert fifo["mb"][0, M] == 0 and lifo["mb"][0, M] == M - 1
+            kind, _, mb = orc.order("gpipe_fifo", P, M)
+            assert list(mb[0, M:]) == list(range(M)) and (kind[:, M:] == 1).all()
+    rng = np.random.default_rng(29)
+    for _ in range(20):
+        P, M = int(rng.integers(1, 7)), int(rng.integers(1, 10))
+        r = orc.evaluate("gpipe_fifo", P, M, 1, rng.integers(0, 9, (P, M)), rng.integers(0, 9, (P, M)),
+                         rng.integers(0, 4, max(P - 1, 1)), method=2)
+        assert r["makespan"] >= 0
+
+
+def test_separate_forward_backward_comm(orc):
+    """Forward edges with latency c_f and backward edges with c_b: GPipe at
+    uniform costs ends at (M+P-1)(t_f+t_b) + (P-1)(c_f+c_b) (the forward chain
+    crosses P-1 forward edges and the gradient chain P-1 backward edges; the
+    case c_f = c_b is the invariant above); c_b = c_f everywhere equals a
+    single comm; both evaluators agree on heterogeneous inputs."""
+    for P, M in ((2, 3), (4, 8), (6, 5)):
+        for cf_, cb_ in ((1, 4), (3, 0), (2, 2)):
+            r = orc.evaluate("gpipe", P, M, 1, 2, 3, cf_, comm_b=cb_)
+            assert r["makespan"] == (M + P - 1) * 5 + (P - 1) * (cf_ + cb_)
+    rng = np.random.default_rng(31)
+    for _ in range(30):
+        P, M = int(rng.integers(1, 6)), int(rng.integers(1, 9))
+        pol = ["gpipe", "1f1b", "gpipe_fifo"][int(rng.integers(0, 3))]
+        tf, tb = rng.integers(0, 9, (P, M)), rng.integers(0, 9, (P, M))
+        c = rng.integers(0, 5, max(P - 1, 1))
+        a = orc.evaluate(pol, P, M, 1, tf, tb, c, comm_b=c, method=2)
+        b = orc.evaluate(pol, P, M, 1, tf, tb, c, method=2)
+        assert np.array_equal(a["start"], b["start"])
+        orc.evaluate(pol, P, M, 1, tf, tb, c, comm_b=rng.integers(0, 5, max(P - 1, 1)), method=2)
+
+
 MUTANTS = {
     1: "forward edges carry no comm",
     2: "1F1B warmup off by one",
@@ -389,6 +436,7 @@ MUTANTS = {
     9: "ZB runs a pending W before a ready F/B",
     10: "ZB2P keeps 1F1B's warmup",
     11: "ZB admits an F at the activation limit",
+    12: "backward edges take the forward latency",
 }
 
 
@@ -469,6 +517,12 @@ def _pin_suite(orc, lib):
     check("splitmix", sm)
     check("unrank", unrank)
     check("zb", zb)
+
+    def comm_fb():
+        r = orc.evaluate("gpipe", 4, 8, 1, 2, 3, 1, lib=lib, comm_b=4)
+        return r["makespan"] == 11 * 5 + 3 * 5
+
+    check("comm_fb", comm_fb)
     return failed
 
 
