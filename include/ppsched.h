@@ -166,6 +166,25 @@ int pp_sched_eval(pp_policy_t policy, int P, int M, int v,
                   int32_t *op_start, int32_t *op_end, int64_t op_stride_inst, int64_t op_stride_op,
                   int8_t *status, cudaStream_t stream);
 
+/* pp_sched_eval with a separate latency on the backward edges ([M040] §05: a
+ * forward boundary carries the hidden activations, a backward boundary their
+ * gradients).  comm_f[b] is added to F(b+1,i)'s input from F(b,i) and comm_b[b]
+ * to B(b,i)'s input from B(b+1,i); both use comm_stride_inst and
+ * comm_stride_bnd; either may be NULL (comm_b NULL: the same as comm_f, which
+ * is pp_sched_eval).  With comm_b given, every policy runs on the generic
+ * (lane) evaluator, which needs cost-row offsets below 2^30 elements
+ * (PP_ERR_SIZE otherwise).  Everything else as pp_sched_eval. */
+int pp_sched_eval_fb(pp_policy_t policy, int P, int M, int v,
+                     const int32_t *cost_f, const int32_t *cost_b,
+                     int64_t stride_inst, int64_t stride_stage, int64_t stride_mb,
+                     const int32_t *comm_f, const int32_t *comm_b,
+                     int64_t comm_stride_inst, int64_t comm_stride_bnd,
+                     int64_t n_instances,
+                     int32_t *makespan, int32_t *idle, int64_t *bub_num, int64_t *bub_den,
+                     int32_t *peak,
+                     int32_t *op_start, int32_t *op_end, int64_t op_stride_inst, int64_t op_stride_op,
+                     int8_t *status, cudaStream_t stream);
+
 /* Score contiguous layer-to-stage partitions under 1F1B and return the best.
  * This is the profiling-based load balancing of [GPipe->ZB] (PipeDream and GPipe
  * sections: split layers into stages by measured cost) and [M040] §05, on the

@@ -23,7 +23,7 @@ ST_OK, ST_NEG_COST, ST_OVERFLOW, ST_ZERO_COST = 0, 1, 2, 3
 EXPORTS = ("pp_sched_plan", "pp_sched_plan_info", "pp_sched_plan_ops", "pp_sched_plan_destroy",
            "pp_sched_eval", "pp_sched_partition_search", "pp_sched_status_str",
            "pp_sched_cache_clear", "pp_sched_eval_noalloc", "pp_sched_eval_zb",
-           "pp_sched_partition_search_ranks", "pp_sched_partition_search_interleaved")
+           "pp_sched_partition_search_ranks", "pp_sched_partition_search_interleaved", "pp_sched_eval_fb")
 
 
 class PPSchedError(RuntimeError):
@@ -51,6 +51,9 @@ def _load():
     lib.pp_sched_eval.argtypes = [i32, i32, i32, i32, vp, vp, i64, i64, i64, vp, i64, i64, i64,
                                   vp, vp, vp, vp, vp, vp, vp, i64, i64, vp, vp]
     lib.pp_sched_eval.restype = i32
+    lib.pp_sched_eval_fb.argtypes = [i32, i32, i32, i32, vp, vp, i64, i64, i64, vp, vp, i64, i64, i64,
+                                     vp, vp, vp, vp, vp, vp, vp, i64, i64, vp, vp]
+    lib.pp_sched_eval_fb.restype = i32
     lib.pp_sched_partition_search.argtypes = [vp, vp, vp, i32, i32, i32, ctypes.c_int32, i64, u64,
                                               i64, i64, vp, vp, vp, vp, vp]
     lib.pp_sched_partition_search.restype = i32
@@ -138,8 +141,9 @@ def op_fields(ops):
 
 def evaluate(policy, P, M, v, cost_f, cost_b, strides, n, comm=None, comm_strides=(0, 0),
              outputs=("makespan", "idle", "bub_num", "bub_den", "peak", "status"),
-             op_times=False, op_strides=None, out=None, stream=None):
-    """Call pp_sched_eval on DEVICE tensors.
+             op_times=False, op_strides=None, out=None, stream=None, comm_b=None):
+    """Call pp_sched_eval (pp_sched_eval_fb when comm_b, the backward edges'
+    latency with comm's strides, is given) on DEVICE tensors.
 
     cost_f / cost_b / comm are int32 CUDA tensors addressed through element
     strides (see the header).  Returns a dict of int32/int64/int8 CUDA tensors;
@@ -171,6 +175,13 @@ def evaluate(policy, P, M, v, cost_f, cost_b, strides, n, comm=None, comm_stride
             op_strides = (P * O, 1)
     else:
         op_strides = (0, 0)
+    if comm_b is not None:
+        rc = LIB.pp_sched_eval_fb(pol, P, M, v, _ptr(cost_f), _ptr(cost_b), strides[0], strides[1], strides[2],
+                                  _ptr(comm), _ptr(comm_b), comm_strides[0], comm_strides[1], n,
+                                  _ptr(mk), _ptr(idle), _ptr(bn), _ptr(bd), _ptr(pk), _ptr(os_), _ptr(oe),
+                                  op_strides[0], op_strides[1], _ptr(stt), _stream(stream))
+        _check(rc, "pp_sched_eval_fb")
+        return out
     rc = LIB.pp_sched_eval(pol, P, M, v, _ptr(cost_f), _ptr(cost_b), strides[0], strides[1], strides[2],
                            _ptr(comm), comm_strides[0], comm_strides[1], n,
                            _ptr(mk), _ptr(idle), _ptr(bn), _ptr(bd), _ptr(pk), _ptr(os_), _ptr(oe),

@@ -33,6 +33,7 @@ struct EvalArgs {
     const int32_t *cost_f, *cost_b;
     int64_t s_inst, s_stage, s_mb;
     const int32_t *comm;
+    const int32_t *comm_b;   // latency of the backward edges (same strides), null: comm
     int64_t c_inst, c_bnd;
     int64_t n;
     int64_t inst_begin;      // first instance of this launch

@@ -20,7 +20,8 @@
 //          the most inputs one device has in flight, not the plan's total
 //   ctab   2v rows + a zero row: the comm latency on the input edge of this
 //          lane's ops, row 2c for a forward of chunk c (boundary s-1|s) and
-//          row 2c+1 for a backward (boundary s|s+1)
+//          row 2c+1 for a backward (boundary s|s+1; the backward latency when
+//          it is given separately)
 // An op without an input reads the zero rows, an op without a consumer
 // writes the scratch row, and an idle slot runs as a zero-cost op, so the
 // round body has no branch.
@@ -255,8 +256,9 @@ __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4
             const int s = (cr >> 1) * a.P + k;
             const int bnd = (cr & 1) ? s : s - 1;
             int32_t c = 0;
-            if (a.comm && x < a.n && k < a.P && bnd >= 0 && bnd < a.S - 1)
-                c = a.comm[x * a.c_inst + (int64_t)bnd * a.c_bnd];
+            const int32_t *src = (cr & 1) && a.comm_b ? a.comm_b : a.comm;
+            if (src && x < a.n && k < a.P && bnd >= 0 && bnd < a.S - 1)
+                c = src[x * a.c_inst + (int64_t)bnd * a.c_bnd];
             ncomm[i] |= (uint32_t)c;
             ctab[cr * kRow + 32 * i + lane] = (uint32_t)c;
         }

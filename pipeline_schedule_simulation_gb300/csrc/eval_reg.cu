@@ -421,14 +421,15 @@ int launch_eval_reg_tables(int pmax, const EvalArgs &a, bool vec, bool ops, cuda
 
 }  // namespace pps
 
-extern "C" int pp_sched_eval(pp_policy_t policy, int P, int M, int v, const int32_t *cost_f,
-                             const int32_t *cost_b, int64_t stride_inst, int64_t stride_stage,
-                             int64_t stride_mb, const int32_t *comm, int64_t comm_stride_inst,
-                             int64_t comm_stride_bnd, int64_t n_instances, int32_t *makespan,
-                             int32_t *idle, int64_t *bub_num, int64_t *bub_den, int32_t *peak,
-                             int32_t *op_start, int32_t *op_end, int64_t op_stride_inst,
-                             int64_t op_stride_op, int8_t *status, cudaStream_t stream) {
-    using namespace pps;
+namespace pps {
+namespace {
+
+int eval_impl(pp_policy_t policy, int P, int M, int v, const int32_t *cost_f, const int32_t *cost_b,
+              int64_t stride_inst, int64_t stride_stage, int64_t stride_mb, const int32_t *comm,
+              const int32_t *comm_b, int64_t comm_stride_inst, int64_t comm_stride_bnd, int64_t n_instances,
+              int32_t *makespan, int32_t *idle, int64_t *bub_num, int64_t *bub_den, int32_t *peak,
+              int32_t *op_start, int32_t *op_end, int64_t op_stride_inst, int64_t op_stride_op, int8_t *status,
+              cudaStream_t stream) {
     int rc = check_shape((int)policy, P, M, v);
     if (rc) return rc;
     if (n_instances < 0) return PP_ERR_ARG;
@@ -443,14 +444,14 @@ extern "C" int pp_sched_eval(pp_policy_t policy, int P, int M, int v, const int3
     if (peak)
         PPS_CUDA_TRY(cudaMemcpyAsync(peak, plan->d_peak, P * sizeof(int32_t), cudaMemcpyDeviceToDevice, stream));
     if (n_instances == 0) return PP_OK;
-    EvalArgs a;
+    EvalArgs a{};
     a.desc = plan->d_desc; a.desc2 = plan->d_desc2; a.rw = plan->d_rw;
     a.seg = plan->d_seg; a.nseg = plan->nseg;
     a.ktab = nullptr; a.ktab_words = 0;
     a.R = plan->R; a.P = P; a.M = M; a.v = v; a.S = plan->S; a.O = plan->O; a.nslots = plan->nslots;
     a.cost_f = cost_f; a.cost_b = cost_b;
     a.s_inst = stride_inst; a.s_stage = stride_stage; a.s_mb = stride_mb;
-    a.comm = comm; a.c_inst = comm_stride_inst; a.c_bnd = comm_stride_bnd;
+    a.comm = comm; a.comm_b = comm_b; a.c_inst = comm_stride_inst; a.c_bnd = comm_stride_bnd;
     a.n = n_instances;
     a.inst_begin = 0;
     a.makespan = makespan; a.idle = idle; a.bub_num = bub_num; a.bub_den = bub_den; a.status = status;
@@ -460,7 +461,39 @@ extern "C" int pp_sched_eval(pp_policy_t policy, int P, int M, int v, const int3
                      stride_mb % 4 == 0 &&
                      (int64_t)(plan->S - 1) * stride_stage + (int64_t)(M - 1) * stride_mb < ((int64_t)1 << 31);
     const bool ops = op_start || op_end;
+    if (comm_b) {
+        // a separate backward latency: the lane evaluator takes it for every policy
+        if (!lane_path(plan, a)) return PP_ERR_SIZE;
+        return launch_eval_lane(plan, a, vec, ops, stream);
+    }
     if (plan->reg_ok) return launch_eval_reg(plan, a, vec, ops, stream);
     if (lane_path(plan, a)) return launch_eval_lane(plan, a, vec, ops, stream);
     return launch_eval_slot(plan, a, vec, ops, stream);
+}
+
+}  // namespace
+}  // namespace pps
+
+extern "C" int pp_sched_eval(pp_policy_t policy, int P, int M, int v, const int32_t *cost_f,
+                             const int32_t *cost_b, int64_t stride_inst, int64_t stride_stage,
+                             int64_t stride_mb, const int32_t *comm, int64_t comm_stride_inst,
+                             int64_t comm_stride_bnd, int64_t n_instances, int32_t *makespan,
+                             int32_t *idle, int64_t *bub_num, int64_t *bub_den, int32_t *peak,
+                             int32_t *op_start, int32_t *op_end, int64_t op_stride_inst,
+                             int64_t op_stride_op, int8_t *status, cudaStream_t stream) {
+    return pps::eval_impl(policy, P, M, v, cost_f, cost_b, stride_inst, stride_stage, stride_mb, comm, nullptr,
+                          comm_stride_inst, comm_stride_bnd, n_instances, makespan, idle, bub_num, bub_den, peak,
+                          op_start, op_end, op_stride_inst, op_stride_op, status, stream);
+}
+
+extern "C" int pp_sched_eval_fb(pp_policy_t policy, int P, int M, int v, const int32_t *cost_f,
+                                const int32_t *cost_b, int64_t stride_inst, int64_t stride_stage,
+                                int64_t stride_mb, const int32_t *comm_f, const int32_t *comm_b,
+                                int64_t comm_stride_inst, int64_t comm_stride_bnd, int64_t n_instances,
+                                int32_t *makespan, int32_t *idle, int64_t *bub_num, int64_t *bub_den,
+                                int32_t *peak, int32_t *op_start, int32_t *op_end, int64_t op_stride_inst,
+                                int64_t op_stride_op, int8_t *status, cudaStream_t stream) {
+    return pps::eval_impl(policy, P, M, v, cost_f, cost_b, stride_inst, stride_stage, stride_mb, comm_f, comm_b,
+                          comm_stride_inst, comm_stride_bnd, n_instances, makespan, idle, bub_num, bub_den, peak,
+                          op_start, op_end, op_stride_inst, op_stride_op, status, stream);
 }

@@ -430,7 +430,12 @@ static int build_plan(int policy, int P, int M, int v, cudaStream_t st, pp_plan 
         reg_ok = h_info[2] == 0;
     }
     int nslots = 0, nlslots = 0;
-    if (!reg_ok) {
+    // Value slots: needed by the generic evaluators (interleaved, or a plan
+    // the register evaluator cannot run); built for the register plans too so
+    // that the lane evaluator can take their variants (a separate backward
+    // latency), where a plan with too many results in flight just goes
+    // without them.
+    {
         PPS_CUDA_TRY(cudaMalloc(&desc2.p, (int64_t)R * pmax * sizeof(uint32_t)));
         PPS_CUDA_TRY(cudaMalloc(&slot_of.p, npos * sizeof(int32_t)));
         PPS_CUDA_TRY(cudaMemsetAsync(slot_of.p, 0xFF, npos * sizeof(int32_t), st));
@@ -440,19 +445,24 @@ static int build_plan(int policy, int P, int M, int v, cudaStream_t st, pp_plan 
         PPS_CUDA_TRY(cudaMemcpyAsync(h_info, info.p, sizeof(h_info), cudaMemcpyDeviceToHost, st));
         PPS_CUDA_TRY(cudaStreamSynchronize(st));
         if (h_info[5]) return PP_ERR_INTERNAL;
-        if (h_info[4]) return PP_ERR_SIZE;
-        nslots = h_info[3];
-        // per-consumer slots of the lane evaluator: lrd then lwr, [R][pmax] bytes each
-        const int64_t cells = (int64_t)R * pmax;
-        PPS_CUDA_TRY(cudaMalloc(&lslot.p, 2 * cells));
-        PPS_CUDA_TRY(cudaMemsetAsync(lslot.p, 0xFF, 2 * cells, st));
-        k_cslots<<<1, 32, 0, st>>>(desc.as<uint32_t>(), desc2.as<uint32_t>(), R, P, pmax, lslot.as<uint8_t>(),
-                                   lslot.as<uint8_t>() + cells, info.as<int32_t>());
-        PPS_CUDA_TRY(cudaGetLastError());
-        PPS_CUDA_TRY(cudaMemcpyAsync(h_info, info.p, sizeof(h_info), cudaMemcpyDeviceToHost, st));
-        PPS_CUDA_TRY(cudaStreamSynchronize(st));
-        if (h_info[7] < 0) return PP_ERR_INTERNAL;
-        nlslots = h_info[7];
+        if (h_info[4]) {
+            if (!reg_ok) return PP_ERR_SIZE;
+            cudaFree(desc2.p);  // a register plan without value slots
+            desc2.p = nullptr;
+        } else {
+            nslots = h_info[3];
+            // per-consumer slots of the lane evaluator: lrd then lwr, [R][pmax] bytes each
+            const int64_t cells = (int64_t)R * pmax;
+            PPS_CUDA_TRY(cudaMalloc(&lslot.p, 2 * cells));
+            PPS_CUDA_TRY(cudaMemsetAsync(lslot.p, 0xFF, 2 * cells, st));
+            k_cslots<<<1, 32, 0, st>>>(desc.as<uint32_t>(), desc2.as<uint32_t>(), R, P, pmax, lslot.as<uint8_t>(),
+                                       lslot.as<uint8_t>() + cells, info.as<int32_t>());
+            PPS_CUDA_TRY(cudaGetLastError());
+            PPS_CUDA_TRY(cudaMemcpyAsync(h_info, info.p, sizeof(h_info), cudaMemcpyDeviceToHost, st));
+            PPS_CUDA_TRY(cudaStreamSynchronize(st));
+            if (h_info[7] < 0) return PP_ERR_INTERNAL;
+            nlslots = h_info[7];
+        }
     }
     pp_plan *p = new pp_plan();
     p->policy = policy; p->P = P; p->M = M; p->v = v; p->S = S; p->O = O;

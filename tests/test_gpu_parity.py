@@ -259,3 +259,34 @@ def test_host_entry_end_to_end(B):
     assert h2d == batch.cost_f.nbytes * 2 + batch.comm.nbytes
     for k in ("makespan", "idle", "bub_num", "bub_den", "status"):
         assert np.array_equal(host[k].numpy(), ref[k])
+
+
+FB_SHAPES = [(W.GPIPE, 4, 8, 1), (W.ONEF1B, 8, 16, 1), (W.ONEF1B, 3, 2, 1), (W.GPIPE_FIFO, 5, 6, 1),
+             (W.INTERLEAVED, 4, 8, 2), (W.INTERLEAVED, 8, 16, 3), (W.ONEF1B, 16, 20, 1)]
+
+
+@pytest.mark.parametrize("policy,P,M,v", FB_SHAPES)
+@pytest.mark.parametrize("layout", ["inst_minor", "inst_major"])
+def test_separate_backward_comm(orc, B, policy, P, M, v, layout):
+    """pp_sched_eval_fb: a backward latency of its own on every boundary;
+    every op time against the oracle's evaluation with comm_b."""
+    import torch
+    for n, seed in ((61, 3), (130, 4)):
+        batch = W.random_batch(policy, P, M, v, n, seed=seed + P + M, hi=12, comm_hi=6, layout=layout,
+                               pad_to=4)
+        cb = np.random.default_rng(seed).integers(0, 9, size=batch.comm.shape).astype(np.int32)
+        out = B.evaluate(batch.policy, P, M, v, to_dev(batch.cost_f), to_dev(batch.cost_b), batch.strides, n,
+                         comm=to_dev(batch.comm), comm_strides=batch.comm_strides, op_times=True, comm_b=to_dev(cb))
+        torch.cuda.synchronize()
+        g = {k: t.cpu().numpy() for k, t in out.items()}
+        r = orc.eval_batch(batch.policy, P, M, v, batch.cost_f, batch.cost_b, batch.strides, comm=batch.comm,
+                           comm_strides=batch.comm_strides, n=n, op_times=True, nthreads=8, comm_b=cb)
+        assert_same(g, r, op_times=True)
+    # comm_b equal to comm: the same numbers as pp_sched_eval
+    same = B.evaluate(batch.policy, P, M, v, to_dev(batch.cost_f), to_dev(batch.cost_b), batch.strides, n,
+                      comm=to_dev(batch.comm), comm_strides=batch.comm_strides, comm_b=to_dev(batch.comm))
+    base = B.evaluate(batch.policy, P, M, v, to_dev(batch.cost_f), to_dev(batch.cost_b), batch.strides, n,
+                      comm=to_dev(batch.comm), comm_strides=batch.comm_strides)
+    torch.cuda.synchronize()
+    for k in ("makespan", "idle", "bub_num", "bub_den", "status"):
+        assert torch.equal(same[k], base[k])
