@@ -1,0 +1,43 @@
+"""Timeline export (host formatting of op times), checked on op times the
+oracle computes; no GPU needed."""
+import csv
+import json
+
+import numpy as np
+
+from pipeline_schedule_simulation_gb300 import timeline as T
+
+
+def _packed(kind, chunk, mb):
+    return (np.asarray(kind, np.int64) << 31) | (np.asarray(chunk, np.int64) << 24) | np.asarray(mb, np.int64)
+
+
+def test_records_and_trace_from_plan_order(orc, tmp_path):
+    r = orc.evaluate("interleaved", 2, 4, 2, 1, 2, 1)
+    ops = _packed(r["kind"], r["chunk"], r["mb"])
+    recs = T.records(r["start"], r["end"], ops)
+    assert len(recs) == 2 * 16
+    for rec in recs:
+        assert rec["end"] - rec["start"] == (1 if rec["kind"] == "F" else 2)
+    # per device, records are in time order and do not overlap
+    for k in range(2):
+        dev = [x for x in recs if x["device"] == k]
+        assert all(a["end"] <= b["start"] for a, b in zip(dev, dev[1:]))
+    tr = T.chrome_trace(recs, us_per_tick=10)
+    ev = [e for e in tr["traceEvents"] if e["ph"] == "X"]
+    assert len(ev) == 32 and max(e["ts"] + e["dur"] for e in ev) == 10 * r["makespan"]
+    assert {e["cat"] for e in ev} == {"F", "B"}
+    p = tmp_path / "t.json"
+    T.write_chrome_trace(p, recs)
+    assert json.loads(p.read_text())["traceEvents"][0]["ph"] == "M"
+    c = tmp_path / "t.csv"
+    T.write_csv(c, recs)
+    rows = list(csv.DictReader(open(c)))
+    assert len(rows) == 32 and rows[0].keys() == {"device", "kind", "chunk", "mb", "start", "end"}
+
+
+def test_records_zero_bubble(orc):
+    r = orc.zb_evaluate("zb1p", 2, 2, 1, 1, 1)
+    recs = T.records(r["start"], r["end"], zb=True)
+    assert len(recs) == 12
+    assert [x["kind"] + str(x["mb"]) for x in recs if x["device"] == 0] == ["F0", "F1", "B0", "W0", "B1", "W1"]
