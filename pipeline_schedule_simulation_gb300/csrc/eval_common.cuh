@@ -308,12 +308,26 @@ __device__ __forceinline__ int wrap_add(int x, int y) {
     return static_cast<int>(static_cast<uint32_t>(x) + static_cast<uint32_t>(y));
 }
 
-// Launchers (defined in eval_reg.cu / eval_slot.cu / eval_lane.cu).
+// SMs of device `dev` (cached per device and translation unit).
+inline int sm_count(int dev) {
+    static int cached[64] = {};
+    if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+        (void)cudaGetLastError();
+        n = 1;
+    }
+    if (dev >= 0 && dev < 64) cached[dev] = n;
+    return n;
+}
+
+// Launchers (defined in eval_reg.cu / eval_slot.cu / eval_lane.cu / eval_split.cu).
 int launch_eval_reg(pp_plan *plan, EvalArgs &a, bool vec, bool ops, cudaStream_t st);
 bool reg_table_path(int pmax, const EvalArgs &a, bool vec);
 int launch_eval_reg_tables(int pmax, const EvalArgs &a, bool vec, bool ops, cudaStream_t st);
 int launch_eval_slot(const pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st);
 bool lane_path(const pp_plan *plan, const EvalArgs &a);
+int launch_eval_split8(const EvalArgs &a, cudaStream_t st);
 int launch_eval_lane(pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st);
 
 }  // namespace pps

@@ -407,19 +407,6 @@ size_t lane_smem(const EvalArgs &a, int warps, int ni) {
 // GPU about eight such warps per SM.
 constexpr int64_t kLaneWarpsForTwoSets = 152 * 8;
 
-// SMs of the current device (cached per device).
-int sm_count(int dev) {
-    static int cached[64] = {};
-    if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
-        (void)cudaGetLastError();
-        n = 1;
-    }
-    if (dev >= 0 && dev < 64) cached[dev] = n;
-    return n;
-}
-
 // Warps per CTA: every CTA copies the whole table, so larger CTAs are
 // cheaper, but a batch of a few thousand warps is one wave of CTAs and the
 // busiest SM sets the time.  Take the size (8, 4 or 2 warps) whose busiest

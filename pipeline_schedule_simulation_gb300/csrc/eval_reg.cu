@@ -389,6 +389,15 @@ static int launch_reg_p(pp_plan *plan, EvalArgs &a, bool vec, bool ops, cudaStre
         if (rc) return rc;
         a.ktab = t->d;
         a.ktab_words = t->words;
+        // 8-wide plans without per-op output, in batches too small to give
+        // every SM eight warps of 32 instances: two lanes per instance, twice
+        // the warps (on larger batches the one-lane kernel is as fast or
+        // faster and moves fewer, larger rows)
+        if constexpr (PMAX == 8) {
+            int dev = 0;
+            PPS_CUDA_TRY(cudaGetDevice(&dev));
+            if (!ops && a.n < (int64_t)sm_count(dev) * 8 * 32) return launch_eval_split8(a, st);
+        }
     }
     return ops ? launch_reg_o<PMAX, true>(a, vec, lt, st) : launch_reg_o<PMAX, false>(a, vec, lt, st);
 }

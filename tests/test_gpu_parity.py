@@ -290,3 +290,26 @@ def test_separate_backward_comm(orc, B, policy, P, M, v, layout):
     torch.cuda.synchronize()
     for k in ("makespan", "idle", "bub_num", "bub_den", "status"):
         assert torch.equal(same[k], base[k])
+
+
+@pytest.mark.parametrize("policy,P,M", [(W.ONEF1B, 8, 16), (W.ONEF1B, 5, 9), (W.GPIPE, 6, 7), (W.GPIPE_FIFO, 8, 5),
+                                        (W.ONEF1B, 7, 64)])
+def test_two_lanes_per_instance(orc, B, policy, P, M):
+    """Small batches of 8-wide GPipe / 1F1B plans without per-op output run
+    with two lanes per instance (devices 0-3 and 4-7 exchanging boundary
+    arrivals every round): against the oracle, with ragged tails, negative
+    costs and overflow."""
+    for n, seed in ((1, 1), (17, 2), (250, 3), (1000, 4)):
+        batch = W.random_batch(policy, P, M, 1, n, seed=seed * 7 + P + M, hi=30, comm_hi=7, pad_to=4)
+        if n >= 250:
+            cf = batch.cost_f.reshape(P, M, -1)
+            cb = batch.cost_b.reshape(P, M, -1)
+            cf[3, M - 1, 5] = -3
+            cb[4, 0, 9] = 2**31 - 5
+            cf[0, 0, 11] = 2**30
+            cb[P - 1, M // 2, 11] = 2**30
+        g = run_gpu(batch)
+        r = run_oracle(orc, batch)
+        assert_same(g, r)
+        if n >= 250:
+            assert g["status"][5] == B.ST_NEG_COST and g["status"][9] == B.ST_OVERFLOW
