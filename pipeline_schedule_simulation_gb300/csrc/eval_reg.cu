@@ -472,6 +472,10 @@ int eval_impl(pp_policy_t policy, int P, int M, int v, const int32_t *cost_f, co
     const bool ops = op_start || op_end;
     if (comm_b) {
         // a separate backward latency: the lane evaluator takes it for every policy
+        rc = plan_value_slots(plan, stream);
+        if (rc) return rc;
+        a.desc2 = plan->d_desc2;
+        a.nslots = plan->nslots;
         if (!lane_path(plan, a)) return PP_ERR_SIZE;
         return launch_eval_lane(plan, a, vec, ops, stream);
     }

@@ -111,6 +111,9 @@ int cuda_status(cudaError_t e);
 // Plan cache used by the evaluation entry points: returns the plan of the
 // shape on the current device, building it on first use.
 int cached_plan(int policy, int P, int M, int v, cudaStream_t stream, pp_plan **out);
+// Value slots for a plan built without them (register plans get them on
+// first need); PP_ERR_SIZE if too many results would be in flight.
+int plan_value_slots(pp_plan *plan, cudaStream_t stream);
 
 // Argument validation shared by plan construction and evaluation.
 int check_shape(int policy, int P, int M, int v);

@@ -385,12 +385,50 @@ int check_shape(int policy, int P, int M, int v) {
     return PP_OK;
 }
 
+// Value slots of a plan: the plan-wide colouring (k_slots, for the generic
+// slot evaluator) and the per-consumer one (k_cslots, for the lane
+// evaluator).  Allocates *desc2 [R][pmax] and *lslot [2][R][pmax]; returns
+// PP_ERR_SIZE when more than kMaxValueSlots results would be in flight.
+static int build_slots(const uint32_t *desc, int R, int P, int M, int v, int pmax, cudaStream_t st,
+                       uint32_t **desc2_out, uint8_t **lslot_out, int *nslots, int *nlslots) {
+    const int64_t npos = 2LL * P * v * M;
+    const int64_t cells = (int64_t)R * pmax;
+    DevBuf desc2, slot_of, info, lslot;
+    int32_t h_info[8];
+    PPS_CUDA_TRY(cudaMalloc(&info.p, 8 * sizeof(int32_t)));
+    PPS_CUDA_TRY(cudaMemsetAsync(info.p, 0, 8 * sizeof(int32_t), st));
+    PPS_CUDA_TRY(cudaMalloc(&desc2.p, cells * sizeof(uint32_t)));
+    PPS_CUDA_TRY(cudaMalloc(&slot_of.p, npos * sizeof(int32_t)));
+    PPS_CUDA_TRY(cudaMemsetAsync(slot_of.p, 0xFF, npos * sizeof(int32_t), st));
+    k_slots<<<1, 32, 0, st>>>(desc, R, P, M, v, pmax, slot_of.as<int32_t>(), desc2.as<uint32_t>(),
+                              info.as<int32_t>());
+    PPS_CUDA_TRY(cudaGetLastError());
+    PPS_CUDA_TRY(cudaMemcpyAsync(h_info, info.p, sizeof(h_info), cudaMemcpyDeviceToHost, st));
+    PPS_CUDA_TRY(cudaStreamSynchronize(st));
+    if (h_info[5]) return PP_ERR_INTERNAL;
+    if (h_info[4]) return PP_ERR_SIZE;
+    // per-consumer slots of the lane evaluator: lrd then lwr, [R][pmax] bytes each
+    PPS_CUDA_TRY(cudaMalloc(&lslot.p, 2 * cells));
+    PPS_CUDA_TRY(cudaMemsetAsync(lslot.p, 0xFF, 2 * cells, st));
+    k_cslots<<<1, 32, 0, st>>>(desc, desc2.as<uint32_t>(), R, P, pmax, lslot.as<uint8_t>(),
+                               lslot.as<uint8_t>() + cells, info.as<int32_t>());
+    PPS_CUDA_TRY(cudaGetLastError());
+    PPS_CUDA_TRY(cudaMemcpyAsync(h_info, info.p, sizeof(h_info), cudaMemcpyDeviceToHost, st));
+    PPS_CUDA_TRY(cudaStreamSynchronize(st));
+    if (h_info[7] < 0) return PP_ERR_INTERNAL;
+    *nslots = h_info[3];
+    *nlslots = h_info[7];
+    *desc2_out = desc2.as<uint32_t>(); desc2.p = nullptr;
+    *lslot_out = lslot.as<uint8_t>(); lslot.p = nullptr;
+    return PP_OK;
+}
+
 static int build_plan(int policy, int P, int M, int v, cudaStream_t st, pp_plan **out) {
     int rc = check_shape(policy, P, M, v);
     if (rc) return rc;
     const int S = P * v, O = 2 * M * v, pmax = pmax_for(P);
     const int64_t nops = (int64_t)P * O, npos = 2LL * S * M;
-    DevBuf ops, pos, round, info, peak, desc, desc2, slot_of, rw, seg, lslot;
+    DevBuf ops, pos, round, info, peak, desc, desc2, rw, seg, lslot;
     PPS_CUDA_TRY(cudaMalloc(&ops.p, nops * sizeof(uint32_t)));
     PPS_CUDA_TRY(cudaMalloc(&pos.p, npos * sizeof(int32_t)));
     PPS_CUDA_TRY(cudaMalloc(&round.p, nops * sizeof(int32_t)));
@@ -430,39 +468,10 @@ static int build_plan(int policy, int P, int M, int v, cudaStream_t st, pp_plan 
         reg_ok = h_info[2] == 0;
     }
     int nslots = 0, nlslots = 0;
-    // Value slots: needed by the generic evaluators (interleaved, or a plan
-    // the register evaluator cannot run); built for the register plans too so
-    // that the lane evaluator can take their variants (a separate backward
-    // latency), where a plan with too many results in flight just goes
-    // without them.
-    {
-        PPS_CUDA_TRY(cudaMalloc(&desc2.p, (int64_t)R * pmax * sizeof(uint32_t)));
-        PPS_CUDA_TRY(cudaMalloc(&slot_of.p, npos * sizeof(int32_t)));
-        PPS_CUDA_TRY(cudaMemsetAsync(slot_of.p, 0xFF, npos * sizeof(int32_t), st));
-        k_slots<<<1, 32, 0, st>>>(desc.as<uint32_t>(), R, P, M, v, pmax, slot_of.as<int32_t>(),
-                                  desc2.as<uint32_t>(), info.as<int32_t>());
-        PPS_CUDA_TRY(cudaGetLastError());
-        PPS_CUDA_TRY(cudaMemcpyAsync(h_info, info.p, sizeof(h_info), cudaMemcpyDeviceToHost, st));
-        PPS_CUDA_TRY(cudaStreamSynchronize(st));
-        if (h_info[5]) return PP_ERR_INTERNAL;
-        if (h_info[4]) {
-            if (!reg_ok) return PP_ERR_SIZE;
-            cudaFree(desc2.p);  // a register plan without value slots
-            desc2.p = nullptr;
-        } else {
-            nslots = h_info[3];
-            // per-consumer slots of the lane evaluator: lrd then lwr, [R][pmax] bytes each
-            const int64_t cells = (int64_t)R * pmax;
-            PPS_CUDA_TRY(cudaMalloc(&lslot.p, 2 * cells));
-            PPS_CUDA_TRY(cudaMemsetAsync(lslot.p, 0xFF, 2 * cells, st));
-            k_cslots<<<1, 32, 0, st>>>(desc.as<uint32_t>(), desc2.as<uint32_t>(), R, P, pmax, lslot.as<uint8_t>(),
-                                       lslot.as<uint8_t>() + cells, info.as<int32_t>());
-            PPS_CUDA_TRY(cudaGetLastError());
-            PPS_CUDA_TRY(cudaMemcpyAsync(h_info, info.p, sizeof(h_info), cudaMemcpyDeviceToHost, st));
-            PPS_CUDA_TRY(cudaStreamSynchronize(st));
-            if (h_info[7] < 0) return PP_ERR_INTERNAL;
-            nlslots = h_info[7];
-        }
+    if (!reg_ok) {
+        rc = build_slots(desc.as<uint32_t>(), R, P, M, v, pmax, st, reinterpret_cast<uint32_t **>(&desc2.p),
+                         reinterpret_cast<uint8_t **>(&lslot.p), &nslots, &nlslots);
+        if (rc) return rc;
     }
     pp_plan *p = new pp_plan();
     p->policy = policy; p->P = P; p->M = M; p->v = v; p->S = S; p->O = O;
@@ -483,6 +492,22 @@ static int build_plan(int policy, int P, int M, int v, cudaStream_t st, pp_plan 
     p->nseg = h_info[6];
     p->d_peak = peak.as<int32_t>(); peak.p = nullptr;
     *out = p;
+    return PP_OK;
+}
+
+int plan_value_slots(pp_plan *plan, cudaStream_t stream) {
+    std::lock_guard<std::mutex> lk(plan->ktab_mu);
+    if (plan->d_lslot) return PP_OK;
+    uint32_t *desc2 = nullptr;
+    uint8_t *lslot = nullptr;
+    int nslots = 0, nlslots = 0;
+    const int rc = build_slots(plan->d_desc, plan->R, plan->P, plan->M, plan->v, plan->pmax, stream, &desc2, &lslot,
+                               &nslots, &nlslots);
+    if (rc) return rc;
+    plan->d_desc2 = desc2;
+    plan->d_lslot = lslot;
+    plan->nslots = nslots;
+    plan->nlslots = nlslots;
     return PP_OK;
 }
 
