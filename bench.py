@@ -209,6 +209,14 @@ def parse():
     return ap.parse_args()
 
 
+def bench_config(n, world):
+    """The workload description shared by both arms."""
+    return {"workload": f"1f1b_hetero_P{P}_M{M}_n{n}", "P": P, "M": M,
+            "instances_per_gpu": n, "layout": "instance-minor [S][M][n]",
+            "l2": f"inputs {2 * P * M * n * 4 / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB, no flush",
+            "parallelism": f"instance-sharded x{world}"}
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
@@ -240,7 +248,7 @@ def reference_arm(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
         "data": "synthetic",
-        "config": {"workload": f"1f1b_hetero_P{P}_M{M}_n{args.n}", "sample_instances_per_step": per_step},
+        "config": dict(bench_config(args.n, world), sample_instances_per_step=per_step),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"first {per_step} instances per step, event simulation, {threads} threads"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -357,10 +365,7 @@ def main():
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
-            "config": {"workload": f"1f1b_hetero_P{P}_M{M}_n{n}", "P": P, "M": M,
-                       "instances_per_gpu": n, "layout": "instance-minor [S][M][n]",
-                       "l2": f"inputs {2 * P * M * n * 4 / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB, no flush",
-                       "parallelism": f"instance-sharded x{world}"},
+            "config": bench_config(n, world),
             "gpu_launches": K,
             "roofline": {"bound": "hbm", "kernel": "k_eval_reg<8,1,true,false,true>", "achieved": achieved,
                          "peak": peak_gbs, "unit": "GB/s", "frac": achieved / peak_gbs,
