@@ -13,6 +13,7 @@
 // 64-bit atomicMin per warp into the caller's best_idx word, which a one-thread
 // kernel then turns into the index, makespan and cut positions.
 #include "internal.cuh"
+#include "search_common.cuh"
 
 namespace pps {
 
@@ -37,15 +38,6 @@ struct SearchArgs {
     unsigned long long *key;  // the caller's best_idx word, used as the reduction cell
 };
 
-// SplitMix64 (Steele, Lea & Flood, OOPSLA 2014): add the golden gamma to the
-// state, then apply the two xor-shift-multiply rounds and a final xor-shift.
-__device__ __forceinline__ uint64_t splitmix64(uint64_t s) {
-    uint64_t z = s + 0x9E3779B97F4A7C15ull;
-    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-    return z ^ (z >> 31);
-}
-
 // Shared tables: prefix sums of layer costs and bytes, and C(n, i) for
 // n < L, i < P, computed with the multiplicative formula in 128-bit-safe steps.
 struct Tables {
@@ -53,23 +45,11 @@ struct Tables {
     uint64_t C[kMaxL][PP_MAX_P];  // C[n][i]; saturates at ~0
 };
 
-__device__ uint64_t binom_mul(int n, int i) {
-    if (i < 0 || i > n) return 0;
-    if (i > n - i) i = n - i;
-    // C(n, i) = prod_{t=1..i} (n - i + t) / t, exact at every step
-    unsigned __int128 acc = 1;
-    for (int t = 1; t <= i; ++t) {
-        acc = acc * (unsigned)(n - i + t) / (unsigned)t;
-        if (acc > (unsigned __int128)0xFFFFFFFFFFFFFFFFull) return ~0ull;
-    }
-    return (uint64_t)acc;
-}
-
 __device__ void build_tables(const SearchArgs &a, Tables &t) {
     const int tid = threadIdx.x;
     for (int e = tid; e < a.L * a.P; e += blockDim.x) {
         const int n = e / a.P, i = e % a.P;
-        t.C[n][i] = binom_mul(n, i);
+        t.C[n][i] = binom_u64(n, i);
     }
     if (tid == 0) {
         int64_t f = 0, b = 0, c = 0;
@@ -272,17 +252,6 @@ __global__ void k_search_finish(const SearchArgs a, int64_t *best_idx, int32_t *
     *best_idx = a.begin + ci;
 }
 
-uint64_t host_binom(int n, int k) {
-    if (k < 0 || k > n) return 0;
-    if (k > n - k) k = n - k;
-    unsigned __int128 acc = 1;
-    for (int t = 1; t <= k; ++t) {
-        acc = acc * (unsigned)(n - k + t) / (unsigned)t;
-        if (acc > (unsigned __int128)0xFFFFFFFFFFFFFFFFull) return ~0ull;
-    }
-    return (uint64_t)acc;
-}
-
 template <int PMAX, bool EXH>
 int run_search(SearchArgs &a, int64_t *best_idx, int32_t *best_mk, int32_t *best_cuts, cudaStream_t st) {
     int dev = 0, sms = 0, per_sm = 0;
@@ -315,7 +284,7 @@ int search_entry(const int32_t *layer_tf, const int32_t *layer_tb, const int64_t
     if (P < 1 || M < 1 || L < P || n < 0 || begin < 0 || comm < 0) return PP_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(best_idx) & 7) != 0) return PP_ERR_ARG;
     if (P > PP_MAX_P || L > kMaxL || M > PP_MAX_MV || n >= (int64_t)1 << 32) return PP_ERR_SIZE;
-    const uint64_t ncomb = host_binom(L - 1, P - 1);
+    const uint64_t ncomb = binom_u64(L - 1, P - 1);
     if (ncomb == ~0ull || ncomb == 0) return PP_ERR_SIZE;
     if (exhaustive && (uint64_t)begin + (uint64_t)n > ncomb) return PP_ERR_ARG;
     pp_plan *plan = nullptr;

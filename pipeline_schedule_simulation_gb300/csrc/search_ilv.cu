@@ -22,6 +22,7 @@
 #include <mutex>
 
 #include "eval_common.cuh"
+#include "search_common.cuh"
 
 namespace pps {
 namespace {
@@ -43,25 +44,6 @@ struct IlvArgs {
     int cn;                // stride of the scratch tables
 };
 
-__device__ __forceinline__ uint64_t ilv_splitmix64(uint64_t s) {
-    // SplitMix64 (Steele, Lea & Flood, OOPSLA 2014)
-    uint64_t z = s + 0x9E3779B97F4A7C15ull;
-    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-    return z ^ (z >> 31);
-}
-
-__device__ uint64_t ilv_binom(int n, int i) {
-    if (i < 0 || i > n) return 0;
-    if (i > n - i) i = n - i;
-    unsigned __int128 acc = 1;
-    for (int t = 1; t <= i; ++t) {
-        acc = acc * (unsigned)(n - i + t) / (unsigned)t;
-        if (acc > (unsigned __int128)0xFFFFFFFFFFFFFFFFull) return ~0ull;
-    }
-    return (uint64_t)acc;
-}
-
 // Dynamic shared memory: prefix sums of the layer costs and bytes, then
 // C(n, i) for n < L, i < S.
 struct IlvTables {
@@ -75,7 +57,7 @@ __device__ IlvTables ilv_tables(const IlvArgs &a, unsigned char *smem) {
     t.pre_tb = t.pre_tf + (a.L + 1);
     t.pre_act = t.pre_tb + (a.L + 1);
     t.C = reinterpret_cast<uint64_t *>(t.pre_act + (a.L + 1));
-    for (int e = threadIdx.x; e < a.L * a.S; e += blockDim.x) t.C[e] = ilv_binom(e / a.S, e % a.S);
+    for (int e = threadIdx.x; e < a.L * a.S; e += blockDim.x) t.C[e] = binom_u64(e / a.S, e % a.S);
     if (threadIdx.x == 0) {
         int64_t f = 0, b = 0, c = 0;
         t.pre_tf[0] = t.pre_tb[0] = t.pre_act[0] = 0;
@@ -111,7 +93,7 @@ __global__ void __launch_bounds__(256) k_ilv_cands(const IlvArgs a, int64_t chun
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nchunk; i += gridDim.x * blockDim.x) {
         int first[PP_MAX_S + 1];
         int64_t act[PP_MAX_S];
-        const uint64_t r = ilv_splitmix64(a.seed + (uint64_t)(a.begin + chunk0 + i)) % a.ncomb;
+        const uint64_t r = splitmix64(a.seed + (uint64_t)(a.begin + chunk0 + i)) % a.ncomb;
         ilv_unrank(a, t, r, first);
         int8_t fl = 0;
         for (int s = 0; s < a.S; ++s) {
@@ -176,22 +158,11 @@ __global__ void k_ilv_finish(const IlvArgs a, const unsigned long long *key, int
     const int64_t ci = (int64_t)(k & 0xFFFFFFFFull);
     if (best_cuts) {
         int first[PP_MAX_S + 1];
-        ilv_unrank(a, t, ilv_splitmix64(a.seed + (uint64_t)(a.begin + ci)) % a.ncomb, first);
+        ilv_unrank(a, t, splitmix64(a.seed + (uint64_t)(a.begin + ci)) % a.ncomb, first);
         for (int s = 1; s < a.S; ++s) best_cuts[s - 1] = first[s];
     }
     if (best_mk) *best_mk = (int)(k >> 32);
     *best_idx = a.begin + ci;
-}
-
-uint64_t ilv_host_binom(int n, int k) {
-    if (k < 0 || k > n) return 0;
-    if (k > n - k) k = n - k;
-    unsigned __int128 acc = 1;
-    for (int t = 1; t <= k; ++t) {
-        acc = acc * (unsigned)(n - k + t) / (unsigned)t;
-        if (acc > (unsigned __int128)0xFFFFFFFFFFFFFFFFull) return ~0ull;
-    }
-    return (uint64_t)acc;
 }
 
 // Per-device scratch: cost tables [S][cn] x 2, makespan, status, flag, comm.
@@ -236,7 +207,7 @@ extern "C" int pp_sched_partition_search_interleaved(const int32_t *layer_tf, co
         return PP_ERR_SIZE;
     if (L < S) return PP_ERR_ARG;
     if (M % P != 0) return PP_ERR_DIVISIBILITY;
-    const uint64_t ncomb = ilv_host_binom(L - 1, S - 1);
+    const uint64_t ncomb = binom_u64(L - 1, S - 1);
     if (ncomb == ~0ull || ncomb == 0) return PP_ERR_SIZE;
     pp_plan *plan = nullptr;
     int rc = cached_plan(PP_INTERLEAVED_1F1B, P, M, v, stream, &plan);
