@@ -332,8 +332,7 @@ def main():
     host_c = torch.from_numpy(batch.comm).pin_memory()
     staging = {}
     for _ in range(2):
-        B.evaluate_host(batch.policy, P, M, 1, host_f, host_b, batch.strides, n, comm=host_c,
-                        comm_strides=batch.comm_strides, stream=stream, staging=staging)
+        B.evaluate_host(batch.policy, P, M, 1, host_f, host_b, n, comm=host_c, stream=stream, staging=staging)
     torch.cuda.synchronize()
     Ke = max(3, min(K, 100))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -342,8 +341,7 @@ def main():
     e0.record(stream)
     h2d = d2h = 0
     for _ in range(Ke):
-        _, h2d, d2h = B.evaluate_host(batch.policy, P, M, 1, host_f, host_b, batch.strides, n,
-                                      comm=host_c, comm_strides=batch.comm_strides, stream=stream,
+        _, h2d, d2h = B.evaluate_host(batch.policy, P, M, 1, host_f, host_b, n, comm=host_c, stream=stream,
                                       staging=staging)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -354,7 +352,7 @@ def main():
         e2e_s = float(t.item())
     e2e = {"value": world * ops_step * Ke / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "steps": Ke,
-           "api": "binding.evaluate_host (pinned host buffers -> pp_sched_eval -> host)"}
+           "api": "pp_sched_eval_host (C ABI, pinned host buffers in, host results out)"}
 
     extra = {}
     if not args.no_extra and rank == 0:

@@ -185,6 +185,29 @@ int pp_sched_eval_fb(pp_policy_t policy, int P, int M, int v,
                      int32_t *op_start, int32_t *op_end, int64_t op_stride_inst, int64_t op_stride_op,
                      int8_t *status, cudaStream_t stream);
 
+/* pp_sched_eval from HOST memory: the entry for callers whose cost tables
+ * are in host memory.  h_cost_f, h_cost_b are instance-minor [S][M][n] int32
+ * (element (s, i, x) at (s*M + i)*n + x) and h_comm [S-1][n] or NULL, in host
+ * memory (page-locked memory makes the copies asynchronous).  The call copies
+ * the instances chunk by chunk into the caller's device workspace d_work
+ * (256-byte aligned, work_bytes long; pp_sched_eval_host_workspace gives the
+ * size that holds the whole batch in one chunk, and any smaller size down to
+ * one chunk of 32 instances works), evaluates each chunk with pp_sched_eval
+ * and copies the chunk's results into the HOST outputs h_makespan [n], h_idle
+ * [n][P], h_bub_num [n], h_bub_den [n], h_peak [P], h_status [n] (each may be
+ * NULL), all on `stream`: the host outputs are valid once it completes.
+ * Errors: as pp_sched_eval; PP_ERR_ARG for a misaligned workspace; PP_ERR_SIZE
+ * when the workspace is smaller than a 32-instance chunk. */
+int pp_sched_eval_host(pp_policy_t policy, int P, int M, int v,
+                       const int32_t *h_cost_f, const int32_t *h_cost_b, const int32_t *h_comm,
+                       int64_t n_instances, void *d_work, size_t work_bytes,
+                       int32_t *h_makespan, int32_t *h_idle, int64_t *h_bub_num, int64_t *h_bub_den,
+                       int32_t *h_peak, int8_t *h_status, cudaStream_t stream);
+
+/* Device workspace bytes pp_sched_eval_host needs to take n_instances in one
+ * chunk (0 for bad arguments). */
+size_t pp_sched_eval_host_workspace(int P, int M, int v, int64_t n_instances);
+
 /* Score contiguous layer-to-stage partitions under 1F1B and return the best.
  * This is the profiling-based load balancing of [GPipe->ZB] (PipeDream and GPipe
  * sections: split layers into stages by measured cost) and [M040] §05, on the

@@ -23,7 +23,8 @@ ST_OK, ST_NEG_COST, ST_OVERFLOW, ST_ZERO_COST = 0, 1, 2, 3
 EXPORTS = ("pp_sched_plan", "pp_sched_plan_info", "pp_sched_plan_ops", "pp_sched_plan_destroy",
            "pp_sched_eval", "pp_sched_partition_search", "pp_sched_status_str",
            "pp_sched_cache_clear", "pp_sched_eval_noalloc", "pp_sched_eval_zb",
-           "pp_sched_partition_search_ranks", "pp_sched_partition_search_interleaved", "pp_sched_eval_fb")
+           "pp_sched_partition_search_ranks", "pp_sched_partition_search_interleaved", "pp_sched_eval_fb",
+           "pp_sched_eval_host", "pp_sched_eval_host_workspace")
 
 
 class PPSchedError(RuntimeError):
@@ -71,6 +72,11 @@ def _load():
     lib.pp_sched_eval_zb.argtypes = [i32, i32, i32, vp, vp, vp, i64, i64, i64, vp, i64, i64, i64,
                                      vp, vp, vp, vp, vp, vp, vp, i64, i64, vp, vp]
     lib.pp_sched_eval_zb.restype = i32
+    lib.pp_sched_eval_host.argtypes = [i32, i32, i32, i32, vp, vp, vp, i64, vp, ctypes.c_size_t,
+                                       vp, vp, vp, vp, vp, vp, vp]
+    lib.pp_sched_eval_host.restype = i32
+    lib.pp_sched_eval_host_workspace.argtypes = [i32, i32, i32, i64]
+    lib.pp_sched_eval_host_workspace.restype = ctypes.c_size_t
     lib.pp_sched_cache_clear.argtypes = []
     lib.pp_sched_cache_clear.restype = None
     return lib
@@ -232,45 +238,41 @@ def evaluate_zb(policy, P, M, cost_f, cost_b, cost_w, strides, n, comm=None, com
     return out
 
 
-def evaluate_host(policy, P, M, v, cost_f, cost_b, strides, n, comm=None, comm_strides=(0, 0),
-                  device="cuda", stream=None, staging=None):
-    """End-to-end call from HOST buffers (the public entry for CPU-resident
-    inputs): copies the inputs to the device, calls pp_sched_eval and copies
-    the summary outputs back, all on one stream.  `staging` may hold reusable
-    device buffers (dict) to avoid re-allocation across calls.  Returns
-    (outputs on host, bytes host->device, bytes device->host)."""
+def evaluate_host(policy, P, M, v, cost_f, cost_b, n, comm=None, stream=None, staging=None, workspace_bytes=None):
+    """End-to-end call from HOST buffers through pp_sched_eval_host (the public
+    entry for host-resident inputs): cost_f / cost_b are host int32 tensors in
+    the instance-minor layout [S][M][n] (page-locked for asynchronous copies),
+    comm [S-1][n] or None.  The library copies them to a device workspace,
+    evaluates and copies the summary outputs back on `stream`.  `staging` (a
+    dict) keeps the workspace and the host output tensors across calls;
+    `workspace_bytes` bounds the workspace (the default holds the whole batch).
+    Returns (outputs on host, bytes host->device, bytes device->host); the
+    outputs are valid once the stream has completed."""
     staging = staging if staging is not None else {}
-    s = stream or torch.cuda.current_stream()
-
-    def dev_copy(name, t):
-        if t is None:
-            return None
-        d = staging.get(name)
-        if d is None or d.numel() != t.numel() or d.dtype != t.dtype:
-            d = torch.empty(t.shape, dtype=t.dtype, device=device)
-            staging[name] = d
-        d.copy_(t, non_blocking=True)
-        return d
-
-    h2d = 0
-    with torch.cuda.stream(s):
-        df = dev_copy("cost_f", cost_f)
-        db = dev_copy("cost_b", cost_b)
-        dc = dev_copy("comm", comm)
-        h2d = sum(t.numel() * t.element_size() for t in (cost_f, cost_b, comm) if t is not None)
-        res = evaluate(policy, P, M, v, df, db, strides, n, comm=dc, comm_strides=comm_strides,
-                       out=staging.get("out"), stream=s)
-        staging["out"] = res
-        host = {}
-        d2h = 0
-        for k, t in res.items():
-            hk = staging.get("host_" + k)
-            if hk is None or hk.shape != t.shape:
-                hk = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                staging["host_" + k] = hk
-            hk.copy_(t, non_blocking=True)
-            host[k] = hk
-            d2h += t.numel() * t.element_size()
+    S = P * v
+    need = LIB.pp_sched_eval_host_workspace(P, M, v, n)
+    want_ws = int(workspace_bytes) if workspace_bytes is not None else int(need)
+    ws = staging.get("workspace")
+    if ws is None or ws.numel() != want_ws:
+        ws = torch.empty(max(want_ws, 1), dtype=torch.uint8, device="cuda")
+        staging["workspace"] = ws
+    host = {}
+    shapes = {"makespan": ((n,), torch.int32), "idle": ((n, P), torch.int32), "bub_num": ((n,), torch.int64),
+              "bub_den": ((n,), torch.int64), "peak": ((P,), torch.int32), "status": ((n,), torch.int8)}
+    for k, (shape, dt) in shapes.items():
+        hk = staging.get("host_" + k)
+        if hk is None or tuple(hk.shape) != shape:
+            hk = torch.empty(shape, dtype=dt, pin_memory=True)
+            staging["host_" + k] = hk
+        host[k] = hk
+    rc = LIB.pp_sched_eval_host(_policy(policy), P, M, v, cost_f.data_ptr(), cost_b.data_ptr(),
+                                None if comm is None else comm.data_ptr(), n, ws.data_ptr(), ws.numel(),
+                                host["makespan"].data_ptr(), host["idle"].data_ptr(), host["bub_num"].data_ptr(),
+                                host["bub_den"].data_ptr(), host["peak"].data_ptr(), host["status"].data_ptr(),
+                                _stream(stream))
+    _check(rc, "pp_sched_eval_host")
+    h2d = 4 * (2 * S * M * n + (0 if comm is None else max(S - 1, 0) * n))
+    d2h = sum(t.numel() * t.element_size() for t in host.values())
     return host, h2d, d2h
 
 

@@ -247,18 +247,28 @@ def test_split_call_equals_whole(orc, B):
         assert np.array_equal(np.concatenate([p[k] for p in parts]), whole[k])
 
 
-def test_host_entry_end_to_end(B):
+@pytest.mark.parametrize("policy,P,M,v,n,ws", [(W.ONEF1B, 8, 64, 1, 1000, None), (W.ONEF1B, 8, 64, 1, 1000, 200_000),
+                                               (W.INTERLEAVED, 4, 8, 2, 333, 40_000), (W.GPIPE, 3, 5, 1, 77, None)])
+def test_host_entry_end_to_end(orc, B, policy, P, M, v, n, ws):
+    """pp_sched_eval_host from pinned host buffers: the whole batch in one
+    chunk or in several (a small workspace), against the oracle."""
     import torch
-    batch = W.hetero_1f1b(n=1000)
-    ref = run_gpu(batch)
-    host, h2d, d2h = B.evaluate_host(batch.policy, 8, 64, 1, torch.from_numpy(batch.cost_f).pin_memory(),
-                                     torch.from_numpy(batch.cost_b).pin_memory(), batch.strides, batch.n,
-                                     comm=torch.from_numpy(batch.comm).pin_memory(),
-                                     comm_strides=batch.comm_strides)
+    if policy == W.ONEF1B and P == 8:
+        batch = W.hetero_1f1b(n=n)
+    else:
+        batch = W.random_batch(policy, P, M, v, n, seed=n, hi=20, comm_hi=5)
+    staging = {}
+    host, h2d, d2h = B.evaluate_host(batch.policy, P, M, v, torch.from_numpy(batch.cost_f).pin_memory(),
+                                     torch.from_numpy(batch.cost_b).pin_memory(), batch.n,
+                                     comm=torch.from_numpy(batch.comm).pin_memory(), staging=staging,
+                                     workspace_bytes=ws)
     torch.cuda.synchronize()
     assert h2d == batch.cost_f.nbytes * 2 + batch.comm.nbytes
-    for k in ("makespan", "idle", "bub_num", "bub_den", "status"):
-        assert np.array_equal(host[k].numpy(), ref[k])
+    r = run_oracle(orc, batch)
+    g = {k: t.numpy() for k, t in host.items()}
+    assert_same(g, r)
+    if ws is not None:
+        assert ws < B.LIB.pp_sched_eval_host_workspace(P, M, v, n)   # really several chunks
 
 
 FB_SHAPES = [(W.GPIPE, 4, 8, 1), (W.ONEF1B, 8, 16, 1), (W.ONEF1B, 3, 2, 1), (W.GPIPE_FIFO, 5, 6, 1),
