@@ -104,10 +104,11 @@ __global__ void k_ltab(const uint32_t *desc, const uint8_t *lrd, const uint8_t *
                     if (kind != kIdle) {
                         act = kLaneActive;
                         const uint32_t rs = lrd[(int64_t)r * PMAX + k], ws = lwr[(int64_t)r * PMAX + k];
-                        if (rs != kNoSlot) {
-                            rd = rs * row_bytes + col;
-                            cm = (2u * desc_chunk(d) + (kind == kBwd ? 1u : 0u)) * row_bytes + col;
-                        }
+                        // the op's (chunk, kind) row: its input edge's comm (0 where
+                        // there is no edge) and, with costs shared by all
+                        // microbatches, its cost
+                        cm = (2u * desc_chunk(d) + (kind == kBwd ? 1u : 0u)) * row_bytes + col;
+                        if (rs != kNoSlot) rd = rs * row_bytes + col;
                         if (ws != kNoSlot) {
                             const int kc = kind == kFwd ? (k + 1) % P : (k + P - 1) % P;
                             wr = ws * row_bytes + (uint32_t)(kc * G::kIPW * 4);
@@ -203,6 +204,11 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
     return v;
 }
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+    return v;
+}
 __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared.u32 [%0], %1;\n" ::"r"(addr), "r"(v) : "memory");
 }
@@ -219,16 +225,21 @@ __device__ __forceinline__ void lane_copy_block(const uint4 *blocks, int b, uint
 // NI instance sets per lane: a warp holds NI * 32/PMAX instances; every row
 // of the warp's shared memory is 32*NI words, set i in words 32i .. 32i+31,
 // so the second set of a row sits at a fixed +128 bytes.
-template <int PMAX, int NI, bool VEC, bool OPS>
+// MBZ: the costs are the same for every microbatch (stride_mb == 0), so each
+// lane keeps its (chunk, kind) costs next to the comm in shared memory -- the
+// ctab rows hold {cost, comm} pairs -- and the cost ring and its loader go.
+template <int PMAX, int NI, bool VEC, bool OPS, bool MBZ>
 __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4 *tab, int nblocks) {
     using G = LaneGeom<PMAX>;
     constexpr int kRow = 32 * NI;  // words per row
+    constexpr int kRingRows = MBZ ? 0 : G::kSlices;
+    constexpr int kCw = MBZ ? 2 : 1;  // words per ctab cell
     extern __shared__ __align__(16) uint32_t lsm[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const int j = lane % G::kIPW, k = lane / G::kIPW;
-    const int rows = G::kSlices + a.nslots + 2 + 2 * a.v + 1;
+    const int rows = kRingRows + a.nslots + 2 + (2 * a.v + 1) * kCw;
     uint32_t *ring = lsm + 2 * G::kBlockWords + warp * rows * kRow;
-    uint32_t *val = ring + G::kSlices * kRow;
+    uint32_t *val = ring + kRingRows * kRow;
     uint32_t *ctab = val + (a.nslots + 2) * kRow;
     const int64_t inst0 = ((int64_t)blockIdx.x * nwarps + warp) * (G::kIPW * NI);
     const int64_t x0 = inst0 + j;  // set i holds instance x0 + i * kIPW
@@ -241,10 +252,12 @@ __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4
     const uint32_t *head = reinterpret_cast<const uint32_t *>(tab);
     const LaneLoader<PMAX, NI, VEC> ld(a, lane, j, k, inst0);
     const uint32_t ring_s = smem_addr(ring);
+    if constexpr (!MBZ) {
 #pragma unroll 1
-    for (int q = 0; q < G::kAhead; ++q) {
-        ld.issue(__ldg(head + q * PMAX + k), ring_s + q * kRow * 4);
-        cp_async_commit();
+        for (int q = 0; q < G::kAhead; ++q) {
+            ld.issue(__ldg(head + q * PMAX + k), ring_s + q * kRow * 4);
+            cp_async_commit();
+        }
     }
     uint32_t ncomm[NI];
 #pragma unroll
@@ -260,15 +273,33 @@ __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4
             if (src && x < a.n && k < a.P && bnd >= 0 && bnd < a.S - 1)
                 c = src[x * a.c_inst + (int64_t)bnd * a.c_bnd];
             ncomm[i] |= (uint32_t)c;
-            ctab[cr * kRow + 32 * i + lane] = (uint32_t)c;
+            if constexpr (MBZ) {
+                int32_t cost = 0;
+                if (x < a.n && k < a.P)
+                    cost = ((cr & 1) ? a.cost_b : a.cost_f)[x * a.s_inst + (int64_t)s * a.s_stage];
+                ctab[(cr * kRow + 32 * i + lane) * 2] = (uint32_t)cost;
+                ctab[(cr * kRow + 32 * i + lane) * 2 + 1] = (uint32_t)c;
+            } else {
+                ctab[cr * kRow + 32 * i + lane] = (uint32_t)c;
+            }
         }
-        ctab[2 * a.v * kRow + 32 * i + lane] = 0;
+        if constexpr (MBZ) {
+            ctab[(2 * a.v * kRow + 32 * i + lane) * 2] = 0;
+            ctab[(2 * a.v * kRow + 32 * i + lane) * 2 + 1] = 0;
+        } else {
+            ctab[2 * a.v * kRow + 32 * i + lane] = 0;
+        }
         val[a.nslots * kRow + 32 * i + lane] = 0;
     }
-    cp_async_wait<G::kAhead>();
+    // the first table block (with MBZ nothing else is in flight)
+    if constexpr (MBZ) cp_async_wait<0>();
+    else cp_async_wait<G::kAhead>();
     __syncthreads();
 
-    const uint32_t val_s = smem_addr(val + j), ctab_s = smem_addr(ctab + j), cost_s = smem_addr(ring + lane);
+    const uint32_t val_s = smem_addr(val + j), cost_s = smem_addr(ring + lane);
+    // ctab cell of this lane's instance j: word offsets in the table entries
+    // count 4 bytes per cell, MBZ cells are 8 bytes
+    const uint32_t ctab_s = smem_addr(ctab + j * kCw);
     uint32_t fr[NI], busy[NI], flag[NI];
 #pragma unroll
     for (int i = 0; i < NI; ++i) { fr[i] = 0; busy[i] = 0; flag[i] = 0; }
@@ -276,6 +307,7 @@ __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4
 #pragma unroll 1
     for (int b = 0; b < nblocks; ++b) {
         if (b + 1 < nblocks) lane_copy_block<PMAX>(blocks, b + 1, lsm + ((b + 1) & 1) * G::kBlockWords);
+        if constexpr (MBZ) cp_async_commit();  // otherwise the copy joins the next round's group
         const uint32_t ent_s = smem_addr(lsm + (b & 1) * G::kBlockWords) + k * 16;
         const int n_r = min(R - b * G::kBR, G::kBR);
         // One round: the loader runs kAhead rounds ahead into ring row nxt,
@@ -288,15 +320,25 @@ __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4
         auto round = [&](int q, int cur, int nxt) {
             const uint4 e = nx;
             nx = lds128(ent_s + (q + 1) * PMAX * 16);
-            ld.issue(e.w, ring_s + nxt * kRow * 4);
-            cp_async_commit();
-            cp_async_wait<G::kAhead>();
+            if constexpr (!MBZ) {
+                ld.issue(e.w, ring_s + nxt * kRow * 4);
+                cp_async_commit();
+                cp_async_wait<G::kAhead>();
+            }
             __syncwarp();
-            const uint32_t vr = val_s + e.x, cr = ctab_s + e.y, vw = val_s + (e.z & ~kLaneActive);
+            const uint32_t vr = val_s + e.x, cr = ctab_s + e.y * kCw, vw = val_s + (e.z & ~kLaneActive);
 #pragma unroll
             for (int i = 0; i < NI; ++i) {
-                const uint32_t c = lds32(cost_s + (cur * kRow + 32 * i) * 4);
-                const uint32_t arr = lds32(vr + 128 * i) + lds32(cr + 128 * i);
+                uint32_t c, cm;
+                if constexpr (MBZ) {
+                    const uint2 cc = lds64(cr + 256 * i);
+                    c = cc.x;
+                    cm = cc.y;
+                } else {
+                    c = lds32(cost_s + (cur * kRow + 32 * i) * 4);
+                    cm = lds32(cr + 128 * i);
+                }
+                const uint32_t arr = lds32(vr + 128 * i) + cm;
                 const uint32_t st = max(fr[i], arr);
                 const uint32_t en = st + c;
                 flag[i] |= st | c;
@@ -322,6 +364,7 @@ __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4
         }
 #pragma unroll 1
         for (; q < n_r; ++q) round(q, q % G::kSlices, (q + G::kAhead) % G::kSlices);
+        if constexpr (MBZ) cp_async_wait<0>();  // the next block's table
         __syncthreads();
     }
     cp_async_wait<0>();
@@ -396,9 +439,9 @@ int lane_tables_t(pp_plan *plan, int64_t s_stage, int64_t s_mb, cudaStream_t str
 constexpr size_t kLaneSmemLimit = 227 * 1024;
 
 template <int PMAX>
-size_t lane_smem(const EvalArgs &a, int warps, int ni) {
+size_t lane_smem(const EvalArgs &a, int warps, int ni, bool mbz = false) {
     using G = LaneGeom<PMAX>;
-    const size_t rows = (size_t)G::kSlices + a.nslots + 2 + 2 * a.v + 1;
+    const size_t rows = (size_t)(mbz ? 0 : G::kSlices) + a.nslots + 2 + (size_t)(2 * a.v + 1) * (mbz ? 2 : 1);
     return 2 * (size_t)G::kBlockWords * 4 + (size_t)warps * rows * 32 * ni * 4;
 }
 
@@ -412,15 +455,15 @@ constexpr int64_t kLaneWarpsForTwoSets = 152 * 8;
 // busiest SM sets the time.  Take the size (8, 4 or 2 warps) whose busiest
 // SM holds the fewest warps with every CTA resident at once, the larger size
 // on a tie; with more than one wave, the largest size that fits.
-template <int PMAX, int NI, bool VEC, bool OPS>
+template <int PMAX, int NI, bool VEC, bool OPS, bool MBZ>
 int lane_warps(const EvalArgs &a, int64_t warps_total, int sms) {
     int best = 0;
     int64_t best_load = 0;
     for (int w = 8; w >= 2; w >>= 1) {
-        const size_t smem = lane_smem<PMAX>(a, w, NI);
+        const size_t smem = lane_smem<PMAX>(a, w, NI, MBZ);
         if (smem > kLaneSmemLimit) continue;
         int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_eval_lane<PMAX, NI, VEC, OPS>, w * 32, smem) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_eval_lane<PMAX, NI, VEC, OPS, MBZ>, w * 32, smem) !=
             cudaSuccess) {
             (void)cudaGetLastError();
             continue;
@@ -434,25 +477,25 @@ int lane_warps(const EvalArgs &a, int64_t warps_total, int sms) {
     return best;
 }
 
-template <int PMAX, int NI, bool VEC, bool OPS>
+template <int PMAX, int NI, bool VEC, bool OPS, bool MBZ>
 int launch_lane_t(const EvalArgs &a, const pp_ktab *t, cudaStream_t st) {
     using G = LaneGeom<PMAX>;
     int dev = 0;
     PPS_CUDA_TRY(cudaGetDevice(&dev));
     static bool attr_set[64] = {};
     if (dev < 64 && !attr_set[dev]) {
-        PPS_CUDA_TRY(cudaFuncSetAttribute(k_eval_lane<PMAX, NI, VEC, OPS>,
+        PPS_CUDA_TRY(cudaFuncSetAttribute(k_eval_lane<PMAX, NI, VEC, OPS, MBZ>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLaneSmemLimit));
         attr_set[dev] = true;
     }
     const int64_t nw = (a.n + G::kIPW * NI - 1) / (G::kIPW * NI);
-    const int warps = lane_warps<PMAX, NI, VEC, OPS>(a, nw, sm_count(dev));
+    const int warps = lane_warps<PMAX, NI, VEC, OPS, MBZ>(a, nw, sm_count(dev));
     if (!warps) return PP_ERR_SIZE;
-    const size_t smem = lane_smem<PMAX>(a, warps, NI);
+    const size_t smem = lane_smem<PMAX>(a, warps, NI, MBZ);
     const int64_t grid = (nw + warps - 1) / warps;
     if (grid > 0x7FFFFFFF) return PP_ERR_SIZE;
     const int nblocks = (a.R + G::kBR - 1) / G::kBR;
-    k_eval_lane<PMAX, NI, VEC, OPS><<<(unsigned)grid, warps * 32, smem, st>>>(a, t->d, nblocks);
+    k_eval_lane<PMAX, NI, VEC, OPS, MBZ><<<(unsigned)grid, warps * 32, smem, st>>>(a, t->d, nblocks);
     PPS_CUDA_TRY(cudaGetLastError());
     return PP_OK;
 }
@@ -462,9 +505,15 @@ int launch_lane_n(pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStre
     const pp_ktab *t = nullptr;
     const int rc = lane_tables_t<PMAX, NI>(plan, a.s_stage, a.s_mb, st, &t);
     if (rc) return rc;
+    // costs shared by every microbatch: kept per lane, no cost ring
+    if (a.s_mb == 0)
+        return ops ? launch_lane_t<PMAX, NI, false, true, true>(a, t, st)
+                   : launch_lane_t<PMAX, NI, false, false, true>(a, t, st);
     if (vec)
-        return ops ? launch_lane_t<PMAX, NI, true, true>(a, t, st) : launch_lane_t<PMAX, NI, true, false>(a, t, st);
-    return ops ? launch_lane_t<PMAX, NI, false, true>(a, t, st) : launch_lane_t<PMAX, NI, false, false>(a, t, st);
+        return ops ? launch_lane_t<PMAX, NI, true, true, false>(a, t, st)
+                   : launch_lane_t<PMAX, NI, true, false, false>(a, t, st);
+    return ops ? launch_lane_t<PMAX, NI, false, true, false>(a, t, st)
+               : launch_lane_t<PMAX, NI, false, false, false>(a, t, st);
 }
 
 template <int PMAX>

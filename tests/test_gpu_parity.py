@@ -281,9 +281,9 @@ def test_separate_backward_comm(orc, B, policy, P, M, v, layout):
     """pp_sched_eval_fb: a backward latency of its own on every boundary;
     every op time against the oracle's evaluation with comm_b."""
     import torch
-    for n, seed in ((61, 3), (130, 4)):
+    for n, seed, mbz in ((61, 3, False), (130, 4, True)):
         batch = W.random_batch(policy, P, M, v, n, seed=seed + P + M, hi=12, comm_hi=6, layout=layout,
-                               pad_to=4)
+                               pad_to=4, stride_mb_zero=mbz)
         cb = np.random.default_rng(seed).integers(0, 9, size=batch.comm.shape).astype(np.int32)
         out = B.evaluate(batch.policy, P, M, v, to_dev(batch.cost_f), to_dev(batch.cost_b), batch.strides, n,
                          comm=to_dev(batch.comm), comm_strides=batch.comm_strides, op_times=True, comm_b=to_dev(cb))
