@@ -340,6 +340,136 @@ __global__ void __launch_bounds__(128) k_eval_reg(const EvalArgs a) {
                                  ring);
 }
 
+// The register evaluator for costs shared by every microbatch (stride_mb ==
+// 0, e.g. per-stage costs): an op's cost depends only on its device and
+// kind, so there is nothing to load per round.  Each lane writes its
+// instance's costs once into four static round slices, one per round pattern
+// (alternating A and B, all-F, all-B), in the same [device][lane] layout the
+// round bodies read; a round that follows no pattern gets its slice from its
+// kind word.  No cost ring, no loader, no waits.
+template <int PMAX, bool OPS>
+__global__ void __launch_bounds__(128) k_eval_reg_mbz(const EvalArgs a) {
+    constexpr int kSl = PMAX * 32;  // words per slice
+    extern __shared__ __align__(16) int32_t smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    for (int i = threadIdx.x; i < a.ktab_words / 4; i += blockDim.x)
+        cp_async16(smem_addr(smem + 4 * i), a.ktab + i, 16u);
+    cp_async_commit();
+    const int tw = (a.R * PMAX + 3) & ~3;
+    const uint64_t *rws = reinterpret_cast<const uint64_t *>(smem + tw);
+    const uint4 *segs = reinterpret_cast<const uint4 *>(smem + tw + 2 * ((a.R + 1) & ~1));
+    int32_t *sl_alt_a = smem + a.ktab_words + warp * 5 * kSl;
+    int32_t *sl_alt_b = sl_alt_a + kSl, *sl_f = sl_alt_b + kSl, *sl_b = sl_f + kSl, *sl_gen = sl_b + kSl;
+    const int64_t inst0 = a.inst_begin + ((int64_t)blockIdx.x * nwarps + warp) * 32;
+    Lanes<1> L;
+    L.lane = lane;
+    L.x[0] = inst0 + lane;
+    L.live[0] = L.x[0] < a.n;
+    RegState<PMAX, 1> S;
+    uint32_t negc = 0;
+    S.flag[0] = 0;
+#pragma unroll
+    for (int k = 0; k < PMAX; ++k) {
+        int c = 0, f = 0, b = 0;
+        if (L.live[0] && k < a.P) {
+            if (a.comm && k < a.P - 1) c = a.comm[L.x[0] * a.c_inst + (int64_t)k * a.c_bnd];
+            f = a.cost_f[L.x[0] * a.s_inst + (int64_t)k * a.s_stage];
+            b = a.cost_b[L.x[0] * a.s_inst + (int64_t)k * a.s_stage];
+        }
+        negc |= (uint32_t)c;
+        S.cF[0][k] = (uint32_t)c;
+        S.fr[0][k] = 0; S.rf[0][k] = 0; S.rb[0][k] = 0; S.busy[0][k] = 0;
+        S.cnt[k] = 0;
+        sl_alt_a[k * 32 + lane] = (k & 1) ? b : f;
+        sl_alt_b[k * 32 + lane] = (k & 1) ? f : b;
+        sl_f[k * 32 + lane] = f;
+        sl_b[k * 32 + lane] = b;
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    if (inst0 >= a.n) return;  // warp-uniform, after the block barrier
+
+    // a lane reads only its own column of a slice, so no warp barrier is needed
+    auto round_w = [&](uint64_t w) {
+        const int32_t *sl;
+        switch (rw_pattern(w)) {
+            case kPatAltA: case kPatMasked + kPatAltA: sl = sl_alt_a; break;
+            case kPatAltB: case kPatMasked + kPatAltB: sl = sl_alt_b; break;
+            case kPatAllF: case kPatMasked + kPatAllF: sl = sl_f; break;
+            case kPatAllB: case kPatMasked + kPatAllB: sl = sl_b; break;
+            default: {
+                const uint32_t kinds = rw_kinds(w);
+#pragma unroll
+                for (int k = 0; k < PMAX; ++k)
+                    sl_gen[k * 32 + lane] = sl_f[(((kinds >> (2 * k)) & 3u) == kBwd ? kSl : 0) + k * 32 + lane];
+                sl = sl_gen;
+            }
+        }
+        run_round<PMAX, 1, OPS>(S, w, sl, a, L);
+    };
+#pragma unroll 1
+    for (int si = 0; si < a.nseg; ++si) {
+        const uint4 sg = segs[si];
+        int r = (int)sg.y;
+        const int r1 = (int)sg.z;
+        switch (sg.x) {
+            case kSegAltA:
+            case kSegAltB: {
+                bool a_next = sg.x == kSegAltA;
+#pragma unroll 1
+                for (; r + 1 < r1; r += 2) {
+                    if (a_next) {
+                        round_alt<PMAX, 1, OPS, false, true>(S, 0u, sl_alt_a, a, L);
+                        round_alt<PMAX, 1, OPS, false, false>(S, 0u, sl_alt_b, a, L);
+                    } else {
+                        round_alt<PMAX, 1, OPS, false, false>(S, 0u, sl_alt_b, a, L);
+                        round_alt<PMAX, 1, OPS, false, true>(S, 0u, sl_alt_a, a, L);
+                    }
+                }
+                if (r < r1) {
+                    if (a_next) round_alt<PMAX, 1, OPS, false, true>(S, 0u, sl_alt_a, a, L);
+                    else round_alt<PMAX, 1, OPS, false, false>(S, 0u, sl_alt_b, a, L);
+                }
+                break;
+            }
+            case kSegAllF:
+#pragma unroll 1
+                for (; r < r1; ++r) round_all_f<PMAX, 1, OPS, false>(S, 0u, sl_f, a, L);
+                break;
+            case kSegAllB:
+#pragma unroll 1
+                for (; r < r1; ++r) round_all_b<PMAX, 1, OPS, false>(S, 0u, sl_b, a, L);
+                break;
+            default:
+                round_w(rws[r]);
+                break;
+        }
+    }
+    __syncwarp();  // the slices are free: stage the idle block through them
+    write_results_warp<PMAX>(a, inst0, lane, S.fr[0], S.busy[0], S.flag[0], (negc >> 31) != 0, sl_alt_a);
+}
+
+template <int PMAX, bool OPS>
+static int launch_reg_mbz(const EvalArgs &a, cudaStream_t st) {
+    constexpr int kWarps = 4;
+    const size_t smem = (size_t)a.ktab_words * sizeof(uint32_t) + (size_t)kWarps * 5 * PMAX * 32 * sizeof(int32_t);
+    int dev = 0;
+    PPS_CUDA_TRY(cudaGetDevice(&dev));
+    static bool attr_set[64] = {};
+    if (dev < 64 && !attr_set[dev]) {
+        PPS_CUDA_TRY(cudaFuncSetAttribute(k_eval_reg_mbz<PMAX, OPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          160 * 1024));
+        attr_set[dev] = true;
+    }
+    const int64_t warps = (a.n + 31) / 32;
+    const int64_t blocks = (warps + kWarps - 1) / kWarps;
+    if (blocks > 0x7FFFFFFF) return PP_ERR_SIZE;
+    k_eval_reg_mbz<PMAX, OPS><<<(unsigned)blocks, kWarps * 32, smem, st>>>(a);
+    PPS_CUDA_TRY(cudaGetLastError());
+    return PP_OK;
+}
+
 template <int PMAX, int NI, bool VEC, bool OPS, bool LT>
 static int launch_reg_t(const EvalArgs &a, int64_t begin, int64_t end, cudaStream_t st) {
     // two-instance warps hold twice the ring: use two warps per block so the
@@ -380,6 +510,16 @@ constexpr int kMaxLtWords = 8192;
 
 template <int PMAX>
 static int launch_reg_p(pp_plan *plan, EvalArgs &a, bool vec, bool ops, cudaStream_t st) {
+    // costs shared by every microbatch: no loads per round
+    if (a.s_mb == 0 && ktab_words(a.R, PMAX, a.nseg) <= kMaxLtWords &&
+        (int64_t)(a.S - 1) * a.s_stage < ((int64_t)1 << 30)) {
+        const pp_ktab *t = nullptr;
+        const int rc = kernel_tables(plan, a.s_stage, a.s_mb, st, &t);
+        if (rc) return rc;
+        a.ktab = t->d;
+        a.ktab_words = t->words;
+        return ops ? launch_reg_mbz<PMAX, true>(a, st) : launch_reg_mbz<PMAX, false>(a, st);
+    }
     // the table path needs 16-byte aligned rows and offsets below 2^30
     const bool lt = vec && ktab_words(a.R, PMAX, a.nseg) <= kMaxLtWords &&
                     (int64_t)(a.S - 1) * a.s_stage + (int64_t)(a.M - 1) * a.s_mb < ((int64_t)1 << 30);

@@ -323,3 +323,24 @@ def test_two_lanes_per_instance(orc, B, policy, P, M):
         assert_same(g, r)
         if n >= 250:
             assert g["status"][5] == B.ST_NEG_COST and g["status"][9] == B.ST_OVERFLOW
+
+
+@pytest.mark.parametrize("policy,P,M", [(W.ONEF1B, 6, 9), (W.GPIPE, 8, 16), (W.GPIPE_FIFO, 4, 5), (W.ONEF1B, 16, 33)])
+@pytest.mark.parametrize("layout", ["inst_minor", "inst_major"])
+def test_costs_shared_by_microbatches(orc, B, policy, P, M, layout):
+    """stride_mb = 0 (a cost per instance and stage): the register evaluator
+    keeps the costs in static round slices; every output against the oracle,
+    with and without per-op times, a negative cost and an overflow."""
+    for n, seed, ops in ((1, 1, True), (45, 2, False), (300, 3, False), (300, 4, True)):
+        batch = W.random_batch(policy, P, M, 1, n, seed=seed + P, hi=40, comm_hi=6, layout=layout,
+                               stride_mb_zero=True)
+        if n == 300:
+            cf = batch.cost_f
+            si, ss, _ = batch.strides
+            cf[7 * si + 2 * ss] = -1
+            batch.cost_b[9 * si + (P - 1) * ss] = 2**31 - 3
+        g = run_gpu(batch, op_times=ops)
+        r = run_oracle(orc, batch, op_times=ops)
+        assert_same(g, r, op_times=ops)
+        if n == 300:
+            assert g["status"][7] == B.ST_NEG_COST and g["status"][9] == B.ST_OVERFLOW
