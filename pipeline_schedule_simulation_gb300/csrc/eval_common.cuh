@@ -37,6 +37,8 @@ struct EvalArgs {
     int64_t c_inst, c_bnd;
     int64_t n;
     int64_t inst_begin;      // first instance of this launch
+    int64_t tasks;           // register evaluator: > 0 when block b takes warp tasks
+                             // [b*tasks/grid, (b+1)*tasks/grid); 0: one per warp in grid order
     int32_t *makespan, *idle;
     int64_t *bub_num, *bub_den;
     int8_t *status;
@@ -64,6 +66,14 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
                  : "memory");
+}
+
+// 16 bytes, or 16 zero bytes without reading the source when `zero` is set.
+__device__ __forceinline__ void cp_async16_or_zero(uint32_t dst, const void *src, bool zero) {
+    asm volatile(
+        "{\n .reg .pred z;\n setp.ne.b32 z, %2, 0;\n cp.async.cg.shared.global [%0], [%1], 16, z;\n}\n" ::"r"(dst),
+        "l"(src), "r"((uint32_t)zero)
+        : "memory");
 }
 
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t src_bytes) {
@@ -171,6 +181,23 @@ __device__ __forceinline__ void load_round_lt(const uint32_t *lt, int rl, int32_
             nb = bytes_in;
         }
         cp_async16(smem_addr(slice + k * (NI * 32) + 4 * g), src, nb);
+    }
+}
+
+// The same loader for a warp whose 32*NI instances all exist: every copy is a
+// whole 16 bytes, and an idle slot is zero-filled without a read.  `e` holds
+// this lane's table entries of the round (rows 32/(8*NI)*i + lane/(8*NI)),
+// read ahead by the caller; `dst` is the shared address of this lane's first
+// chunk in the round's slice.
+template <int PMAX, int NI>
+__device__ __forceinline__ void load_round_lt_q(const uint32_t (&e)[PMAX * NI / 4], uint32_t dst, const int32_t *fbase,
+                                                const int32_t *bbase) {
+    constexpr int kRowsPerInst = 32 / (8 * NI);
+#pragma unroll
+    for (int i = 0; i < PMAX * NI / 4; ++i) {
+        const bool idle = e[i] == kLtIdle;
+        const int32_t *src = ((e[i] & 1u) ? bbase : fbase) + (idle ? 0u : (e[i] >> 1));
+        cp_async16_or_zero(dst + (uint32_t)(i * kRowsPerInst * NI * 32 * 4), src, idle);
     }
 }
 

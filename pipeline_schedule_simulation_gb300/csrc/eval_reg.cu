@@ -13,6 +13,7 @@
 // neighbouring device at the start of the op's round, so the whole state of an
 // instance is four registers per device: the device's free tick, the arrival
 // tick of its latest F and latest B at the neighbour, and its busy ticks.
+#include <type_traits>
 #include <utility>
 
 #include "eval_common.cuh"
@@ -197,10 +198,14 @@ __device__ __forceinline__ void run_round(RegState<PMAX, NI> &S, uint64_t w, con
 // in the alternating case), so the instances' state stays in the same
 // registers across iterations; warmup and cooldown rounds are dispatched one
 // at a time by their round word.  Copies run D = kAhead2 rounds ahead, one
-// cp.async group per round; a two-round step commits both rounds' groups and
-// then waits for both.
+// cp.async group per round.  A step waits for its rounds' groups, runs their
+// bodies and only then issues the copies D rounds ahead: those land in the
+// slices of the two rounds before the step, which every lane finished reading
+// before the step's warp barrier, and the address work of the copies overlaps
+// the bodies' arithmetic.  The table loader reads its entries two rounds
+// before it issues them, so no shared-memory load sits on the issue path.
 template <int PMAX, int NI, bool VEC, bool OPS, bool LT>
-__global__ void __launch_bounds__(128) k_eval_reg(const EvalArgs a) {
+__global__ void __maxnreg__(PMAX == 16 ? 168 : 96) k_eval_reg(const EvalArgs a) {
     static_assert(NI == 1 || LT, "two instances per thread need the table loader");
     using RG = Ring<PMAX, NI>;
     constexpr int D = RG::kAhead2;
@@ -222,7 +227,15 @@ __global__ void __launch_bounds__(128) k_eval_reg(const EvalArgs a) {
         segs = reinterpret_cast<const uint4 *>(smem + tw + 2 * ((a.R + 1) & ~1));
     }
     int32_t *ring = smem + lt_words + warp * RG::kWords;
-    const int64_t inst0 = a.inst_begin + ((int64_t)blockIdx.x * nwarps + warp) * (32 * NI);
+    int64_t task = (int64_t)blockIdx.x * nwarps + warp;
+    bool has_task = true;
+    if (a.tasks > 0) {
+        const int64_t t0 = (int64_t)blockIdx.x * a.tasks / gridDim.x;
+        const int64_t t1 = ((int64_t)blockIdx.x + 1) * a.tasks / gridDim.x;
+        task = t0 + warp;
+        has_task = task < t1;
+    }
+    const int64_t inst0 = has_task ? a.inst_begin + task * (32 * NI) : a.n;
     Lanes<NI> L;
     L.lane = lane;
 #pragma unroll
@@ -263,10 +276,28 @@ __global__ void __launch_bounds__(128) k_eval_reg(const EvalArgs a) {
     const int32_t *fbase = a.cost_f + (bytes_in ? x0 : 0);
     const int32_t *bbase = a.cost_b + (bytes_in ? x0 : 0);
     const int R = a.R;
-    auto issue = [&](int rl) {
+    constexpr uint32_t kSliceWords = PMAX * NI * 32;
+    // shared address of this lane's first 16-byte chunk in slice 0 (table loader)
+    const uint32_t dst_lane = smem_addr(ring) + (uint32_t)(((lane / (8 * NI)) * NI * 32 + 4 * g) * 4);
+    // the table loader's entries for the next two rounds it issues; the walk
+    // with `full` set (every instance of the warp exists) copies whole 16-byte
+    // chunks, the other (the last warp of a ragged batch) partial ones
+    constexpr int kRPL = PMAX * NI / 4;  // table entries a lane reads per round
+    uint32_t eq0[kRPL], eq1[kRPL];
+    auto ent = [&](int q, uint32_t (&e)[kRPL]) {
+        const uint32_t *row = lt + min(q, R - 1) * PMAX + lane / (8 * NI);
+#pragma unroll
+        for (int i = 0; i < kRPL; ++i) e[i] = row[(32 / (8 * NI)) * i];
+    };
+    if constexpr (LT) { ent(0, eq0); ent(1, eq1); }
+    auto issue = [&](int rl, auto full) {
         if (rl < R) {
             if constexpr (LT) {
-                load_round_lt<PMAX, NI>(lt, rl, ring, fbase, bbase, bytes_in, lane);
+                if constexpr (decltype(full)::value)
+                    load_round_lt_q<PMAX, NI>(eq0, dst_lane + ((uint32_t)rl & (RG::kSlices - 1)) * kSliceWords * 4,
+                                              fbase, bbase);
+                else
+                    load_round_lt<PMAX, NI>(lt, rl, ring, fbase, bbase, bytes_in, lane);
             } else {
                 LoadDesc<PMAX, VEC> ld;
                 fetch_load_desc<PMAX, VEC>(a, rl, lane, ld);
@@ -274,64 +305,70 @@ __global__ void __launch_bounds__(128) k_eval_reg(const EvalArgs a) {
             }
         }
         cp_async_commit();
+        if constexpr (LT && decltype(full)::value) {
+#pragma unroll
+            for (int i = 0; i < kRPL; ++i) eq0[i] = eq1[i];
+            ent(rl + 2, eq1);
+        }
     };
-    auto slice = [&](int r) { return ring + (r % RG::kSlices) * (PMAX * NI * 32); };
-    // one round: its copies D ahead, wait for it, run `body`
-    auto step1 = [&](int r, auto &&body) {
-        issue(r + D);
-        cp_async_wait<D>();
-        __syncwarp();
-        body(slice(r));
-        __syncwarp();
-    };
-    // two rounds: copies for both, then wait for both
-    auto step2 = [&](int r, auto &&body0, auto &&body1) {
-        issue(r + D);
-        issue(r + D + 1);
-        cp_async_wait<D>();
-        __syncwarp();
-        body0(slice(r));
-        body1(slice(r + 1));
-        __syncwarp();
-    };
+    auto slice = [&](int r) { return ring + ((uint32_t)r & (RG::kSlices - 1)) * kSliceWords; };
     auto altA = [&](const int32_t *sl) { round_alt<PMAX, NI, OPS, false, true>(S, 0u, sl, a, L); };
     auto altB = [&](const int32_t *sl) { round_alt<PMAX, NI, OPS, false, false>(S, 0u, sl, a, L); };
     auto allF = [&](const int32_t *sl) { round_all_f<PMAX, NI, OPS, false>(S, 0u, sl, a, L); };
     auto allB = [&](const int32_t *sl) { round_all_b<PMAX, NI, OPS, false>(S, 0u, sl, a, L); };
 
+    auto walk = [&](auto full) {
+        // one round: its copies D ahead, wait for it, run `body`
+        auto step1 = [&](int r, auto &&body) {
+            cp_async_wait<D - 1>();
+            __syncwarp();
+            body(slice(r));
+            issue(r + D, full);
+        };
+        auto step2 = [&](int r, auto &&body0, auto &&body1) {
+            cp_async_wait<D - 2>();
+            __syncwarp();
+            body0(slice(r));
+            body1(slice(r + 1));
+            issue(r + D, full);
+            issue(r + D + 1, full);
+        };
 #pragma unroll 1
-    for (int q = 0; q < D; ++q) issue(q);
+        for (int q = 0; q < D; ++q) issue(q, full);
 #pragma unroll 1
-    for (int si = 0; si < a.nseg; ++si) {
-        const uint4 sg = segs[si];
-        int r = (int)sg.y;
-        const int r1 = (int)sg.z;
-        switch (sg.x) {
-            case kSegAltA:
+        for (int si = 0; si < a.nseg; ++si) {
+            const uint4 sg = segs[si];
+            int r = (int)sg.y;
+            const int r1 = (int)sg.z;
+            switch (sg.x) {
+                case kSegAltA:
 #pragma unroll 1
-                for (; r + 1 < r1; r += 2) step2(r, altA, altB);
-                if (r < r1) step1(r, altA);
-                break;
-            case kSegAltB:
+                    for (; r + 1 < r1; r += 2) step2(r, altA, altB);
+                    if (r < r1) step1(r, altA);
+                    break;
+                case kSegAltB:
 #pragma unroll 1
-                for (; r + 1 < r1; r += 2) step2(r, altB, altA);
-                if (r < r1) step1(r, altB);
-                break;
-            case kSegAllF:
+                    for (; r + 1 < r1; r += 2) step2(r, altB, altA);
+                    if (r < r1) step1(r, altB);
+                    break;
+                case kSegAllF:
 #pragma unroll 1
-                for (; r < r1; ++r) step1(r, allF);
-                break;
-            case kSegAllB:
+                    for (; r < r1; ++r) step1(r, allF);
+                    break;
+                case kSegAllB:
 #pragma unroll 1
-                for (; r < r1; ++r) step1(r, allB);
-                break;
-            default: {
-                const uint64_t w = rws[r];
-                step1(r, [&](const int32_t *sl) { run_round<PMAX, NI, OPS>(S, w, sl, a, L); });
-                break;
+                    for (; r < r1; ++r) step1(r, allB);
+                    break;
+                default: {
+                    const uint64_t w = rws[r];
+                    step1(r, [&](const int32_t *sl) { run_round<PMAX, NI, OPS>(S, w, sl, a, L); });
+                    break;
+                }
             }
         }
-    }
+    };
+    if (LT && inst0 + 32 * NI <= a.n) walk(std::true_type{});
+    else walk(std::false_type{});
     cp_async_wait<0>();
     __syncwarp();  // the ring is free: stage the idle block through it
 #pragma unroll
@@ -476,23 +513,57 @@ static int launch_reg_t(const EvalArgs &a, int64_t begin, int64_t end, cudaStrea
     // blocks still spread evenly over the SMs
     constexpr int kWarps = NI == 1 ? 4 : 2;
     if (end <= begin) return PP_OK;
+    const auto kern = k_eval_reg<PMAX, NI, VEC, OPS, LT>;
     const size_t lt_bytes = LT ? (size_t)a.ktab_words * sizeof(uint32_t) : 0;
-    const size_t smem = lt_bytes + (size_t)kWarps * Ring<PMAX, NI>::kWords * sizeof(int32_t);
+    const size_t ring_bytes = (size_t)Ring<PMAX, NI>::kWords * sizeof(int32_t);
     int dev = 0;
     PPS_CUDA_TRY(cudaGetDevice(&dev));
-    static bool attr_set[64] = {};
-    if (dev < 64 && !attr_set[dev]) {
-        PPS_CUDA_TRY(cudaFuncSetAttribute(k_eval_reg<PMAX, NI, VEC, OPS, LT>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024));
-        attr_set[dev] = true;
+    if (dev >= 64) return PP_ERR_INTERNAL;
+    // per device: the shared memory a block may opt into (set on the kernel)
+    // and an SM's total
+    static int smem_optin[64] = {}, smem_sm[64] = {};
+    if (!smem_optin[dev]) {
+        int optin = 0, per_sm = 0;
+        PPS_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+        PPS_CUDA_TRY(cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev));
+        PPS_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin));
+        smem_sm[dev] = per_sm;
+        smem_optin[dev] = optin;
     }
     const int64_t warps = (end - begin + 32 * NI - 1) / (32 * NI);
-    const int64_t blocks = (warps + kWarps - 1) / kWarps;
-    if (blocks > 0x7FFFFFFF) return PP_ERR_SIZE;
     EvalArgs b = a;
     b.inst_begin = begin;
     b.n = end;
-    k_eval_reg<PMAX, NI, VEC, OPS, LT><<<(unsigned)blocks, kWarps * 32, smem, st>>>(b);
+    b.tasks = 0;
+    // A batch whose warps all fit on the GPU at once: one block per SM, block
+    // i taking warp tasks [i*T/G, (i+1)*T/G), so SMs differ by one warp at
+    // most (fixed-size blocks would leave some SMs a whole block more than
+    // others).  Asking for more than half an SM's shared memory keeps a
+    // second block off every SM.
+    if constexpr (NI == 1) {
+        const int nsm = sm_count(dev);
+        const int64_t grid = warps < nsm ? warps : nsm;
+        const int64_t wpb = (warps + grid - 1) / grid;
+        if (wpb <= 32) {
+            size_t smem = lt_bytes + (size_t)wpb * ring_bytes;
+            const size_t half = (size_t)smem_sm[dev] / 2;
+            if (smem < half) smem = half;
+            int fit = 0;
+            if (smem <= (size_t)smem_optin[dev] &&
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, kern, (int)wpb * 32, smem) == cudaSuccess &&
+                fit >= 1) {
+                b.tasks = warps;
+                kern<<<(unsigned)grid, (unsigned)wpb * 32, smem, st>>>(b);
+                PPS_CUDA_TRY(cudaGetLastError());
+                return PP_OK;
+            }
+            (void)cudaGetLastError();
+        }
+    }
+    const size_t smem = lt_bytes + (size_t)kWarps * ring_bytes;
+    const int64_t blocks = (warps + kWarps - 1) / kWarps;
+    if (blocks > 0x7FFFFFFF) return PP_ERR_SIZE;
+    kern<<<(unsigned)blocks, kWarps * 32, smem, st>>>(b);
     PPS_CUDA_TRY(cudaGetLastError());
     return PP_OK;
 }
