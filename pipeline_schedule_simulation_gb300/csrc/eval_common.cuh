@@ -44,7 +44,17 @@ struct EvalArgs {
     int8_t *status;
     int32_t *op_start, *op_end;
     int64_t o_inst, o_op;
+    const int32_t *peak_src;  // the plan's peak held activations per device [P]
+    int32_t *peak_dst;        // the caller's copy of it, written by block 0; null: none
 };
+
+// The cost-independent peak of the plan goes to the caller's array from inside
+// the evaluation kernel, so a call is one launch (no separate copy on the
+// stream).  Block 0's first P threads, before any early exit; every block has
+// at least one warp and P <= 16.
+__device__ __forceinline__ void copy_peak(const EvalArgs &a) {
+    if (a.peak_dst && blockIdx.x == 0 && threadIdx.x < (unsigned)a.P) a.peak_dst[threadIdx.x] = a.peak_src[threadIdx.x];
+}
 
 // Loader-table entry of an idle (round, device) slot.
 constexpr uint32_t kLtIdle = 0xFFFFFFFFu;

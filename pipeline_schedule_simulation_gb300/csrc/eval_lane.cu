@@ -230,6 +230,7 @@ __device__ __forceinline__ void lane_copy_block(const uint4 *blocks, int b, uint
 // ctab rows hold {cost, comm} pairs -- and the cost ring and its loader go.
 template <int PMAX, int NI, bool VEC, bool OPS, bool MBZ>
 __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4 *tab, int nblocks) {
+    copy_peak(a);
     using G = LaneGeom<PMAX>;
     constexpr int kRow = 32 * NI;  // words per row
     constexpr int kRingRows = MBZ ? 0 : G::kSlices;

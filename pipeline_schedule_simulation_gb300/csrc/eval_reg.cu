@@ -13,6 +13,7 @@
 // neighbouring device at the start of the op's round, so the whole state of an
 // instance is four registers per device: the device's free tick, the arrival
 // tick of its latest F and latest B at the neighbour, and its busy ticks.
+#include <atomic>
 #include <type_traits>
 #include <utility>
 
@@ -206,6 +207,7 @@ __device__ __forceinline__ void run_round(RegState<PMAX, NI> &S, uint64_t w, con
 // before it issues them, so no shared-memory load sits on the issue path.
 template <int PMAX, int NI, bool VEC, bool OPS, bool LT>
 __global__ void __maxnreg__(PMAX == 16 ? 168 : 96) k_eval_reg(const EvalArgs a) {
+    copy_peak(a);
     static_assert(NI == 1 || LT, "two instances per thread need the table loader");
     using RG = Ring<PMAX, NI>;
     constexpr int D = RG::kAhead2;
@@ -386,6 +388,7 @@ __global__ void __maxnreg__(PMAX == 16 ? 168 : 96) k_eval_reg(const EvalArgs a) 
 // kind word.  No cost ring, no loader, no waits.
 template <int PMAX, bool OPS>
 __global__ void __launch_bounds__(128) k_eval_reg_mbz(const EvalArgs a) {
+    copy_peak(a);
     constexpr int kSl = PMAX * 32;  // words per slice
     extern __shared__ __align__(16) int32_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -548,16 +551,27 @@ static int launch_reg_t(const EvalArgs &a, int64_t begin, int64_t end, cudaStrea
             size_t smem = lt_bytes + (size_t)wpb * ring_bytes;
             const size_t half = (size_t)smem_sm[dev] / 2;
             if (smem < half) smem = half;
-            int fit = 0;
-            if (smem <= (size_t)smem_optin[dev] &&
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, kern, (int)wpb * 32, smem) == cudaSuccess &&
-                fit >= 1) {
+            // whether such a block fits, remembered per device for the last
+            // (warps, shared memory) pair asked
+            // (key in the high word, blocks per SM in the low word)
+            static std::atomic<uint64_t> fit_memo[64];
+            const uint64_t key = ((uint64_t)wpb << 16 | (uint64_t)(smem >> 4)) + 1;
+            uint64_t memo = fit_memo[dev].load(std::memory_order_relaxed);
+            if (memo >> 32 != key) {
+                int fit = 0;
+                if (smem > (size_t)smem_optin[dev] ||
+                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, kern, (int)wpb * 32, smem) != cudaSuccess)
+                    fit = 0;
+                (void)cudaGetLastError();
+                memo = key << 32 | (uint32_t)fit;
+                fit_memo[dev].store(memo, std::memory_order_relaxed);
+            }
+            if ((int)(uint32_t)memo >= 1) {
                 b.tasks = warps;
                 kern<<<(unsigned)grid, (unsigned)wpb * 32, smem, st>>>(b);
                 PPS_CUDA_TRY(cudaGetLastError());
                 return PP_OK;
             }
-            (void)cudaGetLastError();
         }
     }
     const size_t smem = lt_bytes + (size_t)kWarps * ring_bytes;
@@ -661,10 +675,14 @@ int eval_impl(pp_policy_t policy, int P, int M, int v, const int32_t *cost_f, co
     pp_plan *plan = nullptr;
     rc = cached_plan((int)policy, P, M, v, stream, &plan);
     if (rc) return rc;
-    if (peak)
-        PPS_CUDA_TRY(cudaMemcpyAsync(peak, plan->d_peak, P * sizeof(int32_t), cudaMemcpyDeviceToDevice, stream));
-    if (n_instances == 0) return PP_OK;
+    if (n_instances == 0) {
+        // no evaluation kernel to carry the peak
+        if (peak)
+            PPS_CUDA_TRY(cudaMemcpyAsync(peak, plan->d_peak, P * sizeof(int32_t), cudaMemcpyDeviceToDevice, stream));
+        return PP_OK;
+    }
     EvalArgs a{};
+    a.peak_src = plan->d_peak; a.peak_dst = peak;
     a.desc = plan->d_desc; a.desc2 = plan->d_desc2; a.rw = plan->d_rw;
     a.seg = plan->d_seg; a.nseg = plan->nseg;
     a.ktab = nullptr; a.ktab_words = 0;

@@ -14,6 +14,7 @@ namespace pps {
 
 template <int PMAX, bool VEC, bool OPS>
 __global__ void __launch_bounds__(128) k_eval_slot(const EvalArgs a) {
+    copy_peak(a);
     using RG = Ring<PMAX>;
     extern __shared__ __align__(16) int32_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;

@@ -128,6 +128,7 @@ __device__ __forceinline__ void split_round(SplitState<H> &S, uint64_t w, int h,
 
 template <int PMAX>
 __global__ void __launch_bounds__(128) k_eval_split(const EvalArgs a) {
+    copy_peak(a);
     using G = SplitGeom<PMAX>;
     constexpr int H = G::kH, D = G::kAhead2;
     extern __shared__ __align__(16) int32_t smem[];

@@ -344,3 +344,45 @@ def test_costs_shared_by_microbatches(orc, B, policy, P, M, layout):
         assert_same(g, r, op_times=ops)
         if n == 300:
             assert g["status"][7] == B.ST_NEG_COST and g["status"][9] == B.ST_OVERFLOW
+
+
+# Every evaluator kernel writes the plan's peak itself (block 0), so a call is a
+# single launch; an empty batch still gets it (a copy on the stream).  Each
+# case lands on a different kernel: the one-lane register kernel (inst_minor,
+# full and ragged), the microbatch-shared register kernel (stride_mb 0), the
+# two-lane 8-wide kernel (small batch, summary outputs), the generic gather
+# (instance-major), the lane evaluator (interleaved; GPipe with comm_b).
+@pytest.mark.gpu
+@pytest.mark.parametrize("policy,P,M,v,n,layout,mbz,comm_b", [
+    (W.ONEF1B, 8, 64, 1, 4096, "inst_minor", False, False),
+    (W.ONEF1B, 8, 16, 1, 301, "inst_minor", False, False),
+    (W.GPIPE, 4, 12, 1, 500, "inst_minor", True, False),
+    (W.ONEF1B, 8, 12, 1, 90, "inst_minor", False, False),
+    (W.GPIPE_FIFO, 16, 9, 1, 77, "inst_major", False, False),
+    (W.INTERLEAVED, 4, 8, 2, 161, "inst_minor", False, False),
+    (W.INTERLEAVED, 8, 16, 4, 70, "inst_minor", True, False),
+    (W.GPIPE, 4, 8, 1, 33, "inst_major", False, True),
+    (W.ONEF1B, 8, 32, 1, 0, "inst_minor", False, False),
+])
+def test_peak_written_by_every_evaluator(policy, P, M, v, n, layout, mbz, comm_b):
+    import torch
+
+    import oracle
+    from pipeline_schedule_simulation_gb300 import binding as B
+    b = W.random_batch(policy, P, M, v, n, seed=900 + P + M + n, hi=20, layout=layout, stride_mb_zero=mbz)
+    out = {"peak": torch.full((P,), -5, dtype=torch.int32, device="cuda")}
+    if n:
+        out.update(makespan=torch.full((n,), -5, dtype=torch.int32, device="cuda"),
+                   status=torch.full((n,), -5, dtype=torch.int8, device="cuda"))
+    cm = to_dev(b.comm) if n else None
+    B.evaluate(b.policy, P, M, v, to_dev(b.cost_f) if n else torch.zeros(4, dtype=torch.int32, device="cuda"),
+               to_dev(b.cost_b) if n else torch.zeros(4, dtype=torch.int32, device="cuda"), b.strides, n,
+               comm=cm, comm_strides=b.comm_strides, outputs=("makespan", "peak", "status") if n else ("peak",),
+               out=out, comm_b=cm if comm_b else None)
+    torch.cuda.synchronize()
+    ref = oracle.eval_batch(policy, P, M, v, b.cost_f, b.cost_b, b.strides, comm=b.comm,
+                            comm_strides=b.comm_strides, n=n)
+    assert np.array_equal(out["peak"].cpu().numpy(), ref["peak"])
+    if n:
+        assert np.array_equal(out["status"].cpu().numpy(), ref["status"])
+        assert np.array_equal(out["makespan"].cpu().numpy(), ref["makespan"])
