@@ -167,9 +167,29 @@ class ClockSampler:
 # the CPU oracle baseline (bounded sample of the same workload)
 # ---------------------------------------------------------------------------
 
-def oracle_baseline(batch, target_s=10.0, max_inst=None):
+def cpu_model():
+    """The host CPU's name from /proc/cpuinfo (x86 "model name"; on Arm the
+    implementer / part codes), else the platform's processor string."""
+    import platform
+    try:
+        fields = {}
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+        if fields.get("model name"):
+            return fields["model name"]
+        if "CPU implementer" in fields:
+            return f"arm implementer {fields['CPU implementer']} part {fields.get('CPU part', '?')}"
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def oracle_baseline(batch, target_s=10.0, max_inst=None, threads=None):
     import oracle
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
     # calibrate on a small chunk, then run a sample sized for ~target_s of wall time
     def run(n):
         sub_f = batch.cost_f.reshape(P, M, batch.n)[:, :, :n]
@@ -376,6 +396,10 @@ def main():
         if not args.no_cpu:
             line["cpu_baseline"] = {k: v for k, v in oracle_baseline(batch).items()
                                     if k not in ("seconds", "instances")}
+            one = oracle_baseline(batch, target_s=3.0, threads=1)
+            line["cpu_baseline"]["single_thread"] = {"value": one["value"], "unit": UNIT, "cores": 1,
+                                                     "sample": one["sample"]}
+            line["cpu_baseline"]["cpu"] = cpu_model()
         if extra:
             line["secondary"] = extra
         print(json.dumps(line), flush=True)
