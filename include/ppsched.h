@@ -229,7 +229,9 @@ size_t pp_sched_eval_host_workspace(int P, int M, int v, int64_t n_instances);
  *   best_makespan int32 [1] (-1 then), best_cuts int32 [P-1] (first layer of
  *   stages 1..P-1; -1 then), all_makespan int32 [n_cand] or NULL (makespan, -1 if
  *   rejected by the cap, -2 if a tick would exceed INT32_MAX).
- * Limits: 1 <= P <= PP_MAX_P, P <= L <= 256, 0 <= n_cand < 2^32.
+ * Limits: 1 <= P <= PP_MAX_P, P <= L <= 256, 0 <= n_cand < 2^32, M <= PP_MAX_MV,
+ * and the number of splits C(L-1, P-1) below 2^64 - 1 (e.g. L <= 131 at P = 16);
+ * PP_ERR_SIZE otherwise.
  * Errors: PP_ERR_ARG, PP_ERR_SIZE, PP_ERR_CUDA. */
 int pp_sched_partition_search(const int32_t *layer_tf, const int32_t *layer_tb,
                               const int64_t *layer_act, int L, int P, int M, int32_t comm,
@@ -246,6 +248,8 @@ int pp_sched_partition_search(const int32_t *layer_tf, const int32_t *layer_tb,
  * feasible) and all_makespan indexed by rank - rank_begin.  A whole search is
  * rank_begin = 0, n_ranks = C(L-1, P-1) (2,898,753,715 for 80 layers into 8
  * stages); disjoint rank ranges reduce by (makespan, rank).
+ * Ranks are int64, so where C(L-1, P-1) exceeds 2^63 only the ranks below 2^63
+ * can be named.
  * Extra error: PP_ERR_ARG if rank_begin + n_ranks > C(L-1, P-1). */
 int pp_sched_partition_search_ranks(const int32_t *layer_tf, const int32_t *layer_tb,
                                     const int64_t *layer_act, int L, int P, int M, int32_t comm,
@@ -270,7 +274,9 @@ int pp_sched_partition_search_ranks(const int32_t *layer_tf, const int32_t *laye
  * 2 MB per virtual stage) and keeps; calls on one device share it, so calls
  * that overlap on the GPU must be serialized.  The first call for a shape also
  * builds its plan.
- * Limits: v >= 2, P*v <= PP_MAX_S, M % P == 0, S <= L <= 256, n_cand < 2^32.
+ * Limits: v >= 2, P*v <= PP_MAX_S, M % P == 0, M*v <= PP_MAX_MV, S <= L <= 256,
+ * n_cand < 2^32, and C(L-1, S-1) below 2^64 - 1 (e.g. L <= 84 at S = 64);
+ * PP_ERR_SIZE otherwise.
  * Errors: PP_ERR_ARG, PP_ERR_DIVISIBILITY, PP_ERR_SIZE, PP_ERR_CUDA. */
 int pp_sched_partition_search_interleaved(const int32_t *layer_tf, const int32_t *layer_tb,
                                           const int64_t *layer_act, int L, int P, int v, int M, int32_t comm,

@@ -74,3 +74,39 @@ def test_host_argument_errors_without_gpu():
     assert ps(80, 8, 8, ptr=12) == B.PP_ERR_ARG  # best_idx not 8-byte aligned
     for c in range(7):
         assert L.pp_sched_status_str(c)
+
+
+def test_one_past_each_limit_is_refused_without_gpu():
+    """One step past each declared limit answers PP_ERR_SIZE before any CUDA
+    call (the shapes at the limits themselves run in test_gpu_limits.py)."""
+    from pipeline_schedule_simulation_gb300 import binding as B
+    L = B.LIB
+    nul = None
+
+    def ev(pol, P, M, v):
+        return L.pp_sched_eval(pol, P, M, v, 8, 8, 1, 0, 0, nul, 0, 0, 4, nul, nul, nul, nul,
+                               nul, nul, nul, 0, 0, nul, nul)
+    assert ev(B.ONEF1B, 16, 32769, 1) == B.PP_ERR_SIZE       # M*v = PP_MAX_MV + 1
+    assert ev(B.GPIPE, 16, 32769, 1) == B.PP_ERR_SIZE
+    assert ev(B.INTERLEAVED, 2, 16386, 2) == B.PP_ERR_SIZE   # M*v = 32,772
+    assert ev(B.INTERLEAVED, 13, 13, 5) == B.PP_ERR_SIZE     # P*v = 65
+    assert L.pp_sched_eval_zb(B.ZB1P, 16, 32769, 8, 8, 8, 1, 0, 0, nul, 0, 0, 4, nul, nul, nul, nul, nul,
+                              nul, nul, 0, 0, nul, nul) == B.PP_ERR_SIZE
+    assert L.pp_sched_eval_zb(B.ZB2P, 17, 8, 8, 8, 8, 1, 0, 0, nul, 0, 0, 4, nul, nul, nul, nul, nul,
+                              nul, nul, 0, 0, nul, nul) == B.PP_ERR_SIZE
+
+    def ps(L_, P, M):
+        return L.pp_sched_partition_search(8, 8, 8, L_, P, M, 0, 0, 0, 0, 10, 8, 8, 8, nul, nul)
+
+    def pr(L_, P, M, begin, n):
+        return L.pp_sched_partition_search_ranks(8, 8, 8, L_, P, M, 0, 0, begin, n, 8, 8, 8, nul, nul)
+
+    def pi(L_, P, v, M):
+        return L.pp_sched_partition_search_interleaved(8, 8, 8, L_, P, v, M, 0, 0, 0, 0, 10, 8, 8, 8, nul, nul)
+    assert ps(132, 16, 8) == B.PP_ERR_SIZE         # C(131, 15) does not fit 64 bits
+    assert ps(257, 2, 8) == B.PP_ERR_SIZE
+    assert ps(131, 16, 32769) == B.PP_ERR_SIZE     # M beyond PP_MAX_MV
+    assert pr(132, 16, 8, 0, 10) == B.PP_ERR_SIZE
+    assert pr(20, 4, 8, 969 - 5, 6) == B.PP_ERR_ARG   # past the last rank, C(19, 3) = 969
+    assert pi(85, 16, 4, 16) == B.PP_ERR_SIZE      # C(84, 63) does not fit 64 bits
+    assert pi(84, 16, 4, 8208) == B.PP_ERR_SIZE    # M*v = 32,832
