@@ -4,8 +4,9 @@ The limits (ppsched.h): P <= PP_MAX_P = 16 devices, P*v <= PP_MAX_S = 64
 virtual stages, M*v <= PP_MAX_MV = 32,768 (65,536 ops per device), and in the
 searches L <= 256 layers with C(L-1, S-1) below 2^64.  Each case sits on one or
 more of them at once, with a ragged batch where the kernel works in warps of
-instances, and compares every output (per-op times included) bit for bit.  The refusals one step past each
-limit are host-side and tested without a GPU (test_abi.py).
+instances, and compares every output (per-op times included) bit for bit.
+The refusals one step past each limit are host-side and tested without a GPU
+(test_abi.py).
 """
 import numpy as np
 import pytest
