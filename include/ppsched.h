@@ -195,7 +195,15 @@ int pp_sched_eval_fb(pp_policy_t policy, int P, int M, int v,
  * one chunk of 32 instances works), evaluates each chunk with pp_sched_eval
  * and copies the chunk's results into the HOST outputs h_makespan [n], h_idle
  * [n][P], h_bub_num [n], h_bub_den [n], h_peak [P], h_status [n] (each may be
- * NULL), all on `stream`: the host outputs are valid once it completes.
+ * NULL).  The host outputs are valid once `stream` completes.  When the
+ * workspace holds two chunks of about n/4 instances (the size below does), the
+ * chunks alternate between two workspace slots and the evaluation and result
+ * copies of one chunk run on an auxiliary stream of the library while the
+ * next chunk is copied in on `stream`; events join the auxiliary stream back
+ * into `stream` before the call's work ends there.  The first such call on a
+ * device creates that stream and its events (make it before any stream
+ * capture); calls on one device enqueue one at a time.  With room for one
+ * chunk only, chunks run one after another on `stream`.
  * Errors: as pp_sched_eval; PP_ERR_ARG for a misaligned workspace; PP_ERR_SIZE
  * when the workspace is smaller than a 32-instance chunk. */
 int pp_sched_eval_host(pp_policy_t policy, int P, int M, int v,

@@ -248,25 +248,29 @@ def test_split_call_equals_whole(orc, B):
 
 
 @pytest.mark.parametrize("policy,P,M,v,n,ws", [(W.ONEF1B, 8, 64, 1, 1000, None), (W.ONEF1B, 8, 64, 1, 1000, 200_000),
-                                               (W.INTERLEAVED, 4, 8, 2, 333, 40_000), (W.GPIPE, 3, 5, 1, 77, None)])
+                                               (W.INTERLEAVED, 4, 8, 2, 333, 40_000), (W.GPIPE, 3, 5, 1, 77, None),
+                                               (W.ONEF1B, 4, 6, 1, 30, None), (W.ONEF1B, 8, 64, 1, 20000, None)])
 def test_host_entry_end_to_end(orc, B, policy, P, M, v, n, ws):
-    """pp_sched_eval_host from pinned host buffers: the whole batch in one
-    chunk or in several (a small workspace), against the oracle."""
+    """pp_sched_eval_host from pinned host buffers, two calls in a row: one
+    chunk (n <= 32), chunks one after another (a workspace with room for one
+    32-instance slot), or the two-slot pipeline over two streams (the default
+    workspace, and a small one with room for two slots), against the oracle."""
     import torch
     if policy == W.ONEF1B and P == 8:
-        batch = W.hetero_1f1b(n=n)
+        batches = [W.hetero_1f1b(n=n, seed=s) for s in (3, 4)]
     else:
-        batch = W.random_batch(policy, P, M, v, n, seed=n, hi=20, comm_hi=5)
+        batches = [W.random_batch(policy, P, M, v, n, seed=n + s, hi=20, comm_hi=5) for s in (0, 1)]
     staging = {}
-    host, h2d, d2h = B.evaluate_host(batch.policy, P, M, v, torch.from_numpy(batch.cost_f).pin_memory(),
-                                     torch.from_numpy(batch.cost_b).pin_memory(), batch.n,
-                                     comm=torch.from_numpy(batch.comm).pin_memory(), staging=staging,
-                                     workspace_bytes=ws)
-    torch.cuda.synchronize()
-    assert h2d == batch.cost_f.nbytes * 2 + batch.comm.nbytes
-    r = run_oracle(orc, batch)
-    g = {k: t.numpy() for k, t in host.items()}
-    assert_same(g, r)
+    for batch in batches:
+        host, h2d, d2h = B.evaluate_host(batch.policy, P, M, v, torch.from_numpy(batch.cost_f).pin_memory(),
+                                         torch.from_numpy(batch.cost_b).pin_memory(), batch.n,
+                                         comm=torch.from_numpy(batch.comm).pin_memory(), staging=staging,
+                                         workspace_bytes=ws)
+        torch.cuda.synchronize()
+        assert h2d == batch.cost_f.nbytes * 2 + batch.comm.nbytes
+        r = run_oracle(orc, batch)
+        g = {k: t.numpy().copy() for k, t in host.items()}
+        assert_same(g, r)
     if ws is not None:
         assert ws < B.LIB.pp_sched_eval_host_workspace(P, M, v, n)   # really several chunks
 
