@@ -432,7 +432,11 @@ def secondary(B, W, torch, stream):
                "op_end": torch.empty((P, O, N_INST), dtype=torch.int32, device="cuda")}
     t = timed(lambda: B.evaluate(1, P, M, 1, cf, cb, b3.strides, N_INST, comm=cm, comm_strides=b3.comm_strides,
                                  op_times=True, op_strides=(1, N_INST), out=ops_out, stream=stream), 20)
-    out["1f1b_P8_M64_with_op_times"] = {"op_times_per_s": 2 * P * M * N_INST / t, "ms": t * 1e3}
+    ob = algorithmic_bytes(N_INST) + 2 * 4 * 2 * P * M * N_INST  # + op_start and op_end, int32 each
+    peak_gbs, peak_src = measured_peaks()
+    out["1f1b_P8_M64_with_op_times"] = {"op_times_per_s": 2 * P * M * N_INST / t, "ms": t * 1e3,
+                                        "algorithmic_bytes": ob, "gbs": ob / t / 1e9,
+                                        "frac_of_hbm_peak": ob / t / 1e9 / peak_gbs, "peak_source": peak_src}
     del ops_out, cf, cb, cm
     for v in (2, 4):
         il, base = W.interleaved_vs_1f1b(v)
