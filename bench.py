@@ -187,7 +187,10 @@ def cpu_model():
     return platform.processor() or platform.machine()
 
 
-def oracle_baseline(batch, target_s=10.0, max_inst=None, threads=None):
+def oracle_baseline(batch, target_s=10.0, max_inst=None, threads=None, fixed=False):
+    """Time the oracle on the first instances of `batch`: a sample sized for
+    about target_s seconds after a short calibration, or (fixed) exactly
+    max_inst instances."""
     import oracle
     threads = threads or os.cpu_count() or 1
     # calibrate on a small chunk, then run a sample sized for ~target_s of wall time
@@ -202,11 +205,14 @@ def oracle_baseline(batch, target_s=10.0, max_inst=None, threads=None):
         oracle.eval_batch(1, P, M, 1, cf, cb, (1, M * n, n), comm=cm, comm_strides=(1, n), n=n,
                           method=0, nthreads=threads)
         return time.perf_counter() - t0
-    n0 = min(batch.n, 64 * threads)
-    t0 = run(n0)
-    n = int(min(batch.n, max(n0, n0 * target_s / max(t0, 1e-6))))
-    if max_inst:
-        n = min(n, max_inst)
+    if fixed and max_inst:
+        n = int(min(batch.n, max_inst))
+    else:
+        n0 = min(batch.n, 64 * threads)
+        t0 = run(n0)
+        n = int(min(batch.n, max(n0, n0 * target_s / max(t0, 1e-6))))
+        if max_inst:
+            n = min(n, max_inst)
     t = run(n)
     ops = 2 * P * M * n
     return {"value": ops / t, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -244,20 +250,23 @@ def dist_env():
     return rank, world, local
 
 
-def reference_arm(args):
+def reference_arm(args, budget_s=90.0):
     """The oracle, as it stands, on this machine's host cores: each step is a
-    bounded sample of the same workload."""
+    bounded sample of the same workload, sized once so that all warm-up and
+    timed steps together take about `budget_s` seconds of oracle time."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     import pipeline_schedule_simulation_gb300.workloads as W
     batch = W.hetero_1f1b(n=args.n)
     threads = os.cpu_count() or 1
-    per_step = None
+    steps = args.warmup + args.steps
+    cal = oracle_baseline(batch, target_s=min(2.0, budget_s / 10))
+    per_inst = cal["seconds"] / cal["instances"]
+    per_step = int(min(batch.n, max(threads, budget_s / max(steps, 1) / per_inst)))
     times = []
-    for i in range(args.warmup + args.steps):
-        r = oracle_baseline(batch, target_s=2.0, max_inst=per_step)
-        per_step = r["instances"]
+    for i in range(steps):
+        r = oracle_baseline(batch, max_inst=per_step, fixed=True)
         if i >= args.warmup:
             times.append(r["seconds"])
     total = sum(times)
@@ -270,7 +279,8 @@ def reference_arm(args):
         "data": "synthetic",
         "config": dict(bench_config(args.n, world), sample_instances_per_step=per_step),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"first {per_step} instances per step, event simulation, {threads} threads"},
+                         "sample": f"first {per_step} of the {batch.n} instances per step, event simulation, "
+                                   f"{threads} threads"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
