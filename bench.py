@@ -466,6 +466,7 @@ def secondary(B, W, torch, stream):
         out[f"{name}_P8_M64_n{N_INST}"] = {"op_times_per_s": bz.op_times / t, "ms": t * 1e3,
                                            "mean_makespan": float(zout["makespan"].float().mean().item())}
         del f, g, w, c, zout
+    out["closed_form_sweep"] = closed_form_sweep(B, W, torch, stream, timed)
     p = W.layer_split()
     lt, lb, la = (torch.from_numpy(x).cuda() for x in (p.layer_tf, p.layer_tb, p.layer_act))
     res = {}
@@ -491,6 +492,70 @@ def secondary(B, W, torch, stream):
         "best_rank": int(ex["best_idx"].item()), "best_makespan": int(ex["best_makespan"].item()),
         "best_cuts": ex["best_cuts"].cpu().tolist()}
     return out
+
+
+def closed_form_sweep(B, W, torch, stream, timed):
+    """The closed-form sweep (GPipe and 1F1B at P 2..16 x M 1..128, interleaved
+    v = 2 where P divides M; 16 scalar-cost instances per shape).  Timed as one
+    pp_sched_eval per shape -- the first pass (every shape's plan is built
+    then), later passes driven from Python, the same calls replayed from a CUDA
+    graph -- and as one prepared set of problems (pp_sched_many_*: a few fused
+    launches), called from Python and replayed from a CUDA graph."""
+    calls = []
+    op_times = 0
+    for pol, P_, M_, v_ in W.sweep_shapes():
+        bt = W.sweep_batch(pol, P_, M_, v_)
+        f, g, c = (torch.from_numpy(x).cuda() for x in (bt.cost_f, bt.cost_b, bt.comm))
+        o = {"makespan": torch.empty(bt.n, dtype=torch.int32, device="cuda"),
+             "idle": torch.empty((bt.n, P_), dtype=torch.int32, device="cuda"),
+             "bub_num": torch.empty(bt.n, dtype=torch.int64, device="cuda"),
+             "bub_den": torch.empty(bt.n, dtype=torch.int64, device="cuda"),
+             "peak": torch.empty(P_, dtype=torch.int32, device="cuda"),
+             "status": torch.empty(bt.n, dtype=torch.int8, device="cuda")}
+        calls.append((bt, f, g, c, o))
+        op_times += bt.op_times
+
+    def one_pass(st):
+        for bt, f, g, c, o in calls:
+            B.evaluate(bt.policy, bt.P, bt.M, bt.v, f, g, bt.strides, bt.n, comm=c,
+                       comm_strides=bt.comm_strides, out=o, stream=st)
+
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    one_pass(stream)
+    torch.cuda.synchronize()
+    first = time.perf_counter() - t0
+    loop = timed(lambda: one_pass(stream), 3)
+    res = {"shapes": len(calls), "instances": 16 * len(calls), "op_times": op_times,
+           "first_pass_ms": first * 1e3, "loop_ms": loop * 1e3, "loop_op_times_per_s": op_times / loop}
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            one_pass(side)
+        gt = timed(graph.replay, 3)
+        res.update(graph_ms=gt * 1e3, graph_op_times_per_s=op_times / gt)
+    except Exception as e:  # capture is a measurement aid here, not part of the path
+        res.update(graph_ms=None, graph_error=str(e)[:200])
+    # the same problems prepared once and evaluated together (pp_sched_many_*)
+    many = B.Many([{"policy": bt.policy, "P": bt.P, "M": bt.M, "v": bt.v, "n": bt.n, "strides": bt.strides,
+                    "cost_f": f, "cost_b": g, "comm": c, "comm_strides": bt.comm_strides, "out": o}
+                   for bt, f, g, c, o in calls], stream=stream)
+    mt = timed(lambda: many(stream=stream), 20)
+    res.update(many_ms=mt * 1e3, many_op_times_per_s=op_times / mt, many_info=many.info())
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            many(stream=side)
+        gt = timed(graph.replay, 20)
+        res.update(many_graph_ms=gt * 1e3, many_graph_op_times_per_s=op_times / gt)
+    except Exception as e:
+        res.update(many_graph_ms=None, many_graph_error=str(e)[:200])
+    many.close()
+    return res
 
 
 if __name__ == "__main__":

@@ -216,6 +216,67 @@ int pp_sched_eval_host(pp_policy_t policy, int P, int M, int v,
  * chunk (0 for bad arguments). */
 size_t pp_sched_eval_host_workspace(int P, int M, int v, int64_t n_instances);
 
+/* Many evaluation problems, each with its own shape (policy, P, M, v), cost
+ * tables and outputs, evaluated together.  This serves sweeps over schedule
+ * shapes -- the bubble's dependence on P, M and v in [1F1B] §4.3 and §6.1 and
+ * [M040] §04 -- where each shape has only a few instances: evaluated one call
+ * at a time, each problem is a CTA or two walking hundreds of dependent rounds
+ * and the GPU stays nearly idle.
+ *
+ * pp_problem_t holds the arguments of pp_sched_eval without per-op output;
+ * every pointer is caller-owned device memory, as there.
+ *
+ * pp_sched_many_prepare checks every problem as pp_sched_eval would (the first
+ * error found is returned and no handle is made), builds each shape's plan and
+ * the kernel tables of its strides (allocating and synchronizing `stream`),
+ * and records each problem in the handle:
+ *   - GPipe, GPipe FIFO and 1F1B problems whose costs are the same for every
+ *     microbatch (stride_mb == 0), and interleaved problems likewise, go to a
+ *     fused kernel: one launch per kernel kind and table width (at most six)
+ *     evaluates all of them, each problem's CTAs finding their problem in a
+ *     job table the handle keeps in device memory;
+ *   - every other problem (costs varying per microbatch, empty batches, shapes
+ *     whose tables do not fit the fused kernels) is evaluated by pp_sched_eval
+ *     inside pp_sched_many_eval.
+ * The handle records the problems' pointers, not their data: between
+ * evaluations the caller may rewrite the cost tables and read the outputs.
+ *
+ * pp_sched_many_eval enqueues the evaluation of every problem on `stream` (the
+ * device must be the one the handle was prepared on); the results equal those
+ * of pp_sched_eval on each problem.  It allocates nothing; when every problem
+ * went to a fused kernel it only launches kernels, and can be captured in a
+ * CUDA graph.  Evaluations of one handle that overlap on the GPU write the
+ * same outputs; serialize them.
+ *
+ * pp_sched_many_info reports how many problems were fused, in how many
+ * launches, and how many are evaluated one by one.
+ *
+ * The handle refers to the library's cached plans: call pp_sched_cache_clear
+ * only after destroying every handle.  Free a handle with
+ * pp_sched_many_destroy once its evaluations have completed.
+ * Errors: as pp_sched_eval; PP_ERR_ARG for a null handle pointer, a negative
+ * count or a null problem array with a positive count. */
+typedef struct pp_problem {
+    pp_policy_t policy;
+    int P, M, v;
+    const int32_t *cost_f, *cost_b;
+    int64_t stride_inst, stride_stage, stride_mb;
+    const int32_t *comm;
+    int64_t comm_stride_inst, comm_stride_bnd;
+    int64_t n_instances;
+    int32_t *makespan, *idle;
+    int64_t *bub_num, *bub_den;
+    int32_t *peak;
+    int8_t *status;
+} pp_problem_t;
+
+typedef struct pp_many pp_many_t;
+
+int pp_sched_many_prepare(const pp_problem_t *problems, int n_problems, pp_many_t **many, cudaStream_t stream);
+int pp_sched_many_eval(const pp_many_t *many, cudaStream_t stream);
+int pp_sched_many_info(const pp_many_t *many, int *fused_problems, int *launches, int *other_problems);
+void pp_sched_many_destroy(pp_many_t *many);
+
 /* Score contiguous layer-to-stage partitions under 1F1B and return the best.
  * This is the profiling-based load balancing of [GPipe->ZB] (PipeDream and GPipe
  * sections: split layers into stages by measured cost) and [M040] §05, on the

@@ -24,7 +24,20 @@ EXPORTS = ("pp_sched_plan", "pp_sched_plan_info", "pp_sched_plan_ops", "pp_sched
            "pp_sched_eval", "pp_sched_partition_search", "pp_sched_status_str",
            "pp_sched_cache_clear", "pp_sched_eval_noalloc", "pp_sched_eval_zb",
            "pp_sched_partition_search_ranks", "pp_sched_partition_search_interleaved", "pp_sched_eval_fb",
-           "pp_sched_eval_host", "pp_sched_eval_host_workspace")
+           "pp_sched_eval_host", "pp_sched_eval_host_workspace", "pp_sched_many_prepare", "pp_sched_many_eval",
+           "pp_sched_many_info", "pp_sched_many_destroy")
+
+
+class Problem(ctypes.Structure):
+    """pp_problem_t: one problem of pp_sched_many_* (the arguments of
+    pp_sched_eval without per-op output)."""
+    _fields_ = [("policy", ctypes.c_int), ("P", ctypes.c_int), ("M", ctypes.c_int), ("v", ctypes.c_int),
+                ("cost_f", ctypes.c_void_p), ("cost_b", ctypes.c_void_p),
+                ("stride_inst", ctypes.c_int64), ("stride_stage", ctypes.c_int64), ("stride_mb", ctypes.c_int64),
+                ("comm", ctypes.c_void_p), ("comm_stride_inst", ctypes.c_int64), ("comm_stride_bnd", ctypes.c_int64),
+                ("n_instances", ctypes.c_int64), ("makespan", ctypes.c_void_p), ("idle", ctypes.c_void_p),
+                ("bub_num", ctypes.c_void_p), ("bub_den", ctypes.c_void_p), ("peak", ctypes.c_void_p),
+                ("status", ctypes.c_void_p)]
 
 
 class PPSchedError(RuntimeError):
@@ -52,6 +65,14 @@ def _load():
     lib.pp_sched_eval.argtypes = [i32, i32, i32, i32, vp, vp, i64, i64, i64, vp, i64, i64, i64,
                                   vp, vp, vp, vp, vp, vp, vp, i64, i64, vp, vp]
     lib.pp_sched_eval.restype = i32
+    lib.pp_sched_many_prepare.argtypes = [vp, i32, ctypes.POINTER(vp), vp]
+    lib.pp_sched_many_prepare.restype = i32
+    lib.pp_sched_many_eval.argtypes = [vp, vp]
+    lib.pp_sched_many_eval.restype = i32
+    lib.pp_sched_many_info.argtypes = [vp, vp, vp, vp]
+    lib.pp_sched_many_info.restype = i32
+    lib.pp_sched_many_destroy.argtypes = [vp]
+    lib.pp_sched_many_destroy.restype = None
     lib.pp_sched_eval_fb.argtypes = [i32, i32, i32, i32, vp, vp, i64, i64, i64, vp, vp, i64, i64, i64,
                                      vp, vp, vp, vp, vp, vp, vp, i64, i64, vp, vp]
     lib.pp_sched_eval_fb.restype = i32
@@ -236,6 +257,64 @@ def evaluate_zb(policy, P, M, cost_f, cost_b, cost_w, strides, n, comm=None, com
                               op_strides[0], op_strides[1], _ptr(stt), _stream(stream))
     _check(rc, "pp_sched_eval_zb")
     return out
+
+
+class Many:
+    """pp_sched_many_*: many problems, each with its own shape, evaluated
+    together.  `problems` is a list of dicts with the keys policy, P, M, v,
+    cost_f, cost_b, strides (inst, stage, mb), n and optionally comm,
+    comm_strides, and `out` (a dict of preallocated CUDA output tensors:
+    makespan, idle, bub_num, bub_den, peak, status; missing ones are
+    allocated).  The tensors are kept alive by this object; the library keeps
+    their pointers, so rewrite their contents in place between evaluations.
+    prepare() builds plans and tables (it may allocate and synchronize);
+    __call__ enqueues one evaluation of every problem on `stream`."""
+
+    def __init__(self, problems, stream=None):
+        self.handle = None
+        self.problems = []
+        arr = (Problem * max(len(problems), 1))()
+        for i, q in enumerate(problems):
+            P, n = q["P"], q["n"]
+            out = dict(q.get("out") or {})
+            dev = q["cost_f"].device
+            for k, shape, dt in (("makespan", (n,), torch.int32), ("idle", (n, P), torch.int32),
+                                 ("bub_num", (n,), torch.int64), ("bub_den", (n,), torch.int64),
+                                 ("peak", (P,), torch.int32), ("status", (n,), torch.int8)):
+                if k not in out:
+                    out[k] = torch.empty(shape, dtype=dt, device=dev)
+            comm = q.get("comm")
+            cs = q.get("comm_strides", (0, 0))
+            si, ss, sm = q["strides"]
+            arr[i] = Problem(_policy(q["policy"]), P, q["M"], q.get("v", 1), _ptr(q["cost_f"]), _ptr(q["cost_b"]),
+                             si, ss, sm, _ptr(comm), cs[0], cs[1], n, _ptr(out["makespan"]), _ptr(out["idle"]),
+                             _ptr(out["bub_num"]), _ptr(out["bub_den"]), _ptr(out["peak"]), _ptr(out["status"]))
+            self.problems.append(dict(q, out=out))
+        h = ctypes.c_void_p()
+        _check(LIB.pp_sched_many_prepare(ctypes.cast(arr, ctypes.c_void_p), len(problems), ctypes.byref(h),
+                                         _stream(stream)), "pp_sched_many_prepare")
+        self.handle = h
+
+    def info(self):
+        f, l_, o = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+        _check(LIB.pp_sched_many_info(self.handle, ctypes.byref(f), ctypes.byref(l_), ctypes.byref(o)),
+               "pp_sched_many_info")
+        return {"fused_problems": f.value, "launches": l_.value, "other_problems": o.value}
+
+    def __call__(self, stream=None):
+        _check(LIB.pp_sched_many_eval(self.handle, _stream(stream)), "pp_sched_many_eval")
+        return [q["out"] for q in self.problems]
+
+    def close(self):
+        if self.handle:
+            LIB.pp_sched_many_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def evaluate_host(policy, P, M, v, cost_f, cost_b, n, comm=None, stream=None, staging=None, workspace_bytes=None):

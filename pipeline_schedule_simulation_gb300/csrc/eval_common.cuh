@@ -52,8 +52,32 @@ struct EvalArgs {
 // the evaluation kernel, so a call is one launch (no separate copy on the
 // stream).  Block 0's first P threads, before any early exit; every block has
 // at least one warp and P <= 16.
-__device__ __forceinline__ void copy_peak(const EvalArgs &a) {
-    if (a.peak_dst && blockIdx.x == 0 && threadIdx.x < (unsigned)a.P) a.peak_dst[threadIdx.x] = a.peak_src[threadIdx.x];
+__device__ __forceinline__ void copy_peak(const EvalArgs &a, int64_t bid) {
+    if (a.peak_dst && bid == 0 && threadIdx.x < (unsigned)a.P) a.peak_dst[threadIdx.x] = a.peak_src[threadIdx.x];
+}
+__device__ __forceinline__ void copy_peak(const EvalArgs &a) { copy_peak(a, blockIdx.x); }
+
+// One problem of a fused launch over many problems (pp_sched_many_*): its
+// arguments as pp_sched_eval would pass them, the lane evaluator's table and
+// block count (unused by the register kernel), and the problem's first CTA in
+// the fused grid.  A fused kernel finds its problem by binary search over
+// block_begin (ascending) and runs the single-problem body with the CTA's
+// index within the problem.
+struct ManyJob {
+    EvalArgs a;
+    const uint4 *tab;
+    int nblocks;
+    int64_t block_begin;
+};
+
+__device__ __forceinline__ int many_job_of(const ManyJob *jobs, int njobs, int64_t cta) {
+    int lo = 0, hi = njobs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (jobs[mid].block_begin <= cta) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
 }
 
 // Loader-table entry of an idle (round, device) slot.
@@ -366,5 +390,37 @@ int launch_eval_slot(const pp_plan *plan, const EvalArgs &a, bool vec, bool ops,
 bool lane_path(const pp_plan *plan, const EvalArgs &a);
 int launch_eval_split8(const EvalArgs &a, cudaStream_t st);
 int launch_eval_lane(pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st);
+
+// Fused launches over many problems (pp_sched_many_*).  *_job prepares one
+// problem's arguments (its tables built, allocating and synchronizing on first
+// use) and answers whether the fused kernel takes it; *_warps is the warps its
+// instances fill, *_ctas the CTAs of `warps` warps it needs, *_smem the
+// dynamic shared memory of such a CTA; launch_*_many runs a group of jobs of
+// one table width, already in device memory, with CTAs of `warps` warps (at
+// most kManyRegWarps / kManyLaneWarps).
+constexpr int kManyRegWarps = 4, kManyLaneWarps = 2;
+bool reg_mbz_job(pp_plan *plan, EvalArgs &a, cudaStream_t st, int *rc);
+int64_t reg_mbz_warps(const EvalArgs &a);
+int64_t reg_mbz_ctas(const EvalArgs &a, int warps);
+size_t reg_mbz_smem(int pmax, const EvalArgs &a, int warps);
+int launch_reg_mbz_many(int pmax, int warps, const ManyJob *d_jobs, int njobs, int64_t ctas, size_t smem,
+                        cudaStream_t st);
+bool lane_mbz_job(pp_plan *plan, EvalArgs &a, const uint4 **tab, int *nblocks, cudaStream_t st, int *rc);
+int64_t lane_mbz_warps(int pmax, const EvalArgs &a);
+int64_t lane_mbz_ctas(int pmax, const EvalArgs &a, int warps);
+size_t lane_mbz_smem(int pmax, const EvalArgs &a, int warps);
+int launch_lane_mbz_many(int pmax, int warps, const ManyJob *d_jobs, int njobs, int64_t ctas, size_t smem,
+                         cudaStream_t st);
+
+// Argument checks and EvalArgs of pp_sched_eval (eval_reg.cu), shared with
+// the multi-problem entry points.
+int eval_check(pp_policy_t policy, int P, int M, int v, const int32_t *cost_f, const int32_t *cost_b,
+               int64_t stride_inst, int64_t stride_stage, int64_t stride_mb, int64_t comm_stride_inst,
+               int64_t comm_stride_bnd, int64_t n_instances);
+EvalArgs eval_args(const pp_plan *plan, const int32_t *cost_f, const int32_t *cost_b, int64_t stride_inst,
+                   int64_t stride_stage, int64_t stride_mb, const int32_t *comm, const int32_t *comm_b,
+                   int64_t comm_stride_inst, int64_t comm_stride_bnd, int64_t n_instances, int32_t *makespan,
+                   int32_t *idle, int64_t *bub_num, int64_t *bub_den, int32_t *peak, int32_t *op_start,
+                   int32_t *op_end, int64_t op_stride_inst, int64_t op_stride_op, int8_t *status);
 
 }  // namespace pps

@@ -228,9 +228,11 @@ __device__ __forceinline__ void lane_copy_block(const uint4 *blocks, int b, uint
 // MBZ: the costs are the same for every microbatch (stride_mb == 0), so each
 // lane keeps its (chunk, kind) costs next to the comm in shared memory -- the
 // ctab rows hold {cost, comm} pairs -- and the cost ring and its loader go.
+// The body takes the CTA's index within its problem (`bid`), so the fused
+// kernel over many problems runs it too.
 template <int PMAX, int NI, bool VEC, bool OPS, bool MBZ>
-__global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4 *tab, int nblocks) {
-    copy_peak(a);
+__device__ __forceinline__ void lane_body(const EvalArgs &a, const uint4 *tab, int nblocks, int64_t bid) {
+    copy_peak(a, bid);
     using G = LaneGeom<PMAX>;
     constexpr int kRow = 32 * NI;  // words per row
     constexpr int kRingRows = MBZ ? 0 : G::kSlices;
@@ -242,7 +244,7 @@ __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4
     uint32_t *ring = lsm + 2 * G::kBlockWords + warp * rows * kRow;
     uint32_t *val = ring + kRingRows * kRow;
     uint32_t *ctab = val + (a.nslots + 2) * kRow;
-    const int64_t inst0 = ((int64_t)blockIdx.x * nwarps + warp) * (G::kIPW * NI);
+    const int64_t inst0 = (bid * nwarps + warp) * (G::kIPW * NI);
     const int64_t x0 = inst0 + j;  // set i holds instance x0 + i * kIPW
     const uint4 *blocks = tab + G::kHeadWords / 4;
     const int R = a.R;
@@ -406,6 +408,20 @@ __global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4
     }
 }
 
+template <int PMAX, int NI, bool VEC, bool OPS, bool MBZ>
+__global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4 *tab, int nblocks) {
+    lane_body<PMAX, NI, VEC, OPS, MBZ>(a, tab, nblocks, blockIdx.x);
+}
+
+// Many interleaved problems with microbatch-shared costs in one launch (one
+// instance set per lane): CTA c runs CTA c - block_begin of its problem.
+template <int PMAX>
+__global__ void __launch_bounds__(256) k_eval_lane_mbz_many(const ManyJob *jobs, int njobs) {
+    const int j = many_job_of(jobs, njobs, blockIdx.x);
+    const EvalArgs &a = jobs[j].a;  // read in place: uniform per CTA, cached
+    lane_body<PMAX, 1, false, false, true>(a, jobs[j].tab, jobs[j].nblocks, (int64_t)blockIdx.x - jobs[j].block_begin);
+}
+
 namespace {
 
 template <int PMAX, int NI>
@@ -549,6 +565,73 @@ int launch_eval_lane(pp_plan *plan, const EvalArgs &args, bool vec, bool ops, cu
         case 4: return launch_lane_p<4>(plan, a, vec, ops, st);
         case 8: return launch_lane_p<8>(plan, a, vec, ops, st);
         case 16: return launch_lane_p<16>(plan, a, vec, ops, st);
+        default: return PP_ERR_INTERNAL;
+    }
+}
+
+// The fused lane path over many problems: plans without the register path
+// (interleaved) whose costs are the same for every microbatch, without
+// per-op output or a separate backward latency.
+bool lane_mbz_job(pp_plan *plan, EvalArgs &a, const uint4 **tab, int *nblocks, cudaStream_t st, int *rc) {
+    *rc = PP_OK;
+    if (plan->reg_ok || a.comm_b || a.op_start || a.op_end || a.s_mb != 0 || a.n <= 0) return false;
+    if (!lane_path(plan, a)) return false;
+    a.nslots = plan->nlslots;
+    if (lane_mbz_smem(plan->pmax, a, kManyLaneWarps) > kLaneSmemLimit) return false;
+    const pp_ktab *t = nullptr;
+    switch (plan->pmax) {
+        case 4: *rc = lane_tables_t<4, 1>(plan, a.s_stage, a.s_mb, st, &t); *nblocks = (a.R + LaneGeom<4>::kBR - 1) / LaneGeom<4>::kBR; break;
+        case 8: *rc = lane_tables_t<8, 1>(plan, a.s_stage, a.s_mb, st, &t); *nblocks = (a.R + LaneGeom<8>::kBR - 1) / LaneGeom<8>::kBR; break;
+        case 16: *rc = lane_tables_t<16, 1>(plan, a.s_stage, a.s_mb, st, &t); *nblocks = (a.R + LaneGeom<16>::kBR - 1) / LaneGeom<16>::kBR; break;
+        default: *rc = PP_ERR_INTERNAL;
+    }
+    if (*rc) return false;
+    *tab = t->d;
+    return true;
+}
+
+int64_t lane_mbz_warps(int pmax, const EvalArgs &a) {
+    const int64_t ipw = 32 / pmax;  // instances per warp
+    return (a.n + ipw - 1) / ipw;
+}
+
+int64_t lane_mbz_ctas(int pmax, const EvalArgs &a, int warps) {
+    return (lane_mbz_warps(pmax, a) + warps - 1) / warps;
+}
+
+size_t lane_mbz_smem(int pmax, const EvalArgs &a, int warps) {
+    switch (pmax) {
+        case 4: return lane_smem<4>(a, warps, 1, true);
+        case 8: return lane_smem<8>(a, warps, 1, true);
+        case 16: return lane_smem<16>(a, warps, 1, true);
+        default: return ~(size_t)0;
+    }
+}
+
+template <int PMAX>
+static int launch_lane_many_t(int warps, const ManyJob *d_jobs, int njobs, int64_t ctas, size_t smem,
+                              cudaStream_t st) {
+    int dev = 0;
+    PPS_CUDA_TRY(cudaGetDevice(&dev));
+    static bool attr_set[64] = {};
+    if (dev < 64 && !attr_set[dev]) {
+        PPS_CUDA_TRY(cudaFuncSetAttribute(k_eval_lane_mbz_many<PMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)kLaneSmemLimit));
+        attr_set[dev] = true;
+    }
+    k_eval_lane_mbz_many<PMAX><<<(unsigned)ctas, warps * 32, smem, st>>>(d_jobs, njobs);
+    PPS_CUDA_TRY(cudaGetLastError());
+    return PP_OK;
+}
+
+int launch_lane_mbz_many(int pmax, int warps, const ManyJob *d_jobs, int njobs, int64_t ctas, size_t smem,
+                         cudaStream_t st) {
+    if (njobs <= 0 || ctas <= 0) return PP_OK;
+    if (ctas > 0x7FFFFFFF || smem > kLaneSmemLimit || warps < 1 || warps > kManyLaneWarps) return PP_ERR_SIZE;
+    switch (pmax) {
+        case 4: return launch_lane_many_t<4>(warps, d_jobs, njobs, ctas, smem, st);
+        case 8: return launch_lane_many_t<8>(warps, d_jobs, njobs, ctas, smem, st);
+        case 16: return launch_lane_many_t<16>(warps, d_jobs, njobs, ctas, smem, st);
         default: return PP_ERR_INTERNAL;
     }
 }

@@ -386,9 +386,11 @@ __global__ void __maxnreg__(PMAX == 16 ? 168 : 96) k_eval_reg(const EvalArgs a) 
 // (alternating A and B, all-F, all-B), in the same [device][lane] layout the
 // round bodies read; a round that follows no pattern gets its slice from its
 // kind word.  No cost ring, no loader, no waits.
+// The body takes the CTA's index within its problem (`bid`), so the fused
+// kernel over many problems runs it too.
 template <int PMAX, bool OPS>
-__global__ void __launch_bounds__(128) k_eval_reg_mbz(const EvalArgs a) {
-    copy_peak(a);
+__device__ __forceinline__ void reg_mbz_body(const EvalArgs &a, int64_t bid) {
+    copy_peak(a, bid);
     constexpr int kSl = PMAX * 32;  // words per slice
     extern __shared__ __align__(16) int32_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -401,7 +403,7 @@ __global__ void __launch_bounds__(128) k_eval_reg_mbz(const EvalArgs a) {
     const uint4 *segs = reinterpret_cast<const uint4 *>(smem + tw + 2 * ((a.R + 1) & ~1));
     int32_t *sl_alt_a = smem + a.ktab_words + warp * 5 * kSl;
     int32_t *sl_alt_b = sl_alt_a + kSl, *sl_f = sl_alt_b + kSl, *sl_b = sl_f + kSl, *sl_gen = sl_b + kSl;
-    const int64_t inst0 = a.inst_begin + ((int64_t)blockIdx.x * nwarps + warp) * 32;
+    const int64_t inst0 = a.inst_begin + (bid * nwarps + warp) * 32;
     Lanes<1> L;
     L.lane = lane;
     L.x[0] = inst0 + lane;
@@ -488,6 +490,19 @@ __global__ void __launch_bounds__(128) k_eval_reg_mbz(const EvalArgs a) {
     }
     __syncwarp();  // the slices are free: stage the idle block through them
     write_results_warp<PMAX>(a, inst0, lane, S.fr[0], S.busy[0], S.flag[0], (negc >> 31) != 0, sl_alt_a);
+}
+
+template <int PMAX, bool OPS>
+__global__ void __launch_bounds__(128) k_eval_reg_mbz(const EvalArgs a) {
+    reg_mbz_body<PMAX, OPS>(a, blockIdx.x);
+}
+
+// Many problems in one launch: CTA c runs CTA c - block_begin of its problem.
+template <int PMAX>
+__global__ void __launch_bounds__(128) k_eval_reg_mbz_many(const ManyJob *jobs, int njobs) {
+    const int j = many_job_of(jobs, njobs, blockIdx.x);
+    const EvalArgs &a = jobs[j].a;  // read in place: uniform per CTA, cached
+    reg_mbz_body<PMAX, false>(a, (int64_t)blockIdx.x - jobs[j].block_begin);
 }
 
 template <int PMAX, bool OPS>
@@ -653,9 +668,99 @@ int launch_eval_reg_tables(int pmax, const EvalArgs &a, bool vec, bool ops, cuda
     }
 }
 
+// The fused register path over many problems: GPipe / 1F1B plans whose costs
+// are the same for every microbatch (stride_mb == 0), without per-op output;
+// the conditions of the single-problem microbatch-shared path.
+bool reg_mbz_job(pp_plan *plan, EvalArgs &a, cudaStream_t st, int *rc) {
+    *rc = PP_OK;
+    if (!plan->reg_ok || a.comm_b || a.op_start || a.op_end || a.s_mb != 0 || a.n <= 0) return false;
+    if (ktab_words(a.R, plan->pmax, a.nseg) > kMaxLtWords || (int64_t)(a.S - 1) * a.s_stage >= ((int64_t)1 << 30))
+        return false;
+    const pp_ktab *t = nullptr;
+    *rc = kernel_tables(plan, a.s_stage, a.s_mb, st, &t);
+    if (*rc) return false;
+    a.ktab = t->d;
+    a.ktab_words = t->words;
+    return true;
+}
+
+int64_t reg_mbz_warps(const EvalArgs &a) { return (a.n + 31) / 32; }
+
+int64_t reg_mbz_ctas(const EvalArgs &a, int warps) { return (reg_mbz_warps(a) + warps - 1) / warps; }
+
+size_t reg_mbz_smem(int pmax, const EvalArgs &a, int warps) {
+    return (size_t)a.ktab_words * sizeof(uint32_t) + (size_t)warps * 5 * pmax * 32 * sizeof(int32_t);
+}
+
+template <int PMAX>
+static int launch_mbz_many_t(int warps, const ManyJob *d_jobs, int njobs, int64_t ctas, size_t smem,
+                             cudaStream_t st) {
+    int dev = 0;
+    PPS_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev >= 64) return PP_ERR_INTERNAL;
+    static int optin[64] = {};
+    if (!optin[dev]) {
+        int o = 0;
+        PPS_CUDA_TRY(cudaDeviceGetAttribute(&o, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+        PPS_CUDA_TRY(cudaFuncSetAttribute(k_eval_reg_mbz_many<PMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, o));
+        optin[dev] = o;
+    }
+    if (smem > (size_t)optin[dev]) return PP_ERR_SIZE;
+    k_eval_reg_mbz_many<PMAX><<<(unsigned)ctas, warps * 32, smem, st>>>(d_jobs, njobs);
+    PPS_CUDA_TRY(cudaGetLastError());
+    return PP_OK;
+}
+
+int launch_reg_mbz_many(int pmax, int warps, const ManyJob *d_jobs, int njobs, int64_t ctas, size_t smem,
+                        cudaStream_t st) {
+    if (njobs <= 0 || ctas <= 0) return PP_OK;
+    if (ctas > 0x7FFFFFFF || warps < 1 || warps > kManyRegWarps) return PP_ERR_SIZE;
+    switch (pmax) {
+        case 4: return launch_mbz_many_t<4>(warps, d_jobs, njobs, ctas, smem, st);
+        case 8: return launch_mbz_many_t<8>(warps, d_jobs, njobs, ctas, smem, st);
+        case 16: return launch_mbz_many_t<16>(warps, d_jobs, njobs, ctas, smem, st);
+        default: return PP_ERR_INTERNAL;
+    }
+}
+
 }  // namespace pps
 
 namespace pps {
+
+int eval_check(pp_policy_t policy, int P, int M, int v, const int32_t *cost_f, const int32_t *cost_b,
+               int64_t stride_inst, int64_t stride_stage, int64_t stride_mb, int64_t comm_stride_inst,
+               int64_t comm_stride_bnd, int64_t n_instances) {
+    const int rc = check_shape((int)policy, P, M, v);
+    if (rc) return rc;
+    if (n_instances < 0) return PP_ERR_ARG;
+    if (n_instances > 0 && (!cost_f || !cost_b)) return PP_ERR_ARG;
+    if (stride_inst < 0 || stride_stage < 0 || stride_mb < 0 || comm_stride_inst < 0 || comm_stride_bnd < 0)
+        return PP_ERR_ARG;
+    return PP_OK;
+}
+
+EvalArgs eval_args(const pp_plan *plan, const int32_t *cost_f, const int32_t *cost_b, int64_t stride_inst,
+                   int64_t stride_stage, int64_t stride_mb, const int32_t *comm, const int32_t *comm_b,
+                   int64_t comm_stride_inst, int64_t comm_stride_bnd, int64_t n_instances, int32_t *makespan,
+                   int32_t *idle, int64_t *bub_num, int64_t *bub_den, int32_t *peak, int32_t *op_start,
+                   int32_t *op_end, int64_t op_stride_inst, int64_t op_stride_op, int8_t *status) {
+    EvalArgs a{};
+    a.peak_src = plan->d_peak; a.peak_dst = peak;
+    a.desc = plan->d_desc; a.desc2 = plan->d_desc2; a.rw = plan->d_rw;
+    a.seg = plan->d_seg; a.nseg = plan->nseg;
+    a.ktab = nullptr; a.ktab_words = 0;
+    a.R = plan->R; a.P = plan->P; a.M = plan->M; a.v = plan->v; a.S = plan->S; a.O = plan->O;
+    a.nslots = plan->nslots;
+    a.cost_f = cost_f; a.cost_b = cost_b;
+    a.s_inst = stride_inst; a.s_stage = stride_stage; a.s_mb = stride_mb;
+    a.comm = comm; a.comm_b = comm_b; a.c_inst = comm_stride_inst; a.c_bnd = comm_stride_bnd;
+    a.n = n_instances;
+    a.inst_begin = 0;
+    a.makespan = makespan; a.idle = idle; a.bub_num = bub_num; a.bub_den = bub_den; a.status = status;
+    a.op_start = op_start; a.op_end = op_end; a.o_inst = op_stride_inst; a.o_op = op_stride_op;
+    return a;
+}
+
 namespace {
 
 int eval_impl(pp_policy_t policy, int P, int M, int v, const int32_t *cost_f, const int32_t *cost_b,
@@ -664,13 +769,9 @@ int eval_impl(pp_policy_t policy, int P, int M, int v, const int32_t *cost_f, co
               int32_t *makespan, int32_t *idle, int64_t *bub_num, int64_t *bub_den, int32_t *peak,
               int32_t *op_start, int32_t *op_end, int64_t op_stride_inst, int64_t op_stride_op, int8_t *status,
               cudaStream_t stream) {
-    int rc = check_shape((int)policy, P, M, v);
+    int rc = eval_check(policy, P, M, v, cost_f, cost_b, stride_inst, stride_stage, stride_mb, comm_stride_inst,
+                        comm_stride_bnd, n_instances);
     if (rc) return rc;
-    if (n_instances < 0) return PP_ERR_ARG;
-    if (n_instances > 0 && (!cost_f || !cost_b)) return PP_ERR_ARG;
-    if (stride_inst < 0 || stride_stage < 0 || stride_mb < 0 || comm_stride_inst < 0 ||
-        comm_stride_bnd < 0)
-        return PP_ERR_ARG;
     if ((op_start || op_end) && (op_stride_inst < 0 || op_stride_op < 0)) return PP_ERR_ARG;
     pp_plan *plan = nullptr;
     rc = cached_plan((int)policy, P, M, v, stream, &plan);
@@ -681,19 +782,9 @@ int eval_impl(pp_policy_t policy, int P, int M, int v, const int32_t *cost_f, co
             PPS_CUDA_TRY(cudaMemcpyAsync(peak, plan->d_peak, P * sizeof(int32_t), cudaMemcpyDeviceToDevice, stream));
         return PP_OK;
     }
-    EvalArgs a{};
-    a.peak_src = plan->d_peak; a.peak_dst = peak;
-    a.desc = plan->d_desc; a.desc2 = plan->d_desc2; a.rw = plan->d_rw;
-    a.seg = plan->d_seg; a.nseg = plan->nseg;
-    a.ktab = nullptr; a.ktab_words = 0;
-    a.R = plan->R; a.P = P; a.M = M; a.v = v; a.S = plan->S; a.O = plan->O; a.nslots = plan->nslots;
-    a.cost_f = cost_f; a.cost_b = cost_b;
-    a.s_inst = stride_inst; a.s_stage = stride_stage; a.s_mb = stride_mb;
-    a.comm = comm; a.comm_b = comm_b; a.c_inst = comm_stride_inst; a.c_bnd = comm_stride_bnd;
-    a.n = n_instances;
-    a.inst_begin = 0;
-    a.makespan = makespan; a.idle = idle; a.bub_num = bub_num; a.bub_den = bub_den; a.status = status;
-    a.op_start = op_start; a.op_end = op_end; a.o_inst = op_stride_inst; a.o_op = op_stride_op;
+    EvalArgs a = eval_args(plan, cost_f, cost_b, stride_inst, stride_stage, stride_mb, comm, comm_b,
+                           comm_stride_inst, comm_stride_bnd, n_instances, makespan, idle, bub_num, bub_den, peak,
+                           op_start, op_end, op_stride_inst, op_stride_op, status);
     const bool vec = stride_inst == 1 && (reinterpret_cast<uintptr_t>(cost_f) & 15) == 0 &&
                      (reinterpret_cast<uintptr_t>(cost_b) & 15) == 0 && stride_stage % 4 == 0 &&
                      stride_mb % 4 == 0 &&

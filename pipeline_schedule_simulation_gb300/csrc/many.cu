@@ -1,0 +1,180 @@
+// many.cu -- pp_sched_many_*: many evaluation problems, each with its own
+// shape, costs and outputs, evaluated in a few launches.
+//
+// A single problem of a few instances is one CTA walking hundreds of
+// dependent rounds: launched on its own it leaves the GPU idle.  Preparing a
+// set of problems builds every problem's plan and kernel tables once, sorts
+// the problems by the kernel that takes them (the microbatch-shared register
+// evaluator for GPipe / 1F1B, the microbatch-shared lane evaluator for
+// interleaved plans; one group per table width) and uploads one job record per
+// problem.  An evaluation is then one launch per group, in which each CTA finds
+// its problem by binary search over the jobs' first CTAs, plus one
+// pp_sched_eval per problem that no fused kernel takes.  A group's CTAs are as
+// wide as its widest problem needs (up to the single-problem kernels' width),
+// so problems of a few instances do not hold idle warps and their shared
+// memory.
+#include <algorithm>
+#include <vector>
+
+#include "eval_common.cuh"
+
+struct pp_many {
+    int device = 0;
+    pps::ManyJob *d_jobs = nullptr;  // every group's jobs, group after group
+    struct Group {
+        int kind;       // 0: register evaluator, 1: lane evaluator
+        int pmax;       // table width the group's kernel is compiled for
+        int first;      // index of the group's first job in d_jobs
+        int count;
+        int warps;      // warps per CTA: what the widest job fills, capped
+        int64_t ctas;   // CTAs of the fused launch
+        size_t smem;    // dynamic shared memory per CTA (the largest job's)
+    };
+    std::vector<Group> groups;
+    std::vector<pp_problem_t> rest;  // evaluated one by one
+};
+
+namespace pps {
+namespace {
+
+struct Pending {
+    int kind, pmax;
+    ManyJob job;
+};
+
+int prepare(const pp_problem_t *problems, int n_problems, pp_many *h, cudaStream_t stream) {
+    std::vector<Pending> jobs;
+    for (int i = 0; i < n_problems; ++i) {
+        const pp_problem_t &p = problems[i];
+        int rc = eval_check(p.policy, p.P, p.M, p.v, p.cost_f, p.cost_b, p.stride_inst, p.stride_stage, p.stride_mb,
+                            p.comm_stride_inst, p.comm_stride_bnd, p.n_instances);
+        if (rc) return rc;
+        pp_plan *plan = nullptr;
+        rc = cached_plan((int)p.policy, p.P, p.M, p.v, stream, &plan);
+        if (rc) return rc;
+        if (p.n_instances == 0) {
+            h->rest.push_back(p);
+            continue;
+        }
+        EvalArgs a = eval_args(plan, p.cost_f, p.cost_b, p.stride_inst, p.stride_stage, p.stride_mb, p.comm,
+                               nullptr, p.comm_stride_inst, p.comm_stride_bnd, p.n_instances, p.makespan, p.idle,
+                               p.bub_num, p.bub_den, p.peak, nullptr, nullptr, 0, 0, p.status);
+        if (reg_mbz_job(plan, a, stream, &rc)) {
+            jobs.push_back({0, plan->pmax, {a, nullptr, 0, 0}});
+            continue;
+        }
+        if (rc) return rc;
+        const uint4 *tab = nullptr;
+        int nblocks = 0;
+        if (lane_mbz_job(plan, a, &tab, &nblocks, stream, &rc)) {
+            jobs.push_back({1, plan->pmax, {a, tab, nblocks, 0}});
+            continue;
+        }
+        if (rc) return rc;
+        h->rest.push_back(p);
+    }
+    // groups by kernel and table width; within a group the jobs with the most
+    // rounds first, so that CTAs handed out last are short ones
+    std::stable_sort(jobs.begin(), jobs.end(), [](const Pending &x, const Pending &y) {
+        if (x.kind != y.kind) return x.kind < y.kind;
+        if (x.pmax != y.pmax) return x.pmax < y.pmax;
+        return x.job.a.R > y.job.a.R;
+    });
+    std::vector<ManyJob> flat;
+    flat.reserve(jobs.size());
+    for (size_t i = 0; i < jobs.size();) {
+        pp_many::Group g{jobs[i].kind, jobs[i].pmax, (int)i, 0, 1, 0, 0};
+        size_t end = i;
+        int64_t widest = 1;
+        for (; end < jobs.size() && jobs[end].kind == g.kind && jobs[end].pmax == g.pmax; ++end) {
+            const EvalArgs &a = jobs[end].job.a;
+            widest = std::max(widest, g.kind == 0 ? reg_mbz_warps(a) : lane_mbz_warps(g.pmax, a));
+        }
+        g.warps = (int)std::min<int64_t>(widest, g.kind == 0 ? kManyRegWarps : kManyLaneWarps);
+        for (; i < end; ++i) {
+            ManyJob j = jobs[i].job;
+            j.block_begin = g.ctas;
+            const EvalArgs &a = j.a;
+            g.ctas += g.kind == 0 ? reg_mbz_ctas(a, g.warps) : lane_mbz_ctas(g.pmax, a, g.warps);
+            g.smem = std::max(g.smem, g.kind == 0 ? reg_mbz_smem(g.pmax, a, g.warps)
+                                                  : lane_mbz_smem(g.pmax, a, g.warps));
+            flat.push_back(j);
+            ++g.count;
+        }
+        if (g.ctas > 0x7FFFFFFF) return PP_ERR_SIZE;
+        h->groups.push_back(g);
+    }
+    if (!flat.empty()) {
+        PPS_CUDA_TRY(cudaMalloc(&h->d_jobs, flat.size() * sizeof(ManyJob)));
+        PPS_CUDA_TRY(cudaMemcpyAsync(h->d_jobs, flat.data(), flat.size() * sizeof(ManyJob), cudaMemcpyHostToDevice,
+                                     stream));
+        PPS_CUDA_TRY(cudaStreamSynchronize(stream));
+    }
+    return PP_OK;
+}
+
+}  // namespace
+}  // namespace pps
+
+extern "C" int pp_sched_many_prepare(const pp_problem_t *problems, int n_problems, pp_many_t **many,
+                                     cudaStream_t stream) {
+    using namespace pps;
+    if (!many) return PP_ERR_ARG;
+    *many = nullptr;
+    if (n_problems < 0 || (n_problems > 0 && !problems)) return PP_ERR_ARG;
+    // argument errors first, before any CUDA call
+    for (int i = 0; i < n_problems; ++i) {
+        const pp_problem_t &p = problems[i];
+        const int rc = eval_check(p.policy, p.P, p.M, p.v, p.cost_f, p.cost_b, p.stride_inst, p.stride_stage,
+                                  p.stride_mb, p.comm_stride_inst, p.comm_stride_bnd, p.n_instances);
+        if (rc) return rc;
+    }
+    pp_many *h = new pp_many;
+    const cudaError_t e = cudaGetDevice(&h->device);
+    int rc = e == cudaSuccess ? PP_OK : cuda_status(e);
+    if (!rc) rc = prepare(problems, n_problems, h, stream);
+    if (rc) {
+        pp_sched_many_destroy(h);
+        return rc;
+    }
+    *many = h;
+    return PP_OK;
+}
+
+extern "C" int pp_sched_many_eval(const pp_many_t *many, cudaStream_t stream) {
+    using namespace pps;
+    if (!many) return PP_ERR_ARG;
+    int dev = 0;
+    PPS_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev != many->device) return PP_ERR_ARG;
+    for (const pp_many::Group &g : many->groups) {
+        const ManyJob *d = many->d_jobs + g.first;
+        const int rc = g.kind == 0 ? launch_reg_mbz_many(g.pmax, g.warps, d, g.count, g.ctas, g.smem, stream)
+                                   : launch_lane_mbz_many(g.pmax, g.warps, d, g.count, g.ctas, g.smem, stream);
+        if (rc) return rc;
+    }
+    for (const pp_problem_t &p : many->rest) {
+        const int rc = pp_sched_eval(p.policy, p.P, p.M, p.v, p.cost_f, p.cost_b, p.stride_inst, p.stride_stage,
+                                     p.stride_mb, p.comm, p.comm_stride_inst, p.comm_stride_bnd, p.n_instances,
+                                     p.makespan, p.idle, p.bub_num, p.bub_den, p.peak, nullptr, nullptr, 0, 0,
+                                     p.status, stream);
+        if (rc) return rc;
+    }
+    return PP_OK;
+}
+
+extern "C" int pp_sched_many_info(const pp_many_t *many, int *fused_problems, int *launches, int *other_problems) {
+    if (!many) return PP_ERR_ARG;
+    int fused = 0;
+    for (const pp_many::Group &g : many->groups) fused += g.count;
+    if (fused_problems) *fused_problems = fused;
+    if (launches) *launches = (int)many->groups.size();
+    if (other_problems) *other_problems = (int)many->rest.size();
+    return PP_OK;
+}
+
+extern "C" void pp_sched_many_destroy(pp_many_t *many) {
+    if (!many) return;
+    if (many->d_jobs) cudaFree(many->d_jobs);
+    delete many;
+}

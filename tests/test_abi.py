@@ -110,3 +110,33 @@ def test_one_past_each_limit_is_refused_without_gpu():
     assert pr(20, 4, 8, 969 - 5, 6) == B.PP_ERR_ARG   # past the last rank, C(19, 3) = 969
     assert pi(85, 16, 4, 16) == B.PP_ERR_SIZE      # C(84, 63) does not fit 64 bits
     assert pi(84, 16, 4, 8208) == B.PP_ERR_SIZE    # M*v = 32,832
+
+
+def test_many_argument_errors_without_gpu():
+    """pp_sched_many_*: argument errors are answered before any CUDA call."""
+    from pipeline_schedule_simulation_gb300 import binding as B
+    L = B.LIB
+    h = ctypes.c_void_p()
+
+    def prob(policy=B.ONEF1B, P=4, M=8, v=1, n=4, f=8, si=1):
+        return B.Problem(policy, P, M, v, f, f, si, 0, 0, None, 0, 0, n, None, None, None, None, None, None)
+
+    def prep(probs, n=None, handle=True):
+        arr = (B.Problem * max(len(probs), 1))(*probs)
+        return L.pp_sched_many_prepare(ctypes.cast(arr, ctypes.c_void_p), len(probs) if n is None else n,
+                                       ctypes.byref(h) if handle else None, None)
+    assert prep([prob()], handle=False) == B.PP_ERR_ARG
+    assert prep([prob()], n=-1) == B.PP_ERR_ARG
+    assert L.pp_sched_many_prepare(None, 3, ctypes.byref(h), None) == B.PP_ERR_ARG
+    assert prep([prob(), prob(P=0)]) == B.PP_ERR_ARG          # the second problem's P < 1
+    assert prep([prob(P=17)]) == B.PP_ERR_SIZE
+    assert prep([prob(policy=B.INTERLEAVED, P=4, M=6, v=2)]) == B.PP_ERR_DIVISIBILITY
+    assert prep([prob(f=0)]) == B.PP_ERR_ARG                  # NULL costs with n > 0
+    assert prep([prob(si=-1)]) == B.PP_ERR_ARG
+    assert prep([prob(policy=B.ZB1P)]) == B.PP_ERR_ARG        # Zero Bubble has its own entry point
+    assert not h.value                                        # no handle after an error
+    assert L.pp_sched_many_eval(None, None) == B.PP_ERR_ARG
+    assert L.pp_sched_many_info(None, None, None, None) == B.PP_ERR_ARG
+    L.pp_sched_many_destroy(None)
+    # the structure's layout: pointers and 64-bit fields on their natural boundaries
+    assert ctypes.sizeof(B.Problem) == 16 + 2 * 8 + 3 * 8 + 8 + 2 * 8 + 8 + 6 * 8
