@@ -243,10 +243,15 @@ size_t pp_sched_eval_host_workspace(int P, int M, int v, int64_t n_instances);
  *
  * pp_sched_many_eval enqueues the evaluation of every problem on `stream` (the
  * device must be the one the handle was prepared on); the results equal those
- * of pp_sched_eval on each problem.  It allocates nothing; when every problem
- * went to a fused kernel it only launches kernels, and can be captured in a
- * CUDA graph.  Evaluations of one handle that overlap on the GPU write the
- * same outputs; serialize them.
+ * of pp_sched_eval on each problem.  The fused launches run side by side on
+ * streams the library creates once per device (at the first evaluation with
+ * more than one launch: make it before any stream capture), forked from
+ * `stream` by an event and joined back into it, so the evaluation is ordered
+ * on `stream` alone; evaluations on one device enqueue one at a time.  It
+ * allocates no device memory; when every problem went to a fused kernel it
+ * only launches kernels and records events, and can be captured in a CUDA
+ * graph.  Evaluations of one handle that overlap on the GPU write the same
+ * outputs; serialize them.
  *
  * pp_sched_many_info reports how many problems were fused, in how many
  * launches, and how many are evaluated one by one.

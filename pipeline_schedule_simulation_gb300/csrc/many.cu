@@ -7,13 +7,16 @@
 // the problems by the kernel that takes them (the microbatch-shared register
 // evaluator for GPipe / 1F1B, the microbatch-shared lane evaluator for
 // interleaved plans; one group per table width) and uploads one job record per
-// problem.  An evaluation is then one launch per group, in which each CTA finds
+// problem.  An evaluation is then one launch per group (the groups side by side
+// on streams of the library, forked from the caller's stream and joined back
+// into it), in which each CTA finds
 // its problem by binary search over the jobs' first CTAs, plus one
 // pp_sched_eval per problem that no fused kernel takes.  A group's CTAs are as
 // wide as its widest problem needs (up to the single-problem kernels' width),
 // so problems of a few instances do not hold idle warps and their shared
 // memory.
 #include <algorithm>
+#include <mutex>
 #include <vector>
 
 #include "eval_common.cuh"
@@ -113,6 +116,62 @@ int prepare(const pp_problem_t *problems, int n_problems, pp_many *h, cudaStream
     return PP_OK;
 }
 
+// Per device: streams that run the groups of one evaluation side by side
+// (one group per stream), with the events that fork them from the caller's
+// stream and join them back.  Evaluations on one device enqueue under a
+// mutex, so each wait names its own evaluation's record.
+constexpr int kMaxGroups = 6;  // 2 kernels x 3 table widths
+struct Fork {
+    bool ready = false;
+    cudaStream_t s[kMaxGroups] = {};
+    cudaEvent_t start = nullptr, done[kMaxGroups] = {};
+};
+std::mutex g_fork_mu;
+Fork g_fork[64];
+
+int fork_for_device(int dev, Fork **out) {
+    if (dev < 0 || dev >= 64) return PP_ERR_INTERNAL;
+    Fork &f = g_fork[dev];
+    if (!f.ready) {
+        for (int i = 0; i < kMaxGroups; ++i) {
+            PPS_CUDA_TRY(cudaStreamCreateWithFlags(&f.s[i], cudaStreamNonBlocking));
+            PPS_CUDA_TRY(cudaEventCreateWithFlags(&f.done[i], cudaEventDisableTiming));
+        }
+        PPS_CUDA_TRY(cudaEventCreateWithFlags(&f.start, cudaEventDisableTiming));
+        f.ready = true;
+    }
+    *out = &f;
+    return PP_OK;
+}
+
+int launch_group(const pp_many &m, const pp_many::Group &g, cudaStream_t st) {
+    const ManyJob *d = m.d_jobs + g.first;
+    return g.kind == 0 ? launch_reg_mbz_many(g.pmax, g.warps, d, g.count, g.ctas, g.smem, st)
+                       : launch_lane_mbz_many(g.pmax, g.warps, d, g.count, g.ctas, g.smem, st);
+}
+
+// The fused launches: one group on `stream`, several side by side on the
+// device's group streams, forked from and joined back into `stream`.
+int launch_groups(const pp_many &m, cudaStream_t stream) {
+    const int ng = (int)m.groups.size();
+    if (ng == 0) return PP_OK;
+    if (ng == 1) return launch_group(m, m.groups[0], stream);
+    if (ng > kMaxGroups) return PP_ERR_INTERNAL;
+    std::lock_guard<std::mutex> lk(g_fork_mu);
+    Fork *f = nullptr;
+    int rc = fork_for_device(m.device, &f);
+    if (rc) return rc;
+    PPS_CUDA_TRY(cudaEventRecord(f->start, stream));
+    for (int i = 0; i < ng && !rc; ++i) {
+        PPS_CUDA_TRY(cudaStreamWaitEvent(f->s[i], f->start, 0));
+        rc = launch_group(m, m.groups[i], f->s[i]);
+        PPS_CUDA_TRY(cudaEventRecord(f->done[i], f->s[i]));
+    }
+    // joined also after an error, so that nothing is left unordered
+    for (int i = 0; i < ng; ++i) PPS_CUDA_TRY(cudaStreamWaitEvent(stream, f->done[i], 0));
+    return rc;
+}
+
 }  // namespace
 }  // namespace pps
 
@@ -147,12 +206,8 @@ extern "C" int pp_sched_many_eval(const pp_many_t *many, cudaStream_t stream) {
     int dev = 0;
     PPS_CUDA_TRY(cudaGetDevice(&dev));
     if (dev != many->device) return PP_ERR_ARG;
-    for (const pp_many::Group &g : many->groups) {
-        const ManyJob *d = many->d_jobs + g.first;
-        const int rc = g.kind == 0 ? launch_reg_mbz_many(g.pmax, g.warps, d, g.count, g.ctas, g.smem, stream)
-                                   : launch_lane_mbz_many(g.pmax, g.warps, d, g.count, g.ctas, g.smem, stream);
-        if (rc) return rc;
-    }
+    const int rc = launch_groups(*many, stream);
+    if (rc) return rc;
     for (const pp_problem_t &p : many->rest) {
         const int rc = pp_sched_eval(p.policy, p.P, p.M, p.v, p.cost_f, p.cost_b, p.stride_inst, p.stride_stage,
                                      p.stride_mb, p.comm, p.comm_stride_inst, p.comm_stride_bnd, p.n_instances,
