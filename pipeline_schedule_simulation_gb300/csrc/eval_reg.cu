@@ -27,6 +27,10 @@ namespace pps {
 // Instances per thread of the table-driven register evaluator.
 constexpr int kRegNI = PPS_REG_NI;
 
+// Words of the kernel tables in front of the round words (the loader table,
+// padded to 16 bytes); the microbatch-shared kernels skip them.
+__host__ __device__ inline int reg_mbz_table_skip(int R, int pmax) { return (R * pmax + 3) & ~3; }
+
 // Overflow and negative-cost detection.  All true ticks are >= 0.  Ticks are
 // carried as uint32 and compared unsigned, and every op ORs its start tick and
 // its cost into one sticky word; the final makespan is ORed in too.  If no cost
@@ -395,13 +399,16 @@ __device__ __forceinline__ void reg_mbz_body(const EvalArgs &a, int64_t bid) {
     extern __shared__ __align__(16) int32_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
-    for (int i = threadIdx.x; i < a.ktab_words / 4; i += blockDim.x)
-        cp_async16(smem_addr(smem + 4 * i), a.ktab + i, 16u);
+    // only the round words and segments of the kernel tables: the loader
+    // table in front of them serves per-microbatch costs
+    const int tw = reg_mbz_table_skip(a.R, PMAX);
+    const int words = a.ktab_words - tw;
+    for (int i = threadIdx.x; i < words / 4; i += blockDim.x)
+        cp_async16(smem_addr(smem + 4 * i), a.ktab + tw / 4 + i, 16u);
     cp_async_commit();
-    const int tw = (a.R * PMAX + 3) & ~3;
-    const uint64_t *rws = reinterpret_cast<const uint64_t *>(smem + tw);
-    const uint4 *segs = reinterpret_cast<const uint4 *>(smem + tw + 2 * ((a.R + 1) & ~1));
-    int32_t *sl_alt_a = smem + a.ktab_words + warp * 5 * kSl;
+    const uint64_t *rws = reinterpret_cast<const uint64_t *>(smem);
+    const uint4 *segs = reinterpret_cast<const uint4 *>(smem + 2 * ((a.R + 1) & ~1));
+    int32_t *sl_alt_a = smem + words + warp * 5 * kSl;
     int32_t *sl_alt_b = sl_alt_a + kSl, *sl_f = sl_alt_b + kSl, *sl_b = sl_f + kSl, *sl_gen = sl_b + kSl;
     const int64_t inst0 = a.inst_begin + (bid * nwarps + warp) * 32;
     Lanes<1> L;
@@ -508,7 +515,8 @@ __global__ void __launch_bounds__(128) k_eval_reg_mbz_many(const ManyJob *jobs, 
 template <int PMAX, bool OPS>
 static int launch_reg_mbz(const EvalArgs &a, cudaStream_t st) {
     constexpr int kWarps = 4;
-    const size_t smem = (size_t)a.ktab_words * sizeof(uint32_t) + (size_t)kWarps * 5 * PMAX * 32 * sizeof(int32_t);
+    const size_t smem = (size_t)(a.ktab_words - reg_mbz_table_skip(a.R, PMAX)) * sizeof(uint32_t) +
+                        (size_t)kWarps * 5 * PMAX * 32 * sizeof(int32_t);
     int dev = 0;
     PPS_CUDA_TRY(cudaGetDevice(&dev));
     static bool attr_set[64] = {};
@@ -689,7 +697,8 @@ int64_t reg_mbz_warps(const EvalArgs &a) { return (a.n + 31) / 32; }
 int64_t reg_mbz_ctas(const EvalArgs &a, int warps) { return (reg_mbz_warps(a) + warps - 1) / warps; }
 
 size_t reg_mbz_smem(int pmax, const EvalArgs &a, int warps) {
-    return (size_t)a.ktab_words * sizeof(uint32_t) + (size_t)warps * 5 * pmax * 32 * sizeof(int32_t);
+    return (size_t)(a.ktab_words - reg_mbz_table_skip(a.R, pmax)) * sizeof(uint32_t) +
+           (size_t)warps * 5 * pmax * 32 * sizeof(int32_t);
 }
 
 template <int PMAX>
