@@ -210,6 +210,28 @@ __global__ void __launch_bounds__(256) k_search(const SearchArgs a) {
                     cf[k] = (int)sf; cb[k] = (int)sb;
                 }
             }
+            if (ok && !a.all_mk) {
+                // Only the winner is wanted: skip a candidate that provably
+                // ends after the best makespan found so far.  Stage k runs its
+                // M forwards and M backwards one at a time; its first forward
+                // starts after microbatch 0 crossed stages 0..k-1 and their
+                // boundaries, and its last backward's gradient still has to
+                // cross them back, so every 1F1B makespan (costs >= 0) is at
+                // least max_k [ sum_{j<k} (f_j + b_j) + 2k comm + M (f_k + b_k) ].
+                // A candidate equal to the best is still evaluated (ties go to
+                // the lower index), so the argmin is exact.  A stage sum beyond
+                // int32 (big) makes the candidate unselectable either way.
+                int64_t pre = 0, lb = 0;
+#pragma unroll
+                for (int k = 0; k < PMAX; ++k)
+                    if (k < a.P) {
+                        const int64_t w = (int64_t)cf[k] + cb[k];
+                        lb = max(lb, pre + (int64_t)a.M * w);
+                        pre += w + 2 * (int64_t)a.comm;
+                    }
+                const unsigned long long best = *reinterpret_cast<volatile unsigned long long *>(a.key);
+                if (lb > (int64_t)(best >> 32)) ok = false;
+            }
             if (ok) {
                 SState<PMAX> S;
                 S.acc = big | (uint32_t)a.comm;

@@ -219,3 +219,27 @@ def test_interleaved_search_layer_split(orc, B):
         rs = orc.search_interleaved(p.layer_tf, p.layer_tb, p.layer_act, p.P, 2, p.M, p.comm, p.cap, p.seed,
                                     int(lo), int(lo) + 8, nthreads=8)
         assert np.array_equal(mk[lo:lo + 8], rs["all_makespan"])
+
+
+@pytest.mark.parametrize("comm", [0, 3])
+def test_pruned_search_equals_full_scoring(B, comm):
+    """Without all_makespan the searches skip candidates whose 1F1B lower
+    bound exceeds the best makespan found so far; with it they score every
+    candidate.  Both must return the same winner: the seeded 80-layer search
+    (1,048,576 candidates) and an exhaustive window of 2^26 splits."""
+    p = W.layer_split()
+    d = [to_dev(x) for x in (p.layer_tf, p.layer_tb, p.layer_act)]
+    keys = ("best_idx", "best_makespan", "best_cuts")
+    full = B.partition_search(*d, p.P, p.M, comm, p.cap, p.seed, 0, p.n_cand, all_makespan=True)
+    pruned = B.partition_search(*d, p.P, p.M, comm, p.cap, p.seed, 0, p.n_cand)
+    n = 1 << 26
+    e_full = B.partition_search_ranks(*d, p.P, p.M, comm, p.cap, 123456, n, all_makespan=True)
+    e_pruned = B.partition_search_ranks(*d, p.P, p.M, comm, p.cap, 123456, n)
+    torch.cuda.synchronize()
+    for x, y in ((full, pruned), (e_full, e_pruned)):
+        for k in keys:
+            assert torch.equal(x[k].cpu(), y[k].cpu()), k
+    mk = full["all_makespan"].cpu().numpy()
+    assert int(full["best_makespan"].item()) == mk[mk >= 0].min()
+    mk = e_full["all_makespan"].cpu().numpy()
+    assert int(e_full["best_makespan"].item()) == mk[mk >= 0].min()

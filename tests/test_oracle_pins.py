@@ -538,3 +538,36 @@ def test_pins_catch_planted_mistakes(orc, mutant):
         lib = orc.load(path)
         failed = _pin_suite(orc, lib)
     assert failed, f"mutant {mutant} ({MUTANTS[mutant]}) passed every pin"
+
+
+def test_1f1b_makespan_lower_bound(orc):
+    """The bound the GPU searches prune with, checked on the oracle: for 1F1B
+    with stage costs f_k, b_k >= 0 and latency c on every boundary, stage k
+    runs 2M ops one at a time between microbatch 0's forward arriving (after
+    sum_{j<k} f_j + k c) and the last backward leaving (sum_{j<k} b_j + k c
+    before the end), so makespan >= max_k [sum_{j<k} (f_j + b_j) + 2 k c +
+    M (f_k + b_k)].  It is exact for a single stage; a bound one microbatch
+    too large (M + 1 in place of M) fails on some instance, so the check is not
+    vacuous."""
+    rng = np.random.default_rng(77)
+    too_big_fails = False
+    for _ in range(400):
+        P = int(rng.integers(1, 9))
+        M = int(rng.integers(1, 20))
+        c = int(rng.integers(0, 4))
+        f = rng.integers(0, 30, P)
+        b = rng.integers(0, 60, P)
+        r = orc.evaluate("1f1b", P, M, 1, f[:, None], b[:, None], comm=c)
+        pre, lb = 0, 0
+        for k in range(P):
+            lb = max(lb, pre + M * (int(f[k]) + int(b[k])))
+            pre += int(f[k]) + int(b[k]) + 2 * c
+        assert r["makespan"] >= lb
+        if P == 1:
+            assert r["makespan"] == lb
+        pre, lb1 = 0, 0
+        for k in range(P):
+            lb1 = max(lb1, pre + (M + 1) * (int(f[k]) + int(b[k])))
+            pre += int(f[k]) + int(b[k]) + 2 * c
+        too_big_fails |= r["makespan"] < lb1
+    assert too_big_fails
