@@ -296,7 +296,11 @@ void pp_sched_many_destroy(pp_many_t *many);
  * latency `comm`.  A candidate is rejected when some stage's peak held
  * activations under 1F1B times its activation bytes exceeds act_cap.  The rest
  * are evaluated with M microbatches and the argmin (makespan, candidate index)
- * is returned.
+ * is returned.  When all_makespan is NULL, a candidate whose makespan provably
+ * exceeds the best found so far is not evaluated: every 1F1B makespan is at
+ * least max_k [sum_{j<k} (f_j + b_j) + 2k comm + M (f_k + b_k)] (stage k runs
+ * its 2M ops one at a time after microbatch 0 crossed the stages before it,
+ * and its last backward must cross them back); the result is the same.
  *
  * Inputs (device): layer_tf, layer_tb int32 [L]; layer_act int64 [L].
  * Outputs (device): best_idx int64 [1] (-1 if nothing is feasible),
