@@ -19,7 +19,9 @@
 // caller's best_idx word.  The scratch table is allocated on a device's first
 // call and kept (grown when a call needs more).
 #include <algorithm>
+#include <deque>
 #include <mutex>
+#include <vector>
 
 #include "eval_common.cuh"
 #include "search_common.cuh"
@@ -39,6 +41,8 @@ struct IlvArgs {
     int64_t begin;
     uint64_t ncomb;        // C(L-1, S-1)
     const uint32_t *ops;   // plan: [P][O] packed ops (kind bit 31, chunk bits 24..30)
+    const uint16_t *lvec;  // held-count vectors that can be a device's ledger maximum, [..][v]
+    const int *loff;       // device d's vectors are lvec rows loff[d] .. loff[d+1]-1
     int32_t *cf, *cb;      // scratch [S][cn]
     int8_t *flag;          // scratch [cn]: 0 feasible, 1 over the cap, 2 a stage sum out of int32
     int cn;                // stride of the scratch tables
@@ -104,8 +108,23 @@ __global__ void __launch_bounds__(256) k_ilv_cands(const IlvArgs a, int64_t chun
             a.cf[(int64_t)s * a.cn + i] = (int32_t)sf;
             a.cb[(int64_t)s * a.cn + i] = (int32_t)sb;
         }
-        // held bytes per device: + the chunk's bytes at F, - at B, running max
-        for (int d = 0; d < a.P && fl == 0; ++d) {
+        // held bytes per device: + the chunk's bytes at F, - at B, running
+        // max.  With every range's bytes >= 0 the maximum over the order is
+        // the largest dot product of the bytes with the device's held-count
+        // vectors that no other vector of its order dominates (the plan's
+        // ledger table, a few per device); otherwise walk the order.
+        bool nonneg = a.lvec != nullptr;
+        for (int s = 0; s < a.S; ++s) nonneg = nonneg && act[s] >= 0;
+        for (int d = 0; d < a.P && fl == 0 && nonneg; ++d) {
+            int64_t top = 0;
+            for (int q = a.loff[d]; q < a.loff[d + 1]; ++q) {
+                int64_t held = 0;
+                for (int c = 0; c < a.v; ++c) held += (int64_t)a.lvec[q * a.v + c] * act[c * a.P + d];
+                top = max(top, held);
+            }
+            if (top > a.cap) fl = 1;
+        }
+        for (int d = 0; d < a.P && fl == 0 && !nonneg; ++d) {
             int64_t held = 0, top = 0;
             const uint32_t *row = a.ops + (int64_t)d * a.O;
             for (int j = 0; j < a.O; ++j) {
@@ -189,6 +208,63 @@ int ilv_scratch(size_t need, void **out) {
     return PP_OK;
 }
 
+// Per shape and device: the ledger table of the plan's order.  For device d
+// it holds the held-count vectors h (h[c] = forwards minus backwards of chunk
+// c so far, the empty prefix included) that no other vector of the order
+// dominates in every component; for non-negative bytes the ledger's maximum
+// is the largest dot product of the bytes with one of them.  Built once from
+// the plan (a copy to the host and back) and kept; guarded by g_ilv_mu.
+struct LedgerTab {
+    int dev, P, M, v;
+    uint16_t *d_vec = nullptr;
+    int *d_off = nullptr;
+};
+std::deque<LedgerTab> g_ledger;
+
+int ledger_tab(const pp_plan *plan, int dev, const LedgerTab **out) {
+    for (const LedgerTab &t : g_ledger)
+        if (t.dev == dev && t.P == plan->P && t.M == plan->M && t.v == plan->v) { *out = &t; return PP_OK; }
+    const int P = plan->P, v = plan->v, O = plan->O;
+    std::vector<uint32_t> ops((size_t)P * O);
+    PPS_CUDA_TRY(cudaMemcpy(ops.data(), plan->d_ops, ops.size() * sizeof(uint32_t), cudaMemcpyDeviceToHost));
+    std::vector<uint16_t> vec;
+    std::vector<int> off(1, 0);
+    for (int d = 0; d < P; ++d) {
+        std::vector<std::vector<int>> seen(1, std::vector<int>(v, 0));
+        std::vector<int> h(v, 0);
+        for (int j = 0; j < O; ++j) {
+            const uint32_t op = ops[(size_t)d * O + j];
+            h[PP_OP_CHUNK(op)] += PP_OP_KIND(op) ? -1 : 1;
+            seen.push_back(h);
+        }
+        std::sort(seen.begin(), seen.end());
+        seen.erase(std::unique(seen.begin(), seen.end()), seen.end());
+        for (size_t x = 0; x < seen.size(); ++x) {
+            bool dominated = false;
+            for (size_t y = 0; y < seen.size() && !dominated; ++y) {
+                if (y == x) continue;
+                bool ge = true;
+                for (int c = 0; c < v && ge; ++c) ge = seen[y][c] >= seen[x][c];
+                dominated = ge;  // distinct vectors: >= everywhere means > somewhere
+            }
+            if (dominated) continue;
+            for (int c = 0; c < v; ++c) {
+                if (seen[x][c] < 0 || seen[x][c] > 0xFFFF) return PP_ERR_INTERNAL;
+                vec.push_back((uint16_t)seen[x][c]);
+            }
+        }
+        off.push_back((int)(vec.size() / v));
+    }
+    LedgerTab t{dev, P, plan->M, v};
+    PPS_CUDA_TRY(cudaMalloc(&t.d_vec, vec.size() * sizeof(uint16_t)));
+    PPS_CUDA_TRY(cudaMalloc(&t.d_off, off.size() * sizeof(int)));
+    PPS_CUDA_TRY(cudaMemcpy(t.d_vec, vec.data(), vec.size() * sizeof(uint16_t), cudaMemcpyHostToDevice));
+    PPS_CUDA_TRY(cudaMemcpy(t.d_off, off.data(), off.size() * sizeof(int), cudaMemcpyHostToDevice));
+    g_ledger.push_back(t);
+    *out = &g_ledger.back();
+    return PP_OK;
+}
+
 }  // namespace
 }  // namespace pps
 
@@ -233,10 +309,14 @@ extern "C" int pp_sched_partition_search_interleaved(const int32_t *layer_tf, co
     a.L = L; a.P = P; a.v = v; a.S = S; a.M = M; a.O = plan->O;
     a.cap = act_cap; a.seed = seed; a.begin = cand_begin; a.ncomb = ncomb;
     a.ops = plan->d_ops; a.cf = cf; a.cb = cb; a.flag = flag; a.cn = cn;
-    const size_t smem = ilv_smem(L, S);
-    static bool attr_set[64] = {};
     int dev = 0;
     PPS_CUDA_TRY(cudaGetDevice(&dev));
+    const LedgerTab *lt = nullptr;
+    rc = ledger_tab(plan, dev, &lt);
+    if (rc) return rc;
+    a.lvec = lt->d_vec; a.loff = lt->d_off;
+    const size_t smem = ilv_smem(L, S);
+    static bool attr_set[64] = {};
     if (dev < 64 && !attr_set[dev]) {
         PPS_CUDA_TRY(cudaFuncSetAttribute(k_ilv_cands, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
         PPS_CUDA_TRY(cudaFuncSetAttribute(k_ilv_finish, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
@@ -255,7 +335,10 @@ extern "C" int pp_sched_partition_search_interleaved(const int32_t *layer_tf, co
     for (int64_t c0 = 0; c0 < n_cand; c0 += cn) {
         const int nc = (int)std::min<int64_t>(cn, n_cand - c0);
         const unsigned blocks = (unsigned)((nc + 255) / 256);
-        k_ilv_cands<<<blocks, 256, smem, stream>>>(a, c0, nc);
+        // a grid-stride loop over the chunk: a few CTAs per SM, each building
+        // its binomial and prefix tables once for many candidates
+        const unsigned cand_blocks = std::min<unsigned>(blocks, (unsigned)sm_count(dev) * 4u);
+        k_ilv_cands<<<cand_blocks, 256, smem, stream>>>(a, c0, nc);
         PPS_CUDA_TRY(cudaGetLastError());
         e.n = nc;
         rc = lane_path(plan, e) ? launch_eval_lane(plan, e, true, false, stream)

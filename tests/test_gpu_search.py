@@ -243,3 +243,23 @@ def test_pruned_search_equals_full_scoring(B, comm):
     assert int(full["best_makespan"].item()) == mk[mk >= 0].min()
     mk = e_full["all_makespan"].cpu().numpy()
     assert int(e_full["best_makespan"].item()) == mk[mk >= 0].min()
+
+
+def test_interleaved_search_negative_bytes(orc, B):
+    """Layouts whose ranges include negative activation bytes take the full
+    ledger walk instead of the per-plan table of dominant held counts; mixed
+    signs and a binding cap, every makespan against the oracle."""
+    rng = np.random.default_rng(11)
+    L, P, v, M, cap = 24, 4, 2, 8, 60
+    ltf = rng.integers(1, 20, L).astype(np.int32)
+    ltb = rng.integers(1, 40, L).astype(np.int32)
+    lact = rng.integers(-3, 5, L).astype(np.int64)
+    n = 3000
+    g = B.partition_search_interleaved(to_dev(ltf), to_dev(ltb), to_dev(lact), P, v, M, 1, cap, 99, 0, n,
+                                       all_makespan=True)
+    torch.cuda.synchronize()
+    r = orc.search_interleaved(ltf, ltb, lact, P, v, M, 1, cap, 99, 0, n, nthreads=8)
+    mk = g["all_makespan"].cpu().numpy()
+    assert np.array_equal(mk, r["all_makespan"])
+    assert (mk == -1).any() and (mk >= 0).any()
+    assert int(g["best_idx"].item()) == r["best_idx"]
