@@ -32,6 +32,7 @@ struct SearchArgs {
     int64_t cap;
     uint64_t seed;
     int64_t begin, n;
+    int64_t step;          // candidate ci of a launch is call index ci * step
     uint64_t ncomb;        // C(L-1, P-1)
     int32_t peak[PP_MAX_P];
     int32_t *all_mk;
@@ -178,8 +179,8 @@ __device__ __forceinline__ int eval_1f1b(const SearchArgs &a, SState<PMAX> &S, c
 // number of splits) or, for the exhaustive search, the index itself.
 template <bool EXH>
 __device__ __forceinline__ uint64_t cand_rank(const SearchArgs &a, int64_t ci) {
-    if constexpr (EXH) return (uint64_t)(a.begin + ci);
-    return splitmix64(a.seed + (uint64_t)(a.begin + ci)) % a.ncomb;
+    if constexpr (EXH) return (uint64_t)(a.begin + ci * a.step);
+    return splitmix64(a.seed + (uint64_t)(a.begin + ci * a.step)) % a.ncomb;
 }
 
 template <int PMAX, bool EXH>
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(256) k_search(const SearchArgs a) {
             if (a.all_mk) a.all_mk[ci] = mk;
         }
         unsigned long long key = ~0ull;
-        if (live && mk >= 0) key = ((unsigned long long)(uint32_t)mk << 32) | (uint32_t)ci;
+        if (live && mk >= 0) key = ((unsigned long long)(uint32_t)mk << 32) | (uint32_t)(ci * a.step);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
@@ -285,6 +286,19 @@ int run_search(SearchArgs &a, int64_t *best_idx, int32_t *best_mk, int32_t *best
     int64_t grid = (int64_t)sms * per_sm;
     if (want < grid) grid = want;
     if (grid < 1) grid = 1;
+    // Only the winner wanted from an exhaustive range: first score every
+    // kProbe-th split, so that the main pass prunes against a near-best
+    // makespan from its start (colex order puts the balanced splits far into
+    // the range).  Both passes reduce into the same word; the probe's splits
+    // are scored again by the main pass, so the result is unchanged.
+    constexpr int64_t kProbe = 1024;
+    if (EXH && !a.all_mk && a.n >= 64 * kProbe) {
+        SearchArgs pa = a;
+        pa.step = kProbe;
+        pa.n = (a.n + kProbe - 1) / kProbe;
+        const int64_t pgrid = std::min<int64_t>((int64_t)sms * per_sm, (pa.n + 255) / 256);
+        k_search<PMAX, EXH><<<(unsigned)pgrid, 256, 0, st>>>(pa);
+    }
     if (a.n > 0) k_search<PMAX, EXH><<<(unsigned)grid, 256, 0, st>>>(a);
     k_search_finish<PMAX, EXH><<<1, 64, 0, st>>>(a, best_idx, best_mk, best_cuts);
     PPS_CUDA_TRY(cudaGetLastError());
@@ -316,7 +330,7 @@ int search_entry(const int32_t *layer_tf, const int32_t *layer_tb, const int64_t
     SearchArgs a;
     a.rw = plan->d_rw; a.seg = plan->d_seg; a.nseg = plan->nseg; a.R = plan->R; a.P = P; a.M = M; a.L = L;
     a.ltf = layer_tf; a.ltb = layer_tb; a.lact = layer_act;
-    a.comm = comm; a.cap = act_cap; a.seed = seed; a.begin = begin; a.n = n; a.ncomb = ncomb;
+    a.comm = comm; a.cap = act_cap; a.seed = seed; a.begin = begin; a.n = n; a.ncomb = ncomb; a.step = 1;
     for (int k = 0; k < PP_MAX_P; ++k) a.peak[k] = k < P ? plan->h_peak[k] : 0;
     a.all_mk = all_makespan;
     a.key = reinterpret_cast<unsigned long long *>(best_idx);
