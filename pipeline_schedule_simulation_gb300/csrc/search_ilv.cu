@@ -44,7 +44,12 @@ struct IlvArgs {
     const uint16_t *lvec;  // held-count vectors that can be a device's ledger maximum, [..][v]
     const int *loff;       // device d's vectors are lvec rows loff[d] .. loff[d+1]-1
     int32_t *cf, *cb;      // scratch [S][cn]
-    int8_t *flag;          // scratch [cn]: 0 feasible, 1 over the cap, 2 a stage sum out of int32
+    int8_t *flag;          // scratch [cn]: kIlvScored, kIlvOverCap, kIlvBig or kIlvBound
+    int *slot;             // scratch [cn]: the candidate's column in cf / cb, -1 if not scored
+    int *count;            // columns handed out in this chunk
+    const unsigned long long *key;  // the call's reduction word (best so far)
+    int32_t comm;
+    bool prune;            // only the winner is wanted: skip candidates by the makespan bound
     int cn;                // stride of the scratch tables
 };
 
@@ -91,56 +96,107 @@ __device__ void ilv_unrank(const IlvArgs &a, const IlvTables &t, uint64_t r, int
     first[a.S] = a.L;
 }
 
+// Flags of a chunk candidate: 0 scored, 1 over the byte cap, 2 a stage sum
+// out of int32, 3 skipped by the makespan bound (only when the winner alone
+// is wanted).  Only flag-0 candidates are written to the scratch table, packed
+// in the order a warp-aggregated counter hands out columns; slot[i] is chunk
+// candidate i's column.
+constexpr int8_t kIlvScored = 0, kIlvOverCap = 1, kIlvBig = 2, kIlvBound = 3;
+
 __global__ void __launch_bounds__(256) k_ilv_cands(const IlvArgs a, int64_t chunk0, int nchunk) {
     extern __shared__ __align__(16) unsigned char ilv_sm[];
     const IlvTables t = ilv_tables(a, ilv_sm);
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nchunk; i += gridDim.x * blockDim.x) {
+    const int lane = threadIdx.x & 31;
+    for (int base = blockIdx.x * blockDim.x; base < nchunk; base += gridDim.x * blockDim.x) {
+        const int i = base + threadIdx.x;
+        const bool live = i < nchunk;
         int first[PP_MAX_S + 1];
-        int64_t act[PP_MAX_S];
-        const uint64_t r = splitmix64(a.seed + (uint64_t)(a.begin + chunk0 + i)) % a.ncomb;
-        ilv_unrank(a, t, r, first);
-        int8_t fl = 0;
-        for (int s = 0; s < a.S; ++s) {
-            const int64_t sf = t.pre_tf[first[s + 1]] - t.pre_tf[first[s]];
-            const int64_t sb = t.pre_tb[first[s + 1]] - t.pre_tb[first[s]];
-            act[s] = t.pre_act[first[s + 1]] - t.pre_act[first[s]];
-            if (sf < 0 || sb < 0 || sf > 0x7FFFFFFF || sb > 0x7FFFFFFF) fl = 2;
-            a.cf[(int64_t)s * a.cn + i] = (int32_t)sf;
-            a.cb[(int64_t)s * a.cn + i] = (int32_t)sb;
-        }
-        // held bytes per device: + the chunk's bytes at F, - at B, running
-        // max.  With every range's bytes >= 0 the maximum over the order is
-        // the largest dot product of the bytes with the device's held-count
-        // vectors that no other vector of its order dominates (the plan's
-        // ledger table, a few per device); otherwise walk the order.
-        bool nonneg = a.lvec != nullptr;
-        for (int s = 0; s < a.S; ++s) nonneg = nonneg && act[s] >= 0;
-        for (int d = 0; d < a.P && fl == 0 && nonneg; ++d) {
-            int64_t top = 0;
-            for (int q = a.loff[d]; q < a.loff[d + 1]; ++q) {
-                int64_t held = 0;
-                for (int c = 0; c < a.v; ++c) held += (int64_t)a.lvec[q * a.v + c] * act[c * a.P + d];
-                top = max(top, held);
+        int8_t fl = kIlvBig;
+        if (live) {
+            int64_t act[PP_MAX_S];
+            const uint64_t r = splitmix64(a.seed + (uint64_t)(a.begin + chunk0 + i)) % a.ncomb;
+            ilv_unrank(a, t, r, first);
+            fl = kIlvScored;
+            for (int s = 0; s < a.S; ++s) {
+                const int64_t sf = t.pre_tf[first[s + 1]] - t.pre_tf[first[s]];
+                const int64_t sb = t.pre_tb[first[s + 1]] - t.pre_tb[first[s]];
+                act[s] = t.pre_act[first[s + 1]] - t.pre_act[first[s]];
+                if (sf < 0 || sb < 0 || sf > 0x7FFFFFFF || sb > 0x7FFFFFFF) fl = kIlvBig;
             }
-            if (top > a.cap) fl = 1;
-        }
-        for (int d = 0; d < a.P && fl == 0 && !nonneg; ++d) {
-            int64_t held = 0, top = 0;
-            const uint32_t *row = a.ops + (int64_t)d * a.O;
-            for (int j = 0; j < a.O; ++j) {
-                const uint32_t op = __ldg(row + j);
-                const int64_t b = act[((op >> 24) & 0x7Fu) * a.P + d];
-                held += (op >> 31) ? -b : b;
-                top = max(top, held);
+            // held bytes per device: + the chunk's bytes at F, - at B, running
+            // max.  With every range's bytes >= 0 the maximum over the order is
+            // the largest dot product of the bytes with the device's held-count
+            // vectors that no other vector of its order dominates (the plan's
+            // ledger table, a few per device); otherwise walk the order.
+            bool nonneg = a.lvec != nullptr;
+            for (int s = 0; s < a.S; ++s) nonneg = nonneg && act[s] >= 0;
+            for (int d = 0; d < a.P && fl == kIlvScored && nonneg; ++d) {
+                int64_t top = 0;
+                for (int q = a.loff[d]; q < a.loff[d + 1]; ++q) {
+                    int64_t held = 0;
+                    for (int c = 0; c < a.v; ++c) held += (int64_t)a.lvec[q * a.v + c] * act[c * a.P + d];
+                    top = max(top, held);
+                }
+                if (top > a.cap) fl = kIlvOverCap;
             }
-            if (top > a.cap) fl = 1;
+            for (int d = 0; d < a.P && fl == kIlvScored && !nonneg; ++d) {
+                int64_t held = 0, top = 0;
+                const uint32_t *row = a.ops + (int64_t)d * a.O;
+                for (int j = 0; j < a.O; ++j) {
+                    const uint32_t op = __ldg(row + j);
+                    const int64_t b = act[((op >> 24) & 0x7Fu) * a.P + d];
+                    held += (op >> 31) ? -b : b;
+                    top = max(top, held);
+                }
+                if (top > a.cap) fl = kIlvOverCap;
+            }
+            if (fl == kIlvScored && a.prune) {
+                // Only the winner is wanted: with M a multiple of P, device d
+                // starts with microbatch 0's forward of virtual stage d (after
+                // the stages before it and their boundaries), ends with the
+                // backward of virtual stage d for microbatch M-1 (whose gradient
+                // still crosses them back) and runs its 2Mv ops one at a time,
+                // so the makespan is at least
+                //   max_d [sum_{s<d} (f_s + b_s) + 2 d comm + M sum_chunks (f + b)].
+                // A candidate above the best makespan of the chunks already
+                // scored cannot win (ties are still scored).
+                int64_t lb = 0, pre = 0;
+                for (int d = 0; d < a.P; ++d) {
+                    int64_t busy = 0;
+                    for (int c = 0; c < a.v; ++c) {
+                        const int s = c * a.P + d;
+                        busy += (t.pre_tf[first[s + 1]] - t.pre_tf[first[s]]) +
+                                (t.pre_tb[first[s + 1]] - t.pre_tb[first[s]]);
+                    }
+                    lb = max(lb, pre + 2 * (int64_t)d * a.comm + (int64_t)a.M * busy);
+                    pre += (t.pre_tf[first[d + 1]] - t.pre_tf[first[d]]) + (t.pre_tb[first[d + 1]] - t.pre_tb[first[d]]);
+                }
+                const unsigned long long best = *reinterpret_cast<volatile const unsigned long long *>(a.key);
+                if (lb > (int64_t)(best >> 32)) fl = kIlvBound;
+            }
+        }
+        // columns for the candidates to score, one atomic per warp
+        const bool keep = live && fl == kIlvScored;
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, keep);
+        int col0 = 0;
+        if (lane == 0 && m) col0 = atomicAdd(a.count, __popc(m));
+        col0 = __shfl_sync(0xFFFFFFFFu, col0, 0);
+        if (!live) continue;
+        int col = -1;
+        if (keep) {
+            col = col0 + __popc(m & ((1u << lane) - 1u));
+            for (int s = 0; s < a.S; ++s) {
+                a.cf[(int64_t)s * a.cn + col] = (int32_t)(t.pre_tf[first[s + 1]] - t.pre_tf[first[s]]);
+                a.cb[(int64_t)s * a.cn + col] = (int32_t)(t.pre_tb[first[s + 1]] - t.pre_tb[first[s]]);
+            }
         }
         a.flag[i] = fl;
+        a.slot[i] = col;
     }
 }
 
 __global__ void __launch_bounds__(256) k_ilv_select(const int32_t *mk, const int8_t *status, const int8_t *flag,
-                                                    int nchunk, int64_t chunk0, int32_t *all_mk,
+                                                    const int *slot, int nchunk, int64_t chunk0, int32_t *all_mk,
                                                     unsigned long long *key) {
     const int lane = threadIdx.x & 31;
     for (int base = blockIdx.x * blockDim.x; base < nchunk; base += gridDim.x * blockDim.x) {
@@ -148,7 +204,9 @@ __global__ void __launch_bounds__(256) k_ilv_select(const int32_t *mk, const int
         int m = -1;
         if (i < nchunk) {
             const int8_t f = flag[i];
-            m = f == 1 ? -1 : ((f == 2 || status[i] != PP_ST_OK) ? -2 : mk[i]);
+            if (f == kIlvOverCap || f == kIlvBound) m = -1;
+            else if (f == kIlvBig) m = -2;
+            else m = status[slot[i]] != PP_ST_OK ? -2 : mk[slot[i]];
             if (all_mk) all_mk[chunk0 + i] = m;
         }
         unsigned long long k = ~0ull;
@@ -292,7 +350,7 @@ extern "C" int pp_sched_partition_search_interleaved(const int32_t *layer_tf, co
     std::lock_guard<std::mutex> lk(g_ilv_mu);
     const int cn = (int)std::min<int64_t>(kChunk, std::max<int64_t>(32, (n_cand + 31) / 32 * 32));
     const size_t cost_bytes = (size_t)S * cn * sizeof(int32_t);
-    const size_t need = 2 * cost_bytes + (size_t)cn * (sizeof(int32_t) + 2) + 256;
+    const size_t need = 2 * cost_bytes + (size_t)cn * (2 * sizeof(int32_t) + 2) + 512;
     void *scratch = nullptr;
     rc = ilv_scratch(need, &scratch);
     if (rc) return rc;
@@ -303,12 +361,15 @@ extern "C" int pp_sched_partition_search_interleaved(const int32_t *layer_tf, co
     int32_t *dcomm = mk + cn;  // one word, broadcast to every instance and boundary
     int8_t *st = reinterpret_cast<int8_t *>(dcomm + 4);
     int8_t *flag = st + cn;
+    int *slot = reinterpret_cast<int *>((reinterpret_cast<uintptr_t>(flag + cn) + 255) & ~(uintptr_t)255);
+    int *count = slot + cn;
 
     IlvArgs a;
     a.ltf = layer_tf; a.ltb = layer_tb; a.lact = layer_act;
     a.L = L; a.P = P; a.v = v; a.S = S; a.M = M; a.O = plan->O;
     a.cap = act_cap; a.seed = seed; a.begin = cand_begin; a.ncomb = ncomb;
     a.ops = plan->d_ops; a.cf = cf; a.cb = cb; a.flag = flag; a.cn = cn;
+    a.slot = slot; a.count = count; a.comm = comm; a.prune = all_makespan == nullptr;
     int dev = 0;
     PPS_CUDA_TRY(cudaGetDevice(&dev));
     const LedgerTab *lt = nullptr;
@@ -323,6 +384,7 @@ extern "C" int pp_sched_partition_search_interleaved(const int32_t *layer_tf, co
         attr_set[dev] = true;
     }
     unsigned long long *key = reinterpret_cast<unsigned long long *>(best_idx);
+    a.key = key;
     PPS_CUDA_TRY(cudaMemsetAsync(best_idx, 0xFF, sizeof(int64_t), stream));
     PPS_CUDA_TRY(cudaMemcpyAsync(dcomm, &comm, sizeof(int32_t), cudaMemcpyHostToDevice, stream));
 
@@ -338,13 +400,20 @@ extern "C" int pp_sched_partition_search_interleaved(const int32_t *layer_tf, co
         // a grid-stride loop over the chunk: a few CTAs per SM, each building
         // its binomial and prefix tables once for many candidates
         const unsigned cand_blocks = std::min<unsigned>(blocks, (unsigned)sm_count(dev) * 4u);
+        PPS_CUDA_TRY(cudaMemsetAsync(count, 0, sizeof(int), stream));
         k_ilv_cands<<<cand_blocks, 256, smem, stream>>>(a, c0, nc);
         PPS_CUDA_TRY(cudaGetLastError());
-        e.n = nc;
-        rc = lane_path(plan, e) ? launch_eval_lane(plan, e, true, false, stream)
-                                : launch_eval_slot(plan, e, true, false, stream);
-        if (rc) return rc;
-        k_ilv_select<<<blocks, 256, 0, stream>>>(mk, st, flag, nc, c0, all_makespan, key);
+        // only the packed candidates that passed the cap (and the bound) are scored
+        int scored = 0;
+        PPS_CUDA_TRY(cudaMemcpyAsync(&scored, count, sizeof(int), cudaMemcpyDeviceToHost, stream));
+        PPS_CUDA_TRY(cudaStreamSynchronize(stream));
+        if (scored > 0) {
+            e.n = scored;
+            rc = lane_path(plan, e) ? launch_eval_lane(plan, e, true, false, stream)
+                                    : launch_eval_slot(plan, e, true, false, stream);
+            if (rc) return rc;
+        }
+        k_ilv_select<<<blocks, 256, 0, stream>>>(mk, st, flag, slot, nc, c0, all_makespan, key);
         PPS_CUDA_TRY(cudaGetLastError());
     }
     k_ilv_finish<<<1, 64, smem, stream>>>(a, key, best_idx, best_makespan, best_cuts);

@@ -263,3 +263,21 @@ def test_interleaved_search_negative_bytes(orc, B):
     assert np.array_equal(mk, r["all_makespan"])
     assert (mk == -1).any() and (mk >= 0).any()
     assert int(g["best_idx"].item()) == r["best_idx"]
+
+
+@pytest.mark.parametrize("comm", [0, 3])
+def test_pruned_interleaved_search_equals_full_scoring(B, comm):
+    """Without all_makespan the interleaved search skips, from its second
+    chunk of 262,144 candidates on, layouts whose interleaved makespan bound
+    exceeds the best so far; with it every layout within the cap is scored.
+    The same winner either way (1,048,576 layouts of the 80-layer model)."""
+    p = W.layer_split()
+    d = [to_dev(x) for x in (p.layer_tf, p.layer_tb, p.layer_act)]
+    args = (*d, p.P, 2, p.M, comm, p.cap, p.seed, 0, 1 << 20)
+    full = B.partition_search_interleaved(*args, all_makespan=True)
+    pruned = B.partition_search_interleaved(*args)
+    torch.cuda.synchronize()
+    for k in ("best_idx", "best_makespan", "best_cuts"):
+        assert torch.equal(full[k].cpu(), pruned[k].cpu()), k
+    mk = full["all_makespan"].cpu().numpy()
+    assert int(full["best_makespan"].item()) == mk[mk >= 0].min()

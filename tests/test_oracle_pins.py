@@ -571,3 +571,34 @@ def test_1f1b_makespan_lower_bound(orc):
             pre += int(f[k]) + int(b[k]) + 2 * c
         too_big_fails |= r["makespan"] < lb1
     assert too_big_fails
+
+
+def test_interleaved_makespan_lower_bound(orc):
+    """The bound the interleaved search prunes with, checked on the oracle:
+    with M a multiple of P, device d's first op is microbatch 0's forward of
+    its chunk 0 (virtual stage d) and its last op the backward of chunk 0 for
+    microbatch M - 1, and it runs all 2 M v of its ops one at a time, so
+    makespan >= max_d [sum_{s<d} (f_s + b_s) + 2 d c + M sum_chunks (f + b)]
+    (virtual stage s = chunk * P + d).  A bound one microbatch too large fails
+    somewhere."""
+    rng = np.random.default_rng(78)
+    too_big_fails = False
+    for _ in range(300):
+        P = int(rng.integers(1, 6))
+        v = int(rng.integers(2, 4))
+        M = P * int(rng.integers(1, 4))
+        c = int(rng.integers(0, 4))
+        f = rng.integers(0, 30, P * v)
+        b = rng.integers(0, 60, P * v)
+        r = orc.evaluate("interleaved", P, M, v, f[:, None], b[:, None], comm=c)
+        for extra, check in ((0, True), (1, False)):
+            lb, pre = 0, 0
+            for d in range(P):
+                busy = sum(int(f[ch * P + d]) + int(b[ch * P + d]) for ch in range(v))
+                lb = max(lb, pre + 2 * d * c + (M + extra) * busy)
+                pre += int(f[d]) + int(b[d])
+            if check:
+                assert r["makespan"] >= lb
+            else:
+                too_big_fails |= r["makespan"] < lb
+    assert too_big_fails
