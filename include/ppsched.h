@@ -351,7 +351,13 @@ int pp_sched_partition_search_ranks(const int32_t *layer_tf, const int32_t *laye
  * scratch cost table the library allocates on a device's first call (about
  * 2 MB per virtual stage) and keeps; calls on one device share it, so calls
  * that overlap on the GPU must be serialized.  The first call for a shape also
- * builds its plan.
+ * builds its plan and a small table of its held-count vectors.  Only layouts
+ * within the cap are evaluated, packed into the table; the call synchronizes
+ * `stream` once per chunk to read how many there are.  When all_makespan is
+ * NULL, a layout is not evaluated either when its makespan provably exceeds
+ * the best of the chunks already scored (device d starts with microbatch 0's
+ * forward of virtual stage d, ends with the backward of virtual stage d for
+ * microbatch M-1 and runs its 2Mv ops one at a time); the result is the same.
  * Limits: v >= 2, P*v <= PP_MAX_S, M % P == 0, M*v <= PP_MAX_MV, S <= L <= 256,
  * n_cand < 2^32, and C(L-1, S-1) below 2^64 - 1 (e.g. L <= 84 at S = 64);
  * PP_ERR_SIZE otherwise.
