@@ -7,14 +7,13 @@
 // the problems by the kernel that takes them (the microbatch-shared register
 // evaluator for GPipe / 1F1B, the microbatch-shared lane evaluator for
 // interleaved plans; one group per table width) and uploads one job record per
-// problem.  An evaluation is then one launch per group (the groups side by side
-// on streams of the library, forked from the caller's stream and joined back
-// into it), in which each CTA finds
-// its problem by binary search over the jobs' first CTAs, plus one
-// pp_sched_eval per problem that no fused kernel takes.  A group's CTAs are as
-// wide as its widest problem needs (up to the single-problem kernels' width),
-// so problems of a few instances do not hold idle warps and their shared
-// memory.
+// problem.  An evaluation is then one launch per group, the groups side by
+// side on streams of the library (forked from the caller's stream and joined
+// back into it); each CTA finds its problem by binary search over the jobs'
+// first CTAs.  Problems that no fused kernel takes get one pp_sched_eval each.
+// A group's CTAs are as wide as its widest problem needs (up to the
+// single-problem kernels' width), so problems of a few instances do not hold
+// idle warps and their shared memory.
 #include <algorithm>
 #include <mutex>
 #include <vector>
