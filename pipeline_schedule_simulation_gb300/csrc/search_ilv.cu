@@ -11,11 +11,14 @@
 // above the cap, and otherwise scored by its interleaved 1F1B makespan.
 //
 // The candidates of a call are processed in chunks of up to kChunk: one
-// kernel draws each candidate's split, writes its virtual stages' costs into a
-// scratch cost table laid out [S][chunk] (the evaluator's instance-minor
-// layout, costs the same for every microbatch) and runs the byte ledger; the
-// interleaved evaluator scores the chunk; a third kernel combines the results
-// and reduces (makespan, candidate) with one 64-bit atomicMin per warp into the
+// kernel draws each candidate's split, checks the byte ledger (from the
+// shape's table of dominant held-count vectors) and, when only the winner is
+// wanted, a makespan lower bound against the best of the chunks already
+// scored; the candidates left are packed into a scratch cost table laid out
+// [S][column] (the evaluator's instance-minor layout, costs the same for every
+// microbatch); the host reads how many there are and the interleaved evaluator
+// scores them; a third kernel maps the results back to the candidates and
+// reduces (makespan, candidate) with one 64-bit atomicMin per warp into the
 // caller's best_idx word.  The scratch table is allocated on a device's first
 // call and kept (grown when a call needs more).
 #include <algorithm>
