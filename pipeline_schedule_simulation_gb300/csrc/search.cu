@@ -11,7 +11,10 @@
 // (stage costs are constant over microbatches, so they live in registers).
 // The best (makespan, candidate) pair is reduced with warp shuffles and one
 // 64-bit atomicMin per warp into the caller's best_idx word, which a one-thread
-// kernel then turns into the index, makespan and cut positions.
+// kernel then turns into the index, makespan and cut positions.  When only the
+// winner is wanted, a candidate whose 1F1B makespan lower bound exceeds the
+// word's current best is not evaluated, and an exhaustive range first scores
+// every kProbe-th split so that the bound is tight from the start.
 #include "internal.cuh"
 #include "search_common.cuh"
 
