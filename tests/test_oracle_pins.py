@@ -602,3 +602,31 @@ def test_interleaved_makespan_lower_bound(orc):
             else:
                 too_big_fails |= r["makespan"] < lb
     assert too_big_fails
+
+
+def test_interleaved_ledger_peak_from_dominant_counts(orc):
+    """The identity the interleaved search's byte cap relies on, checked on the
+    oracle's orders: for non-negative chunk bytes, the peak of the ledger (+ a
+    chunk's bytes at its F, - at its B, [1F1B] §4.1 weighted) over a device's
+    order equals the largest dot product of the bytes with the held-count
+    vectors of the order that no other vector dominates; with a negative byte
+    count it may not, which is why the search walks the order then."""
+    rng = np.random.default_rng(79)
+    differs = False
+    for P, M, v in ((2, 4, 2), (3, 6, 3), (4, 8, 2), (8, 16, 4), (5, 10, 2)):
+        kind, chunk, mb = orc.order("interleaved", P, M, v)
+        for d in range(P):
+            h = np.zeros(v, np.int64)
+            path = [h.copy()]
+            for j in range(kind.shape[1]):
+                h[chunk[d, j]] += 1 if kind[d, j] == 0 else -1
+                path.append(h.copy())
+            vecs = np.unique(np.array(path), axis=0)
+            dom = np.array([x for x in vecs if not any((y >= x).all() and (y != x).any() for y in vecs)])
+            for _ in range(40):
+                act = rng.integers(0, 1000, v)
+                walk = max(int(p @ act) for p in path)
+                assert walk == max(int(x @ act) for x in dom)
+                neg = rng.integers(-1000, 1000, v)
+                differs |= max(int(p @ neg) for p in path) != max(int(x @ neg) for x in dom)
+    assert differs
