@@ -132,6 +132,9 @@ int orc_order(int policy, int P, int M, int v, int k, int *kind, int *chunk, int
         if (M % P != 0) return -ORC_ERR_DIVISIBILITY;
         int total = M * v;
         int w = 2 * (P - k - 1) + (v - 1) * P;
+#if ORC_MUTANT == 13  /* mistake: one forward too many in the interleaved warmup */
+        w += 1;
+#endif
         if (w > total) w = total;
         int group = P * v;
         /* forward virtual index j */

@@ -170,6 +170,41 @@ def test_interleaved_placement(orc):
                 assert sorted(mb[k][sel]) == list(range(M))
 
 
+def test_interleaved_warmup_from_first_gradient(orc):
+    """The interleaved order's warmup (reading R4), pinned by the timing it is
+    built for.  The pages name Megatron's interleaved schedule ("2. 1F1B" §6.1,
+    M040 §06) but print neither its order nor its warmup count; the reading
+    takes the order whose warmup fills device k with forwards until the first
+    gradient can reach it.  Derivation at one tick per op and no latency:
+    microbatch 0 enters virtual stage s at tick s, so its forward leaves the
+    last of the S = vP virtual stages at tick S; its gradient then walks back
+    one virtual stage per tick and reaches virtual stage (v-1)P + k -- device
+    k's last chunk, whose backward comes first -- at tick S + (P-1-k).  Device
+    k receives its first input at tick k, so it runs S + P - 1 - 2k forwards
+    back to back before it (at most the vM it has), then its first backward
+    (chunk v-1, microbatch 0) at that tick.  Its ledger peaks there, since each
+    later forward is paired with a backward."""
+    for P in (1, 2, 3, 4, 5, 8):
+        for v in (2, 3, 4):
+            for M in (P, 2 * P, 3 * P, 4 * P):
+                kind, chunk, mb = orc.order("interleaved", P, M, v)
+                r = orc.evaluate("interleaved", P, M, v, 1, 1)
+                S = v * P
+                for k in range(P):
+                    want = min(S + P - 1 - 2 * k, v * M)
+                    seq = list(kind[k])
+                    first_b = seq.index(1)
+                    assert first_b == want, (P, v, M, k)
+                    assert r["peak"][k] == want
+                    assert (chunk[k][first_b], mb[k][first_b]) == (v - 1, 0)
+                    if want < v * M:
+                        # no idle tick in the warmup, and the backward at its arrival
+                        assert list(r["start"][k][:first_b + 1]) == list(range(k, k + first_b + 1))
+                        assert r["start"][k][first_b] == S + P - 1 - k
+    # P = 4, v = 2, M = 8: the counts written out
+    assert [list(orc.order("interleaved", 4, 8, 2)[0][k]).index(1) for k in range(4)] == [11, 9, 7, 5]
+
+
 def test_gpipe_comm_invariant(orc):
     # GPipe with every stage equally fast and uniform comm c: the forward wave
     # reaches the last stage after (P-1)(t_f+c) + M t_f, the backward wave needs
@@ -179,6 +214,74 @@ def test_gpipe_comm_invariant(orc):
             for tf, tb, c in ((1, 1, 1), (1, 2, 3), (2, 3, 1)):
                 r = orc.evaluate("gpipe", P, M, 1, tf, tb, comm=c, method=2)
                 assert r["makespan"] == (M + P - 1) * (tf + tb) + 2 * (P - 1) * c
+
+
+def _census_by_graph(P, M):
+    """Independent enumeration for tiny P, M at unit cost: every combination of
+    per-stage orders with each F_i before its B_i, run as a plain dependency
+    graph (stage order, F(s-1,i) -> F(s,i), B(s+1,i) -> B(s,i)); a cycle is a
+    deadlock, else the makespan is the longest path counted in ops.  Returns
+    (valid, deadlocked, min makespan, orders reaching it, min stage-0 peak
+    among them)."""
+    ops = [(0, i) for i in range(M)] + [(1, i) for i in range(M)]
+    stage_orders = [q for q in itertools.permutations(ops)
+                    if all(q.index((0, i)) < q.index((1, i)) for i in range(M))]
+    valid = dead = 0
+    best, nbest, pk0 = None, 0, None
+    for combo in itertools.product(stage_orders, repeat=P):
+        preds = {}
+        for s, q in enumerate(combo):
+            for j, (kd, i) in enumerate(q):
+                p = [(s, *q[j - 1])] if j else []
+                if kd == 0 and s > 0:
+                    p.append((s - 1, 0, i))
+                if kd == 1 and s < P - 1:
+                    p.append((s + 1, 1, i))
+                preds[(s, kd, i)] = p
+        depth, state = {}, {}
+
+        def longest(node):
+            # iterative DFS; returns None on a cycle
+            stack = [node]
+            while stack:
+                x = stack[-1]
+                if x in depth:
+                    stack.pop()
+                    continue
+                state[x] = 1
+                todo = [y for y in preds[x] if y not in depth]
+                for y in todo:
+                    if state.get(y) == 1:
+                        return None
+                if todo:
+                    stack.extend(todo)
+                    continue
+                depth[x] = 1 + max((depth[y] for y in preds[x]), default=0)
+                state[x] = 2
+                stack.pop()
+            return depth[node]
+
+        mk = 0
+        for x in preds:
+            d = longest(x)
+            if d is None:
+                mk = None
+                break
+            mk = max(mk, d)
+        if mk is None:
+            dead += 1
+            continue
+        valid += 1
+        held, peak0 = 0, 0
+        for kd, _ in combo[0]:
+            held += 1 if kd == 0 else -1
+            peak0 = max(peak0, held)
+        if best is None or mk < best:
+            best, nbest, pk0 = mk, 0, peak0
+        if mk == best:
+            nbest += 1
+            pk0 = min(pk0, peak0)
+    return valid, dead, best, nbest, pk0
 
 
 def test_bruteforce_optimality(orc):
@@ -192,6 +295,31 @@ def test_bruteforce_optimality(orc):
             for policy in ("gpipe", "1f1b"):
                 assert orc.evaluate(policy, P, M, 1, 1, 1)["makespan"] == b["min_makespan"]
             assert orc.evaluate("1f1b", P, M, 1, 1, 1)["peak"][0] == b["min_peak0"]
+
+
+def test_bruteforce_census(orc):
+    """The census of the exhaustive check, cell by cell for P, M <= 3."""
+    for P in (1, 2, 3):
+        for M in (1, 2, 3):
+            b = orc.bruteforce(P, M)
+            # A stage runs 2M ops with each F_i before its B_i: (2M)!/2^M orders,
+            # independently on each of the P stages.
+            assert b["valid"] + b["deadlocked"] == (math.factorial(2 * M) // 2 ** M) ** P
+            if P == 1:
+                # one stage has no cross-stage edge: nothing deadlocks and every
+                # order keeps the stage busy for all 2M ticks
+                assert b["deadlocked"] == 0 and b["n_optimal"] == b["valid"]
+            if M == 1:
+                assert (b["valid"], b["deadlocked"], b["n_optimal"]) == (1, 0, 1)
+            if (P, M) != (3, 3):
+                # an enumeration of its own (a dependency graph per combination)
+                want = _census_by_graph(P, M)
+                got = (b["valid"], b["deadlocked"], b["min_makespan"], b["n_optimal"], b["min_peak0"])
+                assert got == want, (P, M)
+    # P = M = 3: 729,000 combinations, of which 138,294 run, 590,706 deadlock
+    # and 210 reach the minimum 10 ticks (an independent enumeration's census).
+    b = orc.bruteforce(3, 3)
+    assert (b["valid"], b["deadlocked"], b["n_optimal"]) == (138294, 590706, 210)
 
 
 def test_deadlock_detected_by_both_evaluators(orc):
@@ -437,6 +565,7 @@ MUTANTS = {
     10: "ZB2P keeps 1F1B's warmup",
     11: "ZB admits an F at the activation limit",
     12: "backward edges take the forward latency",
+    13: "interleaved warmup one forward too long",
 }
 
 
@@ -523,6 +652,16 @@ def _pin_suite(orc, lib):
         return r["makespan"] == 11 * 5 + 3 * 5
 
     check("comm_fb", comm_fb)
+
+    def ilv_warmup():
+        P, M, v = 4, 8, 2
+        kind, chunk, _ = orc.order("interleaved", P, M, v, lib=lib)
+        r = orc.evaluate("interleaved", P, M, v, 1, 1, lib=lib)
+        want = [min(v * P + P - 1 - 2 * k, v * M) for k in range(P)]
+        return ([list(kind[k]).index(1) for k in range(P)] == want
+                and list(r["peak"]) == want)
+
+    check("ilv_warmup", ilv_warmup)
     return failed
 
 
