@@ -136,8 +136,12 @@ class ClockSampler:
         while not self._stop.is_set():
             if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) == 0 and \
                     self._reason_fn(self.h, ctypes.byref(r)) == 0:
-                self.samples.append((c.value, r.value))
+                self.samples.append((time.perf_counter(), c.value, r.value))
             time.sleep(0.002)
+
+    def loaded(self):
+        """Samples taken while the GPU was not idle."""
+        return [s for s in self.samples if not s[2] & 0x1]
 
     def __enter__(self):
         if self.ok:
@@ -150,17 +154,28 @@ class ClockSampler:
             self._stop.set()
             self._t.join()
 
-    def summary(self):
-        if not self.ok or not self.samples:
+    def summary(self, timed=None):
+        """Median SM clock and the active reasons over the samples taken under
+        load; `timed` = (t0, t1) host times of the timed region, whose samples
+        are also counted."""
+        load = self.loaded() if self.ok else []
+        if not load:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
-                    "source": "nvml unavailable"}
-        mhz = [s[0] for s in self.samples]
+                    "source": "nvml unavailable" if not self.ok else "nvml: no sample under load"}
         bits = 0
-        for _, r in self.samples:
+        for _, _, r in load:
             bits |= r
-        reasons = [name for b, name in self.REASONS.items() if bits & b]
-        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": reasons,
-                "samples": len(self.samples), "source": "nvml during timed region"}
+        out = {"sm_mhz": statistics.median(s[1] for s in load), "sm_max_mhz": self.max_mhz,
+               "reasons": [name for b, name in self.REASONS.items() if bits & b],
+               "samples": len(load),
+               "source": "nvml every 2 ms from the first warm-up step through the timed region and "
+                         "a tail of the same step (idle samples dropped)"}
+        if timed:
+            inside = [s for s in load if timed[0] <= s[0] <= timed[1]]
+            out["samples_in_timed_region"] = len(inside)
+            if inside:
+                out["sm_mhz_timed_region"] = statistics.median(s[1] for s in inside)
+        return out
 
 
 # ---------------------------------------------------------------------------
@@ -277,7 +292,8 @@ def reference_arm(args, budget_s=90.0):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
         "data": "synthetic",
-        "config": dict(bench_config(args.n, world), sample_instances_per_step=per_step),
+        "config": bench_config(args.n, world),
+        "sample_instances_per_step": per_step,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"first {per_step} of the {batch.n} instances per step, event simulation, "
                                    f"{threads} threads"},
@@ -323,6 +339,8 @@ def main():
         B.evaluate(batch.policy, P, M, 1, cf, cb, batch.strides, n, comm=cm,
                    comm_strides=batch.comm_strides, out=outs, stream=stream)
 
+    sampler = ClockSampler(local)
+    sampler.__enter__()
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
@@ -331,17 +349,27 @@ def main():
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     t_all0, t_all1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local)
     barrier()
     torch.cuda.synchronize()
-    with sampler:
-        t_all0.record(stream)
-        for i in range(K):
-            ev[i][0].record(stream)
+    h0 = time.perf_counter()
+    t_all0.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize()
+    h1 = time.perf_counter()
+    # A short timed region gives few clock samples: keep running the same step,
+    # untimed, until the sampler holds at least 25 samples under load (at
+    # least 0.1 s, at most 2 s).
+    tail0 = time.perf_counter()
+    while sampler.ok and time.perf_counter() - tail0 < 2.0 and \
+            (time.perf_counter() - tail0 < 0.1 or len(sampler.loaded()) < 25):
+        for _ in range(20):
             step()
-            ev[i][1].record(stream)
-        t_all1.record(stream)
         torch.cuda.synchronize()
+    sampler.__exit__(None, None, None)
     barrier()
     elapsed = t_all0.elapsed_time(t_all1) / 1e3
     kern = [a.elapsed_time(b) / 1e3 for a, b in ev]
@@ -400,7 +428,7 @@ def main():
                          "peak_source": peak_src, "traffic": profiled_traffic(),
                          "algorithmic_bytes_per_launch": abytes, "avg_launch_us": kavg * 1e6},
             "instances_per_s": world * n * K / elapsed,
-            "clocks": sampler.summary(),
+            "clocks": sampler.summary(timed=(h0, h1)),
             "e2e": e2e,
         }
         if not args.no_cpu:

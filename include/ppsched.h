@@ -378,11 +378,17 @@ int pp_sched_partition_search_interleaved(const int32_t *layer_tf, const int32_t
  * at file scope on every GPU that loads it and keeps until the process exits.
  *   - The first call on a device looks up that array's device address
  *     (cudaGetSymbolAddress); make that first call before any stream capture.
- *   - A call whose shape (policy, P, M) or stride pair differs from the previous
- *     call on the device rebuilds the tables in the array and synchronizes
- *     `stream`; a repeated shape and stride pair reuses them and just launches.
+ *   - A call whose shape (policy, P, M) differs from the previous call's on the
+ *     device rebuilds all tables in the array and synchronizes `stream` once
+ *     (to read the plan's size).  A call with the previous shape but another
+ *     stride pair (stride_stage, stride_mb) only enqueues the rebuild of the
+ *     stride-dependent tables on `stream`, without a synchronization.  A call
+ *     that repeats the previous shape and stride pair reuses the tables and
+ *     just launches.
  *   - Every call shares the array: calls that overlap on the GPU (other streams,
- *     other threads) race; serialize them.
+ *     other threads) race; serialize them.  In particular a call on another
+ *     stream must first wait for `stream` (an event), since a rebuild enqueued
+ *     on `stream` may still be writing the tables it would read.
  *   - Shapes whose tables do not fit in the array return PP_ERR_SIZE;
  *     PP_INTERLEAVED_1F1B returns PP_ERR_ARG.
  * Inputs, outputs and strides: as pp_sched_eval.  Errors: as pp_sched_eval. */

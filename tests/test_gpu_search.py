@@ -1,5 +1,7 @@
 """GPU partition search against the oracle's candidate scorer (bit-exact
 makespans, identical argmin with ties to the lower candidate index)."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -48,25 +50,19 @@ def test_nothing_feasible(B):
 
 
 def test_layer_split_full(orc, B):
-    """1,048,576 candidates of the 80-layer model at P=8, M=128: the winner is
-    the lowest-index minimum of all makespans; the oracle re-scores the winner,
-    its stage split and 200 sampled candidates."""
+    """1,048,576 candidates of the 80-layer model at P=8, M=128: every
+    candidate's makespan (or rejection) equals the oracle's, and so do the
+    argmin (lowest index of the minimum), its makespan and its stage split."""
     p = W.layer_split()
     g = _gpu_search(B, p, 0, p.n_cand)
+    r = orc.search(p.layer_tf, p.layer_tb, p.layer_act, p.P, p.M, p.comm, p.cap, p.seed, 0, p.n_cand,
+                   nthreads=os.cpu_count() or 8)
     mk = g["all_makespan"]
-    feas = mk >= 0
-    assert feas.any()
-    best = int(g["best_idx"][0])
-    assert mk[best] == mk[feas].min() == int(g["best_makespan"][0])
-    assert best == int(np.nonzero(mk == mk[feas].min())[0][0])
-    r = orc.search(p.layer_tf, p.layer_tb, p.layer_act, p.P, p.M, p.comm, p.cap, p.seed, best, best + 1)
-    assert r["best_makespan"] == mk[best]
+    assert np.array_equal(mk, r["all_makespan"])
+    assert (mk >= 0).any()
+    assert int(g["best_idx"][0]) == r["best_idx"]
+    assert int(g["best_makespan"][0]) == r["best_makespan"]
     assert list(g["best_cuts"]) == list(r["first"][1:p.P])
-    rng = np.random.default_rng(55)
-    for start in rng.choice(p.n_cand - 8, 25, replace=False):
-        rs = orc.search(p.layer_tf, p.layer_tb, p.layer_act, p.P, p.M, p.comm, p.cap, p.seed,
-                        int(start), int(start) + 8, nthreads=8)
-        assert np.array_equal(rs["all_makespan"], mk[start:start + 8])
 
 
 def test_split_ranges_reduce_to_whole(B):

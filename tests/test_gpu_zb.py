@@ -1,6 +1,8 @@
 """GPU Zero Bubble evaluator (pp_sched_eval_zb) against the oracle's ZB
 simulator: every output bit-exact, including per-op times and the per-instance
 peak of held microbatches."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -96,15 +98,14 @@ def test_broadcast_strides(orc):
 
 
 @pytest.mark.parametrize("policy", [W.ZB1P, W.ZB2P])
-def test_hetero_full_batch_sampled(orc, policy):
-    """65,536 heterogeneous instances (P=8, M=64): 300 sampled instances
-    re-derived by the oracle, invariants on all."""
+def test_hetero_full_batch(orc, policy):
+    """65,536 heterogeneous instances (P=8, M=64): every instance against the
+    oracle, plus invariants."""
     batch = W.hetero_zb(policy)
     g = run_gpu_zb(batch)
     assert (g["status"] == 0).all()
-    sel = np.unique(np.random.default_rng(31 + policy).choice(batch.n, 300, replace=False))
-    r = run_oracle_zb(orc, batch, select=sel)
-    assert_same_zb(g, r, select=sel)
+    r = run_oracle_zb(orc, batch, nthreads=os.cpu_count() or 8)
+    assert_same_zb(g, r)
     busy = np.zeros((batch.n, 8), np.int64)
     for c in (batch.cost_f, batch.cost_b, batch.cost_w):
         busy += c.reshape(8, 64, batch.n).sum(axis=1).T

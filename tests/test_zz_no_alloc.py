@@ -2,11 +2,19 @@
 
 It serves callers that cannot let a library call cudaMalloc (their device
 memory belongs to another allocator, or must not grow while they run).  These
-tests call it through the C ABI and check that its outputs equal those of
-pp_sched_eval, bit for bit, on consecutive calls: a new shape (tables built in
-the library's fixed array), another shape and layout (tables rebuilt), and the
-first shape again with new costs (tables reused).  The file is collected last
-on purpose and depends on no other test.
+tests call it through the C ABI and check every output against pp_sched_eval,
+bit for bit, and against the CPU oracle, instance by instance, on a sequence
+of calls that walks every state of the library's fixed table array:
+
+  1. a new shape: the tables are built in the array;
+  2. the same shape and strides with new costs: the tables are reused as they
+     are (nothing rebuilt, one launch);
+  3. the same shape with another stride pair (rows padded to a multiple of 8
+     instances): only the stride-dependent kernel tables are rebuilt;
+  4. another shape and layout: everything is rebuilt;
+  5. the first shape again: rebuilt once more, then reused by a sixth call.
+
+The file is collected last on purpose and depends on no other test.
 """
 import ctypes
 
@@ -15,6 +23,7 @@ import pytest
 import torch
 
 import pipeline_schedule_simulation_gb300.workloads as W
+from gpu_helpers import assert_same, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -58,17 +67,28 @@ def _same(x, y):
         assert torch.equal(x[k].cpu(), y[k].cpu()), k
 
 
-def test_noalloc_matches_eval_on_consecutive_calls():
+def test_noalloc_matches_eval_and_oracle_on_consecutive_calls(orc):
     from pipeline_schedule_simulation_gb300 import binding as B
-    first = W.hetero_1f1b(n=5004, seed=21)                      # instance-minor, ragged tail
-    second = W.random_batch(W.GPIPE, 4, 16, 1, 777, seed=22, hi=30, layout="inst_major")
-    third = W.hetero_1f1b(n=5004, seed=23)                      # the first shape again, new costs
-    for b in (first, second, third):
+    P, M = 8, 64
+    calls = [
+        ("new shape", W.hetero_1f1b(n=5004, seed=21)),
+        ("same shape and strides, new costs", W.hetero_1f1b(n=5004, seed=22)),
+        ("same shape, rows padded to 8", W.random_batch(W.ONEF1B, P, M, 1, 5001, seed=23, lo=1, hi=200,
+                                                        pad_to=8)),
+        ("another shape and layout", W.random_batch(W.GPIPE, 4, 16, 1, 777, seed=24, hi=30,
+                                                    layout="inst_major")),
+        ("first shape again", W.hetero_1f1b(n=5004, seed=25)),
+        ("first shape, reused", W.hetero_1f1b(n=5004, seed=26)),
+    ]
+    assert calls[0][1].strides != calls[2][1].strides      # a different stride pair at the same shape
+    for what, b in calls:
         cf, cb, cm = _dev(b.cost_f), _dev(b.cost_b), _dev(b.comm)
         got = _noalloc(B, b, cf, cb, cm)
         want = _reference(B, b, cf, cb, cm)
         _same(got, want)
-        assert (got["status"].cpu() == 0).all()
+        g = {k: v.cpu().numpy() for k, v in got.items()}
+        assert (g["status"] == 0).all(), what
+        assert_same(g, run_oracle(orc, b, nthreads=8))
 
 
 def test_noalloc_rejects_what_it_does_not_cover():
