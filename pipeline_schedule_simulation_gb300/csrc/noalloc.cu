@@ -113,7 +113,8 @@ extern "C" int pp_sched_eval_noalloc(pp_policy_t policy, int P, int M, const int
     a.ktab = nullptr; a.ktab_words = 0;
     if (reg_table_path(d->sp.pmax, a, vec)) {
         if (!d->with_ktab || d->s_stage != stride_stage || d->s_mb != stride_mb) {
-            d->sp.used_words -= d->sp.ktab_words;  // the tables of another stride pair are replaced
+            // ktab_into writes right after the plan's tables (used_words, which it
+            // does not advance), so another stride pair's tables are replaced in place.
             d->sp.ktab_words = 0;
             d->with_ktab = false;
             rc = ktab_into(&d->sp, stride_stage, stride_mb, stream);

@@ -588,6 +588,8 @@ int plan_into(int policy, int P, int M, uint32_t *region, int64_t region_words, 
     return PP_OK;
 }
 
+// The kernel tables go right after the plan's tables (at used_words, which is
+// not advanced), so a later call for another stride pair replaces them in place.
 int ktab_into(ScratchPlan *sp, int64_t s_stage, int64_t s_mb, cudaStream_t st) {
     const int words = ktab_words(sp->R, sp->pmax, sp->nseg);
     if (sp->used_words + words > sp->region_words) return PP_ERR_SIZE;
