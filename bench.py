@@ -525,10 +525,12 @@ def secondary(B, W, torch, stream):
 def closed_form_sweep(B, W, torch, stream, timed):
     """The closed-form sweep (GPipe and 1F1B at P 2..16 x M 1..128, interleaved
     v = 2 where P divides M; 16 scalar-cost instances per shape).  Timed as one
-    pp_sched_eval per shape -- the first pass (every shape's plan is built
-    then), later passes driven from Python, the same calls replayed from a CUDA
-    graph -- and as one prepared set of problems (pp_sched_many_*: a few fused
-    launches), called from Python and replayed from a CUDA graph."""
+    pp_sched_eval per shape -- the first pass from an empty plan cache (every
+    shape's plan is built then, one at a time), later passes driven from
+    Python, the same calls replayed from a CUDA graph -- and as one prepared
+    set of problems (pp_sched_many_*: every plan and table built in one batch,
+    then a few fused launches): its preparation from an empty plan cache, its
+    evaluation called from Python and replayed from a CUDA graph."""
     calls = []
     op_times = 0
     for pol, P_, M_, v_ in W.sweep_shapes():
@@ -548,14 +550,26 @@ def closed_form_sweep(B, W, torch, stream, timed):
             B.evaluate(bt.policy, bt.P, bt.M, bt.v, f, g, bt.strides, bt.n, comm=c,
                        comm_strides=bt.comm_strides, out=o, stream=st)
 
+    # both first passes start from an empty plan cache (as in a fresh process)
     torch.cuda.synchronize()
+    B.cache_clear()
     t0 = time.perf_counter()
     one_pass(stream)
     torch.cuda.synchronize()
     first = time.perf_counter() - t0
+    problems = [{"policy": bt.policy, "P": bt.P, "M": bt.M, "v": bt.v, "n": bt.n, "strides": bt.strides,
+                 "cost_f": f, "cost_b": g, "comm": c, "comm_strides": bt.comm_strides, "out": o}
+                for bt, f, g, c, o in calls]
+    B.cache_clear()
+    t0 = time.perf_counter()
+    cold = B.Many(problems, stream=stream)
+    torch.cuda.synchronize()
+    prepare_cold = time.perf_counter() - t0
+    cold.close()
     loop = timed(lambda: one_pass(stream), 3)
     res = {"shapes": len(calls), "instances": 16 * len(calls), "op_times": op_times,
-           "first_pass_ms": first * 1e3, "loop_ms": loop * 1e3, "loop_op_times_per_s": op_times / loop}
+           "first_pass_ms": first * 1e3, "many_prepare_cold_ms": prepare_cold * 1e3,
+           "loop_ms": loop * 1e3, "loop_op_times_per_s": op_times / loop}
     try:
         side = torch.cuda.Stream()
         side.wait_stream(stream)
@@ -567,9 +581,7 @@ def closed_form_sweep(B, W, torch, stream, timed):
     except Exception as e:  # capture is a measurement aid here, not part of the path
         res.update(graph_ms=None, graph_error=str(e)[:200])
     # the same problems prepared once and evaluated together (pp_sched_many_*)
-    many = B.Many([{"policy": bt.policy, "P": bt.P, "M": bt.M, "v": bt.v, "n": bt.n, "strides": bt.strides,
-                    "cost_f": f, "cost_b": g, "comm": c, "comm_strides": bt.comm_strides, "out": o}
-                   for bt, f, g, c, o in calls], stream=stream)
+    many = B.Many(problems, stream=stream)
     mt = timed(lambda: many(stream=stream), 20)
     res.update(many_ms=mt * 1e3, many_op_times_per_s=op_times / mt, many_info=many.info())
     try:

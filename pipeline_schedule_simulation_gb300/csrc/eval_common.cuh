@@ -391,21 +391,22 @@ bool lane_path(const pp_plan *plan, const EvalArgs &a);
 int launch_eval_split8(const EvalArgs &a, cudaStream_t st);
 int launch_eval_lane(pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st);
 
-// Fused launches over many problems (pp_sched_many_*).  *_job prepares one
-// problem's arguments (its tables built, allocating and synchronizing on first
-// use) and answers whether the fused kernel takes it; *_warps is the warps its
+// Fused launches over many problems (pp_sched_many_*).  *_ok answers whether
+// the fused kernel takes a problem (lane_mbz_ok also sets a.nslots); its
+// tables are built by build_tables (register evaluator's for reg, lane
+// evaluator's with one instance set per lane for lane); *_warps is the warps its
 // instances fill, *_ctas the CTAs of `warps` warps it needs, *_smem the
 // dynamic shared memory of such a CTA; launch_*_many runs a group of jobs of
 // one table width, already in device memory, with CTAs of `warps` warps (at
 // most kManyRegWarps / kManyLaneWarps).
 constexpr int kManyRegWarps = 4, kManyLaneWarps = 2;
-bool reg_mbz_job(pp_plan *plan, EvalArgs &a, cudaStream_t st, int *rc);
+bool reg_mbz_ok(const pp_plan *plan, const EvalArgs &a);
 int64_t reg_mbz_warps(const EvalArgs &a);
 int64_t reg_mbz_ctas(const EvalArgs &a, int warps);
 size_t reg_mbz_smem(int pmax, const EvalArgs &a, int warps);
 int launch_reg_mbz_many(int pmax, int warps, const ManyJob *d_jobs, int njobs, int64_t ctas, size_t smem,
                         cudaStream_t st);
-bool lane_mbz_job(pp_plan *plan, EvalArgs &a, const uint4 **tab, int *nblocks, cudaStream_t st, int *rc);
+bool lane_mbz_ok(const pp_plan *plan, EvalArgs &a);
 int64_t lane_mbz_warps(int pmax, const EvalArgs &a);
 int64_t lane_mbz_ctas(int pmax, const EvalArgs &a, int warps);
 size_t lane_mbz_smem(int pmax, const EvalArgs &a, int warps);

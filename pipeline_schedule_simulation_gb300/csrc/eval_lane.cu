@@ -74,52 +74,69 @@ __device__ __forceinline__ uint32_t lane_lt(const uint32_t *desc, int R, int P, 
 
 // Table of the lane evaluator for one stride pair: head (loader entries of
 // rounds 0 .. kAhead-1), then ceil(R / kBR) blocks laid out as described at
-// the top of the file.
+// the top of the file.  Word e of that table:
+template <int PMAX>
+__device__ uint32_t ltab_word(const uint32_t *desc, const uint8_t *lrd, const uint8_t *lwr, int R, int P, int v,
+                              int nslots, int s_stage, int s_mb, uint32_t row_bytes, int64_t e) {
+    using G = LaneGeom<PMAX>;
+    uint32_t w = kLtIdle;
+    if (e < G::kHeadWords) {
+        const int q = (int)e;
+        if (q < G::kAhead * PMAX) w = lane_lt(desc, R, P, PMAX, q / PMAX, q % PMAX, s_stage, s_mb);
+    } else {
+        const int64_t e2 = e - G::kHeadWords;
+        const int b = (int)(e2 / G::kBlockWords);
+        const int o = (int)(e2 % G::kBlockWords);
+        const int idx = o >> 2, q = idx / PMAX, k = idx % PMAX, r = b * G::kBR + q;
+        if ((o & 3) == 3) {
+            w = lane_lt(desc, R, P, PMAX, r + G::kAhead, k, s_stage, s_mb);
+        } else {
+            const uint32_t col = (uint32_t)(k * G::kIPW * 4);
+            uint32_t rd = (uint32_t)nslots * row_bytes + col;           // zero row
+            uint32_t wr = (uint32_t)(nslots + 1) * row_bytes + col;     // scratch row
+            uint32_t cm = (uint32_t)(2 * v) * row_bytes + col, act = 0;  // zero comm row
+            if (r < R) {
+                const uint32_t d = desc[(int64_t)r * PMAX + k];
+                const uint32_t kind = desc_kind(d);
+                if (kind != kIdle) {
+                    act = kLaneActive;
+                    const uint32_t rs = lrd[(int64_t)r * PMAX + k], ws = lwr[(int64_t)r * PMAX + k];
+                    // the op's (chunk, kind) row: its input edge's comm (0 where
+                    // there is no edge) and, with costs shared by all
+                    // microbatches, its cost
+                    cm = (2u * desc_chunk(d) + (kind == kBwd ? 1u : 0u)) * row_bytes + col;
+                    if (rs != kNoSlot) rd = rs * row_bytes + col;
+                    if (ws != kNoSlot) {
+                        const int kc = kind == kFwd ? (k + 1) % P : (k + P - 1) % P;
+                        wr = ws * row_bytes + (uint32_t)(kc * G::kIPW * 4);
+                    }
+                }
+            }
+            w = (o & 3) == 0 ? rd : ((o & 3) == 1 ? cm : (wr | act));
+        }
+    }
+    return w;
+}
+
 template <int PMAX>
 __global__ void k_ltab(const uint32_t *desc, const uint8_t *lrd, const uint8_t *lwr, int R, int P, int v, int nslots,
                        int s_stage, int s_mb, int nblocks, uint32_t row_bytes, uint32_t *out) {
     using G = LaneGeom<PMAX>;
     const int64_t total = G::kHeadWords + (int64_t)nblocks * G::kBlockWords;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-         e += (int64_t)gridDim.x * blockDim.x) {
-        uint32_t w = kLtIdle;
-        if (e < G::kHeadWords) {
-            const int q = (int)e;
-            if (q < G::kAhead * PMAX) w = lane_lt(desc, R, P, PMAX, q / PMAX, q % PMAX, s_stage, s_mb);
-        } else {
-            const int64_t e2 = e - G::kHeadWords;
-            const int b = (int)(e2 / G::kBlockWords);
-            const int o = (int)(e2 % G::kBlockWords);
-            const int idx = o >> 2, q = idx / PMAX, k = idx % PMAX, r = b * G::kBR + q;
-            if ((o & 3) == 3) {
-                w = lane_lt(desc, R, P, PMAX, r + G::kAhead, k, s_stage, s_mb);
-            } else {
-                const uint32_t col = (uint32_t)(k * G::kIPW * 4);
-                uint32_t rd = (uint32_t)nslots * row_bytes + col;           // zero row
-                uint32_t wr = (uint32_t)(nslots + 1) * row_bytes + col;     // scratch row
-                uint32_t cm = (uint32_t)(2 * v) * row_bytes + col, act = 0;  // zero comm row
-                if (r < R) {
-                    const uint32_t d = desc[(int64_t)r * PMAX + k];
-                    const uint32_t kind = desc_kind(d);
-                    if (kind != kIdle) {
-                        act = kLaneActive;
-                        const uint32_t rs = lrd[(int64_t)r * PMAX + k], ws = lwr[(int64_t)r * PMAX + k];
-                        // the op's (chunk, kind) row: its input edge's comm (0 where
-                        // there is no edge) and, with costs shared by all
-                        // microbatches, its cost
-                        cm = (2u * desc_chunk(d) + (kind == kBwd ? 1u : 0u)) * row_bytes + col;
-                        if (rs != kNoSlot) rd = rs * row_bytes + col;
-                        if (ws != kNoSlot) {
-                            const int kc = kind == kFwd ? (k + 1) % P : (k + P - 1) % P;
-                            wr = ws * row_bytes + (uint32_t)(kc * G::kIPW * 4);
-                        }
-                    }
-                }
-                w = (o & 3) == 0 ? rd : ((o & 3) == 1 ? cm : (wr | act));
-            }
-        }
-        out[e] = w;
-    }
+         e += (int64_t)gridDim.x * blockDim.x)
+        out[e] = ltab_word<PMAX>(desc, lrd, lwr, R, P, v, nslots, s_stage, s_mb, row_bytes, e);
+}
+
+// Many tables with one instance set per lane, one TableJob per table (blockIdx.y).
+template <int PMAX>
+__global__ void kb_ltab(const TableJob *jobs) {
+    const TableJob &b = jobs[blockIdx.y];
+    const int64_t cells = (int64_t)b.R * PMAX;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < b.words;
+         e += (int64_t)gridDim.x * blockDim.x)
+        b.out[e] = ltab_word<PMAX>(b.desc, b.lslot, b.lslot + cells, b.R, b.P, b.v, b.nslots, b.s_stage, b.s_mb,
+                                   128u, e);
 }
 
 // This lane's share of a round's cost copies.  Vector path: a device row of
@@ -569,25 +586,39 @@ int launch_eval_lane(pp_plan *plan, const EvalArgs &args, bool vec, bool ops, cu
     }
 }
 
+int64_t lane_table_words(int pmax, int R, int *nblocks) {
+    switch (pmax) {
+        case 4: *nblocks = (R + LaneGeom<4>::kBR - 1) / LaneGeom<4>::kBR;
+                return LaneGeom<4>::kHeadWords + (int64_t)*nblocks * LaneGeom<4>::kBlockWords;
+        case 8: *nblocks = (R + LaneGeom<8>::kBR - 1) / LaneGeom<8>::kBR;
+                return LaneGeom<8>::kHeadWords + (int64_t)*nblocks * LaneGeom<8>::kBlockWords;
+        case 16: *nblocks = (R + LaneGeom<16>::kBR - 1) / LaneGeom<16>::kBR;
+                 return LaneGeom<16>::kHeadWords + (int64_t)*nblocks * LaneGeom<16>::kBlockWords;
+        default: return -1;
+    }
+}
+
+int launch_ltab_batch(int pmax, const TableJob *d_jobs, int njobs, int64_t max_words, cudaStream_t st) {
+    const dim3 grid((unsigned)std::min<int64_t>(1024, std::max<int64_t>(1, (max_words + 255) / 256)),
+                    (unsigned)njobs);
+    switch (pmax) {
+        case 4: kb_ltab<4><<<grid, 256, 0, st>>>(d_jobs); break;
+        case 8: kb_ltab<8><<<grid, 256, 0, st>>>(d_jobs); break;
+        case 16: kb_ltab<16><<<grid, 256, 0, st>>>(d_jobs); break;
+        default: return PP_ERR_INTERNAL;
+    }
+    PPS_CUDA_TRY(cudaGetLastError());
+    return PP_OK;
+}
+
 // The fused lane path over many problems: plans without the register path
 // (interleaved) whose costs are the same for every microbatch, without
 // per-op output or a separate backward latency.
-bool lane_mbz_job(pp_plan *plan, EvalArgs &a, const uint4 **tab, int *nblocks, cudaStream_t st, int *rc) {
-    *rc = PP_OK;
+bool lane_mbz_ok(const pp_plan *plan, EvalArgs &a) {
     if (plan->reg_ok || a.comm_b || a.op_start || a.op_end || a.s_mb != 0 || a.n <= 0) return false;
     if (!lane_path(plan, a)) return false;
     a.nslots = plan->nlslots;
-    if (lane_mbz_smem(plan->pmax, a, kManyLaneWarps) > kLaneSmemLimit) return false;
-    const pp_ktab *t = nullptr;
-    switch (plan->pmax) {
-        case 4: *rc = lane_tables_t<4, 1>(plan, a.s_stage, a.s_mb, st, &t); *nblocks = (a.R + LaneGeom<4>::kBR - 1) / LaneGeom<4>::kBR; break;
-        case 8: *rc = lane_tables_t<8, 1>(plan, a.s_stage, a.s_mb, st, &t); *nblocks = (a.R + LaneGeom<8>::kBR - 1) / LaneGeom<8>::kBR; break;
-        case 16: *rc = lane_tables_t<16, 1>(plan, a.s_stage, a.s_mb, st, &t); *nblocks = (a.R + LaneGeom<16>::kBR - 1) / LaneGeom<16>::kBR; break;
-        default: *rc = PP_ERR_INTERNAL;
-    }
-    if (*rc) return false;
-    *tab = t->d;
-    return true;
+    return lane_mbz_smem(plan->pmax, a, kManyLaneWarps) <= kLaneSmemLimit;
 }
 
 int64_t lane_mbz_warps(int pmax, const EvalArgs &a) {

@@ -676,20 +676,12 @@ int launch_eval_reg_tables(int pmax, const EvalArgs &a, bool vec, bool ops, cuda
     }
 }
 
-// The fused register path over many problems: GPipe / 1F1B plans whose costs
-// are the same for every microbatch (stride_mb == 0), without per-op output;
-// the conditions of the single-problem microbatch-shared path.
-bool reg_mbz_job(pp_plan *plan, EvalArgs &a, cudaStream_t st, int *rc) {
-    *rc = PP_OK;
+// The fused register path over many problems takes GPipe / 1F1B plans whose
+// costs are the same for every microbatch (stride_mb == 0), without per-op
+// output: the conditions of the single-problem microbatch-shared path.
+bool reg_mbz_ok(const pp_plan *plan, const EvalArgs &a) {
     if (!plan->reg_ok || a.comm_b || a.op_start || a.op_end || a.s_mb != 0 || a.n <= 0) return false;
-    if (ktab_words(a.R, plan->pmax, a.nseg) > kMaxLtWords || (int64_t)(a.S - 1) * a.s_stage >= ((int64_t)1 << 30))
-        return false;
-    const pp_ktab *t = nullptr;
-    *rc = kernel_tables(plan, a.s_stage, a.s_mb, st, &t);
-    if (*rc) return false;
-    a.ktab = t->d;
-    a.ktab_words = t->words;
-    return true;
+    return ktab_words(a.R, plan->pmax, a.nseg) <= kMaxLtWords && (int64_t)(a.S - 1) * a.s_stage < ((int64_t)1 << 30);
 }
 
 int64_t reg_mbz_warps(const EvalArgs &a) { return (a.n + 31) / 32; }

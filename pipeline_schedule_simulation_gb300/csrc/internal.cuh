@@ -1,6 +1,7 @@
 // internal.cuh -- definitions shared by the library's translation units.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <deque>
 #include <mutex>
@@ -69,6 +70,13 @@ inline int pmax_for(int P) { return P <= 4 ? 4 : (P <= 8 ? 8 : 16); }
 
 }  // namespace pps
 
+// One device allocation shared by the tables of many plans (a batched build):
+// freed when the last plan or table that references it is destroyed.
+struct pp_arena {
+    void *base = nullptr;
+    std::atomic<int> refs{0};
+};
+
 // Kernel tables of the register evaluator for one (stride_stage, stride_mb)
 // pair: loader table, round words and segments, contiguous, ready to be copied
 // into shared memory.
@@ -77,6 +85,7 @@ struct pp_ktab {
     uint4 *d;         // words / 4 uint4
     int words;        // 32-bit words
     int variant = 0;  // layout variant (lane evaluator: instance sets per lane)
+    pp_arena *arena = nullptr;  // the allocation d lives in, or null if d is its own
 };
 
 // The plan object (opaque to callers).
@@ -101,6 +110,11 @@ struct pp_plan {
     std::deque<pp_ktab> ltabs;   // lane evaluator's tables, per stride pair (guarded by ktab_mu)
     int32_t *d_peak;    // [P]
     int32_t h_peak[PP_MAX_P];
+    // Allocations the tables live in: [0] ops, rounds and peak; [1] desc, round
+    // words and segments; [2] desc2 and lslot when built with the plan (then
+    // slots_in_arena), else those two are allocations of their own.
+    pp_arena *arena[3] = {nullptr, nullptr, nullptr};
+    bool slots_in_arena = false;
 };
 
 namespace pps {
@@ -111,6 +125,46 @@ int cuda_status(cudaError_t e);
 // Plan cache used by the evaluation entry points: returns the plan of the
 // shape on the current device, building it on first use.
 int cached_plan(int policy, int P, int M, int v, cudaStream_t stream, pp_plan **out);
+
+// Build the plans of n shapes together: every step is one batched launch over
+// all shapes, the tables of all shapes share three allocations, and the build
+// synchronizes `stream` three times whatever n is.  out[i] is a new plan
+// (value slots included for plans without the register path).
+struct PlanShape {
+    int policy, P, M, v;
+};
+int build_plans(const PlanShape *shapes, int n, cudaStream_t stream, pp_plan **out);
+// cached_plan for n shapes: the shapes not cached yet are built in one batch.
+int cached_plans(const PlanShape *shapes, int n, cudaStream_t stream, pp_plan **out);
+
+// Kernel tables of many (plan, stride pair) requests: the missing ones are
+// built in one allocation and a few batched launches on `stream`, without a
+// synchronization (later work on `stream` sees them; other streams must wait
+// for it).  lane = 0: the register evaluator's tables (kernel_tables);
+// lane = 1: the lane evaluator's tables with one instance set per lane.
+struct TableReq {
+    pp_plan *plan;
+    int64_t s_stage, s_mb;
+    int lane;
+    const pp_ktab *out;
+};
+int build_tables(TableReq *reqs, int n, cudaStream_t stream);
+
+// One table of a batched table build (device-side record).
+struct TableJob {
+    const uint32_t *desc;
+    const uint64_t *rw;
+    const uint4 *seg;
+    const uint8_t *lslot;  // [2][R][pmax] (lane tables)
+    int R, P, v, pmax, nseg, nslots, nblocks;
+    int s_stage, s_mb;
+    int64_t words;
+    uint32_t *out;
+};
+// Lane evaluator tables (eval_lane.cu): words of one table with one instance
+// set per lane, and the batched build of such tables for one table width.
+int64_t lane_table_words(int pmax, int R, int *nblocks);
+int launch_ltab_batch(int pmax, const TableJob *d_jobs, int njobs, int64_t max_words, cudaStream_t stream);
 // Value slots for a plan built without them (register plans get them on
 // first need); PP_ERR_SIZE if too many results would be in flight.
 int plan_value_slots(pp_plan *plan, cudaStream_t stream);

@@ -42,18 +42,23 @@ namespace {
 struct Pending {
     int kind, pmax;
     ManyJob job;
+    int req;  // index of its table request
 };
 
 int prepare(const pp_problem_t *problems, int n_problems, pp_many *h, cudaStream_t stream) {
+    // every shape's plan, the missing ones built in one batch
+    std::vector<PlanShape> shapes(n_problems);
+    for (int i = 0; i < n_problems; ++i)
+        shapes[i] = PlanShape{(int)problems[i].policy, problems[i].P, problems[i].M, problems[i].v};
+    std::vector<pp_plan *> plans(n_problems, nullptr);
+    int rc = cached_plans(shapes.data(), n_problems, stream, plans.data());
+    if (rc) return rc;
+    // which fused kernel takes each problem, and the tables it needs
     std::vector<Pending> jobs;
+    std::vector<TableReq> reqs;
     for (int i = 0; i < n_problems; ++i) {
         const pp_problem_t &p = problems[i];
-        int rc = eval_check(p.policy, p.P, p.M, p.v, p.cost_f, p.cost_b, p.stride_inst, p.stride_stage, p.stride_mb,
-                            p.comm_stride_inst, p.comm_stride_bnd, p.n_instances);
-        if (rc) return rc;
-        pp_plan *plan = nullptr;
-        rc = cached_plan((int)p.policy, p.P, p.M, p.v, stream, &plan);
-        if (rc) return rc;
+        pp_plan *plan = plans[i];
         if (p.n_instances == 0) {
             h->rest.push_back(p);
             continue;
@@ -61,19 +66,25 @@ int prepare(const pp_problem_t *problems, int n_problems, pp_many *h, cudaStream
         EvalArgs a = eval_args(plan, p.cost_f, p.cost_b, p.stride_inst, p.stride_stage, p.stride_mb, p.comm,
                                nullptr, p.comm_stride_inst, p.comm_stride_bnd, p.n_instances, p.makespan, p.idle,
                                p.bub_num, p.bub_den, p.peak, nullptr, nullptr, 0, 0, p.status);
-        if (reg_mbz_job(plan, a, stream, &rc)) {
-            jobs.push_back({0, plan->pmax, {a, nullptr, 0, 0}});
+        const int kind = reg_mbz_ok(plan, a) ? 0 : (lane_mbz_ok(plan, a) ? 1 : -1);
+        if (kind < 0) {
+            h->rest.push_back(p);
             continue;
         }
-        if (rc) return rc;
-        const uint4 *tab = nullptr;
-        int nblocks = 0;
-        if (lane_mbz_job(plan, a, &tab, &nblocks, stream, &rc)) {
-            jobs.push_back({1, plan->pmax, {a, tab, nblocks, 0}});
-            continue;
+        jobs.push_back({kind, plan->pmax, {a, nullptr, 0, 0}, (int)reqs.size()});
+        reqs.push_back({plan, a.s_stage, a.s_mb, kind, nullptr});
+    }
+    rc = build_tables(reqs.data(), (int)reqs.size(), stream);
+    if (rc) return rc;
+    for (Pending &j : jobs) {
+        const pp_ktab *t = reqs[j.req].out;
+        if (j.kind == 0) {
+            j.job.a.ktab = t->d;
+            j.job.a.ktab_words = t->words;
+        } else {
+            j.job.tab = t->d;
+            if (lane_table_words(j.pmax, j.job.a.R, &j.job.nblocks) < 0) return PP_ERR_INTERNAL;
         }
-        if (rc) return rc;
-        h->rest.push_back(p);
     }
     // groups by kernel and table width; within a group the jobs with the most
     // rounds first, so that CTAs handed out last are short ones

@@ -44,13 +44,15 @@ def _host(out):
 
 
 def test_closed_form_sweep_fused(orc):
-    """The whole sweep in one prepared set: every problem fused, a handful of
-    launches, every output of every problem equal to pp_sched_eval's and to
-    the oracle's."""
+    """The whole sweep in one prepared set, its plans and tables built from an
+    empty cache in one batch: every problem fused, a handful of launches,
+    every output of every problem equal to pp_sched_eval's and to the
+    oracle's."""
     from pipeline_schedule_simulation_gb300 import binding as B
     shapes = W.sweep_shapes()
     batches = [W.sweep_batch(*s) for s in shapes]
     problems = [_problem(b) for b in batches]
+    B.cache_clear()  # every plan and table is built by the preparation's batched build
     many = B.Many(problems)
     info = many.info()
     assert info == {"fused_problems": len(shapes), "launches": info["launches"], "other_problems": 0}
