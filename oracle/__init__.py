@@ -100,6 +100,11 @@ def _bind(lib):
     lib.orc_zb_batch.argtypes = [c_int, c_int, c_int, c_i64, vp, vp, vp, c_i64, c_i64, c_i64,
                                  vp, c_i64, c_i64, vp, vp, vp, vp, vp, vp, vp, vp, c_int]
     lib.orc_zb_batch.restype = c_int
+    lib.orc_dp_inst.argtypes = [c_int, c_int, c_int, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.orc_dp_inst.restype = c_int
+    lib.orc_dp_batch.argtypes = [c_int, c_int, c_int, c_i64, vp, vp, c_i64, c_i64, c_i64,
+                                 vp, c_i64, c_i64, vp, vp, vp, vp, vp, vp, vp, vp, c_int]
+    lib.orc_dp_batch.restype = c_int
     del i32p, i64p
     return lib
 
@@ -362,6 +367,65 @@ def zb_batch(policy, P, M, cost_f, cost_b, cost_w, strides, comm=None, comm_stri
                           _ptr(out["peak"]), _ptr(out["status"]), _ptr(os_), _ptr(oe), nthreads)
     if rc != OK:
         raise OracleError(rc, "zb_batch")
+    if op_times:
+        out["op_start"], out["op_end"] = os_, oe
+    return out
+
+
+def dp_evaluate(P, MA, MB, tf, tb, comm=None, lib=None):
+    """One DualPipe instance: route A carries microbatches 0..MA-1 from device 0,
+    route B microbatches MA..MA+MB-1 from device P-1 (see orc_dp_inst).
+
+    tf, tb: [P blocks][M] costs >= 1 (scalars broadcast); comm: [P-1] per link
+    or None.  Returns start, end ([P][2][M]: block, kind F/B, microbatch),
+    makespan, busy, idle, bub (num, den) and peak per device (+1 at F, -1 at B).
+    Parity: pinned by the reduction of one route to 1F1B, the mirror symmetry,
+    the page's peak of p+1 and an independent tick-stepped simulation
+    (tests/test_oracle_dualpipe.py)."""
+    lib = lib or load()
+    M = MA + MB
+    full = lambda a: np.ascontiguousarray(np.broadcast_to(np.asarray(a, np.int64), (P, M)))
+    tf, tb = full(tf), full(tb)
+    cm = None if comm is None else np.ascontiguousarray(np.broadcast_to(np.asarray(comm, np.int64), (max(P - 1, 1),)))
+    start = np.zeros((P, 2, M), np.int64)
+    end = np.zeros((P, 2, M), np.int64)
+    mk = np.zeros(1, np.int64)
+    busy = np.zeros(P, np.int64)
+    idle = np.zeros(P, np.int64)
+    bub = np.zeros(2, np.int64)
+    peak = np.zeros(P, np.int32)
+    rc = lib.orc_dp_inst(P, MA, MB, _ptr(tf), _ptr(tb), _ptr(cm), _ptr(start), _ptr(end), _ptr(mk), _ptr(busy),
+                         _ptr(idle), _ptr(bub), _ptr(peak))
+    if rc != OK:
+        raise OracleError(rc, "dp_evaluate")
+    return dict(start=start, end=end, makespan=int(mk[0]), busy=busy, idle=idle,
+                bub=(int(bub[0]), int(bub[1])), peak=peak)
+
+
+def dp_batch(P, MA, MB, cost_f, cost_b, strides, comm=None, comm_strides=(0, 0), n=None, op_times=False,
+             nthreads=1, lib=None):
+    """DualPipe batch with the library's input conventions (int32 costs
+    [inst][block][microbatch] through element strides; comm [inst][link]).
+    Returns makespan, idle [n][P], bub_num, bub_den, peak [n][P], status and
+    optionally op_start / op_end [n][P][2][M]."""
+    lib = lib or load()
+    M = MA + MB
+    cf = np.ascontiguousarray(cost_f, np.int32)
+    cb = np.ascontiguousarray(cost_b, np.int32)
+    cm = None if comm is None else np.ascontiguousarray(comm, np.int32)
+    out = dict(makespan=np.zeros(n, np.int64), idle=np.zeros((n, P), np.int64),
+               bub_num=np.zeros(n, np.int64), bub_den=np.zeros(n, np.int64),
+               peak=np.zeros((n, P), np.int32), status=np.zeros(n, np.int8))
+    os_ = oe = None
+    if op_times:
+        os_ = np.zeros((n, P, 2, M), np.int64)
+        oe = np.zeros((n, P, 2, M), np.int64)
+    rc = lib.orc_dp_batch(P, MA, MB, n, _ptr(cf), _ptr(cb), strides[0], strides[1], strides[2], _ptr(cm),
+                          comm_strides[0], comm_strides[1], _ptr(out["makespan"]), _ptr(out["idle"]),
+                          _ptr(out["bub_num"]), _ptr(out["bub_den"]), _ptr(out["peak"]), _ptr(out["status"]),
+                          _ptr(os_), _ptr(oe), nthreads)
+    if rc != OK:
+        raise OracleError(rc, "dp_batch")
     if op_times:
         out["op_start"], out["op_end"] = os_, oe
     return out

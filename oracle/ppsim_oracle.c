@@ -27,6 +27,9 @@
  *   5. the validity checks [M040] §08 lists (no overlap on a device, every B
  *      has its F before it, gradients flow back, every device runs M*v F and
  *      M*v B).
+ * Further schedules whose order depends on the costs, each simulated event by
+ * event: Zero Bubble ZB1P / ZB2P (orc_zb_inst) and DualPipe's two routes
+ * (orc_dp_inst); their readings are stated at their sections below.
  *
  * Readings taken where the pages are silent (each listed in the design notes):
  *   - GPipe backward order is last-in-first-out (D..A), from [M040] §02's table.
@@ -1411,6 +1414,311 @@ int orc_zb_batch(int policy, int P, int M, int64_t n,
     if (nthreads == 1) zb_worker(&jobs[0]);
     else {
         for (int t = 0; t < nthreads; ++t) pthread_create(&th[t], NULL, zb_worker, &jobs[t]);
+        for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+    }
+    for (int t = 0; t < nthreads; ++t) if (jobs[t].rc) return jobs[t].rc;
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* DualPipe: two routes through the same stages in opposite directions       */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * [GPipe->ZB] "DualPipe (DeepSeek-V3)": with P devices and the model cut into
+ * P blocks of layers, one group of microbatches enters at device 0 and runs
+ * blocks 0..P-1 on devices 0..P-1 (route A); the other group enters at device
+ * P-1 and runs the same blocks in the same order on devices P-1..0 (route B).
+ * So device d holds block d for route A and block P-1-d for route B (two
+ * copies of the parameters), and a device that waits for one route's input
+ * can run the other route's ready op.  The page leaves the merged order to the
+ * original authors; the reading taken here:
+ *   - route A carries microbatches 0..MA-1, route B microbatches MA..MA+MB-1;
+ *   - on each route every stage keeps its 1F1B order ([1F1B] §2.3/§3.2):
+ *     F^w (B F)^(Mr-w) B^w with w = min(P - s, Mr) at stage s of a route with
+ *     Mr microbatches;
+ *   - a device that is free at tick t runs an op whose input has arrived by t,
+ *     taken from the front of either route's order; when both fronts are
+ *     ready it takes a backward before a forward and, between two ops of the
+ *     same kind, the route in which it is the earlier stage (route A when d <=
+ *     P-1-d); when neither is ready it waits for the first arrival;
+ *   - comm[l] is the latency of the link between devices l and l+1, the same
+ *     for both routes and both directions; it occupies neither device;
+ *   - costs are per (block s, microbatch g): F and B of microbatch g on block s
+ *     take tf[s][g], tb[s][g] ticks wherever the block runs.  F and B costs
+ *     are at least 1 tick, so whether an input "has arrived by t" depends on
+ *     the costs alone and not on the order in which simultaneous decisions are
+ *     taken;
+ *   - the ledger counts held activations per device: +1 at each F, -1 at
+ *     each B of either route.
+ * Op times are stored by (block s, kind, microbatch g): index (s*2 + kind)*M + g.
+ */
+typedef struct {
+    int P, MA, MB, M;
+    const int64_t *tf, *tb, *comm;
+    int64_t *start, *end;
+    int nf[2][16], nb[2][16];
+} dp_sim;
+
+static int dp_stage(int P, int route, int d) { return route == 0 ? d : P - 1 - d; }
+
+static int dp_link(int P, int route, int b)   /* link of the boundary between blocks b and b+1 */
+{
+#if ORC_MUTANT == 15  /* mistake: route B crosses the boundary on route A's link */
+    (void)P; (void)route;
+    return b;
+#else
+    return route == 0 ? b : P - 2 - b;
+#endif
+}
+
+/* The front of route r's order on device d: 1 with *isF, *g (global
+ * microbatch) and *s (block), or 0 when the route is done on d. */
+static int dp_front(const dp_sim *z, int r, int d, int *isF, int *g, int *s)
+{
+    int Mr = r == 0 ? z->MA : z->MB, st = dp_stage(z->P, r, d);
+    int w = z->P - st < Mr ? z->P - st : Mr;
+    int nf = z->nf[r][d], nb = z->nb[r][d], q = nf + nb - w;
+    if (nf + nb == 2 * Mr) return 0;
+    *isF = q < 0 || (q < 2 * (Mr - w) && (q & 1));
+    *g = (r == 0 ? 0 : z->MA) + (*isF ? nf : nb);
+    *s = st;
+    return 1;
+}
+
+/* Arrival tick of the input of op (route r, block s, kind, microbatch g), or
+ * -1 while a producer is not placed. */
+static int64_t dp_arrival(const dp_sim *z, int r, int s, int isF, int g)
+{
+    int P = z->P, M = z->M;
+    if (isF) {
+        if (s == 0) return 0;
+        int64_t e = z->end[((s - 1) * 2 + ORC_F) * M + g];
+        return e < 0 ? -1 : e + (z->comm ? z->comm[dp_link(P, r, s - 1)] : 0);
+    }
+    int64_t a = z->end[(s * 2 + ORC_F) * M + g];   /* its own forward, on the same device */
+    if (a < 0) return -1;
+    if (s < P - 1) {
+        int64_t e = z->end[((s + 1) * 2 + ORC_B) * M + g];
+        if (e < 0) return -1;
+        e += z->comm ? z->comm[dp_link(P, r, s)] : 0;
+        if (e > a) a = e;
+    }
+    return a;
+}
+
+int orc_dp_inst(int P, int MA, int MB, const int64_t *tf, const int64_t *tb, const int64_t *comm,
+                int64_t *start, int64_t *end, int64_t *makespan, int64_t *busy, int64_t *idle,
+                int64_t *bub, int *peak)
+{
+    if (P < 1 || P > 16 || MA < 0 || MB < 0 || MA + MB < 1) return ORC_ERR_ARG;
+    int M = MA + MB;
+    for (int q = 0; q < P * M; ++q)
+        if (tf[q] < 1 || tb[q] < 1) return ORC_ERR_ARG;
+    dp_sim z;
+    memset(&z, 0, sizeof(z));
+    z.P = P; z.MA = MA; z.MB = MB; z.M = M;
+    z.tf = tf; z.tb = tb; z.comm = comm; z.start = start; z.end = end;
+    int64_t t_free[16];
+    int held[16];
+    for (int d = 0; d < P; ++d) { t_free[d] = 0; held[d] = 0; peak[d] = 0; busy[d] = 0; }
+    for (int q = 0; q < 2 * P * M; ++q) { start[q] = -1; end[q] = -1; }
+    int64_t T = 0;
+    for (;;) {
+        /* every device free by T takes the op the rules give it at T; what it
+         * places ends after T, so no decision at T sees another one */
+        for (int d = 0; d < P; ++d) {
+            if (t_free[d] > T) continue;
+            int best = -1, bF = 0, bg = 0, bs = 0;
+            int pref = d <= P - 1 - d ? 0 : 1;
+            for (int k = 0; k < 2; ++k) {
+                int r = k == 0 ? pref : 1 - pref;   /* preferred route first */
+                int isF, g, s;
+                if (!dp_front(&z, r, d, &isF, &g, &s)) continue;
+                int64_t a = dp_arrival(&z, r, s, isF, g);
+                if (a < 0 || a > T) continue;
+#if ORC_MUTANT == 14  /* mistake: a ready forward goes before a ready backward */
+                if (best < 0 || (isF && !bF)) { best = r; bF = isF; bg = g; bs = s; }
+#else
+                if (best < 0 || (!isF && bF)) { best = r; bF = isF; bg = g; bs = s; }
+#endif
+            }
+            if (best < 0) continue;
+            int idx = (bs * 2 + (bF ? ORC_F : ORC_B)) * M + bg;
+            int64_t c = bF ? tf[bs * M + bg] : tb[bs * M + bg];
+            start[idx] = T;
+            end[idx] = T + c;
+            t_free[d] = T + c;
+            busy[d] += c;
+            if (bF) { z.nf[best][d]++; held[d]++; if (held[d] > peak[d]) peak[d] = held[d]; }
+            else { z.nb[best][d]++; held[d]--; }
+        }
+        /* the next tick at which something can change: a device becomes free,
+         * or an input a free device waits for arrives */
+        int64_t next = -1;
+        int left = 0;
+        for (int d = 0; d < P; ++d) {
+            int isF, g, s, any = 0;
+            for (int r = 0; r < 2; ++r) {
+                if (!dp_front(&z, r, d, &isF, &g, &s)) continue;
+                any = 1;
+                if (t_free[d] > T) continue;
+                int64_t a = dp_arrival(&z, r, s, isF, g);
+                if (a > T && (next < 0 || a < next)) next = a;
+            }
+            if (!any) continue;
+            left = 1;
+            if (t_free[d] > T && (next < 0 || t_free[d] < next)) next = t_free[d];
+        }
+        if (!left) break;
+        if (next < 0) return ORC_ERR_DEADLOCK;
+        T = next;
+    }
+    /* validity ([M040] §08): every op placed, no overlap on a device, every
+     * input arrived before its op starts, every B after its F */
+    for (int d = 0; d < P; ++d) {
+        /* the device's ops in start order: collect and check pairwise */
+        for (int r = 0; r < 2; ++r)
+            for (int r2 = 0; r2 < 2; ++r2) {
+                int s = dp_stage(P, r, d), s2 = dp_stage(P, r2, d);
+                int g0 = r == 0 ? 0 : MA, g1 = r == 0 ? MA : M;
+                int h0 = r2 == 0 ? 0 : MA, h1 = r2 == 0 ? MA : M;
+                for (int g = g0; g < g1; ++g)
+                    for (int kd = 0; kd < 2; ++kd) {
+                        int64_t a0 = start[(s * 2 + kd) * M + g], a1 = end[(s * 2 + kd) * M + g];
+                        if (a0 < 0 || a1 < a0) return ORC_ERR_INVARIANT;
+                        for (int h = h0; h < h1; ++h)
+                            for (int kd2 = 0; kd2 < 2; ++kd2) {
+                                if (r == r2 && g == h && kd == kd2) continue;
+                                int64_t b0 = start[(s2 * 2 + kd2) * M + h], b1 = end[(s2 * 2 + kd2) * M + h];
+                                if (a0 < b1 && b0 < a1) return ORC_ERR_INVARIANT;
+                            }
+                    }
+            }
+    }
+    for (int r = 0; r < 2; ++r) {
+        int g0 = r == 0 ? 0 : MA, g1 = r == 0 ? MA : M;
+        for (int g = g0; g < g1; ++g)
+            for (int s = 0; s < P; ++s) {
+                int64_t fs = start[(s * 2 + ORC_F) * M + g], fe = end[(s * 2 + ORC_F) * M + g];
+                int64_t bs = start[(s * 2 + ORC_B) * M + g];
+                if (bs < fe) return ORC_ERR_INVARIANT;
+                if (s > 0 && fs < end[((s - 1) * 2 + ORC_F) * M + g] + (comm ? comm[dp_link(P, r, s - 1)] : 0))
+                    return ORC_ERR_INVARIANT;
+                if (s < P - 1 && bs < end[((s + 1) * 2 + ORC_B) * M + g] + (comm ? comm[dp_link(P, r, s)] : 0))
+                    return ORC_ERR_INVARIANT;
+            }
+    }
+    int64_t mk = 0, num = 0;
+    for (int q = 0; q < 2 * P * M; ++q) if (end[q] > mk) mk = end[q];
+    for (int d = 0; d < P; ++d) { idle[d] = mk - busy[d]; num += idle[d]; }
+    *makespan = mk;
+    bub[0] = num;
+    bub[1] = (int64_t)P * mk;
+    return ORC_OK;
+}
+
+typedef struct {
+    int P, MA, MB;
+    const int32_t *cost_f, *cost_b;
+    int64_t cs_inst, cs_stage, cs_mb;
+    const int32_t *comm;
+    int64_t ms_inst, ms_link;
+    int64_t *makespan, *idle, *bub_num, *bub_den;
+    int32_t *peak;                       /* [n][P] */
+    int8_t *status;
+    int64_t *op_start, *op_end;          /* [n][P][2][M] or NULL */
+    int64_t lo, hi;
+    int rc;
+} orc_dp_job;
+
+static void *dp_worker(void *arg)
+{
+    orc_dp_job *jb = (orc_dp_job *)arg;
+    int P = jb->P, M = jb->MA + jb->MB, n2 = 2 * P * M;
+    int64_t *tf = (int64_t *)malloc((size_t)P * M * sizeof(int64_t));
+    int64_t *tb = (int64_t *)malloc((size_t)P * M * sizeof(int64_t));
+    int64_t *cm = (int64_t *)malloc((size_t)(P > 1 ? P - 1 : 1) * sizeof(int64_t));
+    int64_t *st = (int64_t *)malloc((size_t)n2 * sizeof(int64_t));
+    int64_t *en = (int64_t *)malloc((size_t)n2 * sizeof(int64_t));
+    int64_t busy[16], idle[16];
+    int peak[16];
+    jb->rc = ORC_OK;
+    if (!tf || !tb || !cm || !st || !en) { jb->rc = ORC_ERR_NOMEM; goto out; }
+    for (int64_t x = jb->lo; x < jb->hi; ++x) {
+        int neg = 0, zero = 0;
+        for (int s = 0; s < P; ++s)
+            for (int g = 0; g < M; ++g) {
+                int64_t off = x * jb->cs_inst + s * jb->cs_stage + g * jb->cs_mb;
+                tf[s * M + g] = jb->cost_f[off];
+                tb[s * M + g] = jb->cost_b[off];
+                if (tf[s * M + g] < 0 || tb[s * M + g] < 0) neg = 1;
+                if (tf[s * M + g] < 1 || tb[s * M + g] < 1) zero = 1;
+            }
+        for (int l = 0; l < P - 1; ++l) {
+            cm[l] = jb->comm ? jb->comm[x * jb->ms_inst + l * jb->ms_link] : 0;
+            if (cm[l] < 0) neg = 1;
+        }
+        int64_t mk = 0, bub[2] = {0, 0};
+        int8_t status = neg ? ORC_ST_NEG_COST : (zero ? ORC_ST_ZERO_COST : ORC_ST_OK);
+        if (status == ORC_ST_OK) {
+            int rc = orc_dp_inst(P, jb->MA, jb->MB, tf, tb, cm, st, en, &mk, busy, idle, bub, peak);
+            if (rc) { jb->rc = rc; goto out; }
+            if (mk > ORC_INT32_MAX) status = ORC_ST_OVERFLOW;
+        } else {
+            for (int q = 0; q < n2; ++q) { st[q] = 0; en[q] = 0; }
+            for (int d = 0; d < P; ++d) { idle[d] = 0; peak[d] = 0; }
+        }
+        if (jb->status) jb->status[x] = status;
+        jb->makespan[x] = mk;
+        for (int d = 0; d < P; ++d) {
+            jb->idle[x * P + d] = idle[d];
+            if (jb->peak) jb->peak[x * P + d] = peak[d];
+        }
+        jb->bub_num[x] = bub[0];
+        jb->bub_den[x] = bub[1];
+        if (jb->op_start)
+            for (int q = 0; q < n2; ++q) {
+                jb->op_start[x * n2 + q] = st[q];
+                jb->op_end[x * n2 + q] = en[q];
+            }
+    }
+out:
+    free(tf); free(tb); free(cm); free(st); free(en);
+    return NULL;
+}
+
+/* Evaluate n DualPipe instances (route A: microbatches 0..MA-1, route B:
+ * MA..MA+MB-1).  Costs are int32 [inst][block][microbatch] through element
+ * strides; comm int32 [inst][link] or NULL.  Outputs as orc_zb_batch, with
+ * op times [n][P blocks][2 kinds][M]. */
+int orc_dp_batch(int P, int MA, int MB, int64_t n,
+                 const int32_t *cost_f, const int32_t *cost_b,
+                 int64_t cs_inst, int64_t cs_stage, int64_t cs_mb,
+                 const int32_t *comm, int64_t ms_inst, int64_t ms_link,
+                 int64_t *makespan, int64_t *idle, int64_t *bub_num, int64_t *bub_den,
+                 int32_t *peak, int8_t *status, int64_t *op_start, int64_t *op_end, int nthreads)
+{
+    if (P < 1 || P > 16 || MA < 0 || MB < 0 || MA + MB < 1 || n < 0) return ORC_ERR_ARG;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if ((int64_t)nthreads > n) nthreads = n > 0 ? (int)n : 1;
+    orc_dp_job jobs[256];
+    pthread_t th[256];
+    for (int t = 0; t < nthreads; ++t) {
+        orc_dp_job *jb = &jobs[t];
+        jb->P = P; jb->MA = MA; jb->MB = MB;
+        jb->cost_f = cost_f; jb->cost_b = cost_b;
+        jb->cs_inst = cs_inst; jb->cs_stage = cs_stage; jb->cs_mb = cs_mb;
+        jb->comm = comm; jb->ms_inst = ms_inst; jb->ms_link = ms_link;
+        jb->makespan = makespan; jb->idle = idle; jb->bub_num = bub_num; jb->bub_den = bub_den;
+        jb->peak = peak; jb->status = status; jb->op_start = op_start; jb->op_end = op_end;
+        jb->lo = n * t / nthreads; jb->hi = n * (t + 1) / nthreads;
+        jb->rc = ORC_OK;
+    }
+    if (nthreads == 1) dp_worker(&jobs[0]);
+    else {
+        for (int t = 0; t < nthreads; ++t) pthread_create(&th[t], NULL, dp_worker, &jobs[t]);
         for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
     }
     for (int t = 0; t < nthreads; ++t) if (jobs[t].rc) return jobs[t].rc;

@@ -566,6 +566,8 @@ MUTANTS = {
     11: "ZB admits an F at the activation limit",
     12: "backward edges take the forward latency",
     13: "interleaved warmup one forward too long",
+    14: "DualPipe runs a ready forward before a ready backward",
+    15: "DualPipe route B crosses a boundary on route A's link",
 }
 
 
@@ -662,6 +664,22 @@ def _pin_suite(orc, lib):
                 and list(r["peak"]) == want)
 
     check("ilv_warmup", ilv_warmup)
+
+    def dualpipe():
+        from test_oracle_dualpipe import dp_tick_sim
+        rng = np.random.default_rng(8)
+        for P, MA, MB in ((4, 5, 4), (3, 2, 4), (6, 7, 7)):
+            M = MA + MB
+            tf = rng.integers(1, 5, size=(P, M))
+            tb = rng.integers(1, 5, size=(P, M))
+            cm = rng.integers(0, 4, size=P - 1)
+            r = orc.dp_evaluate(P, MA, MB, tf, tb, cm, lib=lib)
+            if not np.array_equal(r["start"], dp_tick_sim(P, MA, MB, tf, tb, cm)[0]):
+                return False
+        r = orc.dp_evaluate(8, 16, 16, 1, 2, lib=lib)
+        return list(r["idle"]) == [3 * 5] * 8
+
+    check("dualpipe", dualpipe)
     return failed
 
 
