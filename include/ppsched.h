@@ -368,6 +368,45 @@ int pp_sched_partition_search_interleaved(const int32_t *layer_tf, const int32_t
                                           int64_t *best_idx, int32_t *best_makespan, int32_t *best_cuts,
                                           int32_t *all_makespan, cudaStream_t stream);
 
+/* Evaluate n_instances DualPipe schedule instances: two routes through the
+ * same P blocks of layers in opposite directions.  [GPipe->ZB] "DualPipe
+ * (DeepSeek-V3)": microbatches 0..m_a-1 (route A) enter at device 0 and run
+ * blocks 0..P-1 on devices 0..P-1; microbatches m_a..M-1 (route B) enter at
+ * device P-1 and run the same blocks on devices P-1..0, so device d holds
+ * block d of route A and block P-1-d of route B (two parameter copies).  The
+ * page names the layout and its costs (peak p+1 activations, parameters x2)
+ * but not the merged order; the library's reading:
+ *   - at each of its stages a route keeps its 1F1B order F^w (B F)^(Mr-w) B^w,
+ *     w = min(P - stage, Mr), Mr its microbatch count;
+ *   - a device free at tick t runs an op at the front of either route whose
+ *     input has arrived by t: a backward before a forward, and between two
+ *     ops of one kind the route in which the device is the earlier stage
+ *     (route A when d <= P-1-d); with neither input arrived it waits for the
+ *     first arrival;
+ *   - F and B costs must be at least 1 tick (else PP_ST_ZERO_COST).
+ * The order depends on the costs, so there is no plan.
+ *
+ * Inputs (device, int32): cost_f, cost_b of (instance x, block s, microbatch
+ *   g) at x*stride_inst + s*stride_stage + g*stride_mb (strides may be 0);
+ *   comm of (instance x, link l), the latency between devices l and l+1 in
+ *   both directions, at x*comm_stride_inst + l*comm_stride_link, NULL means 0.
+ * Outputs (device; each may be NULL):
+ *   makespan [n], idle [n][P], bub_num [n], bub_den [n]  as pp_sched_eval
+ *   peak [n][P]      most activations held at once per device (+1 at F, -1 at B
+ *                    of either route); it depends on the costs, hence per instance
+ *   op_start, op_end op (block s, kind k (0 F, 1 B), microbatch g) of instance x
+ *                    at x*op_stride_inst + ((s*2 + k)*M + g)*op_stride_op
+ *   status [n]       PP_ST_* (negative cost or comm first, then a zero F/B
+ *                    cost, then overflow)
+ * Limits: 1 <= P <= PP_MAX_P, 1 <= M <= PP_MAX_MV, 0 <= m_a <= M.
+ * Errors: PP_ERR_ARG, PP_ERR_SIZE, PP_ERR_CUDA. */
+int pp_sched_eval_dualpipe(int P, int M, int m_a, const int32_t *cost_f, const int32_t *cost_b,
+                           int64_t stride_inst, int64_t stride_stage, int64_t stride_mb,
+                           const int32_t *comm, int64_t comm_stride_inst, int64_t comm_stride_link,
+                           int64_t n_instances, int32_t *makespan, int32_t *idle, int64_t *bub_num,
+                           int64_t *bub_den, int32_t *peak, int32_t *op_start, int32_t *op_end,
+                           int64_t op_stride_inst, int64_t op_stride_op, int8_t *status, cudaStream_t stream);
+
 /* pp_sched_eval for GPipe and 1F1B that allocates no device memory.  (This
  * entry point has no counterpart on the pages; it exists for callers that
  * cannot let a library call cudaMalloc, e.g. code whose device memory belongs to

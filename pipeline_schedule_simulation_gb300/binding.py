@@ -25,7 +25,7 @@ EXPORTS = ("pp_sched_plan", "pp_sched_plan_info", "pp_sched_plan_ops", "pp_sched
            "pp_sched_cache_clear", "pp_sched_eval_noalloc", "pp_sched_eval_zb",
            "pp_sched_partition_search_ranks", "pp_sched_partition_search_interleaved", "pp_sched_eval_fb",
            "pp_sched_eval_host", "pp_sched_eval_host_workspace", "pp_sched_many_prepare", "pp_sched_many_eval",
-           "pp_sched_many_info", "pp_sched_many_destroy")
+           "pp_sched_many_info", "pp_sched_many_destroy", "pp_sched_eval_dualpipe")
 
 
 class Problem(ctypes.Structure):
@@ -93,6 +93,9 @@ def _load():
     lib.pp_sched_eval_zb.argtypes = [i32, i32, i32, vp, vp, vp, i64, i64, i64, vp, i64, i64, i64,
                                      vp, vp, vp, vp, vp, vp, vp, i64, i64, vp, vp]
     lib.pp_sched_eval_zb.restype = i32
+    lib.pp_sched_eval_dualpipe.argtypes = [i32, i32, i32, vp, vp, i64, i64, i64, vp, i64, i64, i64,
+                                           vp, vp, vp, vp, vp, vp, vp, i64, i64, vp, vp]
+    lib.pp_sched_eval_dualpipe.restype = i32
     lib.pp_sched_eval_host.argtypes = [i32, i32, i32, i32, vp, vp, vp, i64, vp, ctypes.c_size_t,
                                        vp, vp, vp, vp, vp, vp, vp]
     lib.pp_sched_eval_host.restype = i32
@@ -214,6 +217,48 @@ def evaluate(policy, P, M, v, cost_f, cost_b, strides, n, comm=None, comm_stride
                            _ptr(mk), _ptr(idle), _ptr(bn), _ptr(bd), _ptr(pk), _ptr(os_), _ptr(oe),
                            op_strides[0], op_strides[1], _ptr(stt), _stream(stream))
     _check(rc, "pp_sched_eval")
+    return out
+
+
+def evaluate_dualpipe(P, M, m_a, cost_f, cost_b, strides, n, comm=None, comm_strides=(0, 0),
+                      outputs=("makespan", "idle", "bub_num", "bub_den", "peak", "status"),
+                      op_times=False, op_strides=None, out=None, stream=None):
+    """Call pp_sched_eval_dualpipe on DEVICE tensors: microbatches 0..m_a-1
+    enter at device 0, m_a..M-1 at device P-1.
+
+    cost_f / cost_b are indexed (instance, block, microbatch) through the
+    element strides; comm (instance, link).  Returns a dict of CUDA tensors;
+    `peak` is per instance [n][P].  op_times adds op_start / op_end
+    [n][P blocks][2][M] (kind 0 = F, 1 = B), or through op_strides = (inst, op)."""
+    dev = cost_f.device
+    out = dict(out or {})
+
+    def want(name, shape, dtype):
+        if name in out:
+            return out[name]
+        t = torch.empty(shape, dtype=dtype, device=dev)
+        out[name] = t
+        return t
+
+    mk = want("makespan", (n,), torch.int32) if "makespan" in outputs else None
+    idle = want("idle", (n, P), torch.int32) if "idle" in outputs else None
+    bn = want("bub_num", (n,), torch.int64) if "bub_num" in outputs else None
+    bd = want("bub_den", (n,), torch.int64) if "bub_den" in outputs else None
+    pk = want("peak", (n, P), torch.int32) if "peak" in outputs else None
+    stt = want("status", (n,), torch.int8) if "status" in outputs else None
+    os_ = oe = None
+    if op_times:
+        os_ = want("op_start", (n, P, 2, M), torch.int32)
+        oe = want("op_end", (n, P, 2, M), torch.int32)
+        if op_strides is None:
+            op_strides = (P * 2 * M, 1)
+    else:
+        op_strides = (0, 0)
+    rc = LIB.pp_sched_eval_dualpipe(P, M, m_a, _ptr(cost_f), _ptr(cost_b), strides[0], strides[1], strides[2],
+                                    _ptr(comm), comm_strides[0], comm_strides[1], n, _ptr(mk), _ptr(idle),
+                                    _ptr(bn), _ptr(bd), _ptr(pk), _ptr(os_), _ptr(oe), op_strides[0],
+                                    op_strides[1], _ptr(stt), _stream(stream))
+    _check(rc, "pp_sched_eval_dualpipe")
     return out
 
 

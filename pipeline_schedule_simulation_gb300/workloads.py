@@ -192,6 +192,15 @@ def hetero_zb(policy=ZB1P, n=65536, seed=6, P=8, M=64):
                  meta={"workload": f"{name}_hetero_P{P}_M{M}_n{n}"}, cost_w=cw.reshape(-1))
 
 
+def hetero_dualpipe(n=65536, seed=7, P=8, M=64):
+    """Heterogeneous DualPipe batch: the 1F1B batch's distributions (t_f ~
+    U[80,120], t_b ~ U[160,240] per (instance, block, microbatch), comm ~
+    U[2,8] per (instance, link)), half of the microbatches on each route."""
+    b = hetero_1f1b(n=n, seed=seed, P=P, M=M)
+    b.meta = {"workload": f"dualpipe_hetero_P{P}_M{M}_n{n}", "m_a": (M + 1) // 2}
+    return b
+
+
 def random_zb(policy, P, M, n, seed, lo=1, hi=9, w_lo=0, w_hi=9, comm_hi=4, layout="inst_minor", pad_to=1):
     """Small random Zero Bubble instances for parity tests (F, B in [lo, hi],
     W in [w_lo, w_hi], comm in [0, comm_hi])."""

@@ -93,3 +93,16 @@ def assert_same_zb(gpu, ref, select=None, op_times=False):
     if op_times:
         assert np.array_equal(g["op_start"][ok], ref["op_start"][ok])
         assert np.array_equal(g["op_end"][ok], ref["op_end"][ok])
+
+
+def run_gpu_dp(batch, m_a, op_times=False):
+    from pipeline_schedule_simulation_gb300 import binding as B
+    out = B.evaluate_dualpipe(batch.P, batch.M, m_a, to_dev(batch.cost_f), to_dev(batch.cost_b), batch.strides,
+                              batch.n, comm=to_dev(batch.comm), comm_strides=batch.comm_strides, op_times=op_times)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def run_oracle_dp(orc, batch, m_a, op_times=False, nthreads=8):
+    return orc.dp_batch(batch.P, m_a, batch.M - m_a, batch.cost_f, batch.cost_b, batch.strides, comm=batch.comm,
+                        comm_strides=batch.comm_strides, n=batch.n, op_times=op_times, nthreads=nthreads)

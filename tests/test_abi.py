@@ -95,6 +95,19 @@ def test_one_past_each_limit_is_refused_without_gpu():
     assert L.pp_sched_eval_zb(B.ZB2P, 17, 8, 8, 8, 8, 1, 0, 0, nul, 0, 0, 4, nul, nul, nul, nul, nul,
                               nul, nul, 0, 0, nul, nul) == B.PP_ERR_SIZE
 
+    def dp(P, M, m_a, n=4, f=8, si=1):
+        return L.pp_sched_eval_dualpipe(P, M, m_a, f, f, si, 0, 0, nul, 0, 0, n, nul, nul, nul, nul, nul,
+                                        nul, nul, 0, 0, nul, nul)
+    assert dp(0, 8, 4) == B.PP_ERR_ARG             # P < 1
+    assert dp(4, 0, 0) == B.PP_ERR_ARG             # M < 1
+    assert dp(4, 8, 9) == B.PP_ERR_ARG             # route A larger than M
+    assert dp(4, 8, -1) == B.PP_ERR_ARG
+    assert dp(4, 8, 4, n=-1) == B.PP_ERR_ARG
+    assert dp(4, 8, 4, f=0) == B.PP_ERR_ARG        # NULL costs with n > 0
+    assert dp(4, 8, 4, si=-1) == B.PP_ERR_ARG
+    assert dp(17, 8, 4) == B.PP_ERR_SIZE
+    assert dp(16, 32769, 4) == B.PP_ERR_SIZE
+
     def ps(L_, P, M):
         return L.pp_sched_partition_search(8, 8, 8, L_, P, M, 0, 0, 0, 0, 10, 8, 8, 8, nul, nul)
 
