@@ -494,6 +494,20 @@ def secondary(B, W, torch, stream):
         out[f"{name}_P8_M64_n{N_INST}"] = {"op_times_per_s": bz.op_times / t, "ms": t * 1e3,
                                            "mean_makespan": float(zout["makespan"].float().mean().item())}
         del f, g, w, c, zout
+    bd = W.hetero_dualpipe(n=N_INST)
+    m_a = bd.meta["m_a"]
+    f, g, c = (torch.from_numpy(x).cuda() for x in (bd.cost_f, bd.cost_b, bd.comm))
+    dout = B.evaluate_dualpipe(P, M, m_a, f, g, bd.strides, N_INST, comm=c, comm_strides=bd.comm_strides,
+                               stream=stream)
+    t = timed(lambda: B.evaluate_dualpipe(P, M, m_a, f, g, bd.strides, N_INST, comm=c,
+                                          comm_strides=bd.comm_strides, out=dout, stream=stream), 10)
+    one = B.evaluate(1, P, M, 1, f, g, bd.strides, N_INST, comm=c, comm_strides=bd.comm_strides, stream=stream)
+    out[f"dualpipe_P8_M64_n{N_INST}"] = {
+        "op_times_per_s": bd.op_times / t, "ms": t * 1e3, "microbatches_per_route": [m_a, M - m_a],
+        "mean_makespan": float(dout["makespan"].double().mean().item()),
+        "mean_makespan_1f1b_same_costs": float(one["makespan"].double().mean().item()),
+        "max_peak": int(dout["peak"].max().item())}
+    del f, g, c, dout, one
     out["closed_form_sweep"] = closed_form_sweep(B, W, torch, stream, timed)
     p = W.layer_split()
     lt, lb, la = (torch.from_numpy(x).cuda() for x in (p.layer_tf, p.layer_tb, p.layer_act))

@@ -87,30 +87,28 @@ __global__ void __launch_bounds__(128) k_eval_dp(const EvalArgs a, int MA, int32
     const int P = a.P, M = a.M, MB = M - MA;
     const bool dev = x < a.n && d < P;  // this lane simulates a device
 
-    // per-lane constants of the two routes: block (= stage index on the
-    // route), microbatches, warmup, first global microbatch
-    const int blk[2] = {d, P - 1 - d};
-    const int Mr[2] = {MA, MB};
-    const int wr[2] = {min(P - d, MA), min(d + 1, MB)};
-    const int g0[2] = {0, MA};
-    const int pref = d <= P - 1 - d ? 0 : 1;
+    // per-lane constants of the two routes (A, B): block (= stage index on
+    // the route), microbatches, warmup, first global microbatch
+    const int blkA = d, blkB = P - 1 - d, MB_ = MB;
+    const int wA = min(P - d, MA), wB = min(d + 1, MB);
+    const bool prefA = d <= P - 1 - d;
     uint32_t cmL = 0, cmR = 0, ncomm = 0;
     if (dev && a.comm) {
         if (d > 0) cmL = (uint32_t)a.comm[x * a.c_inst + (int64_t)(d - 1) * a.c_bnd];
         if (d < P - 1) cmR = (uint32_t)a.comm[x * a.c_inst + (int64_t)d * a.c_bnd];
         ncomm = cmL | cmR;
     }
-    // stream q = route * 2 + kind (0 F, 1 B)
-    const int32_t *src[4];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int64_t row = dev ? x * a.s_inst + (int64_t)blk[r] * a.s_stage + (int64_t)g0[r] * a.s_mb : 0;
-        src[2 * r] = a.cost_f + row;
-        src[2 * r + 1] = a.cost_b + row;
-    }
+    // stream q = route * 2 + kind (0 F, 1 B); srcA / srcB: element offset of
+    // the route's first microbatch in its block's cost rows
+    const int64_t srcA = dev ? x * a.s_inst + (int64_t)blkA * a.s_stage : 0;
+    const int64_t srcB = dev ? x * a.s_inst + (int64_t)blkB * a.s_stage + (int64_t)MA * a.s_mb : 0;
     auto fetch = [&](int q, int i) {
-        if (dev && i < Mr[q >> 1])
-            cp_async4(smem_addr(cring + (q * G::kRing + i % G::kRing) * 32 + lane), src[q] + (int64_t)i * a.s_mb, 4);
+        const bool rb = q >= 2;
+        if (dev && i < (rb ? MB_ : MA)) {
+            const int32_t *base = (q & 1) ? a.cost_b : a.cost_f;
+            cp_async4(smem_addr(cring + (q * G::kRing + i % G::kRing) * 32 + lane),
+                      base + (rb ? srcB : srcA) + (int64_t)i * a.s_mb, 4);
+        }
     };
 #pragma unroll 1
     for (int i = 0; i < G::kAheadC; ++i)
@@ -125,7 +123,7 @@ __global__ void __launch_bounds__(128) k_eval_dp(const EvalArgs a, int MA, int32
     };
 
     uint32_t T = 0, tfree = 0, busy = 0, flag = 0, zero = 0;
-    int nf[2] = {0, 0}, nb[2] = {0, 0};
+    int nfA = 0, nbA = 0, nfB = 0, nbB = 0;
     int held = 0, peak = 0;
     // the neighbours' counts: from the left lane its route-A forwards and
     // route-B backwards, from the right lane its route-A backwards and route-B
@@ -139,30 +137,31 @@ __global__ void __launch_bounds__(128) k_eval_dp(const EvalArgs a, int MA, int32
         __syncwarp();
         // ---- the fronts of both routes: present, kind, local microbatch,
         // input known, arrival tick
-        bool has[2], isF[2], known[2];
-        int mi[2];
-        uint32_t arr[2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            dp_front(nf[r], nb[r], Mr[r], wr[r], has[r], isF[r], mi[r]);
-            const bool first = isF[r] ? blk[r] == 0 : blk[r] == P - 1;  // no producer on another device
-            const int made = r == 0 ? (isF[r] ? nfA_L : nbA_R) : (isF[r] ? nfB_R : nbB_L);
-            known[r] = first || made > mi[r];
-            arr[r] = first ? 0u : ring(r, isF[r] ? 0 : 1, mi[r])[lane];
-        }
-        // ---- decide at T
-        int pick = -1;
+        bool hA, fA, hB, fB;
+        int iA, iB;
+        dp_front(nfA, nbA, MA, wA, hA, fA, iA);
+        dp_front(nfB, nbB, MB_, wB, hB, fB, iB);
+        // no producer on another device: a route's first forward, last backward
+        const bool firstA = fA ? blkA == 0 : blkA == P - 1;
+        const bool firstB = fB ? blkB == 0 : blkB == P - 1;
+        const bool knownA = firstA || (fA ? nfA_L : nbA_R) > iA;
+        const bool knownB = firstB || (fB ? nfB_R : nbB_L) > iB;
+        const uint32_t arrA = firstA ? 0u : ring(0, fA ? 0 : 1, iA)[lane];
+        const uint32_t arrB = firstB ? 0u : ring(1, fB ? 0 : 1, iB)[lane];
+        // ---- decide at T: 0 none, 1 route A, 2 route B
+        int pick = 0;
         if (dev && tfree <= T) {
-            const bool rp = has[pref] && known[pref] && arr[pref] <= T;
-            const bool ro = has[1 - pref] && known[1 - pref] && arr[1 - pref] <= T;
-            if (rp && ro) pick = (isF[pref] && !isF[1 - pref]) ? 1 - pref : pref;
-            else if (rp) pick = pref;
-            else if (ro) pick = 1 - pref;
+            const bool rA = hA && knownA && arrA <= T;
+            const bool rB = hB && knownB && arrB <= T;
+            if (rA && rB) pick = (fA != fB) ? (fA ? 2 : 1) : (prefA ? 1 : 2);
+            else if (rA) pick = 1;
+            else if (rB) pick = 2;
         }
-        // ---- place (predicated on pick >= 0)
-        if (pick >= 0) {
-            const bool f = isF[pick];
-            const int i = mi[pick], q = pick * 2 + (f ? 0 : 1);
+        // ---- place (predicated on pick)
+        if (pick) {
+            const bool rb = pick == 2;
+            const bool f = rb ? fB : fA;
+            const int i = rb ? iB : iA, q = (rb ? 2 : 0) + (f ? 0 : 1);
             const uint32_t c = cring[(q * G::kRing + i % G::kRing) * 32 + lane];
             const uint32_t e = T + c;
             flag |= T | c;
@@ -172,22 +171,28 @@ __global__ void __launch_bounds__(128) k_eval_dp(const EvalArgs a, int MA, int32
             fetch(q, i + G::kAheadC);
             // the consumer: route A forwards go right, backwards left; route B
             // the other way round
-            const bool right = (pick == 0) == f;
-            if (right && d + 1 < P) ring(pick, f ? 0 : 1, i)[lane + G::kIPW] = e + cmR;
-            if (!right && d > 0) ring(pick, f ? 0 : 1, i)[lane - G::kIPW] = e + cmL;
+            uint32_t *row = ring(rb ? 1 : 0, f ? 0 : 1, i);
+            const bool right = rb != f;
+            if (right && d + 1 < P) row[lane + G::kIPW] = e + cmR;
+            if (!right && d > 0) row[lane - G::kIPW] = e + cmL;
             if constexpr (OPS) {
-                const int64_t off = x * a.o_inst + ((int64_t)(blk[pick] * 2 + (f ? 0 : 1)) * M + g0[pick] + i) * a.o_op;
+                const int blk = rb ? blkB : blkA, g = (rb ? MA : 0) + i;
+                const int64_t off = x * a.o_inst + ((int64_t)(blk * 2 + (f ? 0 : 1)) * M + g) * a.o_op;
                 if (a.op_start) a.op_start[off] = (int32_t)T;
                 if (a.op_end) a.op_end[off] = (int32_t)e;
             }
-            if (f) { nf[pick]++; held++; peak = max(peak, held); }
-            else { nb[pick]++; held--; }
+            nfA += !rb && f;
+            nbA += !rb && !f;
+            nfB += rb && f;
+            nbB += rb && !f;
+            held += f ? 1 : -1;
+            peak = max(peak, held);
         }
         cp_async_commit();
         __syncwarp();
         // ---- publish the counts the neighbours' inputs depend on
-        const uint32_t toR = (uint32_t)nf[0] | ((uint32_t)nb[1] << 16);  // read by the right lane
-        const uint32_t toL = (uint32_t)nb[0] | ((uint32_t)nf[1] << 16);  // read by the left lane
+        const uint32_t toR = (uint32_t)nfA | ((uint32_t)nbB << 16);  // read by the right lane
+        const uint32_t toL = (uint32_t)nbA | ((uint32_t)nfB << 16);  // read by the left lane
         const uint32_t fromL = __shfl_up_sync(0xFFFFFFFFu, toR, G::kIPW);
         const uint32_t fromR = __shfl_down_sync(0xFFFFFFFFu, toL, G::kIPW);
         nfA_L = (int)(fromL & 0xFFFFu);
@@ -195,23 +200,23 @@ __global__ void __launch_bounds__(128) k_eval_dp(const EvalArgs a, int MA, int32
         nbA_R = (int)(fromR & 0xFFFFu);
         nfB_R = (int)(fromR >> 16);
         // ---- the instance's next event tick
-        const bool done = !dev || (nf[0] + nb[0] == 2 * MA && nf[1] + nb[1] == 2 * MB);
+        const bool done = !dev || (nfA + nbA == 2 * MA && nfB + nbB == 2 * MB_);
         uint32_t nxt = 0xFFFFFFFFu;
         if (!done) {
             if (tfree > T) {
                 nxt = tfree;
             } else {
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    bool h, fF;
-                    int i;
-                    dp_front(nf[r], nb[r], Mr[r], wr[r], h, fF, i);
-                    const bool first = fF ? blk[r] == 0 : blk[r] == P - 1;
-                    const int made = r == 0 ? (fF ? nfA_L : nbA_R) : (fF ? nfB_R : nbB_L);
-                    if (h && !first && made > i) {
-                        const uint32_t t = ring(r, fF ? 0 : 1, i)[lane];
-                        if (t > T) nxt = min(nxt, t);
-                    }
+                dp_front(nfA, nbA, MA, wA, hA, fA, iA);
+                dp_front(nfB, nbB, MB_, wB, hB, fB, iB);
+                const bool fstA = fA ? blkA == 0 : blkA == P - 1;
+                const bool fstB = fB ? blkB == 0 : blkB == P - 1;
+                if (hA && !fstA && (fA ? nfA_L : nbA_R) > iA) {
+                    const uint32_t t = ring(0, fA ? 0 : 1, iA)[lane];
+                    if (t > T) nxt = min(nxt, t);
+                }
+                if (hB && !fstB && (fB ? nfB_R : nbB_L) > iB) {
+                    const uint32_t t = ring(1, fB ? 0 : 1, iB)[lane];
+                    if (t > T) nxt = min(nxt, t);
                 }
             }
         }
@@ -225,7 +230,7 @@ __global__ void __launch_bounds__(128) k_eval_dp(const EvalArgs a, int MA, int32
     // per-instance reductions over the instance's lanes (as the other
     // evaluators: window = last end tick, idle = window - busy, bubble = total
     // idle over P windows)
-    const bool left_over = dev && (nf[0] + nb[0] < 2 * MA || nf[1] + nb[1] < 2 * MB);
+    const bool left_over = dev && (nfA + nbA < 2 * MA || nfB + nbB < 2 * MB);
     uint32_t mk = dev ? tfree : 0u, fl = flag, zr = zero, nc = ncomm;
     uint32_t cp = capped && left_over ? 1u : 0u;
 #pragma unroll
