@@ -399,6 +399,10 @@ int pp_sched_partition_search_interleaved(const int32_t *layer_tf, const int32_t
  *   status [n]       PP_ST_* (negative cost or comm first, then a zero F/B
  *                    cost, then overflow)
  * Limits: 1 <= P <= PP_MAX_P, 1 <= M <= PP_MAX_MV, 0 <= m_a <= M.
+ * The kernel runs in two exact phases (each lane on its own tick, then the
+ * instances left unfinished on a common tick); the environment variable
+ * PPSCHED_DP_PHASE1_STEPS, read at each call, sets the first phase's step cap
+ * (default 8*M + 64).  The results do not depend on it; only the time does.
  * Errors: PP_ERR_ARG, PP_ERR_SIZE, PP_ERR_CUDA. */
 int pp_sched_eval_dualpipe(int P, int M, int m_a, const int32_t *cost_f, const int32_t *cost_b,
                            int64_t stride_inst, int64_t stride_stage, int64_t stride_mb,

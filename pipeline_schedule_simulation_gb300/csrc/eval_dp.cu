@@ -16,14 +16,15 @@
 //
 // The order depends on the costs, so there is no plan.  One lane per
 // (instance, device), a warp holds 32/PMAX instances (lane = device * 32/PMAX
-// + instance).  The lanes of an instance step through its event ticks
-// together: in a step every lane that is free at the instance's tick T takes
-// the op the rules give it at T (an op placed at T ends after T, so no other
-// decision at T depends on it), then the instance's next tick is the smallest
-// of the busy lanes' free ticks and the known arrivals the free lanes wait for
-// (an arrival not known yet comes after its producer ends, which is itself a
-// candidate).  The ticks increase strictly and each is an op's end or an
-// input's arrival, so an instance takes at most 4*P*M + 1 steps.
+// + instance).  Two phases, both exact:
+//   1. each lane on its own tick, deciding only what the rules already fix
+//      (the Zero Bubble kernel's scheme: a neighbour's published lower bound
+//      on the end of the op a lane waits for proves that its input has not
+//      arrived); capped at cap1 steps (8*M + 64 unless the environment
+//      variable PPSCHED_DP_PHASE1_STEPS sets it; the results do not depend on
+//      it);
+//   2. for instances phase 1 left unfinished, the lanes of the instance step
+//      through its event ticks together, at most 4*P*M + 1 steps.
 //
 // Per warp, in shared memory ([row][lane], conflict-free):
 //   cost rings    [4 streams][kRing]: F and B costs of route A's block and of
@@ -35,6 +36,8 @@
 //                 written by the producing neighbour.  Under 1F1B a producer
 //                 runs at most w <= P ops of a kind ahead of its consumer, so
 //                 kQ = PMAX rows never wrap onto an unread one.
+#include <cstdlib>
+
 #include "eval_common.cuh"
 
 namespace pps {
@@ -76,7 +79,7 @@ static __device__ __noinline__ int8_t dp_classify(const EvalArgs &a, int64_t x) 
 }
 
 template <int PMAX, bool OPS>
-__global__ void __launch_bounds__(128) k_eval_dp(const EvalArgs a, int MA, int32_t *peak_out) {
+__global__ void __launch_bounds__(128) k_eval_dp(const EvalArgs a, int MA, int32_t *peak_out, int cap1) {
     using G = DpGeom<PMAX>;
     extern __shared__ __align__(16) uint32_t dsm[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -122,75 +125,65 @@ __global__ void __launch_bounds__(128) k_eval_dp(const EvalArgs a, int MA, int32
         return aring + (((r * 2 + kind) * G::kQ) + (i & (G::kQ - 1))) * 32;
     };
 
-    uint32_t T = 0, tfree = 0, busy = 0, flag = 0, zero = 0;
+    constexpr uint32_t kInf = 0xFFFFFFFFu;
+    auto sat = [](uint32_t x, uint32_t y) -> uint32_t {  // x + y, kInf when it does not fit
+        const uint64_t z = (uint64_t)x + y;
+        return z >= kInf ? kInf : (uint32_t)z;
+    };
+    uint32_t tfree = 0, busy = 0, flag = 0, zero = 0;
     int nfA = 0, nbA = 0, nfB = 0, nbB = 0;
     int held = 0, peak = 0;
     // the neighbours' counts: from the left lane its route-A forwards and
     // route-B backwards, from the right lane its route-A backwards and route-B
     // forwards (the producers of this lane's inputs)
     int nfA_L = 0, nbB_L = 0, nbA_R = 0, nfB_R = 0;
-    const int max_steps = 4 * P * M + 2;
-    bool capped = true;
-#pragma unroll 1
-    for (int step = 0; step < max_steps; ++step) {
-        cp_async_wait<G::kAheadC - 2>();
-        __syncwarp();
-        // ---- the fronts of both routes: present, kind, local microbatch,
-        // input known, arrival tick
-        bool hA, fA, hB, fB;
-        int iA, iB;
-        dp_front(nfA, nbA, MA, wA, hA, fA, iA);
-        dp_front(nfB, nbB, MB_, wB, hB, fB, iB);
-        // no producer on another device: a route's first forward, last backward
-        const bool firstA = fA ? blkA == 0 : blkA == P - 1;
-        const bool firstB = fB ? blkB == 0 : blkB == P - 1;
-        const bool knownA = firstA || (fA ? nfA_L : nbA_R) > iA;
-        const bool knownB = firstB || (fB ? nfB_R : nbB_L) > iB;
-        const uint32_t arrA = firstA ? 0u : ring(0, fA ? 0 : 1, iA)[lane];
-        const uint32_t arrB = firstB ? 0u : ring(1, fB ? 0 : 1, iB)[lane];
-        // ---- decide at T: 0 none, 1 route A, 2 route B
-        int pick = 0;
-        if (dev && tfree <= T) {
-            const bool rA = hA && knownA && arrA <= T;
-            const bool rB = hB && knownB && arrB <= T;
-            if (rA && rB) pick = (fA != fB) ? (fA ? 2 : 1) : (prefA ? 1 : 2);
-            else if (rA) pick = 1;
-            else if (rB) pick = 2;
+    bool done = !dev;
+
+    // Place the front op of route `rb` (0 A, 1 B) at tick `t0`: its cost,
+    // the arrival tick for the consumer neighbour, op times, counts, ledger.
+    auto place = [&](bool rb, bool f, int i, uint32_t t0) {
+        const int q = (rb ? 2 : 0) + (f ? 0 : 1);
+        const uint32_t c = cring[(q * G::kRing + i % G::kRing) * 32 + lane];
+        const uint32_t e = t0 + c;
+        flag |= t0 | c;
+        zero |= c == 0 ? 1u : 0u;
+        busy += c;
+        tfree = e;
+        fetch(q, i + G::kAheadC);
+        // the consumer: route A forwards go right, backwards left; route B
+        // the other way round
+        uint32_t *row = ring(rb ? 1 : 0, f ? 0 : 1, i);
+        const bool right = rb != f;
+        if (right && d + 1 < P) row[lane + G::kIPW] = e + cmR;
+        if (!right && d > 0) row[lane - G::kIPW] = e + cmL;
+        if constexpr (OPS) {
+            const int blk = rb ? blkB : blkA, g = (rb ? MA : 0) + i;
+            const int64_t off = x * a.o_inst + ((int64_t)(blk * 2 + (f ? 0 : 1)) * M + g) * a.o_op;
+            if (a.op_start) a.op_start[off] = (int32_t)t0;
+            if (a.op_end) a.op_end[off] = (int32_t)e;
         }
-        // ---- place (predicated on pick)
-        if (pick) {
-            const bool rb = pick == 2;
-            const bool f = rb ? fB : fA;
-            const int i = rb ? iB : iA, q = (rb ? 2 : 0) + (f ? 0 : 1);
-            const uint32_t c = cring[(q * G::kRing + i % G::kRing) * 32 + lane];
-            const uint32_t e = T + c;
-            flag |= T | c;
-            zero |= c == 0 ? 1u : 0u;
-            busy += c;
-            tfree = e;
-            fetch(q, i + G::kAheadC);
-            // the consumer: route A forwards go right, backwards left; route B
-            // the other way round
-            uint32_t *row = ring(rb ? 1 : 0, f ? 0 : 1, i);
-            const bool right = rb != f;
-            if (right && d + 1 < P) row[lane + G::kIPW] = e + cmR;
-            if (!right && d > 0) row[lane - G::kIPW] = e + cmL;
-            if constexpr (OPS) {
-                const int blk = rb ? blkB : blkA, g = (rb ? MA : 0) + i;
-                const int64_t off = x * a.o_inst + ((int64_t)(blk * 2 + (f ? 0 : 1)) * M + g) * a.o_op;
-                if (a.op_start) a.op_start[off] = (int32_t)T;
-                if (a.op_end) a.op_end[off] = (int32_t)e;
-            }
-            nfA += !rb && f;
-            nbA += !rb && !f;
-            nfB += rb && f;
-            nbB += rb && !f;
-            held += f ? 1 : -1;
-            peak = max(peak, held);
-        }
-        cp_async_commit();
-        __syncwarp();
-        // ---- publish the counts the neighbours' inputs depend on
+        nfA += !rb && f;
+        nbA += !rb && !f;
+        nfB += rb && f;
+        nbB += rb && !f;
+        held += f ? 1 : -1;
+        peak = max(peak, held);
+    };
+    // The fronts of both routes: present, kind, local microbatch, input known
+    // (no producer on another device -- a route's first forward or last
+    // backward -- or the producer has placed it), arrival tick if known.
+    struct Front { bool h, f, known; int i; uint32_t arr; };
+    auto fronts = [&](Front &A, Front &Bf) {
+        dp_front(nfA, nbA, MA, wA, A.h, A.f, A.i);
+        dp_front(nfB, nbB, MB_, wB, Bf.h, Bf.f, Bf.i);
+        const bool firstA = A.f ? blkA == 0 : blkA == P - 1;
+        const bool firstB = Bf.f ? blkB == 0 : blkB == P - 1;
+        A.known = firstA || (A.f ? nfA_L : nbA_R) > A.i;
+        Bf.known = firstB || (Bf.f ? nfB_R : nbB_L) > Bf.i;
+        A.arr = firstA ? 0u : ring(0, A.f ? 0 : 1, A.i)[lane];
+        Bf.arr = firstB ? 0u : ring(1, Bf.f ? 0 : 1, Bf.i)[lane];
+    };
+    auto publish_counts = [&]() {
         const uint32_t toR = (uint32_t)nfA | ((uint32_t)nbB << 16);  // read by the right lane
         const uint32_t toL = (uint32_t)nbA | ((uint32_t)nfB << 16);  // read by the left lane
         const uint32_t fromL = __shfl_up_sync(0xFFFFFFFFu, toR, G::kIPW);
@@ -199,31 +192,134 @@ __global__ void __launch_bounds__(128) k_eval_dp(const EvalArgs a, int MA, int32
         nbB_L = (int)(fromL >> 16);
         nbA_R = (int)(fromR & 0xFFFFu);
         nfB_R = (int)(fromR >> 16);
-        // ---- the instance's next event tick
-        const bool done = !dev || (nfA + nbA == 2 * MA && nfB + nbB == 2 * MB_);
-        uint32_t nxt = 0xFFFFFFFFu;
+    };
+
+    // ---- Phase 1: every lane on its own tick t (no op of the lane starts
+    // before t).  A lane decides only what the rules already fix at t: a
+    // front whose input has arrived by t runs at t when the other front is
+    // absent, provably not arrived by t, or would lose the tie-break anyway;
+    // when neither front can have arrived by t, t moves to the earliest tick
+    // either could arrive.  "Provably not arrived": the producer neighbour
+    // publishes after each step a lower bound on the end of its next op of
+    // each (route, kind) -- its own t plus the costs its route order puts up
+    // to that op (F and B cost at least one tick) -- and a consumer whose
+    // input is not placed yet waits for exactly that op.  A lane that waits
+    // does so on a neighbour whose t is smaller (the bound exceeds the
+    // neighbour's t), so in every step some lane of each unfinished instance
+    // places an op or moves its t.  The step count of this phase has no small
+    // bound, so it is capped; an instance still unfinished continues in
+    // phase 2, which is exact from any state reached here.
+    uint32_t t = 0;
+    // the neighbours' bounds this lane's inputs depend on (0 until published)
+    uint32_t lbFA_L = 0, lbBB_L = 0, lbBA_R = 0, lbFB_R = 0;
+#pragma unroll 1
+    for (int step = 0; step < cap1; ++step) {
+        cp_async_wait<G::kAheadC - 2>();
+        __syncwarp();
+        Front A, Bf;
+        fronts(A, Bf);
         if (!done) {
-            if (tfree > T) {
-                nxt = tfree;
-            } else {
-                dp_front(nfA, nbA, MA, wA, hA, fA, iA);
-                dp_front(nfB, nbB, MB_, wB, hB, fB, iB);
-                const bool fstA = fA ? blkA == 0 : blkA == P - 1;
-                const bool fstB = fB ? blkB == 0 : blkB == P - 1;
-                if (hA && !fstA && (fA ? nfA_L : nbA_R) > iA) {
-                    const uint32_t t = ring(0, fA ? 0 : 1, iA)[lane];
-                    if (t > T) nxt = min(nxt, t);
-                }
-                if (hB && !fstB && (fB ? nfB_R : nbB_L) > iB) {
-                    const uint32_t t = ring(1, fB ? 0 : 1, iB)[lane];
-                    if (t > T) nxt = min(nxt, t);
-                }
+            // earliest tick each front's input can arrive: known, or the bound
+            const uint32_t lowA = A.known ? A.arr : (A.f ? sat(lbFA_L, cmL) : sat(lbBA_R, cmR));
+            const uint32_t lowB = Bf.known ? Bf.arr : (Bf.f ? sat(lbFB_R, cmR) : sat(lbBB_L, cmL));
+            const bool rA = A.h && A.known && A.arr <= t, rB = Bf.h && Bf.known && Bf.arr <= t;
+            const bool uA = A.h && !A.known && lowA <= t, uB = Bf.h && !Bf.known && lowB <= t;
+            // route A's front beats route B's whatever B's readiness (and back)
+            const bool aWins = (!A.f && Bf.f) || (A.f == Bf.f && prefA);
+            int pick = 0;
+            if (rA && rB) pick = aWins ? 1 : 2;
+            else if (rA && (!uB || aWins)) pick = 1;
+            else if (rB && (!uA || !aWins)) pick = 2;
+            if (pick) {
+                const bool rb = pick == 2;
+                place(rb, rb ? Bf.f : A.f, rb ? Bf.i : A.i, t);
+                t = tfree;
+            } else if (!rA && !rB && !uA && !uB) {
+                t = min(A.h ? lowA : kInf, Bf.h ? lowB : kInf);
             }
         }
+        cp_async_commit();
+        __syncwarp();
+        publish_counts();
+        done = !dev || (nfA + nbA == 2 * MA && nfB + nbB == 2 * MB_);
+        // the bounds on the ends of this lane's next ops of each (route, kind):
+        // t plus the costs of the ops its route order puts up to them
+        uint32_t lbF[2], lbB[2];
 #pragma unroll
-        for (int o = G::kIPW; o < 32; o <<= 1) nxt = min(nxt, __shfl_xor_sync(0xFFFFFFFFu, nxt, o));
-        if (__all_sync(0xFFFFFFFFu, done)) { capped = false; break; }
-        if (nxt != 0xFFFFFFFFu) T = nxt;
+        for (int r = 0; r < 2; ++r) {
+            const int nf = r ? nfB : nfA, nb = r ? nbB : nbA, Mr = r ? MB_ : MA;
+            bool h, f;
+            int i;
+            dp_front(nf, nb, Mr, r ? wB : wA, h, f, i);
+            const uint32_t cF = nf < Mr ? cring[((2 * r) * G::kRing + nf % G::kRing) * 32 + lane] : 0u;
+            const uint32_t cB = nb < Mr ? cring[((2 * r + 1) * G::kRing + nb % G::kRing) * 32 + lane] : 0u;
+            lbF[r] = nf >= Mr ? kInf : sat(sat(t, f ? 0u : cB), cF);
+            lbB[r] = nb >= Mr ? kInf : sat(sat(t, f ? cF : 0u), cB);
+        }
+        lbFA_L = __shfl_up_sync(0xFFFFFFFFu, lbF[0], G::kIPW);
+        lbBB_L = __shfl_up_sync(0xFFFFFFFFu, lbB[1], G::kIPW);
+        lbBA_R = __shfl_down_sync(0xFFFFFFFFu, lbB[0], G::kIPW);
+        lbFB_R = __shfl_down_sync(0xFFFFFFFFu, lbF[1], G::kIPW);
+        if (__all_sync(0xFFFFFFFFu, done)) break;
+    }
+
+    // ---- Phase 2 (instances phase 1 left unfinished): the lanes of an
+    // instance step through its event ticks together.  At the instance's tick
+    // T every lane free by T takes the op the rules give it at T (an op placed
+    // at T ends after T, so no other decision at T depends on it); the next T
+    // is the smallest of the busy lanes' free ticks and the known arrivals the
+    // free lanes wait for (an arrival not known yet comes after its
+    // producer's end, itself a candidate).  It starts at the smallest t of the
+    // instance's unfinished lanes: every op that starts before it is placed,
+    // and no lane has an input arrived before its own t.  The ticks increase
+    // strictly and each is an op's end or an input's arrival, so the phase
+    // takes at most 4*P*M + 1 steps.
+    bool capped = false;
+    if (!__all_sync(0xFFFFFFFFu, done)) {
+        uint32_t T = done ? kInf : t;
+#pragma unroll
+        for (int o = G::kIPW; o < 32; o <<= 1) T = min(T, __shfl_xor_sync(0xFFFFFFFFu, T, o));
+        capped = true;
+        const int max_steps = 4 * P * M + 2;
+#pragma unroll 1
+        for (int step = 0; step < max_steps; ++step) {
+            cp_async_wait<G::kAheadC - 2>();
+            __syncwarp();
+            Front A, Bf;
+            fronts(A, Bf);
+            // ---- decide at T: 0 none, 1 route A, 2 route B
+            int pick = 0;
+            if (!done && tfree <= T) {
+                const bool rA = A.h && A.known && A.arr <= T;
+                const bool rB = Bf.h && Bf.known && Bf.arr <= T;
+                if (rA && rB) pick = (A.f != Bf.f) ? (A.f ? 2 : 1) : (prefA ? 1 : 2);
+                else if (rA) pick = 1;
+                else if (rB) pick = 2;
+            }
+            if (pick) {
+                const bool rb = pick == 2;
+                place(rb, rb ? Bf.f : A.f, rb ? Bf.i : A.i, T);
+            }
+            cp_async_commit();
+            __syncwarp();
+            publish_counts();
+            done = !dev || (nfA + nbA == 2 * MA && nfB + nbB == 2 * MB_);
+            // ---- the instance's next event tick
+            uint32_t nxt = kInf;
+            if (!done) {
+                if (tfree > T) {
+                    nxt = tfree;
+                } else {
+                    fronts(A, Bf);
+                    if (A.h && A.known && A.arr > T) nxt = min(nxt, A.arr);
+                    if (Bf.h && Bf.known && Bf.arr > T) nxt = min(nxt, Bf.arr);
+                }
+            }
+#pragma unroll
+            for (int o = G::kIPW; o < 32; o <<= 1) nxt = min(nxt, __shfl_xor_sync(0xFFFFFFFFu, nxt, o));
+            if (__all_sync(0xFFFFFFFFu, done)) { capped = false; break; }
+            if (nxt != kInf) T = nxt;
+        }
     }
     cp_async_wait<0>();
 
@@ -265,20 +361,20 @@ __global__ void __launch_bounds__(128) k_eval_dp(const EvalArgs a, int MA, int32
 namespace {
 
 template <int PMAX, bool OPS>
-int launch_dp_t(const EvalArgs &a, int MA, int32_t *peak, cudaStream_t st) {
+int launch_dp_t(const EvalArgs &a, int MA, int32_t *peak, int cap1, cudaStream_t st) {
     using G = DpGeom<PMAX>;
     const size_t smem = (size_t)G::kWarps * G::kWords * sizeof(uint32_t);
     const int64_t warps = (a.n + G::kIPW - 1) / G::kIPW;
     const int64_t blocks = (warps + G::kWarps - 1) / G::kWarps;
     if (blocks > 0x7FFFFFFF) return PP_ERR_SIZE;
-    k_eval_dp<PMAX, OPS><<<(unsigned)blocks, G::kWarps * 32, smem, st>>>(a, MA, peak);
+    k_eval_dp<PMAX, OPS><<<(unsigned)blocks, G::kWarps * 32, smem, st>>>(a, MA, peak, cap1);
     PPS_CUDA_TRY(cudaGetLastError());
     return PP_OK;
 }
 
 template <int PMAX>
-int launch_dp_p(const EvalArgs &a, int MA, int32_t *peak, bool ops, cudaStream_t st) {
-    return ops ? launch_dp_t<PMAX, true>(a, MA, peak, st) : launch_dp_t<PMAX, false>(a, MA, peak, st);
+int launch_dp_p(const EvalArgs &a, int MA, int32_t *peak, int cap1, bool ops, cudaStream_t st) {
+    return ops ? launch_dp_t<PMAX, true>(a, MA, peak, cap1, st) : launch_dp_t<PMAX, false>(a, MA, peak, cap1, st);
 }
 
 }  // namespace
@@ -308,10 +404,16 @@ extern "C" int pp_sched_eval_dualpipe(int P, int M, int m_a, const int32_t *cost
     a.n = n_instances; a.inst_begin = 0;
     a.makespan = makespan; a.idle = idle; a.bub_num = bub_num; a.bub_den = bub_den; a.status = status;
     a.op_start = op_start; a.op_end = op_end; a.o_inst = op_stride_inst; a.o_op = op_stride_op;
+    // the first phase's step cap (results do not depend on it; see the kernel)
+    int cap1 = 8 * M + 64;
+    if (const char *env = std::getenv("PPSCHED_DP_PHASE1_STEPS")) {
+        const long v = std::strtol(env, nullptr, 10);
+        if (v >= 0 && v <= (1L << 30)) cap1 = (int)v;
+    }
     switch (pmax_for(P)) {
-        case 4: return launch_dp_p<4>(a, m_a, peak, ops, stream);
-        case 8: return launch_dp_p<8>(a, m_a, peak, ops, stream);
-        case 16: return launch_dp_p<16>(a, m_a, peak, ops, stream);
+        case 4: return launch_dp_p<4>(a, m_a, peak, cap1, ops, stream);
+        case 8: return launch_dp_p<8>(a, m_a, peak, cap1, ops, stream);
+        case 16: return launch_dp_p<16>(a, m_a, peak, cap1, ops, stream);
         default: return PP_ERR_INTERNAL;
     }
 }

@@ -20,7 +20,13 @@ SHAPES = [(1, 1, 1), (1, 5, 2), (2, 4, 2), (2, 7, 0), (2, 7, 7), (3, 6, 3), (4, 
 
 @pytest.mark.parametrize("P,M,m_a", SHAPES)
 @pytest.mark.parametrize("layout", ["inst_minor", "inst_major"])
-def test_random_batches_every_op(orc, P, M, m_a, layout):
+@pytest.mark.parametrize("cap1", [None, 0, 5])
+def test_random_batches_every_op(orc, monkeypatch, P, M, m_a, layout, cap1):
+    """Every op time against the oracle, with the kernel's first phase as
+    configured (None), skipped (0: every instance on the common-tick phase)
+    and cut short (5 steps: instances handed over part-way)."""
+    if cap1 is not None:
+        monkeypatch.setenv("PPSCHED_DP_PHASE1_STEPS", str(cap1))
     for n in (37, 133):
         b = W.random_batch(W.ONEF1B, P, M, 1, n, seed=P * 100 + M + n, lo=1, hi=9, comm_hi=4, layout=layout)
         g = run_gpu_dp(b, m_a, op_times=True)
@@ -58,9 +64,13 @@ def test_statuses(orc):
     assert_same_zb(g, r)
 
 
-def test_hetero_full_batch(orc):
+@pytest.mark.parametrize("cap1", [None, 0, 40])
+def test_hetero_full_batch(orc, monkeypatch, cap1):
     """65,536 heterogeneous instances (P=8, M=64, 32 microbatches per route):
-    every instance against the oracle, and the page's peak of at most p+1."""
+    every instance against the oracle, and the page's peak of at most p+1;
+    with the first phase as configured, skipped, and cut short."""
+    if cap1 is not None:
+        monkeypatch.setenv("PPSCHED_DP_PHASE1_STEPS", str(cap1))
     b = W.hetero_dualpipe()
     m_a = b.meta["m_a"]
     g = run_gpu_dp(b, m_a)
