@@ -127,8 +127,8 @@ __global__ void __launch_bounds__(128) k_eval_dp(const EvalArgs a, int MA, int32
 
     constexpr uint32_t kInf = 0xFFFFFFFFu;
     auto sat = [](uint32_t x, uint32_t y) -> uint32_t {  // x + y, kInf when it does not fit
-        const uint64_t z = (uint64_t)x + y;
-        return z >= kInf ? kInf : (uint32_t)z;
+        const uint32_t z = x + y;
+        return z < x ? kInf : z;
     };
     uint32_t tfree = 0, busy = 0, flag = 0, zero = 0;
     int nfA = 0, nbA = 0, nfB = 0, nbB = 0;
@@ -139,11 +139,10 @@ __global__ void __launch_bounds__(128) k_eval_dp(const EvalArgs a, int MA, int32
     int nfA_L = 0, nbB_L = 0, nbA_R = 0, nfB_R = 0;
     bool done = !dev;
 
-    // Place the front op of route `rb` (0 A, 1 B) at tick `t0`: its cost,
+    // Place the front op of route `rb` (0 A, 1 B), of cost c, at tick `t0`:
     // the arrival tick for the consumer neighbour, op times, counts, ledger.
-    auto place = [&](bool rb, bool f, int i, uint32_t t0) {
+    auto place = [&](bool rb, bool f, int i, uint32_t t0, uint32_t c) {
         const int q = (rb ? 2 : 0) + (f ? 0 : 1);
-        const uint32_t c = cring[(q * G::kRing + i % G::kRing) * 32 + lane];
         const uint32_t e = t0 + c;
         flag |= t0 | c;
         zero |= c == 0 ? 1u : 0u;
@@ -212,54 +211,68 @@ __global__ void __launch_bounds__(128) k_eval_dp(const EvalArgs a, int MA, int32
     uint32_t t = 0;
     // the neighbours' bounds this lane's inputs depend on (0 until published)
     uint32_t lbFA_L = 0, lbBB_L = 0, lbBA_R = 0, lbFB_R = 0;
+    // each route's front and the costs of its next F and B, kept across
+    // steps and refreshed when the route places an op (the ring rows of the
+    // next ops were copied at least kAheadC - 1 steps ago)
+    struct Route { bool h, f, moreF, moreB; int i; uint32_t cF, cB; };
+    auto refresh = [&](int r, Route &S) {
+        const int nf = r ? nfB : nfA, nb = r ? nbB : nbA, Mr = r ? MB_ : MA;
+        dp_front(nf, nb, Mr, r ? wB : wA, S.h, S.f, S.i);
+        S.moreF = nf < Mr;
+        S.moreB = nb < Mr;
+        S.cF = S.moreF ? cring[((2 * r) * G::kRing + nf % G::kRing) * 32 + lane] : 0u;
+        S.cB = S.moreB ? cring[((2 * r + 1) * G::kRing + nb % G::kRing) * 32 + lane] : 0u;
+    };
+    Route RA, RB;
+    refresh(0, RA);
+    refresh(1, RB);
 #pragma unroll 1
     for (int step = 0; step < cap1; ++step) {
         cp_async_wait<G::kAheadC - 2>();
         __syncwarp();
-        Front A, Bf;
-        fronts(A, Bf);
         if (!done) {
+            // input known (no producer on another device, or placed), arrival
+            const bool firstA = RA.f ? blkA == 0 : blkA == P - 1;
+            const bool firstB = RB.f ? blkB == 0 : blkB == P - 1;
+            const bool knownA = firstA || (RA.f ? nfA_L : nbA_R) > RA.i;
+            const bool knownB = firstB || (RB.f ? nfB_R : nbB_L) > RB.i;
+            const uint32_t arrA = firstA ? 0u : ring(0, RA.f ? 0 : 1, RA.i)[lane];
+            const uint32_t arrB = firstB ? 0u : ring(1, RB.f ? 0 : 1, RB.i)[lane];
             // earliest tick each front's input can arrive: known, or the bound
-            const uint32_t lowA = A.known ? A.arr : (A.f ? sat(lbFA_L, cmL) : sat(lbBA_R, cmR));
-            const uint32_t lowB = Bf.known ? Bf.arr : (Bf.f ? sat(lbFB_R, cmR) : sat(lbBB_L, cmL));
-            const bool rA = A.h && A.known && A.arr <= t, rB = Bf.h && Bf.known && Bf.arr <= t;
-            const bool uA = A.h && !A.known && lowA <= t, uB = Bf.h && !Bf.known && lowB <= t;
+            const uint32_t lowA = knownA ? arrA : (RA.f ? sat(lbFA_L, cmL) : sat(lbBA_R, cmR));
+            const uint32_t lowB = knownB ? arrB : (RB.f ? sat(lbFB_R, cmR) : sat(lbBB_L, cmL));
+            const bool rA = RA.h && knownA && arrA <= t, rB = RB.h && knownB && arrB <= t;
+            const bool uA = RA.h && !knownA && lowA <= t, uB = RB.h && !knownB && lowB <= t;
             // route A's front beats route B's whatever B's readiness (and back)
-            const bool aWins = (!A.f && Bf.f) || (A.f == Bf.f && prefA);
+            const bool aWins = (!RA.f && RB.f) || (RA.f == RB.f && prefA);
             int pick = 0;
             if (rA && rB) pick = aWins ? 1 : 2;
             else if (rA && (!uB || aWins)) pick = 1;
             else if (rB && (!uA || !aWins)) pick = 2;
             if (pick) {
                 const bool rb = pick == 2;
-                place(rb, rb ? Bf.f : A.f, rb ? Bf.i : A.i, t);
+                Route &S = rb ? RB : RA;
+                place(rb, S.f, S.i, t, S.f ? S.cF : S.cB);
                 t = tfree;
+                refresh(rb ? 1 : 0, S);
             } else if (!rA && !rB && !uA && !uB) {
-                t = min(A.h ? lowA : kInf, Bf.h ? lowB : kInf);
+                t = min(RA.h ? lowA : kInf, RB.h ? lowB : kInf);
             }
         }
         cp_async_commit();
         __syncwarp();
         publish_counts();
-        done = !dev || (nfA + nbA == 2 * MA && nfB + nbB == 2 * MB_);
+        done = !dev || (!RA.h && !RB.h);
         // the bounds on the ends of this lane's next ops of each (route, kind):
         // t plus the costs of the ops its route order puts up to them
-        uint32_t lbF[2], lbB[2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int nf = r ? nfB : nfA, nb = r ? nbB : nbA, Mr = r ? MB_ : MA;
-            bool h, f;
-            int i;
-            dp_front(nf, nb, Mr, r ? wB : wA, h, f, i);
-            const uint32_t cF = nf < Mr ? cring[((2 * r) * G::kRing + nf % G::kRing) * 32 + lane] : 0u;
-            const uint32_t cB = nb < Mr ? cring[((2 * r + 1) * G::kRing + nb % G::kRing) * 32 + lane] : 0u;
-            lbF[r] = nf >= Mr ? kInf : sat(sat(t, f ? 0u : cB), cF);
-            lbB[r] = nb >= Mr ? kInf : sat(sat(t, f ? cF : 0u), cB);
-        }
-        lbFA_L = __shfl_up_sync(0xFFFFFFFFu, lbF[0], G::kIPW);
-        lbBB_L = __shfl_up_sync(0xFFFFFFFFu, lbB[1], G::kIPW);
-        lbBA_R = __shfl_down_sync(0xFFFFFFFFu, lbB[0], G::kIPW);
-        lbFB_R = __shfl_down_sync(0xFFFFFFFFu, lbF[1], G::kIPW);
+        const uint32_t lbFA = RA.moreF ? sat(sat(t, RA.f ? 0u : RA.cB), RA.cF) : kInf;
+        const uint32_t lbBA = RA.moreB ? sat(sat(t, RA.f ? RA.cF : 0u), RA.cB) : kInf;
+        const uint32_t lbFB = RB.moreF ? sat(sat(t, RB.f ? 0u : RB.cB), RB.cF) : kInf;
+        const uint32_t lbBB = RB.moreB ? sat(sat(t, RB.f ? RB.cF : 0u), RB.cB) : kInf;
+        lbFA_L = __shfl_up_sync(0xFFFFFFFFu, lbFA, G::kIPW);
+        lbBB_L = __shfl_up_sync(0xFFFFFFFFu, lbBB, G::kIPW);
+        lbBA_R = __shfl_down_sync(0xFFFFFFFFu, lbBA, G::kIPW);
+        lbFB_R = __shfl_down_sync(0xFFFFFFFFu, lbFB, G::kIPW);
         if (__all_sync(0xFFFFFFFFu, done)) break;
     }
 
@@ -298,7 +311,9 @@ __global__ void __launch_bounds__(128) k_eval_dp(const EvalArgs a, int MA, int32
             }
             if (pick) {
                 const bool rb = pick == 2;
-                place(rb, rb ? Bf.f : A.f, rb ? Bf.i : A.i, T);
+                const bool f = rb ? Bf.f : A.f;
+                const int i = rb ? Bf.i : A.i, q = (rb ? 2 : 0) + (f ? 0 : 1);
+                place(rb, f, i, T, cring[(q * G::kRing + i % G::kRing) * 32 + lane]);
             }
             cp_async_commit();
             __syncwarp();
