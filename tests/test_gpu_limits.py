@@ -6,14 +6,15 @@ searches L <= 256 layers with C(L-1, S-1) below 2^64.  Each case sits on one or
 more of them at once, with a ragged batch where the kernel works in warps of
 instances, and compares every output (per-op times included) bit for bit.
 The refusals one step past each limit are host-side and tested without a GPU
-(test_abi.py).
+(test_abi.py).  Zero Bubble and DualPipe sit at P = 16 and M = 32,768.
 """
 import numpy as np
 import pytest
 import torch
 
 import pipeline_schedule_simulation_gb300.workloads as W
-from gpu_helpers import assert_same, assert_same_zb, run_gpu, run_gpu_zb, run_oracle, run_oracle_zb, to_dev
+from gpu_helpers import (assert_same, assert_same_zb, run_gpu, run_gpu_dp, run_gpu_zb, run_oracle, run_oracle_dp,
+                         run_oracle_zb, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -39,6 +40,18 @@ def test_zero_bubble_at_limits(orc, policy):
     batch = W.random_zb(policy, 16, 32768, 2, seed=3 + policy, hi=30, w_hi=30, comm_hi=6)
     g = run_gpu_zb(batch, op_times=True)
     r = run_oracle_zb(orc, batch, op_times=True, nthreads=2)
+    assert (r["status"] == 0).all()
+    assert_same_zb(g, r, op_times=True)
+
+
+@pytest.mark.parametrize("m_a", [16384, 32768, 0, 1])
+def test_dualpipe_at_limits(orc, m_a):
+    """P = 16 and M = 32,768 (65,536 F and B ops per device): both routes
+    half full, every microbatch on route A, every one on route B, and a
+    single one on route A."""
+    batch = W.random_batch(W.ONEF1B, 16, 32768, 1, 2, seed=71 + m_a % 7, lo=1, hi=30, comm_hi=6)
+    g = run_gpu_dp(batch, m_a, op_times=True)
+    r = run_oracle_dp(orc, batch, m_a, op_times=True, nthreads=2)
     assert (r["status"] == 0).all()
     assert_same_zb(g, r, op_times=True)
 
