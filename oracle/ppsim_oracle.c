@@ -1507,6 +1507,12 @@ static int64_t dp_arrival(const dp_sim *z, int r, int s, int isF, int g)
     return a;
 }
 
+static int dp_cmp_start(const void *x, const void *y)
+{
+    int64_t a = ((const int64_t *)x)[0], b = ((const int64_t *)y)[0];
+    return a < b ? -1 : (a > b ? 1 : 0);
+}
+
 int orc_dp_inst(int P, int MA, int MB, const int64_t *tf, const int64_t *tb, const int64_t *comm,
                 int64_t *start, int64_t *end, int64_t *makespan, int64_t *busy, int64_t *idle,
                 int64_t *bub, int *peak)
@@ -1575,26 +1581,31 @@ int orc_dp_inst(int P, int MA, int MB, const int64_t *tf, const int64_t *tb, con
         T = next;
     }
     /* validity ([M040] §08): every op placed, no overlap on a device, every
-     * input arrived before its op starts, every B after its F */
-    for (int d = 0; d < P; ++d) {
-        /* the device's ops in start order: collect and check pairwise */
-        for (int r = 0; r < 2; ++r)
-            for (int r2 = 0; r2 < 2; ++r2) {
-                int s = dp_stage(P, r, d), s2 = dp_stage(P, r2, d);
-                int g0 = r == 0 ? 0 : MA, g1 = r == 0 ? MA : M;
-                int h0 = r2 == 0 ? 0 : MA, h1 = r2 == 0 ? MA : M;
+     * input arrived before its op starts, every B after its F.  The overlap
+     * check sorts each device's ops by start tick and compares neighbours. */
+    {
+        int64_t (*iv)[2] = (int64_t (*)[2])malloc((size_t)2 * M * sizeof(*iv));
+        if (!iv) return ORC_ERR_NOMEM;
+        for (int d = 0; d < P; ++d) {
+            int n = 0;
+            for (int r = 0; r < 2; ++r) {
+                int s = dp_stage(P, r, d), g0 = r == 0 ? 0 : MA, g1 = r == 0 ? MA : M;
                 for (int g = g0; g < g1; ++g)
                     for (int kd = 0; kd < 2; ++kd) {
-                        int64_t a0 = start[(s * 2 + kd) * M + g], a1 = end[(s * 2 + kd) * M + g];
-                        if (a0 < 0 || a1 < a0) return ORC_ERR_INVARIANT;
-                        for (int h = h0; h < h1; ++h)
-                            for (int kd2 = 0; kd2 < 2; ++kd2) {
-                                if (r == r2 && g == h && kd == kd2) continue;
-                                int64_t b0 = start[(s2 * 2 + kd2) * M + h], b1 = end[(s2 * 2 + kd2) * M + h];
-                                if (a0 < b1 && b0 < a1) return ORC_ERR_INVARIANT;
-                            }
+                        iv[n][0] = start[(s * 2 + kd) * M + g];
+                        iv[n][1] = end[(s * 2 + kd) * M + g];
+                        ++n;
                     }
             }
+            qsort(iv, (size_t)n, sizeof(*iv), dp_cmp_start);
+            for (int q = 0; q < n; ++q) {
+                if (iv[q][0] < 0 || iv[q][1] < iv[q][0] || (q > 0 && iv[q][0] < iv[q - 1][1])) {
+                    free(iv);
+                    return ORC_ERR_INVARIANT;
+                }
+            }
+        }
+        free(iv);
     }
     for (int r = 0; r < 2; ++r) {
         int g0 = r == 0 ? 0 : MA, g1 = r == 0 ? MA : M;
