@@ -121,7 +121,7 @@ def test_two_blocks_per_device_and_the_page_peak(orc):
     """Each device runs route A's block d and route B's block P-1-d (its busy
     time is exactly those ops' costs: two copies of the parameters), and holds
     at most P+1 activations; with at least P microbatches on each route the
-    peak is P+1 ("from p to p+1")."""
+    peak is P+1, one more than 1F1B's P, as the page states."""
     rng = np.random.default_rng(2)
     for P in (2, 3, 4, 6, 8, 16):
         for MA, MB in ((1, 1), (P, P), (P + 3, P), (2 * P, 2 * P + 1), (3, 2 * P)):
