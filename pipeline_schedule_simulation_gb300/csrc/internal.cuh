@@ -138,9 +138,10 @@ int build_plans(const PlanShape *shapes, int n, cudaStream_t stream, pp_plan **o
 int cached_plans(const PlanShape *shapes, int n, cudaStream_t stream, pp_plan **out);
 
 // Kernel tables of many (plan, stride pair) requests: the missing ones are
-// built in one allocation and a few batched launches on `stream`, without a
-// synchronization (later work on `stream` sees them; other streams must wait
-// for it).  lane = 0: the register evaluator's tables (kernel_tables);
+// built in one allocation and a few batched launches on `stream`; the only
+// synchronization is the upload of the job records from pageable host memory,
+// which waits for `stream` to drain first.  Later work on `stream` sees the
+// tables; other streams must wait for `stream`.  lane = 0: the register evaluator's tables (kernel_tables);
 // lane = 1: the lane evaluator's tables with one instance set per lane.
 struct TableReq {
     pp_plan *plan;

@@ -24,6 +24,7 @@
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <utility>
 #include <vector>
 
 #include "internal.cuh"
@@ -970,9 +971,13 @@ int build_tables(TableReq *reqs, int n, cudaStream_t st) {
     int rc = A.alloc(jobs_at + pad4((int64_t)q.size() * (int64_t)sizeof(TableJob) / 4 + 1));
     if (rc) return rc;
     TableJob *d_jobs = reinterpret_cast<TableJob *>(A.w() + jobs_at);
-    for (int kind = 0; kind < 2 && !rc; ++kind) {
+    // every job record, grouped by kind and table width, in one upload
+    std::vector<TableJob> jobs;
+    std::vector<std::pair<int, int>> groups;  // (kind, pmax) of each run of records
+    std::vector<size_t> first;
+    for (int kind = 0; kind < 2; ++kind) {
         for (int pmax : {4, 8, 16}) {
-            std::vector<TableJob> jobs;
+            const size_t f0 = jobs.size();
             for (const Q &e : q) {
                 if (e.lane != kind || e.plan->pmax != pmax) continue;
                 const pp_plan *p = e.plan;
@@ -984,15 +989,23 @@ int build_tables(TableReq *reqs, int n, cudaStream_t st) {
                 j.words = e.words; j.out = A.w() + e.off;
                 jobs.push_back(j);
             }
-            if (jobs.empty()) continue;
-            rc = for_chunks(jobs, d_jobs, st, [&](TableJob *d, int c) {
-                if (kind == 0) kb_ktab<<<dim3(grid_x(max_reg), c), 256, 0, st>>>(d);
-                else launch_ltab_batch(pmax, d, c, max_lane, st);
-            });
-            if (rc) break;
-            d_jobs += jobs.size();
+            if (jobs.size() > f0) {
+                groups.emplace_back(kind, pmax);
+                first.push_back(f0);
+            }
         }
     }
+    first.push_back(jobs.size());
+    PPS_CUDA_TRY(cudaMemcpyAsync(d_jobs, jobs.data(), jobs.size() * sizeof(TableJob), cudaMemcpyHostToDevice, st));
+    for (size_t gi = 0; gi < groups.size() && !rc; ++gi) {
+        const int kind = groups[gi].first, pmax = groups[gi].second;
+        for (size_t j0 = first[gi]; j0 < first[gi + 1] && !rc; j0 += 65535) {
+            const int c = (int)std::min<size_t>(65535, first[gi + 1] - j0);
+            if (kind == 0) kb_ktab<<<dim3(grid_x(max_reg), c), 256, 0, st>>>(d_jobs + j0);
+            else rc = launch_ltab_batch(pmax, d_jobs + j0, c, max_lane, st);
+        }
+    }
+    if (!rc) PPS_CUDA_TRY(cudaGetLastError());
     if (rc) return rc;
     std::vector<const pp_ktab *> made(q.size());
     for (size_t x = 0; x < q.size(); ++x) {
