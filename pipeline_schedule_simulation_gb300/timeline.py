@@ -2,10 +2,11 @@
 Chrome trace (the JSON "traceEvents" format that chrome://tracing and
 Perfetto open) or CSV.
 
-The times come from the library (op_start / op_end of pp_sched_eval or
-pp_sched_eval_zb); this module only formats them.  Each record is one op:
-device, kind ("F", "B" or, for Zero Bubble, "W"), chunk, microbatch, start
-and end tick.
+The times come from the library (op_start / op_end of pp_sched_eval,
+pp_sched_eval_zb or pp_sched_eval_dualpipe); this module only formats them.
+Each record is one op: device, kind ("F", "B" or, for Zero Bubble, "W"),
+chunk, microbatch, start and end tick, and for DualPipe the route ("A" enters
+at device 0, "B" at device P-1).
 """
 from __future__ import annotations
 
@@ -17,17 +18,28 @@ import numpy as np
 KINDS = ("F", "B", "W")
 
 
-def records(op_start, op_end, ops=None, zb=False):
+def records(op_start, op_end, ops=None, zb=False, dualpipe_m_a=None):
     """Records of one instance.
 
     op_start, op_end: [P][O] ticks (pp_sched_eval, O = 2*M*v ops per device,
     in the device's order) with `ops` the plan's packed op words [P][O]
     (binding.Plan.tables()[0]); or, with zb=True, [P][3][M] ticks of
-    pp_sched_eval_zb (kind F, B, W; microbatch)."""
+    pp_sched_eval_zb (kind F, B, W; microbatch); or, with dualpipe_m_a set
+    (route A's microbatch count), [P][2][M] ticks of pp_sched_eval_dualpipe
+    (block, kind F / B, microbatch): block s of microbatch g runs on device s
+    for route A (g < m_a) and on device P-1-s for route B."""
     st = np.asarray(op_start)
     en = np.asarray(op_end)
     out = []
-    if zb:
+    if dualpipe_m_a is not None:
+        P, _, M = st.shape
+        for s in range(P):
+            for kd in range(2):
+                for g in range(M):
+                    a = g < dualpipe_m_a
+                    out.append(dict(device=s if a else P - 1 - s, kind=KINDS[kd], chunk=0, mb=g,
+                                    start=int(st[s, kd, g]), end=int(en[s, kd, g]), route="A" if a else "B"))
+    elif zb:
         P, _, M = st.shape
         for k in range(P):
             for kd in range(3):
@@ -53,7 +65,8 @@ def chrome_trace(recs, us_per_tick=1.0, name="schedule"):
     for k in sorted({r["device"] for r in recs}):
         events.append({"name": "thread_name", "ph": "M", "pid": 0, "tid": k, "args": {"name": f"device {k}"}})
     for r in recs:
-        label = f"{r['kind']}{r['mb']}" + (f".c{r['chunk']}" if r["chunk"] else "")
+        label = f"{r['kind']}{r['mb']}" + (f".c{r['chunk']}" if r["chunk"] else "") + \
+            (f".{r['route']}" if "route" in r else "")
         events.append({"name": label, "cat": r["kind"], "ph": "X", "pid": 0, "tid": r["device"],
                        "ts": r["start"] * us_per_tick, "dur": (r["end"] - r["start"]) * us_per_tick,
                        "args": {"chunk": r["chunk"], "mb": r["mb"], "start": r["start"], "end": r["end"]}})
@@ -66,7 +79,8 @@ def write_chrome_trace(path, recs, us_per_tick=1.0, name="schedule"):
 
 
 def write_csv(path, recs):
+    fields = ["device", "kind", "chunk", "mb", "start", "end"] + (["route"] if recs and "route" in recs[0] else [])
     with open(path, "w", newline="") as f:
-        w = csv.DictWriter(f, fieldnames=["device", "kind", "chunk", "mb", "start", "end"])
+        w = csv.DictWriter(f, fieldnames=fields)
         w.writeheader()
         w.writerows(recs)

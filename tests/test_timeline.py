@@ -41,3 +41,26 @@ def test_records_zero_bubble(orc):
     recs = T.records(r["start"], r["end"], zb=True)
     assert len(recs) == 12
     assert [x["kind"] + str(x["mb"]) for x in recs if x["device"] == 0] == ["F0", "F1", "B0", "W0", "B1", "W1"]
+
+
+def test_records_dualpipe(orc, tmp_path):
+    """DualPipe op times by (block, kind, microbatch) become per-device records:
+    route A's block s on device s, route B's on device P-1-s; on every device
+    the records are in time order without overlap, and each device holds both
+    routes' ops."""
+    rng = np.random.default_rng(3)
+    P, MA, MB = 4, 5, 4
+    r = orc.dp_evaluate(P, MA, MB, rng.integers(1, 5, (P, MA + MB)), rng.integers(1, 5, (P, MA + MB)),
+                        rng.integers(0, 3, P - 1))
+    recs = T.records(r["start"], r["end"], dualpipe_m_a=MA)
+    assert len(recs) == 2 * P * (MA + MB)
+    for k in range(P):
+        dev = [x for x in recs if x["device"] == k]
+        assert len(dev) == 2 * (MA + MB)
+        assert {x["route"] for x in dev} == {"A", "B"}
+        assert all(a["end"] <= b["start"] for a, b in zip(dev, dev[1:]))
+    assert max(x["end"] for x in recs) == r["makespan"]
+    c = tmp_path / "dp.csv"
+    T.write_csv(c, recs)
+    rows = list(csv.DictReader(open(c)))
+    assert rows[0].keys() == {"device", "kind", "chunk", "mb", "start", "end", "route"}
