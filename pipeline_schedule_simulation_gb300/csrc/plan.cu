@@ -593,6 +593,35 @@ unsigned grid_x(int64_t elems) {
     return (unsigned)std::min<int64_t>(1024, std::max<int64_t>(1, (elems + 255) / 256));
 }
 
+// The build's temporary words (inverse op positions, info words, job records):
+// one grow-only buffer per device, kept for the process, so a build neither
+// allocates nor frees it again (a free would synchronize the device).  Builds
+// hold g_build_mu while they use it.
+std::mutex g_build_mu;
+struct TempBuf {
+    void *p = nullptr;
+    size_t bytes = 0;
+};
+TempBuf g_temp[64];
+
+int temp_words(int64_t words, uint32_t **out) {
+    int dev = 0;
+    PPS_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return PP_ERR_INTERNAL;
+    TempBuf &t = g_temp[dev];
+    const size_t need = (size_t)std::max<int64_t>(words, 4) * sizeof(uint32_t);
+    if (t.bytes < need) {
+        if (t.p) PPS_CUDA_TRY(cudaFree(t.p));
+        t.p = nullptr;
+        t.bytes = 0;
+        const size_t grow = std::max(need, (size_t)1 << 20);
+        PPS_CUDA_TRY(cudaMalloc(&t.p, grow));
+        t.bytes = grow;
+    }
+    *out = static_cast<uint32_t *>(t.p);
+    return PP_OK;
+}
+
 void arena_ref(pp_arena *a) {
     if (a) a->refs.fetch_add(1);
 }
@@ -637,11 +666,13 @@ int build_plans(const PlanShape *shapes, int n, cudaStream_t st, pp_plan **out) 
     wT += 8LL * n;
     const int64_t jobs_at = pad4(wT);
     wT = jobs_at + pad4((int64_t)n * (int64_t)sizeof(BuildJob) / 4 + 1);
-    Arena A, T, B, C;
+    std::lock_guard<std::mutex> build_lock(g_build_mu);
+    Arena A, B, C;
+    uint32_t *Tw = nullptr;
     int rc = A.alloc(wA);
-    if (!rc) rc = T.alloc(wT);
+    if (!rc) rc = temp_words(wT, &Tw);
     if (rc) return rc;
-    BuildJob *d_jobs = reinterpret_cast<BuildJob *>(T.w() + jobs_at);
+    BuildJob *d_jobs = reinterpret_cast<BuildJob *>(Tw + jobs_at);
     int64_t pk = 0;
     for (int i = 0; i < n; ++i) {
         const PlanShape &sh = shapes[i];
@@ -653,17 +684,17 @@ int build_plans(const PlanShape *shapes, int n, cudaStream_t st, pp_plan **out) 
         b.round = reinterpret_cast<int32_t *>(A.w() + offA[i] + pad4(nops));
         b.peak = reinterpret_cast<int32_t *>(A.w() + peak_at + pk);
         pk += sh.P;
-        b.pos = reinterpret_cast<int32_t *>(T.w() + offT[i]);
-        b.info = reinterpret_cast<int32_t *>(T.w() + info_at) + 8LL * i;
+        b.pos = reinterpret_cast<int32_t *>(Tw + offT[i]);
+        b.info = reinterpret_cast<int32_t *>(Tw + info_at) + 8LL * i;
     }
-    PPS_CUDA_TRY(cudaMemsetAsync(T.w() + info_at, 0, 8LL * n * sizeof(int32_t), st));
+    PPS_CUDA_TRY(cudaMemsetAsync(Tw + info_at, 0, 8LL * n * sizeof(int32_t), st));
     rc = for_chunks(jobs, d_jobs, st, [&](BuildJob *d, int c) {
         kb_order<<<dim3(grid_x(max_ops), c), 256, 0, st>>>(d);
         kb_rounds<<<c, 32, 0, st>>>(d);
     });
     if (rc) return rc;
     std::vector<int32_t> h_info(8LL * n);
-    PPS_CUDA_TRY(cudaMemcpyAsync(h_info.data(), T.w() + info_at, h_info.size() * sizeof(int32_t),
+    PPS_CUDA_TRY(cudaMemcpyAsync(h_info.data(), Tw + info_at, h_info.size() * sizeof(int32_t),
                                  cudaMemcpyDeviceToHost, st));
     PPS_CUDA_TRY(cudaStreamSynchronize(st));
 
@@ -699,7 +730,7 @@ int build_plans(const PlanShape *shapes, int n, cudaStream_t st, pp_plan **out) 
     });
     if (rc) return rc;
     std::vector<int32_t> h_peak(npeak);
-    PPS_CUDA_TRY(cudaMemcpyAsync(h_info.data(), T.w() + info_at, h_info.size() * sizeof(int32_t),
+    PPS_CUDA_TRY(cudaMemcpyAsync(h_info.data(), Tw + info_at, h_info.size() * sizeof(int32_t),
                                  cudaMemcpyDeviceToHost, st));
     PPS_CUDA_TRY(cudaMemcpyAsync(h_peak.data(), A.w() + peak_at, npeak * sizeof(int32_t), cudaMemcpyDeviceToHost,
                                  st));
@@ -722,7 +753,7 @@ int build_plans(const PlanShape *shapes, int n, cudaStream_t st, pp_plan **out) 
         rc = C.alloc(wC);
         if (rc) return rc;
         PPS_CUDA_TRY(cudaMemsetAsync(C.w(), 0xFF, (size_t)std::max<int64_t>(wC, 4) * sizeof(uint32_t), st));
-        PPS_CUDA_TRY(cudaMemsetAsync(T.w(), 0xFF, (size_t)info_at * sizeof(uint32_t), st));  // slot_of := -1
+        PPS_CUDA_TRY(cudaMemsetAsync(Tw, 0xFF, (size_t)info_at * sizeof(uint32_t), st));  // slot_of := -1
         for (int i : sidx) {
             BuildJob b = jobs[i];
             const int64_t cells = (int64_t)b.R * b.pmax;
@@ -739,7 +770,7 @@ int build_plans(const PlanShape *shapes, int n, cudaStream_t st, pp_plan **out) 
             kb_cslots<<<c, 32, 0, st>>>(d);
         });
         if (rc) return rc;
-        PPS_CUDA_TRY(cudaMemcpyAsync(h_info.data(), T.w() + info_at, h_info.size() * sizeof(int32_t),
+        PPS_CUDA_TRY(cudaMemcpyAsync(h_info.data(), Tw + info_at, h_info.size() * sizeof(int32_t),
                                      cudaMemcpyDeviceToHost, st));
         PPS_CUDA_TRY(cudaStreamSynchronize(st));
         for (int i : sidx) {
