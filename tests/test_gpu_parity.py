@@ -392,3 +392,34 @@ def test_peak_written_by_every_evaluator(policy, P, M, v, n, layout, mbz, comm_b
     if n:
         assert np.array_equal(out["status"].cpu().numpy(), ref["status"])
         assert np.array_equal(out["makespan"].cpu().numpy(), ref["makespan"])
+
+
+def test_eval_captured_in_cuda_graph(orc, B):
+    """pp_sched_eval once its plan and tables exist launches one kernel and
+    allocates nothing, so a CUDA graph can capture it (the benchmark times its
+    steps that way): several evaluations captured on a side stream, the graph
+    replayed twice after the inputs change in place, every output equal to
+    direct calls and to the oracle."""
+    import torch
+    b = W.hetero_1f1b(n=3001, seed=41)
+    cf, cb, cm = to_dev(b.cost_f), to_dev(b.cost_b), to_dev(b.comm)
+    out = B.evaluate(b.policy, b.P, b.M, 1, cf, cb, b.strides, b.n, comm=cm, comm_strides=b.comm_strides)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for _ in range(3):
+            B.evaluate(b.policy, b.P, b.M, 1, cf, cb, b.strides, b.n, comm=cm, comm_strides=b.comm_strides, out=out,
+                       stream=side)
+    for seed in (42, 43):
+        nb = W.hetero_1f1b(n=3001, seed=seed)
+        cf.copy_(torch.from_numpy(nb.cost_f))
+        cb.copy_(torch.from_numpy(nb.cost_b))
+        cm.copy_(torch.from_numpy(nb.comm))
+        for t in out.values():
+            t.fill_(-5)
+        graph.replay()
+        torch.cuda.synchronize()
+        got = {k: v.cpu().numpy() for k, v in out.items()}
+        assert_same(got, run_oracle(orc, nb, nthreads=NCPU))
