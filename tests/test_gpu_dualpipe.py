@@ -35,6 +35,17 @@ def test_random_batches_every_op(orc, monkeypatch, P, M, m_a, layout, cap1):
         assert (g["status"] == 0).all()
 
 
+@pytest.mark.parametrize("layout", ["inst_minor", "inst_major"])
+def test_costs_shared_by_microbatches(orc, layout):
+    """Costs per (block) only, broadcast over microbatches (stride 0)."""
+    for P, M, m_a in ((4, 12, 6), (8, 17, 9), (16, 9, 0)):
+        b = W.random_batch(W.ONEF1B, P, M, 1, 101, seed=P + M, lo=1, hi=9, layout=layout, stride_mb_zero=True)
+        assert b.strides[2] == 0
+        g = run_gpu_dp(b, m_a, op_times=True)
+        r = run_oracle_dp(orc, b, m_a, op_times=True, nthreads=NCPU)
+        assert_same_zb(g, r, op_times=True)
+
+
 def test_one_route_is_the_1f1b_evaluator(orc):
     """All microbatches on route A is 1F1B: the same makespans, idle ticks and
     bubble pairs as pp_sched_eval's 1F1B kernel."""
