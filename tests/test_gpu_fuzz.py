@@ -1,0 +1,80 @@
+"""Seeded random shapes for every evaluator, every op time against the oracle.
+
+The hand-picked shapes of the other parity tests cover the limits and the
+kernels' switch points; these cases draw P, M, v, the policy, the layout
+(instance-minor with a random row padding, or instance-major), the batch size
+and the cost ranges at random (fixed seeds), so that combinations nobody
+picked are checked too.  Costs include zeros where the schedule allows them
+(GPipe, 1F1B and interleaved; Zero Bubble and DualPipe need F and B >= 1)."""
+import os
+
+import numpy as np
+import pytest
+
+import pipeline_schedule_simulation_gb300.workloads as W
+from gpu_helpers import (assert_same, assert_same_zb, run_gpu, run_gpu_dp, run_gpu_zb, run_oracle, run_oracle_dp,
+                         run_oracle_zb)
+
+pytestmark = pytest.mark.gpu
+
+NCPU = os.cpu_count() or 8
+
+
+def _shape(rng):
+    policy = int(rng.choice([W.GPIPE, W.ONEF1B, W.INTERLEAVED, W.GPIPE_FIFO]))
+    P = int(rng.integers(1, 17))
+    if policy == W.INTERLEAVED:
+        v = int(rng.integers(2, max(3, min(8, 64 // P) + 1)))
+        M = P * int(rng.integers(1, 5))
+    else:
+        v = 1
+        M = int(rng.integers(1, 41))
+    return policy, P, M, v
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_eval_random_shapes(orc, seed):
+    rng = np.random.default_rng(1000 + seed)
+    for _ in range(12):
+        policy, P, M, v = _shape(rng)
+        n = int(rng.integers(1, 140))
+        layout = "inst_minor" if rng.random() < 0.6 else "inst_major"
+        hi = int(rng.choice([3, 20, 500]))
+        b = W.random_batch(policy, P, M, v, n, seed=int(rng.integers(1 << 30)), lo=0, hi=hi,
+                           comm_hi=int(rng.integers(0, 7)), layout=layout, pad_to=int(rng.choice([1, 4, 8])),
+                           stride_mb_zero=bool(rng.random() < 0.25))
+        g = run_gpu(b, op_times=True)
+        r = run_oracle(orc, b, op_times=True, nthreads=NCPU)
+        assert_same(g, r, op_times=True)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_zero_bubble_random_shapes(orc, seed):
+    rng = np.random.default_rng(2000 + seed)
+    for _ in range(10):
+        policy = int(rng.choice([W.ZB1P, W.ZB2P]))
+        P, M = int(rng.integers(1, 17)), int(rng.integers(1, 41))
+        n = int(rng.integers(1, 140))
+        b = W.random_zb(policy, P, M, n, seed=int(rng.integers(1 << 30)), lo=1, hi=int(rng.choice([3, 20, 300])),
+                        w_lo=0, w_hi=int(rng.choice([0, 5, 300])), comm_hi=int(rng.integers(0, 7)),
+                        layout="inst_minor" if rng.random() < 0.5 else "inst_major",
+                        pad_to=int(rng.choice([1, 4])))
+        g = run_gpu_zb(b, op_times=True)
+        r = run_oracle_zb(orc, b, op_times=True, nthreads=NCPU)
+        assert_same_zb(g, r, op_times=True)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_dualpipe_random_shapes(orc, seed):
+    rng = np.random.default_rng(3000 + seed)
+    for _ in range(10):
+        P, M = int(rng.integers(1, 17)), int(rng.integers(1, 41))
+        m_a = int(rng.integers(0, M + 1))
+        n = int(rng.integers(1, 140))
+        b = W.random_batch(W.ONEF1B, P, M, 1, n, seed=int(rng.integers(1 << 30)), lo=1,
+                           hi=int(rng.choice([3, 20, 300])), comm_hi=int(rng.integers(0, 7)),
+                           layout="inst_minor" if rng.random() < 0.5 else "inst_major",
+                           stride_mb_zero=bool(rng.random() < 0.2))
+        g = run_gpu_dp(b, m_a, op_times=True)
+        r = run_oracle_dp(orc, b, m_a, op_times=True, nthreads=NCPU)
+        assert_same_zb(g, r, op_times=True)
