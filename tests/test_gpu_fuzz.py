@@ -32,10 +32,10 @@ def _shape(rng):
     return policy, P, M, v
 
 
-@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("seed", range(24))
 def test_eval_random_shapes(orc, seed):
     rng = np.random.default_rng(1000 + seed)
-    for _ in range(12):
+    for _ in range(16):
         policy, P, M, v = _shape(rng)
         n = int(rng.integers(1, 140))
         layout = "inst_minor" if rng.random() < 0.6 else "inst_major"
@@ -48,10 +48,10 @@ def test_eval_random_shapes(orc, seed):
         assert_same(g, r, op_times=True)
 
 
-@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("seed", range(8))
 def test_zero_bubble_random_shapes(orc, seed):
     rng = np.random.default_rng(2000 + seed)
-    for _ in range(10):
+    for _ in range(16):
         policy = int(rng.choice([W.ZB1P, W.ZB2P]))
         P, M = int(rng.integers(1, 17)), int(rng.integers(1, 41))
         n = int(rng.integers(1, 140))
@@ -64,10 +64,10 @@ def test_zero_bubble_random_shapes(orc, seed):
         assert_same_zb(g, r, op_times=True)
 
 
-@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("seed", range(8))
 def test_dualpipe_random_shapes(orc, seed):
     rng = np.random.default_rng(3000 + seed)
-    for _ in range(10):
+    for _ in range(16):
         P, M = int(rng.integers(1, 17)), int(rng.integers(1, 41))
         m_a = int(rng.integers(0, M + 1))
         n = int(rng.integers(1, 140))
