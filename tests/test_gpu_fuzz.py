@@ -1,4 +1,4 @@
-"""Seeded random shapes for every evaluator, every op time against the oracle.
+"""Seeded random shapes for every evaluator and search, against the oracle.
 
 The hand-picked shapes of the other parity tests cover the limits and the
 kernels' switch points; these cases draw P, M, v, the policy, the layout
@@ -78,3 +78,56 @@ def test_dualpipe_random_shapes(orc, seed):
         g = run_gpu_dp(b, m_a, op_times=True)
         r = run_oracle_dp(orc, b, m_a, op_times=True, nthreads=NCPU)
         assert_same_zb(g, r, op_times=True)
+
+
+def _layers(rng, L):
+    return (rng.integers(1, int(rng.choice([5, 40, 200])), L).astype(np.int32),
+            rng.integers(1, int(rng.choice([5, 80, 400])), L).astype(np.int32),
+            rng.integers(1, int(rng.choice([3, 50])), L).astype(np.int64))
+
+
+def _check_search(got, ref, ncut):
+    import torch
+    torch.cuda.synchronize()
+    assert np.array_equal(got["all_makespan"].cpu().numpy(), ref["all_makespan"])
+    assert int(got["best_idx"].item()) == ref["best_idx"]
+    assert int(got["best_makespan"].item()) == ref["best_makespan"]
+    if ref["best_idx"] >= 0:
+        assert list(got["best_cuts"].cpu().numpy()) == list(ref["first"][1:ncut + 1])
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_searches_random_problems(orc, seed):
+    """The seeded, exhaustive and interleaved searches on random problems:
+    every candidate's makespan (or rejection), the winner and its cuts."""
+    from gpu_helpers import to_dev
+    from pipeline_schedule_simulation_gb300 import binding as B
+    rng = np.random.default_rng(4000 + seed)
+    for _ in range(4):
+        P = int(rng.integers(1, 9))
+        L = int(rng.integers(P, 3 * P + 12))
+        M = int(rng.integers(1, 40))
+        comm = int(rng.integers(0, 5))
+        ltf, ltb, lact = _layers(rng, L)
+        cap = int(lact.sum() * rng.choice([0.3, 1.0, 10.0])) * max(1, min(P, M))
+        d = [to_dev(x) for x in (ltf, ltb, lact)]
+        sd = int(rng.integers(1 << 40))
+        c0, n = int(rng.integers(0, 50)), int(rng.integers(1, 700))
+        _check_search(B.partition_search(*d, P, M, comm, cap, sd, c0, n, all_makespan=True),
+                      orc.search(ltf, ltb, lact, P, M, comm, cap, sd, c0, c0 + n, nthreads=NCPU), P - 1)
+        total = int(orc.binom(L - 1, P - 1))
+        r0 = int(rng.integers(0, total))
+        nr = min(600, total - r0)
+        _check_search(B.partition_search_ranks(*d, P, M, comm, cap, r0, nr, all_makespan=True),
+                      orc.search_ranks(ltf, ltb, lact, P, M, comm, cap, r0, r0 + nr, nthreads=NCPU), P - 1)
+        # interleaved: v >= 2 chunks per device, M a multiple of P, L >= P*v layers
+        Pi = int(rng.integers(1, 5))
+        v = int(rng.integers(2, 4))
+        Li = int(rng.integers(Pi * v, Pi * v + 10))
+        Mi = Pi * int(rng.integers(1, 5))
+        ltf, ltb, lact = _layers(rng, Li)
+        d = [to_dev(x) for x in (ltf, ltb, lact)]
+        capi = int(lact.sum() * rng.choice([0.5, 10.0])) * Mi
+        _check_search(B.partition_search_interleaved(*d, Pi, v, Mi, comm, capi, sd, c0, n, all_makespan=True),
+                      orc.search_interleaved(ltf, ltb, lact, Pi, v, Mi, comm, capi, sd, c0, c0 + n, nthreads=NCPU),
+                      Pi * v - 1)
