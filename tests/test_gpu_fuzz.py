@@ -93,7 +93,8 @@ def _check_search(got, ref, ncut):
     assert int(got["best_idx"].item()) == ref["best_idx"]
     assert int(got["best_makespan"].item()) == ref["best_makespan"]
     if ref["best_idx"] >= 0:
-        assert list(got["best_cuts"].cpu().numpy()) == list(ref["first"][1:ncut + 1])
+        # the buffer holds at least one word; a one-stage split has no cuts
+        assert list(got["best_cuts"].cpu().numpy()[:ncut]) == list(ref["first"][1:ncut + 1])
 
 
 @pytest.mark.parametrize("seed", range(6))
