@@ -132,3 +132,60 @@ def test_searches_random_problems(orc, seed):
         _check_search(B.partition_search_interleaved(*d, Pi, v, Mi, comm, capi, sd, c0, n, all_makespan=True),
                       orc.search_interleaved(ltf, ltb, lact, Pi, v, Mi, comm, capi, sd, c0, c0 + n, nthreads=NCPU),
                       Pi * v - 1)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_many_random_sets(orc, seed):
+    """pp_sched_many_* on random sets of problems (random shapes, layouts,
+    broadcast strides, empty batches, repeated shapes with other strides),
+    prepared from an empty plan cache so the batched builder makes every plan
+    and table; every output of every problem against the oracle."""
+    import torch
+
+    from gpu_helpers import to_dev
+    from pipeline_schedule_simulation_gb300 import binding as B
+    rng = np.random.default_rng(5000 + seed)
+    batches = []
+    for _ in range(int(rng.integers(10, 40))):
+        policy, P, M, v = _shape(rng)
+        n = int(rng.integers(0, 80))
+        batches.append(W.random_batch(policy, P, M, v, n, seed=int(rng.integers(1 << 30)), hi=int(rng.choice([5, 60])),
+                                      comm_hi=int(rng.integers(0, 5)),
+                                      layout="inst_minor" if rng.random() < 0.5 else "inst_major",
+                                      pad_to=int(rng.choice([1, 4])), stride_mb_zero=bool(rng.random() < 0.6)))
+    batches += [W.random_batch(b.policy, b.P, b.M, b.v, 9, seed=7, hi=9, layout="inst_major") for b in batches[:3]]
+    problems = [{"policy": b.policy, "P": b.P, "M": b.M, "v": b.v, "n": b.n, "strides": b.strides,
+                 "cost_f": to_dev(b.cost_f), "cost_b": to_dev(b.cost_b), "comm": to_dev(b.comm) if b.n else None,
+                 "comm_strides": b.comm_strides} for b in batches]
+    B.cache_clear()
+    many = B.Many(problems)
+    outs = many()
+    torch.cuda.synchronize()
+    for b, o in zip(batches, outs):
+        got = {k: o[k].cpu().numpy() for k in ("makespan", "idle", "bub_num", "bub_den", "peak", "status")}
+        ref = run_oracle(orc, b, nthreads=NCPU)
+        assert np.array_equal(got["peak"], ref["peak"])
+        if b.n:
+            assert_same(got, ref)
+    many.close()
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_separate_backward_latency_random(orc, seed):
+    """pp_sched_eval_fb (a latency of its own on backward edges) on random
+    shapes of every policy, every op time against the oracle."""
+    from gpu_helpers import to_dev
+    from pipeline_schedule_simulation_gb300 import binding as B
+    rng = np.random.default_rng(6000 + seed)
+    for _ in range(10):
+        policy, P, M, v = _shape(rng)
+        n = int(rng.integers(1, 100))
+        b = W.random_batch(policy, P, M, v, n, seed=int(rng.integers(1 << 30)), hi=20, comm_hi=5,
+                           layout="inst_minor" if rng.random() < 0.5 else "inst_major")
+        comm_b = rng.integers(0, 7, b.comm.shape).astype(np.int32)
+        out = B.evaluate(b.policy, b.P, b.M, b.v, to_dev(b.cost_f), to_dev(b.cost_b), b.strides, b.n,
+                         comm=to_dev(b.comm), comm_strides=b.comm_strides, op_times=True, comm_b=to_dev(comm_b))
+        got = {k: t.cpu().numpy() for k, t in out.items()}
+        ref = orc.eval_batch(b.policy, b.P, b.M, b.v, b.cost_f, b.cost_b, b.strides, comm=b.comm,
+                             comm_strides=b.comm_strides, n=b.n, op_times=True, nthreads=NCPU, comm_b=comm_b)
+        assert_same(got, ref, op_times=True)
