@@ -189,3 +189,30 @@ def test_separate_backward_latency_random(orc, seed):
         ref = orc.eval_batch(b.policy, b.P, b.M, b.v, b.cost_f, b.cost_b, b.strides, comm=b.comm,
                              comm_strides=b.comm_strides, n=b.n, op_times=True, nthreads=NCPU, comm_b=comm_b)
         assert_same(got, ref, op_times=True)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_host_entry_random(orc, seed):
+    """pp_sched_eval_host from pinned host buffers on random shapes, batch
+    sizes and workspace sizes (from one 32-instance chunk to the whole batch,
+    so every chunking and both the one-slot and two-slot paths run); every
+    output against the oracle, two calls in a row with the same staging."""
+    import torch
+
+    from pipeline_schedule_simulation_gb300 import binding as B
+    rng = np.random.default_rng(7000 + seed)
+    for _ in range(6):
+        policy, P, M, v = _shape(rng)
+        n = int(rng.integers(1, 3000))
+        lo_ws = int(B.LIB.pp_sched_eval_host_workspace(P, M, v, 32))
+        hi_ws = int(B.LIB.pp_sched_eval_host_workspace(P, M, v, n))
+        ws = int(rng.choice([lo_ws, (lo_ws + hi_ws) // 2, hi_ws]))
+        ws = (ws + 255) // 256 * 256
+        staging = {}
+        for call in range(2):
+            b = W.random_batch(policy, P, M, v, n, seed=int(rng.integers(1 << 30)), hi=30, comm_hi=5)
+            hf, hb, hc = (torch.from_numpy(x).pin_memory() for x in (b.cost_f, b.cost_b, b.comm))
+            host, _, _ = B.evaluate_host(policy, P, M, v, hf, hb, n, comm=hc, staging=staging, workspace_bytes=ws)
+            torch.cuda.synchronize()
+            got = {k: t.numpy().copy() for k, t in host.items()}
+            assert_same(got, run_oracle(orc, b, nthreads=NCPU))
