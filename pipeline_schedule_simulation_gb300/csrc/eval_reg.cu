@@ -203,12 +203,12 @@ __device__ __forceinline__ void run_round(RegState<PMAX, NI> &S, uint64_t w, con
 // in the alternating case), so the instances' state stays in the same
 // registers across iterations; warmup and cooldown rounds are dispatched one
 // at a time by their round word.  Copies run D = kAhead2 rounds ahead, one
-// cp.async group per round.  A step waits for its rounds' groups, runs their
-// bodies and only then issues the copies D rounds ahead: those land in the
-// slices of the two rounds before the step, which every lane finished reading
-// before the step's warp barrier, and the address work of the copies overlaps
-// the bodies' arithmetic.  The table loader reads its entries two rounds
-// before it issues them, so no shared-memory load sits on the issue path.
+// cp.async group per round.  A step waits for its rounds' groups, then issues
+// the copies D rounds ahead before it runs their bodies: those copies land in
+// the slices of the two rounds before the step, which every lane finished
+// reading before the step's warp barrier, so they are in flight while the
+// bodies compute.  The table loader reads its entries two rounds before it
+// issues them, so no shared-memory load sits on the issue path.
 template <int PMAX, int NI, bool VEC, bool OPS, bool LT>
 __global__ void __maxnreg__(PMAX == 16 ? 168 : 96) k_eval_reg(const EvalArgs a) {
     copy_peak(a);
@@ -254,17 +254,27 @@ __global__ void __maxnreg__(PMAX == 16 ? 168 : 96) k_eval_reg(const EvalArgs a) 
     uint32_t negc[NI];
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
-        negc[i] = 0;
         S.flag[i] = 0;
 #pragma unroll
         for (int k = 0; k < PMAX; ++k) {
-            int c = 0;
-            if (a.comm && L.live[i] && k < a.P - 1) c = a.comm[L.x[i] * a.c_inst + (int64_t)k * a.c_bnd];
-            negc[i] |= (uint32_t)c;
-            S.cF[i][k] = (uint32_t)c;
             S.fr[i][k] = 0; S.rf[i][k] = 0; S.rb[i][k] = 0; S.busy[i][k] = 0;
         }
     }
+    // the comm values; loaded once the first rounds' cost copies are in
+    // flight, so their latency hides behind the copies'
+    auto load_comm = [&]() {
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            negc[i] = 0;
+#pragma unroll
+            for (int k = 0; k < PMAX; ++k) {
+                int c = 0;
+                if (a.comm && L.live[i] && k < a.P - 1) c = a.comm[L.x[i] * a.c_inst + (int64_t)k * a.c_bnd];
+                negc[i] |= (uint32_t)c;
+                S.cF[i][k] = (uint32_t)c;
+            }
+        }
+    };
 #pragma unroll
     for (int k = 0; k < PMAX; ++k) S.cnt[k] = 0;
     if constexpr (LT) {
@@ -328,19 +338,20 @@ __global__ void __maxnreg__(PMAX == 16 ? 168 : 96) k_eval_reg(const EvalArgs a) 
         auto step1 = [&](int r, auto &&body) {
             cp_async_wait<D - 1>();
             __syncwarp();
-            body(slice(r));
             issue(r + D, full);
+            body(slice(r));
         };
         auto step2 = [&](int r, auto &&body0, auto &&body1) {
             cp_async_wait<D - 2>();
             __syncwarp();
-            body0(slice(r));
-            body1(slice(r + 1));
             issue(r + D, full);
             issue(r + D + 1, full);
+            body0(slice(r));
+            body1(slice(r + 1));
         };
 #pragma unroll 1
         for (int q = 0; q < D; ++q) issue(q, full);
+        load_comm();
 #pragma unroll 1
         for (int si = 0; si < a.nseg; ++si) {
             const uint4 sg = segs[si];
