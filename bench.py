@@ -365,20 +365,36 @@ def main():
     # The timed region: the K evaluations captured once in a CUDA graph (each
     # node one evaluation of the whole batch, in stream order) and replayed
     # once, so consecutive evaluations are not separated by host launch gaps.
-    # The same K evaluations launched one by one are timed too and reported.
+    # Where this PyTorch can record timing events inside a captured graph
+    # (external events), the graph's first and last nodes are such events and
+    # the K evaluations are timed between them on the device; the events on
+    # the stream around the replay, which also count the host's graph launch,
+    # are reported beside them.  The same K evaluations launched one by one
+    # are timed too and reported.
     graph = None
+    inner = None
     try:
         side = torch.cuda.Stream()
         side.wait_stream(stream)
+        try:
+            inner = (torch.cuda.Event(enable_timing=True, external=True),
+                     torch.cuda.Event(enable_timing=True, external=True))
+        except TypeError:
+            inner = None
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=side):
+            if inner:
+                inner[0].record(side)
             for _ in range(K):
                 B.evaluate(batch.policy, P, M, 1, cf, cb, batch.strides, n, comm=cm,
                            comm_strides=batch.comm_strides, out=outs, stream=side)
+            if inner:
+                inner[1].record(side)
         graph.replay()
         torch.cuda.synchronize()
     except Exception as e:  # the timed region then launches the evaluations one by one
         graph = None
+        inner = None
         graph_error = str(e)[:200]
 
     def direct():
@@ -388,6 +404,9 @@ def main():
     h0 = time.perf_counter()
     elapsed = region(graph.replay if graph is not None else direct)
     h1 = time.perf_counter()
+    outer_s = elapsed
+    if inner:
+        elapsed = inner[0].elapsed_time(inner[1]) / 1e3
     # A short timed region gives few clock samples: keep running the same step,
     # untimed, until the sampler holds at least 25 samples under load (at
     # least 0.1 s, at most 2 s).
@@ -400,9 +419,9 @@ def main():
     sampler.__exit__(None, None, None)
     direct_s = region(direct)
     if world > 1:
-        t = torch.tensor([elapsed, direct_s], device="cuda", dtype=torch.float64)
+        t = torch.tensor([elapsed, direct_s, outer_s], device="cuda", dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed, direct_s = float(t[0].item()), float(t[1].item())
+        elapsed, direct_s, outer_s = float(t[0].item()), float(t[1].item()), float(t[2].item())
     ops_step = 2 * P * M * n
     value = world * ops_step * K / elapsed
     kavg = elapsed / K  # one kernel launch per evaluation
@@ -453,10 +472,16 @@ def main():
                          "peak": peak_gbs, "unit": "GB/s", "frac": achieved / peak_gbs,
                          "peak_source": peak_src, "traffic": profiled_traffic(),
                          "algorithmic_bytes_per_launch": abytes, "avg_launch_us": kavg * 1e6,
+                         "graph_replay_us": outer_s / K * 1e6,
+                         "graph_replay_frac": abytes / (outer_s / K) / 1e9 / peak_gbs,
                          "direct_launch_us": direct_s / K * 1e6,
                          "direct_launch_frac": abytes / (direct_s / K) / 1e9 / peak_gbs},
-            "timing": ("K evaluations captured in one CUDA graph and replayed once; CUDA events on the "
-                       "launching stream around the replay; average launch = elapsed / K"
+            "timing": (("K evaluations captured in one CUDA graph and replayed once; CUDA events captured as "
+                        "the graph's first and last nodes (device time of the K evaluations); average launch "
+                        "= elapsed / K; graph_replay_us: events on the stream around the replay, host graph "
+                        "launch included" if inner else
+                        "K evaluations captured in one CUDA graph and replayed once; CUDA events on the "
+                        "launching stream around the replay; average launch = elapsed / K")
                        if graph is not None else f"K direct launches (graph capture failed: {graph_error})"),
             "instances_per_s": world * n * K / elapsed,
             "clocks": sampler.summary(timed=(h0, h1)),
