@@ -126,6 +126,78 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _reach(count, strides):
+    """Elements a strided access reaches from its base pointer: 1 + the largest
+    offset sum((extent - 1) * stride), or 0 when any extent is 0.  `count` and
+    `strides` pair each extent with its element stride."""
+    if any(c <= 0 for c in count):
+        return 0
+    return 1 + sum((c - 1) * int(st) for c, st in zip(count, strides))
+
+
+def _arg(t, name, dtype, device, reach, host=False):
+    """Refuse, before any library call, a buffer the library would address
+    wrongly: not a tensor, on the wrong device (CUDA device `device`, or the
+    CPU for host inputs), of the wrong dtype, or too short for the `reach`
+    elements its strides address from its data pointer (the library reads raw
+    pointers and element strides, not the tensor's own shape)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if host:
+        if t.device.type != "cpu":
+            raise ValueError(f"{name}: expected a host (CPU) tensor, got one on {t.device}")
+    elif t.device.type != "cuda" or (device is not None and t.device != device):
+        raise ValueError(f"{name}: expected a tensor on {device or 'a CUDA device'}, got one on {t.device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected dtype {dtype}, got {t.dtype}")
+    avail = t.untyped_storage().nbytes() // t.element_size() - t.storage_offset()
+    if reach > avail:
+        raise ValueError(f"{name}: the strides reach {reach} elements from its data pointer but its storage "
+                         f"holds {avail}")
+    return t
+
+
+def _inputs(P, M, v, S, cost_tensors, strides, n, comm_tensors, comm_strides):
+    """Check the cost tables (int32, indexed (instance, stage, microbatch)) and
+    the comm tables (int32, (instance, boundary)) of one evaluation; returns
+    their device."""
+    dev = next((t.device for _, t in cost_tensors if isinstance(t, torch.Tensor) and t.is_cuda), None)
+    if len(strides) != 3 or len(comm_strides) != 2:
+        raise ValueError("strides must be (inst, stage, mb) and comm_strides (inst, boundary)")
+    if min(int(x) for x in strides) < 0 or min(int(x) for x in comm_strides) < 0:
+        raise ValueError("strides must be non-negative")
+    reach = _reach((n, S, M), strides)
+    for name, t in cost_tensors:
+        if t is not None:  # a missing table is the library's argument error
+            _arg(t, name, torch.int32, dev, reach)
+    creach = _reach((n, S - 1), comm_strides)
+    for name, t in comm_tensors:
+        if t is not None:
+            _arg(t, name, torch.int32, dev, creach)
+    return dev
+
+
+def _check_outputs(out, n, P, op_count, op_strides, op_names, peak_per_instance=False):
+    """The summary outputs hold n (makespan, bub_num, bub_den, status), n*P
+    (idle) and P or n*P (peak) elements; the per-op outputs reach what their
+    (instance, op) strides address."""
+    sizes = {"makespan": n, "bub_num": n, "bub_den": n, "status": n, "idle": n * P,
+             "peak": n * P if peak_per_instance else P}
+    for k, need in sizes.items():
+        t = out.get(k)
+        if t is not None and n > 0:
+            avail = t.untyped_storage().nbytes() // t.element_size() - t.storage_offset()
+            if need > avail:
+                raise ValueError(f"{k}: needs {need} elements, its storage holds {avail}")
+    for k in op_names:
+        t = out.get(k)
+        if t is not None:
+            reach = _reach(op_count, op_strides)
+            avail = t.untyped_storage().nbytes() // t.element_size() - t.storage_offset()
+            if reach > avail:
+                raise ValueError(f"{k}: the op strides reach {reach} elements, its storage holds {avail}")
+
+
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -180,13 +252,14 @@ def evaluate(policy, P, M, v, cost_f, cost_b, strides, n, comm=None, comm_stride
     `out` may supply preallocated ones.  op_times adds op_start / op_end
     [n][P][O] (or through op_strides = (inst, op))."""
     pol = _policy(policy)
-    dev = cost_f.device
+    dev = _inputs(P, M, v, P * v, (("cost_f", cost_f), ("cost_b", cost_b)), strides, n,
+                  (("comm", comm), ("comm_b", comm_b)), comm_strides)
     out = dict(out or {})
     O = 2 * M * v
 
     def want(name, shape, dtype):
         if name in out:
-            return out[name]
+            return _arg(out[name], name, dtype, dev, 0)
         t = torch.empty(shape, dtype=dtype, device=dev)
         out[name] = t
         return t
@@ -203,8 +276,10 @@ def evaluate(policy, P, M, v, cost_f, cost_b, strides, n, comm=None, comm_stride
         oe = want("op_end", (n, P, O), torch.int32)
         if op_strides is None:
             op_strides = (P * O, 1)
+        _check_outputs(out, n, P, (n, P * O), op_strides, ("op_start", "op_end"))
     else:
         op_strides = (0, 0)
+    _check_outputs(out, n, P, None, None, ())
     if comm_b is not None:
         rc = LIB.pp_sched_eval_fb(pol, P, M, v, _ptr(cost_f), _ptr(cost_b), strides[0], strides[1], strides[2],
                                   _ptr(comm), _ptr(comm_b), comm_strides[0], comm_strides[1], n,
@@ -230,12 +305,13 @@ def evaluate_dualpipe(P, M, m_a, cost_f, cost_b, strides, n, comm=None, comm_str
     element strides; comm (instance, link).  Returns a dict of CUDA tensors;
     `peak` is per instance [n][P].  op_times adds op_start / op_end
     [n][P blocks][2][M] (kind 0 = F, 1 = B), or through op_strides = (inst, op)."""
-    dev = cost_f.device
+    dev = _inputs(P, M, 1, P, (("cost_f", cost_f), ("cost_b", cost_b)), strides, n, (("comm", comm),),
+                  comm_strides)
     out = dict(out or {})
 
     def want(name, shape, dtype):
         if name in out:
-            return out[name]
+            return _arg(out[name], name, dtype, dev, 0)
         t = torch.empty(shape, dtype=dtype, device=dev)
         out[name] = t
         return t
@@ -252,8 +328,10 @@ def evaluate_dualpipe(P, M, m_a, cost_f, cost_b, strides, n, comm=None, comm_str
         oe = want("op_end", (n, P, 2, M), torch.int32)
         if op_strides is None:
             op_strides = (P * 2 * M, 1)
+        _check_outputs(out, n, P, (n, P * 2 * M), op_strides, ("op_start", "op_end"), True)
     else:
         op_strides = (0, 0)
+    _check_outputs(out, n, P, None, None, (), True)
     rc = LIB.pp_sched_eval_dualpipe(P, M, m_a, _ptr(cost_f), _ptr(cost_b), strides[0], strides[1], strides[2],
                                     _ptr(comm), comm_strides[0], comm_strides[1], n, _ptr(mk), _ptr(idle),
                                     _ptr(bn), _ptr(bd), _ptr(pk), _ptr(os_), _ptr(oe), op_strides[0],
@@ -272,12 +350,13 @@ def evaluate_zb(policy, P, M, cost_f, cost_b, cost_w, strides, n, comm=None, com
     adds op_start / op_end [n][P][3][M] (kind 0 = F, 1 = B, 2 = W), or through
     op_strides = (inst, op)."""
     pol = _policy(policy)
-    dev = cost_f.device
+    dev = _inputs(P, M, 1, P, (("cost_f", cost_f), ("cost_b", cost_b), ("cost_w", cost_w)), strides, n,
+                  (("comm", comm),), comm_strides)
     out = dict(out or {})
 
     def want(name, shape, dtype):
         if name in out:
-            return out[name]
+            return _arg(out[name], name, dtype, dev, 0)
         t = torch.empty(shape, dtype=dtype, device=dev)
         out[name] = t
         return t
@@ -294,8 +373,10 @@ def evaluate_zb(policy, P, M, cost_f, cost_b, cost_w, strides, n, comm=None, com
         oe = want("op_end", (n, P, 3, M), torch.int32)
         if op_strides is None:
             op_strides = (P * 3 * M, 1)
+        _check_outputs(out, n, P, (n, P * 3 * M), op_strides, ("op_start", "op_end"), True)
     else:
         op_strides = (0, 0)
+    _check_outputs(out, n, P, None, None, (), True)
     rc = LIB.pp_sched_eval_zb(pol, P, M, _ptr(cost_f), _ptr(cost_b), _ptr(cost_w), strides[0], strides[1],
                               strides[2], _ptr(comm), comm_strides[0], comm_strides[1], n,
                               _ptr(mk), _ptr(idle), _ptr(bn), _ptr(bd), _ptr(pk), _ptr(os_), _ptr(oe),
@@ -322,14 +403,19 @@ class Many:
         for i, q in enumerate(problems):
             P, n = q["P"], q["n"]
             out = dict(q.get("out") or {})
-            dev = q["cost_f"].device
+            comm = q.get("comm")
+            cs = q.get("comm_strides", (0, 0))
+            v = q.get("v", 1)
+            dev = _inputs(P, q["M"], v, P * v, (("cost_f", q["cost_f"]), ("cost_b", q["cost_b"])), q["strides"],
+                          n, (("comm", comm),), cs)
             for k, shape, dt in (("makespan", (n,), torch.int32), ("idle", (n, P), torch.int32),
                                  ("bub_num", (n,), torch.int64), ("bub_den", (n,), torch.int64),
                                  ("peak", (P,), torch.int32), ("status", (n,), torch.int8)):
                 if k not in out:
                     out[k] = torch.empty(shape, dtype=dt, device=dev)
-            comm = q.get("comm")
-            cs = q.get("comm_strides", (0, 0))
+                else:
+                    _arg(out[k], k, dt, dev, 0)
+            _check_outputs(out, n, P, None, None, ())
             si, ss, sm = q["strides"]
             arr[i] = Problem(_policy(q["policy"]), P, q["M"], q.get("v", 1), _ptr(q["cost_f"]), _ptr(q["cost_b"]),
                              si, ss, sm, _ptr(comm), cs[0], cs[1], n, _ptr(out["makespan"]), _ptr(out["idle"]),
@@ -374,6 +460,12 @@ def evaluate_host(policy, P, M, v, cost_f, cost_b, n, comm=None, stream=None, st
     outputs are valid once the stream has completed."""
     staging = staging if staging is not None else {}
     S = P * v
+    for name, t, count in (("cost_f", cost_f, S * M * n), ("cost_b", cost_b, S * M * n),
+                           ("comm", comm, max(S - 1, 0) * n)):
+        if t is not None:
+            _arg(t, name, torch.int32, None, count, host=True)
+            if not t.is_contiguous():
+                raise ValueError(f"{name}: the host entry reads a contiguous [S][M][n] table")
     need = LIB.pp_sched_eval_host_workspace(P, M, v, n)
     want_ws = int(workspace_bytes) if workspace_bytes is not None else int(need)
     ws = staging.get("workspace")
@@ -400,12 +492,31 @@ def evaluate_host(policy, P, M, v, cost_f, cost_b, n, comm=None, stream=None, st
     return host, h2d, d2h
 
 
+def _layers(layer_tf, layer_tb, layer_act):
+    """The per-layer tables of a search: int32 t_f and t_b, int64 activation
+    bytes, one entry per layer, on one CUDA device; returns (L, device)."""
+    L = layer_tf.numel() if isinstance(layer_tf, torch.Tensor) else 0
+    dev = layer_tf.device if isinstance(layer_tf, torch.Tensor) and layer_tf.is_cuda else None
+    _arg(layer_tf, "layer_tf", torch.int32, dev, L)
+    _arg(layer_tb, "layer_tb", torch.int32, dev, L)
+    _arg(layer_act, "layer_act", torch.int64, dev, L)
+    return L, dev
+
+
+def _search_outputs(bi, bm, bc, am, ncuts, ncand, dev):
+    _arg(bi, "best_idx", torch.int64, dev, 1)
+    _arg(bm, "best_makespan", torch.int32, dev, 1)
+    _arg(bc, "best_cuts", torch.int32, dev, ncuts)
+    if am is not None:
+        _arg(am, "all_makespan", torch.int32, dev, ncand)
+
+
 def partition_search(layer_tf, layer_tb, layer_act, P, M, comm, cap, seed, cand_begin, n_cand,
                      all_makespan=False, out=None, stream=None):
     """Call pp_sched_partition_search; layer arrays are CUDA tensors (int32,
     int32, int64).  Returns dict(best_idx int64[1], best_makespan int32[1],
     best_cuts int32[P-1], all_makespan int32[n_cand] if requested)."""
-    dev = layer_tf.device
+    L, dev = _layers(layer_tf, layer_tb, layer_act)
     out = dict(out or {})
     bi = out.setdefault("best_idx", torch.empty(1, dtype=torch.int64, device=dev))
     bm = out.setdefault("best_makespan", torch.empty(1, dtype=torch.int32, device=dev))
@@ -413,7 +524,7 @@ def partition_search(layer_tf, layer_tb, layer_act, P, M, comm, cap, seed, cand_
     am = None
     if all_makespan:
         am = out.setdefault("all_makespan", torch.empty(n_cand, dtype=torch.int32, device=dev))
-    L = layer_tf.numel()
+    _search_outputs(bi, bm, bc, am, max(P - 1, 1), n_cand, dev)
     rc = LIB.pp_sched_partition_search(_ptr(layer_tf), _ptr(layer_tb), _ptr(layer_act), L, P, M,
                                        int(comm), int(cap), ctypes.c_uint64(seed & (2**64 - 1)),
                                        int(cand_begin), int(n_cand), _ptr(bi), _ptr(bm),
@@ -427,7 +538,7 @@ def partition_search_ranks(layer_tf, layer_tb, layer_act, P, M, comm, cap, rank_
     """Call pp_sched_partition_search_ranks (the exhaustive search over colex
     ranks [rank_begin, rank_begin + n_ranks)).  Returns dict(best_idx (the
     winning rank) int64[1], best_makespan, best_cuts, all_makespan if asked)."""
-    dev = layer_tf.device
+    L, dev = _layers(layer_tf, layer_tb, layer_act)
     out = dict(out or {})
     bi = out.setdefault("best_idx", torch.empty(1, dtype=torch.int64, device=dev))
     bm = out.setdefault("best_makespan", torch.empty(1, dtype=torch.int32, device=dev))
@@ -435,7 +546,7 @@ def partition_search_ranks(layer_tf, layer_tb, layer_act, P, M, comm, cap, rank_
     am = None
     if all_makespan:
         am = out.setdefault("all_makespan", torch.empty(n_ranks, dtype=torch.int32, device=dev))
-    L = layer_tf.numel()
+    _search_outputs(bi, bm, bc, am, max(P - 1, 1), n_ranks, dev)
     rc = LIB.pp_sched_partition_search_ranks(_ptr(layer_tf), _ptr(layer_tb), _ptr(layer_act), L, P, M,
                                              int(comm), int(cap), int(rank_begin), int(n_ranks), _ptr(bi),
                                              _ptr(bm), _ptr(bc) if P > 1 else None, _ptr(am), _stream(stream))
@@ -447,7 +558,7 @@ def partition_search_interleaved(layer_tf, layer_tb, layer_act, P, v, M, comm, c
                                  all_makespan=False, out=None, stream=None):
     """Call pp_sched_partition_search_interleaved (S = P*v ranges).  Returns
     dict(best_idx, best_makespan, best_cuts int32[S-1], all_makespan)."""
-    dev = layer_tf.device
+    L, dev = _layers(layer_tf, layer_tb, layer_act)
     out = dict(out or {})
     bi = out.setdefault("best_idx", torch.empty(1, dtype=torch.int64, device=dev))
     bm = out.setdefault("best_makespan", torch.empty(1, dtype=torch.int32, device=dev))
@@ -455,7 +566,7 @@ def partition_search_interleaved(layer_tf, layer_tb, layer_act, P, v, M, comm, c
     am = None
     if all_makespan:
         am = out.setdefault("all_makespan", torch.empty(n_cand, dtype=torch.int32, device=dev))
-    L = layer_tf.numel()
+    _search_outputs(bi, bm, bc, am, P * v - 1, n_cand, dev)
     rc = LIB.pp_sched_partition_search_interleaved(_ptr(layer_tf), _ptr(layer_tb), _ptr(layer_act), L, P, v, M,
                                                    int(comm), int(cap), ctypes.c_uint64(seed & (2**64 - 1)),
                                                    int(cand_begin), int(n_cand), _ptr(bi), _ptr(bm), _ptr(bc),
