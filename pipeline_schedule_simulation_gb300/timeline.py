@@ -5,8 +5,15 @@ Perfetto open) or CSV.
 The times come from the library (op_start / op_end of pp_sched_eval,
 pp_sched_eval_zb or pp_sched_eval_dualpipe); this module only formats them.
 Each record is one op: device, kind ("F", "B" or, for Zero Bubble, "W"),
-chunk, microbatch, start and end tick, and for DualPipe the route ("A" enters
-at device 0, "B" at device P-1).
+chunk, microbatch, start and end tick, its phase on the device, and for
+DualPipe the route ("A" enters at device 0, "B" at device P-1).
+
+Phases ("1F1B" §3.1's warmup / steady / cooldown, asked per stage by "Pipeline
+scheduling" (M040) §09's checklist), read off each device's op order: the
+warmup is the run of forwards before the device's first backward (P - k of
+them on device k under 1F1B, the pages' count), the cooldown is everything
+after its last forward, the steady phase everything between.  GPipe has no
+steady phase: all forwards are its warmup, all backwards its cooldown.
 """
 from __future__ import annotations
 
@@ -54,7 +61,43 @@ def records(op_start, op_end, ops=None, zb=False, dualpipe_m_a=None):
                 w = int(ops[k, j])
                 out.append(dict(device=k, kind=KINDS[(w >> 31) & 1], chunk=(w >> 24) & 0x7F, mb=w & 0xFFFFFF,
                                 start=int(st[k, j]), end=int(en[k, j])))
-    out.sort(key=lambda r: (r["device"], r["start"], r["end"]))
+    if dualpipe_m_a is not None or zb:
+        # no plan order: a device's order is its time order (F and B take at
+        # least one tick, so they never tie; a W never precedes its B)
+        out.sort(key=lambda r: (r["device"], r["start"], r["end"]))
+        _label_phases(out)
+    else:
+        _label_phases(out)  # plan order: records were built device by device in op order
+        out.sort(key=lambda r: (r["device"], r["start"], r["end"]))
+    return out
+
+
+def _label_phases(recs):
+    """Add each record's phase; `recs` lists each device's ops contiguously in
+    the device's order."""
+    by_dev = {}
+    for r in recs:
+        by_dev.setdefault(r["device"], []).append(r)
+    for dev in by_dev.values():
+        kinds = [r["kind"] for r in dev]
+        first_b = kinds.index("B") if "B" in kinds else len(kinds)
+        last_f = len(kinds) - 1 - kinds[::-1].index("F") if "F" in kinds else -1
+        for i, r in enumerate(dev):
+            r["phase"] = "warmup" if i < first_b else ("cooldown" if i > last_f else "steady")
+
+
+def phase_summary(recs):
+    """Per device and phase: op count, first start and last end tick (None
+    for an empty phase), and busy ticks."""
+    out = []
+    for k in sorted({r["device"] for r in recs}):
+        row = {"device": k}
+        for ph in ("warmup", "steady", "cooldown"):
+            rs = [r for r in recs if r["device"] == k and r["phase"] == ph]
+            row[ph] = {"ops": len(rs), "start": min((r["start"] for r in rs), default=None),
+                       "end": max((r["end"] for r in rs), default=None),
+                       "busy": sum(r["end"] - r["start"] for r in rs)}
+        out.append(row)
     return out
 
 
@@ -69,7 +112,8 @@ def chrome_trace(recs, us_per_tick=1.0, name="schedule"):
             (f".{r['route']}" if "route" in r else "")
         events.append({"name": label, "cat": r["kind"], "ph": "X", "pid": 0, "tid": r["device"],
                        "ts": r["start"] * us_per_tick, "dur": (r["end"] - r["start"]) * us_per_tick,
-                       "args": {"chunk": r["chunk"], "mb": r["mb"], "start": r["start"], "end": r["end"]}})
+                       "args": {"chunk": r["chunk"], "mb": r["mb"], "start": r["start"], "end": r["end"],
+                                "phase": r["phase"]}})
     return {"traceEvents": events, "displayTimeUnit": "ms"}
 
 
@@ -79,7 +123,8 @@ def write_chrome_trace(path, recs, us_per_tick=1.0, name="schedule"):
 
 
 def write_csv(path, recs):
-    fields = ["device", "kind", "chunk", "mb", "start", "end"] + (["route"] if recs and "route" in recs[0] else [])
+    fields = ["device", "kind", "chunk", "mb", "start", "end", "phase"] + \
+        (["route"] if recs and "route" in recs[0] else [])
     with open(path, "w", newline="") as f:
         w = csv.DictWriter(f, fieldnames=fields)
         w.writeheader()

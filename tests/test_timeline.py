@@ -33,7 +33,7 @@ def test_records_and_trace_from_plan_order(orc, tmp_path):
     c = tmp_path / "t.csv"
     T.write_csv(c, recs)
     rows = list(csv.DictReader(open(c)))
-    assert len(rows) == 32 and rows[0].keys() == {"device", "kind", "chunk", "mb", "start", "end"}
+    assert len(rows) == 32 and rows[0].keys() == {"device", "kind", "chunk", "mb", "start", "end", "phase"}
 
 
 def test_records_zero_bubble(orc):
@@ -63,4 +63,56 @@ def test_records_dualpipe(orc, tmp_path):
     c = tmp_path / "dp.csv"
     T.write_csv(c, recs)
     rows = list(csv.DictReader(open(c)))
-    assert rows[0].keys() == {"device", "kind", "chunk", "mb", "start", "end", "route"}
+    assert rows[0].keys() == {"device", "kind", "chunk", "mb", "start", "end", "phase", "route"}
+
+
+def _summary(orc, policy, P, M, v=1):
+    r = orc.evaluate(policy, P, M, v, 1, 2, 1)
+    return T.phase_summary(T.records(r["start"], r["end"], _packed(r["kind"], r["chunk"], r["mb"]))), r
+
+
+def test_phases_1f1b_and_gpipe(orc):
+    """1F1B device k: P-k forwards of warmup ("1F1B" §3.1, the pages' count
+    before the first backward), then 2(M-P+k) steady ops, then P-k backwards
+    of cooldown; with M < P-k the warmup is all M forwards and nothing is
+    steady.  GPipe: every forward warmup, every backward cooldown."""
+    for P, M in ((4, 8), (8, 16), (5, 3)):
+        summ, _ = _summary(orc, "1f1b", P, M)
+        for row in summ:
+            k, w = row["device"], min(P - row["device"], M)
+            assert (row["warmup"]["ops"], row["steady"]["ops"], row["cooldown"]["ops"]) == (w, 2 * (M - w), w)
+            # the warmup runs first, the cooldown last, without overlap
+            if row["steady"]["ops"]:
+                assert row["warmup"]["end"] <= row["steady"]["start"]
+                assert row["steady"]["end"] <= row["cooldown"]["start"]
+            assert row["warmup"]["busy"] == w * 1 and row["cooldown"]["busy"] == w * 2
+        summ, _ = _summary(orc, "gpipe", P, M)
+        assert all((x["warmup"]["ops"], x["steady"]["ops"], x["cooldown"]["ops"]) == (M, 0, M) for x in summ)
+
+
+def test_phases_interleaved(orc):
+    """Interleaved 1F1B (reading R4): device k runs min(vP + P - 1 - 2k, vM)
+    forwards before its first backward, so that is its warmup."""
+    for P, M, v in ((4, 8, 2), (4, 4, 3), (8, 16, 2)):
+        summ, _ = _summary(orc, "interleaved", P, M, v)
+        for row in summ:
+            k = row["device"]
+            w = min(v * P + P - 1 - 2 * k, v * M)
+            assert row["warmup"]["ops"] == w
+            assert row["warmup"]["ops"] + row["steady"]["ops"] + row["cooldown"]["ops"] == 2 * M * v
+
+
+def test_phases_zero_bubble_and_dualpipe(orc):
+    """Zero Bubble with free W keeps 1F1B's F/B order, so its warmup is 1F1B's;
+    every W falls after the warmup.  DualPipe: phases cover every op."""
+    P, M = 4, 8
+    r = orc.zb_evaluate("zb1p", P, M, 1, 2, 0)
+    summ = T.phase_summary(T.records(r["start"], r["end"], zb=True))
+    for row in summ:
+        assert row["warmup"]["ops"] == min(P - row["device"], M)
+    recs = T.records(r["start"], r["end"], zb=True)
+    assert all(x["phase"] != "warmup" for x in recs if x["kind"] == "W")
+    rng = np.random.default_rng(4)
+    d = orc.dp_evaluate(P, 4, 4, rng.integers(1, 5, (P, 8)), rng.integers(1, 5, (P, 8)), rng.integers(0, 3, P - 1))
+    summ = T.phase_summary(T.records(d["start"], d["end"], dualpipe_m_a=4))
+    assert sum(x[ph]["ops"] for x in summ for ph in ("warmup", "steady", "cooldown")) == 2 * P * 8
