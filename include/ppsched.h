@@ -450,6 +450,22 @@ const char *pp_sched_status_str(int code);
  * evaluations are in flight. */
 void pp_sched_cache_clear(void);
 
+/* The bounds-checked build.  (No counterpart on the pages: a debugging aid for
+ * machines without a GPU memory checker.)  Compiled with -DPPS_CHECKED, the
+ * kernels check every address they take from a run-time table or from the
+ * call's sizes before using it: cost elements against what the strides reach,
+ * value-slot and comm cells against the warp's rows in shared memory, slot
+ * indices against the plan's slot count, split points against 0..L.  A failed
+ * check skips the access (a load reads 0, a copy is zero-filled, a store is
+ * dropped; the results are then wrong) and records the failure; nothing traps.
+ * Returns 1 for a checked build, 0 otherwise.  *first_failure (may be NULL)
+ * receives the first failure recorded since the previous call, 0 if none, and
+ * the records are cleared: bit 63 set, the check site in bits 40..55 (1 cost
+ * read, 2 slot read, 3 slot write, 4 comm cell, 5 slot index, 6 split point),
+ * the low 40 bits of the offending offset below.  Synchronizes the device;
+ * call it with no kernel of the library in flight. */
+int pp_sched_debug_checks(uint64_t *first_failure);
+
 /* Evaluate n_instances Zero Bubble schedule instances (policy PP_ZB1P or
  * PP_ZB2P, one stage per device).  [GPipe->ZB] "Zero Bubble" and "ZB1P and
  * ZB2P"; [1F1B] §6.2.  The backward of microbatch i on stage k splits into

@@ -25,7 +25,7 @@ EXPORTS = ("pp_sched_plan", "pp_sched_plan_info", "pp_sched_plan_ops", "pp_sched
            "pp_sched_cache_clear", "pp_sched_eval_noalloc", "pp_sched_eval_zb",
            "pp_sched_partition_search_ranks", "pp_sched_partition_search_interleaved", "pp_sched_eval_fb",
            "pp_sched_eval_host", "pp_sched_eval_host_workspace", "pp_sched_many_prepare", "pp_sched_many_eval",
-           "pp_sched_many_info", "pp_sched_many_destroy", "pp_sched_eval_dualpipe")
+           "pp_sched_many_info", "pp_sched_many_destroy", "pp_sched_eval_dualpipe", "pp_sched_debug_checks")
 
 
 class Problem(ctypes.Structure):
@@ -47,11 +47,13 @@ class PPSchedError(RuntimeError):
 
 
 def _load():
-    path = build_lib.LIB
+    # PPSCHED_CHECKED=1 loads the bounds-checked build (build_lib.build(checked=True))
+    checked = os.environ.get("PPSCHED_CHECKED", "0") not in ("", "0")
+    path = build_lib.LIB_CHECKED if checked else build_lib.LIB
     if not os.path.exists(path):
         raise ImportError(
-            f"libppsched.so is not built ({path}); run __graft_entry__.build() or "
-            "python -m pipeline_schedule_simulation_gb300.build_lib")
+            f"{os.path.basename(path)} is not built ({path}); run __graft_entry__.build() or "
+            "python -m pipeline_schedule_simulation_gb300.build_lib" + (" --checked" if checked else ""))
     lib = ctypes.CDLL(path)
     vp, i32, i64, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64
     lib.pp_sched_plan.argtypes = [i32, i32, i32, i32, ctypes.POINTER(vp), vp]
@@ -103,6 +105,8 @@ def _load():
     lib.pp_sched_eval_host_workspace.restype = ctypes.c_size_t
     lib.pp_sched_cache_clear.argtypes = []
     lib.pp_sched_cache_clear.restype = None
+    lib.pp_sched_debug_checks.argtypes = [vp]
+    lib.pp_sched_debug_checks.restype = i32
     return lib
 
 
@@ -577,3 +581,11 @@ def partition_search_interleaved(layer_tf, layer_tb, layer_act, P, v, M, comm, c
 
 def cache_clear():
     LIB.pp_sched_cache_clear()
+
+
+def debug_checks():
+    """(checked build?, first failure word since the last call or 0); see
+    pp_sched_debug_checks.  Synchronizes the device."""
+    w = ctypes.c_uint64(0)
+    checked = LIB.pp_sched_debug_checks(ctypes.byref(w))
+    return bool(checked), int(w.value)

@@ -18,6 +18,11 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libppsched.so")
+# The bounds-checked build (-DPPS_CHECKED: every table-driven address checked
+# in the kernels, failures recorded for pp_sched_debug_checks), in a folder of
+# its own so that both builds can coexist.
+BUILD_CHECKED = os.path.join(PKG, "_build_checked")
+LIB_CHECKED = os.path.join(BUILD_CHECKED, "libppsched_checked.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++20", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "-I", os.path.join(ROOT, "include")]
@@ -41,15 +46,18 @@ def _stale(out, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra=(), checked: bool = False) -> str:
+    build_dir, lib_path = (BUILD_CHECKED, LIB_CHECKED) if checked else (BUILD, LIB)
+    if checked:
+        extra = ["-DPPS_CHECKED", *extra]
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers.append(os.path.join(ROOT, "include", "ppsched.h"))
     jobs = []
     objs = []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src, *headers]):
             jobs.append((src, obj))
@@ -68,17 +76,18 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
             for src, log in ex.map(compile_one, jobs):
                 if verbose and log.strip():
                     print(f"== {os.path.basename(src)}\n{log}", file=sys.stderr)
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib_path, objs):
+        tmp = lib_path + f".tmp{os.getpid()}"
         cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
     v = "-v" in sys.argv
     extra = ["-Xptxas", "-v"] if "--ptxas" in sys.argv else []
-    print(build(force="--force" in sys.argv or bool(extra), verbose=v or bool(extra), extra=extra))
+    print(build(force="--force" in sys.argv or bool(extra), verbose=v or bool(extra), extra=extra,
+                checked="--checked" in sys.argv))

@@ -17,6 +17,7 @@
 
 #include <cstdint>
 
+#include "checks.cuh"
 #include "internal.cuh"
 
 namespace pps {
@@ -163,8 +164,12 @@ __device__ __forceinline__ void load_round(const EvalArgs &a, int rl, const Load
             const int32_t *src = base;
             uint32_t nb = 0;
             if (kind != kIdle && bytes_in) {
-                src = base + (s * s_stage + (int)desc_mb(d) * s_mb) + x0;
-                nb = bytes_in;
+                const int64_t off = (int64_t)(s * s_stage + (int)desc_mb(d) * s_mb) + x0;
+                if (PPS_CHECK(off + bytes_in / 4 <= cost_reach(a.n, a.S, a.M, a.s_inst, a.s_stage, a.s_mb),
+                              kChkCostRead, off)) {
+                    src = base + off;
+                    nb = bytes_in;
+                }
             }
             cp_async16(smem_addr(slice + k * 32 + 4 * g), src, nb);
         }
@@ -180,8 +185,11 @@ __device__ __forceinline__ void load_round(const EvalArgs &a, int rl, const Load
             uint32_t nb = 0;
             if (kind != kIdle && live) {
                 const int64_t s = (int64_t)desc_chunk(d) * a.P + k;
-                src = base + s * a.s_stage + (int64_t)desc_mb(d) * a.s_mb + x * a.s_inst;
-                nb = 4;
+                const int64_t off = s * a.s_stage + (int64_t)desc_mb(d) * a.s_mb + x * a.s_inst;
+                if (PPS_CHECK(off < cost_reach(a.n, a.S, a.M, a.s_inst, a.s_stage, a.s_mb), kChkCostRead, off)) {
+                    src = base + off;
+                    nb = 4;
+                }
             }
             cp_async4(smem_addr(slice + k * 32 + lane), src, nb);
         }
@@ -197,9 +205,12 @@ __device__ __forceinline__ void load_round(const EvalArgs &a, int rl, const Load
 // 32*NI instances) takes 8*NI lanes, 16 bytes (4 instances) each; lane copies
 // row 32/(8*NI)*i + lane/(8*NI) for i = 0 .. PMAX*NI/4 - 1.  The slice is laid
 // out [device][instance]; fbase/bbase already point at this lane's instances.
+// (x0, reach: the element offset of fbase / bbase from the tables' bases and
+// the elements the strides reach; used by the checked build only.)
 template <int PMAX, int NI>
 __device__ __forceinline__ void load_round_lt(const uint32_t *lt, int rl, int32_t *ring, const int32_t *fbase,
-                                              const int32_t *bbase, uint32_t bytes_in, int lane) {
+                                              const int32_t *bbase, uint32_t bytes_in, int lane,
+                                              [[maybe_unused]] int64_t x0, [[maybe_unused]] int64_t reach) {
     using RG = Ring<PMAX, NI>;
     constexpr int kLanesPerRow = 8 * NI, kRowsPerInst = 32 / kLanesPerRow;
     int32_t *slice = ring + (rl % RG::kSlices) * (PMAX * NI * 32);
@@ -210,7 +221,7 @@ __device__ __forceinline__ void load_round_lt(const uint32_t *lt, int rl, int32_
         const uint32_t e = lt[rl * PMAX + k];
         const int32_t *src = (e & 1u) ? bbase : fbase;
         uint32_t nb = 0;
-        if (e != kLtIdle) {
+        if (e != kLtIdle && PPS_CHECK(x0 + (e >> 1) + bytes_in / 4 <= reach, kChkCostRead, x0 + (e >> 1))) {
             src += e >> 1;
             nb = bytes_in;
         }
@@ -225,11 +236,13 @@ __device__ __forceinline__ void load_round_lt(const uint32_t *lt, int rl, int32_
 // chunk in the round's slice.
 template <int PMAX, int NI>
 __device__ __forceinline__ void load_round_lt_q(const uint32_t (&e)[PMAX * NI / 4], uint32_t dst, const int32_t *fbase,
-                                                const int32_t *bbase) {
+                                                const int32_t *bbase, [[maybe_unused]] int64_t x0,
+                                                [[maybe_unused]] int64_t reach) {
     constexpr int kRowsPerInst = 32 / (8 * NI);
 #pragma unroll
     for (int i = 0; i < PMAX * NI / 4; ++i) {
-        const bool idle = e[i] == kLtIdle;
+        const bool idle = e[i] == kLtIdle || !PPS_CHECK(e[i] == kLtIdle || x0 + (e[i] >> 1) + 4 <= reach,
+                                                        kChkCostRead, x0 + (e[i] >> 1));
         const int32_t *src = ((e[i] & 1u) ? bbase : fbase) + (idle ? 0u : (e[i] >> 1));
         cp_async16_or_zero(dst + (uint32_t)(i * kRowsPerInst * NI * 32 * 4), src, idle);
     }

@@ -105,9 +105,11 @@ __global__ void __launch_bounds__(128) k_eval_dp(const EvalArgs a, int MA, int32
     // the route's first microbatch in its block's cost rows
     const int64_t srcA = dev ? x * a.s_inst + (int64_t)blkA * a.s_stage : 0;
     const int64_t srcB = dev ? x * a.s_inst + (int64_t)blkB * a.s_stage + (int64_t)MA * a.s_mb : 0;
+    [[maybe_unused]] const int64_t reach = cost_reach(a.n, P, MA + MB_, a.s_inst, a.s_stage, a.s_mb);
     auto fetch = [&](int q, int i) {
         const bool rb = q >= 2;
-        if (dev && i < (rb ? MB_ : MA)) {
+        if (dev && i < (rb ? MB_ : MA) &&
+            PPS_CHECK((rb ? srcB : srcA) + (int64_t)i * a.s_mb < reach, kChkCostRead, (rb ? srcB : srcA) + (int64_t)i * a.s_mb)) {
             const int32_t *base = (q & 1) ? a.cost_b : a.cost_f;
             cp_async4(smem_addr(cring + (q * G::kRing + i % G::kRing) * 32 + lane),
                       base + (rb ? srcB : srcA) + (int64_t)i * a.s_mb, 4);

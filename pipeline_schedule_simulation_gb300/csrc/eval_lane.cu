@@ -154,16 +154,18 @@ struct LaneLoader {
     uint32_t bytes[kN];    // bytes of a non-idle op's copy (0 past the last instance)
     uint32_t doff[kN];     // byte offset of the copy in the ring row
     uint32_t on;           // this lane issues copies
+    int64_t e0, reach;     // element offset of fb / bb and the elements the strides reach (checked build)
 
     __device__ __forceinline__ LaneLoader(const EvalArgs &a, int lane, int j, int k, int64_t inst0) {
         using G = LaneGeom<PMAX>;
+        reach = cost_reach(a.n, a.S, a.M, a.s_inst, a.s_stage, a.s_mb);
         if constexpr (VEC) {
             constexpr int kPerSet = G::kIPW / G::kCopy;
             const int set = j / kPerSet, piece = j % kPerSet;
             on = j < NI * kPerSet;
             const int64_t xi = inst0 + set * G::kIPW + piece * G::kCopy;
             const int64_t left = a.n - xi;
-            const int64_t e0 = on && left > 0 ? xi : 0;
+            e0 = on && left > 0 ? xi : 0;
             fb = reinterpret_cast<const char *>(a.cost_f + e0);
             bb = reinterpret_cast<const char *>(a.cost_b + e0);
             bytes[0] = !on || left <= 0 ? 0u : (uint32_t)(left < G::kCopy ? left : G::kCopy) * 4u;
@@ -171,7 +173,7 @@ struct LaneLoader {
             doff[0] = (uint32_t)(set * 32 + k * G::kIPW + piece * G::kCopy) * 4u;
         } else {
             const int64_t x0 = inst0 + j;
-            const int64_t e0 = x0 < a.n ? x0 * a.s_inst : 0;
+            e0 = x0 < a.n ? x0 * a.s_inst : 0;
             fb = reinterpret_cast<const char *>(a.cost_f + e0);
             bb = reinterpret_cast<const char *>(a.cost_b + e0);
             on = 1;
@@ -193,7 +195,10 @@ struct LaneLoader {
 #pragma unroll
         for (int i = 0; i < kN; ++i) {
             const char *s = src + step[i];
-            const uint32_t nb = idle ? 0u : bytes[i];
+            uint32_t nb = idle ? 0u : bytes[i];
+            if (nb && !PPS_CHECK(e0 + (int64_t)((lt & ~3u) + step[i] + nb) / 4 <= reach, kChkCostRead,
+                                 e0 + (int64_t)((lt & ~3u) + step[i]) / 4))
+                nb = 0;
             const uint32_t d = row + doff[i];
             if constexpr (VEC && G::kCopy == 4)
                 asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %3, 0;\n"
@@ -347,24 +352,32 @@ __device__ __forceinline__ void lane_body(const EvalArgs &a, const uint4 *tab, i
             }
             __syncwarp();
             const uint32_t vr = val_s + e.x, cr = ctab_s + e.y * kCw, vw = val_s + (e.z & ~kLaneActive);
+            // (checked build: the entry's offsets inside the warp's value rows
+            // and comm rows; row bytes = 128*NI)
+            const bool okr = PPS_CHECK(e.x < (uint32_t)(a.nslots + 2) * 128u * NI, kChkLaneSlotRead, e.x);
+            const bool okw = PPS_CHECK((e.z & ~kLaneActive) < (uint32_t)(a.nslots + 2) * 128u * NI,
+                                       kChkLaneSlotWrite, e.z & ~kLaneActive);
+            const bool okc = PPS_CHECK(e.y < (uint32_t)(2 * a.v + 1) * 128u * NI, kChkLaneComm, e.y);
 #pragma unroll
             for (int i = 0; i < NI; ++i) {
-                uint32_t c, cm;
+                uint32_t c = 0, cm = 0;
                 if constexpr (MBZ) {
-                    const uint2 cc = lds64(cr + 256 * i);
-                    c = cc.x;
-                    cm = cc.y;
+                    if (okc) {
+                        const uint2 cc = lds64(cr + 256 * i);
+                        c = cc.x;
+                        cm = cc.y;
+                    }
                 } else {
                     c = lds32(cost_s + (cur * kRow + 32 * i) * 4);
-                    cm = lds32(cr + 128 * i);
+                    if (okc) cm = lds32(cr + 128 * i);
                 }
-                const uint32_t arr = lds32(vr + 128 * i) + cm;
+                const uint32_t arr = (okr ? lds32(vr + 128 * i) : 0u) + cm;
                 const uint32_t st = max(fr[i], arr);
                 const uint32_t en = st + c;
                 flag[i] |= st | c;
                 busy[i] += c;
                 fr[i] = en;
-                sts32(vw + 128 * i, en);
+                if (okw) sts32(vw + 128 * i, en);
                 if constexpr (OPS) {
                     const int64_t x = x0 + i * G::kIPW;
                     if ((e.z & kLaneActive) && x < a.n) {

@@ -289,8 +289,10 @@ __global__ void __maxnreg__(PMAX == 16 ? 168 : 96) k_eval_reg(const EvalArgs a) 
     const int64_t x0 = inst0 + 4 * g;
     const int64_t left = a.n - x0;
     const uint32_t bytes_in = left <= 0 ? 0u : (left >= 4 ? 16u : (uint32_t)left * 4u);
-    const int32_t *fbase = a.cost_f + (bytes_in ? x0 : 0);
-    const int32_t *bbase = a.cost_b + (bytes_in ? x0 : 0);
+    const int64_t xoff = bytes_in ? x0 : 0;
+    const int32_t *fbase = a.cost_f + xoff;
+    const int32_t *bbase = a.cost_b + xoff;
+    [[maybe_unused]] const int64_t reach = cost_reach(a.n, a.S, a.M, a.s_inst, a.s_stage, a.s_mb);
     const int R = a.R;
     constexpr uint32_t kSliceWords = PMAX * NI * 32;
     // shared address of this lane's first 16-byte chunk in slice 0 (table loader)
@@ -311,9 +313,9 @@ __global__ void __maxnreg__(PMAX == 16 ? 168 : 96) k_eval_reg(const EvalArgs a) 
             if constexpr (LT) {
                 if constexpr (decltype(full)::value)
                     load_round_lt_q<PMAX, NI>(eq0, dst_lane + ((uint32_t)rl & (RG::kSlices - 1)) * kSliceWords * 4,
-                                              fbase, bbase);
+                                              fbase, bbase, xoff, reach);
                 else
-                    load_round_lt<PMAX, NI>(lt, rl, ring, fbase, bbase, bytes_in, lane);
+                    load_round_lt<PMAX, NI>(lt, rl, ring, fbase, bbase, bytes_in, lane, xoff, reach);
             } else {
                 LoadDesc<PMAX, VEC> ld;
                 fetch_load_desc<PMAX, VEC>(a, rl, lane, ld);

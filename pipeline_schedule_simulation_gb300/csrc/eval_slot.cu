@@ -81,7 +81,9 @@ __global__ void __launch_bounds__(128) k_eval_slot(const EvalArgs a) {
         for (int k = 0; k < PMAX; ++k) {
             arr[k] = 0;
             const uint32_t rs = d2_rslot(d2[k]);
-            if (desc_kind(d[k]) != kIdle && rs != kNoSlot)
+            if (desc_kind(d[k]) != kIdle && rs != kNoSlot &&
+                PPS_CHECK(rs < (uint32_t)a.nslots, kChkSlotIndex, rs) &&
+                PPS_CHECK(d2_cbnd(d2[k]) < (uint32_t)a.S, kChkSlotIndex, d2_cbnd(d2[k])))
                 arr[k] = wrap_add(val[rs * 32 + lane], ctab[d2_cbnd(d2[k]) * 32 + lane]);
         }
 #pragma unroll
@@ -95,7 +97,7 @@ __global__ void __launch_bounds__(128) k_eval_slot(const EvalArgs a) {
             accE |= (uint32_t)en | (uint32_t)arr[k];
             accC |= (uint32_t)c;
             const uint32_t ws = d2_wslot(d2[k]);
-            if (ws != kNoSlot) val[ws * 32 + lane] = en;
+            if (ws != kNoSlot && PPS_CHECK(ws < (uint32_t)a.nslots, kChkSlotIndex, ws)) val[ws * 32 + lane] = en;
             if constexpr (OPS) {
                 if (live) {
                     const int64_t off = x * a.o_inst + ((int64_t)k * a.O + cnt[k]) * a.o_op;

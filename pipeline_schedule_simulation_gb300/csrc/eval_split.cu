@@ -171,8 +171,10 @@ __global__ void __launch_bounds__(128) k_eval_split(const EvalArgs a) {
     const int64_t x4 = inst0 + 4 * q;
     const int64_t left = a.n - x4;
     const uint32_t bytes_in = left <= 0 ? 0u : (left >= 4 ? 16u : (uint32_t)left * 4u);
-    const int32_t *fbase = a.cost_f + (bytes_in ? x4 : 0);
-    const int32_t *bbase = a.cost_b + (bytes_in ? x4 : 0);
+    const int64_t xoff = bytes_in ? x4 : 0;
+    const int32_t *fbase = a.cost_f + xoff;
+    const int32_t *bbase = a.cost_b + xoff;
+    [[maybe_unused]] const int64_t reach = cost_reach(a.n, a.S, a.M, a.s_inst, a.s_stage, a.s_mb);
     const int dst_word = ((d % H) * 2 + d / H) * G::kIPW + 4 * q;
     const int R = a.R;
     auto issue = [&](int rl) {
@@ -180,7 +182,7 @@ __global__ void __launch_bounds__(128) k_eval_split(const EvalArgs a) {
             const uint32_t e = lt[rl * PMAX + d];
             const int32_t *src = (e & 1u) ? bbase : fbase;
             uint32_t nb = 0;
-            if (e != kLtIdle) {
+            if (e != kLtIdle && PPS_CHECK(xoff + (e >> 1) + bytes_in / 4 <= reach, kChkCostRead, xoff + (e >> 1))) {
                 src += e >> 1;
                 nb = bytes_in;
             }

@@ -93,8 +93,9 @@ __global__ void __launch_bounds__(128) k_eval_zb(const EvalArgs a, const int32_t
     }
     const int64_t row0 = dev ? x * a.s_inst + (int64_t)k * a.s_stage : 0;
     const int32_t *src[3] = {a.cost_f + row0, a.cost_b + row0, cost_w + row0};
+    [[maybe_unused]] const int64_t reach = cost_reach(a.n, P, M, a.s_inst, a.s_stage, a.s_mb);
     auto fetch = [&](int kind, int m) {
-        if (dev && m < M) {
+        if (dev && m < M && PPS_CHECK(row0 + (int64_t)m * a.s_mb < reach, kChkCostRead, row0 + (int64_t)m * a.s_mb)) {
             const int32_t *p = kind == kZbF ? src[0] : (kind == kZbB ? src[1] : src[2]);
             cp_async4(smem_addr(cring + (kind * G::kRing + m % G::kRing) * 32 + lane), p + (int64_t)m * a.s_mb, 4);
         }

@@ -15,7 +15,9 @@
 // chunks run one after another on `stream`.
 #include <algorithm>
 #include <mutex>
+#include <vector>
 
+#include "checks.cuh"
 #include "internal.cuh"
 
 namespace pps {
@@ -245,4 +247,38 @@ extern "C" int pp_sched_eval_host(pp_policy_t policy, int P, int M, int v, const
 extern "C" size_t pp_sched_eval_host_workspace(int P, int M, int v, int64_t n_instances) {
     if (P < 1 || M < 1 || v < 1 || n_instances < 0) return 0;
     return pps::chunk_bytes(std::max<int64_t>(n_instances, 1), P * v, M, P);
+}
+
+// ---- the bounds-checked build's failure records ----
+
+namespace pps {
+namespace {
+std::mutex g_check_mu;
+std::vector<uint64_t (*)()> &check_readers() {
+    static std::vector<uint64_t (*)()> readers;
+    return readers;
+}
+}  // namespace
+
+int register_check_reader(uint64_t (*reader)()) {
+    std::lock_guard<std::mutex> lk(g_check_mu);
+    check_readers().push_back(reader);
+    return 0;
+}
+}  // namespace pps
+
+extern "C" int pp_sched_debug_checks(uint64_t *first_failure) {
+    uint64_t first = 0;
+#ifdef PPS_CHECKED
+    std::lock_guard<std::mutex> lk(pps::g_check_mu);
+    for (uint64_t (*reader)() : pps::check_readers()) {
+        const uint64_t w = reader();
+        if (!first) first = w;
+    }
+    if (first_failure) *first_failure = first;
+    return 1;
+#else
+    if (first_failure) *first_failure = first;
+    return 0;
+#endif
 }

@@ -201,6 +201,17 @@ __global__ void __launch_bounds__(256) k_search(const SearchArgs a) {
             unrank<PMAX>(a, t, cand_rank<EXH>(a, ci), first);
             int cf[PMAX], cb[PMAX];
             bool ok = true;
+            // (checked build: the split points increase strictly from 0 to L)
+#pragma unroll
+            for (int k = 0; k < PMAX; ++k)
+                if (k < a.P)
+                    ok = ok && PPS_CHECK(first[k] >= 0 && first[k] < first[k + 1] && first[k + 1] <= a.L &&
+                                             (k + 1 < a.P || first[k + 1] == a.L),
+                                         kChkSearchSplit, first[k + 1]);
+            if (!ok) {
+#pragma unroll
+                for (int k = 0; k <= PMAX; ++k) first[k] = 0;
+            }
             uint32_t big = 0;
 #pragma unroll
             for (int k = 0; k < PMAX; ++k) {

@@ -4,6 +4,8 @@
 
 #include <cstdint>
 
+#include "checks.cuh"
+
 namespace pps {
 
 // SplitMix64 (Steele, Lea & Flood, OOPSLA 2014): add the golden gamma to the

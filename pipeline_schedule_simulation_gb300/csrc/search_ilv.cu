@@ -120,6 +120,15 @@ __global__ void __launch_bounds__(256) k_ilv_cands(const IlvArgs a, int64_t chun
             const uint64_t r = splitmix64(a.seed + (uint64_t)(a.begin + chunk0 + i)) % a.ncomb;
             ilv_unrank(a, t, r, first);
             fl = kIlvScored;
+            // (checked build: the split points increase strictly from 0 to L)
+            for (int s = 0; s < a.S; ++s)
+                if (!PPS_CHECK(first[s] >= 0 && first[s] < first[s + 1] && first[s + 1] <= a.L &&
+                                   (s + 1 < a.S || first[s + 1] == a.L),
+                               kChkSearchSplit, first[s + 1])) {
+                    for (int q = 0; q <= a.S; ++q) first[q] = 0;
+                    fl = kIlvBig;
+                    break;
+                }
             for (int s = 0; s < a.S; ++s) {
                 const int64_t sf = t.pre_tf[first[s + 1]] - t.pre_tf[first[s]];
                 const int64_t sb = t.pre_tb[first[s + 1]] - t.pre_tb[first[s]];
