@@ -518,48 +518,81 @@ def secondary(B, W, torch, stream):
         torch.cuda.synchronize()
         return a.elapsed_time(b) / 1e3 / reps
 
+    def timed_eval(fn, reps):
+        """An evaluation's seconds per call: `fn(s)` enqueues one call on stream
+        s.  The calls are timed launched one by one and, where they can be
+        captured, as `reps` calls in one CUDA graph between events captured
+        inside it (the device time, without the host's per-call cost, which
+        exceeds a short kernel's).  Returns (seconds, direct seconds, how)."""
+        direct = timed(lambda: fn(stream), reps)
+        try:
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            e0 = torch.cuda.Event(enable_timing=True, external=True)
+            e1 = torch.cuda.Event(enable_timing=True, external=True)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                e0.record(side)
+                for _ in range(reps):
+                    fn(side)
+                e1.record(side)
+            for _ in range(2):
+                g.replay()
+                torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / 1e3 / reps, direct, "graph"
+        except Exception:  # not capturable (or no external events): the direct launches
+            torch.cuda.synchronize()
+            return direct, direct, "direct"
+
+    def line(ops, t):
+        sec, direct, how = t
+        return {"op_times_per_s": ops / sec, "ms": sec * 1e3, "direct_ms": direct * 1e3, "timing": how}
+
     # per-op start/end stored (instance-minor op layout)
     b3 = W.hetero_1f1b(n=N_INST)
     cf, cb, cm = (torch.from_numpy(x).cuda() for x in (b3.cost_f, b3.cost_b, b3.comm))
     O = 2 * M
     ops_out = {"op_start": torch.empty((P, O, N_INST), dtype=torch.int32, device="cuda"),
                "op_end": torch.empty((P, O, N_INST), dtype=torch.int32, device="cuda")}
-    t = timed(lambda: B.evaluate(1, P, M, 1, cf, cb, b3.strides, N_INST, comm=cm, comm_strides=b3.comm_strides,
-                                 op_times=True, op_strides=(1, N_INST), out=ops_out, stream=stream), 20)
+    tt = timed_eval(lambda s: B.evaluate(1, P, M, 1, cf, cb, b3.strides, N_INST, comm=cm,
+                                         comm_strides=b3.comm_strides, op_times=True, op_strides=(1, N_INST),
+                                         out=ops_out, stream=s), 20)
+    t = tt[0]
     ob = algorithmic_bytes(N_INST) + 2 * 4 * 2 * P * M * N_INST  # + op_start and op_end, int32 each
     peak_gbs, peak_src = measured_peaks()
-    out["1f1b_P8_M64_with_op_times"] = {"op_times_per_s": 2 * P * M * N_INST / t, "ms": t * 1e3,
-                                        "algorithmic_bytes": ob, "gbs": ob / t / 1e9,
-                                        "frac_of_hbm_peak": ob / t / 1e9 / peak_gbs, "peak_source": peak_src}
+    out["1f1b_P8_M64_with_op_times"] = dict(line(2 * P * M * N_INST, tt), algorithmic_bytes=ob, gbs=ob / t / 1e9,
+                                            frac_of_hbm_peak=ob / t / 1e9 / peak_gbs, peak_source=peak_src)
     del ops_out, cf, cb, cm
     for v in (2, 4):
         il, base = W.interleaved_vs_1f1b(v)
         for tag, bt in (("interleaved", il), ("1f1b_equal_work", base)):
             f, g, c = (torch.from_numpy(x).cuda() for x in (bt.cost_f, bt.cost_b, bt.comm))
-            t = timed(lambda: B.evaluate(bt.policy, bt.P, bt.M, bt.v, f, g, bt.strides, bt.n, comm=c,
-                                         comm_strides=bt.comm_strides, stream=stream), 20)
-            out[f"{tag}_P8_v{v}_M128_n16384"] = {"op_times_per_s": bt.op_times / t, "ms": t * 1e3}
+            res_il = B.evaluate(bt.policy, bt.P, bt.M, bt.v, f, g, bt.strides, bt.n, comm=c,
+                                comm_strides=bt.comm_strides, stream=stream)
+            tt = timed_eval(lambda s: B.evaluate(bt.policy, bt.P, bt.M, bt.v, f, g, bt.strides, bt.n, comm=c,
+                                                 comm_strides=bt.comm_strides, out=res_il, stream=s), 20)
+            out[f"{tag}_P8_v{v}_M128_n16384"] = line(bt.op_times, tt)
     for pol, name in ((W.ZB1P, "zb1p"), (W.ZB2P, "zb2p")):
         bz = W.hetero_zb(pol, n=N_INST)
         f, g, w, c = (torch.from_numpy(x).cuda() for x in (bz.cost_f, bz.cost_b, bz.cost_w, bz.comm))
         zout = {}
         zout.update(B.evaluate_zb(pol, P, M, f, g, w, bz.strides, N_INST, comm=c, comm_strides=bz.comm_strides,
                                   stream=stream))
-        t = timed(lambda: B.evaluate_zb(pol, P, M, f, g, w, bz.strides, N_INST, comm=c,
-                                        comm_strides=bz.comm_strides, out=zout, stream=stream), 10)
-        out[f"{name}_P8_M64_n{N_INST}"] = {"op_times_per_s": bz.op_times / t, "ms": t * 1e3,
-                                           "mean_makespan": float(zout["makespan"].float().mean().item())}
+        tt = timed_eval(lambda s: B.evaluate_zb(pol, P, M, f, g, w, bz.strides, N_INST, comm=c,
+                                                comm_strides=bz.comm_strides, out=zout, stream=s), 10)
+        out[f"{name}_P8_M64_n{N_INST}"] = dict(line(bz.op_times, tt),
+                                               mean_makespan=float(zout["makespan"].float().mean().item()))
         del f, g, w, c, zout
     bd = W.hetero_dualpipe(n=N_INST)
     m_a = bd.meta["m_a"]
     f, g, c = (torch.from_numpy(x).cuda() for x in (bd.cost_f, bd.cost_b, bd.comm))
     dout = B.evaluate_dualpipe(P, M, m_a, f, g, bd.strides, N_INST, comm=c, comm_strides=bd.comm_strides,
                                stream=stream)
-    t = timed(lambda: B.evaluate_dualpipe(P, M, m_a, f, g, bd.strides, N_INST, comm=c,
-                                          comm_strides=bd.comm_strides, out=dout, stream=stream), 10)
+    tt = timed_eval(lambda s: B.evaluate_dualpipe(P, M, m_a, f, g, bd.strides, N_INST, comm=c,
+                                                  comm_strides=bd.comm_strides, out=dout, stream=s), 10)
     one = B.evaluate(1, P, M, 1, f, g, bd.strides, N_INST, comm=c, comm_strides=bd.comm_strides, stream=stream)
     out[f"dualpipe_P8_M64_n{N_INST}"] = {
-        "op_times_per_s": bd.op_times / t, "ms": t * 1e3, "microbatches_per_route": [m_a, M - m_a],
+        **line(bd.op_times, tt), "microbatches_per_route": [m_a, M - m_a],
         "mean_makespan": float(dout["makespan"].double().mean().item()),
         "mean_makespan_1f1b_same_costs": float(one["makespan"].double().mean().item()),
         "max_peak": int(dout["peak"].max().item())}

@@ -134,9 +134,17 @@ def _reach(count, strides):
     """Elements a strided access reaches from its base pointer: 1 + the largest
     offset sum((extent - 1) * stride), or 0 when any extent is 0.  `count` and
     `strides` pair each extent with its element stride."""
-    if any(c <= 0 for c in count):
-        return 0
-    return 1 + sum((c - 1) * int(st) for c, st in zip(count, strides))
+    r = 1
+    for c, st in zip(count, strides):
+        if c <= 0:
+            return 0
+        r += (c - 1) * st
+    return r
+
+
+def _avail(t):
+    """Elements of t's storage from its data pointer on."""
+    return t.untyped_storage().nbytes() // t.element_size() - t.storage_offset()
 
 
 def _arg(t, name, dtype, device, reach, host=False):
@@ -148,16 +156,19 @@ def _arg(t, name, dtype, device, reach, host=False):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
     if host:
-        if t.device.type != "cpu":
+        if t.is_cuda:
             raise ValueError(f"{name}: expected a host (CPU) tensor, got one on {t.device}")
-    elif t.device.type != "cuda" or (device is not None and t.device != device):
+    elif not t.is_cuda or (device is not None and t.device != device):
         raise ValueError(f"{name}: expected a tensor on {device or 'a CUDA device'}, got one on {t.device}")
     if t.dtype != dtype:
         raise TypeError(f"{name}: expected dtype {dtype}, got {t.dtype}")
-    avail = t.untyped_storage().nbytes() // t.element_size() - t.storage_offset()
-    if reach > avail:
-        raise ValueError(f"{name}: the strides reach {reach} elements from its data pointer but its storage "
-                         f"holds {avail}")
+    # a contiguous tensor of at least `reach` elements holds them from its data
+    # pointer; otherwise ask its storage
+    if reach > 0 and not (t.numel() >= reach and t.is_contiguous()):
+        avail = _avail(t)
+        if reach > avail:
+            raise ValueError(f"{name}: the strides reach {reach} elements from its data pointer but its storage "
+                             f"holds {avail}")
     return t
 
 
@@ -185,21 +196,18 @@ def _check_outputs(out, n, P, op_count, op_strides, op_names, peak_per_instance=
     """The summary outputs hold n (makespan, bub_num, bub_den, status), n*P
     (idle) and P or n*P (peak) elements; the per-op outputs reach what their
     (instance, op) strides address."""
-    sizes = {"makespan": n, "bub_num": n, "bub_den": n, "status": n, "idle": n * P,
-             "peak": n * P if peak_per_instance else P}
-    for k, need in sizes.items():
-        t = out.get(k)
-        if t is not None and n > 0:
-            avail = t.untyped_storage().nbytes() // t.element_size() - t.storage_offset()
-            if need > avail:
-                raise ValueError(f"{k}: needs {need} elements, its storage holds {avail}")
+    if n > 0:
+        for k, need in (("makespan", n), ("bub_num", n), ("bub_den", n), ("status", n), ("idle", n * P),
+                        ("peak", n * P if peak_per_instance else P)):
+            t = out.get(k)
+            if t is not None and not (t.numel() >= need and t.is_contiguous()) and need > _avail(t):
+                raise ValueError(f"{k}: needs {need} elements, its storage holds {_avail(t)}")
     for k in op_names:
         t = out.get(k)
         if t is not None:
             reach = _reach(op_count, op_strides)
-            avail = t.untyped_storage().nbytes() // t.element_size() - t.storage_offset()
-            if reach > avail:
-                raise ValueError(f"{k}: the op strides reach {reach} elements, its storage holds {avail}")
+            if not (t.numel() >= reach and t.is_contiguous()) and reach > _avail(t):
+                raise ValueError(f"{k}: the op strides reach {reach} elements, its storage holds {_avail(t)}")
 
 
 def _stream(stream):

@@ -211,7 +211,12 @@ __device__ __forceinline__ void run_round(RegState<PMAX, NI> &S, uint64_t w, con
 // issues them, so no shared-memory load sits on the issue path.
 template <int PMAX, int NI, bool VEC, bool OPS, bool LT>
 __global__ void __maxnreg__(PMAX == 16 ? 168 : 96) k_eval_reg(const EvalArgs a) {
-    copy_peak(a);
+    // Programmatic dependent launch: the next evaluation on the stream may
+    // start its blocks as this grid's blocks retire; it copies the plan's
+    // tables (complete before either launch) and waits below for this grid's
+    // end before it touches any input or output.  Without the launch
+    // attribute both instructions do nothing.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     static_assert(NI == 1 || LT, "two instances per thread need the table loader");
     using RG = Ring<PMAX, NI>;
     constexpr int D = RG::kAhead2;
@@ -281,6 +286,9 @@ __global__ void __maxnreg__(PMAX == 16 ? 168 : 96) k_eval_reg(const EvalArgs a) 
         cp_async_wait<0>();
         __syncthreads();
     }
+    // the previous grid on the stream has finished and its writes are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    copy_peak(a);
     if (inst0 >= a.n) return;  // warp-uniform, after the block barrier
 
     // loader state: lane copies 16 bytes (4 instances) at instance offset 4g
@@ -546,8 +554,31 @@ static int launch_reg_mbz(const EvalArgs &a, cudaStream_t st) {
     return PP_OK;
 }
 
+// Launch `kern` on `st`, as a programmatic dependent launch when `pdl` (the
+// kernel waits for the previous grid before it reads inputs or writes
+// outputs; its tables must be complete before the launch).
+template <typename Kern>
+static cudaError_t launch_pdl(Kern kern, unsigned grid, unsigned block, size_t smem, cudaStream_t st, bool pdl,
+                              const EvalArgs &b) {
+    if (!pdl) {
+        kern<<<grid, block, smem, st>>>(b);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, b);
+}
+
 template <int PMAX, int NI, bool VEC, bool OPS, bool LT>
-static int launch_reg_t(const EvalArgs &a, int64_t begin, int64_t end, cudaStream_t st) {
+static int launch_reg_t(const EvalArgs &a, int64_t begin, int64_t end, cudaStream_t st, bool pdl = false) {
     // two-instance warps hold twice the ring: use two warps per block so the
     // blocks still spread evenly over the SMs
     constexpr int kWarps = NI == 1 ? 4 : 2;
@@ -604,25 +635,28 @@ static int launch_reg_t(const EvalArgs &a, int64_t begin, int64_t end, cudaStrea
             }
             if ((int)(uint32_t)memo >= 1) {
                 b.tasks = warps;
-                kern<<<(unsigned)grid, (unsigned)wpb * 32, smem, st>>>(b);
-                PPS_CUDA_TRY(cudaGetLastError());
+                PPS_CUDA_TRY(launch_pdl(kern, (unsigned)grid, (unsigned)wpb * 32, smem, st, pdl, b));
                 return PP_OK;
             }
         }
     }
+    // several blocks per SM here: an early-started next grid could pile its
+    // blocks onto the SMs that free up first, so these launches keep plain
+    // stream order
     const size_t smem = lt_bytes + (size_t)kWarps * ring_bytes;
     const int64_t blocks = (warps + kWarps - 1) / kWarps;
     if (blocks > 0x7FFFFFFF) return PP_ERR_SIZE;
-    kern<<<(unsigned)blocks, kWarps * 32, smem, st>>>(b);
-    PPS_CUDA_TRY(cudaGetLastError());
+    PPS_CUDA_TRY(launch_pdl(kern, (unsigned)blocks, kWarps * 32, smem, st, false, b));
     return PP_OK;
 }
 
+// pdl: the tables are the plan's cached ones (built and synchronized before
+// this call), so the kernel may copy them before the previous grid ends.
 template <int PMAX, bool OPS>
-static int launch_reg_o(const EvalArgs &a, bool vec, bool lt, cudaStream_t st) {
-    if (lt) return launch_reg_t<PMAX, kRegNI, true, OPS, true>(a, 0, a.n, st);
-    if (vec) return launch_reg_t<PMAX, 1, true, OPS, false>(a, 0, a.n, st);
-    return launch_reg_t<PMAX, 1, false, OPS, false>(a, 0, a.n, st);
+static int launch_reg_o(const EvalArgs &a, bool vec, bool lt, cudaStream_t st, bool pdl = false) {
+    if (lt) return launch_reg_t<PMAX, kRegNI, true, OPS, true>(a, 0, a.n, st, pdl);
+    if (vec) return launch_reg_t<PMAX, 1, true, OPS, false>(a, 0, a.n, st, pdl);
+    return launch_reg_t<PMAX, 1, false, OPS, false>(a, 0, a.n, st, pdl);
 }
 
 // Largest per-CTA table area kept in shared memory (words); bigger plans use
@@ -660,7 +694,7 @@ static int launch_reg_p(pp_plan *plan, EvalArgs &a, bool vec, bool ops, cudaStre
             if (!ops && a.n < (int64_t)sm_count(dev) * 8 * 32) return launch_eval_split8(a, st);
         }
     }
-    return ops ? launch_reg_o<PMAX, true>(a, vec, lt, st) : launch_reg_o<PMAX, false>(a, vec, lt, st);
+    return ops ? launch_reg_o<PMAX, true>(a, vec, lt, st, true) : launch_reg_o<PMAX, false>(a, vec, lt, st, true);
 }
 
 int launch_eval_reg(pp_plan *plan, EvalArgs &a, bool vec, bool ops, cudaStream_t st) {

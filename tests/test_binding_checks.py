@@ -98,3 +98,12 @@ def test_short_and_mismatched_device_buffers_are_refused():
         B.evaluate_zb(3, P, M, c, c, c[2:], st, n)
     with pytest.raises(ValueError, match="cost_b"):
         B.evaluate_dualpipe(P, M, 4, c, c.cpu(), st, n)
+
+
+def test_binding_api_is_complete():
+    """Every public call of the binding is present (a CPU-side guard: most of
+    them only run on a GPU)."""
+    for name in ("Plan", "op_fields", "evaluate", "evaluate_zb", "evaluate_dualpipe", "evaluate_host", "Many",
+                 "partition_search", "partition_search_ranks", "partition_search_interleaved", "cache_clear",
+                 "debug_checks", "status_str", "_stream"):
+        assert callable(getattr(B, name)), name
