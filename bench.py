@@ -49,6 +49,7 @@ def algorithmic_bytes(n, P_=P, M_=M):
 
 KERNEL_SOURCES = ("pipeline_schedule_simulation_gb300/csrc/eval_reg.cu",
                   "pipeline_schedule_simulation_gb300/csrc/eval_common.cuh",
+                  "pipeline_schedule_simulation_gb300/csrc/checks.cuh",
                   "pipeline_schedule_simulation_gb300/csrc/internal.cuh")
 PROFILE = os.path.join(ROOT, "profiles", "eval_reg_1f1b_P8_M64_n65536.md")
 
