@@ -423,3 +423,58 @@ def test_eval_captured_in_cuda_graph(orc, B):
         torch.cuda.synchronize()
         got = {k: v.cpu().numpy() for k, v in out.items()}
         assert_same(got, run_oracle(orc, nb, nthreads=NCPU))
+
+
+def test_back_to_back_calls_see_previous_outputs(orc, B):
+    """Evaluations launched back to back on one stream may overlap their
+    starts (programmatic dependent launch); each must still read its inputs
+    only after the previous one's writes.  Call 1 writes every op's start and
+    end tick (instance-minor, [P*2M][n]); call 2 reads them as its forward and
+    backward costs ([S][2M][n], per microbatch, so both calls run the
+    one-block-per-SM register kernel).  Three pairs in a row on one stream,
+    then the pair captured in a CUDA graph and replayed on new inputs: every
+    call 2 equals the oracle run on call 1's times."""
+    import torch
+    P, M, n = 8, 16, 65536  # enough warps for the one-block-per-SM launch
+    O = 2 * M
+    b = W.random_batch(W.ONEF1B, P, M, 1, n, seed=21, hi=20, comm_hi=4)
+    cf, cb, cm = to_dev(b.cost_f), to_dev(b.cost_b), to_dev(b.comm)
+    st = torch.empty(P * O * n, dtype=torch.int32, device="cuda")
+    en = torch.empty(P * O * n, dtype=torch.int32, device="cuda")
+    out1 = {"op_start": st, "op_end": en}
+    s2 = (1, O * n, n)  # call 2: cost of (x, stage k, microbatch j) = time of op j on device k
+
+    def pair(stream):
+        B.evaluate(W.ONEF1B, P, M, 1, cf, cb, b.strides, n, comm=cm, comm_strides=b.comm_strides,
+                   op_times=True, op_strides=(1, n), out=out1, stream=stream)
+        return B.evaluate(W.ONEF1B, P, O, 1, st, en, s2, n, stream=stream)
+
+    def check(o2, shift):
+        r1 = orc.eval_batch(W.ONEF1B, P, M, 1, b.cost_f + shift, b.cost_b, b.strides, comm=b.comm,
+                            comm_strides=b.comm_strides, n=n, op_times=True, nthreads=16)
+        # r1 op times are [n][P][O]: as call 2's costs, strides (P*O, O, 1)
+        f2 = r1["op_start"].astype(np.int32).reshape(-1)
+        b2 = r1["op_end"].astype(np.int32).reshape(-1)
+        r2 = orc.eval_batch(W.ONEF1B, P, O, 1, f2, b2, (P * O, O, 1), n=n, nthreads=16)
+        assert_same({k: v.cpu().numpy() for k, v in o2.items()}, r2)
+
+    s = torch.cuda.Stream()
+    outs = []
+    with torch.cuda.stream(s):
+        for rep in range(3):
+            o2 = pair(s)
+            outs.append({k: v.clone() for k, v in o2.items()})
+            cf.add_(1)  # the next pair's call 1 gets new costs
+    torch.cuda.synchronize()
+    for rep, o2 in enumerate(outs):
+        check(o2, rep)
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=side):
+        o2 = pair(side)
+    cf.copy_(to_dev(b.cost_f) + 7)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    check(o2, 7)
