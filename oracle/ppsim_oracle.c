@@ -908,11 +908,19 @@ static void *search_worker(void *arg)
         for (int d = 0; d < P && !rejected; ++d) {
             int64_t held = 0, top = 0;
             for (int j = 0; j < O; ++j) {
+#if ORC_MUTANT == 18  /* mistake: every op weighted by the device's first chunk's bytes */
+                int s = d;
+#else
                 int s = jb->chunk[d * O + j] * P + d;
+#endif
                 held += jb->kind[d * O + j] == ORC_F ? act[s] : -act[s];
                 if (held > top) top = held;
             }
+#if ORC_MUTANT == 16  /* mistake: a layout exactly at the cap is rejected */
+            if (top >= jb->cap) rejected = 1;
+#else
             if (top > jb->cap) rejected = 1;
+#endif
         }
         int64_t mk = -1, bub[2];
         if (!rejected) {
@@ -922,7 +930,11 @@ static void *search_worker(void *arg)
             if (mk > ORC_INT32_MAX) mk = -2;
         }
         if (jb->all_mk) jb->all_mk[c - jb->lo] = (int32_t)mk;
+#if ORC_MUTANT == 17  /* mistake: a tie goes to the later candidate */
+        if (mk >= 0 && (jb->best_idx < 0 || mk <= jb->best_mk)) { jb->best_mk = mk; jb->best_idx = c; }
+#else
         if (mk >= 0 && (jb->best_idx < 0 || mk < jb->best_mk)) { jb->best_mk = mk; jb->best_idx = c; }
+#endif
     }
     free(tf); free(tb); free(act); free(cm); free(st); free(en); free(busy); free(idle); free(pk);
     return NULL;

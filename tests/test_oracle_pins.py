@@ -568,6 +568,9 @@ MUTANTS = {
     13: "interleaved warmup one forward too long",
     14: "DualPipe runs a ready forward before a ready backward",
     15: "DualPipe route B crosses a boundary on route A's link",
+    16: "search rejects a layout exactly at the byte cap",
+    17: "search breaks a makespan tie toward the later candidate",
+    18: "interleaved search weighs every op by the device's first chunk",
 }
 
 
@@ -680,6 +683,62 @@ def _pin_suite(orc, lib):
         return list(r["idle"]) == [3 * 5] * 8
 
     check("dualpipe", dualpipe)
+
+    def search_cap():
+        # reading R11: stage k holds min(P-k, M) microbatches of its layers'
+        # bytes at its peak; a layout is rejected only when that exceeds the
+        # cap (a layout exactly at the cap is kept)
+        P, L, M = 3, 6, 4
+        ltf = np.ones(L, np.int32)
+        ltb = np.full(L, 2, np.int32)
+        lact = np.array([5, 1, 3, 2, 4, 6], np.int64)
+        C = math.comb(L - 1, P - 1)
+        need = []
+        for r in range(C):
+            f = list(orc.rank_split(r, L, P, lib=lib))
+            need.append(max(min(P - k, M) * int(lact[f[k]:f[k + 1]].sum()) for k in range(P)))
+        cap = sorted(set(need))[len(set(need)) // 2]
+        res = orc.search_ranks(ltf, ltb, lact, P, M, 0, cap, 0, C, lib=lib)
+        return all((int(res["all_makespan"][r]) == -1) == (need[r] > cap) for r in range(C))
+
+    def search_tie():
+        # with one microbatch every split runs the same chain of all forwards
+        # then all backwards: every makespan ties and the lowest rank wins
+        L, P = 6, 3
+        C = math.comb(L - 1, P - 1)
+        res = orc.search_ranks(np.arange(1, L + 1, dtype=np.int32), np.full(L, 3, np.int32), np.ones(L, np.int64),
+                               P, 1, 0, 10**12, 0, C, lib=lib)
+        mks = set(int(x) for x in res["all_makespan"])
+        return mks == {int(np.arange(1, L + 1).sum()) + 3 * L} and res["best_idx"] == 0
+
+    def ilv_ledger():
+        # reading R22: each device's held bytes run over its interleaved order,
+        # + the bytes of the op's range at F, - at B; reject above the cap
+        P, v, M, L = 2, 2, 4, 11
+        S = P * v
+        rng = np.random.default_rng(31)
+        ltf = rng.integers(1, 9, L).astype(np.int32)
+        ltb = rng.integers(1, 9, L).astype(np.int32)
+        lact = rng.integers(1, 50, L).astype(np.int64)
+        kind, chunk, _ = orc.order("interleaved", P, M, v, lib=lib)
+        tops = []
+        for c in range(60):
+            f = list(orc.candidate_split(9, c, L, S, lib=lib))
+            act = [int(lact[f[q]:f[q + 1]].sum()) for q in range(S)]
+            top = 0
+            for d in range(P):
+                held = 0
+                for j in range(2 * M * v):
+                    held += (1 if kind[d][j] == 0 else -1) * act[chunk[d][j] * P + d]
+                    top = max(top, held)
+            tops.append(top)
+        cap = int(np.median(tops))
+        res = orc.search_interleaved(ltf, ltb, lact, P, v, M, 0, cap, 9, 0, 60, lib=lib)
+        return all((int(res["all_makespan"][c]) == -1) == (tops[c] > cap) for c in range(60))
+
+    check("search_cap", search_cap)
+    check("search_tie", search_tie)
+    check("ilv_ledger", ilv_ledger)
     return failed
 
 
