@@ -1,5 +1,6 @@
 """GPU partition search against the oracle's candidate scorer (bit-exact
 makespans, identical argmin with ties to the lower candidate index)."""
+import math
 import os
 
 import numpy as np
@@ -277,3 +278,56 @@ def test_pruned_interleaved_search_equals_full_scoring(B, comm):
         assert torch.equal(full[k].cpu(), pruned[k].cpu()), k
     mk = full["all_makespan"].cpu().numpy()
     assert int(full["best_makespan"].item()) == mk[mk >= 0].min()
+
+
+def test_cap_boundary_and_ties(orc, B):
+    """Boundaries the random problems rarely hit: a cap exactly equal to some
+    layouts' peak bytes (kept, reading R11; one byte less rejects them), and a
+    problem where every split ties (one microbatch: the same chain of all
+    forwards then all backwards), where the lowest rank must win; the same
+    for the interleaved search with the cap at the median layout's bytes."""
+    L, P, M = 12, 4, 6
+    rng = np.random.default_rng(41)
+    ltf = rng.integers(1, 9, L).astype(np.int32)
+    ltb = rng.integers(1, 9, L).astype(np.int32)
+    lact = rng.integers(1, 20, L).astype(np.int64)
+    C = math.comb(L - 1, P - 1)
+    need = []
+    for r in range(C):
+        f = list(orc.rank_split(r, L, P))
+        need.append(max(min(P - k, M) * int(lact[f[k]:f[k + 1]].sum()) for k in range(P)))
+    dev = [to_dev(x) for x in (ltf, ltb, lact)]
+    for cap in (sorted(need)[C // 2], sorted(need)[C // 2] - 1):
+        g = B.partition_search_ranks(*dev, P, M, 1, cap, 0, C, all_makespan=True)
+        r = orc.search_ranks(ltf, ltb, lact, P, M, 1, cap, 0, C, nthreads=8)
+        am = g["all_makespan"].cpu().numpy()
+        assert np.array_equal(am, r["all_makespan"])
+        assert np.array_equal(am == -1, np.array(need) > cap)
+        assert int(g["best_idx"].item()) == r["best_idx"]
+    g = B.partition_search_ranks(*dev, P, 1, 0, 10**15, 0, C, all_makespan=True)
+    am = g["all_makespan"].cpu().numpy()
+    assert len(set(am.tolist())) == 1 and int(g["best_idx"].item()) == 0
+    g = B.partition_search(*dev, P, 1, 0, 10**15, 5, 0, 4000, all_makespan=True)
+    assert int(g["best_idx"].item()) == 0
+    # interleaved (P divides M): cap at the median of the layouts' own byte peaks
+    v, S, M = 2, P * 2, 8
+    r0 = orc.search_interleaved(ltf, ltb, lact, P, v, M, 1, 10**15, 3, 0, 400, nthreads=8)
+    kind, chunk, _ = orc.order("interleaved", P, M, v)
+    tops = []
+    for c in range(400):
+        f = list(orc.candidate_split(3, c, L, S))
+        act = [int(lact[f[q]:f[q + 1]].sum()) for q in range(S)]
+        top = 0
+        for d in range(P):
+            held = 0
+            for j in range(2 * M * v):
+                held += (1 if kind[d][j] == 0 else -1) * act[chunk[d][j] * P + d]
+                top = max(top, held)
+        tops.append(top)
+    assert (r0["all_makespan"] >= 0).all()
+    cap = int(np.median(tops))
+    g = B.partition_search_interleaved(*dev, P, v, M, 1, cap, 3, 0, 400, all_makespan=True)
+    am = g["all_makespan"].cpu().numpy()
+    r = orc.search_interleaved(ltf, ltb, lact, P, v, M, 1, cap, 3, 0, 400, nthreads=8)
+    assert np.array_equal(am, r["all_makespan"])
+    assert np.array_equal(am == -1, np.array(tops) > cap)
