@@ -107,6 +107,14 @@ __global__ void __launch_bounds__(128) k_eval_zb(const EvalArgs a, const int32_t
         fetch(kZbW, m);
     }
     cp_async_commit();
+    // Zero arrival rings: the first device's forward input and the last
+    // device's backward input have no producer, their column is never
+    // written and reads 0 (arrival at tick 0).
+#pragma unroll
+    for (int q = 0; q < G::kQ; ++q) {
+        fring[q * 32 + lane] = 0u;
+        bring[q * 32 + lane] = 0u;
+    }
     cp_async_wait<0>();
     __syncwarp();
 
@@ -122,21 +130,26 @@ __global__ void __launch_bounds__(128) k_eval_zb(const EvalArgs a, const int32_t
     uint32_t lbL = 0, lbR = 0;
     const int max_steps = 3 * P * M + 2;
     bool capped = true;
+    // whether F/B op number pp of the device's order F^w (B F)^(M-w) B^w is an F
+    auto is_fwd = [&](int pp) {
+        const int q = pp - w;
+        return q < 0 || (q < 2 * (M - w) && (q & 1));
+    };
+    // carried across steps: F/B ops placed, and whether the next one is an F
+    int p = 0;
+    bool isF = is_fwd(0);
 #pragma unroll 1
     for (int step = 0; step < max_steps; ++step) {
         cp_async_wait<G::kAheadC - 2>();
         __syncwarp();
         // ---- decide (every lane evaluates the rules; no divergent paths)
         const bool pend = nw < nb;
-        const int p = nf + nb;
         const bool haveX = p < 2 * M;
-        const int q = p - w;
-        const bool isF = q < 0 || (q < 2 * (M - w) && (q & 1));  // order F^w (B F)^(M-w) B^w
         const int mx = isF ? nf : nb;
-        const uint32_t arrF = k == 0 ? 0u : fring[(mx % G::kQ) * 32 + lane];
-        const uint32_t arrB = k == P - 1 ? 0u : bring[(mx % G::kQ) * 32 + lane];
+        // the input's arrival: row mx of the ring of the op's kind (0 for the
+        // first device's forward and the last device's backward)
+        const uint32_t arr = (isF ? fring : bring)[(mx & (G::kQ - 1)) * 32 + lane];
         const bool known = isF ? (k == 0 || nfL > nf) : (k == P - 1 || nbR > nb);
-        const uint32_t arr = isF ? arrF : arrB;
         // the input has not arrived by t: known and later, or provably later
         const uint32_t lower = isF ? lbL + cmL : lbR + cmR;
         const bool late = known ? arr > t : lower > t;
@@ -177,20 +190,22 @@ __global__ void __launch_bounds__(128) k_eval_zb(const EvalArgs a, const int32_t
         held += (kind == kZbF) - (kind == kZbW);
         peak = max(peak, held);
         // ---- publish
-        const int p2 = nf + nb, q2 = p2 - w;
-        const bool nextF = q2 < 0 || (q2 < 2 * (M - w) && (q2 & 1));
+        p = nf + nb;
+        isF = is_fwd(p);
         const uint32_t cF = nf < M ? cring[(kZbF * G::kRing + nf % G::kRing) * 32 + lane] : 0u;
         const uint32_t cB = nb < M ? cring[(kZbB * G::kRing + nb % G::kRing) * 32 + lane] : 0u;
-        const bool moreX = p2 < 2 * M;
-        const uint32_t lbF = t + ((moreX && !nextF) ? cB : 0u) + cF;
-        const uint32_t lbB = t + ((moreX && nextF) ? cF : 0u) + cB;
+        const bool moreX = p < 2 * M;
+        const uint32_t lbF = t + ((moreX && !isF) ? cB : 0u) + cF;
+        const uint32_t lbB = t + ((moreX && isF) ? cF : 0u) + cB;
         cp_async_commit();
         __syncwarp();
         nfL = __shfl_up_sync(0xFFFFFFFFu, nf, G::kIPW);
         nbR = __shfl_down_sync(0xFFFFFFFFu, nb, G::kIPW);
         lbL = __shfl_up_sync(0xFFFFFFFFu, lbF, G::kIPW);
         lbR = __shfl_down_sync(0xFFFFFFFFu, lbB, G::kIPW);
-        if (__all_sync(0xFFFFFFFFu, done)) { capped = false; break; }
+        // a finished lane takes no decision, so the end is checked every
+        // fourth step
+        if ((step & 3) == 3 && __all_sync(0xFFFFFFFFu, done)) { capped = false; break; }
     }
     cp_async_wait<0>();
 
