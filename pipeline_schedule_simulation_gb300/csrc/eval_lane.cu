@@ -39,6 +39,8 @@
 #include <algorithm>
 #include <climits>
 
+#include <atomic>
+
 #include "eval_common.cuh"
 
 namespace pps {
@@ -529,11 +531,11 @@ int launch_lane_t(const EvalArgs &a, const pp_ktab *t, cudaStream_t st) {
     using G = LaneGeom<PMAX>;
     int dev = 0;
     PPS_CUDA_TRY(cudaGetDevice(&dev));
-    static bool attr_set[64] = {};
-    if (dev < 64 && !attr_set[dev]) {
+    static std::atomic<bool> attr_set[64];  // per device, set once (idempotent)
+    if (dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
         PPS_CUDA_TRY(cudaFuncSetAttribute(k_eval_lane<PMAX, NI, VEC, OPS, MBZ>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLaneSmemLimit));
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     const int64_t nw = (a.n + G::kIPW * NI - 1) / (G::kIPW * NI);
     const int warps = lane_warps<PMAX, NI, VEC, OPS, MBZ>(a, nw, sm_count(dev));
@@ -657,11 +659,11 @@ static int launch_lane_many_t(int warps, const ManyJob *d_jobs, int njobs, int64
                               cudaStream_t st) {
     int dev = 0;
     PPS_CUDA_TRY(cudaGetDevice(&dev));
-    static bool attr_set[64] = {};
-    if (dev < 64 && !attr_set[dev]) {
+    static std::atomic<bool> attr_set[64];  // per device, set once (idempotent)
+    if (dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
         PPS_CUDA_TRY(cudaFuncSetAttribute(k_eval_lane_mbz_many<PMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)kLaneSmemLimit));
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     k_eval_lane_mbz_many<PMAX><<<(unsigned)ctas, warps * 32, smem, st>>>(d_jobs, njobs);
     PPS_CUDA_TRY(cudaGetLastError());

@@ -540,11 +540,11 @@ static int launch_reg_mbz(const EvalArgs &a, cudaStream_t st) {
                         (size_t)kWarps * 5 * PMAX * 32 * sizeof(int32_t);
     int dev = 0;
     PPS_CUDA_TRY(cudaGetDevice(&dev));
-    static bool attr_set[64] = {};
-    if (dev < 64 && !attr_set[dev]) {
+    static std::atomic<bool> attr_set[64];  // per device, set once (idempotent)
+    if (dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
         PPS_CUDA_TRY(cudaFuncSetAttribute(k_eval_reg_mbz<PMAX, OPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           160 * 1024));
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     const int64_t warps = (a.n + 31) / 32;
     const int64_t blocks = (warps + kWarps - 1) / kWarps;
@@ -591,14 +591,14 @@ static int launch_reg_t(const EvalArgs &a, int64_t begin, int64_t end, cudaStrea
     if (dev >= 64) return PP_ERR_INTERNAL;
     // per device: the shared memory a block may opt into (set on the kernel)
     // and an SM's total
-    static int smem_optin[64] = {}, smem_sm[64] = {};
-    if (!smem_optin[dev]) {
+    static std::atomic<int> smem_optin[64], smem_sm[64];
+    if (!smem_optin[dev].load(std::memory_order_acquire)) {
         int optin = 0, per_sm = 0;
         PPS_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
         PPS_CUDA_TRY(cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev));
         PPS_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin));
-        smem_sm[dev] = per_sm;
-        smem_optin[dev] = optin;
+        smem_sm[dev].store(per_sm, std::memory_order_relaxed);
+        smem_optin[dev].store(optin, std::memory_order_release);
     }
     const int64_t warps = (end - begin + 32 * NI - 1) / (32 * NI);
     EvalArgs b = a;
@@ -616,7 +616,7 @@ static int launch_reg_t(const EvalArgs &a, int64_t begin, int64_t end, cudaStrea
         const int64_t wpb = (warps + grid - 1) / grid;
         if (wpb <= 32) {
             size_t smem = lt_bytes + (size_t)wpb * ring_bytes;
-            const size_t half = (size_t)smem_sm[dev] / 2;
+            const size_t half = (size_t)smem_sm[dev].load(std::memory_order_relaxed) / 2;
             if (smem < half) smem = half;
             // whether such a block fits, remembered per device for the last
             // (warps, shared memory) pair asked
@@ -626,7 +626,7 @@ static int launch_reg_t(const EvalArgs &a, int64_t begin, int64_t end, cudaStrea
             uint64_t memo = fit_memo[dev].load(std::memory_order_relaxed);
             if (memo >> 32 != key) {
                 int fit = 0;
-                if (smem > (size_t)smem_optin[dev] ||
+                if (smem > (size_t)smem_optin[dev].load(std::memory_order_relaxed) ||
                     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, kern, (int)wpb * 32, smem) != cudaSuccess)
                     fit = 0;
                 (void)cudaGetLastError();
@@ -746,14 +746,14 @@ static int launch_mbz_many_t(int warps, const ManyJob *d_jobs, int njobs, int64_
     int dev = 0;
     PPS_CUDA_TRY(cudaGetDevice(&dev));
     if (dev >= 64) return PP_ERR_INTERNAL;
-    static int optin[64] = {};
-    if (!optin[dev]) {
+    static std::atomic<int> optin[64];
+    if (!optin[dev].load(std::memory_order_acquire)) {
         int o = 0;
         PPS_CUDA_TRY(cudaDeviceGetAttribute(&o, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
         PPS_CUDA_TRY(cudaFuncSetAttribute(k_eval_reg_mbz_many<PMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, o));
-        optin[dev] = o;
+        optin[dev].store(o, std::memory_order_release);
     }
-    if (smem > (size_t)optin[dev]) return PP_ERR_SIZE;
+    if (smem > (size_t)optin[dev].load(std::memory_order_relaxed)) return PP_ERR_SIZE;
     k_eval_reg_mbz_many<PMAX><<<(unsigned)ctas, warps * 32, smem, st>>>(d_jobs, njobs);
     PPS_CUDA_TRY(cudaGetLastError());
     return PP_OK;

@@ -8,6 +8,8 @@
 // its producer's round to its consumer's round) onto one of at most 64 slots;
 // each warp keeps the slots and the instance's comm table in shared memory as
 // [slot][lane], so every access is conflict-free.
+#include <atomic>
+
 #include "eval_common.cuh"
 
 namespace pps {
@@ -118,11 +120,14 @@ static int launch_slot_t(const EvalArgs &a, cudaStream_t st) {
     constexpr int kWarps = 2;
     const size_t per_warp = (size_t)(Ring<PMAX>::kWords + (a.nslots + a.S) * 32) * sizeof(int32_t);
     const size_t smem = kWarps * per_warp;
-    static bool attr_set = false;  // opt in to > 48 KB once per instantiation
-    if (!attr_set) {
+    // opt in to > 48 KB once per instantiation and device (idempotent)
+    int dev = 0;
+    PPS_CUDA_TRY(cudaGetDevice(&dev));
+    static std::atomic<bool> attr_set[64];
+    if (dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
         PPS_CUDA_TRY(cudaFuncSetAttribute(k_eval_slot<PMAX, VEC, OPS>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
-        attr_set = true;
+        if (dev < 64) attr_set[dev].store(true, std::memory_order_release);
     }
     const int64_t warps = (a.n + 31) / 32;
     const int64_t blocks = (warps + kWarps - 1) / kWarps;

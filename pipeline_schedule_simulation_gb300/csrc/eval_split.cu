@@ -17,6 +17,8 @@
 // compute; one 16-byte copy per lane and round (4 lanes cover the 64 bytes of
 // a device's row for the warp's 16 instances), driven by the same per-stride
 // loader table, round words and segments as k_eval_reg.
+#include <atomic>
+
 #include "eval_common.cuh"
 
 namespace pps {
@@ -292,10 +294,10 @@ int launch_eval_split8(const EvalArgs &a, cudaStream_t st) {
     const size_t smem = (size_t)a.ktab_words * sizeof(uint32_t) + (size_t)G::kWarps * G::kRingWords * sizeof(int32_t);
     int dev = 0;
     PPS_CUDA_TRY(cudaGetDevice(&dev));
-    static bool attr_set[64] = {};
-    if (dev < 64 && !attr_set[dev]) {
+    static std::atomic<bool> attr_set[64];  // per device, set once (idempotent)
+    if (dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
         PPS_CUDA_TRY(cudaFuncSetAttribute(k_eval_split<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024));
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     const int64_t warps = (a.n + G::kIPW - 1) / G::kIPW;
     const int64_t blocks = (warps + G::kWarps - 1) / G::kWarps;

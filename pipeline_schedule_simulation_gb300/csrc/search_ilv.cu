@@ -26,6 +26,8 @@
 #include <mutex>
 #include <vector>
 
+#include <atomic>
+
 #include "eval_common.cuh"
 #include "search_common.cuh"
 
@@ -389,11 +391,11 @@ extern "C" int pp_sched_partition_search_interleaved(const int32_t *layer_tf, co
     if (rc) return rc;
     a.lvec = lt->d_vec; a.loff = lt->d_off;
     const size_t smem = ilv_smem(L, S);
-    static bool attr_set[64] = {};
-    if (dev < 64 && !attr_set[dev]) {
+    static std::atomic<bool> attr_set[64];  // per device, set once (idempotent)
+    if (dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
         PPS_CUDA_TRY(cudaFuncSetAttribute(k_ilv_cands, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
         PPS_CUDA_TRY(cudaFuncSetAttribute(k_ilv_finish, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     unsigned long long *key = reinterpret_cast<unsigned long long *>(best_idx);
     a.key = key;
