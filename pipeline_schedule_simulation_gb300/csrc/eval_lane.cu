@@ -256,7 +256,12 @@ __device__ __forceinline__ void lane_copy_block(const uint4 *blocks, int b, uint
 // kernel over many problems runs it too.
 template <int PMAX, int NI, bool VEC, bool OPS, bool MBZ>
 __device__ __forceinline__ void lane_body(const EvalArgs &a, const uint4 *tab, int nblocks, int64_t bid) {
-    copy_peak(a, bid);
+    // Programmatic dependent launch (the one-CTA-per-SM launch): the next
+    // grid may place its CTAs as this one's retire; a CTA copies its first
+    // table block (the plan's, complete before the launch) and waits for the
+    // previous grid before it reads an input or writes an output.  Without
+    // the launch attribute both instructions do nothing.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     using G = LaneGeom<PMAX>;
     constexpr int kRow = 32 * NI;  // words per row
     constexpr int kRingRows = MBZ ? 0 : G::kSlices;
@@ -268,7 +273,17 @@ __device__ __forceinline__ void lane_body(const EvalArgs &a, const uint4 *tab, i
     uint32_t *ring = lsm + 2 * G::kBlockWords + warp * rows * kRow;
     uint32_t *val = ring + kRingRows * kRow;
     uint32_t *ctab = val + (a.nslots + 2) * kRow;
-    const int64_t inst0 = (bid * nwarps + warp) * (G::kIPW * NI);
+    // a.tasks > 0 (one CTA per SM): CTA b takes warp tasks [b*T/G, (b+1)*T/G),
+    // so SMs differ by one warp at most; a CTA's spare warp runs on
+    // instances past the batch (it still takes part in the CTA's barriers)
+    int64_t wtask = bid * nwarps + warp;
+    bool has_task = true;
+    if (a.tasks > 0) {
+        const int64_t t0 = bid * a.tasks / gridDim.x, t1 = (bid + 1) * a.tasks / gridDim.x;
+        wtask = t0 + warp;
+        has_task = wtask < t1;
+    }
+    const int64_t inst0 = has_task ? wtask * (G::kIPW * NI) : a.n;
     const int64_t x0 = inst0 + j;  // set i holds instance x0 + i * kIPW
     const uint4 *blocks = tab + G::kHeadWords / 4;
     const int R = a.R;
@@ -276,6 +291,8 @@ __device__ __forceinline__ void lane_body(const EvalArgs &a, const uint4 *tab, i
     // every warp stays to the end: the table blocks are shared by the CTA
     lane_copy_block<PMAX>(blocks, 0, lsm);
     cp_async_commit();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    copy_peak(a, bid);
     const uint32_t *head = reinterpret_cast<const uint32_t *>(tab);
     const LaneLoader<PMAX, NI, VEC> ld(a, lane, j, k, inst0);
     const uint32_t ring_s = smem_addr(ring);
@@ -441,7 +458,7 @@ __device__ __forceinline__ void lane_body(const EvalArgs &a, const uint4 *tab, i
 }
 
 template <int PMAX, int NI, bool VEC, bool OPS, bool MBZ>
-__global__ void __launch_bounds__(256) k_eval_lane(const EvalArgs a, const uint4 *tab, int nblocks) {
+__global__ void __launch_bounds__(512) k_eval_lane(const EvalArgs a, const uint4 *tab, int nblocks) {
     lane_body<PMAX, NI, VEC, OPS, MBZ>(a, tab, nblocks, blockIdx.x);
 }
 
@@ -538,12 +555,47 @@ int launch_lane_t(const EvalArgs &a, const pp_ktab *t, cudaStream_t st) {
         attr_set[dev].store(true, std::memory_order_release);
     }
     const int64_t nw = (a.n + G::kIPW * NI - 1) / (G::kIPW * NI);
+    const int nblocks = (a.R + G::kBR - 1) / G::kBR;
+    // A batch whose warps all fit on the GPU at once: one CTA per SM taking
+    // warp tasks by range (SMs differ by one warp), launched as a
+    // programmatic dependent launch.  Asking for at least half an SM's shared
+    // memory keeps a second CTA -- of this grid or the next -- off the SM, so
+    // the next grid's CTAs land one per SM as this grid's retire.
+    {
+        const int nsm = sm_count(dev);
+        const int64_t grid = nw < nsm ? nw : nsm;
+        const int64_t wpb = grid > 0 ? (nw + grid - 1) / grid : 0;
+        int per_sm_smem = 0;
+        PPS_CUDA_TRY(cudaDeviceGetAttribute(&per_sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev));
+        size_t smem = wpb > 0 ? lane_smem<PMAX>(a, (int)wpb, NI, MBZ) : 0;
+        if (smem < (size_t)per_sm_smem / 2) smem = (size_t)per_sm_smem / 2;
+        int fit = 0;
+        if (wpb >= 1 && wpb <= 16 && smem <= kLaneSmemLimit &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, k_eval_lane<PMAX, NI, VEC, OPS, MBZ>, (int)wpb * 32,
+                                                          smem) == cudaSuccess &&
+            fit >= 1) {
+            EvalArgs b = a;
+            b.tasks = nw;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)grid);
+            cfg.blockDim = dim3((unsigned)wpb * 32);
+            cfg.dynamicSmemBytes = smem;
+            cfg.stream = st;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            at[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            PPS_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_eval_lane<PMAX, NI, VEC, OPS, MBZ>, b, t->d, nblocks));
+            return PP_OK;
+        }
+        (void)cudaGetLastError();
+    }
     const int warps = lane_warps<PMAX, NI, VEC, OPS, MBZ>(a, nw, sm_count(dev));
     if (!warps) return PP_ERR_SIZE;
     const size_t smem = lane_smem<PMAX>(a, warps, NI, MBZ);
     const int64_t grid = (nw + warps - 1) / warps;
     if (grid > 0x7FFFFFFF) return PP_ERR_SIZE;
-    const int nblocks = (a.R + G::kBR - 1) / G::kBR;
     k_eval_lane<PMAX, NI, VEC, OPS, MBZ><<<(unsigned)grid, warps * 32, smem, st>>>(a, t->d, nblocks);
     PPS_CUDA_TRY(cudaGetLastError());
     return PP_OK;
