@@ -478,3 +478,40 @@ def test_back_to_back_calls_see_previous_outputs(orc, B):
     g.replay()
     torch.cuda.synchronize()
     check(o2, 7)
+
+
+def test_back_to_back_costs_shared_by_microbatches(orc, B):
+    """Back-to-back calls on the microbatch-shared register kernel: call 1
+    (costs per instance and stage, stride_mb 0) writes every op's start and
+    end tick; call 2 reads device k's first op start and end as stage k's
+    forward and backward cost (stride_mb 0 again), and the next pair's call 1
+    rewrites them.  Three pairs on one stream, each call 2 against the oracle
+    run on call 1's times."""
+    import torch
+    P, M, n = 8, 16, 65536
+    O = 2 * M
+    b = W.random_batch(W.ONEF1B, P, M, 1, n, seed=23, hi=20, comm_hi=4, stride_mb_zero=True)
+    assert b.strides[2] == 0 and b.strides[0] == 1
+    cf, cb, cm = to_dev(b.cost_f), to_dev(b.cost_b), to_dev(b.comm)
+    st = torch.empty(P * O * n, dtype=torch.int32, device="cuda")
+    en = torch.empty(P * O * n, dtype=torch.int32, device="cuda")
+    out1 = {"op_start": st, "op_end": en}
+    s2 = (1, O * n, 0)  # call 2: cost of (x, stage k) = time of op 0 on device k
+
+    s = torch.cuda.Stream()
+    outs = []
+    with torch.cuda.stream(s):
+        for rep in range(3):
+            B.evaluate(W.ONEF1B, P, M, 1, cf, cb, b.strides, n, comm=cm, comm_strides=b.comm_strides,
+                       op_times=True, op_strides=(1, n), out=out1, stream=s)
+            o2 = B.evaluate(W.ONEF1B, P, M, 1, st, en, s2, n, stream=s)
+            outs.append({k: v.clone() for k, v in o2.items()})
+            cf.add_(1)
+    torch.cuda.synchronize()
+    for rep, o2 in enumerate(outs):
+        r1 = orc.eval_batch(W.ONEF1B, P, M, 1, b.cost_f + rep, b.cost_b, b.strides, comm=b.comm,
+                            comm_strides=b.comm_strides, n=n, op_times=True, nthreads=16)
+        f2 = r1["op_start"].astype(np.int32).reshape(-1)  # [n][P][O]
+        b2 = r1["op_end"].astype(np.int32).reshape(-1)
+        r2 = orc.eval_batch(W.ONEF1B, P, M, 1, f2, b2, (P * O, O, 0), n=n, nthreads=16)
+        assert_same({k: v.cpu().numpy() for k, v in o2.items()}, r2)
