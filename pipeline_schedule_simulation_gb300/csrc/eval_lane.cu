@@ -36,6 +36,16 @@
 //   w  loader entry of round r + kAhead: byte offset of the op's cost row
 //      | 1 for a backward op, or kLtIdle; shifted by kAhead rounds so the
 //      loader never needs the next block
+// With costs shared by all microbatches (stride_mb == 0) there is no loader,
+// and the entry is one word, so a block holds four times the rounds and a
+// round reads a quarter of the bytes:
+//   bits 0..14   byte offset of the output slot cell (as z, without bit 31)
+//   bit 15       the op is not idle
+//   bits 16..22  the op's {cost, comm} row (2 * chunk + kind; 2v: the zero row)
+//   bits 23..31  the input slot row's byte offset / 128 (the lane's own
+//                column is added by the lane)
+// which holds while (nslots + 2) * row bytes <= 2^15 and 2v + 1 <= 127
+// (lane_word_entries); past that, such costs run through the cost ring.
 #include <algorithm>
 #include <climits>
 
@@ -52,6 +62,7 @@ struct LaneGeom {
     static constexpr int kAhead = kSlices - 2;          // rounds loaded ahead
     static constexpr int kBR = 512 / PMAX;              // rounds per table block
     static constexpr int kBlockWords = 4 * kBR * PMAX;  // one uint4 per entry
+    static constexpr int kBRw = 4 * kBR;                // rounds per block of one-word entries
     static constexpr int kHeadWords = (kAhead * PMAX + 3) & ~3;
     static constexpr int kCopy = kIPW < 4 ? kIPW : 4;   // instances per loader copy (vector path)
     static_assert(kBR > kAhead, "a table block must outlast the loader's lead");
@@ -79,9 +90,36 @@ __device__ __forceinline__ uint32_t lane_lt(const uint32_t *desc, int R, int P, 
 // the top of the file.  Word e of that table:
 template <int PMAX>
 __device__ uint32_t ltab_word(const uint32_t *desc, const uint8_t *lrd, const uint8_t *lwr, int R, int P, int v,
-                              int nslots, int s_stage, int s_mb, uint32_t row_bytes, int64_t e) {
+                              int nslots, int s_stage, int s_mb, uint32_t row_bytes, bool word, int64_t e) {
     using G = LaneGeom<PMAX>;
     uint32_t w = kLtIdle;
+    if (word) {
+        // one word per entry; the head (loader entries) is not read
+        if (e < G::kHeadWords) return kLtIdle;
+        const int64_t e2 = e - G::kHeadWords;
+        const int b = (int)(e2 / G::kBlockWords);
+        const int o = (int)(e2 % G::kBlockWords);
+        const int q = o / PMAX, k = o % PMAX, r = b * G::kBRw + q;
+        const uint32_t col = (uint32_t)(k * G::kIPW * 4);
+        uint32_t rd = (uint32_t)nslots * row_bytes;              // zero row
+        uint32_t wr = (uint32_t)(nslots + 1) * row_bytes + col;  // scratch row
+        uint32_t cmr = (uint32_t)(2 * v), act = 0;               // zero comm row
+        if (r < R) {
+            const uint32_t d = desc[(int64_t)r * PMAX + k];
+            const uint32_t kind = desc_kind(d);
+            if (kind != kIdle) {
+                act = 1u << 15;
+                const uint32_t rs = lrd[(int64_t)r * PMAX + k], ws = lwr[(int64_t)r * PMAX + k];
+                cmr = 2u * desc_chunk(d) + (kind == kBwd ? 1u : 0u);
+                if (rs != kNoSlot) rd = rs * row_bytes;
+                if (ws != kNoSlot) {
+                    const int kc = kind == kFwd ? (k + 1) % P : (k + P - 1) % P;
+                    wr = ws * row_bytes + (uint32_t)(kc * G::kIPW * 4);
+                }
+            }
+        }
+        return wr | act | ((rd | cmr) << 16);
+    }
     if (e < G::kHeadWords) {
         const int q = (int)e;
         if (q < G::kAhead * PMAX) w = lane_lt(desc, R, P, PMAX, q / PMAX, q % PMAX, s_stage, s_mb);
@@ -122,12 +160,12 @@ __device__ uint32_t ltab_word(const uint32_t *desc, const uint8_t *lrd, const ui
 
 template <int PMAX>
 __global__ void k_ltab(const uint32_t *desc, const uint8_t *lrd, const uint8_t *lwr, int R, int P, int v, int nslots,
-                       int s_stage, int s_mb, int nblocks, uint32_t row_bytes, uint32_t *out) {
+                       int s_stage, int s_mb, int nblocks, uint32_t row_bytes, bool word, uint32_t *out) {
     using G = LaneGeom<PMAX>;
     const int64_t total = G::kHeadWords + (int64_t)nblocks * G::kBlockWords;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
          e += (int64_t)gridDim.x * blockDim.x)
-        out[e] = ltab_word<PMAX>(desc, lrd, lwr, R, P, v, nslots, s_stage, s_mb, row_bytes, e);
+        out[e] = ltab_word<PMAX>(desc, lrd, lwr, R, P, v, nslots, s_stage, s_mb, row_bytes, word, e);
 }
 
 // Many tables with one instance set per lane, one TableJob per table (blockIdx.y).
@@ -138,7 +176,7 @@ __global__ void kb_ltab(const TableJob *jobs) {
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < b.words;
          e += (int64_t)gridDim.x * blockDim.x)
         b.out[e] = ltab_word<PMAX>(b.desc, b.lslot, b.lslot + cells, b.R, b.P, b.v, b.nslots, b.s_stage, b.s_mb,
-                                   128u, e);
+                                   128u, b.word != 0, e);
 }
 
 // This lane's share of a round's cost copies.  Vector path: a device row of
@@ -344,6 +382,10 @@ __device__ __forceinline__ void lane_body(const EvalArgs &a, const uint4 *tab, i
     // ctab cell of this lane's instance j: word offsets in the table entries
     // count 4 bytes per cell, MBZ cells are 8 bytes
     const uint32_t ctab_s = smem_addr(ctab + j * kCw);
+    // one-word entries (MBZ) leave out the lane's own column of the input
+    // slot and comm rows
+    const uint32_t colk = (uint32_t)(k * G::kIPW * 4);
+    const uint32_t valk_s = val_s + colk, ctabk_s = ctab_s + colk * kCw;
     uint32_t fr[NI], busy[NI], flag[NI];
 #pragma unroll
     for (int i = 0; i < NI; ++i) { fr[i] = 0; busy[i] = 0; flag[i] = 0; }
@@ -352,31 +394,54 @@ __device__ __forceinline__ void lane_body(const EvalArgs &a, const uint4 *tab, i
     for (int b = 0; b < nblocks; ++b) {
         if (b + 1 < nblocks) lane_copy_block<PMAX>(blocks, b + 1, lsm + ((b + 1) & 1) * G::kBlockWords);
         if constexpr (MBZ) cp_async_commit();  // otherwise the copy joins the next round's group
-        const uint32_t ent_s = smem_addr(lsm + (b & 1) * G::kBlockWords) + k * 16;
-        const int n_r = min(R - b * G::kBR, G::kBR);
+        constexpr int kEb = MBZ ? 4 : 16;  // bytes per entry
+        constexpr int kBr = MBZ ? G::kBRw : G::kBR;
+        const uint32_t ent_s = smem_addr(lsm + (b & 1) * G::kBlockWords) + k * kEb;
+        const int n_r = min(R - b * kBr, kBr);
         // One round: the loader runs kAhead rounds ahead into ring row nxt,
         // the op reads its cost from row cur (rows are round mod kSlices; a
         // block starts at a multiple of kSlices).  The next round's entry is
         // read one round early; past the block's last round that read lands
         // in the other table buffer or the first warp's ring (still inside
         // the CTA's shared memory) and is discarded.
-        uint4 nx = lds128(ent_s);
+        uint4 nx = make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (MBZ) nx.x = lds32(ent_s);
+        else nx = lds128(ent_s);
         auto round = [&](int q, int cur, int nxt) {
             const uint4 e = nx;
-            nx = lds128(ent_s + (q + 1) * PMAX * 16);
+            if constexpr (MBZ) nx.x = lds32(ent_s + (q + 1) * PMAX * kEb);
+            else nx = lds128(ent_s + (q + 1) * PMAX * kEb);
             if constexpr (!MBZ) {
                 ld.issue(e.w, ring_s + nxt * kRow * 4);
                 cp_async_commit();
                 cp_async_wait<G::kAhead>();
             }
             __syncwarp();
-            const uint32_t vr = val_s + e.x, cr = ctab_s + e.y * kCw, vw = val_s + (e.z & ~kLaneActive);
-            // (checked build: the entry's offsets inside the warp's value rows
-            // and comm rows; row bytes = 128*NI)
-            const bool okr = PPS_CHECK(e.x < (uint32_t)(a.nslots + 2) * 128u * NI, kChkLaneSlotRead, e.x);
-            const bool okw = PPS_CHECK((e.z & ~kLaneActive) < (uint32_t)(a.nslots + 2) * 128u * NI,
-                                       kChkLaneSlotWrite, e.z & ~kLaneActive);
-            const bool okc = PPS_CHECK(e.y < (uint32_t)(2 * a.v + 1) * 128u * NI, kChkLaneComm, e.y);
+            // shared addresses of the input slot cell, the {cost, comm} or
+            // comm cell and the output slot cell; whether the op is not idle
+            // (checked build: the entry's offsets inside the warp's value
+            // rows and comm rows; row bytes = 128*NI)
+            uint32_t vr, cr, vw, act;
+            bool okr, okw, okc;
+            if constexpr (MBZ) {
+                const uint32_t hi = e.x >> 16, xo = hi & 0xFF80u, co = hi & 0x7Fu, wo = e.x & 0x7FFFu;
+                vr = valk_s + xo;
+                cr = ctabk_s + co * (256u * NI);
+                vw = val_s + wo;
+                act = e.x & 0x8000u;
+                okr = PPS_CHECK(xo + colk < (uint32_t)(a.nslots + 2) * 128u * NI, kChkLaneSlotRead, xo);
+                okw = PPS_CHECK(wo < (uint32_t)(a.nslots + 2) * 128u * NI, kChkLaneSlotWrite, wo);
+                okc = PPS_CHECK(co < (uint32_t)(2 * a.v + 1), kChkLaneComm, co);
+            } else {
+                vr = val_s + e.x;
+                cr = ctab_s + e.y * kCw;
+                vw = val_s + (e.z & ~kLaneActive);
+                act = e.z & kLaneActive;
+                okr = PPS_CHECK(e.x < (uint32_t)(a.nslots + 2) * 128u * NI, kChkLaneSlotRead, e.x);
+                okw = PPS_CHECK((e.z & ~kLaneActive) < (uint32_t)(a.nslots + 2) * 128u * NI, kChkLaneSlotWrite,
+                                e.z & ~kLaneActive);
+                okc = PPS_CHECK(e.y < (uint32_t)(2 * a.v + 1) * 128u * NI, kChkLaneComm, e.y);
+            }
 #pragma unroll
             for (int i = 0; i < NI; ++i) {
                 uint32_t c = 0, cm = 0;
@@ -399,14 +464,14 @@ __device__ __forceinline__ void lane_body(const EvalArgs &a, const uint4 *tab, i
                 if (okw) sts32(vw + 128 * i, en);
                 if constexpr (OPS) {
                     const int64_t x = x0 + i * G::kIPW;
-                    if ((e.z & kLaneActive) && x < a.n) {
+                    if (act && x < a.n) {
                         const int64_t off = x * a.o_inst + ((int64_t)k * a.O + cnt) * a.o_op;
                         if (a.op_start) a.op_start[off] = (int32_t)st;
                         if (a.op_end) a.op_end[off] = (int32_t)en;
                     }
                 }
             }
-            if constexpr (OPS) cnt += (e.z & kLaneActive) ? 1 : 0;
+            if constexpr (OPS) cnt += act ? 1 : 0;
         };
         int q = 0;
 #pragma unroll 1
@@ -479,7 +544,9 @@ int lane_tables_t(pp_plan *plan, int64_t s_stage, int64_t s_mb, cudaStream_t str
     std::lock_guard<std::mutex> lk(plan->ktab_mu);
     for (const pp_ktab &t : plan->ltabs)
         if (t.s_stage == s_stage && t.s_mb == s_mb && t.variant == NI) { *out = &t; return PP_OK; }
-    const int nblocks = (plan->R + G::kBR - 1) / G::kBR;
+    const bool word = lane_word_entries(plan->nlslots, plan->v, s_mb, NI);
+    const int br = word ? G::kBRw : G::kBR;
+    const int nblocks = (plan->R + br - 1) / br;
     pp_ktab t;
     t.s_stage = s_stage;
     t.s_mb = s_mb;
@@ -490,7 +557,7 @@ int lane_tables_t(pp_plan *plan, int64_t s_stage, int64_t s_mb, cudaStream_t str
     const int64_t cells = (int64_t)plan->R * PMAX;
     k_ltab<PMAX><<<blocks, 256, 0, stream>>>(plan->d_desc, plan->d_lslot, plan->d_lslot + cells, plan->R, plan->P,
                                              plan->v, plan->nlslots, (int)s_stage, (int)s_mb, nblocks, 128 * NI,
-                                             reinterpret_cast<uint32_t *>(t.d));
+                                             word, reinterpret_cast<uint32_t *>(t.d));
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) {
@@ -555,7 +622,8 @@ int launch_lane_t(const EvalArgs &a, const pp_ktab *t, cudaStream_t st) {
         attr_set[dev].store(true, std::memory_order_release);
     }
     const int64_t nw = (a.n + G::kIPW * NI - 1) / (G::kIPW * NI);
-    const int nblocks = (a.R + G::kBR - 1) / G::kBR;
+    constexpr int kBr = MBZ ? G::kBRw : G::kBR;
+    const int nblocks = (a.R + kBr - 1) / kBr;
     // A batch whose warps all fit on the GPU at once: one CTA per SM taking
     // warp tasks by range (SMs differ by one warp), launched as a
     // programmatic dependent launch.  Asking for at least half an SM's shared
@@ -606,8 +674,9 @@ int launch_lane_n(pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStre
     const pp_ktab *t = nullptr;
     const int rc = lane_tables_t<PMAX, NI>(plan, a.s_stage, a.s_mb, st, &t);
     if (rc) return rc;
-    // costs shared by every microbatch: kept per lane, no cost ring
-    if (a.s_mb == 0)
+    // costs shared by every microbatch: kept per lane, no cost ring (where
+    // the table has one-word entries)
+    if (lane_word_entries(a.nslots, a.v, a.s_mb, NI))
         return ops ? launch_lane_t<PMAX, NI, false, true, true>(a, t, st)
                    : launch_lane_t<PMAX, NI, false, false, true>(a, t, st);
     if (vec)
@@ -620,7 +689,9 @@ int launch_lane_n(pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStre
 template <int PMAX>
 int launch_lane_p(pp_plan *plan, const EvalArgs &a, bool vec, bool ops, cudaStream_t st) {
     using G = LaneGeom<PMAX>;
-    const bool two = a.n / (2 * G::kIPW) >= kLaneWarpsForTwoSets && lane_smem<PMAX>(a, 2, 2) <= kLaneSmemLimit;
+    // (not where one set would have one-word entries and two would not)
+    const bool two = a.n / (2 * G::kIPW) >= kLaneWarpsForTwoSets && lane_smem<PMAX>(a, 2, 2) <= kLaneSmemLimit &&
+                     lane_word_entries(a.nslots, a.v, a.s_mb, 2) == lane_word_entries(a.nslots, a.v, a.s_mb, 1);
     return two ? launch_lane_n<PMAX, 2>(plan, a, vec, ops, st) : launch_lane_n<PMAX, 1>(plan, a, vec, ops, st);
 }
 
@@ -653,14 +724,23 @@ int launch_eval_lane(pp_plan *plan, const EvalArgs &args, bool vec, bool ops, cu
     }
 }
 
-int64_t lane_table_words(int pmax, int R, int *nblocks) {
+bool lane_word_entries(int nslots, int v, int64_t s_mb, int ni) {
+    return s_mb == 0 && (int64_t)(nslots + 2) * 128 * ni <= (1 << 15) && 2 * v + 1 <= 127;
+}
+
+template <int PMAX>
+static int64_t lane_table_words_t(int R, bool word, int *nblocks) {
+    using G = LaneGeom<PMAX>;
+    const int br = word ? G::kBRw : G::kBR;
+    *nblocks = (R + br - 1) / br;
+    return G::kHeadWords + (int64_t)*nblocks * G::kBlockWords;
+}
+
+int64_t lane_table_words(int pmax, int R, bool word, int *nblocks) {
     switch (pmax) {
-        case 4: *nblocks = (R + LaneGeom<4>::kBR - 1) / LaneGeom<4>::kBR;
-                return LaneGeom<4>::kHeadWords + (int64_t)*nblocks * LaneGeom<4>::kBlockWords;
-        case 8: *nblocks = (R + LaneGeom<8>::kBR - 1) / LaneGeom<8>::kBR;
-                return LaneGeom<8>::kHeadWords + (int64_t)*nblocks * LaneGeom<8>::kBlockWords;
-        case 16: *nblocks = (R + LaneGeom<16>::kBR - 1) / LaneGeom<16>::kBR;
-                 return LaneGeom<16>::kHeadWords + (int64_t)*nblocks * LaneGeom<16>::kBlockWords;
+        case 4: return lane_table_words_t<4>(R, word, nblocks);
+        case 8: return lane_table_words_t<8>(R, word, nblocks);
+        case 16: return lane_table_words_t<16>(R, word, nblocks);
         default: return -1;
     }
 }
@@ -683,7 +763,7 @@ int launch_ltab_batch(int pmax, const TableJob *d_jobs, int njobs, int64_t max_w
 // per-op output or a separate backward latency.
 bool lane_mbz_ok(const pp_plan *plan, EvalArgs &a) {
     if (plan->reg_ok || a.comm_b || a.op_start || a.op_end || a.s_mb != 0 || a.n <= 0) return false;
-    if (!lane_path(plan, a)) return false;
+    if (!lane_path(plan, a) || !lane_word_entries(plan->nlslots, plan->v, a.s_mb, 1)) return false;
     a.nslots = plan->nlslots;
     return lane_mbz_smem(plan->pmax, a, kManyLaneWarps) <= kLaneSmemLimit;
 }

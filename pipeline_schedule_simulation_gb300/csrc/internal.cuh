@@ -159,12 +159,16 @@ struct TableJob {
     const uint8_t *lslot;  // [2][R][pmax] (lane tables)
     int R, P, v, pmax, nseg, nslots, nblocks;
     int s_stage, s_mb;
+    int word;  // lane tables: one-word entries
     int64_t words;
     uint32_t *out;
 };
-// Lane evaluator tables (eval_lane.cu): words of one table with one instance
-// set per lane, and the batched build of such tables for one table width.
-int64_t lane_table_words(int pmax, int R, int *nblocks);
+// Lane evaluator tables (eval_lane.cu): whether a table has one-word entries
+// (costs shared by all microbatches, small enough offsets), words of one
+// table with one instance set per lane, and the batched build of such tables
+// for one table width.
+bool lane_word_entries(int nslots, int v, int64_t s_mb, int ni);
+int64_t lane_table_words(int pmax, int R, bool word, int *nblocks);
 int launch_ltab_batch(int pmax, const TableJob *d_jobs, int njobs, int64_t max_words, cudaStream_t stream);
 // Value slots for a plan built without them (register plans get them on
 // first need); PP_ERR_SIZE if too many results would be in flight.

@@ -83,7 +83,7 @@ int prepare(const pp_problem_t *problems, int n_problems, pp_many *h, cudaStream
             j.job.a.ktab_words = t->words;
         } else {
             j.job.tab = t->d;
-            if (lane_table_words(j.pmax, j.job.a.R, &j.job.nblocks) < 0) return PP_ERR_INTERNAL;
+            if (lane_table_words(j.pmax, j.job.a.R, true, &j.job.nblocks) < 0) return PP_ERR_INTERNAL;
         }
     }
     // groups by kernel and table width; within a group the jobs with the most

@@ -983,7 +983,8 @@ int build_tables(TableReq *reqs, int n, cudaStream_t st) {
         if (it != seen.end()) { which[i] = it->second; continue; }
         Q e{r.plan, r.s_stage, r.s_mb, r.lane, 0, total, 0};
         if (r.lane) {
-            e.words = lane_table_words(r.plan->pmax, r.plan->R, &e.nblocks);
+            e.words = lane_table_words(r.plan->pmax, r.plan->R, lane_word_entries(r.plan->nlslots, r.plan->v, r.s_mb, 1),
+                                       &e.nblocks);
             if (e.words < 0) return PP_ERR_INTERNAL;
             max_lane = std::max(max_lane, e.words);
         } else {
@@ -1017,6 +1018,7 @@ int build_tables(TableReq *reqs, int n, cudaStream_t st) {
                 j.R = p->R; j.P = p->P; j.v = p->v; j.pmax = p->pmax; j.nseg = p->nseg;
                 j.nslots = p->nlslots; j.nblocks = e.nblocks;
                 j.s_stage = (int)e.s_stage; j.s_mb = (int)e.s_mb;
+                j.word = e.lane && lane_word_entries(p->nlslots, p->v, e.s_mb, 1);
                 j.words = e.words; j.out = A.w() + e.off;
                 jobs.push_back(j);
             }

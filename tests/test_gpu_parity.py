@@ -515,3 +515,19 @@ def test_back_to_back_costs_shared_by_microbatches(orc, B):
         b2 = r1["op_end"].astype(np.int32).reshape(-1)
         r2 = orc.eval_batch(W.ONEF1B, P, M, 1, f2, b2, (P * O, O, 0), n=n, nthreads=16)
         assert_same({k: v.cpu().numpy() for k, v in o2.items()}, r2)
+
+
+@pytest.mark.parametrize("P,M,v,n,ops", [(1, 4, 64, 40, True), (2, 4, 32, 70, True), (1, 2, 2, 33, False),
+                                         (16, 32, 4, 300, False)])
+def test_lane_table_entry_formats(orc, B, P, M, v, n, ops):
+    """Interleaved plans whose costs are shared by all microbatches run the
+    lane evaluator with one-word table entries while their 2v {cost, comm}
+    rows and the zero row fit 7 bits (v = 32 on 2 devices: 65 rows), and the
+    cost ring with four-word entries past that (v = 64 on one device: 129
+    rows); every output, and every op time where asked, against the oracle."""
+    batch = W.random_batch(W.INTERLEAVED, P, M, v, n, seed=5 + P + v, hi=30, comm_hi=6, stride_mb_zero=True)
+    assert batch.strides[2] == 0
+    g = run_gpu(batch, op_times=ops)
+    r = run_oracle(orc, batch, op_times=ops)
+    assert (r["status"] == 0).all()
+    assert_same(g, r, op_times=ops)
