@@ -341,28 +341,42 @@ __device__ __forceinline__ void lane_body(const EvalArgs &a, const uint4 *tab, i
             cp_async_commit();
         }
     }
+    // The comm rows (and, MBZ, the cost of each row): a lane's rows are read
+    // kFill at a time, every load of a group issued before the first store,
+    // so the fill waits for about 2v*NI/kFill memory latencies, not 2v*NI.
+    constexpr int kFill = 8;
     uint32_t ncomm[NI];
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
         const int64_t x = x0 + i * G::kIPW;
+        const bool xin = x < a.n && k < a.P;
         ncomm[i] = 0;
 #pragma unroll 1
-        for (int cr = 0; cr < 2 * a.v; ++cr) {
-            const int s = (cr >> 1) * a.P + k;
-            const int bnd = (cr & 1) ? s : s - 1;
-            int32_t c = 0;
-            const int32_t *src = (cr & 1) && a.comm_b ? a.comm_b : a.comm;
-            if (src && x < a.n && k < a.P && bnd >= 0 && bnd < a.S - 1)
-                c = src[x * a.c_inst + (int64_t)bnd * a.c_bnd];
-            ncomm[i] |= (uint32_t)c;
-            if constexpr (MBZ) {
-                int32_t cost = 0;
-                if (x < a.n && k < a.P)
-                    cost = ((cr & 1) ? a.cost_b : a.cost_f)[x * a.s_inst + (int64_t)s * a.s_stage];
-                ctab[(cr * kRow + 32 * i + lane) * 2] = (uint32_t)cost;
-                ctab[(cr * kRow + 32 * i + lane) * 2 + 1] = (uint32_t)c;
-            } else {
-                ctab[cr * kRow + 32 * i + lane] = (uint32_t)c;
+        for (int cr0 = 0; cr0 < 2 * a.v; cr0 += kFill) {
+            int32_t c[kFill], cost[kFill];
+#pragma unroll
+            for (int u = 0; u < kFill; ++u) {
+                const int cr = cr0 + u;
+                const int s = (cr >> 1) * a.P + k;
+                const int bnd = (cr & 1) ? s : s - 1;
+                const int32_t *src = (cr & 1) && a.comm_b ? a.comm_b : a.comm;
+                c[u] = src && xin && cr < 2 * a.v && bnd >= 0 && bnd < a.S - 1
+                           ? src[x * a.c_inst + (int64_t)bnd * a.c_bnd] : 0;
+                if constexpr (MBZ)
+                    cost[u] = xin && cr < 2 * a.v
+                                  ? ((cr & 1) ? a.cost_b : a.cost_f)[x * a.s_inst + (int64_t)s * a.s_stage] : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < kFill; ++u) {
+                const int cr = cr0 + u;
+                if (cr >= 2 * a.v) break;
+                ncomm[i] |= (uint32_t)c[u];
+                if constexpr (MBZ) {
+                    ctab[(cr * kRow + 32 * i + lane) * 2] = (uint32_t)cost[u];
+                    ctab[(cr * kRow + 32 * i + lane) * 2 + 1] = (uint32_t)c[u];
+                } else {
+                    ctab[cr * kRow + 32 * i + lane] = (uint32_t)c[u];
+                }
             }
         }
         if constexpr (MBZ) {

@@ -531,3 +531,26 @@ def test_lane_table_entry_formats(orc, B, P, M, v, n, ops):
     r = run_oracle(orc, batch, op_times=ops)
     assert (r["status"] == 0).all()
     assert_same(g, r, op_times=ops)
+
+
+@pytest.mark.parametrize("n,ops", [(4000, True), (12000, False)])
+def test_lane_packed_cells_per_cta(orc, B, n, ops):
+    """Interleaved, costs shared by all microbatches: a CTA packs its
+    {cost, comm} cells into one word when all of its costs and comms lie in
+    0 .. 65,535.  One launch where most CTAs pack and a few do not (a cost of
+    65,536, a comm of 70,000, a negative cost), with values of exactly 65,535
+    in others; one and two instance sets per lane; every output against the
+    oracle."""
+    P, M, v = 8, 16, 2
+    b = W.random_batch(W.INTERLEAVED, P, M, v, n, seed=77 + n, hi=30, comm_hi=6, stride_mb_zero=True)
+    si, ss, _ = b.strides
+    ci, cbd = b.comm_strides
+    b.cost_f[5 * si + 3 * ss] = 65536
+    b.cost_b[11 * si + 9 * ss] = 65535
+    b.comm[3000 * ci + 4 * cbd] = 70000
+    b.comm[3100 * ci + 2 * cbd] = 65535
+    b.cost_b[2000 * si + 0 * ss] = -4
+    g = run_gpu(b, op_times=ops)
+    r = run_oracle(orc, b, op_times=ops)
+    assert_same(g, r, op_times=ops)
+    assert g["status"][2000] == B.ST_NEG_COST and (np.delete(g["status"], 2000) == 0).all()
