@@ -87,7 +87,8 @@ __device__ __forceinline__ uint32_t lane_lt(const uint32_t *desc, int R, int P, 
 
 // Table of the lane evaluator for one stride pair: head (loader entries of
 // rounds 0 .. kAhead-1), then ceil(R / kBR) blocks laid out as described at
-// the top of the file.  Word e of that table:
+// the top of the file (`word`: one-word entries, ceil(R / kBRw) blocks, the
+// head unused).  Word e of that table:
 template <int PMAX>
 __device__ uint32_t ltab_word(const uint32_t *desc, const uint8_t *lrd, const uint8_t *lwr, int R, int P, int v,
                               int nslots, int s_stage, int s_mb, uint32_t row_bytes, bool word, int64_t e) {
