@@ -50,6 +50,7 @@ struct DpGeom {
     static constexpr int kQ = PMAX;         // arrival ring rows
     static constexpr int kWords = (4 * kRing + 4 * kQ) * 32;  // per warp
     static constexpr int kWarps = 4;
+    static_assert((kRing & (kRing - 1)) == 0 && (kQ & (kQ - 1)) == 0, "rings are indexed by masks");
 };
 
 // Route r's next op at a stage with Mr microbatches and warmup w, after nf
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(128) k_eval_dp(const EvalArgs a, int MA, int32
         if (dev && i < (rb ? MB_ : MA) &&
             PPS_CHECK((rb ? srcB : srcA) + (int64_t)i * a.s_mb < reach, kChkCostRead, (rb ? srcB : srcA) + (int64_t)i * a.s_mb)) {
             const int32_t *base = (q & 1) ? a.cost_b : a.cost_f;
-            cp_async4(smem_addr(cring + (q * G::kRing + i % G::kRing) * 32 + lane),
+            cp_async4(smem_addr(cring + (q * G::kRing + (i & (G::kRing - 1))) * 32 + lane),
                       base + (rb ? srcB : srcA) + (int64_t)i * a.s_mb, 4);
         }
     };
@@ -222,8 +223,8 @@ __global__ void __launch_bounds__(128) k_eval_dp(const EvalArgs a, int MA, int32
         dp_front(nf, nb, Mr, r ? wB : wA, S.h, S.f, S.i);
         S.moreF = nf < Mr;
         S.moreB = nb < Mr;
-        S.cF = S.moreF ? cring[((2 * r) * G::kRing + nf % G::kRing) * 32 + lane] : 0u;
-        S.cB = S.moreB ? cring[((2 * r + 1) * G::kRing + nb % G::kRing) * 32 + lane] : 0u;
+        S.cF = S.moreF ? cring[((2 * r) * G::kRing + (nf & (G::kRing - 1))) * 32 + lane] : 0u;
+        S.cB = S.moreB ? cring[((2 * r + 1) * G::kRing + (nb & (G::kRing - 1))) * 32 + lane] : 0u;
     };
     Route RA, RB;
     refresh(0, RA);
@@ -315,7 +316,7 @@ __global__ void __launch_bounds__(128) k_eval_dp(const EvalArgs a, int MA, int32
                 const bool rb = pick == 2;
                 const bool f = rb ? Bf.f : A.f;
                 const int i = rb ? Bf.i : A.i, q = (rb ? 2 : 0) + (f ? 0 : 1);
-                place(rb, f, i, T, cring[(q * G::kRing + i % G::kRing) * 32 + lane]);
+                place(rb, f, i, T, cring[(q * G::kRing + (i & (G::kRing - 1))) * 32 + lane]);
             }
             cp_async_commit();
             __syncwarp();

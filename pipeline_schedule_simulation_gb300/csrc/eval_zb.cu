@@ -48,6 +48,7 @@ struct ZbGeom {
     static constexpr int kQ = 2 * PMAX;     // arrival ring rows
     static constexpr int kWords = (3 * kRing + 2 * kQ) * 32;  // per warp
     static constexpr int kWarps = 4;
+    static_assert((kRing & (kRing - 1)) == 0 && (kQ & (kQ - 1)) == 0, "rings are indexed by masks");
 };
 
 constexpr int kZbF = 0, kZbB = 1, kZbW = 2;
@@ -97,7 +98,8 @@ __global__ void __launch_bounds__(128) k_eval_zb(const EvalArgs a, const int32_t
     auto fetch = [&](int kind, int m) {
         if (dev && m < M && PPS_CHECK(row0 + (int64_t)m * a.s_mb < reach, kChkCostRead, row0 + (int64_t)m * a.s_mb)) {
             const int32_t *p = kind == kZbF ? src[0] : (kind == kZbB ? src[1] : src[2]);
-            cp_async4(smem_addr(cring + (kind * G::kRing + m % G::kRing) * 32 + lane), p + (int64_t)m * a.s_mb, 4);
+            cp_async4(smem_addr(cring + (kind * G::kRing + (m & (G::kRing - 1))) * 32 + lane),
+                      p + (int64_t)m * a.s_mb, 4);
         }
     };
 #pragma unroll 1
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(128) k_eval_zb(const EvalArgs a, const int32_t
         const bool act = kind >= 0;
         const int m = kind == kZbW ? nw : mx;
         const int kr = act ? kind : 0;
-        const uint32_t c = cring[(kr * G::kRing + m % G::kRing) * 32 + lane];
+        const uint32_t c = cring[(kr * G::kRing + (m & (G::kRing - 1))) * 32 + lane];
         const uint32_t e = s + c;
         if (act) {
             flag |= s | c;
@@ -176,8 +178,8 @@ __global__ void __launch_bounds__(128) k_eval_zb(const EvalArgs a, const int32_t
             busy += c;
             t = e;
             fetch(kind, m + G::kAheadC);
-            if (kind == kZbF && k + 1 < P) fring[(m % G::kQ) * 32 + lane + G::kIPW] = e + cmR;
-            if (kind == kZbB && k > 0) bring[(m % G::kQ) * 32 + lane - G::kIPW] = e + cmL;
+            if (kind == kZbF && k + 1 < P) fring[(m & (G::kQ - 1)) * 32 + lane + G::kIPW] = e + cmR;
+            if (kind == kZbB && k > 0) bring[(m & (G::kQ - 1)) * 32 + lane - G::kIPW] = e + cmL;
             if constexpr (OPS) {
                 const int64_t off = x * a.o_inst + ((int64_t)(k * 3 + kind) * M + m) * a.o_op;
                 if (a.op_start) a.op_start[off] = (int32_t)s;
@@ -192,8 +194,8 @@ __global__ void __launch_bounds__(128) k_eval_zb(const EvalArgs a, const int32_t
         // ---- publish
         p = nf + nb;
         isF = is_fwd(p);
-        const uint32_t cF = nf < M ? cring[(kZbF * G::kRing + nf % G::kRing) * 32 + lane] : 0u;
-        const uint32_t cB = nb < M ? cring[(kZbB * G::kRing + nb % G::kRing) * 32 + lane] : 0u;
+        const uint32_t cF = nf < M ? cring[(kZbF * G::kRing + (nf & (G::kRing - 1))) * 32 + lane] : 0u;
+        const uint32_t cB = nb < M ? cring[(kZbB * G::kRing + (nb & (G::kRing - 1))) * 32 + lane] : 0u;
         const bool moreX = p < 2 * M;
         const uint32_t lbF = t + ((moreX && !isF) ? cB : 0u) + cF;
         const uint32_t lbB = t + ((moreX && isF) ? cF : 0u) + cB;
